@@ -1,0 +1,186 @@
+/*
+ * zopt.h — C ABI of libzopt, the rank-local optimizer step of a ZeRO-sharded trainer on one
+ * GB300 (sm_103a).
+ *
+ * Three parts, each a few calls:
+ *   1. the flat bucketed shard layout            (zopt_shard_layout and accessors, host only)
+ *   2. the gradient norm / clip / found_inf stats (zopt_grad_norm_clip, device values)
+ *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step)
+ *   4. Muon's quintic Newton-Schulz               (zopt_ns_orthogonalize)
+ *
+ * Conventions shared by every call:
+ *   - Pointers named d_* and every tensor argument are DEVICE pointers owned by the caller.
+ *     The library allocates no device memory; scratch space is a caller-provided workspace
+ *     whose size a *_workspace() query returns.
+ *   - Every device call is asynchronous on the given stream (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises the host.
+ *   - Arguments are validated before any launch. On failure a call returns a non-zero
+ *     zopt_status, launches nothing, and zopt_last_error() describes the problem.
+ *   - Device arrays must start on a 16-byte boundary (128-bit vector access).
+ *   - All device values that a call writes are plain little-endian structs declared below.
+ */
+#ifndef ZOPT_H
+#define ZOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ZOPT_API __attribute__((visibility("default")))
+#else
+#define ZOPT_API
+#endif
+
+typedef struct CUstream_st* zopt_stream; /* a cudaStream_t */
+
+typedef enum zopt_status {
+  ZOPT_OK = 0,
+  ZOPT_EINVAL = 1,       /* an argument is out of range, misaligned or inconsistent */
+  ZOPT_EUNSUPPORTED = 2, /* a dtype combination or shape class without a kernel */
+  ZOPT_ECUDA = 3,        /* the CUDA runtime reported an error (message in zopt_last_error) */
+  ZOPT_ETIMEOUT = 4      /* a bounded device-side wait gave up (see zopt_ns_orthogonalize) */
+} zopt_status;
+
+typedef enum zopt_dtype { ZOPT_F32 = 0, ZOPT_BF16 = 1 } zopt_dtype;
+
+/* Message of the last failing call on this host thread (never NULL; "" if none). */
+ZOPT_API const char* zopt_last_error(void);
+/* Library version string. */
+ZOPT_API const char* zopt_version(void);
+
+/* ======================================================================================
+ * 1. Flat bucketed shard layout  (host only, pure)
+ *
+ * deg/zero.py, ZeroMaster (class docstring and __init__): the trainable parameters are laid
+ * end to end in a flat vector of N elements, cut into buckets of `bucket` elements after
+ * rounding the bucket down to a multiple of `world` (never below `world`); every bucket
+ * [s, e) is padded to L = ceil((e-s)/world)*world elements; rank r owns the r-th of world
+ * equal pieces (L/world elements) of every bucket, and its shard is those pieces
+ * concatenated in bucket order. Padding slots hold zeros.
+ * ====================================================================================== */
+typedef struct zopt_layout zopt_layout; /* opaque, host memory, owned by the library */
+
+/* Build rank `rank`'s layout. numel[n_params] are the parameter sizes in flat order;
+ * decay[n_params] (may be NULL = every parameter decays) is 1 where AdamW's decoupled
+ * weight decay applies (bluscript_zero_ckpt.cpp, ZeroConfig: 1-D parameters excluded).
+ * Errors: EINVAL for n_params < 1 (ZeroMaster "needs trainable parameters"), a negative
+ * size, a total of 0 or >= 2^62 elements, bucket < 1, world < 1, rank outside [0, world).
+ * On success *out must later be released with zopt_layout_free. */
+ZOPT_API zopt_status zopt_shard_layout(const int64_t* numel, const uint8_t* decay, int32_t n_params,
+                              int64_t bucket, int32_t world, int32_t rank, zopt_layout** out);
+ZOPT_API void zopt_layout_free(zopt_layout* layout);
+
+ZOPT_API int64_t zopt_layout_numel(const zopt_layout* layout);       /* N, the unpadded flat length */
+ZOPT_API int64_t zopt_layout_shard_len(const zopt_layout* layout);   /* S = sum over buckets of L/world */
+ZOPT_API int32_t zopt_layout_world(const zopt_layout* layout);
+ZOPT_API int32_t zopt_layout_rank(const zopt_layout* layout);
+ZOPT_API int32_t zopt_layout_num_buckets(const zopt_layout* layout);
+/* Bucket b: flat [start, end), padded length, and the shard offset of this rank's piece. */
+ZOPT_API zopt_status zopt_layout_bucket(const zopt_layout* layout, int32_t b, int64_t* start, int64_t* end,
+                               int64_t* padded, int64_t* shard_offset);
+/* Segments (ZeroMaster._segments over each of this rank's pieces): maximal runs
+ * (param index, offset inside the param, shard offset, length) in shard order.
+ * The four output arrays (any may be NULL) must hold zopt_layout_num_segments() entries. */
+ZOPT_API int64_t zopt_layout_num_segments(const zopt_layout* layout);
+ZOPT_API zopt_status zopt_layout_segments(const zopt_layout* layout, int32_t* param, int64_t* param_offset,
+                                 int64_t* shard_offset, int64_t* length);
+/* The shard's no-decay runs: sorted, disjoint, non-adjacent half-open ranges
+ * [begin_k, end_k) of shard slots that take NO weight decay (excluded parameters and
+ * padding). Written to runs[2k] = begin_k, runs[2k+1] = end_k; `runs` is host memory of
+ * 2*zopt_layout_num_nodecay_runs() int64 values. The caller copies this table to the device
+ * once and passes it to zopt_adamw_step. */
+ZOPT_API int64_t zopt_layout_num_nodecay_runs(const zopt_layout* layout);
+ZOPT_API zopt_status zopt_layout_nodecay_runs(const zopt_layout* layout, int64_t* runs);
+
+/* ======================================================================================
+ * 2. Gradient norm, clip coefficient, found_inf  (device values, no host sync)
+ *
+ * deg/zero.py, grad_sq_norm: the squared L2 norm of the shard's fp32 gradient (a simulated
+ * rank has no all-reduce, so it is the local shard's). bluscript_zero_ckpt.cpp, global clip
+ * block: coef = min(1, max_norm / (norm + 1e-6)), with a non-finite norm kept away from min.
+ * dmuon PR #16, sync-free clip stats: total_norm / clip_coef / clipped / found_inf are 0-dim
+ * device values; finiteness is judged on the norm; an inf norm gives coef 0,
+ * found_inf = 1, clipped = 0.
+ * ====================================================================================== */
+typedef struct zopt_clip_stats {
+  double sumsq;      /* sum of g^2 over the shard, accumulated in fp64 */
+  float norm;        /* fp32(sqrt(sumsq)) */
+  float clip_coef;   /* min(1, max_norm / (norm + 1e-6f)) in fp32; 0 when found_inf */
+  uint8_t clipped;   /* clip_coef < 1 and !found_inf */
+  uint8_t found_inf; /* norm is inf or NaN */
+  uint8_t reserved[6];
+} zopt_clip_stats; /* 24 bytes, device resident */
+
+/* Workspace bytes zopt_grad_norm_clip needs for n elements (a block-partials array and an
+ * arrival counter). */
+ZOPT_API size_t zopt_grad_norm_workspace(int64_t n);
+/* Reduce grad[n] (fp32 or bf16, bf16 promoted exactly) into *d_stats on `stream`.
+ * d_ws: at least zopt_grad_norm_workspace(n) bytes; it MUST be zero-filled before its first
+ * use, and every call leaves it zero-filled again. Calls sharing a workspace or a stats
+ * struct must be ordered (same stream). The result is deterministic for a given n and GPU.
+ * Errors: EINVAL for n < 1, NULL pointers, misalignment, a short workspace, max_norm
+ * negative or NaN. */
+ZOPT_API zopt_status zopt_grad_norm_clip(const void* grad, zopt_dtype dtype, int64_t n, float max_norm, void* d_ws,
+                                size_t ws_bytes, zopt_clip_stats* d_stats, zopt_stream stream);
+/* Recompute norm / clip_coef / clipped / found_inf from d_stats->sumsq (one thread). This is
+ * where a multi-rank job would all-reduce sumsq between zopt_grad_norm_clip and the step. */
+ZOPT_API zopt_status zopt_clip_finalize(zopt_clip_stats* d_stats, float max_norm, zopt_stream stream);
+
+/* ======================================================================================
+ * 3. Fused AdamW over the flat fp32 shard
+ *
+ * dmuon PR #16, foreach AdamW: decoupled weight decay -> moments -> bias-corrected addcdiv;
+ * bias corrections are per-step scalars. DeepSpeed PR #9021: the gradient is multiplied by
+ * the scale (here the clip coefficient) as it is loaded, after the bf16 -> fp32 promotion;
+ * a bf16 gradient of fp32 masters is read as bf16. bluscript_zero_ckpt.cpp: fp32 master and
+ * fp32 moments (a bf16 master would round the (1 - lr*wd) decay away). deg/zero.py,
+ * gather_params: the updated shard rounded to bf16 compute weights.
+ *
+ * Per element, each operation rounded to fp32 in this order (no fused multiply-add):
+ *   g = g_in * coef;  if decay: p = p * fp32(1 - lr*wd);
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);
+ *   d = sqrt(v) / fp32(sqrt(1 - beta2^t)) + eps;  p = p - fp32(lr / (1 - beta1^t)) * (m / d);
+ *   out = bf16_rne(p)
+ * with t = d_state->step + 1, beta^t an fp64 power by right-to-left square-and-multiply,
+ * and every scalar formed in fp64 from the fp64 hyper-parameters then rounded once to fp32.
+ * ====================================================================================== */
+typedef struct zopt_adamw_hparams {
+  double lr;
+  double beta1;
+  double beta2;
+  double eps;
+  double weight_decay;
+  int32_t skip_on_inf; /* 1: a step whose clip stats report found_inf changes nothing */
+  int32_t reserved;
+} zopt_adamw_hparams;
+
+typedef struct zopt_adam_state {
+  int64_t step;     /* AdamW steps taken; advanced on the device by every step not skipped */
+  uint32_t arrive;  /* internal arrival counter; 0 between calls */
+  int32_t reserved;
+} zopt_adam_state; /* 16 bytes, device resident; all-zero = a fresh optimizer */
+
+/* One AdamW step of this rank's shard, in place, on `stream`.
+ *   master, exp_avg, exp_avg_sq: fp32 [S] device arrays (S = zopt_layout_shard_len);
+ *   grad: [S] of grad_dtype (ZOPT_F32 or ZOPT_BF16), the shard of the summed gradient;
+ *   out_bf16: [S] bf16 bit patterns of the updated master, or NULL to skip the round-out;
+ *   d_nodecay_runs: the device copy of zopt_layout_nodecay_runs (may be NULL only when the
+ *     layout has no such runs);
+ *   d_clip: clip stats from zopt_grad_norm_clip (NULL = coef 1, never skip);
+ *   d_state: the step counter (required).
+ * Padding slots (zero master, zero gradient) stay exactly zero.
+ * Errors: EINVAL for NULL/misaligned pointers, non-finite or out-of-range hyper-parameters
+ * (lr < 0, beta outside [0, 1), eps < 0); EUNSUPPORTED for another gradient dtype. */
+ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d_nodecay_runs, float* master,
+                            float* exp_avg, float* exp_avg_sq, const void* grad, zopt_dtype grad_dtype,
+                            uint16_t* out_bf16, const zopt_adamw_hparams* hparams,
+                            const zopt_clip_stats* d_clip, zopt_adam_state* d_state, zopt_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZOPT_H */

@@ -95,3 +95,26 @@ def decay_mask_of_shard(decay: list, numel: list, bucket: int, world: int, rank:
     flat = np.concatenate([np.full(int(n), 1 if d else 0, dtype=np.uint8) for n, d in zip(numel, decay)]) \
         if numel else np.zeros(0, np.uint8)
     return gather_shard(flat, numel, bucket, world, rank)
+
+
+def flat_index_of_slots(numel: list, bucket: int, world: int, rank: int, slots: np.ndarray) -> np.ndarray:
+    """The flat index held by each of the given shard slots (-1 for padding), for sampled
+    checks of shards too large to enumerate: find the slot's bucket from the pieces' shard
+    offsets, then offset into the rank's piece of that bucket."""
+    ps = pieces(numel, bucket, world)
+    starts = np.array([p[0] for p in ps], dtype=np.int64)
+    ends = np.array([p[1] for p in ps], dtype=np.int64)
+    piece = np.array([p[3] for p in ps], dtype=np.int64)
+    offs = np.array([p[4] for p in ps], dtype=np.int64)
+    slots = np.asarray(slots, dtype=np.int64)
+    k = np.searchsorted(offs, slots, side="right") - 1
+    f = starts[k] + rank * piece[k] + (slots - offs[k])
+    return np.where(f < ends[k], f, -1)
+
+
+def param_of_flat(numel: list, flat: np.ndarray) -> np.ndarray:
+    """Index of the parameter that holds each flat index (-1 stays -1)."""
+    offsets = np.concatenate([[0], np.cumsum(np.asarray(numel, dtype=np.int64))])
+    flat = np.asarray(flat, dtype=np.int64)
+    i = np.searchsorted(offsets, flat, side="right") - 1
+    return np.where(flat >= 0, i, -1)

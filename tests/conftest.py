@@ -26,3 +26,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def zopt():
+    """The built library's binding (built in-tree on first use)."""
+    from zero_sharded_optimizer_flat_gb300 import build_lib
+    build_lib.build()
+    import zero_sharded_optimizer_flat_gb300 as Z
+    Z.lib()
+    return Z

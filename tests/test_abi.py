@@ -1,0 +1,112 @@
+"""CPU checks of the C ABI: the library builds and loads without a GPU, exports every
+function include/zopt.h declares, validates arguments before any launch, and its host-only
+layout (deg/zero.py, ZeroMaster) equals the oracle's bit for bit."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import layout as OL
+from zero_sharded_optimizer_flat_gb300 import build_lib
+
+build_lib.build()
+import zero_sharded_optimizer_flat_gb300 as Z  # noqa: E402
+
+
+def test_exports_every_declared_symbol():
+    names = Z.declared_functions()
+    assert "zopt_adamw_step" in names and "zopt_grad_norm_clip" in names and "zopt_shard_layout" in names
+    L = ctypes.CDLL(Z.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert Z.lib().zopt_version().startswith(b"zopt")
+
+
+def _check_layout(numel, decay, bucket, world):
+    for rank in range(world):
+        lay = Z.ShardLayout(numel, decay, bucket, world, rank)
+        assert lay.numel == sum(numel)
+        assert lay.shard_len == OL.shard_len(numel, bucket, world)
+        assert [(s, e, p) for s, e, p, _ in lay.buckets()] == OL.buckets(numel, bucket, world)
+        segs = [tuple(int(x) for x in r) for r in lay.segments()]
+        assert segs == OL.segments(numel, bucket, world, rank)
+        mask = OL.decay_mask_of_shard(list(decay), numel, bucket, world, rank)
+        ref_nd = np.zeros(lay.shard_len, bool)
+        ref_nd[mask == 0] = True
+        got_nd = np.zeros(lay.shard_len, bool)
+        runs = lay.nodecay_runs()
+        for b, e in runs:
+            assert b < e
+            got_nd[b:e] = True
+        assert np.array_equal(got_nd, ref_nd)
+        # sorted, disjoint and not adjacent
+        assert np.all(runs[1:, 0] > runs[:-1, 1])
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_layout_matches_oracle_random(world):
+    rng = np.random.default_rng(world)
+    for trial in range(25):
+        k = int(rng.integers(1, 12))
+        numel = [int(x) for x in rng.integers(0, 40, size=k)]
+        if sum(numel) == 0:
+            numel[0] = 1
+        decay = [bool(x) for x in rng.integers(0, 2, size=k)]
+        bucket = int(rng.integers(1, 50))
+        _check_layout(numel, decay, bucket, world)
+
+
+def test_layout_matches_oracle_workloads():
+    for name in ("c1", "c2", "c3"):
+        w = workloads.get(name)
+        numel = [p.numel for p in w.adamw]
+        decay = [p.decay for p in w.adamw]
+        lay = Z.ShardLayout(numel, decay, w.bucket, w.world, w.rank)
+        assert lay.shard_len == OL.shard_len(numel, w.bucket, w.world)
+        assert [tuple(int(x) for x in r) for r in lay.segments()] == OL.segments(numel, w.bucket, w.world, w.rank)
+    w = workloads.get("c4")
+    lay = Z.ShardLayout([p.numel for p in w.adamw], [p.decay for p in w.adamw], w.bucket, 8, 0)
+    assert lay.shard_len == 250_000_000 and len(lay.buckets()) == 60
+
+
+@pytest.mark.parametrize("args,frag", [
+    (([], None, 16, 1, 0), "needs trainable parameters"),
+    (([0, 0], None, 16, 1, 0), "empty"),
+    (([4], None, 16, 0, 0), "world"),
+    (([4], None, 16, 2, 2), "rank"),
+    (([4], None, 0, 1, 0), "bucket"),
+    (([-1, 4], None, 16, 1, 0), "negative"),
+])
+def test_layout_rejects_bad_arguments(args, frag):
+    with pytest.raises(Z.ZoptError) as e:
+        Z.ShardLayout(*args)
+    assert e.value.status == 1 and frag in str(e.value)
+
+
+def test_device_calls_validate_before_launch():
+    """Every call below fails validation, so none reaches a launch (the pointers are fake)."""
+    L = Z.lib()
+    stats = ctypes.c_void_p(256)
+    # n < 1, NULL grad, misaligned grad, short workspace: all rejected without touching CUDA
+    assert L.zopt_grad_norm_clip(None, 0, 0, 1.0, None, 0, stats, None) == 1
+    assert L.zopt_grad_norm_clip(None, 0, 8, 1.0, None, 0, stats, None) == 1
+    assert L.zopt_grad_norm_clip(ctypes.c_void_p(4), 0, 8, 1.0, ctypes.c_void_p(256), 4096, stats, None) == 1
+    assert b"aligned" in L.zopt_last_error()
+    assert L.zopt_grad_norm_clip(ctypes.c_void_p(256), 0, 8, 1.0, ctypes.c_void_p(256), 8, stats, None) == 1
+    assert b"workspace" in L.zopt_last_error()
+    assert L.zopt_grad_norm_clip(ctypes.c_void_p(256), 7, 8, 1.0, ctypes.c_void_p(256), 4096, stats, None) == 2
+    assert L.zopt_grad_norm_clip(ctypes.c_void_p(256), 0, 8, -1.0, ctypes.c_void_p(256), 4096, stats, None) == 1
+    lay = Z.ShardLayout([100, 3], [1, 0], 64, 1, 0)
+    hp = Z._Hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1, 0)
+    p = ctypes.c_void_p(1 << 20)
+    tab = ctypes.c_void_p(4096)
+    bad = Z._Hparams(1e-3, 1.0, 0.95, 1e-8, 0.1, 1, 0)
+    assert L.zopt_adamw_step(lay.handle, tab, p, p, p, p, 1, None, ctypes.byref(bad), None, p, None) == 1
+    assert b"betas" in L.zopt_last_error()
+    nan_lr = Z._Hparams(float("nan"), 0.9, 0.95, 1e-8, 0.1, 1, 0)
+    assert L.zopt_adamw_step(lay.handle, tab, p, p, p, p, 1, None, ctypes.byref(nan_lr), None, p, None) == 1
+    assert L.zopt_adamw_step(lay.handle, tab, p, p, p, p, 5, None, ctypes.byref(hp), None, p, None) == 2
+    assert L.zopt_adamw_step(lay.handle, None, p, p, p, p, 1, None, ctypes.byref(hp), None, p, None) == 1
+    assert L.zopt_adamw_step(lay.handle, tab, ctypes.c_void_p(8), p, p, p, 1, None, ctypes.byref(hp), None, p,
+                             None) == 1

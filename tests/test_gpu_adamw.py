@@ -1,0 +1,208 @@
+"""GPU parity of zopt_adamw_step (with zopt_grad_norm_clip feeding the coefficient) against
+the oracle's per-tensor AdamW (dmuon PR #16 op order; DeepSpeed PR #9021 grad scale on load;
+deg/zero.py flat == per-tensor, gather_params bf16 round-out).
+
+The oracle steps every parameter as a whole tensor, then its own layout picks rank r's
+slots. Bar: master, m, v and the bf16 weights bit for bit (the GPU's fp32 clip coefficient
+is fed to the oracle, and checked against the oracle's own within 1e-6 relative); found_inf
+exact; a skipped step changes nothing and does not advance the step counter.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import adamw as OA
+from oracle import clip as OC
+from oracle import layout as OL
+from oracle.bf16 import f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [workloads.Param("w0", (300, 77), True), workloads.Param("s0", (77,), False),
+         workloads.Param("w1", (129, 50), True), workloads.Param("s1", (5,), False),
+         workloads.Param("w2", (1000, 3), True), workloads.Param("s2", (1,), False),
+         workloads.Param("w3", (64, 64), True)]
+
+
+def bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+class Case:
+    """Holds a parameter set, the oracle's full tensors and the GPU shard."""
+
+    def __init__(self, Z, params, bucket, world, rank, seed, gdtype):
+        self.Z, self.params, self.bucket, self.world, self.rank = Z, params, bucket, world, rank
+        self.seed, self.gdtype = seed, gdtype
+        self.numel = [p.numel for p in params]
+        self.decay = [p.decay for p in params]
+        self.full_p = [t.numpy().astype(np.float32) for t in workloads.flat_masters(params, seed)]
+        self.full_m = [np.zeros_like(p) for p in self.full_p]
+        self.full_v = [np.zeros_like(p) for p in self.full_p]
+        self.layout = Z.ShardLayout(self.numel, self.decay, bucket, world, rank)
+        self.table = self.layout.device_table()
+        S = self.layout.shard_len
+        self.S = S
+        self.p = torch.from_numpy(self.shard(self.full_p)).cuda()
+        self.m = torch.zeros(S, device="cuda")
+        self.v = torch.zeros(S, device="cuda")
+        self.out = torch.zeros(S, dtype=torch.int16, device="cuda")
+        self.clip = Z.new_clip_stats()
+        self.state = Z.new_adam_state()
+        self.ws = Z.new_norm_workspace(S)
+        self.t = 0
+
+    def shard(self, tensors):
+        return OL.gather_shard(np.concatenate(tensors), self.numel, self.bucket, self.world, self.rank)
+
+    def step(self, step_idx, h: OA.Hyper, max_norm=1.0, poison=None, skip_on_inf=True):
+        grads = workloads.flat_grads(self.params, self.seed, step_idx, dtype=self.gdtype)
+        g_full = [g.float().numpy() for g in grads]
+        if poison is not None:
+            k, j, val = poison
+            g_full[k][j] = val
+        g_shard = self.shard(g_full)
+        g_dev = torch.from_numpy(g_shard).cuda().to(self.gdtype)
+        self.Z.grad_norm_clip(g_dev, max_norm, self.ws, self.clip)
+        self.Z.adamw_step(self.layout, self.table, self.p, self.m, self.v, g_dev, self.out, lr=h.lr,
+                          beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,
+                          skip_on_inf=skip_on_inf, clip_stats=self.clip, adam_state=self.state)
+        torch.cuda.synchronize()
+        st = self.Z.read_clip_stats(self.clip)
+        ref = OC.clip_stats(g_shard, max_norm)
+        assert st["found_inf"] == ref["found_inf"]
+        assert abs(float(st["clip_coef"]) - float(ref["clip_coef"])) <= 1e-6 * max(float(ref["clip_coef"]), 1e-30)
+        if not (st["found_inf"] and skip_on_inf):
+            self.t += 1
+            OA.step_tensors(self.full_p, self.full_m, self.full_v, g_full, self.decay, st["clip_coef"], h, self.t)
+        return st
+
+    def compare(self):
+        p = self.p.cpu().numpy()
+        assert np.array_equal(bits(p), bits(self.shard(self.full_p)))
+        assert np.array_equal(bits(self.m.cpu().numpy()), bits(self.shard(self.full_m)))
+        assert np.array_equal(bits(self.v.cpu().numpy()), bits(self.shard(self.full_v)))
+        out = self.out.cpu().numpy().view(np.uint16)
+        assert np.array_equal(out, f32_to_bf16_bits(self.shard(self.full_p)))
+        pad = OL.flat_index_of_shard(self.numel, self.bucket, self.world, self.rank) < 0
+        assert np.all(p[pad] == 0)
+        assert self.Z.read_adam_state(self.state) == {"step": self.t, "arrive": 0}
+
+
+H = OA.Hyper(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+@pytest.mark.parametrize("world,rank", [(1, 0), (3, 1), (8, 0), (8, 7)])
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
+def test_small_sets_bitwise(zopt, world, rank, gdtype):
+    case = Case(zopt, SMALL, 4000, world, rank, seed=11, gdtype=gdtype)
+    for s in range(3):
+        case.step(s, H, max_norm=0.05)  # small max_norm: the clip coefficient is active
+        case.compare()
+
+
+def test_c1_three_steps_bitwise(zopt):
+    w = workloads.get("c1")
+    case = Case(zopt, w.adamw, w.bucket, 1, 0, seed=w.seed, gdtype=torch.bfloat16)
+    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    for s in range(w.steps):
+        case.step(s, h, max_norm=w.max_norm)
+        case.compare()
+
+
+def test_wsd_schedule_lr_changes_each_step(zopt):
+    """Per-step lr (the WSD schedule of bluscript_zero_ckpt.cpp) is a host input per call."""
+    params = SMALL[:4]
+    case = Case(zopt, params, 1 << 12, 2, 1, seed=5, gdtype=torch.bfloat16)
+    for s in range(6):
+        lr = workloads.wsd_lr(s, 6e-4, 6e-5, 1, 3, 6)
+        case.step(s, OA.Hyper(lr, 0.9, 0.95, 1e-8, 0.1))
+        case.compare()
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_inf_grad_skips_step(zopt, bad):
+    case = Case(zopt, SMALL, 4000, 1, 0, seed=3, gdtype=torch.bfloat16)
+    case.step(0, H)
+    case.compare()
+    st = case.step(1, H, poison=(2, 17, bad))
+    assert st["found_inf"] and not st["clipped"] and st["clip_coef"] == 0.0
+    case.compare()  # nothing changed, step counter still 1
+    case.step(2, H)
+    case.compare()
+
+
+def test_ragged_lengths(zopt):
+    for n in (1, 3, 4, 5, 2047, 2048, 2049, 4096 * 3 + 1):
+        params = [workloads.Param("a", (n,), True)]
+        case = Case(zopt, params, 1 << 20, 1, 0, seed=n, gdtype=torch.float32)
+        case.step(0, H)
+        case.step(1, H)
+        case.compare()
+
+
+def test_no_output_and_no_clip_stats(zopt):
+    """out_bf16 = NULL skips the round-out; d_clip = NULL means coefficient 1."""
+    case = Case(zopt, SMALL, 4000, 1, 0, seed=9, gdtype=torch.bfloat16)
+    grads = workloads.flat_grads(SMALL, 9, 0)
+    g_full = [g.float().numpy() for g in grads]
+    g_dev = torch.from_numpy(case.shard(g_full)).cuda().bfloat16()
+    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, None, lr=H.lr, clip_stats=None,
+                    adam_state=case.state)
+    torch.cuda.synchronize()
+    OA.step_tensors(case.full_p, case.full_m, case.full_v, g_full, case.decay, 1.0, H, 1)
+    assert np.array_equal(bits(case.p.cpu().numpy()), bits(case.shard(case.full_p)))
+    assert int(case.out.abs().sum()) == 0
+
+
+def test_full_size_zero2_shard_sampled(zopt):
+    """The 2e9-parameter ZeRO-2 shard (rank 0 of 8, S = 250,000,000), in the launch
+    configuration the benchmark times: sampled slots checked bit for bit against the oracle
+    computed one element at a time."""
+    w = workloads.get("c4")
+    numel = [p.numel for p in w.adamw]
+    decay = np.array([p.decay for p in w.adamw])
+    lay = zopt.ShardLayout(numel, decay, w.bucket, w.world, w.rank)
+    S = lay.shard_len
+    table = lay.device_table()
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    p = torch.randn(S, device="cuda", generator=gen) * 0.02
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    out = torch.empty(S, dtype=torch.int16, device="cuda")
+    clip, state = zopt.new_clip_stats(), zopt.new_adam_state()
+    ws = zopt.new_norm_workspace(S)
+    rng = np.random.default_rng(4)
+    # samples: random slots, the first and last slots, and slots around every no-decay run edge
+    runs = lay.nodecay_runs()
+    edges = np.concatenate([runs.reshape(-1) + d for d in (-2, -1, 0, 1)])
+    idx = np.unique(np.clip(np.concatenate([rng.integers(0, S, 200_000), [0, 1, S - 2, S - 1], edges]), 0, S - 1))
+    idx_d = torch.from_numpy(idx).cuda()
+    flat = OL.flat_index_of_slots(numel, w.bucket, w.world, w.rank, idx)
+    owner = OL.param_of_flat(numel, flat)
+    dec = np.where(owner >= 0, decay[np.maximum(owner, 0)], False)
+    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    sp = p[idx_d].cpu().numpy()
+    sm = np.zeros_like(sp)
+    sv = np.zeros_like(sp)
+    for t in range(1, 3):
+        g = torch.randn(S, device="cuda", generator=gen) * 1e-3
+        zopt.grad_norm_clip(g, w.max_norm, ws, clip)
+        zopt.adamw_step(lay, table, p, m, v, g, out, lr=h.lr, beta1=h.beta1, beta2=h.beta2, eps=h.eps,
+                        weight_decay=h.weight_decay, clip_stats=clip, adam_state=state)
+        torch.cuda.synchronize()
+        st = zopt.read_clip_stats(clip)
+        sg = g[idx_d].cpu().numpy()
+        ref_ss = OC.sumsq(g.cpu().numpy())
+        assert abs(st["sumsq"] - ref_ss) <= 1e-6 * ref_ss
+        sc = OA.scalars_f32(h, t)
+        for mask in (dec, ~dec):
+            pp, mm, vv = sp[mask], sm[mask], sv[mask]
+            OA.adamw_tensor_f32(pp, mm, vv, sg[mask], st["clip_coef"], bool(mask is dec), sc)
+            sp[mask], sm[mask], sv[mask] = pp, mm, vv
+        assert np.array_equal(bits(p[idx_d].cpu().numpy()), bits(sp))
+        assert np.array_equal(bits(m[idx_d].cpu().numpy()), bits(sm))
+        assert np.array_equal(bits(v[idx_d].cpu().numpy()), bits(sv))
+        assert np.array_equal(out[idx_d].cpu().numpy().view(np.uint16), f32_to_bf16_bits(sp))
+    assert zopt.read_adam_state(state)["step"] == 2

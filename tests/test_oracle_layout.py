@@ -102,3 +102,16 @@ def test_gather_shard_zero_pads():
     sh = OL.gather_shard(flat, numel, 4, 2, 1)
     assert sh.tolist() == [3.0, 4.0, 7.0, 0.0]
     assert OL.decay_mask_of_shard([True, False], numel, 4, 2, 1).tolist() == [1, 1, 0, 0]
+
+
+@pytest.mark.parametrize("numel,bucket,world", CASES)
+def test_sampled_slot_map_equals_enumeration(numel, bucket, world):
+    for r in range(world):
+        idx = OL.flat_index_of_shard(numel, bucket, world, r)
+        slots = np.arange(idx.shape[0])
+        assert np.array_equal(OL.flat_index_of_slots(numel, bucket, world, r, slots), idx)
+        owner = OL.param_of_flat(numel, idx)
+        offsets = np.concatenate([[0], np.cumsum(numel)])
+        for f, i in zip(idx, owner):
+            if f >= 0:
+                assert offsets[i] <= f < offsets[i + 1]

@@ -1,0 +1,248 @@
+"""Python binding of libzopt — the rank-local optimizer step of a ZeRO-sharded trainer on
+GB300 (sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels. The
+calls keep the C names: ``zopt_shard_layout`` (as :class:`ShardLayout`),
+``zopt_grad_norm_clip``, ``zopt_adamw_step``, ``zopt_ns_orthogonalize``. PyTorch provides
+device memory and streams. The library must be built (``build_lib.build()``); if it is
+missing every call raises — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import struct
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzopt.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "zopt.h")
+
+F32, BF16 = 0, 1
+STATUS = {0: "ZOPT_OK", 1: "ZOPT_EINVAL", 2: "ZOPT_EUNSUPPORTED", 3: "ZOPT_ECUDA", 4: "ZOPT_ETIMEOUT"}
+
+CLIP_STATS_BYTES = 24
+ADAM_STATE_BYTES = 16
+
+_lib = None
+
+
+class ZoptError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("skip_on_inf", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libzopt.so is not built ({LIB_PATH}); run "
+                           "`python -m zero_sharded_optimizer_flat_gb300.build_lib`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, u8p, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "zopt_last_error": (ctypes.c_char_p, []),
+        "zopt_version": (ctypes.c_char_p, []),
+        "zopt_shard_layout": (ctypes.c_int, [vp, u8p, i32, i64, i32, i32, ctypes.POINTER(vp)]),
+        "zopt_layout_free": (None, [vp]),
+        "zopt_layout_numel": (i64, [vp]),
+        "zopt_layout_shard_len": (i64, [vp]),
+        "zopt_layout_world": (i32, [vp]),
+        "zopt_layout_rank": (i32, [vp]),
+        "zopt_layout_num_buckets": (i32, [vp]),
+        "zopt_layout_bucket": (ctypes.c_int, [vp, i32, vp, vp, vp, vp]),
+        "zopt_layout_num_segments": (i64, [vp]),
+        "zopt_layout_segments": (ctypes.c_int, [vp, vp, vp, vp, vp]),
+        "zopt_layout_num_nodecay_runs": (i64, [vp]),
+        "zopt_layout_nodecay_runs": (ctypes.c_int, [vp, vp]),
+        "zopt_grad_norm_workspace": (sz, [i64]),
+        "zopt_grad_norm_clip": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, sz, vp, vp]),
+        "zopt_clip_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp]),
+        "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
+                                           vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def declared_functions() -> list:
+    """Every function the C header declares (used by the ABI export test)."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zopt_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise ZoptError(status, lib().zopt_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    return -1
+
+
+# --------------------------------------------------------------------------- layout
+
+class ShardLayout:
+    """``zopt_shard_layout``: rank ``rank``'s view of the flat bucketed layout."""
+
+    def __init__(self, numel, decay=None, bucket: int = 1 << 25, world: int = 1, rank: int = 0):
+        L = lib()
+        n = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
+        d = None if decay is None else np.ascontiguousarray(np.asarray(decay, dtype=np.uint8))
+        if d is not None and d.shape != n.shape:
+            raise ValueError("decay must have one flag per parameter")
+        out = ctypes.c_void_p()
+        _check(L.zopt_shard_layout(n.ctypes.data if n.size else None, None if d is None else d.ctypes.data,
+                                   int(n.size), int(bucket), int(world), int(rank), ctypes.byref(out)))
+        self._h = out
+        self._keep = (n, d)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.zopt_layout_free(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def numel(self) -> int:
+        return lib().zopt_layout_numel(self._h)
+
+    @property
+    def shard_len(self) -> int:
+        return lib().zopt_layout_shard_len(self._h)
+
+    @property
+    def world(self) -> int:
+        return lib().zopt_layout_world(self._h)
+
+    @property
+    def rank(self) -> int:
+        return lib().zopt_layout_rank(self._h)
+
+    def buckets(self) -> list:
+        L, out = lib(), []
+        for b in range(L.zopt_layout_num_buckets(self._h)):
+            v = [ctypes.c_int64() for _ in range(4)]
+            _check(L.zopt_layout_bucket(self._h, b, *[ctypes.byref(x) for x in v]))
+            out.append(tuple(x.value for x in v))
+        return out
+
+    def segments(self) -> np.ndarray:
+        """(k, 4) int64: param index, offset in param, shard offset, length."""
+        L = lib()
+        k = L.zopt_layout_num_segments(self._h)
+        p = np.zeros(k, np.int32)
+        a = np.zeros((3, k), np.int64)
+        _check(L.zopt_layout_segments(self._h, p.ctypes.data, a[0].ctypes.data, a[1].ctypes.data, a[2].ctypes.data))
+        return np.stack([p.astype(np.int64), a[0], a[1], a[2]], axis=1)
+
+    def nodecay_runs(self) -> np.ndarray:
+        """(k, 2) int64 half-open shard ranges without weight decay."""
+        L = lib()
+        k = L.zopt_layout_num_nodecay_runs(self._h)
+        r = np.zeros(2 * k, np.int64)
+        _check(L.zopt_layout_nodecay_runs(self._h, r.ctypes.data if k else None))
+        return r.reshape(k, 2)
+
+    def device_table(self, device="cuda"):
+        """The no-decay run table copied to the device (pass it to :func:`adamw_step`)."""
+        import torch
+        r = self.nodecay_runs().reshape(-1)
+        return torch.from_numpy(r if r.size else np.zeros(2, np.int64)).to(device)
+
+
+# --------------------------------------------------------------------------- device structs
+
+def new_clip_stats(device="cuda"):
+    import torch
+    return torch.zeros(CLIP_STATS_BYTES, dtype=torch.uint8, device=device)
+
+
+def new_adam_state(device="cuda"):
+    import torch
+    return torch.zeros(ADAM_STATE_BYTES, dtype=torch.uint8, device=device)
+
+
+def read_clip_stats(t) -> dict:
+    """Decode a zopt_clip_stats tensor (copies it to the host: logging/tests only)."""
+    b = bytes(t.detach().cpu().numpy().tobytes())
+    sumsq, norm, coef, clipped, found = struct.unpack("<dffBB6x", b)
+    return {"sumsq": sumsq, "norm": np.float32(norm), "clip_coef": np.float32(coef), "clipped": bool(clipped),
+            "found_inf": bool(found)}
+
+
+def read_adam_state(t) -> dict:
+    b = bytes(t.detach().cpu().numpy().tobytes())
+    step, arrive, _ = struct.unpack("<qIi", b)
+    return {"step": step, "arrive": arrive}
+
+
+# --------------------------------------------------------------------------- calls
+
+def grad_norm_workspace(n: int) -> int:
+    return int(lib().zopt_grad_norm_workspace(int(n)))
+
+
+def new_norm_workspace(n: int, device="cuda"):
+    """A zero-filled workspace for :func:`grad_norm_clip` over n elements."""
+    import torch
+    return torch.zeros(max(grad_norm_workspace(n), 16), dtype=torch.uint8, device=device)
+
+
+def grad_norm_clip(grad, max_norm: float, ws, stats, n: int | None = None, stream=None) -> None:
+    """``zopt_grad_norm_clip`` over the first n elements of ``grad`` (default: all)."""
+    n = grad.numel() if n is None else int(n)
+    _check(lib().zopt_grad_norm_clip(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(ws), ws.numel(),
+                                     _ptr(stats), _stream(stream)))
+
+
+def clip_finalize(stats, max_norm: float, stream=None) -> None:
+    _check(lib().zopt_clip_finalize(_ptr(stats), float(max_norm), _stream(stream)))
+
+
+def adamw_step(layout: ShardLayout, table, master, exp_avg, exp_avg_sq, grad, out_bf16, *, lr: float,
+               beta1: float = 0.9, beta2: float = 0.95, eps: float = 1e-8, weight_decay: float = 0.1,
+               skip_on_inf: bool = True, clip_stats=None, adam_state=None, stream=None) -> None:
+    """``zopt_adamw_step``: one AdamW step of the rank's shard, in place."""
+    hp = _Hparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(bool(skip_on_inf)), 0)
+    _check(lib().zopt_adamw_step(layout.handle, _ptr(table), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                 _ptr(grad), _dtype_code(grad), _ptr(out_bf16), ctypes.byref(hp),
+                                 _ptr(clip_stats), _ptr(adam_state), _stream(stream)))

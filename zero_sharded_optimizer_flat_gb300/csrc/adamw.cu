@@ -1,0 +1,281 @@
+// Fused AdamW over the flat fp32 master shard.
+//
+// dmuon PR #16, foreach AdamW commit: decoupled weight decay, then the moments, then the
+// bias-corrected addcdiv; bias corrections are per-step scalars. DeepSpeed PR #9021: the
+// gradient is scaled as it is loaded (after the bf16 -> fp32 promotion). deg/zero.py: flat
+// AdamW is the same arithmetic as per tensor; the updated shard is rounded to bf16 compute
+// weights (gather_params). bluscript_zero_ckpt.cpp: fp32 master and moments, 1-D parameters
+// excluded from weight decay.
+//
+// Design (HBM-bound, 28-30 algorithmic bytes per element):
+//   * one launch per shard; each block owns a contiguous run of 2048-element tiles; a thread
+//     moves 2 x 4 elements per tile with 128-bit loads and stores, every warp instruction
+//     covering 512 contiguous bytes of each fp32 array;
+//   * the weight-decay flag comes from the layout's sorted no-decay runs: each thread keeps
+//     a cursor that only moves forward, so a tile without a run boundary costs one compare;
+//   * t-dependent scalars are formed once per block by thread 0 in fp64 (IEEE mul/sub/div/
+//     sqrt, no contraction) from the device step counter, so a skipped step (found_inf)
+//     needs no host round trip; the last block to finish advances the counter;
+//   * every per-element operation is an explicitly rounded fp32 intrinsic, so the result
+//     is bitwise the exact-order definition.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+
+namespace zopt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroup = 4;                        // elements per vector access
+constexpr int kTile = kThreads * kGroup * 2;     // 2048 elements per tile
+constexpr int kBlocksPerSm = 4;
+
+struct HostScalars {
+  float b1, omb1, b2, omb2, eps, decay;  // fp64 -> fp32 once
+  double lr, beta1, beta2;               // for the t-dependent scalars
+  int skip_on_inf;
+};
+
+__device__ __forceinline__ double pow_sq_mul(double base, long long e) {
+  double r = 1.0;
+  while (e > 0) {
+    if (e & 1) r = __dmul_rn(r, base);
+    base = __dmul_rn(base, base);
+    e >>= 1;
+  }
+  return r;
+}
+
+struct Vec4 { float x[4]; };
+
+__device__ __forceinline__ Vec4 ld4(const float* p) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  return Vec4{{a.x, a.y, a.z, a.w}};
+}
+__device__ __forceinline__ void st4(float* p, const Vec4& v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
+}
+__device__ __forceinline__ Vec4 ldg4(const float* p) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  return Vec4{{a.x, a.y, a.z, a.w}};
+}
+__device__ __forceinline__ Vec4 ldg4(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  return Vec4{{__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+               __uint_as_float(u.y & 0xFFFF0000u)}};
+}
+__device__ __forceinline__ float ldg1(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldg1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<unsigned int>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+struct StepScalars {
+  float coef, b1, omb1, b2, omb2, eps, decay, step_size, bc2s;
+};
+
+// One element, every operation rounded on its own, in the documented order.
+__device__ __forceinline__ void adamw_elem(float& p, float& m, float& v, float gin, bool decays,
+                                           const StepScalars& s) {
+  const float g = __fmul_rn(gin, s.coef);
+  if (decays) p = __fmul_rn(p, s.decay);
+  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.bc2s), s.eps);
+  p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, d)));
+}
+
+__device__ __forceinline__ unsigned short bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Is shard slot x inside one of the no-decay runs [runs[2k], runs[2k+1]) with k >= cur
+// whose begin is below `limit`?
+__device__ __forceinline__ bool in_nodecay(const int64_t* __restrict__ runs, int64_t nruns, int64_t cur,
+                                           int64_t limit, int64_t x) {
+  for (int64_t k = cur; k < nruns; ++k) {
+    const int64_t b = __ldg(runs + 2 * k);
+    if (b >= limit) break;
+    if (x >= b && x < __ldg(runs + 2 * k + 1)) return true;
+  }
+  return false;
+}
+
+template <typename G, bool kOut>
+__global__ void __launch_bounds__(kThreads) adamw_kernel(float* __restrict__ P, float* __restrict__ M,
+                                                          float* __restrict__ V, const G* __restrict__ Gr,
+                                                          uint16_t* __restrict__ out, int64_t n,
+                                                          const int64_t* __restrict__ runs, int64_t nruns,
+                                                          HostScalars hs, const zopt_clip_stats* clip,
+                                                          zopt_adam_state* state) {
+  __shared__ StepScalars s_sc;
+  __shared__ int s_skip;
+  __shared__ long long s_t;
+  if (threadIdx.x == 0) {
+    float coef = 1.0f;
+    int found = 0;
+    if (clip != nullptr) {
+      coef = *reinterpret_cast<const volatile float*>(&clip->clip_coef);
+      found = *reinterpret_cast<const volatile uint8_t*>(&clip->found_inf);
+    }
+    const long long t = *reinterpret_cast<const volatile long long*>(&state->step) + 1;
+    const double bc1 = __dsub_rn(1.0, pow_sq_mul(hs.beta1, t));
+    const double bc2 = __dsub_rn(1.0, pow_sq_mul(hs.beta2, t));
+    s_sc = StepScalars{coef,   hs.b1,  hs.omb1, hs.b2, hs.omb2, hs.eps, hs.decay,
+                       __double2float_rn(__ddiv_rn(hs.lr, bc1)), __double2float_rn(__dsqrt_rn(bc2))};
+    s_skip = (hs.skip_on_inf && found) ? 1 : 0;
+    s_t = t;
+  }
+  __syncthreads();
+  if (s_skip) return;  // uniform over the grid: nothing is written, the counter stays
+  const StepScalars sc = s_sc;
+
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t t_begin = ntiles * blockIdx.x / gridDim.x;
+  const int64_t t_end = ntiles * (blockIdx.x + 1) / gridDim.x;
+
+  // First no-decay run that ends after this block's first slot (runs are sorted, so their
+  // ends are sorted too).
+  int64_t cur = 0;
+  {
+    int64_t lo = 0, hi = nruns;
+    const int64_t x0 = t_begin * kTile;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (__ldg(runs + 2 * mid + 1) <= x0) lo = mid + 1; else hi = mid;
+    }
+    cur = lo;
+  }
+
+  for (int64_t tile = t_begin; tile < t_end; ++tile) {
+    const int64_t tb = tile * kTile;
+    const int64_t te = (tb + kTile < n) ? tb + kTile : n;
+    while (cur < nruns && __ldg(runs + 2 * cur + 1) <= tb) ++cur;
+    const bool mixed = cur < nruns && __ldg(runs + 2 * cur) < te;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t x = tb + h * (kThreads * kGroup) + kGroup * threadIdx.x;
+      if (x + kGroup <= n) {
+        Vec4 p = ld4(P + x), m = ld4(M + x), v = ld4(V + x);
+        const Vec4 g = ldg4(Gr + x);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          const bool dec = !mixed || !in_nodecay(runs, nruns, cur, te, x + k);
+          adamw_elem(p.x[k], m.x[k], v.x[k], g.x[k], dec, sc);
+        }
+        st4(P + x, p);
+        st4(M + x, m);
+        st4(V + x, v);
+        if (kOut) {
+          const uint2 o = make_uint2(static_cast<unsigned int>(bf16_bits(p.x[0])) |
+                                         (static_cast<unsigned int>(bf16_bits(p.x[1])) << 16),
+                                     static_cast<unsigned int>(bf16_bits(p.x[2])) |
+                                         (static_cast<unsigned int>(bf16_bits(p.x[3])) << 16));
+          *reinterpret_cast<uint2*>(out + x) = o;
+        }
+      } else {
+        for (int64_t y = x; y < n && y < x + kGroup; ++y) {
+          float p = P[y], m = M[y], v = V[y];
+          const bool dec = !mixed || !in_nodecay(runs, nruns, cur, te, y);
+          adamw_elem(p, m, v, ldg1(Gr + y), dec, sc);
+          P[y] = p;
+          M[y] = m;
+          V[y] = v;
+          if (kOut) out[y] = bf16_bits(p);
+        }
+      }
+    }
+  }
+
+  // The last block to finish advances the step counter (every block has read it by now).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&state->arrive, 1u);
+    if (ticket == gridDim.x - 1) {
+      state->step = s_t;
+      state->arrive = 0u;
+      __threadfence();
+    }
+  }
+}
+
+template <typename G, bool kOut>
+zopt_status launch(const HostScalars& hs, float* P, float* M, float* V, const void* g, uint16_t* out, int64_t n,
+                   const int64_t* runs, int64_t nruns, const zopt_clip_stats* clip, zopt_adam_state* state,
+                   cudaStream_t stream) {
+  static int occ = 0;  // resident blocks per SM for this instantiation
+  if (occ == 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, adamw_kernel<G, kOut>, kThreads, 0) != cudaSuccess || o < 1)
+      o = kBlocksPerSm;
+    occ = o < kBlocksPerSm ? o : kBlocksPerSm;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_adamw_step: no CUDA device");
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t blocks = static_cast<int64_t>(sms) * occ;
+  if (blocks > ntiles) blocks = ntiles;
+  adamw_kernel<G, kOut><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+      P, M, V, static_cast<const G*>(g), out, n, runs, nruns, hs, clip, state);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+}  // namespace
+}  // namespace zopt
+
+extern "C" zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d_nodecay_runs, float* master,
+                                       float* exp_avg, float* exp_avg_sq, const void* grad, zopt_dtype grad_dtype,
+                                       uint16_t* out_bf16, const zopt_adamw_hparams* hp,
+                                       const zopt_clip_stats* d_clip, zopt_adam_state* d_state,
+                                       zopt_stream stream) {
+  using namespace zopt;
+  if (layout == nullptr || hp == nullptr) return fail(ZOPT_EINVAL, "zopt_adamw_step: layout or hparams is NULL");
+  if (master == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || grad == nullptr || d_state == nullptr)
+    return fail(ZOPT_EINVAL, "zopt_adamw_step: NULL device pointer");
+  if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(grad) ||
+      (out_bf16 != nullptr && !aligned16(out_bf16)) || !aligned16(d_state) ||
+      (d_clip != nullptr && (reinterpret_cast<uintptr_t>(d_clip) & 7u) != 0))
+    return fail(ZOPT_EINVAL, "zopt_adamw_step: a device pointer is not 16-byte aligned");
+  const int64_t nruns = static_cast<int64_t>(layout->nodecay.size() / 2);
+  if (nruns > 0 && (d_nodecay_runs == nullptr || (reinterpret_cast<uintptr_t>(d_nodecay_runs) & 7u) != 0))
+    return fail(ZOPT_EINVAL, "zopt_adamw_step: the layout has no-decay runs but d_nodecay_runs is NULL/misaligned");
+  if (grad_dtype != ZOPT_F32 && grad_dtype != ZOPT_BF16)
+    return fail(ZOPT_EUNSUPPORTED, "zopt_adamw_step: gradient dtype must be fp32 or bf16 (fp32 master)");
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+  if (!std::isfinite(lr) || lr < 0.0) return fail(ZOPT_EINVAL, "zopt_adamw_step: lr must be finite and >= 0");
+  if (!(b1 >= 0.0 && b1 < 1.0) || !(b2 >= 0.0 && b2 < 1.0))
+    return fail(ZOPT_EINVAL, "zopt_adamw_step: betas must lie in [0, 1)");
+  if (!std::isfinite(eps) || eps < 0.0) return fail(ZOPT_EINVAL, "zopt_adamw_step: eps must be finite and >= 0");
+  if (!std::isfinite(wd)) return fail(ZOPT_EINVAL, "zopt_adamw_step: weight_decay must be finite");
+
+  // Scalars that do not depend on the step: fp64 expressions rounded once to fp32. The host
+  // build uses -ffp-contract=off, so 1 - lr*wd is two roundings, as written.
+  HostScalars hs;
+  hs.b1 = static_cast<float>(b1);
+  hs.omb1 = static_cast<float>(1.0 - b1);
+  hs.b2 = static_cast<float>(b2);
+  hs.omb2 = static_cast<float>(1.0 - b2);
+  hs.eps = static_cast<float>(eps);
+  const double lrwd = lr * wd;
+  hs.decay = static_cast<float>(1.0 - lrwd);
+  hs.lr = lr;
+  hs.beta1 = b1;
+  hs.beta2 = b2;
+  hs.skip_on_inf = hp->skip_on_inf != 0;
+
+  const int64_t n = layout->shard_len;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (grad_dtype == ZOPT_BF16) {
+    return out_bf16 ? launch<__nv_bfloat16, true>(hs, master, exp_avg, exp_avg_sq, grad, out_bf16, n, d_nodecay_runs,
+                                                  nruns, d_clip, d_state, s)
+                    : launch<__nv_bfloat16, false>(hs, master, exp_avg, exp_avg_sq, grad, nullptr, n,
+                                                   d_nodecay_runs, nruns, d_clip, d_state, s);
+  }
+  return out_bf16 ? launch<float, true>(hs, master, exp_avg, exp_avg_sq, grad, out_bf16, n, d_nodecay_runs, nruns,
+                                        d_clip, d_state, s)
+                  : launch<float, false>(hs, master, exp_avg, exp_avg_sq, grad, nullptr, n, d_nodecay_runs, nruns,
+                                         d_clip, d_state, s);
+}

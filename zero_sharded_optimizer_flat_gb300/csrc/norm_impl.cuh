@@ -1,0 +1,157 @@
+// Device-side pieces of the norm / clip reduction, shared by the kernels that produce a
+// sum of squares (the norm pass and the gradient-accumulation pass).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "zopt.h"
+
+namespace zopt {
+
+constexpr int kNormThreads = 256;
+constexpr int kNormBlocksPerSm = 8;
+constexpr int64_t kNormMaxBlocks = 4096;
+
+// Workspace header: the arrival counter, padded to 256 bytes, then one fp64 partial per block.
+struct NormWorkspace {
+  unsigned int arrive;
+  unsigned int reserved[63];
+  double partials[1];  // [grid] in practice
+};
+static_assert(offsetof(NormWorkspace, partials) == 256, "workspace header is 256 bytes");
+
+size_t norm_grid_blocks(int64_t n);
+
+// Stats from a sum of squares, exactly as the pages state the contract (see norm.cu).
+__device__ __forceinline__ void write_clip_stats(zopt_clip_stats* out, double ss, float max_norm) {
+  const double norm64 = (ss >= 0.0) ? __dsqrt_rn(ss) : __longlong_as_double(0x7FF8000000000000LL);
+  const float norm = __double2float_rn(norm64);
+  const bool found_inf = !isfinite(norm);
+  float coef = 0.0f;
+  if (!found_inf) {
+    coef = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
+    if (!(coef < 1.0f)) coef = 1.0f;
+  }
+  out->sumsq = ss;
+  out->norm = norm;
+  out->clip_coef = coef;
+  out->clipped = (!found_inf && coef < 1.0f) ? 1 : 0;
+  out->found_inf = found_inf ? 1 : 0;
+}
+
+// Sum of squares of 8 values: fp32 pairwise, exact fp64 outside the safe fp32 range.
+__device__ __forceinline__ double sumsq8(const float (&x)[8]) {
+  const float s01 = __fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1]));
+  const float s23 = __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3]));
+  const float s45 = __fadd_rn(__fmul_rn(x[4], x[4]), __fmul_rn(x[5], x[5]));
+  const float s67 = __fadd_rn(__fmul_rn(x[6], x[6]), __fmul_rn(x[7], x[7]));
+  const float s = __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+  if (s >= 0x1p-96f && s <= FLT_MAX) return static_cast<double>(s);
+  unsigned int any = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) any |= __float_as_uint(x[k]) & 0x7FFFFFFFu;
+  if (any == 0) return 0.0;
+  double d = 0.0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) d = __dadd_rn(d, __dmul_rn(static_cast<double>(x[k]), static_cast<double>(x[k])));
+  return d;
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const unsigned int w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<unsigned int>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+// Butterfly sum of an fp64 value over the block (fixed order); result valid in thread 0.
+__device__ __forceinline__ double block_sum(double v, double* smem32) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) smem32[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (warp == 0) {
+    r = (lane < static_cast<int>(blockDim.x >> 5)) ? smem32[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = __dadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+  }
+  __syncthreads();
+  return r;
+}
+
+// Publishes this block's partial; the last block to arrive reduces all partials in a fixed
+// order, writes the stats and re-zeroes the arrival counter.
+__device__ __forceinline__ void finish_sumsq(double acc, NormWorkspace* ws, zopt_clip_stats* stats,
+                                             float max_norm) {
+  __shared__ double red[32];
+  __shared__ bool is_last;
+  const double block = block_sum(acc, red);
+  if (threadIdx.x == 0) {
+    ws->partials[blockIdx.x] = block;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&ws->arrive, 1u);
+    is_last = (ticket == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  double a = 0.0;
+  const volatile double* parts = ws->partials;
+  for (unsigned int i = threadIdx.x; i < gridDim.x; i += blockDim.x) a = __dadd_rn(a, parts[i]);
+  const double total = block_sum(a, red);
+  if (threadIdx.x == 0) {
+    write_clip_stats(stats, total, max_norm);
+    ws->arrive = 0u;
+    __threadfence();
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict__ g, int64_t n, float max_norm,
+                                                             NormWorkspace* ws, zopt_clip_stats* stats) {
+  const int64_t nvec = n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  double acc = 0.0;
+  for (; i + stride < nvec; i += 2 * stride) {
+    float x[8], y[8];
+    load8(g + 8 * i, x);
+    load8(g + 8 * (i + stride), y);
+    acc = __dadd_rn(acc, __dadd_rn(sumsq8(x), sumsq8(y)));
+  }
+  if (i < nvec) {
+    float x[8];
+    load8(g + 8 * i, x);
+    acc = __dadd_rn(acc, sumsq8(x));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t k = nvec * 8; k < n; ++k) {
+      const double d = static_cast<double>(load1(g + k));
+      acc = __dadd_rn(acc, __dmul_rn(d, d));
+    }
+  }
+  finish_sumsq(acc, ws, stats, max_norm);
+}
+
+}  // namespace zopt
