@@ -32,13 +32,29 @@ size_t norm_grid_blocks(int64_t n) {
   return static_cast<size_t>(want < kNormMaxBlocks ? want : kNormMaxBlocks);
 }
 
+int norm_launch_blocks(int64_t n, zopt_dtype dtype) {
+  static int occ[2] = {0, 0};  // resident blocks per SM of each instantiation
+  const int k = dtype == ZOPT_F32 ? 0 : 1;
+  if (occ[k] == 0) {
+    int o = 0;
+    const cudaError_t e =
+        k == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, norm_kernel<float>, kNormThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, norm_kernel<__nv_bfloat16>, kNormThreads, 0);
+    if (e != cudaSuccess || o < 1) o = 1;
+    occ[k] = o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  // one wave of resident blocks; never more blocks than the workspace was sized for
+  int64_t blocks = static_cast<int64_t>(norm_grid_blocks(n));
+  const int64_t wave = static_cast<int64_t>(sms) * occ[k];
+  return static_cast<int>(blocks < wave ? blocks : wave);
+}
+
 zopt_status launch_norm(const void* grad, zopt_dtype dtype, int64_t n, float max_norm, NormWorkspace* ws,
                         zopt_clip_stats* stats, cudaStream_t stream) {
-  int sms = sm_count();
-  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_grad_norm_clip: no CUDA device");
-  int64_t blocks = static_cast<int64_t>(norm_grid_blocks(n));
-  const int64_t cap = static_cast<int64_t>(sms) * kNormBlocksPerSm;
-  if (blocks > cap) blocks = cap;
+  const int blocks = norm_launch_blocks(n, dtype);
+  if (blocks <= 0) return fail(ZOPT_ECUDA, "zopt_grad_norm_clip: no CUDA device");
   if (dtype == ZOPT_F32)
     norm_kernel<float><<<static_cast<unsigned>(blocks), kNormThreads, 0, stream>>>(
         static_cast<const float*>(grad), n, max_norm, ws, stats);

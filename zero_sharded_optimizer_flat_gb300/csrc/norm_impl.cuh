@@ -25,6 +25,10 @@ struct NormWorkspace {
 static_assert(offsetof(NormWorkspace, partials) == 256, "workspace header is 256 bytes");
 
 size_t norm_grid_blocks(int64_t n);
+// Blocks one launch over n elements uses on the current device (<= norm_grid_blocks(n)).
+int norm_launch_blocks(int64_t n, zopt_dtype dtype);
+zopt_status check_norm_args(const char* fn, const void* grad, zopt_dtype dtype, int64_t n, float max_norm,
+                            const zopt_clip_stats* stats);
 
 // Stats from a sum of squares, exactly as the pages state the contract (see norm.cu).
 __device__ __forceinline__ void write_clip_stats(zopt_clip_stats* out, double ss, float max_norm) {
