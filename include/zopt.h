@@ -130,6 +130,22 @@ ZOPT_API zopt_status zopt_grad_norm_clip(const void* grad, zopt_dtype dtype, int
  * where a multi-rank job would all-reduce sumsq between zopt_grad_norm_clip and the step. */
 ZOPT_API zopt_status zopt_clip_finalize(zopt_clip_stats* d_stats, float max_norm, zopt_stream stream);
 
+/* zopt_grad_norm_clip without a workspace, for callers that cannot allocate device memory:
+ * a plain-C host or plugin that only receives device pointers from its framework, a training
+ * loop that forbids allocation after start-up, or a process whose device memory another
+ * runtime has already reserved. The source pages have no counterpart to this call; it exists
+ * for those callers only. Same arguments and results as zopt_grad_norm_clip, minus d_ws.
+ * The scratch (an arrival counter and up to 1024 fp64 block partials, 8,448 bytes) is a
+ * file-scope __device__ array that every GPU loading the library holds until the process
+ * exits. The first call on each device looks up that array's device address (once, with the
+ * device current); make that first call before any stream capture. Each call clears the
+ * counter itself. All calls share the one array, so calls that overlap on the GPU (other
+ * streams, unordered host threads) race and give wrong results; order them on one stream.
+ * Errors: those of zopt_grad_norm_clip, and ZOPT_EINVAL when the device's launch would need
+ * more than 1024 block partials (never on a 152-SM GB300). */
+ZOPT_API zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype dtype, int64_t n, float max_norm,
+                                                 zopt_clip_stats* d_stats, zopt_stream stream);
+
 /* ======================================================================================
  * 3. Fused AdamW over the flat fp32 shard
  *

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_norm_workspace": (sz, [i64]),
         "zopt_grad_norm_clip": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, sz, vp, vp]),
         "zopt_clip_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp]),
+        "zopt_grad_norm_clip_noalloc": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, vp]),
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
     }
@@ -232,6 +233,14 @@ def grad_norm_clip(grad, max_norm: float, ws, stats, n: int | None = None, strea
     n = grad.numel() if n is None else int(n)
     _check(lib().zopt_grad_norm_clip(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(ws), ws.numel(),
                                      _ptr(stats), _stream(stream)))
+
+
+def grad_norm_clip_noalloc(grad, max_norm: float, stats, n: int | None = None, stream=None) -> None:
+    """``zopt_grad_norm_clip_noalloc``: the same reduction with the library's static scratch
+    instead of a workspace, for callers that cannot allocate device memory."""
+    n = grad.numel() if n is None else int(n)
+    _check(lib().zopt_grad_norm_clip_noalloc(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(stats),
+                                             _stream(stream)))
 
 
 def clip_finalize(stats, max_norm: float, stream=None) -> None:
