@@ -196,6 +196,40 @@ ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d
                             uint16_t* out_bf16, const zopt_adamw_hparams* hparams,
                             const zopt_clip_stats* d_clip, zopt_adam_state* d_state, zopt_stream stream);
 
+/* ======================================================================================
+ * 4. Muon's quintic Newton-Schulz on whole matrices
+ *
+ * bluscript_zero_ckpt.cpp, ShardedMuon design note: U = NewtonSchulz(M), the iterated matrix
+ * polynomial X <- aX + (bXX' + c(XX')^2)X over the WHOLE matrix (a flat slice would cut it
+ * mid-row, so each matrix has one owner rank); the trainer runs 5 steps.
+ *
+ * X0 = G / (||G||_F + eps); a matrix with more rows than columns is processed as its
+ * transpose (m = min(rows, cols) <= n) and transposed back on output. Per step:
+ * A = X X' (m x m), B = b A + c A A', X = a X + B X. With compute_dtype ZOPT_BF16 the
+ * operands and the products A, B, X are bf16 (round-to-nearest-even) with fp32 accumulation
+ * on the tensor cores. (a, b, c) = abc[0..2] (the pages print no triple; the usual quintic
+ * Muon choice is 3.4445, -4.7750, 2.0315).
+ * ====================================================================================== */
+
+/* Workspace bytes for one rows x cols matrix (0 for an unsupported compute dtype). The
+ * workspace is reused across the matrices of a batch. */
+ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, zopt_dtype compute_dtype);
+/* Orthogonalise `batch` matrices G[b] (rows x cols, row-major, leading dimension ld_g,
+ * matrix b at G + b*batch_stride_g elements) into X[b] (same shape, ld_x, batch_stride_x).
+ *   io_dtype: dtype of G and X (ZOPT_BF16 or ZOPT_F32);
+ *   compute_dtype: ZOPT_BF16 (tcgen05 tensor cores);
+ *   steps >= 1; abc: 3 host floats; eps >= 0 (1e-7 is the usual choice);
+ *   d_ws: at least zopt_ns_workspace(rows, cols, compute_dtype) bytes, 16-byte aligned.
+ * G and X must not overlap. Errors: EINVAL for NULL pointers, empty shapes, dimensions
+ * >= 2^31, leading dimensions < cols, overlapping batch strides, steps < 1, non-finite
+ * coefficients, a short workspace; EUNSUPPORTED for other dtypes; ETIMEOUT when a kernel of
+ * an earlier call gave up on a bounded wait (its results are not valid). */
+ZOPT_API zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io_dtype, int64_t rows, int64_t cols,
+                                           int64_t ld_g, int64_t ld_x, int64_t batch_stride_g,
+                                           int64_t batch_stride_x, int32_t batch, zopt_dtype compute_dtype,
+                                           int32_t steps, const float* abc, float eps, void* d_ws, size_t ws_bytes,
+                                           zopt_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,173 @@
+"""GPU parity of zopt_ns_orthogonalize (bluscript_zero_ckpt.cpp, ShardedMuon note:
+X <- aX + (bXX' + c(XX')^2)X on the whole matrix, 5 steps).
+
+* White box, one step: the normalised X0, A = X0 X0', B = cAA' + bA and the output are read
+  back and each is checked against a float32 product of the kernel's own bf16 inputs
+  (relative Frobenius error <= 4e-3: one bf16 rounding of the output plus fp32 accumulation
+  order); A and B must be exactly symmetric.
+* End to end, 5 steps: relative Frobenius error against the fp64 oracle <= 2e-2 (bf16).
+* Full-size stress matrices: against a float32 torch Newton-Schulz on the GPU (the checker)
+  <= 2e-2, and the oracle on the top-left 256 x 1024 block taken as its own input.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.ns import DEFAULT_ABC, newton_schulz
+
+pytestmark = pytest.mark.gpu
+
+A_, B_, C_ = DEFAULT_ABC
+
+
+def rup(x, a):
+    return -(-x // a) * a
+
+
+def plan(rows, cols):
+    """Offsets of the library's workspace regions (white-box reading of its layout)."""
+    m, n = min(rows, cols), max(rows, cols)
+    ldx, lda = rup(n, 8), rup(m, 8)
+    off_stats = rup(256 + 8 * 4096, 256)
+    off_x0 = rup(off_stats + 256, 1024)
+    xbytes, abytes = rup(m * ldx * 2, 1024), rup(m * lda * 2, 1024)
+    return dict(m=m, n=n, ldx=ldx, lda=lda, x0=off_x0, x1=off_x0 + xbytes, a=off_x0 + 2 * xbytes,
+                b=off_x0 + 2 * xbytes + abytes)
+
+
+def region(ws, off, rows, ld, cols):
+    return ws[off:off + rows * ld * 2].view(torch.bfloat16).view(rows, ld)[:, :cols].float()
+
+
+def rel(a, b):
+    a, b = a.double(), b.double()
+    return float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
+
+
+def gaussian(rows, cols, seed, dtype=torch.bfloat16):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return torch.randn(rows, cols, generator=g, device="cuda").to(dtype)
+
+
+SHAPES_WB = [(256, 1024), (1024, 256), (300, 300), (200, 333), (130, 70), (1, 64), (64, 1), (17, 100), (768, 2304),
+             (384, 640)]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_WB)
+def test_one_step_white_box(zopt, rows, cols):
+    G = gaussian(rows, cols, rows * 7 + cols)
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(rows, cols)
+    zopt.ns_orthogonalize(G, X, ws, steps=1)
+    torch.cuda.synchronize()
+    p = plan(rows, cols)
+    m, n = p["m"], p["n"]
+    Gd = G.double()
+    ref0 = Gd / (torch.linalg.norm(Gd) + 1e-7)
+    if rows > cols:
+        ref0 = ref0.T
+    X0 = region(ws, p["x0"], m, p["ldx"], n)
+    assert rel(X0, ref0) < 4e-3
+    A = region(ws, p["a"], m, p["lda"], m)
+    assert torch.equal(A, A.T)
+    assert rel(A, X0 @ X0.T) < 4e-3
+    B = region(ws, p["b"], m, p["lda"], m)
+    assert torch.equal(B, B.T)
+    assert rel(B, C_ * (A @ A) + B_ * A) < 4e-3
+    out = X.float() if rows <= cols else X.float().T
+    assert rel(out, A_ * X0 + B @ X0) < 4e-3
+
+
+SHAPES_E2E = [(256, 768), (256, 256), (256, 1536), (768, 256),        # tiny decoder
+              (768, 2304), (768, 768), (768, 3072), (3072, 768),       # GPT-2-small body
+              (256, 1024), (1000, 1000), (129, 257), (1, 8), (8, 1), (5, 3)]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_E2E)
+def test_five_steps_match_fp64_oracle(zopt, rows, cols):
+    G = gaussian(rows, cols, rows + 31 * cols)
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(rows, cols)
+    zopt.ns_orthogonalize(G, X, ws, steps=5)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5)
+    err = rel(X.cpu(), torch.from_numpy(ref))
+    assert err <= 2e-2, err
+
+
+def test_fp32_io_and_batch_strides(zopt):
+    rows, cols, batch = 384, 1000, 3
+    G = torch.randn(batch, rows, cols + 24, device="cuda")[:, :, :cols]  # padded rows: ld > cols
+    X = torch.zeros(batch, rows, cols + 8, device="cuda")[:, :, :cols]
+    ws = zopt.new_ns_workspace(rows, cols)
+    zopt.ns_orthogonalize(G, X, ws, steps=5)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref = newton_schulz(G[b].double().cpu().numpy(), steps=5)
+        assert rel(X[b].cpu(), torch.from_numpy(ref)) <= 2e-2
+        one = torch.empty(rows, cols, device="cuda")
+        zopt.ns_orthogonalize(G[b].contiguous(), one, ws, steps=5)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X[b])  # a batch entry is bitwise the single call
+
+
+def test_deterministic(zopt):
+    G = gaussian(768, 3072, 1)
+    ws = zopt.new_ns_workspace(768, 3072)
+    outs = []
+    for _ in range(2):
+        X = torch.empty_like(G)
+        zopt.ns_orthogonalize(G, X, ws, steps=5)
+        outs.append(X)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
+def torch_ns_fp32(G, steps=5, abc=DEFAULT_ABC, eps=1e-7):
+    a, b, c = abc
+    X = G.float()
+    X = X / (torch.linalg.norm(X) + eps)
+    tr = X.shape[0] > X.shape[1]
+    if tr:
+        X = X.T
+    for _ in range(steps):
+        A = X @ X.T
+        B = b * A + c * (A @ A)
+        X = a * X + B @ X
+    return X.T if tr else X
+
+
+@pytest.mark.parametrize("rows,cols", [(4096, 4096), (4096, 14336), (14336, 4096)])
+def test_stress_shapes_against_fp32_checker(zopt, rows, cols):
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        G = gaussian(rows, cols, rows ^ cols)
+        G = (G.float() / torch.linalg.norm(G.float())).to(torch.bfloat16)  # Frobenius-normalised input
+        X = torch.empty_like(G)
+        ws = zopt.new_ns_workspace(rows, cols)
+        zopt.ns_orthogonalize(G, X, ws, steps=5)
+        ref = torch_ns_fp32(G)
+        torch.cuda.synchronize()
+        assert rel(X.float(), ref) <= 2e-2
+        # the top-left 256 x 1024 block as its own input, against the fp64 oracle
+        blk = G[:256, :1024].contiguous()
+        Xb = torch.empty_like(blk)
+        zopt.ns_orthogonalize(blk, Xb, zopt.new_ns_workspace(256, 1024), steps=5)
+        torch.cuda.synchronize()
+        refb = newton_schulz(blk.double().cpu().numpy(), steps=5)
+        assert rel(Xb.cpu(), torch.from_numpy(refb)) <= 2e-2
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def test_rejects_bad_arguments(zopt):
+    G = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(8, 8)
+    with pytest.raises(zopt.ZoptError):
+        zopt.ns_orthogonalize(G, X, ws, steps=0)
+    with pytest.raises(zopt.ZoptError):
+        zopt.ns_orthogonalize(G, X, ws[:16], steps=5)
+    with pytest.raises(zopt.ZoptError):
+        zopt.ns_orthogonalize(G, X, ws, abc=(float("nan"), 1.0, 1.0))

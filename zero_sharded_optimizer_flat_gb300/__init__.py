@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_norm_clip_noalloc": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, vp]),
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
+        "zopt_ns_workspace": (sz, [i64, i64, ctypes.c_int]),
+        "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
+                                                 ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
+                                                 vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -255,3 +259,33 @@ def adamw_step(layout: ShardLayout, table, master, exp_avg, exp_avg_sq, grad, ou
     _check(lib().zopt_adamw_step(layout.handle, _ptr(table), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
                                  _ptr(grad), _dtype_code(grad), _ptr(out_bf16), ctypes.byref(hp),
                                  _ptr(clip_stats), _ptr(adam_state), _stream(stream)))
+
+
+# --------------------------------------------------------------------------- Newton-Schulz
+
+DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
+
+
+def ns_workspace(rows: int, cols: int, compute=BF16) -> int:
+    return int(lib().zopt_ns_workspace(int(rows), int(cols), int(compute)))
+
+
+def new_ns_workspace(rows: int, cols: int, compute=BF16, device="cuda"):
+    import torch
+    return torch.empty(max(ns_workspace(rows, cols, compute), 16), dtype=torch.uint8, device=device)
+
+
+def ns_orthogonalize(G, X, ws, steps: int = 5, abc=DEFAULT_ABC, eps: float = 1e-7, compute=BF16, stream=None) -> None:
+    """``zopt_ns_orthogonalize`` of a 2-D matrix or a batch [b, rows, cols] (last dim contiguous)."""
+    if G.dim() == 2:
+        batch, rows, cols = 1, G.shape[0], G.shape[1]
+        ldg, ldx, sg, sx = G.stride(0), X.stride(0), 0, 0
+    else:
+        batch, rows, cols = G.shape
+        ldg, ldx, sg, sx = G.stride(1), X.stride(1), G.stride(0), X.stride(0)
+    if G.stride(-1) != 1 or X.stride(-1) != 1 or G.dtype != X.dtype or X.shape != G.shape:
+        raise ValueError("G and X must have the same shape and dtype, with a contiguous last dimension")
+    coef = (ctypes.c_float * 3)(*[float(c) for c in abc])
+    _check(lib().zopt_ns_orthogonalize(_ptr(G), _ptr(X), _dtype_code(G), rows, cols, ldg, ldx, sg, sx, batch,
+                                       int(compute), int(steps), coef, float(eps), _ptr(ws), ws.numel(),
+                                       _stream(stream)))

@@ -1,0 +1,640 @@
+// Muon's quintic Newton-Schulz orthogonalisation on whole matrices, on tcgen05 tensor cores.
+//
+// bluscript_zero_ckpt.cpp, ShardedMuon design note: U = NewtonSchulz(M), the iterated matrix
+// polynomial X <- aX + (bXX' + c(XX')^2)X, in which every output entry depends on the whole
+// matrix (so each matrix has one owner rank); 5 steps in the trainer's config.
+//
+// Per step, with X m x n (m <= n; a taller input is processed as its transpose):
+//   A = X X'            (symmetric: only 128x256 tiles touching the upper triangle are
+//                        computed, each writes its upper part directly and its strictly upper
+//                        part mirrored)
+//   B = c A A' + b A    (A is symmetric, so A^2 = A A': the same symmetric kernel, with the
+//                        b*A term added in the epilogue)
+//   X = B X + a X       (plain GEMM whose B-operand X is read MN-major straight from its
+//                        row-major layout; the last step writes the caller's output, in the
+//                        caller's orientation and dtype)
+// Operands and the products A, B, X are bf16; every product accumulates in fp32 in TMEM.
+//
+// One kernel does all three products: a persistent, warp-specialised tcgen05 GEMM. Warp 0
+// streams 128x64 and 256x64 bf16 tiles into a 4-stage shared-memory ring with TMA (128-byte
+// swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
+// accumulators (2 x 256 fp32 columns), committing stage release and accumulator-ready events
+// to mbarriers; warps 2-5 drain the other accumulator (tcgen05.ld), apply alpha*acc +
+// beta*R and store bf16/fp32 while the next tile is being multiplied. Every mbarrier wait is
+// bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "norm_impl.cuh"
+#include "tc.cuh"
+
+namespace zopt {
+namespace ns {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kTileA = BM * BK * 2;          // 16 KiB
+constexpr int kTileB = BN * BK * 2;          // 32 KiB
+constexpr int kBoxMN = 64 * BK * 2;          // one 64 (MN) x 64 (K) box of an MN-major operand
+constexpr int kGemmThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTmemCols = 2 * BN;            // two fp32 accumulators of 128 x 256
+constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256;
+
+struct GemmArgs {
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles;
+  int symmetric;   // M == N and D symmetric: upper-triangle tiles only, mirrored writes
+  int b_mn_major;  // the B-operand is stored [K][N] (N contiguous)
+  float alpha, beta;
+  const __nv_bfloat16* R;  // D += beta * R[i, j] (bf16, row-major, ldr); may be null if beta == 0
+  long long ldr;
+  void* D;  // bf16 or fp32
+  long long ldd;
+  int d_f32;
+  int d_trans;  // write D[i, j] to D[j * ldd + i]
+  int* err;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& ti, int& tj) {
+  if (!a.symmetric) {
+    // column-major raster: the tiles running together share the B-operand columns, and the
+    // whole A-operand (m x m) stays in L2
+    ti = t % a.tiles_m;
+    tj = t / a.tiles_m;
+    return;
+  }
+  // row ti holds tiles tj = ti/2 .. tiles_n-1 (BN = 2 BM): those touching col >= row
+  int r = 0;
+  for (;;) {
+    const int cnt = a.tiles_n - r / 2;
+    if (t < cnt) {
+      ti = r;
+      tj = r / 2 + t;
+      return;
+    }
+    t -= cnt;
+    ++r;
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = tc::globaltimer();
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (tc::globaltimer() - t0 > tc::kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void store1(const GemmArgs& a, long long off, float v) {
+  if (a.d_f32)
+    static_cast<float*>(a.D)[off] = v;
+  else
+    static_cast<__nv_bfloat16*>(a.D)[off] = __float2bfloat16_rn(v);
+}
+
+// 32 consecutive outputs of row i starting at column j0 (all < N), row-major.
+__device__ __forceinline__ void store_row32(const GemmArgs& a, int i, int j0, const float (&o)[32]) {
+  const long long off = static_cast<long long>(i) * a.ldd + j0;
+  if (a.d_f32) {
+    float* p = static_cast<float*>(a.D) + off;
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(p)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) p[k] = o[k];
+    }
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(a.D) + off;
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(o[8 * q + 0], o[8 * q + 1]);
+        __nv_bfloat162 h1 = __floats2bfloat162_rn(o[8 * q + 2], o[8 * q + 3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * q + 4], o[8 * q + 5]);
+        __nv_bfloat162 h3 = __floats2bfloat162_rn(o[8 * q + 6], o[8 * q + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&h0);
+        u.y = *reinterpret_cast<uint32_t*>(&h1);
+        u.z = *reinterpret_cast<uint32_t*>(&h2);
+        u.w = *reinterpret_cast<uint32_t*>(&h3);
+        reinterpret_cast<uint4*>(p)[q] = u;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) p[k] = __float2bfloat16_rn(o[k]);
+    }
+  }
+}
+
+// Epilogue of 32 accumulator columns [j0, j0+32) of row i.
+__device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, const uint32_t (&v)[32]) {
+  if (i >= a.M) return;
+  float o[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
+  const bool full = j0 + 32 <= a.N;
+  if (a.beta != 0.0f) {
+    const __nv_bfloat16* r = a.R + static_cast<long long>(i) * a.ldr + j0;
+    if (full && (reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(r + 8 * q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          o[8 * q + 2 * h] += a.beta * __uint_as_float(w[h] << 16);
+          o[8 * q + 2 * h + 1] += a.beta * __uint_as_float(w[h] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (j0 + k < a.N) o[k] += a.beta * __bfloat162float(r[k]);
+    }
+  }
+  if (!a.symmetric) {
+    if (!a.d_trans) {
+      if (full) {
+        store_row32(a, i, j0, o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (j0 + k < a.N) store1(a, static_cast<long long>(i) * a.ldd + j0 + k, o[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (j0 + k < a.N) store1(a, static_cast<long long>(j0 + k) * a.ldd + i, o[k]);
+    }
+    return;
+  }
+  // symmetric: upper part (j >= i) written in place, strictly upper part mirrored to (j, i)
+  if (full && j0 >= i) {
+    store_row32(a, i, j0, o);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int j = j0 + k;
+      if (j < a.N && j >= i) store1(a, static_cast<long long>(i) * a.ldd + j, o[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int j = j0 + k;
+    if (j < a.N && j > i) store1(a, static_cast<long long>(j) * a.ldd + i, o[k]);
+  }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+                     const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kTileA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kTileB);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tfull + b, 1);
+      tc::mbar_init(tempty + b, 128);
+    }
+    tc::mbar_init(drain, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmP);
+    tc::prefetch_tmap(&tmQ);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const int nk = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int armed[STAGES];
+      for (int q = 0; q < STAGES; ++q) armed[q] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
+        int ti, tj;
+        tile_coords(a, t, ti, tj);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(empty + s, ph ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(full + s, kTileA + kTileB);
+          armed[s] = static_cast<int>(ph);
+          tc::tma_load_2d(sA + s * kTileA, &tmP, full + s, kb * BK, ti * BM);
+          if (!a.b_mn_major) {
+            tc::tma_load_2d(sB + s * kTileB, &tmQ, full + s, kb * BK, tj * BN);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tc::tma_load_2d(sB + s * kTileB + q * kBoxMN, &tmQ, full + s, tj * BN + 64 * q, kb * BK);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // leave no copy in flight: wait (bounded) for every stage armed last
+        for (int q = 0; q < STAGES; ++q)
+          if (armed[q] >= 0) mbar_wait_drain(full + q, static_cast<uint32_t>(armed[q]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, false, a.b_mn_major != 0);
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, ++it) {
+        const int b = it & 1;
+        const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!tc::mbar_wait(tempty + b, tph ^ 1u, a.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(full + s, ph, a.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t abase = tc::smem_u32(sA + s * kTileA);
+          const uint32_t bbase = tc::smem_u32(sB + s * kTileB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(abase + 32u * kk, 16u, 1024u);
+            const uint64_t bd = a.b_mn_major ? tc::smem_desc_sw128(bbase + 2048u * kk, kBoxMN, 1024u)
+                                             : tc::smem_desc_sw128(bbase + 32u * kk, 16u, 1024u);
+            tc::umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc::umma_commit(empty + s);  // the stage is free once these MMAs have read it
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit(tfull + b);  // accumulator b is complete
+      }
+      tc::umma_commit(drain);  // no MMA may still be running when TMEM is released
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int quad = warp & 3;  // this warp may read TMEM lanes [32 quad, 32 quad + 32)
+    const int row = 32 * quad + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc::fence_after_sync();
+      int ti, tj;
+      tile_coords(a, t, ti, tj);
+      const int i = ti * BM + row;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 32 * c), v);
+        tc::tmem_wait_ld();
+        if (c == BN / 32 - 1) {
+          tc::fence_before_sync();
+          tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
+        }
+        epilogue32(a, i, tj * BN + 32 * c, v);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------- prep kernels
+
+// sum of squares of a rows x cols matrix with leading dimension ld (elements).
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) matrix_sumsq_kernel(const T* __restrict__ g, long long rows,
+                                                                     long long cols, long long ld, int vec_ok,
+                                                                     NormWorkspace* ws, zopt_clip_stats* stats) {
+  double acc = 0.0;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long c8 = vec_ok ? cols / 8 : 0;
+  if (c8 > 0) {
+    const long long nvec = rows * c8;
+    for (long long e = tid; e < nvec; e += stride) {
+      const long long r = e / c8, c = e - r * c8;
+      float x[8];
+      load8(g + r * ld + 8 * c, x);
+      acc = __dadd_rn(acc, sumsq8(x));
+    }
+  }
+  const long long tail = cols - 8 * c8;  // scalar columns [8 c8, cols) of every row
+  if (tail > 0) {
+    const long long ntail = rows * tail;
+    for (long long e = tid; e < ntail; e += stride) {
+      const long long r = e / tail, c = 8 * c8 + (e - r * tail);
+      const double d = static_cast<double>(load1(g + r * ld + c));
+      acc = __dadd_rn(acc, __dmul_rn(d, d));
+    }
+  }
+  finish_sumsq(acc, ws, stats, 0.0f);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// X0 = G / (||G||_F + eps) in bf16, oriented so that X0 is m x n with m <= n.
+template <typename T>
+__global__ void scale_orient_kernel(const T* __restrict__ g, long long rows, long long cols, long long ld,
+                                    int transpose, const zopt_clip_stats* stats, double eps,
+                                    __nv_bfloat16* __restrict__ x, long long ldx) {
+  __shared__ float s_inv;
+  __shared__ float tile[32][33];
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    const double nrm = __dsqrt_rn(stats->sumsq);
+    s_inv = __double2float_rn(__ddiv_rn(1.0, __dadd_rn(nrm, eps)));
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  const long long tiles_c = (cols + 31) / 32, tiles_r = (rows + 31) / 32;
+  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
+    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
+    if (!transpose) {
+      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
+        const long long r = r0 + yy, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) x[r * ldx + c] = __float2bfloat16_rn(to_f32(g[r * ld + c]) * inv);
+      }
+    } else {
+      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
+        const long long r = r0 + yy, c = c0 + threadIdx.x;
+        tile[yy][threadIdx.x] = (r < rows && c < cols) ? to_f32(g[r * ld + c]) * inv : 0.0f;
+      }
+      __syncthreads();
+      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
+        const long long xr = c0 + yy, xc = r0 + threadIdx.x;  // X0[c][r] = G[r][c]
+        if (xr < cols && xc < rows) x[xr * ldx + xc] = __float2bfloat16_rn(tile[threadIdx.x][yy]);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor map over a row-major [outer][inner] matrix with `pitch` elements per row.
+zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long pitch,
+                     int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled failed (" + std::to_string(r) + ")");
+  return ok();
+}
+
+// Error word written by timed-out kernels: mapped pinned host memory, so the next call can
+// read it without synchronising the device.
+zopt_status error_word(int** host, int** dev) {
+  static int* h = nullptr;
+  static int* d = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (h == nullptr) {
+    void* p = nullptr;
+    ZOPT_CUDA_TRY(cudaHostAlloc(&p, 64, cudaHostAllocMapped | cudaHostAllocPortable));
+    h = static_cast<int*>(p);
+    *h = 0;
+    void* dp = nullptr;
+    ZOPT_CUDA_TRY(cudaHostGetDevicePointer(&dp, p, 0));
+    d = static_cast<int*>(dp);
+  }
+  *host = h;
+  *dev = d;
+  return ok();
+}
+
+long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  long long m, n, ldx, lda;
+  size_t off_stats, off_x0, off_x1, off_a, off_b, total;
+};
+
+Plan plan(long long rows, long long cols) {
+  Plan p;
+  p.m = rows < cols ? rows : cols;
+  p.n = rows < cols ? cols : rows;
+  p.ldx = round_up(p.n, 8);
+  p.lda = round_up(p.m, 8);
+  p.off_stats = 256 + sizeof(double) * static_cast<size_t>(kNormMaxBlocks);
+  p.off_stats = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats), 256));
+  p.off_x0 = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats + 256), 1024));
+  const size_t xbytes = static_cast<size_t>(round_up(p.m * p.ldx * 2, 1024));
+  const size_t abytes = static_cast<size_t>(round_up(p.m * p.lda * 2, 1024));
+  p.off_x1 = p.off_x0 + xbytes;
+  p.off_a = p.off_x1 + xbytes;
+  p.off_b = p.off_a + abytes;
+  p.total = p.off_b + abytes;
+  return p;
+}
+
+zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    attr_set = true;
+  }
+  a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
+  a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+  if (a.symmetric) {
+    long long cnt = 0;
+    for (int r = 0; r < a.tiles_m; ++r) cnt += a.tiles_n - r / 2;
+    a.num_tiles = static_cast<int>(cnt);
+  } else {
+    a.num_tiles = a.tiles_m * a.tiles_n;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
+  const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+  gemm_bf16_kernel<<<grid, kGemmThreads, kSmemBytes, stream>>>(P, Q, a);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+}  // namespace ns
+}  // namespace zopt
+
+extern "C" size_t zopt_ns_workspace(int64_t rows, int64_t cols, zopt_dtype compute_dtype) {
+  if (rows < 1 || cols < 1 || compute_dtype != ZOPT_BF16) return 0;
+  return zopt::ns::plan(rows, cols).total;
+}
+
+extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io_dtype, int64_t rows, int64_t cols,
+                                             int64_t ld_g, int64_t ld_x, int64_t batch_stride_g,
+                                             int64_t batch_stride_x, int32_t batch, zopt_dtype compute_dtype,
+                                             int32_t steps, const float* abc, float eps, void* d_ws,
+                                             size_t ws_bytes, zopt_stream stream) {
+  using namespace zopt;
+  using namespace zopt::ns;
+  if (G == nullptr || X == nullptr || d_ws == nullptr || abc == nullptr)
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: NULL pointer");
+  if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: empty matrix or batch");
+  if (rows > (1LL << 31) || cols > (1LL << 31)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: dimension >= 2^31");
+  if (ld_g < cols || ld_x < cols) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: leading dimension < cols");
+  if (batch > 1 && (batch_stride_g < rows * ld_g || batch_stride_x < rows * ld_x))
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: batch strides overlap the matrices");
+  if (steps < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: steps < 1");
+  if (io_dtype != ZOPT_F32 && io_dtype != ZOPT_BF16)
+    return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: input/output dtype must be fp32 or bf16");
+  if (compute_dtype != ZOPT_BF16)
+    return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: compute dtype must be bf16 (tcgen05 path)");
+  if (!std::isfinite(abc[0]) || !std::isfinite(abc[1]) || !std::isfinite(abc[2]) || !std::isfinite(eps) || eps < 0)
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: coefficients and eps must be finite (eps >= 0)");
+  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace is not 16-byte aligned");
+  const Plan p = plan(rows, cols);
+  if (ws_bytes < p.total) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace smaller than zopt_ns_workspace");
+  int* err_host = nullptr;
+  int* err_dev = nullptr;
+  zopt_status st = error_word(&err_host, &err_dev);
+  if (st != ZOPT_OK) return st;
+  if (*reinterpret_cast<volatile int*>(err_host) != 0) {
+    *reinterpret_cast<volatile int*>(err_host) = 0;
+    return fail(ZOPT_ETIMEOUT, "zopt_ns_orthogonalize: a tensor-core kernel of an earlier call timed out on a wait");
+  }
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  NormWorkspace* nws = reinterpret_cast<NormWorkspace*>(ws);
+  zopt_clip_stats* nstats = reinterpret_cast<zopt_clip_stats*>(ws + p.off_stats);
+  __nv_bfloat16* xb[2] = {reinterpret_cast<__nv_bfloat16*>(ws + p.off_x0),
+                          reinterpret_cast<__nv_bfloat16*>(ws + p.off_x1)};
+  __nv_bfloat16* A = reinterpret_cast<__nv_bfloat16*>(ws + p.off_a);
+  __nv_bfloat16* B = reinterpret_cast<__nv_bfloat16*>(ws + p.off_b);
+  const bool transpose = rows > cols;
+
+  // Tensor maps over the workspace matrices (the same for every matrix of the batch).
+  CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
+  for (int q = 0; q < 2; ++q) {
+    if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, 64, BN)) != ZOPT_OK) return st;
+    if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, 64, BK)) != ZOPT_OK) return st;
+  }
+  if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+  if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, 64, BN)) != ZOPT_OK) return st;
+  if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+
+  const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
+  for (int bi = 0; bi < batch; ++bi) {
+    const uint8_t* g = static_cast<const uint8_t*>(G) + static_cast<size_t>(bi) * batch_stride_g * esz;
+    uint8_t* xo = static_cast<uint8_t*>(X) + static_cast<size_t>(bi) * batch_stride_x * esz;
+    // X0 = G / (||G||_F + eps), oriented
+    ZOPT_CUDA_TRY(cudaMemsetAsync(nws, 0, sizeof(unsigned int), s));
+    const int vec_ok = ((reinterpret_cast<uintptr_t>(g) & 15u) == 0 && (ld_g * esz) % 16 == 0) ? 1 : 0;
+    const int nblk = sms * 4;
+    if (io_dtype == ZOPT_F32)
+      matrix_sumsq_kernel<float><<<nblk, kNormThreads, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
+                                                               vec_ok, nws, nstats);
+    else
+      matrix_sumsq_kernel<__nv_bfloat16><<<nblk, kNormThreads, 0, s>>>(
+          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, vec_ok, nws, nstats);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+    const dim3 tb(32, 8);
+    if (io_dtype == ZOPT_F32)
+      scale_orient_kernel<float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
+                                                        transpose ? 1 : 0, nstats, eps, xb[0], p.ldx);
+    else
+      scale_orient_kernel<__nv_bfloat16><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g), rows,
+                                                                cols, ld_g, transpose ? 1 : 0, nstats, eps, xb[0],
+                                                                p.ldx);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+
+    int cur = 0;
+    for (int it = 0; it < steps; ++it) {
+      const bool last = it == steps - 1;
+      GemmArgs ga{};
+      ga.err = err_dev;
+      // A = X X'
+      ga.M = static_cast<int>(p.m); ga.N = static_cast<int>(p.m); ga.K = static_cast<int>(p.n);
+      ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
+      ga.D = A; ga.ldd = p.lda; ga.d_f32 = 0; ga.d_trans = 0;
+      if ((st = launch_gemm(mx_p[cur], mx_q[cur], ga, s)) != ZOPT_OK) return st;
+      // B = c A A' + b A
+      ga.K = static_cast<int>(p.m);
+      ga.alpha = abc[2]; ga.beta = abc[1]; ga.R = A; ga.ldr = p.lda; ga.D = B; ga.ldd = p.lda;
+      if ((st = launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
+      // X = B X + a X
+      ga.M = static_cast<int>(p.m); ga.N = static_cast<int>(p.n); ga.K = static_cast<int>(p.m);
+      ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0]; ga.R = xb[cur]; ga.ldr = p.ldx;
+      if (!last) {
+        ga.D = xb[cur ^ 1]; ga.ldd = p.ldx; ga.d_f32 = 0; ga.d_trans = 0;
+      } else {
+        ga.D = xo; ga.ldd = ld_x; ga.d_f32 = io_dtype == ZOPT_F32 ? 1 : 0; ga.d_trans = transpose ? 1 : 0;
+      }
+      if ((st = launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK) return st;
+      cur ^= 1;
+    }
+  }
+  return ok();
+}
