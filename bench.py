@@ -2,14 +2,19 @@
 
 One step = the whole hot path over one batch of synthetic input:
   * the ZeRO-2 flat AdamW shard of a 2e9-parameter model, rank r of W=8 (S = 250,000,000):
-    gradient norm / clip / found_inf (zopt_grad_norm_clip) then the fused AdamW update with
-    bf16 round-out (zopt_adamw_step);
-Inputs are resident in HBM and far larger than L2 (4.5 GB per step), so no L2 flush is
-needed between steps.
+    4 bf16 micro-step gradients summed into the fp32 shard gradient, the last pass also
+    producing the norm / clip / found_inf stats (zopt_grad_accumulate), then the fused AdamW
+    update with bf16 round-out (zopt_adamw_step);
+  * Muon's Newton-Schulz (5 steps, bf16) on the stress set of 48 whole matrices: 16 each of
+    4096x4096, 4096x14336 and 14336x4096 (zopt_ns_orthogonalize, one batched call per shape).
+Inputs are resident in HBM and far larger than L2 (~13 GB touched per step), so no L2 flush
+is needed between steps. `value` is the AdamW part's HBM throughput (66 algorithmic bytes per
+shard element: 36 for the accumulation, 30 for the update, / the part's time); `ns.value` the
+Newton-Schulz TFLOP/s (algorithmic flops, symmetric halves counted once).
 
 `python bench.py [--gpus N --steps K --warmup W] [--impl reference]` prints one JSON line.
-Under torchrun (N > 1) every process simulates a different rank of the W=8 job (weak
-scaling: no data-path collective); rank 0 prints.
+Under torchrun (N > 1) every process simulates a different rank of the W=8 job and runs its
+own copy of the Newton-Schulz set (weak scaling: no data-path collective); rank 0 prints.
 """
 from __future__ import annotations
 
@@ -26,9 +31,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "AdamW shard step HBM GB/s (% peak); Newton-Schulz TFLOP/s (% bf16 peak)"
-WORKLOAD = "zero2-flat-shard-2e9-w8: AdamW+clip over rank r of W=8 (S=250,000,000 fp32 master/m/v, fp32 grad)"
+WORKLOAD = ("zero2-flat-shard-2e9-w8 + ns-stress-48: rank r of W=8 (S=250,000,000): 4 bf16 micro-step grads "
+            "summed into fp32 with the clip stats fused into the last pass, then AdamW with bf16 round-out; "
+            "Newton-Schulz (5 steps, bf16) on 16 x 4096^2, 16 x 4096x14336, 16 x 14336x4096")
 ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m, v (12) + bf16 (2)
-NORM_BYTES = 4     # per element: read the fp32 grad
+MICRO_STEPS = 4
+ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 CPU_SAMPLE = 4_000_000
 
 
@@ -113,12 +121,15 @@ def smi_id(local_rank: int) -> str:
 
 def cpu_oracle_run(seconds: float = 10.0) -> dict:
     """The oracle as it stands (numpy, one core) on a bounded sample of the same workload:
-    norm/clip then AdamW over CPU_SAMPLE shard elements, repeated for ~`seconds`."""
+    4 bf16 micro-steps summed in fp32, norm/clip, AdamW and the bf16 round-out over
+    CPU_SAMPLE shard elements, repeated for ~`seconds`."""
     import numpy as np
+    import torch
 
     import workloads
     from oracle import adamw as OA
     from oracle import clip as OC
+    from oracle.accum import accumulate
     from oracle.bf16 import f32_to_bf16_bits
 
     w = workloads.get("c4")
@@ -129,9 +140,11 @@ def cpu_oracle_run(seconds: float = 10.0) -> dict:
     v = np.zeros(n, np.float32)
     mask = np.ones(n, np.uint8)
     mask[::1000] = 0
-    g = workloads.shard_vector(n, 1e-3, w.seed, 2).numpy()
+    micro = [workloads.shard_vector(n, 1e-3, w.seed, 2 + k, dtype=torch.bfloat16).float().numpy()
+             for k in range(MICRO_STEPS)]
     steps, t0 = 0, time.perf_counter()
     while True:
+        g = accumulate(micro)
         st = OC.clip_stats(g, w.max_norm)
         OA.step_flat_f32(p, m, v, g, mask, st["clip_coef"], h, steps + 1)
         f32_to_bf16_bits(p)
@@ -139,23 +152,84 @@ def cpu_oracle_run(seconds: float = 10.0) -> dict:
         el = time.perf_counter() - t0
         if el >= seconds and steps >= 2:
             break
-    gbs = (ADAMW_BYTES + NORM_BYTES) * n * steps / el / 1e9
+    gbs = (ACC_BYTES + ADAMW_BYTES) * n * steps / el / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} steps of norm/clip + AdamW + bf16 round-out over {n:,} shard elements "
-                      f"(numpy fp32 exact-order oracle, {el:.1f} s)"}
+            "sample": f"{steps} steps of 4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out "
+                      f"over {n:,} shard elements (numpy fp32 exact-order oracle, {el:.1f} s)"}
+
+
+def ns_flops(rows: int, cols: int, steps: int) -> float:
+    """Algorithmic flops of one call, symmetric halves counted once: per step
+    m(m+1)n (X X') + m^2(m+1) (A A') + 2 m^2 n (B X), with m <= n."""
+    m, n = min(rows, cols), max(rows, cols)
+    return float(steps) * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
+
+
+def cpu_oracle_ns(seconds: float = 6.0) -> dict:
+    """The fp64 Newton-Schulz oracle on a 256 x 1024 block shaped like the stress set's,
+    repeated for ~`seconds`; numpy's BLAS uses the host's threads."""
+    import numpy as np
+    import torch
+
+    import workloads
+    from oracle.ns import newton_schulz
+
+    g = workloads.ns_input(256, 1024, 5, 0, dtype=torch.float32).numpy().astype(np.float64)
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        newton_schulz(g, steps=5)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and calls >= 2:
+            break
+    flops = ns_flops(256, 1024, 5) * calls
+    return {"value": round(flops / el / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{calls} fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set ({el:.1f} s)"}
 
 
 def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
-    cpu = cpu_oracle_run(seconds=max(5.0, min(25.0, 2.0 * args.steps)))
+    cpu = cpu_oracle_run(seconds=max(5.0, min(20.0, 2.0 * args.steps)))
+    ns = cpu_oracle_ns(seconds=5.0)
     line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
-            "cpu_baseline": cpu, "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
-                                         "d2h_bytes_per_step": 0}}
+            "ns": {"value": ns["value"], "unit": "TFLOP/s"},
+            "cpu_baseline": cpu, "cpu_baseline_ns": ns,
+            "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+class NsPart:
+    """The Newton-Schulz stress set: bf16 matrices of three shapes, one batched call per shape."""
+
+    def __init__(self, Z, torch, seed: int, steps: int, count_limit: int = 0):
+        import workloads
+        self.Z, self.steps = Z, steps
+        w = workloads.get("c5")
+        shapes = []
+        for prm in w.muon:
+            if prm.shape not in shapes:
+                shapes.append(prm.shape)
+        self.groups = []
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        for (r, c) in shapes:
+            count = sum(1 for prm in w.muon if prm.shape == (r, c))
+            if count_limit > 0:
+                count = min(count, count_limit)
+            G = torch.randn(count, r, c, device="cuda", generator=gen)
+            G /= torch.linalg.vector_norm(G, dim=(1, 2), keepdim=True)  # Frobenius-normalised
+            G = G.to(torch.bfloat16)
+            self.groups.append((G, torch.empty_like(G)))
+        self.ws = torch.empty(max(Z.ns_workspace(r, c) for r, c in shapes), dtype=torch.uint8, device="cuda")
+        self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
+        self.launches = sum(G.shape[0] * (2 + 3 * steps) for G, _ in self.groups)
+
+    def run(self, stream):
+        for G, X in self.groups:
+            self.Z.ns_orthogonalize(G, X, self.ws, steps=self.steps, stream=stream)
 
 
 def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
@@ -171,36 +245,63 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     if world_procs > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    parts = set(args.parts.split(","))
+    stream = torch.cuda.current_stream()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    mean = lambda evs: statistics.mean(a.elapsed_time(b) for a, b in evs)  # noqa: E731
 
+    # ---- part 1: micro-step accumulation with fused clip stats + AdamW over this rank's shard
     w = workloads.get("c4")
     sim_rank = rank % w.world
     lay = Z.ShardLayout([p.numel for p in w.adamw], [p.decay for p in w.adamw], w.bucket, w.world, sim_rank)
     S = lay.shard_len if args.shard_len <= 0 else min(args.shard_len, lay.shard_len)
     if S != lay.shard_len:  # a prefix of the same parameter list, as its own layout
         lay = Z.ShardLayout([S], [1], 1 << 40, 1, 0)
-    table = lay.device_table()
-    gen = torch.Generator(device="cuda").manual_seed(w.seed * 100 + sim_rank)
-    p = torch.randn(S, device="cuda", generator=gen).mul_(0.02)
-    m = torch.zeros(S, device="cuda")
-    v = torch.zeros(S, device="cuda")
-    g = torch.randn(S, device="cuda", generator=gen).mul_(1e-3)
-    out = torch.empty(S, dtype=torch.int16, device="cuda")
-    clip, state = Z.new_clip_stats(), Z.new_adam_state()
-    ws = Z.new_norm_workspace(S)
-    stream = torch.cuda.current_stream()
-    kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip_stats=clip,
-              adam_state=state)
+    if "adamw" in parts:
+        table = lay.device_table()
+        gen = torch.Generator(device="cuda").manual_seed(w.seed * 100 + sim_rank)
+        p = torch.randn(S, device="cuda", generator=gen).mul_(0.02)
+        m = torch.zeros(S, device="cuda")
+        v = torch.zeros(S, device="cuda")
+        micro = [torch.randn(S, device="cuda", generator=gen).mul_(1e-3).to(torch.bfloat16)
+                 for _ in range(MICRO_STEPS)]
+        g = torch.empty(S, device="cuda")  # the fp32 shard gradient (sum of the micro-steps)
+        out = torch.empty(S, dtype=torch.int16, device="cuda")
+        clip, state = Z.new_clip_stats(), Z.new_adam_state()
+        ws = Z.new_norm_workspace(S)
+        kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip_stats=clip,
+                  adam_state=state)
+    # ---- part 2: Newton-Schulz over the stress set (whole matrices owned by this rank)
+    ns = NsPart(Z, torch, 5000 + rank, 5, args.ns_count) if "ns" in parts else None
 
-    n_adamw = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_adamw)]
+    K = args.steps
+    ev_a = [(mk(), mk()) for _ in range(K)]   # accumulation + clip + AdamW part
+    ev_k = [(mk(), mk()) for _ in range(K)]   # adamw_kernel alone
+    ev_n = [(mk(), mk()) for _ in range(K)]   # Newton-Schulz part
 
-    def step(i=None):
-        Z.grad_norm_clip(g, w.max_norm, ws, clip, stream=stream)
+    def adamw_part(i=None):
+        for k, mg in enumerate(micro):
+            Z.grad_accumulate(g, mg, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
+                              stats=clip, stream=stream)
         if i is not None:
-            ev[i][0].record(stream)
+            ev_k[i][0].record(stream)
         Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
         if i is not None:
-            ev[i][1].record(stream)
+            ev_k[i][1].record(stream)
+
+    def step(i=None):
+        if "adamw" in parts:
+            if i is not None:
+                ev_a[i][0].record(stream)
+            adamw_part(i)
+            if i is not None:
+                ev_a[i][1].record(stream)
+        if ns is not None:
+            if i is not None:
+                ev_n[i][0].record(stream)
+            ns.run(stream)
+            if i is not None:
+                ev_n[i][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -208,69 +309,127 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0, t1 = mk(), mk()
     with Clocks(smi_id(local_rank)) as clk:
         t0.record(stream)
-        for i in range(args.steps):
+        for i in range(K):
             step(i)
         t1.record(stream)
         torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / args.steps
-    adamw_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if dist:
-        tt = torch.tensor([ms, adamw_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, adamw_ms = float(tt[0]), float(tt[1])
-        dist.barrier()
     clocks = clk.summary()
+    ms = t0.elapsed_time(t1) / K
+    a_ms = mean(ev_a) if "adamw" in parts else 0.0
+    k_ms = mean(ev_k) if "adamw" in parts else 0.0
+    n_ms = mean(ev_n) if ns is not None else 0.0
+    if dist:
+        tt = torch.tensor([ms, a_ms, k_ms, n_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, a_ms, k_ms, n_ms = (float(x) for x in tt)
+        dist.barrier()
 
-    # end to end through the public API with host buffers: the step's gradient comes from
-    # pinned host memory, the clip stats are read back, each step
-    g_host = g.cpu().pin_memory()
-    stats_host = torch.empty(Z.CLIP_STATS_BYTES, dtype=torch.uint8).pin_memory()
+    # ---- end to end through the public API with host buffers: each part copies its inputs
+    # (the micro-step gradients; the Newton-Schulz inputs) from pinned host memory and reads
+    # its results back (the clip stats; the orthogonalised matrices), timed per part
+    h2d = d2h = 0
+    if "adamw" in parts:
+        micro_host = [mg.cpu().pin_memory() for mg in micro]
+        stats_host = torch.empty(Z.CLIP_STATS_BYTES, dtype=torch.uint8).pin_memory()
+        h2d += 2 * S * MICRO_STEPS
+        d2h += Z.CLIP_STATS_BYTES
+    if ns is not None:
+        ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
+        h2d += sum(G.numel() * 2 for G, _ in ns.groups)
+        d2h += sum(X.numel() * 2 for _, X in ns.groups)
+    e2e_steps = max(2, min(K, 5))
+    ee_a = [(mk(), mk()) for _ in range(e2e_steps)]
+    ee_n = [(mk(), mk()) for _ in range(e2e_steps)]
+
+    def e2e_step(i=None):
+        if "adamw" in parts:
+            if i is not None:
+                ee_a[i][0].record(stream)
+            for mg, mh in zip(micro, micro_host):
+                mg.copy_(mh, non_blocking=True)
+            adamw_part()
+            stats_host.copy_(clip, non_blocking=True)
+            if i is not None:
+                ee_a[i][1].record(stream)
+        if ns is not None:
+            if i is not None:
+                ee_n[i][0].record(stream)
+            for (G, _), (hG, _) in zip(ns.groups, ns_host):
+                G.copy_(hG, non_blocking=True)
+            ns.run(stream)
+            for (_, X), (_, hX) in zip(ns.groups, ns_host):
+                hX.copy_(X, non_blocking=True)
+            if i is not None:
+                ee_n[i][1].record(stream)
+
     for _ in range(2):
-        g.copy_(g_host, non_blocking=True)
-        step()
-        stats_host.copy_(clip, non_blocking=True)
+        e2e_step()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        g.copy_(g_host, non_blocking=True)
-        step()
-        stats_host.copy_(clip, non_blocking=True)
-    e1.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    ea_ms = mean(ee_a) if "adamw" in parts else 0.0
+    en_ms = mean(ee_n) if ns is not None else 0.0
     if dist:
-        tt = torch.tensor([e2e_ms], device="cuda")
+        tt = torch.tensor([ea_ms, en_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt[0])
+        ea_ms, en_ms = float(tt[0]), float(tt[1])
 
-    total_bytes = (ADAMW_BYTES + NORM_BYTES) * S * world_procs
-    value = total_bytes / (ms * 1e-3) / 1e9
     pk = peaks()
-    achieved = ADAMW_BYTES * S / (adamw_ms * 1e-3) / 1e9
+    part_bytes = (ACC_BYTES + ADAMW_BYTES) * S
+    line = {"metric": METRIC, "n_gpus": world_procs, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "shard_len": S, "micro_steps": MICRO_STEPS, "micro_grad_dtype": "bf16",
+                       "simulated_world": w.world,
+                       "ns_set": (f"{sum(G.shape[0] for G, _ in ns.groups)} bf16 matrices "
+                                  f"{[tuple(G.shape[1:]) for G, _ in ns.groups]}, 5 steps") if ns else None,
+                       "l2": "inputs larger than L2 (~13 GB touched per step), no flush"}}
+    if "adamw" in parts:
+        achieved = ADAMW_BYTES * S / (k_ms * 1e-3) / 1e9
+        line["value"] = round(part_bytes * world_procs / (a_ms * 1e-3) / 1e9, 2)
+        line["unit"] = "GB/s"
+        line["adamw_part"] = {"ms": round(a_ms, 4), "bytes_per_element": ACC_BYTES + ADAMW_BYTES,
+                              "accumulate_ms": round(a_ms - k_ms, 4), "adamw_kernel_ms": round(k_ms, 4)}
+        line["roofline_hbm"] = {"kernel": "adamw_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                                "traffic": None, "peak_source": pk["source"],
+                                "algorithmic_bytes_per_launch": ADAMW_BYTES * S, "avg_launch_ms": round(k_ms, 4)}
+    if ns is not None:
+        tflops = ns.flops / (n_ms * 1e-3) / 1e12
+        line["ns"] = {"value": round(tflops * world_procs, 2), "unit": "TFLOP/s", "ms_per_step": round(n_ms, 3),
+                      "algorithmic_flops_per_step": ns.flops}
+        line["roofline"] = {"kernel": "gemm_bf16_kernel (X X', A A', B X)", "bound": "tensor",
+                            "achieved": round(tflops, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                            "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                            "peak_source": pk["source"] + " bf16 sustained (the GEMMs run for ~100 ms per step)",
+                            "note": "achieved = algorithmic flops of the Newton-Schulz calls / their event time "
+                                    "(includes the small normalise/orient kernels)"}
+        if "value" not in line:
+            line["value"], line["unit"] = line["ns"]["value"], "TFLOP/s"
+    elif "adamw" in parts:
+        line["roofline"] = line.pop("roofline_hbm")
+    line["clocks"] = clocks
+    e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if "adamw" in parts:
+        e2e.update(value=round(part_bytes * world_procs / (ea_ms * 1e-3) / 1e9, 2), unit="GB/s",
+                   adamw_part_ms=round(ea_ms, 3))
+    if ns is not None:
+        e2e.update(ns_value=round(ns.flops * world_procs / (en_ms * 1e-3) / 1e12, 2), ns_unit="TFLOP/s",
+                   ns_part_ms=round(en_ms, 3))
+    line["e2e"] = e2e
+    line["gpu_launches"] = K * ((MICRO_STEPS + 1 if "adamw" in parts else 0) + (ns.launches if ns else 0))
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world_procs, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "shard_len": S, "grad_dtype": "f32", "simulated_world": w.world,
-                       "l2": "inputs larger than L2 (4.5 GB/step), no flush"},
-            "roofline": {"kernel": "adamw_kernel", "bound": "hbm", "achieved": round(achieved, 1),
-                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                         "traffic": None, "peak_source": pk["source"],
-                         "algorithmic_bytes_per_launch": ADAMW_BYTES * S, "avg_launch_ms": round(adamw_ms, 4)},
-            "clocks": clocks,
-            "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": 4 * S, "d2h_bytes_per_step": Z.CLIP_STATS_BYTES},
-            "gpu_launches": 2 * args.steps,
-        }
         if world_procs == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_oracle_run(seconds=10.0)
+            if "adamw" in parts:
+                line["cpu_baseline"] = cpu_oracle_run(seconds=10.0)
+            if ns is not None:
+                line["cpu_baseline_ns"] = cpu_oracle_ns(seconds=6.0)
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -279,10 +438,13 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parts", default="adamw,ns", help="comma list of step parts: adamw, ns")
+    ap.add_argument("--ns-count", type=int, default=0,
+                    help="matrices per Newton-Schulz shape (profiling captures); 0 = the full set of 16")
     ap.add_argument("--shard-len", type=int, default=0,
                     help="time a shorter prefix of the shard (profiling captures); 0 = the whole shard")
     args = ap.parse_args()

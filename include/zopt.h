@@ -146,6 +146,21 @@ ZOPT_API zopt_status zopt_clip_finalize(zopt_clip_stats* d_stats, float max_norm
 ZOPT_API zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype dtype, int64_t n, float max_norm,
                                                  zopt_clip_stats* d_stats, zopt_stream stream);
 
+/* Micro-step gradient accumulation into the fp32 shard gradient (deg/zero.py, ZeroMaster
+ * collect / reduce_scatter: the parts of a step are summed in fp32 into the shard gradient,
+ * which grad_sq_norm then reads). acc[n] (fp32) = micro_grad on the micro-step flagged
+ * ZOPT_ACC_FIRST (acc is not read), else acc = acc + micro_grad (fp32, each addition rounded,
+ * in call order). On the micro-step flagged ZOPT_ACC_LAST the same pass also reduces the
+ * finished sum exactly as zopt_grad_norm_clip does and writes *d_stats (d_ws and d_stats are
+ * only used then; d_ws follows zopt_grad_norm_clip's rules). Both flags together: one part.
+ * Errors: EINVAL for n < 1, NULL/misaligned pointers, unknown flags, a missing workspace or
+ * stats on the last micro-step; EUNSUPPORTED for a dtype other than fp32/bf16. */
+#define ZOPT_ACC_FIRST 1
+#define ZOPT_ACC_LAST 2
+ZOPT_API zopt_status zopt_grad_accumulate(float* acc, const void* micro_grad, zopt_dtype dtype, int64_t n,
+                                          int32_t flags, float max_norm, void* d_ws, size_t ws_bytes,
+                                          zopt_clip_stats* d_stats, zopt_stream stream);
+
 /* ======================================================================================
  * 3. Fused AdamW over the flat fp32 shard
  *

@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_norm_clip_noalloc": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, vp]),
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
+        "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
         "zopt_ns_workspace": (sz, [i64, i64, ctypes.c_int]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
                                                  ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
@@ -245,6 +246,20 @@ def grad_norm_clip_noalloc(grad, max_norm: float, stats, n: int | None = None, s
     n = grad.numel() if n is None else int(n)
     _check(lib().zopt_grad_norm_clip_noalloc(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(stats),
                                              _stream(stream)))
+
+
+ACC_FIRST, ACC_LAST = 1, 2
+
+
+def grad_accumulate(acc, micro_grad, *, first: bool, last: bool, max_norm: float = 1.0, ws=None, stats=None,
+                    n: int | None = None, stream=None) -> None:
+    """``zopt_grad_accumulate``: acc (fp32) = / += micro_grad; the last micro-step also
+    writes the clip stats of the finished sum."""
+    n = acc.numel() if n is None else int(n)
+    flags = (ACC_FIRST if first else 0) | (ACC_LAST if last else 0)
+    _check(lib().zopt_grad_accumulate(_ptr(acc), _ptr(micro_grad), _dtype_code(micro_grad), n, flags,
+                                      float(max_norm), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(stats),
+                                      _stream(stream)))
 
 
 def clip_finalize(stats, max_norm: float, stream=None) -> None:

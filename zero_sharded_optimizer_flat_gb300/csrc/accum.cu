@@ -1,0 +1,122 @@
+// Micro-step gradient accumulation into the fp32 shard gradient, with the clip statistics
+// fused into the last micro-step's pass.
+//
+// deg/zero.py, ZeroMaster: a step's bf16 gradients from several parts are summed in fp32
+// (``collect`` keeps an fp32 sum; ``reduce_scatter`` sums into the owner's fp32 shard
+// gradient), and ``grad_sq_norm`` then reads that fp32 shard. Here the sum lives in HBM and
+// the last micro-step's pass produces the sum of squares of the finished sum, so the norm
+// costs no extra read of the shard (4 B per element saved).
+//
+// acc = g_1 (first micro-step: acc is not read), then acc = acc + g_k in fp32, each addition
+// rounded, in micro-step order. Bytes per element: 6 (first, bf16), 10 (later micro-steps).
+// Each thread handles two 8-element vectors per iteration (i and i + grid stride) so that
+// enough loads are in flight to keep HBM busy.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "norm_impl.cuh"
+
+namespace zopt {
+namespace {
+
+template <typename T, bool kFirst>
+__device__ __forceinline__ void accum8(float* acc, const T* g, float (&x)[8]) {
+  load8(g, x);
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  if (!kFirst) {
+    const float4 a = a4[0], b = a4[1];
+    x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]); x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
+    x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]); x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
+  }
+  a4[0] = make_float4(x[0], x[1], x[2], x[3]);
+  a4[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+template <typename T, bool kFirst, bool kLast>
+__global__ void __launch_bounds__(kNormThreads) accum_kernel(float* __restrict__ acc, const T* __restrict__ g, int64_t n,
+                                                              float max_norm, NormWorkspace* ws,
+                                                              zopt_clip_stats* stats) {
+  const int64_t nvec = n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  double ss = 0.0;
+  for (; i + stride < nvec; i += 2 * stride) {
+    float x[8], y[8];
+    accum8<T, kFirst>(acc + 8 * i, g + 8 * i, x);
+    accum8<T, kFirst>(acc + 8 * (i + stride), g + 8 * (i + stride), y);
+    if (kLast) ss = __dadd_rn(ss, __dadd_rn(sumsq8(x), sumsq8(y)));
+  }
+  if (i < nvec) {
+    float x[8];
+    accum8<T, kFirst>(acc + 8 * i, g + 8 * i, x);
+    if (kLast) ss = __dadd_rn(ss, sumsq8(x));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t k = nvec * 8; k < n; ++k) {
+      const float v = kFirst ? load1(g + k) : __fadd_rn(acc[k], load1(g + k));
+      acc[k] = v;
+      if (kLast) ss = __dadd_rn(ss, __dmul_rn(static_cast<double>(v), static_cast<double>(v)));
+    }
+  }
+  if (kLast) finish_sumsq(ss, ws, stats, max_norm);
+}
+
+template <typename T, bool kFirst, bool kLast>
+zopt_status launch(float* acc, const void* g, int64_t n, float max_norm, NormWorkspace* ws, zopt_clip_stats* stats,
+                   cudaStream_t s) {
+  static int occ = 0;
+  if (occ == 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, accum_kernel<T, kFirst, kLast>, kNormThreads, 0) !=
+            cudaSuccess ||
+        o < 1)
+      o = 1;
+    occ = o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_grad_accumulate: no CUDA device");
+  int64_t blocks = static_cast<int64_t>(norm_grid_blocks(n));
+  const int64_t wave = static_cast<int64_t>(sms) * occ;
+  if (blocks > wave) blocks = wave;
+  accum_kernel<T, kFirst, kLast><<<static_cast<unsigned>(blocks), kNormThreads, 0, s>>>(
+      acc, static_cast<const T*>(g), n, max_norm, ws, stats);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+template <typename T>
+zopt_status dispatch(bool first, bool last, float* acc, const void* g, int64_t n, float max_norm, NormWorkspace* ws,
+                     zopt_clip_stats* stats, cudaStream_t s) {
+  if (first && last) return launch<T, true, true>(acc, g, n, max_norm, ws, stats, s);
+  if (first) return launch<T, true, false>(acc, g, n, max_norm, ws, stats, s);
+  if (last) return launch<T, false, true>(acc, g, n, max_norm, ws, stats, s);
+  return launch<T, false, false>(acc, g, n, max_norm, ws, stats, s);
+}
+
+}  // namespace
+}  // namespace zopt
+
+extern "C" zopt_status zopt_grad_accumulate(float* acc, const void* micro_grad, zopt_dtype dtype, int64_t n,
+                                            int32_t flags, float max_norm, void* d_ws, size_t ws_bytes,
+                                            zopt_clip_stats* d_stats, zopt_stream stream) {
+  using namespace zopt;
+  const bool first = (flags & ZOPT_ACC_FIRST) != 0, last = (flags & ZOPT_ACC_LAST) != 0;
+  if ((flags & ~(ZOPT_ACC_FIRST | ZOPT_ACC_LAST)) != 0) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: unknown flags");
+  if (n < 1) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: n < 1");
+  if (acc == nullptr || micro_grad == nullptr) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: NULL pointer");
+  if (!aligned16(acc) || !aligned16(micro_grad))
+    return fail(ZOPT_EINVAL, "zopt_grad_accumulate: acc or micro_grad is not 16-byte aligned");
+  if (dtype != ZOPT_F32 && dtype != ZOPT_BF16) return fail(ZOPT_EUNSUPPORTED, "zopt_grad_accumulate: grad dtype");
+  if (last) {
+    if (d_stats == nullptr || (reinterpret_cast<uintptr_t>(d_stats) & 7u) != 0)
+      return fail(ZOPT_EINVAL, "zopt_grad_accumulate: the last micro-step needs an 8-byte aligned stats struct");
+    if (!(max_norm >= 0.0f)) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: max_norm is negative or NaN");
+    if (d_ws == nullptr || !aligned16(d_ws) || ws_bytes < zopt_grad_norm_workspace(n))
+      return fail(ZOPT_EINVAL, "zopt_grad_accumulate: the last micro-step needs a zopt_grad_norm_workspace(n) workspace");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  NormWorkspace* ws = static_cast<NormWorkspace*>(d_ws);
+  return dtype == ZOPT_F32 ? dispatch<float>(first, last, acc, micro_grad, n, max_norm, ws, d_stats, s)
+                           : dispatch<__nv_bfloat16>(first, last, acc, micro_grad, n, max_norm, ws, d_stats, s);
+}
