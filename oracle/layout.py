@@ -79,10 +79,11 @@ def segments(numel: list, bucket: int, world: int, rank: int) -> list:
     return out
 
 
-def gather_shard(flat: np.ndarray, numel: list, bucket: int, world: int, rank: int) -> np.ndarray:
+def gather_shard(flat: np.ndarray, numel: list, bucket: int, world: int, rank: int, idx=None) -> np.ndarray:
     """Rank ``rank``'s shard of a flat vector, zeros in the padding (ZeroMaster._bucket_values
-    then the rank's piece)."""
-    idx = flat_index_of_shard(numel, bucket, world, rank)
+    then the rank's piece). ``idx`` may pass a precomputed slot -> flat index map."""
+    if idx is None:
+        idx = flat_index_of_slots(numel, bucket, world, rank, np.arange(shard_len(numel, bucket, world)))
     out = np.zeros(idx.shape[0], dtype=flat.dtype)
     ok = idx >= 0
     out[ok] = flat[idx[ok]]

@@ -40,6 +40,8 @@ class Case:
         self.full_p = [t.numpy().astype(np.float32) for t in workloads.flat_masters(params, seed)]
         self.full_m = [np.zeros_like(p) for p in self.full_p]
         self.full_v = [np.zeros_like(p) for p in self.full_p]
+        self.idx = OL.flat_index_of_slots(self.numel, bucket, world, rank,
+                                          np.arange(OL.shard_len(self.numel, bucket, world)))
         self.layout = Z.ShardLayout(self.numel, self.decay, bucket, world, rank)
         self.table = self.layout.device_table()
         S = self.layout.shard_len
@@ -54,10 +56,10 @@ class Case:
         self.t = 0
 
     def shard(self, tensors):
-        return OL.gather_shard(np.concatenate(tensors), self.numel, self.bucket, self.world, self.rank)
+        return OL.gather_shard(np.concatenate(tensors), self.numel, self.bucket, self.world, self.rank, self.idx)
 
-    def step(self, step_idx, h: OA.Hyper, max_norm=1.0, poison=None, skip_on_inf=True):
-        grads = workloads.flat_grads(self.params, self.seed, step_idx, dtype=self.gdtype)
+    def step(self, step_idx, h: OA.Hyper, max_norm=1.0, poison=None, skip_on_inf=True, zero_row_frac=0.0):
+        grads = workloads.flat_grads(self.params, self.seed, step_idx, zero_row_frac=zero_row_frac, dtype=self.gdtype)
         g_full = [g.float().numpy() for g in grads]
         if poison is not None:
             k, j, val = poison
@@ -85,7 +87,7 @@ class Case:
         assert np.array_equal(bits(self.v.cpu().numpy()), bits(self.shard(self.full_v)))
         out = self.out.cpu().numpy().view(np.uint16)
         assert np.array_equal(out, f32_to_bf16_bits(self.shard(self.full_p)))
-        pad = OL.flat_index_of_shard(self.numel, self.bucket, self.world, self.rank) < 0
+        pad = self.idx < 0
         assert np.all(p[pad] == 0)
         assert self.Z.read_adam_state(self.state) == {"step": self.t, "arrive": 0}
 
@@ -109,6 +111,27 @@ def test_c1_three_steps_bitwise(zopt):
     for s in range(w.steps):
         case.step(s, h, max_norm=w.max_norm)
         case.compare()
+
+
+def test_gpt2_small_set_three_wsd_steps_bitwise(zopt):
+    """GPT-2-small AdamW set (embedding 50304x768 + 25 scales, N = 38,652,672, 2 buckets of
+    2^25), 1 % zero gradient rows, the WSD learning rate of a 10-step run, W = 1."""
+    w = workloads.get("c2")
+    case = Case(zopt, w.adamw, w.bucket, 1, 0, seed=w.seed, gdtype=torch.bfloat16)
+    for s in range(3):
+        case.step(s, OA.Hyper(w.lr_at(s), w.beta1, w.beta2, w.eps, w.weight_decay), max_norm=w.max_norm,
+                  zero_row_frac=w.zero_row_frac)
+    case.compare()
+
+
+def test_llama_set_rank0_of_8_two_steps_bitwise(zopt):
+    """Llama-style 1.1B AdamW set (embedding 32000x2048 + 33 scales), simulated rank 0 of 8."""
+    w = workloads.get("c3")
+    case = Case(zopt, w.adamw, w.bucket, w.world, w.rank, seed=w.seed, gdtype=torch.bfloat16)
+    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    for s in range(2):
+        case.step(s, h, max_norm=w.max_norm)
+    case.compare()
 
 
 def test_wsd_schedule_lr_changes_each_step(zopt):

@@ -137,6 +137,17 @@ def torch_ns_fp32(G, steps=5, abc=DEFAULT_ABC, eps=1e-7):
     return X.T if tr else X
 
 
+@pytest.mark.parametrize("rows,cols", [(2048, 2048), (2048, 512), (2048, 11264)])
+def test_llama_owned_matrices_match_fp64_oracle(zopt, rows, cols):
+    """The 1.1B set's matrices owned by rank 0 of 8 (Wq, Wv, gate_up shapes), 5 steps."""
+    G = gaussian(rows, cols, rows + cols)
+    X = torch.empty_like(G)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols), steps=5)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5)
+    assert rel(X.cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
 @pytest.mark.parametrize("rows,cols", [(4096, 4096), (4096, 14336), (14336, 4096)])
 def test_stress_shapes_against_fp32_checker(zopt, rows, cols):
     prev = torch.backends.cuda.matmul.allow_tf32
@@ -171,3 +182,51 @@ def test_rejects_bad_arguments(zopt):
         zopt.ns_orthogonalize(G, X, ws[:16], steps=5)
     with pytest.raises(zopt.ZoptError):
         zopt.ns_orthogonalize(G, X, ws, abc=(float("nan"), 1.0, 1.0))
+
+
+SHAPES_F32 = [(256, 768), (768, 256), (256, 1024), (300, 300), (129, 257), (1, 8), (8, 1), (768, 2304), (1000, 130)]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_F32)
+def test_fp32_mode_matches_fp64_oracle_to_1e4(zopt, rows, cols):
+    """compute_dtype fp32 with fp32 input/output: relative Frobenius error <= 1e-4."""
+    g = torch.Generator(device="cuda").manual_seed(rows * 3 + cols)
+    G = torch.randn(rows, cols, generator=g, device="cuda")
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(rows, cols, compute=zopt.F32)
+    zopt.ns_orthogonalize(G, X, ws, steps=5, compute=zopt.F32)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5)
+    err = rel(X.cpu(), torch.from_numpy(ref))
+    assert err <= 1e-4, err
+
+
+def test_fp32_mode_white_box_symmetric_products(zopt):
+    rows, cols = 200, 333
+    G = torch.randn(rows, cols, device="cuda")
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(rows, cols, compute=zopt.F32)
+    zopt.ns_orthogonalize(G, X, ws, steps=1, compute=zopt.F32)
+    torch.cuda.synchronize()
+    p = plan(rows, cols)
+    m, n = p["m"], p["n"]
+    xbytes = rup(m * p["ldx"] * 4, 1024)
+    abytes = rup(m * p["lda"] * 4, 1024)
+    f32 = lambda off, r, ld, c: ws[off:off + r * ld * 4].view(torch.float32).view(r, ld)[:, :c]  # noqa: E731
+    X0 = f32(p["x0"], m, p["ldx"], n).double()
+    A = f32(p["x0"] + 2 * xbytes, m, p["lda"], m).double()
+    B = f32(p["x0"] + 2 * xbytes + abytes, m, p["lda"], m).double()
+    assert torch.equal(A, A.T) and torch.equal(B, B.T)
+    assert rel(A, X0 @ X0.T) < 1e-5
+    assert rel(B, C_ * (A @ A) + B_ * A) < 1e-5
+    assert rel(X.double(), A_ * X0 + B @ X0) < 1e-5
+
+
+def test_fp32_compute_with_bf16_io(zopt):
+    G = gaussian(384, 1000, 77)
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(384, 1000, compute=zopt.F32)
+    zopt.ns_orthogonalize(G, X, ws, steps=5, compute=zopt.F32)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5)
+    assert rel(X.cpu(), torch.from_numpy(ref)) <= 4e-3  # one bf16 rounding of the output

@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "norm_impl.cuh"
+#include "ns_internal.h"
 #include "tc.cuh"
 
 namespace zopt {
@@ -383,11 +384,14 @@ __global__ void __launch_bounds__(kNormThreads) matrix_sumsq_kernel(const T* __r
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// X0 = G / (||G||_F + eps) in bf16, oriented so that X0 is m x n with m <= n.
-template <typename T>
+__device__ __forceinline__ void to_out(float v, __nv_bfloat16* p) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void to_out(float v, float* p) { *p = v; }
+
+// X0 = G / (||G||_F + eps) in the compute dtype U, oriented so that X0 is m x n with m <= n.
+template <typename T, typename U>
 __global__ void scale_orient_kernel(const T* __restrict__ g, long long rows, long long cols, long long ld,
-                                    int transpose, const zopt_clip_stats* stats, double eps,
-                                    __nv_bfloat16* __restrict__ x, long long ldx) {
+                                    int transpose, const zopt_clip_stats* stats, double eps, U* __restrict__ x,
+                                    long long ldx) {
   __shared__ float s_inv;
   __shared__ float tile[32][33];
   if (threadIdx.x == 0 && threadIdx.y == 0) {
@@ -402,7 +406,7 @@ __global__ void scale_orient_kernel(const T* __restrict__ g, long long rows, lon
     if (!transpose) {
       for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
         const long long r = r0 + yy, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) x[r * ldx + c] = __float2bfloat16_rn(to_f32(g[r * ld + c]) * inv);
+        if (r < rows && c < cols) to_out(to_f32(g[r * ld + c]) * inv, x + r * ldx + c);
       }
     } else {
       for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
@@ -412,7 +416,7 @@ __global__ void scale_orient_kernel(const T* __restrict__ g, long long rows, lon
       __syncthreads();
       for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
         const long long xr = c0 + yy, xc = r0 + threadIdx.x;  // X0[c][r] = G[r][c]
-        if (xr < cols && xc < rows) x[xr * ldx + xc] = __float2bfloat16_rn(tile[threadIdx.x][yy]);
+        if (xr < cols && xc < rows) to_out(tile[threadIdx.x][yy], x + xr * ldx + xc);
       }
       __syncthreads();
     }
@@ -480,7 +484,8 @@ struct Plan {
   size_t off_stats, off_x0, off_x1, off_a, off_b, total;
 };
 
-Plan plan(long long rows, long long cols) {
+// Workspace regions; es = bytes per element of the compute dtype.
+Plan plan(long long rows, long long cols, long long es) {
   Plan p;
   p.m = rows < cols ? rows : cols;
   p.n = rows < cols ? cols : rows;
@@ -489,8 +494,8 @@ Plan plan(long long rows, long long cols) {
   p.off_stats = 256 + sizeof(double) * static_cast<size_t>(kNormMaxBlocks);
   p.off_stats = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats), 256));
   p.off_x0 = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats + 256), 1024));
-  const size_t xbytes = static_cast<size_t>(round_up(p.m * p.ldx * 2, 1024));
-  const size_t abytes = static_cast<size_t>(round_up(p.m * p.lda * 2, 1024));
+  const size_t xbytes = static_cast<size_t>(round_up(p.m * p.ldx * es, 1024));
+  const size_t abytes = static_cast<size_t>(round_up(p.m * p.lda * es, 1024));
   p.off_x1 = p.off_x0 + xbytes;
   p.off_a = p.off_x1 + xbytes;
   p.off_b = p.off_a + abytes;
@@ -525,8 +530,8 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, 
 }  // namespace zopt
 
 extern "C" size_t zopt_ns_workspace(int64_t rows, int64_t cols, zopt_dtype compute_dtype) {
-  if (rows < 1 || cols < 1 || compute_dtype != ZOPT_BF16) return 0;
-  return zopt::ns::plan(rows, cols).total;
+  if (rows < 1 || cols < 1 || (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)) return 0;
+  return zopt::ns::plan(rows, cols, compute_dtype == ZOPT_F32 ? 4 : 2).total;
 }
 
 extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io_dtype, int64_t rows, int64_t cols,
@@ -546,12 +551,13 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
   if (steps < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: steps < 1");
   if (io_dtype != ZOPT_F32 && io_dtype != ZOPT_BF16)
     return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: input/output dtype must be fp32 or bf16");
-  if (compute_dtype != ZOPT_BF16)
-    return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: compute dtype must be bf16 (tcgen05 path)");
+  if (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)
+    return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: compute dtype must be bf16 or fp32");
   if (!std::isfinite(abc[0]) || !std::isfinite(abc[1]) || !std::isfinite(abc[2]) || !std::isfinite(eps) || eps < 0)
     return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: coefficients and eps must be finite (eps >= 0)");
   if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace is not 16-byte aligned");
-  const Plan p = plan(rows, cols);
+  const bool f32c = compute_dtype == ZOPT_F32;
+  const Plan p = plan(rows, cols, f32c ? 4 : 2);
   if (ws_bytes < p.total) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace smaller than zopt_ns_workspace");
   int* err_host = nullptr;
   int* err_dev = nullptr;
@@ -574,14 +580,16 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
 
   // Tensor maps over the workspace matrices (the same for every matrix of the batch).
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
-  for (int q = 0; q < 2; ++q) {
+  for (int q = 0; q < 2 && !f32c; ++q) {
     if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, 64, BM)) != ZOPT_OK) return st;
     if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, 64, BN)) != ZOPT_OK) return st;
     if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, 64, BK)) != ZOPT_OK) return st;
   }
-  if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
-  if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, 64, BN)) != ZOPT_OK) return st;
-  if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+  if (!f32c) {
+    if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, 64, BN)) != ZOPT_OK) return st;
+    if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+  }
 
   const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
   const int sms = sm_count();
@@ -601,14 +609,45 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
           reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, vec_ok, nws, nstats);
     ZOPT_CUDA_TRY(cudaGetLastError());
     const dim3 tb(32, 8);
-    if (io_dtype == ZOPT_F32)
-      scale_orient_kernel<float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
-                                                        transpose ? 1 : 0, nstats, eps, xb[0], p.ldx);
+    const int tr = transpose ? 1 : 0;
+    float* xf0 = reinterpret_cast<float*>(xb[0]);
+    if (io_dtype == ZOPT_F32 && f32c)
+      scale_orient_kernel<float, float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
+                                                               tr, nstats, eps, xf0, p.ldx);
+    else if (io_dtype == ZOPT_F32)
+      scale_orient_kernel<float, __nv_bfloat16><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows,
+                                                                       cols, ld_g, tr, nstats, eps, xb[0], p.ldx);
+    else if (f32c)
+      scale_orient_kernel<__nv_bfloat16, float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g),
+                                                                       rows, cols, ld_g, tr, nstats, eps, xf0, p.ldx);
     else
-      scale_orient_kernel<__nv_bfloat16><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g), rows,
-                                                                cols, ld_g, transpose ? 1 : 0, nstats, eps, xb[0],
-                                                                p.ldx);
+      scale_orient_kernel<__nv_bfloat16, __nv_bfloat16><<<sms * 8, tb, 0, s>>>(
+          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, tr, nstats, eps, xb[0], p.ldx);
     ZOPT_CUDA_TRY(cudaGetLastError());
+
+    if (f32c) {
+      float* xf[2] = {reinterpret_cast<float*>(xb[0]), reinterpret_cast<float*>(xb[1])};
+      float* Af = reinterpret_cast<float*>(A);
+      float* Bf = reinterpret_cast<float*>(B);
+      const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
+      int cur = 0;
+      for (int it = 0; it < steps; ++it) {
+        const bool last = it == steps - 1;
+        // A = X X'
+        GemmF32Args fa{m, m, n, xf[cur], p.ldx, xf[cur], p.ldx, 0, 1, 1.0f, 0.0f, nullptr, 0, Af, p.lda, 1, 0};
+        if ((st = launch_gemm_f32(fa, s)) != ZOPT_OK) return st;
+        // B = c A A' + b A
+        GemmF32Args fb{m, m, m, Af, p.lda, Af, p.lda, 0, 1, abc[2], abc[1], Af, p.lda, Bf, p.lda, 1, 0};
+        if ((st = launch_gemm_f32(fb, s)) != ZOPT_OK) return st;
+        // X = B X + a X
+        GemmF32Args fx{m, n, m, Bf, p.lda, xf[cur], p.ldx, 1, 0, 1.0f, abc[0], xf[cur], p.ldx,
+                       last ? static_cast<void*>(xo) : static_cast<void*>(xf[cur ^ 1]), last ? ld_x : p.ldx,
+                       last ? (io_dtype == ZOPT_F32 ? 1 : 0) : 1, last && transpose ? 1 : 0};
+        if ((st = launch_gemm_f32(fx, s)) != ZOPT_OK) return st;
+        cur ^= 1;
+      }
+      continue;
+    }
 
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
