@@ -223,9 +223,11 @@ class NsPart:
             G /= torch.linalg.vector_norm(G, dim=(1, 2), keepdim=True)  # Frobenius-normalised
             G = G.to(torch.bfloat16)
             self.groups.append((G, torch.empty_like(G)))
-        self.ws = torch.empty(max(Z.ns_workspace(r, c) for r, c in shapes), dtype=torch.uint8, device="cuda")
+        # room for a whole shape group, so each product of a step is one launch over the group
+        self.ws = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], G.shape[0]) for G, _ in self.groups),
+                              dtype=torch.uint8, device="cuda")
         self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
-        self.launches = sum(G.shape[0] * (2 + 3 * steps) for G, _ in self.groups)
+        self.launches = sum(2 + 3 * steps for _ in self.groups)  # one launch per product per group
 
     def run(self, stream):
         for G, X in self.groups:

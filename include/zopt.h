@@ -226,15 +226,18 @@ ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d
  * Muon choice is 3.4445, -4.7750, 2.0315).
  * ====================================================================================== */
 
-/* Workspace bytes for one rows x cols matrix (0 for an unsupported compute dtype). The
- * workspace is reused across the matrices of a batch. */
-ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, zopt_dtype compute_dtype);
+/* Workspace bytes to process `group` rows x cols matrices together (0 for an unsupported
+ * compute dtype or group < 1). A call processes its batch in groups of as many matrices as its
+ * workspace holds: every product of a step is one launch over the whole group, so a larger
+ * group means fewer launches and better use of the SMs. */
+ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zopt_dtype compute_dtype);
 /* Orthogonalise `batch` matrices G[b] (rows x cols, row-major, leading dimension ld_g,
  * matrix b at G + b*batch_stride_g elements) into X[b] (same shape, ld_x, batch_stride_x).
  *   io_dtype: dtype of G and X (ZOPT_BF16 or ZOPT_F32);
- *   compute_dtype: ZOPT_BF16 (tcgen05 tensor cores);
+ *   compute_dtype: ZOPT_BF16 (tcgen05 tensor cores) or ZOPT_F32 (fp32 FMA, for callers that
+ *     need agreement with fp64 to about 1e-4);
  *   steps >= 1; abc: 3 host floats; eps >= 0 (1e-7 is the usual choice);
- *   d_ws: at least zopt_ns_workspace(rows, cols, compute_dtype) bytes, 16-byte aligned.
+ *   d_ws: at least zopt_ns_workspace(rows, cols, 1, compute_dtype) bytes, 16-byte aligned.
  * G and X must not overlap. Errors: EINVAL for NULL pointers, empty shapes, dimensions
  * >= 2^31, leading dimensions < cols, overlapping batch strides, steps < 1, non-finite
  * coefficients, a short workspace; EUNSUPPORTED for other dtypes; ETIMEOUT when a kernel of

@@ -24,15 +24,16 @@ def rup(x, a):
     return -(-x // a) * a
 
 
-def plan(rows, cols):
-    """Offsets of the library's workspace regions (white-box reading of its layout)."""
+def plan(rows, cols, es=2, group=1):
+    """Offsets of the library's workspace regions for matrix 0 of a group (white-box reading of
+    its layout: a header of per-matrix reduction scratch and stats, then one region per matrix)."""
     m, n = min(rows, cols), max(rows, cols)
     ldx, lda = rup(n, 8), rup(m, 8)
-    off_stats = rup(256 + 8 * 4096, 256)
-    off_x0 = rup(off_stats + 256, 1024)
-    xbytes, abytes = rup(m * ldx * 2, 1024), rup(m * lda * 2, 1024)
-    return dict(m=m, n=n, ldx=ldx, lda=lda, x0=off_x0, x1=off_x0 + xbytes, a=off_x0 + 2 * xbytes,
-                b=off_x0 + 2 * xbytes + abytes)
+    off_stats = rup(group * (256 + 8 * 512), 256)
+    header = rup(off_stats + group * 32, 1024)
+    xbytes, abytes = rup(m * ldx * es, 1024), rup(m * lda * es, 1024)
+    return dict(m=m, n=n, ldx=ldx, lda=lda, x0=header, x1=header + xbytes, a=header + 2 * xbytes,
+                b=header + 2 * xbytes + abytes, xbytes=xbytes, abytes=abytes, per=2 * xbytes + 2 * abytes)
 
 
 def region(ws, off, rows, ld, cols):
@@ -109,6 +110,27 @@ def test_fp32_io_and_batch_strides(zopt):
         zopt.ns_orthogonalize(G[b].contiguous(), one, ws, steps=5)
         torch.cuda.synchronize()
         assert torch.equal(one, X[b])  # a batch entry is bitwise the single call
+
+
+@pytest.mark.parametrize("compute", ["bf16", "f32"])
+def test_grouped_batch_equals_single_calls(zopt, compute):
+    """A workspace for 2 matrices runs a batch of 5 as groups of 2, 2, 1: every product is one
+    launch over the group. Each result is bitwise the single-matrix call's."""
+    code = zopt.BF16 if compute == "bf16" else zopt.F32
+    rows, cols, batch = 700, 300, 5  # tall: processed transposed
+    G = torch.randn(batch, rows, cols, device="cuda").to(torch.bfloat16)
+    X = torch.empty_like(G)
+    ws2 = zopt.new_ns_workspace(rows, cols, group=2, compute=code)
+    assert ws2.numel() < zopt.ns_workspace(rows, cols, 3, code)
+    zopt.ns_orthogonalize(G, X, ws2, steps=5, compute=code)
+    ws1 = zopt.new_ns_workspace(rows, cols, compute=code)
+    for b in range(batch):
+        one = torch.empty(rows, cols, device="cuda", dtype=torch.bfloat16)
+        zopt.ns_orthogonalize(G[b], one, ws1, steps=5, compute=code)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X[b]), b
+        ref = newton_schulz(G[b].double().cpu().numpy(), steps=5)
+        assert rel(X[b].cpu(), torch.from_numpy(ref)) <= 2e-2
 
 
 def test_deterministic(zopt):
@@ -208,10 +230,9 @@ def test_fp32_mode_white_box_symmetric_products(zopt):
     ws = zopt.new_ns_workspace(rows, cols, compute=zopt.F32)
     zopt.ns_orthogonalize(G, X, ws, steps=1, compute=zopt.F32)
     torch.cuda.synchronize()
-    p = plan(rows, cols)
+    p = plan(rows, cols, es=4)
     m, n = p["m"], p["n"]
-    xbytes = rup(m * p["ldx"] * 4, 1024)
-    abytes = rup(m * p["lda"] * 4, 1024)
+    xbytes, abytes = p["xbytes"], p["abytes"]
     f32 = lambda off, r, ld, c: ws[off:off + r * ld * 4].view(torch.float32).view(r, ld)[:, :c]  # noqa: E731
     X0 = f32(p["x0"], m, p["ldx"], n).double()
     A = f32(p["x0"] + 2 * xbytes, m, p["lda"], m).double()

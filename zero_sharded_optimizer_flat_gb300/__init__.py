@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
-        "zopt_ns_workspace": (sz, [i64, i64, ctypes.c_int]),
+        "zopt_ns_workspace": (sz, [i64, i64, i32, ctypes.c_int]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
                                                  ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
                                                  vp, sz, vp]),
@@ -281,13 +281,14 @@ def adamw_step(layout: ShardLayout, table, master, exp_avg, exp_avg_sq, grad, ou
 DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
 
 
-def ns_workspace(rows: int, cols: int, compute=BF16) -> int:
-    return int(lib().zopt_ns_workspace(int(rows), int(cols), int(compute)))
+def ns_workspace(rows: int, cols: int, group: int = 1, compute=BF16) -> int:
+    return int(lib().zopt_ns_workspace(int(rows), int(cols), int(group), int(compute)))
 
 
-def new_ns_workspace(rows: int, cols: int, compute=BF16, device="cuda"):
+def new_ns_workspace(rows: int, cols: int, group: int = 1, compute=BF16, device="cuda"):
+    """A workspace for processing ``group`` matrices of this shape per launch."""
     import torch
-    return torch.empty(max(ns_workspace(rows, cols, compute), 16), dtype=torch.uint8, device=device)
+    return torch.empty(max(ns_workspace(rows, cols, group, compute), 16), dtype=torch.uint8, device=device)
 
 
 def ns_orthogonalize(G, X, ws, steps: int = 5, abc=DEFAULT_ABC, eps: float = 1e-7, compute=BF16, stream=None) -> None:

@@ -9,8 +9,8 @@
 //
 // acc = g_1 (first micro-step: acc is not read), then acc = acc + g_k in fp32, each addition
 // rounded, in micro-step order. Bytes per element: 6 (first, bf16), 10 (later micro-steps).
-// Each thread handles two 8-element vectors per iteration (i and i + grid stride) so that
-// enough loads are in flight to keep HBM busy.
+// Each thread issues the loads of four 8-element vectors (i, i + stride, ...) before it adds
+// and stores any of them, so that enough bytes are in flight to keep HBM busy.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -20,17 +20,16 @@
 namespace zopt {
 namespace {
 
-template <typename T, bool kFirst>
-__device__ __forceinline__ void accum8(float* acc, const T* g, float (&x)[8]) {
-  load8(g, x);
-  float4* a4 = reinterpret_cast<float4*>(acc);
-  if (!kFirst) {
-    const float4 a = a4[0], b = a4[1];
-    x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]); x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
-    x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]); x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
-  }
-  a4[0] = make_float4(x[0], x[1], x[2], x[3]);
-  a4[1] = make_float4(x[4], x[5], x[6], x[7]);
+constexpr int kUnroll = 4;  // 8-element vectors per thread per iteration, all loads issued first
+
+__device__ __forceinline__ void ld_acc8(const float* p, float (&a)[8]) {
+  const float4 u = reinterpret_cast<const float4*>(p)[0], w = reinterpret_cast<const float4*>(p)[1];
+  a[0] = u.x; a[1] = u.y; a[2] = u.z; a[3] = u.w; a[4] = w.x; a[5] = w.y; a[6] = w.z; a[7] = w.w;
+}
+
+__device__ __forceinline__ void st_acc8(float* p, const float (&x)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 
 template <typename T, bool kFirst, bool kLast>
@@ -41,15 +40,32 @@ __global__ void __launch_bounds__(kNormThreads) accum_kernel(float* __restrict__
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double ss = 0.0;
-  for (; i + stride < nvec; i += 2 * stride) {
-    float x[8], y[8];
-    accum8<T, kFirst>(acc + 8 * i, g + 8 * i, x);
-    accum8<T, kFirst>(acc + 8 * (i + stride), g + 8 * (i + stride), y);
-    if (kLast) ss = __dadd_rn(ss, __dadd_rn(sumsq8(x), sumsq8(y)));
+  for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+    float x[kUnroll][8], a[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      load8(g + 8 * (i + u * stride), x[u]);
+      if (!kFirst) ld_acc8(acc + 8 * (i + u * stride), a[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (!kFirst) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[u][k] = __fadd_rn(a[u][k], x[u][k]);
+      }
+      st_acc8(acc + 8 * (i + u * stride), x[u]);
+      if (kLast) ss = __dadd_rn(ss, sumsq8(x[u]));
+    }
   }
-  if (i < nvec) {
-    float x[8];
-    accum8<T, kFirst>(acc + 8 * i, g + 8 * i, x);
+  for (; i < nvec; i += stride) {
+    float x[8], a[8];
+    load8(g + 8 * i, x);
+    if (!kFirst) {
+      ld_acc8(acc + 8 * i, a);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = __fadd_rn(a[k], x[k]);
+    }
+    st_acc8(acc + 8 * i, x);
     if (kLast) ss = __dadd_rn(ss, sumsq8(x));
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {

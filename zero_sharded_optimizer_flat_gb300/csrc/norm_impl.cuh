@@ -138,13 +138,13 @@ __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict_
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double acc = 0.0;
-  for (; i + stride < nvec; i += 2 * stride) {
-    float x[8], y[8];
-    load8(g + 8 * i, x);
-    load8(g + 8 * (i + stride), y);
-    acc = __dadd_rn(acc, __dadd_rn(sumsq8(x), sumsq8(y)));
+  for (; i + 3 * stride < nvec; i += 4 * stride) {  // four vectors' loads in flight per thread
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load8(g + 8 * (i + u * stride), x[u]);
+    acc = __dadd_rn(acc, __dadd_rn(__dadd_rn(sumsq8(x[0]), sumsq8(x[1])), __dadd_rn(sumsq8(x[2]), sumsq8(x[3]))));
   }
-  if (i < nvec) {
+  for (; i < nvec; i += stride) {
     float x[8];
     load8(g + 8 * i, x);
     acc = __dadd_rn(acc, sumsq8(x));

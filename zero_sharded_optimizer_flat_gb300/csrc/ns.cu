@@ -49,6 +49,9 @@ constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256;
 struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles;
+  int group;          // matrices processed by this launch (the TMA maps' third coordinate)
+  int tiles_per_mat;  // tiles of one matrix
+  long long r_stride, d_stride;  // elements between consecutive matrices' R and D
   int symmetric;   // M == N and D symmetric: upper-triangle tiles only, mirrored writes
   int b_mn_major;  // the B-operand is stored [K][N] (N contiguous)
   float alpha, beta;
@@ -61,7 +64,9 @@ struct GemmArgs {
   int* err;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& ti, int& tj) {
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& mb, int& ti, int& tj) {
+  mb = t / a.tiles_per_mat;  // matrix-major order: the tiles running together share operands
+  t -= mb * a.tiles_per_mat;
   if (!a.symmetric) {
     // column-major raster: the tiles running together share the B-operand columns, and the
     // whole A-operand (m x m) stays in L2
@@ -241,8 +246,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int q = 0; q < STAGES; ++q) armed[q] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
-        int ti, tj;
-        tile_coords(a, t, ti, tj);
+        int mb, ti, tj;
+        tile_coords(a, t, mb, ti, tj);
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty + s, ph ^ 1u, a.err)) {
             ok = false;
@@ -250,13 +255,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc::mbar_arrive_expect_tx(full + s, kTileA + kTileB);
           armed[s] = static_cast<int>(ph);
-          tc::tma_load_2d(sA + s * kTileA, &tmP, full + s, kb * BK, ti * BM);
+          tc::tma_load_3d(sA + s * kTileA, &tmP, full + s, kb * BK, ti * BM, mb);
           if (!a.b_mn_major) {
-            tc::tma_load_2d(sB + s * kTileB, &tmQ, full + s, kb * BK, tj * BN);
+            tc::tma_load_3d(sB + s * kTileB, &tmQ, full + s, kb * BK, tj * BN, mb);
           } else {
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
-              tc::tma_load_2d(sB + s * kTileB + q * kBoxMN, &tmQ, full + s, tj * BN + 64 * q, kb * BK);
+              tc::tma_load_3d(sB + s * kTileB + q * kBoxMN, &tmQ, full + s, tj * BN + 64 * q, kb * BK, mb);
           }
           if (++s == STAGES) {
             s = 0;
@@ -325,8 +330,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc::fence_after_sync();
-      int ti, tj;
-      tile_coords(a, t, ti, tj);
+      int mb, ti, tj;
+      tile_coords(a, t, mb, ti, tj);
+      GemmArgs am = a;  // this matrix's R and D
+      am.R = a.R + mb * a.r_stride;
+      am.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
       const int i = ti * BM + row;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc::fence_before_sync();
           tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
         }
-        epilogue32(a, i, tj * BN + 32 * c, v);
+        epilogue32(am, i, tj * BN + 32 * c, v);
       }
     }
   }
@@ -351,51 +359,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------------- prep kernels
 
-// sum of squares of a rows x cols matrix with leading dimension ld (elements).
+// Per-matrix reduction scratch: an arrival counter and up to kPrepBlocks fp64 partials.
+constexpr int kPrepBlocks = 512;
+constexpr size_t kPrepWsBytes = 256 + sizeof(double) * kPrepBlocks;
+
+__device__ __forceinline__ NormWorkspace* prep_ws(uint8_t* base, int mb) {
+  return reinterpret_cast<NormWorkspace*>(base + static_cast<size_t>(mb) * kPrepWsBytes);
+}
+
+// Sum of squares of each matrix of the group (blockIdx.y = matrix): G_b is rows x cols with
+// leading dimension ld, matrices batch_stride elements apart. `flat` = rows are contiguous
+// (ld == cols) and 16-byte aligned, so the matrix is one vector.
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads) matrix_sumsq_kernel(const T* __restrict__ g, long long rows,
-                                                                     long long cols, long long ld, int vec_ok,
-                                                                     NormWorkspace* ws, zopt_clip_stats* stats) {
+__global__ void __launch_bounds__(kNormThreads)
+    group_sumsq_kernel(const T* __restrict__ g0, long long rows, long long cols, long long ld,
+                       long long batch_stride, int flat, int vec_rows, uint8_t* ws_base,
+                       zopt_clip_stats* stats) {
+  const int mb = blockIdx.y;
+  const T* g = g0 + mb * batch_stride;
   double acc = 0.0;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long c8 = vec_ok ? cols / 8 : 0;
-  if (c8 > 0) {
-    const long long nvec = rows * c8;
-    for (long long e = tid; e < nvec; e += stride) {
+  if (flat) {
+    const long long n = rows * cols, nvec = n / 8;
+    long long i = tid;
+    for (; i + stride < nvec; i += 2 * stride) {
+      float x[8], y[8];
+      load8(g + 8 * i, x);
+      load8(g + 8 * (i + stride), y);
+      acc = __dadd_rn(acc, __dadd_rn(sumsq8(x), sumsq8(y)));
+    }
+    for (; i < nvec; i += stride) {
+      float x[8];
+      load8(g + 8 * i, x);
+      acc = __dadd_rn(acc, sumsq8(x));
+    }
+    for (long long k = nvec * 8 + tid; k < n; k += stride) {
+      const double d = static_cast<double>(load1(g + k));
+      acc = __dadd_rn(acc, __dmul_rn(d, d));
+    }
+  } else {
+    const long long c8 = vec_rows ? cols / 8 : 0;
+    for (long long e = tid; e < rows * c8; e += stride) {
       const long long r = e / c8, c = e - r * c8;
       float x[8];
       load8(g + r * ld + 8 * c, x);
       acc = __dadd_rn(acc, sumsq8(x));
     }
-  }
-  const long long tail = cols - 8 * c8;  // scalar columns [8 c8, cols) of every row
-  if (tail > 0) {
-    const long long ntail = rows * tail;
-    for (long long e = tid; e < ntail; e += stride) {
+    const long long tail = cols - 8 * c8;
+    for (long long e = tid; e < rows * tail; e += stride) {
       const long long r = e / tail, c = 8 * c8 + (e - r * tail);
       const double d = static_cast<double>(load1(g + r * ld + c));
       acc = __dadd_rn(acc, __dmul_rn(d, d));
     }
   }
-  finish_sumsq(acc, ws, stats, 0.0f);
+  finish_sumsq(acc, prep_ws(ws_base, mb), stats + mb, 0.0f);
 }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-
 __device__ __forceinline__ void to_out(float v, __nv_bfloat16* p) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void to_out(float v, float* p) { *p = v; }
 
-// X0 = G / (||G||_F + eps) in the compute dtype U, oriented so that X0 is m x n with m <= n.
+// X0_b = G_b / (||G_b||_F + eps) in the compute dtype U, oriented so that X0 is m x n with
+// m <= n (blockIdx.y = matrix). 32 x 32 tiles, transposed through shared memory when needed.
 template <typename T, typename U>
-__global__ void scale_orient_kernel(const T* __restrict__ g, long long rows, long long cols, long long ld,
-                                    int transpose, const zopt_clip_stats* stats, double eps, U* __restrict__ x,
-                                    long long ldx) {
+__global__ void group_scale_orient_kernel(const T* __restrict__ g0, long long rows, long long cols, long long ld,
+                                          long long batch_stride, int transpose, const zopt_clip_stats* stats,
+                                          double eps, U* __restrict__ x0, long long ldx, long long x_stride) {
   __shared__ float s_inv;
   __shared__ float tile[32][33];
+  const int mb = blockIdx.y;
+  const T* g = g0 + mb * batch_stride;
+  U* x = x0 + mb * x_stride;
   if (threadIdx.x == 0 && threadIdx.y == 0) {
-    const double nrm = __dsqrt_rn(stats->sumsq);
+    const double nrm = __dsqrt_rn(stats[mb].sumsq);
     s_inv = __double2float_rn(__ddiv_rn(1.0, __dadd_rn(nrm, eps)));
   }
   __syncthreads();
@@ -439,16 +477,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A 2-D bf16 tensor map over a row-major [outer][inner] matrix with `pitch` elements per row.
+// A 3-D bf16 tensor map over `group` row-major [outer][inner] matrices with `pitch` elements
+// per row, `mat_bytes` apart; boxes of box_inner x box_outer x 1.
 zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long pitch,
-                     int box_inner, int box_outer) {
+                     long long group, long long mat_bytes, int box_inner, int box_outer) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
+                              static_cast<cuuint64_t>(group)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 2, static_cast<cuuint64_t>(mat_bytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -479,27 +519,29 @@ zopt_status error_word(int** host, int** dev) {
 
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
 
+// Workspace: a header (per-matrix reduction scratch and stats), then one region per matrix of
+// the group holding X0, X1 (m x ldx), A and B (m x lda) in the compute dtype (es bytes).
 struct Plan {
-  long long m, n, ldx, lda;
-  size_t off_stats, off_x0, off_x1, off_a, off_b, total;
+  long long m, n, ldx, lda, group;
+  size_t off_stats, header, off_x1, off_a, off_b, per_mat, total;
 };
 
-// Workspace regions; es = bytes per element of the compute dtype.
-Plan plan(long long rows, long long cols, long long es) {
+Plan plan(long long rows, long long cols, long long es, long long group) {
   Plan p;
   p.m = rows < cols ? rows : cols;
   p.n = rows < cols ? cols : rows;
+  p.group = group;
   p.ldx = round_up(p.n, 8);
   p.lda = round_up(p.m, 8);
-  p.off_stats = 256 + sizeof(double) * static_cast<size_t>(kNormMaxBlocks);
-  p.off_stats = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats), 256));
-  p.off_x0 = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats + 256), 1024));
+  p.off_stats = static_cast<size_t>(round_up(group * static_cast<long long>(kPrepWsBytes), 256));
+  p.header = static_cast<size_t>(round_up(static_cast<long long>(p.off_stats) + group * 32, 1024));
   const size_t xbytes = static_cast<size_t>(round_up(p.m * p.ldx * es, 1024));
   const size_t abytes = static_cast<size_t>(round_up(p.m * p.lda * es, 1024));
-  p.off_x1 = p.off_x0 + xbytes;
-  p.off_a = p.off_x1 + xbytes;
-  p.off_b = p.off_a + abytes;
-  p.total = p.off_b + abytes;
+  p.off_x1 = xbytes;
+  p.off_a = 2 * xbytes;
+  p.off_b = 2 * xbytes + abytes;
+  p.per_mat = 2 * xbytes + 2 * abytes;
+  p.total = p.header + static_cast<size_t>(group) * p.per_mat;
   return p;
 }
 
@@ -511,13 +553,16 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, 
   }
   a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
   a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+  long long per = 0;
   if (a.symmetric) {
-    long long cnt = 0;
-    for (int r = 0; r < a.tiles_m; ++r) cnt += a.tiles_n - r / 2;
-    a.num_tiles = static_cast<int>(cnt);
+    for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r / 2;
   } else {
-    a.num_tiles = a.tiles_m * a.tiles_n;
+    per = static_cast<long long>(a.tiles_m) * a.tiles_n;
   }
+  const long long total = per * a.group;
+  if (total < 1 || total > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+  a.tiles_per_mat = static_cast<int>(per);
+  a.num_tiles = static_cast<int>(total);
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
@@ -529,9 +574,9 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, 
 }  // namespace ns
 }  // namespace zopt
 
-extern "C" size_t zopt_ns_workspace(int64_t rows, int64_t cols, zopt_dtype compute_dtype) {
-  if (rows < 1 || cols < 1 || (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)) return 0;
-  return zopt::ns::plan(rows, cols, compute_dtype == ZOPT_F32 ? 4 : 2).total;
+extern "C" size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zopt_dtype compute_dtype) {
+  if (rows < 1 || cols < 1 || group < 1 || (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)) return 0;
+  return zopt::ns::plan(rows, cols, compute_dtype == ZOPT_F32 ? 4 : 2, group).total;
 }
 
 extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io_dtype, int64_t rows, int64_t cols,
@@ -557,8 +602,21 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: coefficients and eps must be finite (eps >= 0)");
   if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace is not 16-byte aligned");
   const bool f32c = compute_dtype == ZOPT_F32;
-  const Plan p = plan(rows, cols, f32c ? 4 : 2);
-  if (ws_bytes < p.total) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace smaller than zopt_ns_workspace");
+  const long long es = f32c ? 4 : 2;
+  // the largest group of matrices the workspace holds, at most the batch
+  long long group = 0;
+  {
+    const Plan one = plan(rows, cols, es, 1);
+    if (ws_bytes >= one.total) {
+      group = static_cast<long long>((ws_bytes - one.header) / one.per_mat);
+      if (group > batch) group = batch;
+      if (group > 65535) group = 65535;  // the matrix index is a grid's y coordinate
+      while (group > 1 && plan(rows, cols, es, group).total > ws_bytes) --group;
+    }
+  }
+  if (group < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace smaller than zopt_ns_workspace");
+  const Plan p = plan(rows, cols, es, group);
+
   int* err_host = nullptr;
   int* err_dev = nullptr;
   zopt_status st = error_word(&err_host, &err_dev);
@@ -570,108 +628,124 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
-  NormWorkspace* nws = reinterpret_cast<NormWorkspace*>(ws);
-  zopt_clip_stats* nstats = reinterpret_cast<zopt_clip_stats*>(ws + p.off_stats);
-  __nv_bfloat16* xb[2] = {reinterpret_cast<__nv_bfloat16*>(ws + p.off_x0),
-                          reinterpret_cast<__nv_bfloat16*>(ws + p.off_x1)};
-  __nv_bfloat16* A = reinterpret_cast<__nv_bfloat16*>(ws + p.off_a);
-  __nv_bfloat16* B = reinterpret_cast<__nv_bfloat16*>(ws + p.off_b);
+  zopt_clip_stats* stats = reinterpret_cast<zopt_clip_stats*>(ws + p.off_stats);
+  uint8_t* mat0 = ws + p.header;  // matrix 0's region; matrix b at + b * per_mat
+  uint8_t* xb[2] = {mat0, mat0 + p.off_x1};
+  uint8_t* A = mat0 + p.off_a;
+  uint8_t* B = mat0 + p.off_b;
+  const long long mat_elems = static_cast<long long>(p.per_mat) / es;  // elements between matrices
   const bool transpose = rows > cols;
 
-  // Tensor maps over the workspace matrices (the same for every matrix of the batch).
+  // Tensor maps over the group's workspace matrices (bf16 tensor-core path only).
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
-  for (int q = 0; q < 2 && !f32c; ++q) {
-    if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, 64, BM)) != ZOPT_OK) return st;
-    if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, 64, BN)) != ZOPT_OK) return st;
-    if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, 64, BK)) != ZOPT_OK) return st;
-  }
   if (!f32c) {
-    if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
-    if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, 64, BN)) != ZOPT_OK) return st;
-    if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, 64, BM)) != ZOPT_OK) return st;
+    const long long mb = static_cast<long long>(p.per_mat);
+    for (int q = 0; q < 2; ++q) {
+      if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BM)) != ZOPT_OK) return st;
+      if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BN)) != ZOPT_OK) return st;
+      if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BK)) != ZOPT_OK) return st;
+    }
+    if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, group, mb, 64, BN)) != ZOPT_OK) return st;
+    if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
   }
 
   const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
-  for (int bi = 0; bi < batch; ++bi) {
-    const uint8_t* g = static_cast<const uint8_t*>(G) + static_cast<size_t>(bi) * batch_stride_g * esz;
-    uint8_t* xo = static_cast<uint8_t*>(X) + static_cast<size_t>(bi) * batch_stride_x * esz;
-    // X0 = G / (||G||_F + eps), oriented
-    ZOPT_CUDA_TRY(cudaMemsetAsync(nws, 0, sizeof(unsigned int), s));
-    const int vec_ok = ((reinterpret_cast<uintptr_t>(g) & 15u) == 0 && (ld_g * esz) % 16 == 0) ? 1 : 0;
-    const int nblk = sms * 4;
+  for (long long g0i = 0; g0i < batch; g0i += group) {
+    const int gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
+    const uint8_t* g = static_cast<const uint8_t*>(G) + static_cast<size_t>(g0i) * batch_stride_g * esz;
+    uint8_t* xo = static_cast<uint8_t*>(X) + static_cast<size_t>(g0i) * batch_stride_x * esz;
+
+    // X0 = G / (||G||_F + eps), oriented, for every matrix of the group
+    ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, static_cast<size_t>(gs) * kPrepWsBytes, s));
+    const bool aligned = (reinterpret_cast<uintptr_t>(g) & 15u) == 0 && (batch_stride_g * esz) % 16 == 0;
+    const int flat = (aligned && ld_g == cols) ? 1 : 0;
+    const int vec_rows = (aligned && (ld_g * esz) % 16 == 0) ? 1 : 0;
+    // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
+    // is bitwise the same whatever group it runs in
+    long long bpm = (rows * cols + 32767) / 32768;
+    bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
+    const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
     if (io_dtype == ZOPT_F32)
-      matrix_sumsq_kernel<float><<<nblk, kNormThreads, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
-                                                               vec_ok, nws, nstats);
+      group_sumsq_kernel<float><<<sg, kNormThreads, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
+                                                            batch_stride_g, flat, vec_rows, ws, stats);
     else
-      matrix_sumsq_kernel<__nv_bfloat16><<<nblk, kNormThreads, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, vec_ok, nws, nstats);
+      group_sumsq_kernel<__nv_bfloat16><<<sg, kNormThreads, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g), rows,
+                                                                    cols, ld_g, batch_stride_g, flat, vec_rows, ws,
+                                                                    stats);
     ZOPT_CUDA_TRY(cudaGetLastError());
     const dim3 tb(32, 8);
+    int sblk = (sms * 8 + gs - 1) / gs;
+    sblk = sblk < 1 ? 1 : sblk;
+    const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
     const int tr = transpose ? 1 : 0;
-    float* xf0 = reinterpret_cast<float*>(xb[0]);
     if (io_dtype == ZOPT_F32 && f32c)
-      scale_orient_kernel<float, float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
-                                                               tr, nstats, eps, xf0, p.ldx);
+      group_scale_orient_kernel<float, float><<<sgrid, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols,
+                                                                    ld_g, batch_stride_g, tr, stats, eps,
+                                                                    reinterpret_cast<float*>(xb[0]), p.ldx, mat_elems);
     else if (io_dtype == ZOPT_F32)
-      scale_orient_kernel<float, __nv_bfloat16><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows,
-                                                                       cols, ld_g, tr, nstats, eps, xb[0], p.ldx);
+      group_scale_orient_kernel<float, __nv_bfloat16><<<sgrid, tb, 0, s>>>(
+          reinterpret_cast<const float*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
+          reinterpret_cast<__nv_bfloat16*>(xb[0]), p.ldx, mat_elems);
     else if (f32c)
-      scale_orient_kernel<__nv_bfloat16, float><<<sms * 8, tb, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g),
-                                                                       rows, cols, ld_g, tr, nstats, eps, xf0, p.ldx);
+      group_scale_orient_kernel<__nv_bfloat16, float><<<sgrid, tb, 0, s>>>(
+          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
+          reinterpret_cast<float*>(xb[0]), p.ldx, mat_elems);
     else
-      scale_orient_kernel<__nv_bfloat16, __nv_bfloat16><<<sms * 8, tb, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, tr, nstats, eps, xb[0], p.ldx);
+      group_scale_orient_kernel<__nv_bfloat16, __nv_bfloat16><<<sgrid, tb, 0, s>>>(
+          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
+          reinterpret_cast<__nv_bfloat16*>(xb[0]), p.ldx, mat_elems);
     ZOPT_CUDA_TRY(cudaGetLastError());
 
-    if (f32c) {
-      float* xf[2] = {reinterpret_cast<float*>(xb[0]), reinterpret_cast<float*>(xb[1])};
-      float* Af = reinterpret_cast<float*>(A);
-      float* Bf = reinterpret_cast<float*>(B);
-      const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
-      int cur = 0;
-      for (int it = 0; it < steps; ++it) {
-        const bool last = it == steps - 1;
-        // A = X X'
-        GemmF32Args fa{m, m, n, xf[cur], p.ldx, xf[cur], p.ldx, 0, 1, 1.0f, 0.0f, nullptr, 0, Af, p.lda, 1, 0};
-        if ((st = launch_gemm_f32(fa, s)) != ZOPT_OK) return st;
-        // B = c A A' + b A
-        GemmF32Args fb{m, m, m, Af, p.lda, Af, p.lda, 0, 1, abc[2], abc[1], Af, p.lda, Bf, p.lda, 1, 0};
-        if ((st = launch_gemm_f32(fb, s)) != ZOPT_OK) return st;
-        // X = B X + a X
-        GemmF32Args fx{m, n, m, Bf, p.lda, xf[cur], p.ldx, 1, 0, 1.0f, abc[0], xf[cur], p.ldx,
-                       last ? static_cast<void*>(xo) : static_cast<void*>(xf[cur ^ 1]), last ? ld_x : p.ldx,
-                       last ? (io_dtype == ZOPT_F32 ? 1 : 0) : 1, last && transpose ? 1 : 0};
-        if ((st = launch_gemm_f32(fx, s)) != ZOPT_OK) return st;
-        cur ^= 1;
-      }
-      continue;
-    }
-
+    const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
       const bool last = it == steps - 1;
-      GemmArgs ga{};
-      ga.err = err_dev;
-      // A = X X'
-      ga.M = static_cast<int>(p.m); ga.N = static_cast<int>(p.m); ga.K = static_cast<int>(p.n);
-      ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
-      ga.D = A; ga.ldd = p.lda; ga.d_f32 = 0; ga.d_trans = 0;
-      if ((st = launch_gemm(mx_p[cur], mx_q[cur], ga, s)) != ZOPT_OK) return st;
-      // B = c A A' + b A
-      ga.K = static_cast<int>(p.m);
-      ga.alpha = abc[2]; ga.beta = abc[1]; ga.R = A; ga.ldr = p.lda; ga.D = B; ga.ldd = p.lda;
-      if ((st = launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
-      // X = B X + a X
-      ga.M = static_cast<int>(p.m); ga.N = static_cast<int>(p.n); ga.K = static_cast<int>(p.m);
-      ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0]; ga.R = xb[cur]; ga.ldr = p.ldx;
-      if (!last) {
-        ga.D = xb[cur ^ 1]; ga.ldd = p.ldx; ga.d_f32 = 0; ga.d_trans = 0;
+      void* xnext = last ? static_cast<void*>(xo) : static_cast<void*>(xb[cur ^ 1]);
+      const long long ldnext = last ? ld_x : p.ldx;
+      const long long dstr_next = last ? batch_stride_x : mat_elems;
+      const int next_f32 = last ? (io_dtype == ZOPT_F32 ? 1 : 0) : (f32c ? 1 : 0);
+      const int next_trans = last && transpose ? 1 : 0;
+      if (f32c) {
+        float* X0 = reinterpret_cast<float*>(xb[cur]);
+        float* Af = reinterpret_cast<float*>(A);
+        float* Bf = reinterpret_cast<float*>(B);
+        // A = X X'
+        GemmF32Args fa{m, m, n, gs, X0, p.ldx, mat_elems, X0, p.ldx, mat_elems, 0, 1, 1.0f, 0.0f, nullptr, 0, 0,
+                       Af, p.lda, mat_elems, 1, 0};
+        if ((st = launch_gemm_f32(fa, s)) != ZOPT_OK) return st;
+        // B = c A A' + b A
+        GemmF32Args fb{m, m, m, gs, Af, p.lda, mat_elems, Af, p.lda, mat_elems, 0, 1, abc[2], abc[1], Af, p.lda,
+                       mat_elems, Bf, p.lda, mat_elems, 1, 0};
+        if ((st = launch_gemm_f32(fb, s)) != ZOPT_OK) return st;
+        // X = B X + a X
+        GemmF32Args fx{m, n, m, gs, Bf, p.lda, mat_elems, X0, p.ldx, mat_elems, 1, 0, 1.0f, abc[0], X0, p.ldx,
+                       mat_elems, xnext, ldnext, dstr_next, next_f32, next_trans};
+        if ((st = launch_gemm_f32(fx, s)) != ZOPT_OK) return st;
       } else {
-        ga.D = xo; ga.ldd = ld_x; ga.d_f32 = io_dtype == ZOPT_F32 ? 1 : 0; ga.d_trans = transpose ? 1 : 0;
+        GemmArgs ga{};
+        ga.err = err_dev;
+        ga.group = gs;
+        // A = X X'
+        ga.M = m; ga.N = m; ga.K = n;
+        ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
+        ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
+        if ((st = launch_gemm(mx_p[cur], mx_q[cur], ga, s)) != ZOPT_OK) return st;
+        // B = c A A' + b A
+        ga.K = m;
+        ga.alpha = abc[2]; ga.beta = abc[1];
+        ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
+        ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
+        if ((st = launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
+        // X = B X + a X
+        ga.M = m; ga.N = n; ga.K = m;
+        ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0];
+        ga.R = reinterpret_cast<const __nv_bfloat16*>(xb[cur]); ga.ldr = p.ldx; ga.r_stride = mat_elems;
+        ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
+        if ((st = launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK) return st;
       }
-      if ((st = launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK) return st;
       cur ^= 1;
     }
   }

@@ -14,19 +14,21 @@ namespace ns {
 // is [K][N] (q_kn = 1) or [N][K] (q_kn = 0). symmetric: M == N, D symmetric, only tiles
 // with tile column >= tile row are computed and the strictly upper part is mirrored.
 // D is fp32 (d_f32) or bf16; d_trans writes D[i, j] at D[j * ldd + i].
+// group: matrices in this launch (blockIdx.y), the *_stride fields their distance in elements.
 struct GemmF32Args {
   int M, N, K;
+  int group;
   const float* P;
-  long long ldp;
+  long long ldp, p_stride;
   const float* Q;
-  long long ldq;
+  long long ldq, q_stride;
   int q_kn;
   int symmetric;
   float alpha, beta;
   const float* R;
-  long long ldr;
+  long long ldr, r_stride;
   void* D;
-  long long ldd;
+  long long ldd, d_stride;
   int d_f32;
   int d_trans;
 };

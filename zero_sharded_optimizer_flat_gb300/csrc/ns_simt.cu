@@ -45,7 +45,14 @@ __device__ __forceinline__ void put(const GemmF32Args& a, long long off, float v
     static_cast<__nv_bfloat16*>(a.D)[off] = __float2bfloat16_rn(v);
 }
 
-__global__ void __launch_bounds__(TT) gemm_f32_kernel(const GemmF32Args a, int tiles_n) {
+__global__ void __launch_bounds__(TT) gemm_f32_kernel(GemmF32Args a, int tiles_n) {
+  {  // this block's matrix of the group
+    const long long mb = blockIdx.y;
+    a.P += mb * a.p_stride;
+    a.Q += mb * a.q_stride;
+    if (a.R != nullptr) a.R += mb * a.r_stride;
+    a.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
+  }
   __shared__ __align__(16) float As[2][TK][TM + kPad];
   __shared__ __align__(16) float Bs[2][TK][TN + kPad];
   int ti, tj;
@@ -143,7 +150,8 @@ zopt_status launch_gemm_f32(const GemmF32Args& a, cudaStream_t stream) {
     tiles = static_cast<long long>(tiles_m) * tiles_n;
   }
   if (tiles < 1 || tiles > 0x7FFFFFFF) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: fp32 product too large");
-  gemm_f32_kernel<<<static_cast<unsigned>(tiles), TT, 0, stream>>>(a, tiles_n);
+  if (a.group < 1 || a.group > 65535) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: group out of range");
+  gemm_f32_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(a.group)), TT, 0, stream>>>(a, tiles_n);
   ZOPT_CUDA_TRY(cudaGetLastError());
   return ok();
 }
