@@ -9,8 +9,9 @@
 //
 // acc = g_1 (first micro-step: acc is not read), then acc = acc + g_k in fp32, each addition
 // rounded, in micro-step order. Bytes per element: 6 (first, bf16), 10 (later micro-steps).
-// Each thread issues the loads of four 8-element vectors (i, i + stride, ...) before it adds
-// and stores any of them, so that enough bytes are in flight to keep HBM busy.
+// The arrays are walked in 4-element units, a warp's 32 units contiguous (512 B of fp32, 256 B of
+// bf16 per load instruction); each thread issues the loads of four units before it adds and
+// stores any of them, so that enough bytes are in flight to keep HBM busy.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -20,56 +21,41 @@
 namespace zopt {
 namespace {
 
-constexpr int kUnroll = 4;  // 8-element vectors per thread per iteration, all loads issued first
-
-__device__ __forceinline__ void ld_acc8(const float* p, float (&a)[8]) {
-  const float4 u = reinterpret_cast<const float4*>(p)[0], w = reinterpret_cast<const float4*>(p)[1];
-  a[0] = u.x; a[1] = u.y; a[2] = u.z; a[3] = u.w; a[4] = w.x; a[5] = w.y; a[6] = w.z; a[7] = w.w;
-}
-
-__device__ __forceinline__ void st_acc8(float* p, const float (&x)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+__device__ __forceinline__ float4 add4(const float4& a, const float4& b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
 }
 
 template <typename T, bool kFirst, bool kLast>
 __global__ void __launch_bounds__(kNormThreads) accum_kernel(float* __restrict__ acc, const T* __restrict__ g, int64_t n,
                                                               float max_norm, NormWorkspace* ws,
                                                               zopt_clip_stats* stats) {
-  const int64_t nvec = n / 8;
+  const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float4* acc4 = reinterpret_cast<float4*>(acc);
   double ss = 0.0;
-  for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
-    float x[kUnroll][8], a[kUnroll][8];
+  for (; j + 3 * stride < n4; j += 4 * stride) {
+    float4 x[4], a[4];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      load8(g + 8 * (i + u * stride), x[u]);
-      if (!kFirst) ld_acc8(acc + 8 * (i + u * stride), a[u]);
+    for (int u = 0; u < 4; ++u) {  // every load of the four units first
+      x[u] = load4(g + 4 * (j + u * stride));
+      if (!kFirst) a[u] = acc4[j + u * stride];
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (!kFirst) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[u][k] = __fadd_rn(a[u][k], x[u][k]);
-      }
-      st_acc8(acc + 8 * (i + u * stride), x[u]);
-      if (kLast) ss = __dadd_rn(ss, sumsq8(x[u]));
+    for (int u = 0; u < 4; ++u) {
+      if (!kFirst) x[u] = add4(a[u], x[u]);
+      acc4[j + u * stride] = x[u];
     }
+    if (kLast) ss = __dadd_rn(ss, __dadd_rn(sumsq44(x[0], x[1]), sumsq44(x[2], x[3])));
   }
-  for (; i < nvec; i += stride) {
-    float x[8], a[8];
-    load8(g + 8 * i, x);
-    if (!kFirst) {
-      ld_acc8(acc + 8 * i, a);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = __fadd_rn(a[k], x[k]);
-    }
-    st_acc8(acc + 8 * i, x);
-    if (kLast) ss = __dadd_rn(ss, sumsq8(x));
+  for (; j < n4; j += stride) {
+    float4 x = load4(g + 4 * j);
+    if (!kFirst) x = add4(acc4[j], x);
+    acc4[j] = x;
+    if (kLast) ss = __dadd_rn(ss, sumsq44(x, make_float4(0.f, 0.f, 0.f, 0.f)));
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t k = nvec * 8; k < n; ++k) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
       const float v = kFirst ? load1(g + k) : __fadd_rn(acc[k], load1(g + k));
       acc[k] = v;
       if (kLast) ss = __dadd_rn(ss, __dmul_rn(static_cast<double>(v), static_cast<double>(v)));

@@ -87,6 +87,20 @@ __device__ __forceinline__ float load1(const __nv_bfloat16* p) {
   return __uint_as_float(static_cast<unsigned int>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
 }
 
+// 4-element units: a warp's 32 consecutive units are 512 contiguous bytes of fp32 (256 of
+// bf16), so every load instruction is fully coalesced.
+__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+// sum of squares of two 4-element units (as one run of 8)
+__device__ __forceinline__ double sumsq44(const float4& a, const float4& b) {
+  const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  return sumsq8(x);
+}
+
 // Butterfly sum of an fp64 value over the block (fixed order); result valid in thread 0.
 __device__ __forceinline__ double block_sum(double v, double* smem32) {
 #pragma unroll
@@ -134,23 +148,19 @@ __device__ __forceinline__ void finish_sumsq(double acc, NormWorkspace* ws, zopt
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict__ g, int64_t n, float max_norm,
                                                              NormWorkspace* ws, zopt_clip_stats* stats) {
-  const int64_t nvec = n / 8;
+  const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double acc = 0.0;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {  // four vectors' loads in flight per thread
-    float x[4][8];
+  for (; j + 3 * stride < n4; j += 4 * stride) {  // four units' loads in flight per thread
+    float4 x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) load8(g + 8 * (i + u * stride), x[u]);
-    acc = __dadd_rn(acc, __dadd_rn(__dadd_rn(sumsq8(x[0]), sumsq8(x[1])), __dadd_rn(sumsq8(x[2]), sumsq8(x[3]))));
+    for (int u = 0; u < 4; ++u) x[u] = load4(g + 4 * (j + u * stride));
+    acc = __dadd_rn(acc, __dadd_rn(sumsq44(x[0], x[1]), sumsq44(x[2], x[3])));
   }
-  for (; i < nvec; i += stride) {
-    float x[8];
-    load8(g + 8 * i, x);
-    acc = __dadd_rn(acc, sumsq8(x));
-  }
+  for (; j < n4; j += stride) acc = __dadd_rn(acc, sumsq44(load4(g + 4 * j), make_float4(0.f, 0.f, 0.f, 0.f)));
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t k = nvec * 8; k < n; ++k) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
       const double d = static_cast<double>(load1(g + k));
       acc = __dadd_rn(acc, __dmul_rn(d, d));
     }
