@@ -248,6 +248,58 @@ ZOPT_API zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io
                                            int32_t steps, const float* abc, float eps, void* d_ws, size_t ws_bytes,
                                            zopt_stream stream);
 
+/* ======================================================================================
+ * 5. Muon's update around Newton-Schulz (matrices owned whole by this rank)
+ *
+ * bluscript_zero_ckpt.cpp, ShardedMuon: the owner rank keeps each matrix's fp32 master and
+ * momentum; momentum 0.95 with Nesterov; decoupled weight decay; U = NewtonSchulz(u);
+ * adjust_lr "match_rms_adamw" lifts the update RMS to 0.2 (scale 0.2*sqrt(max(rows, cols))),
+ * "original" uses sqrt(max(1, rows/cols)); nsratio = ||U||_F / sqrt(min(rows, cols)) and a
+ * divergence guard on the largest |U| element.
+ *
+ * Per matrix, each operation rounded to fp32 as written:
+ *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(u) (bf16 compute);
+ *   unless max|U| > guard (or not finite): p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U;
+ *   out = bf16_rne(p).  A rejected matrix keeps its master; its momentum is still updated.
+ * ====================================================================================== */
+#define ZOPT_MUON_MATCH_RMS_ADAMW 0
+#define ZOPT_MUON_ORIGINAL 1
+
+typedef struct zopt_muon_hparams {
+  double lr;
+  double momentum;
+  double weight_decay;
+  int32_t nesterov;  /* 1: u = g + mu*buf */
+  int32_t adjust;    /* ZOPT_MUON_MATCH_RMS_ADAMW or ZOPT_MUON_ORIGINAL */
+  int32_t ns_steps;  /* Newton-Schulz steps (5) */
+  float abc[3];      /* quintic coefficients */
+  float eps;         /* Newton-Schulz normalisation eps (1e-7) */
+  float guard;       /* reject an update with an element of magnitude above this (1000) */
+} zopt_muon_hparams;
+
+typedef struct zopt_muon_stats {
+  float update_fro; /* ||U||_F */
+  float ns_ratio;   /* ||U||_F / sqrt(min(rows, cols)), healthy ~1 */
+  float max_abs;    /* largest |U| element */
+  uint32_t rejected;
+} zopt_muon_stats; /* 16 bytes per matrix, device resident */
+
+/* Workspace bytes to step `group` rows x cols matrices together (the Newton-Schulz workspace
+ * plus two fp32 matrices per group member). A call steps its batch in groups of as many
+ * matrices as the workspace holds. */
+ZOPT_API size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group);
+/* One Muon step of `batch` rows x cols matrices stored back to back (matrix b at offset
+ * b*rows*cols of master, momentum, grad and out_bf16). master, momentum: fp32; grad: fp32 or
+ * bf16; out_bf16: may be NULL; d_stats: `batch` structs. Errors: EINVAL for NULL or
+ * misaligned pointers (16 bytes; a batch needs rows*cols to be a multiple of 4), an empty
+ * shape, out-of-range hyper-parameters (lr < 0, momentum outside [0, 1), steps < 1, guard <=
+ * 0), a short workspace; EUNSUPPORTED for another gradient dtype; and the errors of
+ * zopt_ns_orthogonalize. */
+ZOPT_API zopt_status zopt_muon_step(float* master, float* momentum, const void* grad, zopt_dtype grad_dtype,
+                                    uint16_t* out_bf16, int64_t rows, int64_t cols, int32_t batch,
+                                    const zopt_muon_hparams* hparams, zopt_muon_stats* d_stats, void* d_ws,
+                                    size_t ws_bytes, zopt_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

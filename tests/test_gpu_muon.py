@@ -1,0 +1,100 @@
+"""GPU parity of zopt_muon_step against the oracle's Muon update (bluscript_zero_ckpt.cpp,
+ShardedMuon: momentum with Nesterov, U = NewtonSchulz(u), adjust_lr scale, decoupled decay,
+nsratio and the divergence guard).
+
+Bar: the momentum buffer bit for bit (fp32, same operation order); the applied update
+(p_old*fp32(1 - lr*wd) - p_new) / fp32(lr*scale) within relative Frobenius error 2e-2 of the
+oracle's fp64 Newton-Schulz of the same u (the bf16 Newton-Schulz tolerance); nsratio within
+2e-2; the bf16 weights bit for bit the round-out of the new master; a rejected matrix keeps
+its master bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import muon as OM
+from oracle.bf16 import f32_to_bf16_bits
+from oracle.ns import newton_schulz
+
+pytestmark = pytest.mark.gpu
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+@pytest.mark.parametrize("rows,cols,batch,group", [(256, 768, 1, 1), (768, 256, 1, 1), (384, 1000, 3, 2),
+                                                    (2048, 512, 2, 2), (130, 70, 1, 1)])
+@pytest.mark.parametrize("match", [True, False])
+def test_three_steps_match_oracle(zopt, rows, cols, batch, group, match):
+    h = OM.MuonHyper(lr=8e-4, match_rms_adamw=match)
+    gen = torch.Generator(device="cuda").manual_seed(rows + cols + batch)
+    p = (torch.randn(batch, rows, cols, generator=gen, device="cuda") * 0.02)
+    buf = torch.zeros_like(p)
+    out = torch.zeros(batch, rows, cols, dtype=torch.int16, device="cuda")
+    ws = zopt.new_muon_workspace(rows, cols, group)
+    stats = zopt.new_muon_stats(batch)
+    ref_buf = np.zeros((batch, rows, cols), np.float32)
+    decay = np.float32(1.0 - h.lr * h.weight_decay)
+    step = np.float32(h.lr * OM.lr_scale(rows, cols, match))
+    for s in range(3):
+        g = (torch.randn(batch, rows, cols, generator=gen, device="cuda") * 1e-3).bfloat16()
+        p_old = p.cpu().numpy()
+        zopt.muon_step(p, buf, g, out, ws, stats, lr=h.lr, match_rms_adamw=match)
+        torch.cuda.synchronize()
+        st = zopt.read_muon_stats(stats)
+        pn = p.cpu().numpy()
+        for b in range(batch):
+            u = OM.momentum_f32(ref_buf[b], g[b].float().cpu().numpy(), h)
+            U_ref = newton_schulz(u.astype(np.float64), steps=5)
+            applied = (p_old[b] * decay - pn[b]).astype(np.float64) / float(step)
+            assert rel(applied, U_ref) <= 2e-2, (s, b)
+            assert abs(st[b]["ns_ratio"] - np.linalg.norm(U_ref) / math.sqrt(min(rows, cols))) <= 2e-2
+            assert not st[b]["rejected"] and abs(st[b]["max_abs"] / np.max(np.abs(U_ref)) - 1) < 0.1
+        assert np.array_equal(buf.cpu().numpy().view(np.uint32), ref_buf.view(np.uint32))
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))
+
+
+def test_guard_rejects_keeps_master_updates_momentum(zopt):
+    rows, cols = 200, 300
+    p = torch.randn(rows, cols, device="cuda") * 0.02
+    p0 = p.clone()
+    buf = torch.zeros_like(p)
+    g = torch.randn(rows, cols, device="cuda")
+    out = torch.zeros(rows, cols, dtype=torch.int16, device="cuda")
+    stats = zopt.new_muon_stats()
+    zopt.muon_step(p, buf, g, out, zopt.new_muon_workspace(rows, cols), stats, lr=1e-3, guard=1e-3)
+    torch.cuda.synchronize()
+    st = zopt.read_muon_stats(stats)[0]
+    assert st["rejected"] and torch.equal(p, p0) and torch.equal(buf, g)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(p0.cpu().numpy()))
+
+
+def test_llama_owned_set_one_step(zopt):
+    """The 1.1B set's matrices owned by rank 0 of 8 (round-robin): 4 x Wq, 4 x Wv, 4 x gate_up,
+    one Muon step per shape group."""
+    import workloads
+    w = workloads.get("c3")
+    owned = w.owned_muon()
+    assert len(owned) == 12
+    shapes = sorted({p.shape for p in owned})
+    h = OM.MuonHyper(lr=8e-4)
+    for (r, c) in shapes:
+        k = sum(1 for p in owned if p.shape == (r, c))
+        p = torch.randn(k, r, c, device="cuda") * 0.02
+        p_old = p.cpu().numpy()
+        buf = torch.zeros_like(p)
+        g = (torch.randn(k, r, c, device="cuda") * 1e-3).bfloat16()
+        stats = zopt.new_muon_stats(k)
+        zopt.muon_step(p, buf, g, None, zopt.new_muon_workspace(r, c, k), stats, lr=h.lr)
+        torch.cuda.synchronize()
+        step = np.float32(h.lr * OM.lr_scale(r, c, True))
+        decay = np.float32(1.0 - h.lr * h.weight_decay)
+        b = k - 1  # check the last matrix of the group against the oracle
+        u = OM.momentum_f32(np.zeros((r, c), np.float32), g[b].float().cpu().numpy(), h)
+        U_ref = newton_schulz(u.astype(np.float64), steps=5)
+        applied = (p_old[b] * decay - p[b].cpu().numpy()).astype(np.float64) / float(step)
+        assert rel(applied, U_ref) <= 2e-2

@@ -41,6 +41,12 @@ class _Hparams(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class _MuonHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("momentum", ctypes.c_double), ("weight_decay", ctypes.c_double),
+                ("nesterov", ctypes.c_int32), ("adjust", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
+                ("abc", ctypes.c_float * 3), ("eps", ctypes.c_float), ("guard", ctypes.c_float)]
+
+
 def lib() -> ctypes.CDLL:
     """The loaded library; raises if it has not been built."""
     global _lib
@@ -74,6 +80,9 @@ def lib() -> ctypes.CDLL:
                                            vp, vp, vp]),
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
         "zopt_ns_workspace": (sz, [i64, i64, i32, ctypes.c_int]),
+        "zopt_muon_workspace": (sz, [i64, i64, i32]),
+        "zopt_muon_step": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, vp, i64, i64, i32, ctypes.POINTER(_MuonHparams),
+                                          vp, vp, sz, vp]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
                                                  ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
                                                  vp, sz, vp]),
@@ -305,3 +314,45 @@ def ns_orthogonalize(G, X, ws, steps: int = 5, abc=DEFAULT_ABC, eps: float = 1e-
     _check(lib().zopt_ns_orthogonalize(_ptr(G), _ptr(X), _dtype_code(G), rows, cols, ldg, ldx, sg, sx, batch,
                                        int(compute), int(steps), coef, float(eps), _ptr(ws), ws.numel(),
                                        _stream(stream)))
+
+
+# --------------------------------------------------------------------------- Muon
+
+MUON_STATS_BYTES = 16
+
+
+def muon_workspace(rows: int, cols: int, group: int = 1) -> int:
+    return int(lib().zopt_muon_workspace(int(rows), int(cols), int(group)))
+
+
+def new_muon_workspace(rows: int, cols: int, group: int = 1, device="cuda"):
+    import torch
+    return torch.empty(max(muon_workspace(rows, cols, group), 16), dtype=torch.uint8, device=device)
+
+
+def new_muon_stats(batch: int = 1, device="cuda"):
+    import torch
+    return torch.zeros(MUON_STATS_BYTES * batch, dtype=torch.uint8, device=device)
+
+
+def read_muon_stats(t) -> list:
+    """Decode zopt_muon_stats entries (copies them to the host: logging/tests only)."""
+    b = bytes(t.detach().cpu().numpy().tobytes())
+    out = []
+    for k in range(len(b) // MUON_STATS_BYTES):
+        fro, ratio, mx, rej = struct.unpack("<fffI", b[16 * k:16 * k + 16])
+        out.append({"update_fro": fro, "ns_ratio": ratio, "max_abs": mx, "rejected": bool(rej)})
+    return out
+
+
+def muon_step(master, momentum, grad, out_bf16, ws, stats, *, lr: float, momentum_coef: float = 0.95,
+              weight_decay: float = 0.1, nesterov: bool = True, match_rms_adamw: bool = True, ns_steps: int = 5,
+              abc=DEFAULT_ABC, eps: float = 1e-7, guard: float = 1000.0, stream=None) -> None:
+    """``zopt_muon_step`` on a matrix [rows, cols] or a batch [b, rows, cols] (contiguous)."""
+    shape = tuple(master.shape)
+    batch, rows, cols = (1, *shape) if len(shape) == 2 else shape
+    hp = _MuonHparams(float(lr), float(momentum_coef), float(weight_decay), int(bool(nesterov)),
+                      0 if match_rms_adamw else 1, int(ns_steps), (ctypes.c_float * 3)(*[float(c) for c in abc]),
+                      float(eps), float(guard))
+    _check(lib().zopt_muon_step(_ptr(master), _ptr(momentum), _ptr(grad), _dtype_code(grad), _ptr(out_bf16), rows,
+                                cols, batch, ctypes.byref(hp), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)))

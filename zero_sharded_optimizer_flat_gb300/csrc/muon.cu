@@ -1,0 +1,227 @@
+// Muon's update around Newton-Schulz, for the matrices a rank owns whole.
+//
+// bluscript_zero_ckpt.cpp, ShardedMuon: each matrix has one owner rank holding its fp32 master
+// and momentum; momentum 0.95 with Nesterov, decoupled weight decay, U = NewtonSchulz(u);
+// adjust_lr "match_rms_adamw" lifts the update's RMS to 0.2 (scale 0.2*sqrt(max(rows, cols)))
+// and "original" uses sqrt(max(1, rows/cols)); diagnostics nsratio = ||U||_F/sqrt(min(rows,
+// cols)) and a divergence guard that rejects an update with an element above 1000.
+//
+// Per group of matrices (as many as the workspace holds), four steps on the caller's stream:
+//   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 14-16 B/elem)
+//   2. U = NewtonSchulz(u) through zopt_ns_orthogonalize (fp32 in/out, bf16 tensor cores)
+//   3. per matrix: sum of squares and largest magnitude of U                 (4 B/elem)
+//   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (14 B/elem)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "norm_impl.cuh"
+
+namespace zopt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxBlocksPerMat = 512;
+constexpr size_t kRedBytes = 256 + sizeof(double) * kMaxBlocksPerMat;  // one NormWorkspace per matrix
+
+long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+struct MuonPlan {
+  size_t off_max, off_cs, off_u, off_o, off_ns, ns_bytes, total;
+};
+
+MuonPlan muon_plan(long long rows, long long cols, long long group) {
+  MuonPlan p;
+  const long long n = rows * cols;
+  p.off_max = static_cast<size_t>(round_up(group * static_cast<long long>(kRedBytes), 256));
+  p.off_cs = static_cast<size_t>(round_up(static_cast<long long>(p.off_max) + group * 4, 256));
+  p.off_u = static_cast<size_t>(round_up(static_cast<long long>(p.off_cs) + group * 32, 1024));
+  p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 4, 1024));
+  p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 4, 1024));
+  p.ns_bytes = zopt_ns_workspace(rows, cols, static_cast<int32_t>(group), ZOPT_BF16);
+  p.total = p.off_ns + p.ns_bytes;
+  return p;
+}
+
+__device__ __forceinline__ float4 fma4_momentum(float mu, const float4& b, const float4& g) {
+  return make_float4(__fadd_rn(__fmul_rn(mu, b.x), g.x), __fadd_rn(__fmul_rn(mu, b.y), g.y),
+                     __fadd_rn(__fmul_rn(mu, b.z), g.z), __fadd_rn(__fmul_rn(mu, b.w), g.w));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) momentum_kernel(float* __restrict__ buf, const T* __restrict__ g,
+                                                             float* __restrict__ u, int64_t n, float mu, int nesterov) {
+  const int64_t n4 = n / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float4* b4 = reinterpret_cast<float4*>(buf);
+  float4* u4 = reinterpret_cast<float4*>(u);
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
+    const float4 gv = load4(g + 4 * j);
+    const float4 b = fma4_momentum(mu, b4[j], gv);
+    b4[j] = b;
+    u4[j] = nesterov ? fma4_momentum(mu, b, gv) : b;  // g + mu*buf, as the same two roundings
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
+      const float gv = load1(g + k);
+      const float b = __fadd_rn(__fmul_rn(mu, buf[k]), gv);
+      buf[k] = b;
+      u[k] = nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
+    }
+  }
+}
+
+// Per matrix (blockIdx.y): sum of squares of U (fp64, as the norm kernel) and max |U| (the
+// fp32 bit patterns of non-negative values order as unsigned integers; NaN sorts above inf).
+__global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restrict__ U0, int64_t n, uint8_t* red,
+                                                           unsigned* maxbits, zopt_clip_stats* cs) {
+  const int mb = blockIdx.y;
+  const float* U = U0 + mb * n;
+  const int64_t n4 = n / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  double acc = 0.0;
+  unsigned mx = 0;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
+    const float4 x = load4(U + 4 * j);
+    acc = __dadd_rn(acc, sumsq44(x, make_float4(0.f, 0.f, 0.f, 0.f)));
+    mx = max(mx, max(max(__float_as_uint(x.x) & 0x7FFFFFFFu, __float_as_uint(x.y) & 0x7FFFFFFFu),
+                     max(__float_as_uint(x.z) & 0x7FFFFFFFu, __float_as_uint(x.w) & 0x7FFFFFFFu)));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
+      const float x = U[k];
+      acc = __dadd_rn(acc, __dmul_rn(static_cast<double>(x), static_cast<double>(x)));
+      mx = max(mx, __float_as_uint(x) & 0x7FFFFFFFu);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(maxbits + mb, mx);
+  finish_sumsq(acc, reinterpret_cast<NormWorkspace*>(red + mb * kRedBytes), cs + mb, 0.0f);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    update_kernel(float* __restrict__ p0, const float* __restrict__ U0, uint16_t* __restrict__ out0, int64_t n,
+                  const zopt_clip_stats* cs, const unsigned* maxbits, float decay, float step, float guard,
+                  float sqrt_min_dim, zopt_muon_stats* st) {
+  const int mb = blockIdx.y;
+  float* p = p0 + mb * n;
+  const float* U = U0 + mb * n;
+  uint16_t* out = out0 ? out0 + mb * n : nullptr;
+  const float max_abs = __uint_as_float(maxbits[mb]);
+  const bool rejected = !(max_abs <= guard);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const float fro = cs[mb].norm;
+    st[mb] = zopt_muon_stats{fro, __fdiv_rn(fro, sqrt_min_dim), max_abs, rejected ? 1u : 0u};
+  }
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride) {
+    float v = p[k];
+    if (!rejected) {
+      v = __fsub_rn(__fmul_rn(v, decay), __fmul_rn(step, U[k]));
+      p[k] = v;
+    }
+    if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+}
+
+}  // namespace
+}  // namespace zopt
+
+extern "C" size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group) {
+  if (rows < 1 || cols < 1 || group < 1) return 0;
+  return zopt::muon_plan(rows, cols, group).total;
+}
+
+extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void* grad, zopt_dtype grad_dtype,
+                                      uint16_t* out_bf16, int64_t rows, int64_t cols, int32_t batch,
+                                      const zopt_muon_hparams* hp, zopt_muon_stats* d_stats, void* d_ws,
+                                      size_t ws_bytes, zopt_stream stream) {
+  using namespace zopt;
+  if (master == nullptr || momentum == nullptr || grad == nullptr || hp == nullptr || d_stats == nullptr ||
+      d_ws == nullptr)
+    return fail(ZOPT_EINVAL, "zopt_muon_step: NULL pointer");
+  if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, "zopt_muon_step: empty matrix or batch");
+  if (!aligned16(master) || !aligned16(momentum) || !aligned16(grad) || !aligned16(d_ws) ||
+      (out_bf16 != nullptr && (reinterpret_cast<uintptr_t>(out_bf16) & 1u) != 0) ||
+      (reinterpret_cast<uintptr_t>(d_stats) & 3u) != 0)
+    return fail(ZOPT_EINVAL, "zopt_muon_step: a device pointer is misaligned");
+  if (((rows * cols) & 3) != 0 && batch > 1)
+    return fail(ZOPT_EINVAL, "zopt_muon_step: a batch needs rows*cols to be a multiple of 4 (16-byte matrices)");
+  if (grad_dtype != ZOPT_F32 && grad_dtype != ZOPT_BF16)
+    return fail(ZOPT_EUNSUPPORTED, "zopt_muon_step: gradient dtype must be fp32 or bf16");
+  if (!std::isfinite(hp->lr) || hp->lr < 0 || !(hp->momentum >= 0 && hp->momentum < 1) ||
+      !std::isfinite(hp->weight_decay) || hp->ns_steps < 1 || (hp->adjust != ZOPT_MUON_MATCH_RMS_ADAMW &&
+                                                                hp->adjust != ZOPT_MUON_ORIGINAL) ||
+      !(hp->guard > 0))
+    return fail(ZOPT_EINVAL, "zopt_muon_step: hyper-parameters out of range");
+  const long long n = rows * cols;
+  long long group = 0;
+  {
+    const MuonPlan one = muon_plan(rows, cols, 1);
+    if (ws_bytes >= one.total) {
+      group = batch;
+      if (group > 65535) group = 65535;
+      while (group > 1 && muon_plan(rows, cols, group).total > ws_bytes) --group;
+    }
+  }
+  if (group < 1) return fail(ZOPT_EINVAL, "zopt_muon_step: workspace smaller than zopt_muon_workspace(rows, cols, 1)");
+  const MuonPlan P = muon_plan(rows, cols, group);
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  unsigned* maxbits = reinterpret_cast<unsigned*>(ws + P.off_max);
+  zopt_clip_stats* cs = reinterpret_cast<zopt_clip_stats*>(ws + P.off_cs);
+  float* U_in = reinterpret_cast<float*>(ws + P.off_u);
+  float* U_out = reinterpret_cast<float*>(ws + P.off_o);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_muon_step: no CUDA device");
+
+  const float mu = static_cast<float>(hp->momentum);
+  const double scale = hp->adjust == ZOPT_MUON_MATCH_RMS_ADAMW
+                           ? 0.2 * std::sqrt(static_cast<double>(rows > cols ? rows : cols))
+                           : std::sqrt(rows > cols ? static_cast<double>(rows) / static_cast<double>(cols) : 1.0);
+  const double lrwd = hp->lr * hp->weight_decay;
+  const float decay = static_cast<float>(1.0 - lrwd);
+  const double lrs = hp->lr * scale;
+  const float step = static_cast<float>(lrs);
+  const float sqrt_min = static_cast<float>(std::sqrt(static_cast<double>(rows < cols ? rows : cols)));
+  const size_t gsz = grad_dtype == ZOPT_F32 ? 4 : 2;
+
+  for (long long b0 = 0; b0 < batch; b0 += group) {
+    const int gs = static_cast<int>(batch - b0 < group ? batch - b0 : group);
+    const long long ng = n * gs;
+    float* pm = master + b0 * n;
+    float* bm = momentum + b0 * n;
+    const uint8_t* gm = static_cast<const uint8_t*>(grad) + static_cast<size_t>(b0 * n) * gsz;
+    // 1. momentum over the group's matrices (contiguous), u into the workspace
+    long long blocks = (ng / 4 + kThreads - 1) / kThreads;
+    if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
+    if (blocks < 1) blocks = 1;
+    if (grad_dtype == ZOPT_F32)
+      momentum_kernel<float><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+          bm, reinterpret_cast<const float*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
+    else
+      momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+          bm, reinterpret_cast<const __nv_bfloat16*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+    // 2. U = NewtonSchulz(u), fp32 in and out, bf16 tensor cores
+    zopt_status st = zopt_ns_orthogonalize(U_in, U_out, ZOPT_F32, rows, cols, cols, cols, n, n, gs, ZOPT_BF16,
+                                           hp->ns_steps, hp->abc, hp->eps, ws + P.off_ns, P.ns_bytes, stream);
+    if (st != ZOPT_OK) return st;
+    // 3. per-matrix ||U|| and max |U|
+    ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, P.off_cs, s));  // reduction counters and maxima start at zero
+    long long bpm = (n + 32767) / 32768;
+    bpm = bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm);
+    ustats_kernel<<<dim3(static_cast<unsigned>(bpm), static_cast<unsigned>(gs)), kThreads, 0, s>>>(U_out, n, ws,
+                                                                                                  maxbits, cs);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+    // 4. the guarded update and bf16 round-out
+    update_kernel<<<dim3(static_cast<unsigned>(bpm), static_cast<unsigned>(gs)), kThreads, 0, s>>>(
+        pm, U_out, out_bf16 ? out_bf16 + b0 * n : nullptr, n, cs, maxbits, decay, step, hp->guard, sqrt_min,
+        d_stats + b0);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+  }
+  return ok();
+}
