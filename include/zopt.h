@@ -211,6 +211,22 @@ ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d
                             uint16_t* out_bf16, const zopt_adamw_hparams* hparams,
                             const zopt_clip_stats* d_clip, zopt_adam_state* d_state, zopt_stream stream);
 
+/* Re-target the last step (t = d_state->step, not advanced) from g*old_scale to g*new_scale,
+ * in one pass (DeepSpeed PR #9021, adam_rescale_step commit: a step taken speculatively on
+ * an unclipped gradient becomes the step on the final clip coefficient without an undo and a
+ * redo). Per element, each operation an fp32 rounding: d(m, v) = m / (sqrt(v)/fp32(sqrt(1 -
+ * beta2^t)) + eps); u_old = d(m, v); m += fp32((1-b1)(new-old))*g;
+ * v = max(0, v + fp32((1-b2)(new^2-old^2))*(g*g)) (a NaN stays NaN); p += fp32(lr/(1 -
+ * beta1^t))*(u_old - d(m, v)); out = bf16_rne(p). The decoupled decay cancels. With d_clip
+ * non-NULL new_scale is d_clip->clip_coef, and a found_inf there leaves everything unchanged;
+ * with no step taken yet (step 0) the call changes nothing. Same buffers and errors as
+ * zopt_adamw_step (the no-decay table is not needed). */
+ZOPT_API zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* master, float* exp_avg,
+                                             float* exp_avg_sq, const void* grad, zopt_dtype grad_dtype,
+                                             uint16_t* out_bf16, const zopt_adamw_hparams* hparams, float old_scale,
+                                             float new_scale, const zopt_clip_stats* d_clip,
+                                             const zopt_adam_state* d_state, zopt_stream stream);
+
 /* ======================================================================================
  * 4. Muon's quintic Newton-Schulz on whole matrices
  *

@@ -124,3 +124,39 @@ def step_flat_f32(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray, de
     v[...] = sc.beta2 * v + sc.one_minus_beta2 * (g32 * g32)
     denom = np.sqrt(v) / sc.bc2_sqrt + sc.eps
     p -= sc.step_size * (m / denom)
+
+
+def rescale_step_f32(p: np.ndarray, m: np.ndarray, v: np.ndarray, g_in: np.ndarray, old_scale, new_scale,
+                     h: Hyper, t: int) -> None:
+    """Re-target the AdamW step t that was taken on g*old_scale to the step on g*new_scale, in
+    place and in one pass (DeepSpeed PR #9021, adam_rescale_step commit):
+        m += (1-beta1)*(new-old)*g;  v = max(0, v + (1-beta2)*(new^2-old^2)*g^2)  (NaN kept);
+        p += step_size*(m_old/d_old - m_new/d_new)   (the decay does not depend on g: cancels)
+    with d = sqrt(v)/sqrt(1-beta2^t) + eps. Readings: the page prints the weight change as
+    step_size*(update_new - update_old) in a convention where the update is the signed
+    increment; here it is written as what the commit states it achieves — the weights of the
+    step on the new scale. km = fp32((1-beta1)*(new-old)) and kv = fp32((1-beta2)*(new^2-old^2))
+    are formed in fp64; each array operation is an fp32 rounding in the order written."""
+    sc = scalars_f32(h, t)
+    old, new = float(old_scale), float(new_scale)
+    km = F32((1.0 - h.beta1) * (new - old))
+    kv = F32((1.0 - h.beta2) * (new * new - old * old))
+    g = g_in.astype(np.float32)
+    u_old = m / (np.sqrt(v) / sc.bc2_sqrt + sc.eps)
+    m[...] = m + km * g
+    vv = v + kv * (g * g)
+    v[...] = np.where(vv < 0, F32(0.0), vv)
+    u_new = m / (np.sqrt(v) / sc.bc2_sqrt + sc.eps)
+    p += sc.step_size * (u_old - u_new)
+
+
+def rescale_step_f64(p, m, v, g_in, old_scale, new_scale, h: Hyper, t: int) -> None:
+    """The same re-targeting in fp64 with unrounded scalars (the precision reference)."""
+    g = np.asarray(g_in, dtype=np.float64)
+    bc2 = math.sqrt(1.0 - beta_power(h.beta2, t))
+    step = h.lr / (1.0 - beta_power(h.beta1, t))
+    u_old = m / (np.sqrt(v) / bc2 + h.eps)
+    m[...] = m + (1.0 - h.beta1) * (new_scale - old_scale) * g
+    v[...] = np.maximum(0.0, v + (1.0 - h.beta2) * (new_scale ** 2 - old_scale ** 2) * g * g)
+    u_new = m / (np.sqrt(v) / bc2 + h.eps)
+    p += step * (u_old - u_new)

@@ -229,3 +229,61 @@ def test_full_size_zero2_shard_sampled(zopt):
         assert np.array_equal(bits(v[idx_d].cpu().numpy()), bits(sv))
         assert np.array_equal(out[idx_d].cpu().numpy().view(np.uint16), f32_to_bf16_bits(sp))
     assert zopt.read_adam_state(state)["step"] == 2
+
+
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
+def test_rescale_step_bitwise_and_close_to_direct(zopt, gdtype):
+    """zopt_adamw_rescale_step (DeepSpeed PR #9021 adam_rescale_step): bit for bit the oracle's
+    re-targeting; a rescale to the same scale changes nothing; the result is the step taken
+    directly on the new scale up to rounding (the page measures 7.5e-6 of the update)."""
+    case = Case(zopt, SMALL, 4000, 3, 1, seed=21, gdtype=gdtype)
+    for s in range(2):
+        case.step(s, H, max_norm=1e9)  # warm moments, coefficient 1
+    grads = workloads.flat_grads(SMALL, 21, 2, dtype=gdtype)
+    g = case.shard([x.float().numpy() for x in grads])
+    g_dev = torch.from_numpy(g).cuda().to(gdtype)
+    before = [t.clone() for t in (case.p, case.m, case.v)]
+    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, clip_stats=None,
+                    adam_state=case.state)  # speculative step t = 3 on the unscaled gradient
+    spec = [t.clone() for t in (case.p, case.m, case.v)]
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, old_scale=1.0,
+                            new_scale=1.0, adam_state=case.state)
+    torch.cuda.synchronize()
+    for a, b in zip(spec, (case.p, case.m, case.v)):
+        assert torch.equal(a, b)
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, old_scale=1.0,
+                            new_scale=0.37, adam_state=case.state)
+    torch.cuda.synchronize()
+    ref = [t.cpu().numpy() for t in spec]
+    OA.rescale_step_f32(*ref, g, 1.0, 0.37, H, 3)
+    for r, t in zip(ref, (case.p, case.m, case.v)):
+        assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))
+    assert np.array_equal(case.out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(ref[0]))
+    # against the step taken directly on the new scale
+    direct = [t.cpu().numpy() for t in before]
+    mask = OL.decay_mask_of_shard(case.decay, case.numel, case.bucket, case.world, case.rank)
+    OA.step_flat_f32(*direct, g, mask, np.float32(0.37), H, 3)
+    upd = np.max(np.abs(direct[0] - before[0].cpu().numpy()))
+    # 1e-4 of the update, plus the two roundings of weights near 1 (the RMSNorm scales)
+    assert np.all(np.abs(direct[0] - ref[0]) <= 1e-4 * upd + 2 * np.spacing(np.abs(direct[0])))
+    assert zopt.read_adam_state(case.state)["step"] == 3
+
+
+def test_rescale_to_the_clip_coefficient(zopt):
+    case = Case(zopt, SMALL, 4000, 1, 0, seed=22, gdtype=torch.bfloat16)
+    case.step(0, H, max_norm=1e9)
+    grads = workloads.flat_grads(SMALL, 22, 1)
+    g = case.shard([x.float().numpy() for x in grads])
+    g_dev = torch.from_numpy(g).cuda().bfloat16()
+    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, clip_stats=None,
+                    adam_state=case.state)
+    spec = [t.cpu().numpy() for t in (case.p, case.m, case.v)]
+    zopt.grad_norm_clip(g_dev, 0.01, case.ws, case.clip)  # the final clip, computed afterwards
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, None, lr=H.lr, old_scale=1.0,
+                            clip_stats=case.clip, adam_state=case.state)
+    torch.cuda.synchronize()
+    coef = zopt.read_clip_stats(case.clip)["clip_coef"]
+    assert coef < 1
+    OA.rescale_step_f32(*spec, g, 1.0, float(coef), H, 2)
+    for r, t in zip(spec, (case.p, case.m, case.v)):
+        assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))

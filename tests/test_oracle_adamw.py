@@ -188,3 +188,56 @@ def test_scalars_are_fp64_rounded_once():
     assert sc.step_size == np.float32(1e-3 / (1.0 - 0.9))
     assert sc.bc2_sqrt == np.float32(math.sqrt(1.0 - 0.95))
     assert sc.decay == np.float32(1.0 - 1e-4)
+
+
+def _warm(rng, n, t):
+    p = rng.normal(0, 0.02, n)
+    m = np.zeros(n)
+    v = np.zeros(n)
+    for s in range(1, t):
+        OA.adamw_tensor_f64(p, m, v, rng.normal(0, 1e-3, n), 1.0, True, H, s)
+    return p, m, v
+
+
+def test_rescale_equals_direct_step_in_fp64():
+    """DeepSpeed PR #9021: the rescaled state is the state of the step taken directly on the new
+    scale (here in fp64, up to fp64 rounding)."""
+    rng = np.random.default_rng(11)
+    for t in (1, 5):
+        p, m, v = _warm(rng, 2000, t)
+        g = rng.normal(0, 1e-3, 2000)
+        a = [x.copy() for x in (p, m, v)]
+        b = [x.copy() for x in (p, m, v)]
+        OA.adamw_tensor_f64(*a, g, 1.0, True, H, t)           # speculative step on the old scale
+        OA.rescale_step_f64(*a, g, 1.0, 0.3, H, t)            # re-targeted to 0.3
+        OA.adamw_tensor_f64(*b, g, 0.3, True, H, t)           # the step taken directly on 0.3
+        upd = np.max(np.abs(b[0] - p))
+        assert np.max(np.abs(a[0] - b[0])) < 1e-9 * upd
+        assert np.max(np.abs(a[1] - b[1])) < 1e-12 * np.max(np.abs(b[1]))
+        assert np.max(np.abs(a[2] - b[2])) < 1e-9 * np.max(np.abs(b[2]))
+
+
+def test_rescale_f32_close_to_direct_and_same_scale_is_bitwise():
+    rng = np.random.default_rng(12)
+    p64, m64, v64 = _warm(rng, 4096, 4)
+    p, m, v = (x.astype(np.float32) for x in (p64, m64, v64))
+    g = rng.normal(0, 1e-3, 4096).astype(np.float32)
+    a = [x.copy() for x in (p, m, v)]
+    b = [x.copy() for x in (p, m, v)]
+    OA.adamw_tensor_f32(*a, g, np.float32(1), True, OA.scalars_f32(H, 4))
+    c = [x.copy() for x in a]
+    OA.rescale_step_f32(*c, g, 1.0, 1.0, H, 4)  # to the same scale: moments bit for bit, p too
+    for x, y in zip(a, c):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    OA.rescale_step_f32(*a, g, 1.0, 0.5, H, 4)
+    OA.adamw_tensor_f32(*b, g, np.float32(0.5), True, OA.scalars_f32(H, 4))
+    upd = np.max(np.abs(b[0] - p))
+    assert np.max(np.abs(a[0] - b[0])) < 1e-4 * upd  # the page measures 7.5e-6 of the update
+    assert np.max(np.abs(a[1] - b[1])) < 1e-6 * np.max(np.abs(b[1]))
+
+
+def test_rescale_keeps_nan_in_v():
+    p, m, v = (np.ones(4, np.float32) for _ in range(3))
+    v[1] = np.nan
+    OA.rescale_step_f32(p, m, v, np.ones(4, np.float32), 1.0, 0.0, H, 3)
+    assert np.isnan(v[1]) and np.all(v[[0, 2, 3]] >= 0)

@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_norm_clip_noalloc": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, vp]),
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
+        "zopt_adamw_rescale_step": (ctypes.c_int, [vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
+                                                   ctypes.c_float, ctypes.c_float, vp, vp, vp]),
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
         "zopt_ns_workspace": (sz, [i64, i64, i32, ctypes.c_int]),
         "zopt_muon_workspace": (sz, [i64, i64, i32]),
@@ -255,6 +257,18 @@ def grad_norm_clip_noalloc(grad, max_norm: float, stats, n: int | None = None, s
     n = grad.numel() if n is None else int(n)
     _check(lib().zopt_grad_norm_clip_noalloc(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(stats),
                                              _stream(stream)))
+
+
+def adamw_rescale_step(layout: ShardLayout, master, exp_avg, exp_avg_sq, grad, out_bf16, *, lr: float,
+                       old_scale: float, new_scale: float = 1.0, beta1: float = 0.9, beta2: float = 0.95,
+                       eps: float = 1e-8, weight_decay: float = 0.1, clip_stats=None, adam_state=None,
+                       stream=None) -> None:
+    """``zopt_adamw_rescale_step``: turn the last step on g*old_scale into the step on
+    g*new_scale (or on the clip coefficient in ``clip_stats``)."""
+    hp = _Hparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), 1, 0)
+    _check(lib().zopt_adamw_rescale_step(layout.handle, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(grad),
+                                         _dtype_code(grad), _ptr(out_bf16), ctypes.byref(hp), float(old_scale),
+                                         float(new_scale), _ptr(clip_stats), _ptr(adam_state), _stream(stream)))
 
 
 ACC_FIRST, ACC_LAST = 1, 2
