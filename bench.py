@@ -205,10 +205,10 @@ def run_reference(args, rank: int) -> None:
 class NsPart:
     """The Newton-Schulz stress set: bf16 matrices of three shapes, one batched call per shape."""
 
-    def __init__(self, Z, torch, seed: int, steps: int, count_limit: int = 0):
+    def __init__(self, Z, torch, seed: int, steps: int, count_limit: int = 0, which: str = "c5"):
         import workloads
         self.Z, self.steps = Z, steps
-        w = workloads.get("c5")
+        w = workloads.get(which)
         shapes = []
         for prm in w.muon:
             if prm.shape not in shapes:
@@ -220,7 +220,10 @@ class NsPart:
             if count_limit > 0:
                 count = min(count, count_limit)
             G = torch.randn(count, r, c, device="cuda", generator=gen)
-            G /= torch.linalg.vector_norm(G, dim=(1, 2), keepdim=True)  # Frobenius-normalised
+            if which == "c5":
+                G /= torch.linalg.vector_norm(G, dim=(1, 2), keepdim=True)  # Frobenius-normalised
+            else:
+                G *= 1e-3  # gradient-like scale
             G = G.to(torch.bfloat16)
             self.groups.append((G, torch.empty_like(G)))
         # room for a whole shape group, so each product of a step is one launch over the group
@@ -274,7 +277,8 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip_stats=clip,
                   adam_state=state)
     # ---- part 2: Newton-Schulz over the stress set (whole matrices owned by this rank)
-    ns = NsPart(Z, torch, 5000 + rank, 5, args.ns_count) if "ns" in parts else None
+    ns = NsPart(Z, torch, 5000 + rank, 5, args.ns_count, "c5" if args.ns_set == "stress" else "c2") \
+        if "ns" in parts else None
 
     K = args.steps
     ev_a = [(mk(), mk()) for _ in range(K)]   # accumulation + clip + AdamW part
@@ -445,6 +449,8 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parts", default="adamw,ns", help="comma list of step parts: adamw, ns")
+    ap.add_argument("--ns-set", default="stress", choices=["stress", "gpt2"],
+                    help="Newton-Schulz matrices: the 48-matrix 4096-wide stress set, or the GPT-2-small body's 48")
     ap.add_argument("--ns-count", type=int, default=0,
                     help="matrices per Newton-Schulz shape (profiling captures); 0 = the full set of 16")
     ap.add_argument("--shard-len", type=int, default=0,

@@ -421,43 +421,109 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 __device__ __forceinline__ void to_out(float v, __nv_bfloat16* p) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void to_out(float v, float* p) { *p = v; }
 
-// X0_b = G_b / (||G_b||_F + eps) in the compute dtype U, oriented so that X0 is m x n with
-// m <= n (blockIdx.y = matrix). 32 x 32 tiles, transposed through shared memory when needed.
+__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load2(const __nv_bfloat16* p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+__device__ __forceinline__ void store2(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
+__device__ __forceinline__ void store2(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+__device__ __forceinline__ void store8(float* p, const float (&x)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&x)[8]) {
+  __nv_bfloat162 h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+  *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(h);
+}
+
+__device__ __forceinline__ float inv_norm(const zopt_clip_stats* st, double eps) {
+  return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(__dsqrt_rn(st->sumsq), eps)));
+}
+
+// X0_b = G_b / (||G_b||_F + eps) in the compute dtype U, same orientation (rows <= cols),
+// blockIdx.y = matrix. vec: rows of G are 16-byte aligned with cols % 8 == 0, so each thread
+// moves 8 elements per access; otherwise one element at a time.
 template <typename T, typename U>
-__global__ void group_scale_orient_kernel(const T* __restrict__ g0, long long rows, long long cols, long long ld,
-                                          long long batch_stride, int transpose, const zopt_clip_stats* stats,
-                                          double eps, U* __restrict__ x0, long long ldx, long long x_stride) {
+__global__ void __launch_bounds__(256) group_scale_kernel(const T* __restrict__ g0, long long rows, long long cols,
+                                                          long long ld, long long batch_stride, int vec,
+                                                          const zopt_clip_stats* stats, double eps,
+                                                          U* __restrict__ x0, long long ldx, long long x_stride) {
   __shared__ float s_inv;
-  __shared__ float tile[32][33];
   const int mb = blockIdx.y;
   const T* g = g0 + mb * batch_stride;
   U* x = x0 + mb * x_stride;
-  if (threadIdx.x == 0 && threadIdx.y == 0) {
-    const double nrm = __dsqrt_rn(stats[mb].sumsq);
-    s_inv = __double2float_rn(__ddiv_rn(1.0, __dadd_rn(nrm, eps)));
-  }
+  if (threadIdx.x == 0) s_inv = inv_norm(stats + mb, eps);
   __syncthreads();
   const float inv = s_inv;
-  const long long tiles_c = (cols + 31) / 32, tiles_r = (rows + 31) / 32;
-  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
-    if (!transpose) {
-      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
-        const long long r = r0 + yy, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) to_out(to_f32(g[r * ld + c]) * inv, x + r * ldx + c);
+  if (vec) {
+    const long long c8 = cols / 8;
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+      for (long long c = threadIdx.x; c < c8; c += blockDim.x) {
+        float v[8];
+        load8(g + r * ld + 8 * c, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] *= inv;
+        store8(x + r * ldx + 8 * c, v);
       }
-    } else {
-      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
-        const long long r = r0 + yy, c = c0 + threadIdx.x;
-        tile[yy][threadIdx.x] = (r < rows && c < cols) ? to_f32(g[r * ld + c]) * inv : 0.0f;
-      }
-      __syncthreads();
-      for (int yy = threadIdx.y; yy < 32; yy += blockDim.y) {
-        const long long xr = c0 + yy, xc = r0 + threadIdx.x;  // X0[c][r] = G[r][c]
-        if (xr < cols && xc < rows) to_out(tile[threadIdx.x][yy], x + xr * ldx + xc);
-      }
-      __syncthreads();
     }
+  } else {
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x)
+      for (long long c = threadIdx.x; c < cols; c += blockDim.x) to_out(to_f32(g[r * ld + c]) * inv, x + r * ldx + c);
+  }
+}
+
+// X0_b = (G_b / (||G_b||_F + eps))' for a tall G (rows > cols): 64 x 64 tiles through shared
+// memory, 32 x 8 threads; pair: G's rows allow 2-element accesses (each warp then reads and
+// writes 128 contiguous bytes of bf16).
+template <typename T, typename U>
+__global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restrict__ g0, long long rows, long long cols,
+                                                              long long ld, long long batch_stride, int pair,
+                                                              const zopt_clip_stats* stats, double eps,
+                                                              U* __restrict__ x0, long long ldx, long long x_stride) {
+  __shared__ float s_inv;
+  __shared__ float tile[64][65];
+  const int mb = blockIdx.y;
+  const T* g = g0 + mb * batch_stride;
+  U* x = x0 + mb * x_stride;
+  if (threadIdx.x == 0 && threadIdx.y == 0) s_inv = inv_norm(stats + mb, eps);
+  __syncthreads();
+  const float inv = s_inv;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const long long tiles_c = (cols + 63) / 64, tiles_r = (rows + 63) / 64;
+  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
+    const long long r0 = (tt / tiles_c) * 64, c0 = (tt % tiles_c) * 64;
+    const bool full = r0 + 64 <= rows && c0 + 64 <= cols;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int rr = ty + 8 * k;
+      const long long r = r0 + rr, c = c0 + 2 * tx;
+      if (full && pair) {
+        const float2 v = load2(g + r * ld + c);
+        tile[rr][2 * tx] = v.x * inv;
+        tile[rr][2 * tx + 1] = v.y * inv;
+      } else {
+        tile[rr][2 * tx] = (r < rows && c < cols) ? to_f32(g[r * ld + c]) * inv : 0.0f;
+        tile[rr][2 * tx + 1] = (r < rows && c + 1 < cols) ? to_f32(g[r * ld + c + 1]) * inv : 0.0f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int cc = ty + 8 * k;                    // X0 row = G column c0 + cc
+      const long long xr = c0 + cc, xc = r0 + 2 * tx;  // X0[c][r] = G[r][c]
+      if (full) {
+        store2(x + xr * ldx + xc, tile[2 * tx][cc], tile[2 * tx + 1][cc]);
+      } else {
+        if (xr < cols && xc < rows) to_out(tile[2 * tx][cc], x + xr * ldx + xc);
+        if (xr < cols && xc + 1 < rows) to_out(tile[2 * tx + 1][cc], x + xr * ldx + xc + 1);
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -676,27 +742,34 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
                                                                     cols, ld_g, batch_stride_g, flat, vec_rows, ws,
                                                                     stats);
     ZOPT_CUDA_TRY(cudaGetLastError());
-    const dim3 tb(32, 8);
     int sblk = (sms * 8 + gs - 1) / gs;
     sblk = sblk < 1 ? 1 : sblk;
     const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
-    const int tr = transpose ? 1 : 0;
-    if (io_dtype == ZOPT_F32 && f32c)
-      group_scale_orient_kernel<float, float><<<sgrid, tb, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols,
-                                                                    ld_g, batch_stride_g, tr, stats, eps,
-                                                                    reinterpret_cast<float*>(xb[0]), p.ldx, mat_elems);
-    else if (io_dtype == ZOPT_F32)
-      group_scale_orient_kernel<float, __nv_bfloat16><<<sgrid, tb, 0, s>>>(
-          reinterpret_cast<const float*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
-          reinterpret_cast<__nv_bfloat16*>(xb[0]), p.ldx, mat_elems);
-    else if (f32c)
-      group_scale_orient_kernel<__nv_bfloat16, float><<<sgrid, tb, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
-          reinterpret_cast<float*>(xb[0]), p.ldx, mat_elems);
-    else
-      group_scale_orient_kernel<__nv_bfloat16, __nv_bfloat16><<<sgrid, tb, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(g), rows, cols, ld_g, batch_stride_g, tr, stats, eps,
-          reinterpret_cast<__nv_bfloat16*>(xb[0]), p.ldx, mat_elems);
+    if (!transpose) {
+      const int vec = (aligned && (ld_g * esz) % 16 == 0 && cols % 8 == 0) ? 1 : 0;
+#define ZOPT_SCALE(TI, TO)                                                                                \
+  group_scale_kernel<TI, TO><<<sgrid, 256, 0, s>>>(reinterpret_cast<const TI*>(g), rows, cols, ld_g,     \
+                                                   batch_stride_g, vec, stats, eps, reinterpret_cast<TO*>(xb[0]), \
+                                                   p.ldx, mat_elems)
+      if (io_dtype == ZOPT_F32 && f32c) ZOPT_SCALE(float, float);
+      else if (io_dtype == ZOPT_F32) ZOPT_SCALE(float, __nv_bfloat16);
+      else if (f32c) ZOPT_SCALE(__nv_bfloat16, float);
+      else ZOPT_SCALE(__nv_bfloat16, __nv_bfloat16);
+#undef ZOPT_SCALE
+    } else {
+      const int pair = ((reinterpret_cast<uintptr_t>(g) % (2 * esz)) == 0 && ld_g % 2 == 0 &&
+                        batch_stride_g % 2 == 0) ? 1 : 0;
+      const dim3 tb(32, 8);
+#define ZOPT_TRANSPOSE(TI, TO)                                                                              \
+  group_transpose_kernel<TI, TO><<<sgrid, tb, 0, s>>>(reinterpret_cast<const TI*>(g), rows, cols, ld_g,     \
+                                                      batch_stride_g, pair, stats, eps,                     \
+                                                      reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
+      if (io_dtype == ZOPT_F32 && f32c) ZOPT_TRANSPOSE(float, float);
+      else if (io_dtype == ZOPT_F32) ZOPT_TRANSPOSE(float, __nv_bfloat16);
+      else if (f32c) ZOPT_TRANSPOSE(__nv_bfloat16, float);
+      else ZOPT_TRANSPOSE(__nv_bfloat16, __nv_bfloat16);
+#undef ZOPT_TRANSPOSE
+    }
     ZOPT_CUDA_TRY(cudaGetLastError());
 
     const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
