@@ -51,7 +51,9 @@ def gaussian(rows, cols, seed, dtype=torch.bfloat16):
 
 
 SHAPES_WB = [(256, 1024), (1024, 256), (300, 300), (200, 333), (130, 70), (1, 64), (64, 1), (17, 100), (768, 2304),
-             (384, 640)]
+             (384, 640),
+             # m >= 1024: the CTA-pair kernel (256 x 256 tiles), whole and ragged
+             (1024, 1536), (1100, 1300), (2000, 1030), (1024, 1024)]
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES_WB)
@@ -117,7 +119,7 @@ def test_grouped_batch_equals_single_calls(zopt, compute):
     """A workspace for 2 matrices runs a batch of 5 as groups of 2, 2, 1: every product is one
     launch over the group. Each result is bitwise the single-matrix call's."""
     code = zopt.BF16 if compute == "bf16" else zopt.F32
-    rows, cols, batch = 700, 300, 5  # tall: processed transposed
+    rows, cols, batch = 700, 300, 5  # tall: processed transposed (single-CTA products)
     G = torch.randn(batch, rows, cols, device="cuda").to(torch.bfloat16)
     X = torch.empty_like(G)
     ws2 = zopt.new_ns_workspace(rows, cols, group=2, compute=code)
@@ -131,6 +133,22 @@ def test_grouped_batch_equals_single_calls(zopt, compute):
         assert torch.equal(one, X[b]), b
         ref = newton_schulz(G[b].double().cpu().numpy(), steps=5)
         assert rel(X[b].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
+def test_grouped_batch_pair_kernel(zopt):
+    """The same for m >= 1024 (CTA-pair products): 3 matrices of 1100 x 1300 in groups of 2."""
+    rows, cols, batch = 1100, 1300, 3
+    G = torch.randn(batch, rows, cols, device="cuda").to(torch.bfloat16)
+    X = torch.empty_like(G)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols, group=2), steps=5)
+    ws1 = zopt.new_ns_workspace(rows, cols)
+    for b in range(batch):
+        one = torch.empty(rows, cols, device="cuda", dtype=torch.bfloat16)
+        zopt.ns_orthogonalize(G[b], one, ws1, steps=5)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X[b]), b
+    ref = newton_schulz(G[1].double().cpu().numpy(), steps=5)
+    assert rel(X[1].cpu(), torch.from_numpy(ref)) <= 2e-2
 
 
 def test_deterministic(zopt):

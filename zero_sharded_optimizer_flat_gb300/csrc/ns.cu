@@ -15,6 +15,8 @@
 //                        caller's orientation and dtype)
 // Operands and the products A, B, X are bf16; every product accumulates in fp32 in TMEM.
 //
+// Products with m >= 1024 run on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles, see
+// gemm_bf16_pair_kernel); smaller ones on single CTAs as follows.
 // One kernel does all three products: a persistent, warp-specialised tcgen05 GEMM. Warp 0
 // streams 128x64 and 256x64 bf16 tiles into a 4-stage shared-memory ring with TMA (128-byte
 // swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
@@ -357,6 +359,206 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------- CTA-pair GEMM
+//
+// The same three products with tcgen05.mma.cta_group::2: a cluster of two CTAs on two SMs
+// computes a 256 x 256 tile, each CTA holding its 128 rows of the A-operand and its 128
+// columns of the B-operand, so a CTA streams 32 KiB per 64-deep k-block instead of 48 and the
+// ring holds 6 stages. Both CTAs' TMA loads complete on the leader's (rank 0) stage barrier;
+// the leader's single thread issues the M=256 MMAs, whose commits reach both CTAs; each CTA
+// drains its own 128 TMEM lanes; the epilogue warps of both CTAs release an accumulator on the
+// leader's barrier.
+constexpr int BM2 = 256, STAGES2 = 6;
+constexpr int kHalf = 128 * BK * 2;  // 16 KiB: 128 rows (or columns) of a 64-deep k-block
+constexpr int kSmemBytes2 = STAGES2 * 2 * kHalf + 1024 + 256;
+
+__device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, int& tp, int& tj) {
+  mb = t / a.tiles_per_mat;
+  t -= mb * a.tiles_per_mat;
+  if (!a.symmetric) {
+    tp = t % a.tiles_m;
+    tj = t / a.tiles_m;
+    return;
+  }
+  int r = 0;  // 256 x 256 tiles: row r holds tiles tj = r .. tiles_n - 1
+  for (;;) {
+    const int cnt = a.tiles_n - r;
+    if (t < cnt) {
+      tp = r;
+      tj = r + t;
+      return;
+    }
+    t -= cnt;
+    ++r;
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+                          const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES2 * kHalf;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES2 * kHalf);
+  uint64_t* empty = full + STAGES2;
+  uint64_t* tfull = empty + STAGES2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < STAGES2; ++q) {
+      tc::mbar_init(full + q, 1);
+      tc::mbar_init(empty + q, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tfull + b, 1);
+      tc::mbar_init(tempty + b, 256);  // the epilogue threads of both CTAs (used in the leader)
+    }
+    tc::mbar_init(drain, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmP);
+    tc::prefetch_tmap(&tmQ);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(tslot, kTmemCols);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync();  // the peer's barriers exist before anyone arrives on them
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const int nk = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      int s = 0;
+      uint32_t ph = 0;
+      int armed[STAGES2];
+      for (int q = 0; q < STAGES2; ++q) armed[q] = -1;
+      bool ok = true;
+      for (int t = pair; ok && t < a.num_tiles; t += npairs) {
+        int mb, tp, tj;
+        tile_coords2(a, t, mb, tp, tj);
+        const int row0 = tp * BM2 + static_cast<int>(rank) * 128;  // this CTA's A rows
+        const int col0 = tj * BN + static_cast<int>(rank) * 128;    // this CTA's B columns
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(empty + s, ph ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          if (leader) tc::mbar_arrive_expect_tx(full + s, 4 * kHalf);  // both CTAs' A and B halves
+          armed[s] = static_cast<int>(ph);
+          const uint32_t bar = tc::map_to_rank(tc::smem_u32(full + s), 0);
+          tc::tma_load_3d_pair(sA + s * kHalf, &tmP, bar, kb * BK, row0, mb);
+          if (!a.b_mn_major) {
+            tc::tma_load_3d_pair(sB + s * kHalf, &tmQ, bar, kb * BK, col0, mb);
+          } else {
+            tc::tma_load_3d_pair(sB + s * kHalf, &tmQ, bar, col0, kb * BK, mb);
+            tc::tma_load_3d_pair(sB + s * kHalf + kBoxMN, &tmQ, bar, col0 + 64, kb * BK, mb);
+          }
+          if (++s == STAGES2) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {  // the leader's stage barriers count both CTAs' copies
+        for (int q = 0; q < STAGES2; ++q)
+          if (armed[q] >= 0) mbar_wait_drain(full + q, static_cast<uint32_t>(armed[q]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA issuer (leader)
+      const uint32_t idesc = tc::idesc_bf16_f32(BM2, BN, false, a.b_mn_major != 0);
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < a.num_tiles; t += npairs, ++it) {
+        const int b = it & 1;
+        const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!tc::mbar_wait(tempty + b, tph ^ 1u, a.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(full + s, ph, a.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t abase = tc::smem_u32(sA + s * kHalf);
+          const uint32_t bbase = tc::smem_u32(sB + s * kHalf);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(abase + 32u * kk, 16u, 1024u);
+            const uint64_t bd = a.b_mn_major ? tc::smem_desc_sw128(bbase + 2048u * kk, kBoxMN, 1024u)
+                                             : tc::smem_desc_sw128(bbase + 32u * kk, 16u, 1024u);
+            tc::umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc::umma_commit_pair(empty + s, 3);  // both CTAs' stage s is free
+          if (++s == STAGES2) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit_pair(tfull + b, 3);  // both CTAs' accumulator b is complete
+      }
+      tc::umma_commit_pair(drain, 1);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int quad = warp & 3;
+    const int row = 32 * quad + lane;
+    const uint32_t tempty_leader[2] = {tc::map_to_rank(tc::smem_u32(tempty), 0),
+                                       tc::map_to_rank(tc::smem_u32(tempty + 1), 0)};
+    int it = 0;
+    for (int t = pair; t < a.num_tiles; t += npairs, ++it) {
+      const int b = it & 1;
+      const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc::fence_after_sync();
+      int mb, tp, tj;
+      tile_coords2(a, t, mb, tp, tj);
+      GemmArgs am = a;
+      am.R = a.R + mb * a.r_stride;
+      am.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
+      const int i = tp * BM2 + static_cast<int>(rank) * 128 + row;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 32 * c), v);
+        tc::tmem_wait_ld();
+        if (c == BN / 32 - 1) {
+          tc::fence_before_sync();
+          tc::mbar_arrive_cluster(tempty_leader[b]);
+        }
+        epilogue32(am, i, tj * BN + 32 * c, v);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync();  // every MMA, copy and remote arrival of the pair is done
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------- prep kernels
 
 // Per-matrix reduction scratch: an arrival counter and up to kPrepBlocks fp64 partials.
@@ -611,6 +813,35 @@ Plan plan(long long rows, long long cols, long long es, long long group) {
   return p;
 }
 
+// The CTA-pair kernel for products with at least 256 rows: P is read with 128-row boxes, Q
+// with 128-row (K-major) or 64 x 64 (MN-major) boxes.
+zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    ZOPT_CUDA_TRY(
+        cudaFuncSetAttribute(gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2));
+    attr_set = true;
+  }
+  a.tiles_m = static_cast<int>((a.M + BM2 - 1) / BM2);
+  a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+  long long per = 0;
+  if (a.symmetric) {
+    for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r;
+  } else {
+    per = static_cast<long long>(a.tiles_m) * a.tiles_n;
+  }
+  const long long total = per * a.group;
+  if (total < 1 || total > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+  a.tiles_per_mat = static_cast<int>(per);
+  a.num_tiles = static_cast<int>(total);
+  const int sms = sm_count();
+  if (sms < 2) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
+  const int pairs = a.num_tiles < sms / 2 ? a.num_tiles : sms / 2;
+  gemm_bf16_pair_kernel<<<2 * pairs, kGemmThreads, kSmemBytes2, stream>>>(P, Q, a);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -773,6 +1004,9 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     ZOPT_CUDA_TRY(cudaGetLastError());
 
     const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
+    // products with m >= 1024 run on CTA pairs; below that the single-CTA kernel's twice as
+    // many tiles keep more SMs busy
+    const bool pair = m >= 1024;
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
       const bool last = it == steps - 1;
@@ -805,19 +1039,22 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.M = m; ga.N = m; ga.K = n;
         ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
         ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-        if ((st = launch_gemm(mx_p[cur], mx_q[cur], ga, s)) != ZOPT_OK) return st;
+        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], ga, s) : launch_gemm(mx_p[cur], mx_q[cur], ga, s)) !=
+            ZOPT_OK)
+          return st;
         // B = c A A' + b A
         ga.K = m;
         ga.alpha = abc[2]; ga.beta = abc[1];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
         ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-        if ((st = launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
+        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, ga, s) : launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
         // X = B X + a X
         ga.M = m; ga.N = n; ga.K = m;
         ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(xb[cur]); ga.ldr = p.ldx; ga.r_stride = mat_elems;
         ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
-        if ((st = launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK) return st;
+        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], ga, s) : launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK)
+          return st;
       }
       cur ^= 1;
     }
