@@ -317,6 +317,9 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     torch.cuda.synchronize()
     t0, t1 = mk(), mk()
     with Clocks(smi_id(local_rank)) as clk:
+        # every launch of the timed steps is queued behind a device-side delay, so the events
+        # time GPU execution only, not the host's enqueue rate (dmuon PR #16's timing method)
+        torch.cuda._sleep(int(args.prequeue_ms * 2.0e6))
         t0.record(stream)
         for i in range(K):
             step(i)
@@ -448,6 +451,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prequeue-ms", type=float, default=50.0,
+                    help="device-side delay (about this many ms at 2 GHz) queued before the timed steps")
     ap.add_argument("--parts", default="adamw,ns", help="comma list of step parts: adamw, ns")
     ap.add_argument("--ns-set", default="stress", choices=["stress", "gpt2"],
                     help="Newton-Schulz matrices: the 48-matrix 4096-wide stress set, or the GPT-2-small body's 48")

@@ -31,6 +31,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <utility>
 
 #include "internal.h"
 #include "norm_impl.cuh"
@@ -238,6 +239,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   const int nk = (a.K + BK - 1) / BK;
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();  // the previous product's outputs are complete and visible
 
   if (warp == 0) {
     if (lane == 0) {
@@ -434,6 +437,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   const int nk = (a.K + BK - 1) / BK;
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();  // the previous product's outputs are complete and visible
 
   if (warp == 0) {
     if (lane == 0) {
@@ -577,6 +582,8 @@ __global__ void __launch_bounds__(kNormThreads)
     group_sumsq_kernel(const T* __restrict__ g0, long long rows, long long cols, long long ld,
                        long long batch_stride, int flat, int vec_rows, uint8_t* ws_base,
                        zopt_clip_stats* stats) {
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();
   const int mb = blockIdx.y;
   const T* g = g0 + mb * batch_stride;
   double acc = 0.0;
@@ -656,6 +663,8 @@ __global__ void __launch_bounds__(256) group_scale_kernel(const T* __restrict__ 
                                                           const zopt_clip_stats* stats, double eps,
                                                           U* __restrict__ x0, long long ldx, long long x_stride) {
   __shared__ float s_inv;
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();
   const int mb = blockIdx.y;
   const T* g = g0 + mb * batch_stride;
   U* x = x0 + mb * x_stride;
@@ -689,6 +698,8 @@ __global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restric
                                                               U* __restrict__ x0, long long ldx, long long x_stride) {
   __shared__ float s_inv;
   __shared__ float tile[64][65];
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();
   const int mb = blockIdx.y;
   const T* g = g0 + mb * batch_stride;
   U* x = x0 + mb * x_stride;
@@ -813,6 +824,26 @@ Plan plan(long long rows, long long cols, long long es, long long group) {
   return p;
 }
 
+// Launches `kernel` on `stream` with programmatic stream serialisation: it may start while
+// the previous kernel finishes (every kernel here waits with griddepcontrol.wait before it
+// touches global memory).
+template <typename... KArgs, typename... Args>
+zopt_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ZOPT_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+  return ok();
+}
+
 // The CTA-pair kernel for products with at least 256 rows: P is read with 128-row boxes, Q
 // with 128-row (K-major) or 64 x 64 (MN-major) boxes.
 zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
@@ -837,9 +868,7 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArg
   const int sms = sm_count();
   if (sms < 2) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int pairs = a.num_tiles < sms / 2 ? a.num_tiles : sms / 2;
-  gemm_bf16_pair_kernel<<<2 * pairs, kGemmThreads, kSmemBytes2, stream>>>(P, Q, a);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  return ok();
+  return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(kGemmThreads), kSmemBytes2, stream, P, Q, a);
 }
 
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
@@ -863,9 +892,7 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, 
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-  gemm_bf16_kernel<<<grid, kGemmThreads, kSmemBytes, stream>>>(P, Q, a);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  return ok();
+  return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes, stream, P, Q, a);
 }
 
 }  // namespace ns
@@ -965,23 +992,25 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     long long bpm = (rows * cols + 32767) / 32768;
     bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
     const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
-    if (io_dtype == ZOPT_F32)
-      group_sumsq_kernel<float><<<sg, kNormThreads, 0, s>>>(reinterpret_cast<const float*>(g), rows, cols, ld_g,
-                                                            batch_stride_g, flat, vec_rows, ws, stats);
-    else
-      group_sumsq_kernel<__nv_bfloat16><<<sg, kNormThreads, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(g), rows,
-                                                                    cols, ld_g, batch_stride_g, flat, vec_rows, ws,
-                                                                    stats);
-    ZOPT_CUDA_TRY(cudaGetLastError());
+    st = io_dtype == ZOPT_F32
+             ? launch_pdl(group_sumsq_kernel<float>, sg, dim3(kNormThreads), 0, s, reinterpret_cast<const float*>(g),
+                          static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g),
+                          static_cast<long long>(batch_stride_g), flat, vec_rows, ws, stats)
+             : launch_pdl(group_sumsq_kernel<__nv_bfloat16>, sg, dim3(kNormThreads), 0, s,
+                          reinterpret_cast<const __nv_bfloat16*>(g), static_cast<long long>(rows),
+                          static_cast<long long>(cols), static_cast<long long>(ld_g),
+                          static_cast<long long>(batch_stride_g), flat, vec_rows, ws, stats);
+    if (st != ZOPT_OK) return st;
     int sblk = (sms * 8 + gs - 1) / gs;
     sblk = sblk < 1 ? 1 : sblk;
     const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
     if (!transpose) {
       const int vec = (aligned && (ld_g * esz) % 16 == 0 && cols % 8 == 0) ? 1 : 0;
-#define ZOPT_SCALE(TI, TO)                                                                                \
-  group_scale_kernel<TI, TO><<<sgrid, 256, 0, s>>>(reinterpret_cast<const TI*>(g), rows, cols, ld_g,     \
-                                                   batch_stride_g, vec, stats, eps, reinterpret_cast<TO*>(xb[0]), \
-                                                   p.ldx, mat_elems)
+#define ZOPT_SCALE(TI, TO)                                                                               \
+  st = launch_pdl(group_scale_kernel<TI, TO>, sgrid, dim3(256), 0, s, reinterpret_cast<const TI*>(g),    \
+                  static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g), \
+                  static_cast<long long>(batch_stride_g), vec, static_cast<const zopt_clip_stats*>(stats),  \
+                  static_cast<double>(eps), reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
       if (io_dtype == ZOPT_F32 && f32c) ZOPT_SCALE(float, float);
       else if (io_dtype == ZOPT_F32) ZOPT_SCALE(float, __nv_bfloat16);
       else if (f32c) ZOPT_SCALE(__nv_bfloat16, float);
@@ -991,16 +1020,18 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
       const int pair = ((reinterpret_cast<uintptr_t>(g) % (2 * esz)) == 0 && ld_g % 2 == 0 &&
                         batch_stride_g % 2 == 0) ? 1 : 0;
       const dim3 tb(32, 8);
-#define ZOPT_TRANSPOSE(TI, TO)                                                                              \
-  group_transpose_kernel<TI, TO><<<sgrid, tb, 0, s>>>(reinterpret_cast<const TI*>(g), rows, cols, ld_g,     \
-                                                      batch_stride_g, pair, stats, eps,                     \
-                                                      reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
+#define ZOPT_TRANSPOSE(TI, TO)                                                                            \
+  st = launch_pdl(group_transpose_kernel<TI, TO>, sgrid, tb, 0, s, reinterpret_cast<const TI*>(g),        \
+                  static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g), \
+                  static_cast<long long>(batch_stride_g), pair, static_cast<const zopt_clip_stats*>(stats), \
+                  static_cast<double>(eps), reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
       if (io_dtype == ZOPT_F32 && f32c) ZOPT_TRANSPOSE(float, float);
       else if (io_dtype == ZOPT_F32) ZOPT_TRANSPOSE(float, __nv_bfloat16);
       else if (f32c) ZOPT_TRANSPOSE(__nv_bfloat16, float);
       else ZOPT_TRANSPOSE(__nv_bfloat16, __nv_bfloat16);
 #undef ZOPT_TRANSPOSE
     }
+    if (st != ZOPT_OK) return st;
     ZOPT_CUDA_TRY(cudaGetLastError());
 
     const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);

@@ -23,6 +23,13 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Let the next kernel of the stream launch now (its CTAs take SMs as this grid's CTAs exit).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the previous kernel of the stream has completed and its writes are visible (a
+// no-op for a launch without the programmatic-serialisation attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
