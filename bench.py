@@ -338,39 +338,86 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
 
     # ---- end to end through the public API with host buffers: each part copies its inputs
     # (the micro-step gradients; the Newton-Schulz inputs) from pinned host memory and reads
-    # its results back (the clip stats; the orthogonalised matrices), timed per part
+    # its results back (the clip stats; the orthogonalised matrices). The copies run on two
+    # copy streams, overlapped with the compute of the previous micro-step or matrix group;
+    # each part is timed from its first copy to its last read-back.
     h2d = d2h = 0
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
     if "adamw" in parts:
         micro_host = [mg.cpu().pin_memory() for mg in micro]
         stats_host = torch.empty(Z.CLIP_STATS_BYTES, dtype=torch.uint8).pin_memory()
         h2d += 2 * S * MICRO_STEPS
         d2h += Z.CLIP_STATS_BYTES
+        acc_done = [ev() for _ in micro]
+        for e in acc_done:
+            e.record(stream)
     if ns is not None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
         d2h += sum(X.numel() * 2 for _, X in ns.groups)
+        # chunks of up to 4 matrices, the square group last (its read-back is the shortest)
+        order = sorted(range(len(ns.groups)), key=lambda gi: ns.groups[gi][0].shape[1] == ns.groups[gi][0].shape[2])
+        chunks = []
+        for gi in order:
+            G, X = ns.groups[gi]
+            hG, hX = ns_host[gi]
+            for lo in range(0, G.shape[0], 4):
+                hi = min(G.shape[0], lo + 4)
+                chunks.append((G[lo:hi], X[lo:hi], hG[lo:hi], hX[lo:hi]))
+        ns_done = [ev() for _ in chunks]
+        out_done = [ev() for _ in chunks]
+        for e in ns_done + out_done:
+            e.record(stream)
     e2e_steps = max(2, min(K, 5))
     ee_a = [(mk(), mk()) for _ in range(e2e_steps)]
     ee_n = [(mk(), mk()) for _ in range(e2e_steps)]
 
     def e2e_step(i=None):
         if "adamw" in parts:
-            if i is not None:
-                ee_a[i][0].record(stream)
-            for mg, mh in zip(micro, micro_host):
-                mg.copy_(mh, non_blocking=True)
-            adamw_part()
+            start = mk() if i is None else ee_a[i][0]
+            start.record(stream)
+            h2d_s.wait_event(start)
+            landed = []
+            for k, (mg, mh) in enumerate(zip(micro, micro_host)):
+                h2d_s.wait_event(acc_done[k])  # the previous step has read this buffer
+                with torch.cuda.stream(h2d_s):
+                    mg.copy_(mh, non_blocking=True)
+                e = ev()
+                e.record(h2d_s)
+                landed.append(e)
+            for k, mg in enumerate(micro):
+                stream.wait_event(landed[k])
+                Z.grad_accumulate(g, mg, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
+                                  stats=clip, stream=stream)
+                acc_done[k].record(stream)
+            Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
             stats_host.copy_(clip, non_blocking=True)
             if i is not None:
                 ee_a[i][1].record(stream)
         if ns is not None:
-            if i is not None:
-                ee_n[i][0].record(stream)
-            for (G, _), (hG, _) in zip(ns.groups, ns_host):
-                G.copy_(hG, non_blocking=True)
-            ns.run(stream)
-            for (_, X), (_, hX) in zip(ns.groups, ns_host):
-                hX.copy_(X, non_blocking=True)
+            start = mk() if i is None else ee_n[i][0]
+            start.record(stream)
+            h2d_s.wait_event(start)
+            landed = []
+            for ci, (G, X, hG, hX) in enumerate(chunks):
+                h2d_s.wait_event(ns_done[ci])  # the previous step has read G
+                with torch.cuda.stream(h2d_s):
+                    G.copy_(hG, non_blocking=True)
+                e = ev()
+                e.record(h2d_s)
+                landed.append(e)
+            for ci, (G, X, hG, hX) in enumerate(chunks):
+                stream.wait_event(landed[ci])
+                stream.wait_event(out_done[ci])  # the previous step's X has been read back
+                Z.ns_orthogonalize(G, X, ns.ws, steps=ns.steps, stream=stream)
+                ns_done[ci].record(stream)
+                d2h_s.wait_event(ns_done[ci])
+                with torch.cuda.stream(d2h_s):
+                    hX.copy_(X, non_blocking=True)
+                out_done[ci].record(d2h_s)
+            for e in out_done:
+                stream.wait_event(e)
             if i is not None:
                 ee_n[i][1].record(stream)
 
