@@ -47,7 +47,9 @@ constexpr int kTileB = BN * BK * 2;          // 32 KiB
 constexpr int kBoxMN = 64 * BK * 2;          // one 64 (MN) x 64 (K) box of an MN-major operand
 constexpr int kGemmThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTmemCols = 2 * BN;            // two fp32 accumulators of 128 x 256
-constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256;
+constexpr int kStageWarp = 32 * 33;  // floats: one epilogue warp's 32 x 32 transpose tile (padded)
+constexpr int kStageBytes = 4 * kStageWarp * 4;
+constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256 + kStageBytes;
 
 struct GemmArgs {
   int M, N, K;
@@ -142,14 +144,16 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, int i, int j0, co
   }
 }
 
-// Epilogue of 32 accumulator columns [j0, j0+32) of row i.
-__device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, const uint32_t (&v)[32]) {
-  if (i >= a.M) return;
+// Epilogue of 32 accumulator columns [j0, j0+32) of row i; the warp's 32 lanes hold rows
+// i0 .. i0+31 (i0 = i - lane). `stage` is this warp's 32 x 33 fp32 shared-memory tile.
+__device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, const uint32_t (&v)[32], float* stage,
+                                           int lane) {
+  const int i0 = i - lane;
   float o[32];
 #pragma unroll
   for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
   const bool full = j0 + 32 <= a.N;
-  if (a.beta != 0.0f) {
+  if (a.beta != 0.0f && i < a.M) {
     const __nv_bfloat16* r = a.R + static_cast<long long>(i) * a.ldr + j0;
     if (full && (reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
 #pragma unroll
@@ -169,6 +173,7 @@ __device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, con
     }
   }
   if (!a.symmetric) {
+    if (i >= a.M) return;
     if (!a.d_trans) {
       if (full) {
         store_row32(a, i, j0, o);
@@ -185,19 +190,43 @@ __device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, con
     return;
   }
   // symmetric: upper part (j >= i) written in place, strictly upper part mirrored to (j, i)
-  if (full && j0 >= i) {
-    store_row32(a, i, j0, o);
-  } else {
+  if (i < a.M) {
+    if (full && j0 >= i) {
+      store_row32(a, i, j0, o);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        if (j < a.N && j >= i) store1(a, static_cast<long long>(i) * a.ldd + j, o[k]);
+      }
+    }
+  }
+  // The mirror of a whole 32 x 32 block above the diagonal goes through shared memory: lane L
+  // writes row j0 + L of the transposed block as four 16-byte stores. (Warp-uniform test.)
+  const bool staged = full && j0 >= i0 + 32 && i0 + 32 <= a.M && !a.d_f32 && (a.ldd & 7) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.D) & 15u) == 0;
+  if (staged) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = o[k];
+    __syncwarp();
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.D) + static_cast<long long>(j0 + lane) * a.ldd + i0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float x[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) x[t] = stage[(8 * q + t) * 33 + lane];
+      __nv_bfloat162 h[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) h[t] = __floats2bfloat162_rn(x[2 * t], x[2 * t + 1]);
+      reinterpret_cast<uint4*>(dst)[q] = *reinterpret_cast<const uint4*>(h);
+    }
+    __syncwarp();
+  } else if (i < a.M) {
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       const int j = j0 + k;
-      if (j < a.N && j >= i) store1(a, static_cast<long long>(i) * a.ldd + j, o[k]);
+      if (j < a.N && j > i) store1(a, static_cast<long long>(j) * a.ldd + i, o[k]);
     }
-  }
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int j = j0 + k;
-    if (j < a.N && j > i) store1(a, static_cast<long long>(j) * a.ldd + i, o[k]);
   }
 }
 
@@ -214,6 +243,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -350,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc::fence_before_sync();
           tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
         }
-        epilogue32(am, i, tj * BN + 32 * c, v);
+        epilogue32(am, i, tj * BN + 32 * c, v, stage_base + (warp - 2) * kStageWarp, lane);
       }
     }
   }
@@ -373,7 +403,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // leader's barrier.
 constexpr int BM2 = 256, STAGES2 = 6;
 constexpr int kHalf = 128 * BK * 2;  // 16 KiB: 128 rows (or columns) of a 64-deep k-block
-constexpr int kSmemBytes2 = STAGES2 * 2 * kHalf + 1024 + 256;
+constexpr int kSmemBytes2 = STAGES2 * 2 * kHalf + 1024 + 256 + kStageBytes;
 
 __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, int& tp, int& tj) {
   mb = t / a.tiles_per_mat;
@@ -409,6 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_rank();
@@ -552,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           tc::fence_before_sync();
           tc::mbar_arrive_cluster(tempty_leader[b]);
         }
-        epilogue32(am, i, tj * BN + 32 * c, v);
+        epilogue32(am, i, tj * BN + 32 * c, v, stage_base + (warp - 2) * kStageWarp, lane);
       }
     }
   }
