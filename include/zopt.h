@@ -264,6 +264,18 @@ ZOPT_API zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io
                                            int32_t steps, const float* abc, float eps, void* d_ws, size_t ws_bytes,
                                            zopt_stream stream);
 
+/* Device-side failure reporting. Every wait of the tensor-core kernels is bounded (4 s);
+ * one that runs out records an error word in mapped host memory, drains the kernel's copies
+ * and MMAs, frees its TMEM and returns, so the context stays usable; the next
+ * zopt_ns_orthogonalize / zopt_muon_step then returns ZOPT_ETIMEOUT.
+ * zopt_take_device_error returns the error word (0 = none, -1 if it cannot be set up) and
+ * clears it, without synchronising (read it after the work it covers has completed).
+ * zopt_selftest_wait_timeout launches one thread that waits, limited to limit_ns (at most
+ * 2 s), on an mbarrier phase that nothing completes: the same bounded-wait code, run out on
+ * purpose, so a test can check the reporting path. */
+ZOPT_API int32_t zopt_take_device_error(void);
+ZOPT_API zopt_status zopt_selftest_wait_timeout(int64_t limit_ns, zopt_stream stream);
+
 /* ======================================================================================
  * 5. Muon's update around Newton-Schulz (matrices owned whole by this rank)
  *

@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
         "zopt_ns_workspace": (sz, [i64, i64, i32, ctypes.c_int]),
         "zopt_muon_workspace": (sz, [i64, i64, i32]),
+        "zopt_take_device_error": (i32, []),
+        "zopt_selftest_wait_timeout": (ctypes.c_int, [i64, vp]),
         "zopt_muon_step": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, vp, i64, i64, i32, ctypes.POINTER(_MuonHparams),
                                           vp, vp, sz, vp]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
@@ -370,3 +372,13 @@ def muon_step(master, momentum, grad, out_bf16, ws, stats, *, lr: float, momentu
                       float(eps), float(guard))
     _check(lib().zopt_muon_step(_ptr(master), _ptr(momentum), _ptr(grad), _dtype_code(grad), _ptr(out_bf16), rows,
                                 cols, batch, ctypes.byref(hp), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def take_device_error() -> int:
+    """The device error word (1 = a bounded wait ran out), cleared by the read."""
+    return int(lib().zopt_take_device_error())
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait path on a barrier nothing completes (limit_ns <= 2 s)."""
+    _check(lib().zopt_selftest_wait_timeout(int(limit_ns), _stream(stream)))

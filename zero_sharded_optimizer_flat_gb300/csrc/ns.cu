@@ -807,7 +807,7 @@ zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long lon
 }
 
 // Error word written by timed-out kernels: mapped pinned host memory, so the next call can
-// read it without synchronising the device.
+// read it without synchronising the device. Shared by every kernel with bounded waits.
 zopt_status error_word(int** host, int** dev) {
   static int* h = nullptr;
   static int* d = nullptr;
@@ -1122,4 +1122,44 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     }
   }
   return ok();
+}
+
+namespace zopt {
+namespace ns {
+namespace {
+// One thread waits, with the given limit, for an mbarrier phase that nothing completes: the
+// bounded-wait path of the tensor-core kernels, run on purpose.
+__global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    tc::mbar_wait_for(&bar, 0, err, limit_ns);
+  }
+}
+}  // namespace
+}  // namespace ns
+}  // namespace zopt
+
+extern "C" zopt_status zopt_selftest_wait_timeout(int64_t limit_ns, zopt_stream stream) {
+  using namespace zopt;
+  if (limit_ns < 1 || limit_ns > 2000000000LL)
+    return fail(ZOPT_EINVAL, "zopt_selftest_wait_timeout: limit must lie in (0, 2 s]");
+  int* h = nullptr;
+  int* d = nullptr;
+  zopt_status st = ns::error_word(&h, &d);
+  if (st != ZOPT_OK) return st;
+  ns::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      d, static_cast<unsigned long long>(limit_ns));
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+extern "C" int32_t zopt_take_device_error(void) {
+  int* h = nullptr;
+  int* d = nullptr;
+  if (zopt::ns::error_word(&h, &d) != ZOPT_OK) return -1;
+  const int v = *reinterpret_cast<volatile int*>(h);
+  *reinterpret_cast<volatile int*>(h) = 0;
+  return v;
 }
