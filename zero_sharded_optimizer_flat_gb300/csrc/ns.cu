@@ -1020,7 +1020,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     const int vec_rows = (aligned && (ld_g * esz) % 16 == 0) ? 1 : 0;
     // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
     // is bitwise the same whatever group it runs in
-    long long bpm = (rows * cols + 32767) / 32768;
+    long long bpm = (rows * cols + 8191) / 8192;  // short per-thread chains for small matrices
     bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
     const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
     st = io_dtype == ZOPT_F32

@@ -56,14 +56,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete. Gives up (returning false) when
 // another thread has already reported an error, or after `limit_ns` of polling; then records
 // error code 1 in the error word.
+// The error word lives in host memory, a microsecond away: it is only read once a wait has
+// already lasted a millisecond, so waits that end normally never touch it.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((spin & 63u) == 0) {
-      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-      if (globaltimer() - t0 > limit_ns) {
+      const unsigned long long el = globaltimer() - t0;
+      if (el > 1000000ull && *reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (el > limit_ns) {
         atomicExch(err, 1);
         return false;
       }
