@@ -51,6 +51,18 @@ constexpr int kStageWarp = 32 * 33;  // floats: one epilogue warp's 32 x 32 tran
 constexpr int kStageBytes = 4 * kStageWarp * 4;
 constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256 + kStageBytes;
 
+// The single-CTA kernel's TMA epilogue: each epilogue warp owns the 32 x 256 slice of the tile
+// that its TMEM lanes hold, as four 64-column boxes of 32 rows (128-byte rows, 128-byte
+// swizzle) into which R is prefetched while the tile's MMAs run and over which D is written
+// for the TMA to store; the mirrored blocks of a symmetric product go through two 32 x 32
+// boxes (64-byte rows, 64-byte swizzle). The ring keeps three stages to make room.
+constexpr int kTmaStages = 3;
+constexpr int kEpiBox = 32 * 64 * 2;        // 4 KiB: 32 rows x 64 bf16
+constexpr int kEpiSlice = 4 * kEpiBox;      // one warp's 32 x 256 slice
+constexpr int kMirBox = 32 * 32 * 2;        // 2 KiB: 32 x 32 bf16
+constexpr int kSmemBytesTma = kTmaStages * (kTileA + kTileB) + 4 * kEpiSlice + 4 * 2 * kMirBox + 1024 + 256;
+static_assert(kSmemBytesTma <= 232448, "shared memory of the TMA-epilogue kernel");
+
 struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles;
@@ -230,24 +242,65 @@ __device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, con
   }
 }
 
+// ---------------------------------------------------------------------- TMA epilogue
+//
+// Byte offset, in a 32 x 64 bf16 box of 128-byte rows under the TMA's 128-byte swizzle (the box
+// 1024-byte aligned), of the 16-byte piece p (columns 8p .. 8p + 7) of row r.
+__device__ __forceinline__ uint32_t epi_piece(int r, int p) {
+  return static_cast<uint32_t>(r * 128 + ((p ^ (r & 7)) << 4));
+}
+
+// Whether the epilogue warp whose rows start at i0 handles the 64-column box at column jg: it
+// lies inside the matrix and, for a symmetric product, is not wholly below the diagonal.
+__device__ __forceinline__ bool epi_box_live(const GemmArgs& a, int i0, int jg) {
+  return i0 < a.M && jg < a.N && !(a.symmetric && jg + 63 < i0);
+}
+
+// Lane 0 of epilogue warp `quad`: the R boxes of tile t that the warp reads, into its slice, on
+// bar. Returns whether any load was issued.
+__device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap* tmR, uint8_t* slice, uint64_t* bar,
+                                           int t, int quad) {
+  int mb, ti, tj;
+  tile_coords(a, t, mb, ti, tj);
+  const int i0 = ti * BM + 32 * quad;
+  int n = 0;
+  for (int g = 0; g < 4; ++g) n += epi_box_live(a, i0, tj * BN + 64 * g) ? 1 : 0;
+  if (n == 0) return false;
+  tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * kEpiBox));
+  for (int g = 0; g < 4; ++g)
+    if (epi_box_live(a, i0, tj * BN + 64 * g))
+      tc::tma_load_3d(slice + g * kEpiBox, tmR, bar, tj * BN + 64 * g, i0, mb);
+  return true;
+}
+
+// The single-CTA persistent GEMM. kTma selects the epilogue: through shared memory and the TMA
+// (R prefetched, D and its mirror stored as boxes; D a bf16 row-major matrix that tmD and tmM
+// describe) or through registers and plain stores (any D: fp32, transposed, unaligned). tmR,
+// tmD and tmM are unused without kTma.
+template <bool kTma>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                     const GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ CUtensorMap tmM, const GemmArgs a) {
+  constexpr int S = kTma ? kTmaStages : STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * kTileA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kTileB);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint8_t* sB = smem + S * kTileA;
+  uint8_t* sEpi = sB + S * kTileB;                    // TMA epilogue: four warps' slices
+  uint8_t* sMir = sEpi + (kTma ? 4 * kEpiSlice : 0);  // TMA epilogue: two mirror boxes per warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sMir + (kTma ? 4 * 2 * kMirBox : 0));
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rbar = drain + 1;  // TMA epilogue: one R barrier per epilogue warp
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(rbar + 4);
   float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       tc::mbar_init(full + s, 1);
       tc::mbar_init(empty + s, 1);
     }
@@ -256,9 +309,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(tempty + b, 128);
     }
     tc::mbar_init(drain, 1);
+    if (kTma)
+      for (int q = 0; q < 4; ++q) tc::mbar_init(rbar + q, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmP);
     tc::prefetch_tmap(&tmQ);
+    if (kTma) {
+      if (a.beta != 0.0f) tc::prefetch_tmap(&tmR);
+      tc::prefetch_tmap(&tmD);
+      if (a.symmetric) tc::prefetch_tmap(&tmM);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tslot, kTmemCols);
@@ -277,8 +337,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------------------------------------------------------- TMA producer
       int s = 0;
       uint32_t ph = 0;
-      int armed[STAGES];
-      for (int q = 0; q < STAGES; ++q) armed[q] = -1;
+      int armed[S];
+      for (int q = 0; q < S; ++q) armed[q] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
         int mb, ti, tj;
@@ -298,14 +358,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int q = 0; q < BN / 64; ++q)
               tc::tma_load_3d(sB + s * kTileB + q * kBoxMN, &tmQ, full + s, tj * BN + 64 * q, kb * BK, mb);
           }
-          if (++s == STAGES) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok) {  // leave no copy in flight: wait (bounded) for every stage armed last
-        for (int q = 0; q < STAGES; ++q)
+        for (int q = 0; q < S; ++q)
           if (armed[q] >= 0) mbar_wait_drain(full + q, static_cast<uint32_t>(armed[q]));
       }
     }
@@ -341,7 +401,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc::umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc::umma_commit(empty + s);  // the stage is free once these MMAs have read it
-          if (++s == STAGES) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
@@ -352,6 +412,136 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::umma_commit(drain);  // no MMA may still be running when TMEM is released
       mbar_wait_drain(drain, 0);
     }
+  } else if constexpr (kTma) {
+    // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
+    const int quad = warp & 3;  // this warp may read TMEM lanes [32 quad, 32 quad + 32)
+    uint8_t* slice = sEpi + quad * kEpiSlice;
+    uint8_t* mir = sMir + quad * 2 * kMirBox;
+    uint64_t* rb = rbar + quad;
+    const bool has_r = a.beta != 0.0f;
+    bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
+    uint32_t rph = 0;
+    int t = blockIdx.x;
+    if (has_r && t < a.num_tiles) {
+      int l = 0;
+      if (lane == 0) l = epi_load_r(a, &tmR, slice, rb, t, quad) ? 1 : 0;
+      rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+    }
+    for (int it = 0; t < a.num_tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      if (rpend) {  // every lane waits, so that each sees the TMA's writes
+        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, a.err) ? 1 : 0)) break;
+        rph ^= 1u;
+        rpend = false;
+      }
+      tc::fence_after_sync();
+      int mb, ti, tj;
+      tile_coords(a, t, mb, ti, tj);
+      const int i0 = ti * BM + 32 * quad;
+      const int i = i0 + lane;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        const int jg = tj * BN + 64 * g;
+        if (!epi_box_live(a, i0, jg)) continue;
+        // a symmetric product's box on or above the diagonal (every j >= every i) goes out
+        // whole; one across it is written element by element
+        const bool whole = !a.symmetric || jg >= i0 + 31;
+        uint32_t v[32], w[32];
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 64 * g);
+        tc::tmem_ld32(taddr, v);
+        tc::tmem_ld32(taddr + 32, w);
+        tc::tmem_wait_ld();
+        float o[64];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          o[k] = a.alpha * __uint_as_float(v[k]);
+          o[32 + k] = a.alpha * __uint_as_float(w[k]);
+        }
+        uint8_t* box = slice + g * kEpiBox;
+        if (has_r) {
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const uint4 u = *reinterpret_cast<const uint4*>(box + epi_piece(lane, p));
+            const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              o[8 * p + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
+              o[8 * p + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
+            }
+          }
+        }
+        if (whole) {
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            __nv_bfloat162 h[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(o[8 * p + 2 * q], o[8 * p + 2 * q + 1]);
+            *reinterpret_cast<uint4*>(box + epi_piece(lane, p)) = *reinterpret_cast<const uint4*>(h);
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_3d(&tmD, box, jg, i0, mb);
+            tc::bulk_commit();
+          }
+          if (a.symmetric) {
+            // the transposed 64 x 32 block, as two 32 x 32 boxes: row k of box c holds column
+            // jg + 32c + k; lanes pair up so that each writes two neighbouring bf16 of one row
+            if (lane == 0) tc::bulk_wait_read<1>();  // the previous mirror boxes have been read
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk) {
+                const float mine_even = o[32 * c + 2 * kk], mine_odd = o[32 * c + 2 * kk + 1];
+                const float other = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? mine_even : mine_odd, 1);
+                const __nv_bfloat162 h = (lane & 1) ? __floats2bfloat162_rn(other, mine_odd)
+                                                    : __floats2bfloat162_rn(mine_even, other);
+                const int r = 2 * kk + (lane & 1);
+                const uint32_t off = static_cast<uint32_t>(r * 64 + (((lane >> 3) ^ (kk & 3)) << 4) + (lane & 6) * 2);
+                *reinterpret_cast<__nv_bfloat162*>(mir + c * kMirBox + off) = h;
+              }
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              for (int c = 0; c < 2; ++c)
+                if (jg + 32 * c < a.N) tc::tma_store_3d(&tmM, mir + c * kMirBox, i0, jg + 32 * c, mb);
+              tc::bulk_commit();
+            }
+          }
+        } else if (i < a.M) {
+          __nv_bfloat16* Dm = static_cast<__nv_bfloat16*>(a.D) + mb * a.d_stride;
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const int j = jg + k;
+            if (j < a.N && j >= i) Dm[static_cast<long long>(i) * a.ldd + j] = __float2bfloat16_rn(o[k]);
+            if (j < a.N && j > i) Dm[static_cast<long long>(j) * a.ldd + i] = __float2bfloat16_rn(o[k]);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
+      // the slice is free once the TMA has read it: then prefetch the next tile's R
+      if (lane == 0) tc::bulk_wait_read<0>();
+      __syncwarp();
+      const int tn = t + static_cast<int>(gridDim.x);
+      if (has_r && tn < a.num_tiles) {
+        int l = 0;
+        if (lane == 0) l = epi_load_r(a, &tmR, slice, rb, tn, quad) ? 1 : 0;
+        rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+      }
+    }
+    if (lane == 0) {
+      tc::bulk_wait_all();                  // every store has reached global memory
+      if (rpend) mbar_wait_drain(rb, rph);  // (after a failed wait) no load left in flight
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     const int quad = warp & 3;  // this warp may read TMEM lanes [32 quad, 32 quad + 32)
@@ -788,9 +978,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // A 3-D bf16 tensor map over `group` row-major [outer][inner] matrices with `pitch` elements
-// per row, `mat_bytes` apart; boxes of box_inner x box_outer x 1.
+// per row, `mat_bytes` apart; boxes of box_inner x box_outer x 1 under the given swizzle.
 zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long pitch,
-                     long long group, long long mat_bytes, int box_inner, int box_outer) {
+                     long long group, long long mat_bytes, int box_inner, int box_outer,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
@@ -799,7 +990,7 @@ zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long lon
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled failed (" + std::to_string(r) + ")");
@@ -902,10 +1093,16 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArg
   return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(kGemmThreads), kSmemBytes2, stream, P, Q, a);
 }
 
-zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
+// The single-CTA kernel; with tma, R (if beta != 0) is read through R and D is stored through
+// D (64 x 32 boxes, 128-byte swizzle) and, for a symmetric product, M (32 x 32, 64-byte swizzle).
+zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
+                        const CUtensorMap* M, bool tma, GemmArgs a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    ZOPT_CUDA_TRY(
+        cudaFuncSetAttribute(gemm_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    ZOPT_CUDA_TRY(
+        cudaFuncSetAttribute(gemm_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesTma));
     attr_set = true;
   }
   a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
@@ -923,7 +1120,11 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, 
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-  return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes, stream, P, Q, a);
+  if (!tma) return launch_pdl(gemm_bf16_kernel<false>, dim3(grid), dim3(kGemmThreads), kSmemBytes, stream, P, Q, P, P, P, a);
+  if (D == nullptr || (a.beta != 0.0f && R == nullptr) || (a.symmetric && M == nullptr) || a.d_f32 || a.d_trans)
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
+  return launch_pdl(gemm_bf16_kernel<true>, dim3(grid), dim3(kGemmThreads), kSmemBytesTma, stream, P, Q,
+                    R != nullptr ? *R : P, *D, M != nullptr ? *M : P, a);
 }
 
 }  // namespace ns
@@ -993,16 +1194,23 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
 
   // Tensor maps over the group's workspace matrices (bf16 tensor-core path only).
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
+  // the single-CTA kernel's epilogue boxes: R and D as 64 x 32 boxes, mirrors as 32 x 32
+  CUtensorMap mx_e[2], ma_e, mb_e, ma_m, mb_m;
   if (!f32c) {
     const long long mb = static_cast<long long>(p.per_mat);
     for (int q = 0; q < 2; ++q) {
       if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BM)) != ZOPT_OK) return st;
       if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BN)) != ZOPT_OK) return st;
       if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BK)) != ZOPT_OK) return st;
+      if ((st = make_map(&mx_e[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, 32)) != ZOPT_OK) return st;
     }
     if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
     if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, group, mb, 64, BN)) != ZOPT_OK) return st;
     if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&ma_e, A, p.m, p.m, p.lda, group, mb, 64, 32)) != ZOPT_OK) return st;
+    if ((st = make_map(&mb_e, B, p.m, p.m, p.lda, group, mb, 64, 32)) != ZOPT_OK) return st;
+    if ((st = make_map(&ma_m, A, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+    if ((st = make_map(&mb_m, B, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
   }
 
   const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
@@ -1069,6 +1277,16 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     // products with m >= 1024 run on CTA pairs; below that the single-CTA kernel's twice as
     // many tiles keep more SMs busy
     const bool pair = m >= 1024;
+    // the last product writes the caller's X through the TMA when it is a bf16 row-major
+    // matrix the TMA can address
+    CUtensorMap mo_e;
+    const bool out_tma = !f32c && !pair && io_dtype == ZOPT_BF16 && !transpose &&
+                         (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 && ld_x % 8 == 0 &&
+                         (gs == 1 || (batch_stride_x * 2) % 16 == 0);
+    if (out_tma) {
+      const long long ob = gs == 1 ? p.m * ld_x * 2 : batch_stride_x * 2;
+      if ((st = make_map(&mo_e, xo, p.n, p.m, ld_x, gs, ob, 64, 32)) != ZOPT_OK) return st;
+    }
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
       const bool last = it == steps - 1;
@@ -1101,21 +1319,26 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.M = m; ga.N = m; ga.K = n;
         ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
         ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], ga, s) : launch_gemm(mx_p[cur], mx_q[cur], ga, s)) !=
-            ZOPT_OK)
+        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], ga, s)
+                       : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, &ma_m, true, ga, s)) != ZOPT_OK)
           return st;
         // B = c A A' + b A
         ga.K = m;
         ga.alpha = abc[2]; ga.beta = abc[1];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
         ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, ga, s) : launch_gemm(ma_p, ma_q, ga, s)) != ZOPT_OK) return st;
+        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, ga, s)
+                       : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, &mb_m, true, ga, s)) != ZOPT_OK)
+          return st;
         // X = B X + a X
         ga.M = m; ga.N = n; ga.K = m;
         ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(xb[cur]); ga.ldr = p.ldx; ga.r_stride = mat_elems;
         ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
-        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], ga, s) : launch_gemm(mb_p, mx_mn[cur], ga, s)) != ZOPT_OK)
+        const bool x_tma = !last || out_tma;
+        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], ga, s)
+                       : launch_gemm(mb_p, mx_mn[cur], &mx_e[cur], last ? &mo_e : &mx_e[cur ^ 1], nullptr, x_tma, ga,
+                                     s)) != ZOPT_OK)
           return st;
       }
       cur ^= 1;
