@@ -238,7 +238,8 @@ ZOPT_API zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* m
  * transpose (m = min(rows, cols) <= n) and transposed back on output. Per step:
  * A = X X' (m x m), B = b A + c A A', X = a X + B X. With compute_dtype ZOPT_BF16 the
  * operands and the products A, B, X are bf16 (round-to-nearest-even) with fp32 accumulation
- * on the tensor cores. (a, b, c) = abc[0..2] (the pages print no triple; the usual quintic
+ * on the tensor cores, and the last two are formed as B' = B + a I and X = B' X (the same
+ * map; B' is rounded to bf16 once). ZOPT_F32 computes the products as written. (a, b, c) = abc[0..2] (the pages print no triple; the usual quintic
  * Muon choice is 3.4445, -4.7750, 2.0315).
  * ====================================================================================== */
 

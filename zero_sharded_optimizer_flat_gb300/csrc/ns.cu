@@ -8,22 +8,25 @@
 //   A = X X'            (symmetric: only 128x256 tiles touching the upper triangle are
 //                        computed, each writes its upper part directly and its strictly upper
 //                        part mirrored)
-//   B = c A A' + b A    (A is symmetric, so A^2 = A A': the same symmetric kernel, with the
-//                        b*A term added in the epilogue)
-//   X = B X + a X       (plain GEMM whose B-operand X is read MN-major straight from its
-//                        row-major layout; the last step writes the caller's output, in the
-//                        caller's orientation and dtype)
-// Operands and the products A, B, X are bf16; every product accumulates in fp32 in TMEM.
+//   B' = c A A' + b A + a I
+//                       (A is symmetric, so A^2 = A A': the same symmetric kernel, with the
+//                        b*A term and a on the diagonal added in the epilogue)
+//   X = B' X            (= aX + BX: the step's aX term rides on B's diagonal, so the largest
+//                        product has no second input to read; a plain GEMM whose B-operand X
+//                        is read MN-major straight from its row-major layout; the last step
+//                        writes the caller's output, in the caller's orientation and dtype)
+// Operands and the products A, B', X are bf16; every product accumulates in fp32 in TMEM.
 //
 // Products with m >= 1024 run on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles, see
 // gemm_bf16_pair_kernel); smaller ones on single CTAs as follows.
 // One kernel does all three products: a persistent, warp-specialised tcgen05 GEMM. Warp 0
-// streams 128x64 and 256x64 bf16 tiles into a 4-stage shared-memory ring with TMA (128-byte
-// swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
+// streams 128x64 and 256x64 bf16 tiles into a shared-memory ring with TMA (128-byte swizzle);
+// one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
 // accumulators (2 x 256 fp32 columns), committing stage release and accumulator-ready events
-// to mbarriers; warps 2-5 drain the other accumulator (tcgen05.ld), apply alpha*acc +
-// beta*R and store bf16/fp32 while the next tile is being multiplied. Every mbarrier wait is
-// bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
+// to mbarriers; warps 2-5 drain the other accumulator (tcgen05.ld), apply alpha*acc + beta*R
+// (+ the diagonal term) and hand 32 x 32 bf16 boxes to the TMA while the next tile is being
+// multiplied. Every mbarrier wait is bounded; a timeout sets an error word that the next call
+// reports as ZOPT_ETIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,17 +54,21 @@ constexpr int kStageWarp = 32 * 33;  // floats: one epilogue warp's 32 x 32 tran
 constexpr int kStageBytes = 4 * kStageWarp * 4;
 constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256 + kStageBytes;
 
-// The single-CTA kernel's TMA epilogue: each epilogue warp owns the 32 x 256 slice of the tile
-// that its TMEM lanes hold, as four 64-column boxes of 32 rows (128-byte rows, 128-byte
-// swizzle) into which R is prefetched while the tile's MMAs run and over which D is written
-// for the TMA to store; the mirrored blocks of a symmetric product go through two 32 x 32
-// boxes (64-byte rows, 64-byte swizzle). The ring keeps three stages to make room.
-constexpr int kTmaStages = 3;
-constexpr int kEpiBox = 32 * 64 * 2;        // 4 KiB: 32 rows x 64 bf16
-constexpr int kEpiSlice = 4 * kEpiBox;      // one warp's 32 x 256 slice
-constexpr int kMirBox = 32 * 32 * 2;        // 2 KiB: 32 x 32 bf16
-constexpr int kSmemBytesTma = kTmaStages * (kTileA + kTileB) + 4 * kEpiSlice + 4 * 2 * kMirBox + 1024 + 256;
-static_assert(kSmemBytesTma <= 232448, "shared memory of the TMA-epilogue kernel");
+// Epilogues of the single-CTA kernel. kEpiRegs: registers and plain stores (any D). The TMA
+// epilogues move D, and for a symmetric product its mirror, as 32 x 32 bf16 boxes (64-byte rows,
+// 64-byte swizzle) that a warp fills from its 32 TMEM lanes and one lane hands to the TMA:
+// kEpiTma (no R term) keeps the ring's four stages and cycles four boxes per warp; kEpiTmaR
+// prefetches the warp's 32 x 256 slice of R into eight boxes while the tile's MMAs run, writes D
+// over it in place and has two mirror boxes per warp, at the cost of a ring stage.
+constexpr int kEpiRegs = 0, kEpiTmaR = 1, kEpiTma = 2;
+constexpr int kBox = 32 * 32 * 2;  // 2 KiB
+__host__ __device__ constexpr int stages_of(int e) { return e == kEpiTmaR ? 3 : STAGES; }
+__host__ __device__ constexpr int epi_bytes(int e) { return e == kEpiTmaR ? 4 * (8 + 2) * kBox : (e == kEpiTma ? 4 * 4 * kBox : 0); }
+constexpr int smem_bytes(int e) {
+  return stages_of(e) * (kTileA + kTileB) + epi_bytes(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0);
+}
+static_assert(smem_bytes(kEpiTmaR) <= 232448 && smem_bytes(kEpiTma) <= 232448, "shared memory per CTA");
+static_assert(smem_bytes(kEpiRegs) == kSmemBytes, "register-epilogue layout");
 
 struct GemmArgs {
   int M, N, K;
@@ -78,6 +85,7 @@ struct GemmArgs {
   long long ldd;
   int d_f32;
   int d_trans;  // write D[i, j] to D[j * ldd + i]
+  float diag;  // added to D[i, i] (after alpha * acc + beta * R)
   int* err;
 };
 
@@ -184,6 +192,11 @@ __device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, con
         if (j0 + k < a.N) o[k] += a.beta * __bfloat162float(r[k]);
     }
   }
+  if (a.diag != 0.0f && i >= j0 && i < j0 + 32) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (j0 + k == i) o[k] += a.diag;
+  }
   if (!a.symmetric) {
     if (i >= a.M) return;
     if (!a.d_trans) {
@@ -244,57 +257,117 @@ __device__ __forceinline__ void epilogue32(const GemmArgs& a, int i, int j0, con
 
 // ---------------------------------------------------------------------- TMA epilogue
 //
-// Byte offset, in a 32 x 64 bf16 box of 128-byte rows under the TMA's 128-byte swizzle (the box
-// 1024-byte aligned), of the 16-byte piece p (columns 8p .. 8p + 7) of row r.
-__device__ __forceinline__ uint32_t epi_piece(int r, int p) {
-  return static_cast<uint32_t>(r * 128 + ((p ^ (r & 7)) << 4));
+// A 32 x 32 bf16 box as the TMA lays it out under the 64-byte swizzle (box 512-byte aligned):
+// row r at 64 r, its 16-byte piece q (columns 8q .. 8q + 7) at piece q ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint32_t box_piece(int r, int q) {
+  return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
 }
 
-// Whether the epilogue warp whose rows start at i0 handles the 64-column box at column jg: it
-// lies inside the matrix and, for a symmetric product, is not wholly below the diagonal.
-__device__ __forceinline__ bool epi_box_live(const GemmArgs& a, int i0, int jg) {
-  return i0 < a.M && jg < a.N && !(a.symmetric && jg + 63 < i0);
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Lane 0 of epilogue warp `quad`: the R boxes of tile t that the warp reads, into its slice, on
-// bar. Returns whether any load was issued.
+// Row `lane` of the box <- the lane's 32 values, rounded to bf16.
+__device__ __forceinline__ void box_put_row(uint8_t* box, int lane, const float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = bf16x2_bits(o[8 * q + 0], o[8 * q + 1]);
+    u.y = bf16x2_bits(o[8 * q + 2], o[8 * q + 3]);
+    u.z = bf16x2_bits(o[8 * q + 4], o[8 * q + 5]);
+    u.w = bf16x2_bits(o[8 * q + 6], o[8 * q + 7]);
+    *reinterpret_cast<uint4*>(box + box_piece(lane, q)) = u;
+  }
+}
+
+// The warp's 32 x 32 block transposed into the box: lane L's o[k] lands at row k, column L. Lanes
+// pair up so that each writes two neighbouring bf16 of one row (conflict-free).
+__device__ __forceinline__ void box_put_transposed(uint8_t* box, int lane, const float (&o)[32]) {
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? o[2 * kk] : o[2 * kk + 1], 1);
+    const uint32_t w = (lane & 1) ? bf16x2_bits(other, o[2 * kk + 1]) : bf16x2_bits(o[2 * kk], other);
+    const int r = 2 * kk + (lane & 1);
+    const uint32_t off = static_cast<uint32_t>(r * 64 + (((lane >> 3) ^ (kk & 3)) << 4) + (lane & 6) * 2);
+    *reinterpret_cast<uint32_t*>(box + off) = w;
+  }
+}
+
+// Row `lane` of a symmetric diagonal block: the lane's own values on and right of the diagonal,
+// and left of it row `lane` of `tr`, the block transposed by box_put_transposed (whose column c
+// holds row c's value). Written to `box`.
+__device__ __forceinline__ void box_put_symmetric_row(uint8_t* box, const uint8_t* tr, int lane,
+                                                      const float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 t = *reinterpret_cast<const uint4*>(tr + box_piece(lane, q));
+    const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int c = 8 * q + 2 * h;
+      const uint32_t own = bf16x2_bits(o[c], o[c + 1]);
+      const uint32_t lo = (c >= lane ? own : tw[h]) & 0xFFFFu;
+      const uint32_t hi = (c + 1 >= lane ? own : tw[h]) & 0xFFFF0000u;
+      w[h] = lo | hi;
+    }
+    *reinterpret_cast<uint4*>(box + box_piece(lane, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Where the 32 x 32 block at rows i0, columns j0 stands: 0 out of the matrix, 1 written as is
+// (not symmetric), 2 above the diagonal (written and mirrored), 3 on it (its mirror is itself),
+// 4 below it (written by the mirror of the block above). i0 and j0 are multiples of 32.
+__device__ __forceinline__ int block_kind(const GemmArgs& a, int i0, int j0) {
+  if (i0 >= a.M || j0 >= a.N) return 0;
+  if (!a.symmetric) return 1;
+  return j0 > i0 ? 2 : (j0 == i0 ? 3 : 4);
+}
+
+// Lane 0 of epilogue warp `quad` (kEpiTmaR): the R boxes of tile t that the warp reads, into its
+// slice, on bar. Returns whether any load was issued.
 __device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap* tmR, uint8_t* slice, uint64_t* bar,
                                            int t, int quad) {
   int mb, ti, tj;
   tile_coords(a, t, mb, ti, tj);
   const int i0 = ti * BM + 32 * quad;
   int n = 0;
-  for (int g = 0; g < 4; ++g) n += epi_box_live(a, i0, tj * BN + 64 * g) ? 1 : 0;
+  for (int c = 0; c < BN / 32; ++c) {
+    const int k = block_kind(a, i0, tj * BN + 32 * c);
+    n += (k != 0 && k != 4) ? 1 : 0;
+  }
   if (n == 0) return false;
-  tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * kEpiBox));
-  for (int g = 0; g < 4; ++g)
-    if (epi_box_live(a, i0, tj * BN + 64 * g))
-      tc::tma_load_3d(slice + g * kEpiBox, tmR, bar, tj * BN + 64 * g, i0, mb);
+  tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * kBox));
+  for (int c = 0; c < BN / 32; ++c) {
+    const int k = block_kind(a, i0, tj * BN + 32 * c);
+    if (k != 0 && k != 4) tc::tma_load_3d(slice + c * kBox, tmR, bar, tj * BN + 32 * c, i0, mb);
+  }
   return true;
 }
 
-// The single-CTA persistent GEMM. kTma selects the epilogue: through shared memory and the TMA
-// (R prefetched, D and its mirror stored as boxes; D a bf16 row-major matrix that tmD and tmM
-// describe) or through registers and plain stores (any D: fp32, transposed, unaligned). tmR,
-// tmD and tmM are unused without kTma.
-template <bool kTma>
+// The single-CTA persistent GEMM with the epilogue kEpi (kEpiRegs, kEpiTmaR or kEpiTma). The TMA
+// epilogues store D, and a symmetric product's mirror, through tmD (32 x 32 boxes, 64-byte
+// swizzle; D a bf16 row-major matrix the TMA can address); kEpiTmaR reads R through tmR (the same
+// boxes). Unused maps may be any valid map.
+template <int kEpi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmD,
-                     const __grid_constant__ CUtensorMap tmM, const GemmArgs a) {
-  constexpr int S = kTma ? kTmaStages : STAGES;
+                     const GemmArgs a) {
+  constexpr int S = stages_of(kEpi);
+  constexpr bool kTma = kEpi != kEpiRegs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * kTileA;
-  uint8_t* sEpi = sB + S * kTileB;                    // TMA epilogue: four warps' slices
-  uint8_t* sMir = sEpi + (kTma ? 4 * kEpiSlice : 0);  // TMA epilogue: two mirror boxes per warp
-  uint64_t* full = reinterpret_cast<uint64_t*>(sMir + (kTma ? 4 * 2 * kMirBox : 0));
+  uint8_t* sEpi = sB + S * kTileB;  // the TMA epilogue's boxes
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + epi_bytes(kEpi));
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* rbar = drain + 1;  // TMA epilogue: one R barrier per epilogue warp
+  uint64_t* rbar = drain + 1;  // kEpiTmaR: one R barrier per epilogue warp
   uint32_t* tslot = reinterpret_cast<uint32_t*>(rbar + 4);
   float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
@@ -309,16 +382,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(tempty + b, 128);
     }
     tc::mbar_init(drain, 1);
-    if (kTma)
+    if (kEpi == kEpiTmaR)
       for (int q = 0; q < 4; ++q) tc::mbar_init(rbar + q, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmP);
     tc::prefetch_tmap(&tmQ);
-    if (kTma) {
-      if (a.beta != 0.0f) tc::prefetch_tmap(&tmR);
-      tc::prefetch_tmap(&tmD);
-      if (a.symmetric) tc::prefetch_tmap(&tmM);
-    }
+    if (kEpi == kEpiTmaR) tc::prefetch_tmap(&tmR);
+    if (kTma) tc::prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tc::tmem_alloc(tslot, kTmemCols);
@@ -415,16 +485,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if constexpr (kTma) {
     // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
     const int quad = warp & 3;  // this warp may read TMEM lanes [32 quad, 32 quad + 32)
-    uint8_t* slice = sEpi + quad * kEpiSlice;
-    uint8_t* mir = sMir + quad * 2 * kMirBox;
+    // kEpiTmaR: R slice (8 boxes) then 2 mirror boxes; kEpiTma: 4 boxes, a D and a mirror box for
+    // even blocks and another pair for odd ones
+    uint8_t* mine = sEpi + quad * (epi_bytes(kEpi) / 4);
     uint64_t* rb = rbar + quad;
-    const bool has_r = a.beta != 0.0f;
+    const bool has_r = kEpi == kEpiTmaR && a.beta != 0.0f;
     bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
     uint32_t rph = 0;
+    int last_par = -1;   // (warp-uniform) parity of the last block whose boxes went to the TMA
     int t = blockIdx.x;
     if (has_r && t < a.num_tiles) {
       int l = 0;
-      if (lane == 0) l = epi_load_r(a, &tmR, slice, rb, t, quad) ? 1 : 0;
+      if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, t, quad) ? 1 : 0;
       rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
     }
     for (int it = 0; t < a.num_tiles; t += gridDim.x, ++it) {
@@ -442,99 +514,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int mb, ti, tj;
       tile_coords(a, t, mb, ti, tj);
       const int i0 = ti * BM + 32 * quad;
-      const int i = i0 + lane;
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        const int jg = tj * BN + 64 * g;
-        if (!epi_box_live(a, i0, jg)) continue;
-        // a symmetric product's box on or above the diagonal (every j >= every i) goes out
-        // whole; one across it is written element by element
-        const bool whole = !a.symmetric || jg >= i0 + 31;
-        uint32_t v[32], w[32];
-        const uint32_t taddr =
-            tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 64 * g);
-        tc::tmem_ld32(taddr, v);
-        tc::tmem_ld32(taddr + 32, w);
+      for (int c = 0; c < BN / 32; ++c) {
+        const int j0 = tj * BN + 32 * c;
+        const int kind = block_kind(a, i0, j0);
+        if (kind == 0 || kind == 4) continue;
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 32 * c), v);
         tc::tmem_wait_ld();
-        float o[64];
+        float o[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          o[k] = a.alpha * __uint_as_float(v[k]);
-          o[32 + k] = a.alpha * __uint_as_float(w[k]);
-        }
-        uint8_t* box = slice + g * kEpiBox;
+        for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
+        const int par = c & 1;
+        uint8_t* dbox = kEpi == kEpiTmaR ? mine + c * kBox : mine + (2 * par) * kBox;
+        uint8_t* mbox = kEpi == kEpiTmaR ? mine + (8 + par) * kBox : mine + (2 * par + 1) * kBox;
         if (has_r) {
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const uint4 u = *reinterpret_cast<const uint4*>(box + epi_piece(lane, p));
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = *reinterpret_cast<const uint4*>(dbox + box_piece(lane, q));
             const uint32_t x[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              o[8 * p + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
-              o[8 * p + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
+              o[8 * q + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
+              o[8 * q + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
             }
           }
         }
-        if (whole) {
+        if (a.diag != 0.0f && j0 == i0) {
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            __nv_bfloat162 h[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(o[8 * p + 2 * q], o[8 * p + 2 * q + 1]);
-            *reinterpret_cast<uint4*>(box + epi_piece(lane, p)) = *reinterpret_cast<const uint4*>(h);
-          }
-          tc::fence_proxy_async_smem();
+          for (int k = 0; k < 32; ++k)
+            if (k == lane) o[k] += a.diag;
+        }
+        // the boxes of this parity were last handed to the TMA two blocks ago at the latest:
+        // wait until it has read them (all but the newest group if that one is the other parity's)
+        if (lane == 0) {
+          if (last_par == par || last_par < 0)
+            tc::bulk_wait_read<0>();
+          else
+            tc::bulk_wait_read<1>();
+        }
+        __syncwarp();
+        if (kind == 3) {
+          box_put_transposed(mbox, lane, o);
           __syncwarp();
-          if (lane == 0) {
-            tc::tma_store_3d(&tmD, box, jg, i0, mb);
-            tc::bulk_commit();
-          }
-          if (a.symmetric) {
-            // the transposed 64 x 32 block, as two 32 x 32 boxes: row k of box c holds column
-            // jg + 32c + k; lanes pair up so that each writes two neighbouring bf16 of one row
-            if (lane == 0) tc::bulk_wait_read<1>();  // the previous mirror boxes have been read
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-#pragma unroll
-              for (int kk = 0; kk < 16; ++kk) {
-                const float mine_even = o[32 * c + 2 * kk], mine_odd = o[32 * c + 2 * kk + 1];
-                const float other = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? mine_even : mine_odd, 1);
-                const __nv_bfloat162 h = (lane & 1) ? __floats2bfloat162_rn(other, mine_odd)
-                                                    : __floats2bfloat162_rn(mine_even, other);
-                const int r = 2 * kk + (lane & 1);
-                const uint32_t off = static_cast<uint32_t>(r * 64 + (((lane >> 3) ^ (kk & 3)) << 4) + (lane & 6) * 2);
-                *reinterpret_cast<__nv_bfloat162*>(mir + c * kMirBox + off) = h;
-              }
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              for (int c = 0; c < 2; ++c)
-                if (jg + 32 * c < a.N) tc::tma_store_3d(&tmM, mir + c * kMirBox, i0, jg + 32 * c, mb);
-              tc::bulk_commit();
-            }
-          }
-        } else if (i < a.M) {
-          __nv_bfloat16* Dm = static_cast<__nv_bfloat16*>(a.D) + mb * a.d_stride;
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int j = jg + k;
-            if (j < a.N && j >= i) Dm[static_cast<long long>(i) * a.ldd + j] = __float2bfloat16_rn(o[k]);
-            if (j < a.N && j > i) Dm[static_cast<long long>(j) * a.ldd + i] = __float2bfloat16_rn(o[k]);
-          }
+          box_put_symmetric_row(dbox, mbox, lane, o);
+        } else {
+          box_put_row(dbox, lane, o);
+          if (kind == 2) box_put_transposed(mbox, lane, o);
         }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_3d(&tmD, dbox, j0, i0, mb);
+          if (kind == 2) tc::tma_store_3d(&tmD, mbox, i0, j0, mb);
+          tc::bulk_commit();
+        }
+        last_par = par;
       }
       tc::fence_before_sync();
       tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
-      // the slice is free once the TMA has read it: then prefetch the next tile's R
-      if (lane == 0) tc::bulk_wait_read<0>();
-      __syncwarp();
-      const int tn = t + static_cast<int>(gridDim.x);
-      if (has_r && tn < a.num_tiles) {
-        int l = 0;
-        if (lane == 0) l = epi_load_r(a, &tmR, slice, rb, tn, quad) ? 1 : 0;
-        rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+      if (has_r) {
+        // the slice is free once the TMA has read it: then prefetch the next tile's R
+        if (lane == 0) tc::bulk_wait_read<0>();
+        __syncwarp();
+        const int tn = t + static_cast<int>(gridDim.x);
+        if (tn < a.num_tiles) {
+          int l = 0;
+          if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, tn, quad) ? 1 : 0;
+          rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+        }
       }
     }
     if (lane == 0) {
@@ -1093,16 +1141,18 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArg
   return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(kGemmThreads), kSmemBytes2, stream, P, Q, a);
 }
 
-// The single-CTA kernel; with tma, R (if beta != 0) is read through R and D is stored through
-// D (64 x 32 boxes, 128-byte swizzle) and, for a symmetric product, M (32 x 32, 64-byte swizzle).
+// The single-CTA kernel with epilogue `epi`: kEpiTmaR reads R through *R, the TMA epilogues store
+// D through *D (32 x 32 boxes, 64-byte swizzle).
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
-                        const CUtensorMap* M, bool tma, GemmArgs a, cudaStream_t stream) {
+                        int epi, GemmArgs a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    ZOPT_CUDA_TRY(
-        cudaFuncSetAttribute(gemm_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    ZOPT_CUDA_TRY(
-        cudaFuncSetAttribute(gemm_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesTma));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes(kEpiRegs)));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes(kEpiTmaR)));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes(kEpiTma)));
     attr_set = true;
   }
   a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
@@ -1120,11 +1170,17 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtens
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-  if (!tma) return launch_pdl(gemm_bf16_kernel<false>, dim3(grid), dim3(kGemmThreads), kSmemBytes, stream, P, Q, P, P, P, a);
-  if (D == nullptr || (a.beta != 0.0f && R == nullptr) || (a.symmetric && M == nullptr) || a.d_f32 || a.d_trans)
+  if (epi == kEpiRegs)
+    return launch_pdl(gemm_bf16_kernel<kEpiRegs>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(kSmemBytes),
+                      stream, P, Q, P, P, a);
+  if (D == nullptr || a.d_f32 || a.d_trans || (epi == kEpiTmaR && a.beta != 0.0f && R == nullptr) ||
+      (epi == kEpiTma && a.beta != 0.0f))
     return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
-  return launch_pdl(gemm_bf16_kernel<true>, dim3(grid), dim3(kGemmThreads), kSmemBytesTma, stream, P, Q,
-                    R != nullptr ? *R : P, *D, M != nullptr ? *M : P, a);
+  if (epi == kEpiTmaR)
+    return launch_pdl(gemm_bf16_kernel<kEpiTmaR>, dim3(grid), dim3(kGemmThreads),
+                      static_cast<size_t>(smem_bytes(kEpiTmaR)), stream, P, Q, R != nullptr ? *R : P, *D, a);
+  return launch_pdl(gemm_bf16_kernel<kEpiTma>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
+                    stream, P, Q, P, *D, a);
 }
 
 }  // namespace ns
@@ -1194,23 +1250,22 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
 
   // Tensor maps over the group's workspace matrices (bf16 tensor-core path only).
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
-  // the single-CTA kernel's epilogue boxes: R and D as 64 x 32 boxes, mirrors as 32 x 32
-  CUtensorMap mx_e[2], ma_e, mb_e, ma_m, mb_m;
+  // the single-CTA kernel's epilogue boxes (R, D and mirrors): 32 x 32, 64-byte swizzle
+  CUtensorMap mx_e[2], ma_e, mb_e;
   if (!f32c) {
     const long long mb = static_cast<long long>(p.per_mat);
     for (int q = 0; q < 2; ++q) {
       if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BM)) != ZOPT_OK) return st;
       if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BN)) != ZOPT_OK) return st;
       if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BK)) != ZOPT_OK) return st;
-      if ((st = make_map(&mx_e[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, 32)) != ZOPT_OK) return st;
+      if ((st = make_map(&mx_e[q], xb[q], p.n, p.m, p.ldx, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK)
+        return st;
     }
     if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
     if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, group, mb, 64, BN)) != ZOPT_OK) return st;
     if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
-    if ((st = make_map(&ma_e, A, p.m, p.m, p.lda, group, mb, 64, 32)) != ZOPT_OK) return st;
-    if ((st = make_map(&mb_e, B, p.m, p.m, p.lda, group, mb, 64, 32)) != ZOPT_OK) return st;
-    if ((st = make_map(&ma_m, A, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
-    if ((st = make_map(&mb_m, B, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+    if ((st = make_map(&ma_e, A, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+    if ((st = make_map(&mb_e, B, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
   }
 
   const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
@@ -1285,7 +1340,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
                          (gs == 1 || (batch_stride_x * 2) % 16 == 0);
     if (out_tma) {
       const long long ob = gs == 1 ? p.m * ld_x * 2 : batch_stride_x * 2;
-      if ((st = make_map(&mo_e, xo, p.n, p.m, ld_x, gs, ob, 64, 32)) != ZOPT_OK) return st;
+      if ((st = make_map(&mo_e, xo, p.n, p.m, ld_x, gs, ob, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
     }
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
@@ -1317,28 +1372,27 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.group = gs;
         // A = X X'
         ga.M = m; ga.N = m; ga.K = n;
-        ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.R = nullptr; ga.ldr = 0;
-        ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
+        ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
+        ga.ldr = 0; ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
         if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], ga, s)
-                       : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, &ma_m, true, ga, s)) != ZOPT_OK)
+                       : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, kEpiTma, ga, s)) != ZOPT_OK)
           return st;
-        // B = c A A' + b A
+        // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X
         ga.K = m;
-        ga.alpha = abc[2]; ga.beta = abc[1];
+        ga.alpha = abc[2]; ga.beta = abc[1]; ga.diag = abc[0];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
         ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
         if ((st = pair ? launch_gemm_pair(ma_p, ma_p, ga, s)
-                       : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, &mb_m, true, ga, s)) != ZOPT_OK)
+                       : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, kEpiTmaR, ga, s)) != ZOPT_OK)
           return st;
-        // X = B X + a X
+        // X = B' X
         ga.M = m; ga.N = n; ga.K = m;
-        ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = abc[0];
-        ga.R = reinterpret_cast<const __nv_bfloat16*>(xb[cur]); ga.ldr = p.ldx; ga.r_stride = mat_elems;
+        ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f;
+        ga.R = nullptr; ga.ldr = 0; ga.r_stride = 0;
         ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
-        const bool x_tma = !last || out_tma;
+        const int x_epi = (!last || out_tma) ? kEpiTma : kEpiRegs;
         if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], ga, s)
-                       : launch_gemm(mb_p, mx_mn[cur], &mx_e[cur], last ? &mo_e : &mx_e[cur ^ 1], nullptr, x_tma, ga,
-                                     s)) != ZOPT_OK)
+                       : launch_gemm(mb_p, mx_mn[cur], nullptr, last ? &mo_e : &mx_e[cur ^ 1], x_epi, ga, s)) != ZOPT_OK)
           return st;
       }
       cur ^= 1;
