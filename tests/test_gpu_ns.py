@@ -117,23 +117,25 @@ def test_fp32_io_and_batch_strides(zopt):
         assert torch.equal(one, X[b])  # a batch entry is bitwise the single call
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,cols", [(300, 1000), (1000, 300)])
 @pytest.mark.parametrize("pad,shift", [(8, 0), (3, 0), (0, 1), (8, 1)])
-def test_bf16_output_pitch_and_alignment(zopt, pad, shift):
-    """The last product writes the caller's X through the TMA when its rows are 16-byte aligned
-    and by plain stores otherwise: padded rows (pitch cols + pad) and a base shifted by `shift`
-    elements, in groups of 2 and 1. Every result is bitwise the contiguous single call's, and
-    the padding is left untouched."""
-    rows, cols, batch = 300, 1000, 3
-    G = torch.randn(batch, rows, cols, device="cuda").to(torch.bfloat16)
+def test_output_pitch_and_alignment(zopt, pad, shift, rows, cols, dtype):
+    """The last product writes the caller's X through the TMA (transposed for a tall matrix)
+    when its rows are 16-byte aligned and by plain stores otherwise: padded rows (pitch cols +
+    pad) and a base shifted by `shift` elements, bf16 and fp32, in groups of 2 and 1. Every
+    result is bitwise the contiguous single call's, and the padding is left untouched."""
+    batch = 3
+    G = torch.randn(batch, rows, cols, device="cuda").to(dtype)
     ld = cols + pad
-    flat = torch.full((batch * rows * ld + shift,), 7.0, device="cuda", dtype=torch.bfloat16)
+    flat = torch.full((batch * rows * ld + shift,), 7.0, device="cuda", dtype=dtype)
     full = flat[shift:].view(batch, rows, ld)
     X = full[:, :, :cols]
     zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols, group=2), steps=3)
     ws1 = zopt.new_ns_workspace(rows, cols)
     for b in range(batch):
-        one = torch.empty(rows, cols, device="cuda", dtype=torch.bfloat16)
-        zopt.ns_orthogonalize(G[b], one, ws1, steps=3)
+        one = torch.empty(rows, cols, device="cuda", dtype=dtype)
+        zopt.ns_orthogonalize(G[b].contiguous(), one, ws1, steps=3)
         torch.cuda.synchronize()
         assert torch.equal(one, X[b]), b
     if pad:

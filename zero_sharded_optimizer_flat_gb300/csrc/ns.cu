@@ -316,6 +316,23 @@ __device__ __forceinline__ void box_put_symmetric_row(uint8_t* box, const uint8_
   }
 }
 
+// A 32 x 32 fp32 box under the 128-byte swizzle (box 1024-byte aligned): row r at 128 r, its
+// 16-byte piece q (columns 4q .. 4q + 3) at piece q ^ (r & 7).
+__device__ __forceinline__ uint32_t box32_piece(int r, int q) {
+  return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void box32_put_row(uint8_t* box, int lane, const float (&o)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<float4*>(box + box32_piece(lane, q)) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+// Lane L's o[k] lands at row k, column L: each store of the warp fills one 128-byte row.
+__device__ __forceinline__ void box32_put_transposed(uint8_t* box, int lane, const float (&o)[32]) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    *reinterpret_cast<float*>(box + box32_piece(k, lane >> 2) + (lane & 3) * 4) = o[k];
+}
+
 // Where the 32 x 32 block at rows i0, columns j0 stands: 0 out of the matrix, 1 written as is
 // (not symmetric), 2 above the diagonal (written and mirrored), 3 on it (its mirror is itself),
 // 4 below it (written by the mirror of the block above). i0 and j0 are multiples of 32.
@@ -554,7 +571,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc::bulk_wait_read<1>();
         }
         __syncwarp();
-        if (kind == 3) {
+        if (kEpi == kEpiTma && a.d_f32) {
+          // (the last product, into the caller's fp32 matrix) one fp32 box over both of this
+          // parity's bf16 boxes
+          dbox = mine + par * 2 * kBox;
+          if (a.d_trans)
+            box32_put_transposed(dbox, lane, o);
+          else
+            box32_put_row(dbox, lane, o);
+        } else if (a.d_trans) {
+          box_put_transposed(dbox, lane, o);
+        } else if (kind == 3) {
           box_put_transposed(mbox, lane, o);
           __syncwarp();
           box_put_symmetric_row(dbox, mbox, lane, o);
@@ -565,7 +592,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tc::tma_store_3d(&tmD, dbox, j0, i0, mb);
+          if (a.d_trans)  // D[i, j] goes to row j, column i of the caller's matrix
+            tc::tma_store_3d(&tmD, dbox, i0, j0, mb);
+          else
+            tc::tma_store_3d(&tmD, dbox, j0, i0, mb);
           if (kind == 2) tc::tma_store_3d(&tmD, mbox, i0, j0, mb);
           tc::bulk_commit();
         }
@@ -1025,19 +1055,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A 3-D bf16 tensor map over `group` row-major [outer][inner] matrices with `pitch` elements
-// per row, `mat_bytes` apart; boxes of box_inner x box_outer x 1 under the given swizzle.
+// A 3-D bf16 (or fp32) tensor map over `group` row-major [outer][inner] matrices with `pitch`
+// elements per row, `mat_bytes` apart; boxes of box_inner x box_outer x 1 under the given swizzle.
 zopt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long pitch,
                      long long group, long long mat_bytes, int box_inner, int box_outer,
-                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, bool f32 = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                               static_cast<cuuint64_t>(group)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 2, static_cast<cuuint64_t>(mat_bytes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * (f32 ? 4 : 2), static_cast<cuuint64_t>(mat_bytes)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -1173,8 +1203,9 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtens
   if (epi == kEpiRegs)
     return launch_pdl(gemm_bf16_kernel<kEpiRegs>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(kSmemBytes),
                       stream, P, Q, P, P, a);
-  if (D == nullptr || a.d_f32 || a.d_trans || (epi == kEpiTmaR && a.beta != 0.0f && R == nullptr) ||
-      (epi == kEpiTma && a.beta != 0.0f))
+  if (D == nullptr || (epi == kEpiTmaR && (a.beta != 0.0f && R == nullptr)) ||
+      (epi == kEpiTmaR && (a.d_f32 || a.d_trans)) || (epi == kEpiTma && a.beta != 0.0f) ||
+      (a.symmetric && (a.d_f32 || a.d_trans)))
     return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
   if (epi == kEpiTmaR)
     return launch_pdl(gemm_bf16_kernel<kEpiTmaR>, dim3(grid), dim3(kGemmThreads),
@@ -1332,15 +1363,19 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     // products with m >= 1024 run on CTA pairs; below that the single-CTA kernel's twice as
     // many tiles keep more SMs busy
     const bool pair = m >= 1024;
-    // the last product writes the caller's X through the TMA when it is a bf16 row-major
-    // matrix the TMA can address
+    // the last product writes the caller's X through the TMA (32 x 32 boxes, transposed for a
+    // tall matrix) when the TMA can address it: 16-byte aligned rows and matrices
     CUtensorMap mo_e;
-    const bool out_tma = !f32c && !pair && io_dtype == ZOPT_BF16 && !transpose &&
-                         (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 && ld_x % 8 == 0 &&
-                         (gs == 1 || (batch_stride_x * 2) % 16 == 0);
+    const long long xrows = transpose ? p.n : p.m, xcols = transpose ? p.m : p.n;  // the caller's shape
+    const bool out_tma = !f32c && !pair && (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 &&
+                         (ld_x * static_cast<long long>(esz)) % 16 == 0 &&
+                         (gs == 1 || (batch_stride_x * static_cast<long long>(esz)) % 16 == 0);
     if (out_tma) {
-      const long long ob = gs == 1 ? p.m * ld_x * 2 : batch_stride_x * 2;
-      if ((st = make_map(&mo_e, xo, p.n, p.m, ld_x, gs, ob, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+      const long long ob = (gs == 1 ? xrows * ld_x : batch_stride_x) * static_cast<long long>(esz);
+      const bool of32 = io_dtype == ZOPT_F32;
+      if ((st = make_map(&mo_e, xo, xcols, xrows, ld_x, gs, ob, 32, 32,
+                         of32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, of32)) != ZOPT_OK)
+        return st;
     }
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
