@@ -342,13 +342,11 @@ __device__ __forceinline__ int block_kind(const GemmArgs& a, int i0, int j0) {
   return j0 > i0 ? 2 : (j0 == i0 ? 3 : 4);
 }
 
-// Lane 0 of epilogue warp `quad` (kEpiTmaR): the R boxes of tile t that the warp reads, into its
-// slice, on bar. Returns whether any load was issued.
+// Lane 0 of an epilogue warp (kEpiTmaR): the R boxes that the warp reads for its rows i0 ..
+// i0 + 31 of tile column block tj of matrix mb, into its slice, on bar. Returns whether any
+// load was issued.
 __device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap* tmR, uint8_t* slice, uint64_t* bar,
-                                           int t, int quad) {
-  int mb, ti, tj;
-  tile_coords(a, t, mb, ti, tj);
-  const int i0 = ti * BM + 32 * quad;
+                                           int mb, int i0, int tj) {
   int n = 0;
   for (int c = 0; c < BN / 32; ++c) {
     const int k = block_kind(a, i0, tj * BN + 32 * c);
@@ -361,6 +359,84 @@ __device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap*
     if (k != 0 && k != 4) tc::tma_load_3d(slice + c * kBox, tmR, bar, tj * BN + 32 * c, i0, mb);
   }
   return true;
+}
+
+// One epilogue warp's part of a tile through the TMA: its 32 TMEM lanes (rows i0 .. i0 + 31)
+// x 256 columns from taddr (tile column block tj of matrix mb) become alpha * acc + beta * R +
+// diag on the diagonal, handed to the TMA as 32 x 32 boxes. kSlice: R sits in the warp's eight
+// slice boxes at `mine` (D is written over it) and two mirror boxes follow; otherwise `mine`
+// holds four boxes, a D and a mirror box for even blocks and another pair for odd ones (an
+// fp32 box takes a pair). last_par: parity of the last block whose boxes went to the TMA.
+template <bool kSlice>
+__device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
+                                             int i0, int tj, int mb, bool has_r, int lane, int& last_par) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int j0 = tj * BN + 32 * c;
+    const int kind = block_kind(a, i0, j0);
+    if (kind == 0 || kind == 4) continue;
+    uint32_t v[32];
+    tc::tmem_ld32(taddr + static_cast<uint32_t>(32 * c), v);
+    tc::tmem_wait_ld();
+    float o[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
+    const int par = c & 1;
+    uint8_t* dbox = kSlice ? mine + c * kBox : mine + 2 * par * kBox;
+    uint8_t* mbox = kSlice ? mine + (8 + par) * kBox : dbox + kBox;
+    if (kSlice && has_r) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(dbox + box_piece(lane, q));
+        const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          o[8 * q + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
+          o[8 * q + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
+        }
+      }
+    }
+    if (a.diag != 0.0f && j0 == i0) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (k == lane) o[k] += a.diag;
+    }
+    // the boxes of this parity were last handed to the TMA two blocks ago at the latest: wait
+    // until it has read them (all groups but the newest, if that one is the other parity's)
+    if (lane == 0) {
+      if (last_par == par || last_par < 0)
+        tc::bulk_wait_read<0>();
+      else
+        tc::bulk_wait_read<1>();
+    }
+    __syncwarp();
+    if (!kSlice && a.d_f32) {  // (a last product into the caller's fp32 matrix) one box per pair
+      if (a.d_trans)
+        box32_put_transposed(dbox, lane, o);
+      else
+        box32_put_row(dbox, lane, o);
+    } else if (a.d_trans) {
+      box_put_transposed(dbox, lane, o);
+    } else if (kind == 3) {
+      box_put_transposed(mbox, lane, o);
+      __syncwarp();
+      box_put_symmetric_row(dbox, mbox, lane, o);
+    } else {
+      box_put_row(dbox, lane, o);
+      if (kind == 2) box_put_transposed(mbox, lane, o);
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (a.d_trans)  // D[i, j] goes to row j, column i of the caller's matrix
+        tc::tma_store_3d(tmD, dbox, i0, j0, mb);
+      else
+        tc::tma_store_3d(tmD, dbox, j0, i0, mb);
+      if (kind == 2) tc::tma_store_3d(tmD, mbox, i0, j0, mb);
+      tc::bulk_commit();
+    }
+    last_par = par;
+  }
 }
 
 // The single-CTA persistent GEMM with the epilogue kEpi (kEpiRegs, kEpiTmaR or kEpiTma). The TMA
@@ -502,18 +578,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if constexpr (kTma) {
     // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
     const int quad = warp & 3;  // this warp may read TMEM lanes [32 quad, 32 quad + 32)
-    // kEpiTmaR: R slice (8 boxes) then 2 mirror boxes; kEpiTma: 4 boxes, a D and a mirror box for
-    // even blocks and another pair for odd ones
     uint8_t* mine = sEpi + quad * (epi_bytes(kEpi) / 4);
     uint64_t* rb = rbar + quad;
     const bool has_r = kEpi == kEpiTmaR && a.beta != 0.0f;
     bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
     uint32_t rph = 0;
-    int last_par = -1;   // (warp-uniform) parity of the last block whose boxes went to the TMA
+    int last_par = -1;
     int t = blockIdx.x;
     if (has_r && t < a.num_tiles) {
+      int mb, ti, tj;
+      tile_coords(a, t, mb, ti, tj);
       int l = 0;
-      if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, t, quad) ? 1 : 0;
+      if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, ti * BM + 32 * quad, tj) ? 1 : 0;
       rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
     }
     for (int it = 0; t < a.num_tiles; t += gridDim.x, ++it) {
@@ -530,77 +606,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::fence_after_sync();
       int mb, ti, tj;
       tile_coords(a, t, mb, ti, tj);
-      const int i0 = ti * BM + 32 * quad;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int j0 = tj * BN + 32 * c;
-        const int kind = block_kind(a, i0, j0);
-        if (kind == 0 || kind == 4) continue;
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN + 32 * c), v);
-        tc::tmem_wait_ld();
-        float o[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
-        const int par = c & 1;
-        uint8_t* dbox = kEpi == kEpiTmaR ? mine + c * kBox : mine + (2 * par) * kBox;
-        uint8_t* mbox = kEpi == kEpiTmaR ? mine + (8 + par) * kBox : mine + (2 * par + 1) * kBox;
-        if (has_r) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 u = *reinterpret_cast<const uint4*>(dbox + box_piece(lane, q));
-            const uint32_t x[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              o[8 * q + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
-              o[8 * q + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
-            }
-          }
-        }
-        if (a.diag != 0.0f && j0 == i0) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k == lane) o[k] += a.diag;
-        }
-        // the boxes of this parity were last handed to the TMA two blocks ago at the latest:
-        // wait until it has read them (all but the newest group if that one is the other parity's)
-        if (lane == 0) {
-          if (last_par == par || last_par < 0)
-            tc::bulk_wait_read<0>();
-          else
-            tc::bulk_wait_read<1>();
-        }
-        __syncwarp();
-        if (kEpi == kEpiTma && a.d_f32) {
-          // (the last product, into the caller's fp32 matrix) one fp32 box over both of this
-          // parity's bf16 boxes
-          dbox = mine + par * 2 * kBox;
-          if (a.d_trans)
-            box32_put_transposed(dbox, lane, o);
-          else
-            box32_put_row(dbox, lane, o);
-        } else if (a.d_trans) {
-          box_put_transposed(dbox, lane, o);
-        } else if (kind == 3) {
-          box_put_transposed(mbox, lane, o);
-          __syncwarp();
-          box_put_symmetric_row(dbox, mbox, lane, o);
-        } else {
-          box_put_row(dbox, lane, o);
-          if (kind == 2) box_put_transposed(mbox, lane, o);
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (a.d_trans)  // D[i, j] goes to row j, column i of the caller's matrix
-            tc::tma_store_3d(&tmD, dbox, i0, j0, mb);
-          else
-            tc::tma_store_3d(&tmD, dbox, j0, i0, mb);
-          if (kind == 2) tc::tma_store_3d(&tmD, mbox, i0, j0, mb);
-          tc::bulk_commit();
-        }
-        last_par = par;
-      }
+      epi_tile_tma<kEpi == kEpiTmaR>(a, &tmD, mine,
+                                     tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
+                                     ti * BM + 32 * quad, tj, mb, has_r, lane, last_par);
       tc::fence_before_sync();
       tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
       if (has_r) {
@@ -609,8 +617,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         const int tn = t + static_cast<int>(gridDim.x);
         if (tn < a.num_tiles) {
+          tile_coords(a, tn, mb, ti, tj);
           int l = 0;
-          if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, tn, quad) ? 1 : 0;
+          if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, ti * BM + 32 * quad, tj) ? 1 : 0;
           rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
         }
       }
@@ -669,9 +678,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // the leader's single thread issues the M=256 MMAs, whose commits reach both CTAs; each CTA
 // drains its own 128 TMEM lanes; the epilogue warps of both CTAs release an accumulator on the
 // leader's barrier.
+// The epilogues are the single-CTA kernel's: each CTA drains its own 128 rows of the tile.
+// With R prefetched (kEpiTmaR) the ring keeps four stages, otherwise six.
 constexpr int BM2 = 256, STAGES2 = 6;
 constexpr int kHalf = 128 * BK * 2;  // 16 KiB: 128 rows (or columns) of a 64-deep k-block
-constexpr int kSmemBytes2 = STAGES2 * 2 * kHalf + 1024 + 256 + kStageBytes;
+__host__ __device__ constexpr int stages2_of(int e) { return e == kEpiTmaR ? 4 : STAGES2; }
+constexpr int smem_bytes2(int e) {
+  return stages2_of(e) * 2 * kHalf + epi_bytes(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0);
+}
+static_assert(smem_bytes2(kEpiTma) <= 232448 && smem_bytes2(kEpiTmaR) <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, int& tp, int& tj) {
   mb = t / a.tiles_per_mat;
@@ -694,19 +709,26 @@ __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, 
   }
 }
 
+// tmR, tmD: as for the single-CTA kernel (unused by kEpiRegs).
+template <int kEpi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmD,
                           const GemmArgs a) {
+  constexpr int S2 = stages2_of(kEpi);
+  constexpr bool kTma = kEpi != kEpiRegs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES2 * kHalf;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES2 * kHalf);
-  uint64_t* empty = full + STAGES2;
-  uint64_t* tfull = empty + STAGES2;
+  uint8_t* sB = smem + S2 * kHalf;
+  uint8_t* sEpi = sB + S2 * kHalf;  // the TMA epilogue's boxes
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + epi_bytes(kEpi));
+  uint64_t* empty = full + S2;
+  uint64_t* tfull = empty + S2;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rbar = drain + 1;  // kEpiTmaR: one R barrier per epilogue warp
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(rbar + 4);
   float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -714,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
-    for (int q = 0; q < STAGES2; ++q) {
+    for (int q = 0; q < S2; ++q) {
       tc::mbar_init(full + q, 1);
       tc::mbar_init(empty + q, 1);
     }
@@ -723,9 +745,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(tempty + b, 256);  // the epilogue threads of both CTAs (used in the leader)
     }
     tc::mbar_init(drain, 1);
+    if (kEpi == kEpiTmaR)
+      for (int q = 0; q < 4; ++q) tc::mbar_init(rbar + q, 1);
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmP);
     tc::prefetch_tmap(&tmQ);
+    if (kEpi == kEpiTmaR) tc::prefetch_tmap(&tmR);
+    if (kTma) tc::prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tc::tmem_alloc_pair(tslot, kTmemCols);
@@ -744,8 +770,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // ---------------------------------------------------------------- TMA producer (both CTAs)
       int s = 0;
       uint32_t ph = 0;
-      int armed[STAGES2];
-      for (int q = 0; q < STAGES2; ++q) armed[q] = -1;
+      int armed[S2];
+      for (int q = 0; q < S2; ++q) armed[q] = -1;
       bool ok = true;
       for (int t = pair; ok && t < a.num_tiles; t += npairs) {
         int mb, tp, tj;
@@ -767,14 +793,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tc::tma_load_3d_pair(sB + s * kHalf, &tmQ, bar, col0, kb * BK, mb);
             tc::tma_load_3d_pair(sB + s * kHalf + kBoxMN, &tmQ, bar, col0 + 64, kb * BK, mb);
           }
-          if (++s == STAGES2) {
+          if (++s == S2) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok && leader) {  // the leader's stage barriers count both CTAs' copies
-        for (int q = 0; q < STAGES2; ++q)
+        for (int q = 0; q < S2; ++q)
           if (armed[q] >= 0) mbar_wait_drain(full + q, static_cast<uint32_t>(armed[q]));
       }
     }
@@ -810,7 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tc::umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc::umma_commit_pair(empty + s, 3);  // both CTAs' stage s is free
-          if (++s == STAGES2) {
+          if (++s == S2) {
             s = 0;
             ph ^= 1u;
           }
@@ -821,6 +847,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       tc::umma_commit_pair(drain, 1);
       mbar_wait_drain(drain, 0);
     }
+  } else if constexpr (kTma) {
+    // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
+    const int quad = warp & 3;
+    uint8_t* mine = sEpi + quad * (epi_bytes(kEpi) / 4);
+    uint64_t* rb = rbar + quad;
+    const bool has_r = kEpi == kEpiTmaR && a.beta != 0.0f;
+    const uint32_t tempty_leader[2] = {tc::map_to_rank(tc::smem_u32(tempty), 0),
+                                       tc::map_to_rank(tc::smem_u32(tempty + 1), 0)};
+    const int rows0 = static_cast<int>(rank) * 128 + 32 * quad;  // this warp's rows within a tile
+    bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
+    uint32_t rph = 0;
+    int last_par = -1;
+    int t = pair;
+    if (has_r && t < a.num_tiles) {
+      int mb, tp, tj;
+      tile_coords2(a, t, mb, tp, tj);
+      int l = 0;
+      if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
+      rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+    }
+    for (int it = 0; t < a.num_tiles; t += npairs, ++it) {
+      const int b = it & 1;
+      const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      if (rpend) {  // every lane waits, so that each sees the TMA's writes
+        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, a.err) ? 1 : 0)) break;
+        rph ^= 1u;
+        rpend = false;
+      }
+      tc::fence_after_sync();
+      int mb, tp, tj;
+      tile_coords2(a, t, mb, tp, tj);
+      epi_tile_tma<kEpi == kEpiTmaR>(a, &tmD, mine,
+                                     tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
+                                     tp * BM2 + rows0, tj, mb, has_r, lane, last_par);
+      tc::fence_before_sync();
+      tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
+      if (has_r) {
+        // the slice is free once the TMA has read it: then prefetch the next tile's R
+        if (lane == 0) tc::bulk_wait_read<0>();
+        __syncwarp();
+        const int tn = t + npairs;
+        if (tn < a.num_tiles) {
+          tile_coords2(a, tn, mb, tp, tj);
+          int l = 0;
+          if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
+          rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+        }
+      }
+    }
+    if (lane == 0) {
+      tc::bulk_wait_all();                  // every store has reached global memory
+      if (rpend) mbar_wait_drain(rb, rph);  // (after a failed wait) no load left in flight
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     const int quad = warp & 3;
@@ -1146,11 +1229,17 @@ zopt_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // The CTA-pair kernel for products with at least 256 rows: P is read with 128-row boxes, Q
 // with 128-row (K-major) or 64 x 64 (MN-major) boxes.
-zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArgs a, cudaStream_t stream) {
+// The CTA-pair kernel with epilogue `epi` (maps as for launch_gemm; kEpiTmaR reads R through *R).
+zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
+                             int epi, GemmArgs a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    ZOPT_CUDA_TRY(
-        cudaFuncSetAttribute(gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes2(kEpiRegs)));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes2(kEpiTmaR)));
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes2(kEpiTma)));
     attr_set = true;
   }
   a.tiles_m = static_cast<int>((a.M + BM2 - 1) / BM2);
@@ -1168,7 +1257,19 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, GemmArg
   const int sms = sm_count();
   if (sms < 2) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int pairs = a.num_tiles < sms / 2 ? a.num_tiles : sms / 2;
-  return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(kGemmThreads), kSmemBytes2, stream, P, Q, a);
+  const dim3 grid(static_cast<unsigned>(2 * pairs));
+  if (epi == kEpiRegs)
+    return launch_pdl(gemm_bf16_pair_kernel<kEpiRegs>, grid, dim3(kGemmThreads),
+                      static_cast<size_t>(smem_bytes2(kEpiRegs)), stream, P, Q, P, P, a);
+  if (D == nullptr || (epi == kEpiTmaR && (a.beta != 0.0f && R == nullptr)) ||
+      (epi == kEpiTmaR && (a.d_f32 || a.d_trans)) || (epi == kEpiTma && a.beta != 0.0f) ||
+      (a.symmetric && (a.d_f32 || a.d_trans)))
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
+  if (epi == kEpiTmaR)
+    return launch_pdl(gemm_bf16_pair_kernel<kEpiTmaR>, grid, dim3(kGemmThreads),
+                      static_cast<size_t>(smem_bytes2(kEpiTmaR)), stream, P, Q, R != nullptr ? *R : P, *D, a);
+  return launch_pdl(gemm_bf16_pair_kernel<kEpiTma>, grid, dim3(kGemmThreads), static_cast<size_t>(smem_bytes2(kEpiTma)),
+                    stream, P, Q, P, *D, a);
 }
 
 // The single-CTA kernel with epilogue `epi`: kEpiTmaR reads R through *R, the TMA epilogues store
@@ -1367,7 +1468,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     // tall matrix) when the TMA can address it: 16-byte aligned rows and matrices
     CUtensorMap mo_e;
     const long long xrows = transpose ? p.n : p.m, xcols = transpose ? p.m : p.n;  // the caller's shape
-    const bool out_tma = !f32c && !pair && (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 &&
+    const bool out_tma = !f32c && (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 &&
                          (ld_x * static_cast<long long>(esz)) % 16 == 0 &&
                          (gs == 1 || (batch_stride_x * static_cast<long long>(esz)) % 16 == 0);
     if (out_tma) {
@@ -1409,7 +1510,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.M = m; ga.N = m; ga.K = n;
         ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
         ga.ldr = 0; ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], ga, s)
+        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], nullptr, &ma_e, kEpiTma, ga, s)
                        : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, kEpiTma, ga, s)) != ZOPT_OK)
           return st;
         // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X
@@ -1417,7 +1518,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.alpha = abc[2]; ga.beta = abc[1]; ga.diag = abc[0];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
         ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, ga, s)
+        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, &ma_e, &mb_e, kEpiTmaR, ga, s)
                        : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, kEpiTmaR, ga, s)) != ZOPT_OK)
           return st;
         // X = B' X
@@ -1426,7 +1527,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         ga.R = nullptr; ga.ldr = 0; ga.r_stride = 0;
         ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
         const int x_epi = (!last || out_tma) ? kEpiTma : kEpiRegs;
-        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], ga, s)
+        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], nullptr, last ? &mo_e : &mx_e[cur ^ 1], x_epi, ga, s)
                        : launch_gemm(mb_p, mx_mn[cur], nullptr, last ? &mo_e : &mx_e[cur ^ 1], x_epi, ga, s)) != ZOPT_OK)
           return st;
       }
