@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 #include <utility>
 
@@ -62,10 +63,12 @@ constexpr int kSmemBytes = STAGES * (kTileA + kTileB) + 1024 + 256 + kStageBytes
 // over it in place and has two mirror boxes per warp, at the cost of a ring stage.
 constexpr int kEpiRegs = 0, kEpiTmaR = 1, kEpiTma = 2;
 constexpr int kBox = 32 * 32 * 2;  // 2 KiB
+constexpr int kIdentBytes = 2 * 512;  // kEpiTma: two 16 x 16 bf16 identity tiles (32-byte swizzle)
 __host__ __device__ constexpr int stages_of(int e) { return e == kEpiTmaR ? 3 : STAGES; }
 __host__ __device__ constexpr int epi_bytes(int e) { return e == kEpiTmaR ? 4 * (8 + 2) * kBox : (e == kEpiTma ? 4 * 4 * kBox : 0); }
 constexpr int smem_bytes(int e) {
-  return stages_of(e) * (kTileA + kTileB) + epi_bytes(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0);
+  return stages_of(e) * (kTileA + kTileB) + epi_bytes(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0) +
+         (e == kEpiTma ? kIdentBytes : 0);
 }
 static_assert(smem_bytes(kEpiTmaR) <= 232448 && smem_bytes(kEpiTma) <= 232448, "shared memory per CTA");
 static_assert(smem_bytes(kEpiRegs) == kSmemBytes, "register-epilogue layout");
@@ -86,6 +89,10 @@ struct GemmArgs {
   int d_f32;
   int d_trans;  // write D[i, j] to D[j * ldd + i]
   float diag;  // added to D[i, i] (after alpha * acc + beta * R)
+  // (single-CTA kernel, kEpiTma, M == N == K) the accumulator also takes (h1 + h2) * P[i, j]:
+  // at the k-blocks under the tile's columns the A-operand stage meets a 16 x 16 identity
+  int ident;
+  float h1, h2;
   int* err;
 };
 
@@ -463,8 +470,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* rbar = drain + 1;  // kEpiTmaR: one R barrier per epilogue warp
   uint32_t* tslot = reinterpret_cast<uint32_t*>(rbar + 4);
   float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
+  uint8_t* ident = reinterpret_cast<uint8_t*>(full) + 256;  // kEpiTma (256-byte aligned)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (kEpi == kEpiTma && a.ident) {
+    // tile h (h1, h2): element (n, k) = h if n == k, as the 32-byte swizzle lays it out: row n at
+    // 32 (n % 8) + 256 (n / 8), its 16-byte halves swapped when bit 2 of n is set
+    for (int w = threadIdx.x; w < kIdentBytes / 4; w += blockDim.x) {
+      uint32_t word = 0;
+      for (int e = 0; e < 2; ++e) {
+        const int byte = 4 * w + 2 * e;
+        const int h = byte / 512, bt = byte % 512;
+        const int n = (bt / 256) * 8 + (bt % 256) / 32;
+        const int k = ((((bt % 32) / 16) ^ ((n >> 2) & 1)) * 8) + (bt % 16) / 2;
+        if (n == k) word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(h ? a.h2 : a.h1))) << (16 * e);
+      }
+      *reinterpret_cast<uint32_t*>(ident + 4 * w) = word;
+    }
+    tc::fence_proxy_async_smem();  // the MMAs read the tiles through the async proxy
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(full + s, 1);
@@ -536,12 +560,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       const uint32_t idesc = tc::idesc_bf16_f32(BM, BN, false, a.b_mn_major != 0);
+      const uint32_t idesc16 = tc::idesc_bf16_f32(BM, 16, false, false);
+      const bool ident_on = kEpi == kEpiTma && a.ident != 0;
+      const uint64_t id_desc[2] = {tc::smem_desc(tc::smem_u32(ident), 16u, 256u, 6u),
+                                   tc::smem_desc(tc::smem_u32(ident + 512), 16u, 256u, 6u)};
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, ++it) {
         const int b = it & 1;
         const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
+        int mb, ti, tj;
+        tile_coords(a, t, mb, ti, tj);
         if (!tc::mbar_wait(tempty + b, tph ^ 1u, a.err)) {
           ok = false;
           break;
@@ -562,6 +592,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t bd = a.b_mn_major ? tc::smem_desc_sw128(bbase + 2048u * kk, kBoxMN, 1024u)
                                              : tc::smem_desc_sw128(bbase + 32u * kk, 16u, 1024u);
             tc::umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          const int c0 = kb * BK - tj * BN;  // accumulator column of this k-block's first k
+          if (ident_on && c0 >= 0 && c0 < BN) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = tc::smem_desc_sw128(abase + 32u * kk, 16u, 1024u);
+              tc::umma_bf16(d + static_cast<uint32_t>(c0 + 16 * kk), ad, id_desc[0], idesc16, 1u);
+              tc::umma_bf16(d + static_cast<uint32_t>(c0 + 16 * kk), ad, id_desc[1], idesc16, 1u);
+            }
           }
           tc::umma_commit(empty + s);  // the stage is free once these MMAs have read it
           if (++s == S) {
@@ -1181,6 +1220,17 @@ zopt_status error_word(int** host, int** dev) {
 
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
 
+// A finite float rounded to the nearest bf16 (ties to even), as a float.
+float bf16_round(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  u &= 0xFFFF0000u;
+  float r;
+  std::memcpy(&r, &u, 4);
+  return r;
+}
+
 // Workspace: a header (per-matrix reduction scratch and stats), then one region per matrix of
 // the group holding X0, X1 (m x ldx), A and B (m x lda) in the compute dtype (es bytes).
 struct Plan {
@@ -1461,6 +1511,12 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     ZOPT_CUDA_TRY(cudaGetLastError());
 
     const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
+    // b / c as a sum of two bf16 values, for B' on single CTAs
+    const double bc = abc[2] != 0.0f ? static_cast<double>(abc[1]) / static_cast<double>(abc[2]) : 0.0;
+    const float h1 = bf16_round(static_cast<float>(bc));
+    const float h2 = bf16_round(static_cast<float>(bc - static_cast<double>(h1)));
+    const bool id_ok = abc[2] != 0.0f && std::isfinite(bc) && std::isfinite(h1) && std::isfinite(h2) &&
+                       std::fabs(bc) < 1e30;
     // products with m >= 1024 run on CTA pairs; below that the single-CTA kernel's twice as
     // many tiles keep more SMs busy
     const bool pair = m >= 1024;
@@ -1513,14 +1569,22 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
         if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], nullptr, &ma_e, kEpiTma, ga, s)
                        : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, kEpiTma, ga, s)) != ZOPT_OK)
           return st;
-        // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X
+        // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X.
+        // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
+        // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
         ga.K = m;
         ga.alpha = abc[2]; ga.beta = abc[1]; ga.diag = abc[0];
         ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
         ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-        if ((st = pair ? launch_gemm_pair(ma_p, ma_p, &ma_e, &mb_e, kEpiTmaR, ga, s)
-                       : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, kEpiTmaR, ga, s)) != ZOPT_OK)
-          return st;
+        if (!pair && id_ok) {
+          GemmArgs gi = ga;
+          gi.beta = 0.0f; gi.R = nullptr; gi.ident = 1; gi.h1 = h1; gi.h2 = h2;
+          st = launch_gemm(ma_p, ma_q, nullptr, &mb_e, kEpiTma, gi, s);
+        } else {
+          st = pair ? launch_gemm_pair(ma_p, ma_p, &ma_e, &mb_e, kEpiTmaR, ga, s)
+                    : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, kEpiTmaR, ga, s);
+        }
+        if (st != ZOPT_OK) return st;
         // X = B' X
         ga.M = m; ga.N = n; ga.K = m;
         ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f;
