@@ -446,6 +446,24 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
   }
 }
 
+// The two 16 x 16 identity tiles (h1, h2) of the B' product, written by the whole block: element
+// (n, k) = h if n == k, as the 32-byte swizzle lays it out (row n at 32 (n % 8) + 256 (n / 8),
+// its 16-byte halves swapped when bit 2 of n is set).
+__device__ __forceinline__ void init_identity(uint8_t* ident, float h1, float h2) {
+  for (int w = threadIdx.x; w < kIdentBytes / 4; w += blockDim.x) {
+    uint32_t word = 0;
+    for (int e = 0; e < 2; ++e) {
+      const int byte = 4 * w + 2 * e;
+      const int h = byte / 512, bt = byte % 512;
+      const int n = (bt / 256) * 8 + (bt % 256) / 32;
+      const int k = ((((bt % 32) / 16) ^ ((n >> 2) & 1)) * 8) + (bt % 16) / 2;
+      if (n == k) word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(h ? h2 : h1))) << (16 * e);
+    }
+    *reinterpret_cast<uint32_t*>(ident + 4 * w) = word;
+  }
+  tc::fence_proxy_async_smem();  // the MMAs read the tiles through the async proxy
+}
+
 // The single-CTA persistent GEMM with the epilogue kEpi (kEpiRegs, kEpiTmaR or kEpiTma). The TMA
 // epilogues store D, and a symmetric product's mirror, through tmD (32 x 32 boxes, 64-byte
 // swizzle; D a bf16 row-major matrix the TMA can address); kEpiTmaR reads R through tmR (the same
@@ -473,22 +491,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* ident = reinterpret_cast<uint8_t*>(full) + 256;  // kEpiTma (256-byte aligned)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (kEpi == kEpiTma && a.ident) {
-    // tile h (h1, h2): element (n, k) = h if n == k, as the 32-byte swizzle lays it out: row n at
-    // 32 (n % 8) + 256 (n / 8), its 16-byte halves swapped when bit 2 of n is set
-    for (int w = threadIdx.x; w < kIdentBytes / 4; w += blockDim.x) {
-      uint32_t word = 0;
-      for (int e = 0; e < 2; ++e) {
-        const int byte = 4 * w + 2 * e;
-        const int h = byte / 512, bt = byte % 512;
-        const int n = (bt / 256) * 8 + (bt % 256) / 32;
-        const int k = ((((bt % 32) / 16) ^ ((n >> 2) & 1)) * 8) + (bt % 16) / 2;
-        if (n == k) word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(h ? a.h2 : a.h1))) << (16 * e);
-      }
-      *reinterpret_cast<uint32_t*>(ident + 4 * w) = word;
-    }
-    tc::fence_proxy_async_smem();  // the MMAs read the tiles through the async proxy
-  }
+  if (kEpi == kEpiTma && a.ident) init_identity(ident, a.h1, a.h2);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(full + s, 1);
@@ -1161,6 +1164,304 @@ __global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restric
   }
 }
 
+// ---------------------------------------------------------------------- fused call
+//
+// Below the pair threshold every product of every step of a call can run in one persistent
+// launch of the single-CTA machinery (four-stage ring, TMA epilogue, B' by identity MMAs). Its
+// work list is step-major, then product (X X', B', B'X), then matrix, then tile; CTA c takes
+// items c, c + G, c + 2G, ... Before loading an item, the TMA thread waits until the product
+// the item reads is complete for its matrix: each epilogue warp adds one to its matrix's counter
+// for that product once its stores of an item have landed (release), and the waiter's acquire
+// load is followed by a proxy fence before its TMA loads. An item depends only on earlier items
+// and every CTA is resident (one per SM, a grid no larger than the SM count), so the list always
+// progresses; each wait is bounded like the barrier waits.
+constexpr int kFusedProducts = 4;  // X X', B', B'X, and B'X of the last step (the caller's X)
+constexpr int kCntWord = 16;       // counters at word 16 of each matrix's prep scratch header
+
+struct FusedMaps {
+  CUtensorMap xp[2], xq[2], xmn[2], xe[2];  // X (either buffer): operand boxes, epilogue boxes
+  CUtensorMap ap, aq, ae, bp, be, oe;       // A, B' and the caller's X
+};
+
+struct FusedArgs {
+  GemmArgs prod[kFusedProducts];
+  int steps;
+  int n_item[3];       // items per step of each product (all matrices of the group)
+  int per_step;        // n_item[0] + n_item[1] + n_item[2]
+  uint8_t* prep;       // per-matrix prep scratch (kPrepWsBytes apart); counters at kCntWord
+  int* err;
+};
+
+struct Item {
+  int s, p, mb, ti, tj;
+};
+
+__device__ __forceinline__ Item fused_item(const FusedArgs& f, int t) {
+  Item it;
+  it.s = t / f.per_step;
+  int r = t - it.s * f.per_step;
+  it.p = 0;
+  if (r >= f.n_item[0]) {
+    r -= f.n_item[0];
+    it.p = 1;
+    if (r >= f.n_item[1]) {
+      r -= f.n_item[1];
+      it.p = 2;
+    }
+  }
+  tile_coords(f.prod[it.p], r, it.mb, it.ti, it.tj);
+  return it;
+}
+
+__device__ __forceinline__ const GemmArgs& fused_args(const FusedArgs& f, const Item& it) {
+  return f.prod[it.p == 2 && it.s == f.steps - 1 ? 3 : it.p];
+}
+
+__device__ __forceinline__ uint32_t* fused_counter(const FusedArgs& f, int mb, int p) {
+  return reinterpret_cast<uint32_t*>(f.prep + static_cast<size_t>(mb) * kPrepWsBytes) + kCntWord + p;
+}
+
+// The count the item's input product must reach for its matrix (0: nothing to wait for). Each
+// item of a product is counted once by each of the four epilogue warps of its CTA.
+__device__ __forceinline__ uint32_t fused_need(const FusedArgs& f, const Item& it, int& dep) {
+  if (it.p == 0) {  // X X' of step s reads the X that step s - 1 wrote
+    dep = 2;
+    return static_cast<uint32_t>(4 * it.s * f.prod[2].tiles_per_mat);
+  }
+  dep = it.p - 1;  // B' reads A, B'X reads B' (and X, complete before A started)
+  return static_cast<uint32_t>(4 * (it.s + 1) * f.prod[dep].tiles_per_mat);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait (bounded) until *c >= target; then order the caller's later TMA loads after it.
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, int* err) {
+  if (ld_acquire(c) < target) {
+    const unsigned long long t0 = tc::globaltimer();
+    for (uint32_t spin = 1;; ++spin) {
+      __nanosleep(32);
+      if (ld_acquire(c) >= target) break;
+      if ((spin & 15u) == 0) {
+        const unsigned long long el = tc::globaltimer() - t0;
+        if (el > 1000000ull && *reinterpret_cast<volatile int*>(err) != 0) return false;
+        if (el > tc::kWaitLimitNs) {
+          atomicExch(err, 1);
+          return false;
+        }
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ns_fused_kernel(const __grid_constant__ FusedMaps mp, const FusedArgs f) {
+  constexpr int S = STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * kTileA;
+  uint8_t* sEpi = sB + S * kTileB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + epi_bytes(kEpiTma));
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint8_t* ident = reinterpret_cast<uint8_t*>(full) + 256;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = f.steps * f.per_step;
+  init_identity(ident, f.prod[1].h1, f.prod[1].h2);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tfull + b, 1);
+      tc::mbar_init(tempty + b, 128);
+    }
+    tc::mbar_init(drain, 1);
+    tc::fence_mbar_init();
+    for (int q = 0; q < 2; ++q) {
+      tc::prefetch_tmap(&mp.xp[q]);
+      tc::prefetch_tmap(&mp.xq[q]);
+      tc::prefetch_tmap(&mp.xmn[q]);
+      tc::prefetch_tmap(&mp.xe[q]);
+    }
+    tc::prefetch_tmap(&mp.ap);
+    tc::prefetch_tmap(&mp.aq);
+    tc::prefetch_tmap(&mp.ae);
+    tc::prefetch_tmap(&mp.bp);
+    tc::prefetch_tmap(&mp.be);
+    tc::prefetch_tmap(&mp.oe);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();  // X0 (the normalised input) is complete and visible
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int armed[S];
+      for (int q = 0; q < S; ++q) armed[q] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Item it = fused_item(f, t);
+        const GemmArgs& a = fused_args(f, it);
+        int dep = 0;
+        const uint32_t need = fused_need(f, it, dep);
+        if (need > 0 && !wait_count(fused_counter(f, it.mb, dep), need, f.err)) {
+          ok = false;
+          break;
+        }
+        const int cur = it.s & 1;
+        const CUtensorMap* P = it.p == 0 ? &mp.xp[cur] : (it.p == 1 ? &mp.ap : &mp.bp);
+        const CUtensorMap* Q = it.p == 0 ? &mp.xq[cur] : (it.p == 1 ? &mp.aq : &mp.xmn[cur]);
+        const int nk = (a.K + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(empty + s, ph ^ 1u, f.err)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(full + s, kTileA + kTileB);
+          armed[s] = static_cast<int>(ph);
+          tc::tma_load_3d(sA + s * kTileA, P, full + s, kb * BK, it.ti * BM, it.mb);
+          if (!a.b_mn_major) {
+            tc::tma_load_3d(sB + s * kTileB, Q, full + s, kb * BK, it.tj * BN, it.mb);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tc::tma_load_3d(sB + s * kTileB + q * kBoxMN, Q, full + s, it.tj * BN + 64 * q, kb * BK, it.mb);
+          }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // leave no copy in flight: wait (bounded) for every stage armed last
+        for (int q = 0; q < S; ++q)
+          if (armed[q] >= 0) mbar_wait_drain(full + q, static_cast<uint32_t>(armed[q]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint32_t idesc_k = tc::idesc_bf16_f32(BM, BN, false, false);
+      const uint32_t idesc_mn = tc::idesc_bf16_f32(BM, BN, false, true);
+      const uint32_t idesc16 = tc::idesc_bf16_f32(BM, 16, false, false);
+      const uint64_t id_desc[2] = {tc::smem_desc(tc::smem_u32(ident), 16u, 256u, 6u),
+                                   tc::smem_desc(tc::smem_u32(ident + 512), 16u, 256u, 6u)};
+      int s = 0, n = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++n) {
+        const Item it = fused_item(f, t);
+        const GemmArgs& a = fused_args(f, it);
+        const int b = n & 1;
+        const uint32_t tph = static_cast<uint32_t>(n >> 1) & 1u;
+        if (!tc::mbar_wait(tempty + b, tph ^ 1u, f.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+        const bool mn = a.b_mn_major != 0;
+        const bool ident_on = a.ident != 0;
+        const int nk = (a.K + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(full + s, ph, f.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t abase = tc::smem_u32(sA + s * kTileA);
+          const uint32_t bbase = tc::smem_u32(sB + s * kTileB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(abase + 32u * kk, 16u, 1024u);
+            const uint64_t bd = mn ? tc::smem_desc_sw128(bbase + 2048u * kk, kBoxMN, 1024u)
+                                   : tc::smem_desc_sw128(bbase + 32u * kk, 16u, 1024u);
+            tc::umma_bf16(d, ad, bd, mn ? idesc_mn : idesc_k, (kb | kk) != 0 ? 1u : 0u);
+          }
+          const int c0 = kb * BK - it.tj * BN;
+          if (ident_on && c0 >= 0 && c0 < BN) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = tc::smem_desc_sw128(abase + 32u * kk, 16u, 1024u);
+              tc::umma_bf16(d + static_cast<uint32_t>(c0 + 16 * kk), ad, id_desc[0], idesc16, 1u);
+              tc::umma_bf16(d + static_cast<uint32_t>(c0 + 16 * kk), ad, id_desc[1], idesc16, 1u);
+            }
+          }
+          tc::umma_commit(empty + s);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit(tfull + b);
+      }
+      tc::umma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
+    const int quad = warp & 3;
+    uint8_t* mine = sEpi + quad * (epi_bytes(kEpiTma) / 4);
+    int last_par = -1;
+    int n = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++n) {
+      const Item it = fused_item(f, t);
+      const GemmArgs& a = fused_args(f, it);
+      const int b = n & 1;
+      const uint32_t tph = static_cast<uint32_t>(n >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, f.err) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      tc::fence_after_sync();
+      const int cur = it.s & 1;
+      const CUtensorMap* D = it.p == 0 ? &mp.ae
+                                       : (it.p == 1 ? &mp.be : (it.s == f.steps - 1 ? &mp.oe : &mp.xe[cur ^ 1]));
+      epi_tile_tma<false>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
+                          it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par);
+      tc::fence_before_sync();
+      tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
+      if (lane == 0) {
+        // this warp's part of the item has landed: count it for the item's matrix and product
+        tc::bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(fused_counter(f, it.mb, it.p)) : "memory");
+      }
+      __syncwarp();
+    }
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1322,6 +1623,24 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, const C
                     stream, P, Q, P, *D, a);
 }
 
+// The single-CTA kernel's tiles of a product (128 x 256; a symmetric product only those that
+// touch the upper triangle). False if the group has 2^31 tiles or more.
+bool tiles_1cta(GemmArgs& a) {
+  a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
+  a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+  long long per = 0;
+  if (a.symmetric) {
+    for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r / 2;
+  } else {
+    per = static_cast<long long>(a.tiles_m) * a.tiles_n;
+  }
+  const long long total = per * a.group;
+  if (total < 1 || total > 0x7FFFFFFFLL) return false;
+  a.tiles_per_mat = static_cast<int>(per);
+  a.num_tiles = static_cast<int>(total);
+  return true;
+}
+
 // The single-CTA kernel with epilogue `epi`: kEpiTmaR reads R through *R, the TMA epilogues store
 // D through *D (32 x 32 boxes, 64-byte swizzle).
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
@@ -1336,18 +1655,7 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtens
                                        smem_bytes(kEpiTma)));
     attr_set = true;
   }
-  a.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
-  a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
-  long long per = 0;
-  if (a.symmetric) {
-    for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r / 2;
-  } else {
-    per = static_cast<long long>(a.tiles_m) * a.tiles_n;
-  }
-  const long long total = per * a.group;
-  if (total < 1 || total > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
-  a.tiles_per_mat = static_cast<int>(per);
-  a.num_tiles = static_cast<int>(total);
+  if (!tiles_1cta(a)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
@@ -1363,6 +1671,34 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtens
                       static_cast<size_t>(smem_bytes(kEpiTmaR)), stream, P, Q, R != nullptr ? *R : P, *D, a);
   return launch_pdl(gemm_bf16_kernel<kEpiTma>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
                     stream, P, Q, P, *D, a);
+}
+
+
+// One launch of the fused kernel for every step of a group (see ns_fused_kernel): prod[0..3]
+// hold X X', B', B'X and the last step's B'X with everything but their tile counts.
+zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    ZOPT_CUDA_TRY(cudaFuncSetAttribute(ns_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes(kEpiTma)));
+    attr_set = true;
+  }
+  for (int q = 0; q < kFusedProducts; ++q)
+    if (!tiles_1cta(f.prod[q])) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+  long long per_step = 0;
+  for (int q = 0; q < 3; ++q) {
+    f.n_item[q] = f.prod[q].num_tiles;
+    per_step += f.prod[q].num_tiles;
+  }
+  if (f.prod[3].num_tiles != f.n_item[2] || per_step * f.steps > 0x7FFFFFFFLL)
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+  f.per_step = static_cast<int>(per_step);
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
+  const long long total = per_step * f.steps;
+  const int grid = total < sms ? static_cast<int>(total) : sms;
+  return launch_pdl(ns_fused_kernel, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
+                    stream, maps, f);
 }
 
 }  // namespace ns
@@ -1533,6 +1869,35 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
       if ((st = make_map(&mo_e, xo, xcols, xrows, ld_x, gs, ob, 32, 32,
                          of32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, of32)) != ZOPT_OK)
         return st;
+    }
+    // every product of every step in one persistent launch when each can use it
+    if (!f32c && !pair && out_tma && id_ok) {
+      FusedMaps fm;
+      for (int q = 0; q < 2; ++q) {
+        fm.xp[q] = mx_p[q];
+        fm.xq[q] = mx_q[q];
+        fm.xmn[q] = mx_mn[q];
+        fm.xe[q] = mx_e[q];
+      }
+      fm.ap = ma_p; fm.aq = ma_q; fm.ae = ma_e; fm.bp = mb_p; fm.be = mb_e; fm.oe = mo_e;
+      FusedArgs fa{};
+      fa.steps = steps;
+      fa.prep = ws;
+      fa.err = err_dev;
+      GemmArgs g0{};
+      g0.group = gs; g0.err = err_dev; g0.alpha = 1.0f;
+      GemmArgs& pa = fa.prod[0];  // A = X X'
+      pa = g0; pa.M = m; pa.N = m; pa.K = n; pa.symmetric = 1;
+      GemmArgs& pb = fa.prod[1];  // B' = c A A' + b A + a I (b A by identity MMAs)
+      pb = g0; pb.M = m; pb.N = m; pb.K = m; pb.symmetric = 1;
+      pb.alpha = abc[2]; pb.diag = abc[0]; pb.ident = 1; pb.h1 = h1; pb.h2 = h2;
+      GemmArgs& px = fa.prod[2];  // X = B' X
+      px = g0; px.M = m; px.N = n; px.K = m; px.b_mn_major = 1;
+      fa.prod[3] = px;            // the last step's, into the caller's X
+      fa.prod[3].d_f32 = io_dtype == ZOPT_F32 ? 1 : 0;
+      fa.prod[3].d_trans = transpose ? 1 : 0;
+      if ((st = launch_fused(fm, fa, s)) != ZOPT_OK) return st;
+      continue;
     }
     int cur = 0;
     for (int it = 0; it < steps; ++it) {
