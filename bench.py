@@ -6,7 +6,7 @@ One step = the whole hot path over one batch of synthetic input:
     producing the norm / clip / found_inf stats (zopt_grad_accumulate), then the fused AdamW
     update with bf16 round-out (zopt_adamw_step);
   * Muon's Newton-Schulz (5 steps, bf16) on the stress set of 48 whole matrices: 16 each of
-    4096x4096, 4096x14336 and 14336x4096 (zopt_ns_orthogonalize, one batched call per shape).
+    4096x4096, 4096x14336 and 14336x4096 (zopt_ns_orthogonalize_many, one call over the shapes).
 Inputs are resident in HBM and far larger than L2 (~13 GB touched per step), so no L2 flush
 is needed between steps. `value` is the AdamW part's HBM throughput (66 algorithmic bytes per
 shard element: 36 for the accumulation, 30 for the update, / the part's time); `ns.value` the
@@ -203,7 +203,7 @@ def run_reference(args, rank: int) -> None:
 
 
 class NsPart:
-    """The Newton-Schulz stress set: bf16 matrices of three shapes, one batched call per shape."""
+    """A Newton-Schulz set (the stress set or the GPT-2-small body): bf16 matrices, one call over all shapes."""
 
     def __init__(self, Z, torch, seed: int, steps: int, count_limit: int = 0, which: str = "c5"):
         import workloads
@@ -226,15 +226,20 @@ class NsPart:
                 G *= 1e-3  # gradient-like scale
             G = G.to(torch.bfloat16)
             self.groups.append((G, torch.empty_like(G)))
-        # room for a whole shape group, so each product of a step is one launch over the group
-        self.ws = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], G.shape[0]) for G, _ in self.groups),
-                              dtype=torch.uint8, device="cuda")
+        # one call over every shape (zopt_ns_orthogonalize_many): each shape's whole batch is one
+        # group; shapes below 1024 share persistent fused launches (six to a launch)
+        self.ws = Z.new_ns_workspace_many([(G.shape[1], G.shape[2], G.shape[0]) for G, _ in self.groups])
+        # the end-to-end pass calls zopt_ns_orthogonalize on chunks of up to 4 matrices
+        self.ws_chunk = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], min(4, G.shape[0]))
+                                        for G, _ in self.groups), dtype=torch.uint8, device="cuda")
         self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
-        self.launches = sum(2 + 3 * steps for _ in self.groups)  # one launch per product per group
+        fused = sum(1 for G, _ in self.groups if min(G.shape[1], G.shape[2]) < 1024)
+        # per shape: norm + normalise/orient; then one fused launch per six small shapes, or
+        # three products per step for the large ones
+        self.launches = 2 * len(self.groups) + -(-fused // 6) + 3 * steps * (len(self.groups) - fused)
 
     def run(self, stream):
-        for G, X in self.groups:
-            self.Z.ns_orthogonalize(G, X, self.ws, steps=self.steps, stream=stream)
+        self.Z.ns_orthogonalize_many(self.groups, self.ws, steps=self.steps, stream=stream)
 
 
 def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
@@ -410,7 +415,7 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
             for ci, (G, X, hG, hX) in enumerate(chunks):
                 stream.wait_event(landed[ci])
                 stream.wait_event(out_done[ci])  # the previous step's X has been read back
-                Z.ns_orthogonalize(G, X, ns.ws, steps=ns.steps, stream=stream)
+                Z.ns_orthogonalize(G, X, ns.ws_chunk, steps=ns.steps, stream=stream)
                 ns_done[ci].record(stream)
                 d2h_s.wait_event(ns_done[ci])
                 with torch.cuda.stream(d2h_s):

@@ -265,6 +265,35 @@ ZOPT_API zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io
                                            int32_t steps, const float* abc, float eps, void* d_ws, size_t ws_bytes,
                                            zopt_stream stream);
 
+/* One shape's matrices for zopt_ns_orthogonalize_many: `batch` matrices G[b] -> X[b], rows x
+ * cols, with the meaning zopt_ns_orthogonalize gives its arguments (io_dtype a zopt_dtype;
+ * batch at most 65535). 72 bytes. */
+typedef struct zopt_ns_job {
+  const void* G;
+  void* X;
+  int64_t rows, cols;
+  int64_t ld_g, ld_x;
+  int64_t batch_stride_g, batch_stride_x;
+  int32_t batch;
+  int32_t io_dtype;
+} zopt_ns_job;
+
+/* Workspace bytes for zopt_ns_orthogonalize_many over these jobs (0 if a job is empty or has
+ * more than 65535 matrices): each job's zopt_ns_workspace(rows, cols, batch, ZOPT_BF16),
+ * rounded up to 1 KiB, summed. */
+ZOPT_API size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs);
+/* Orthogonalise every matrix of every job: `steps` quintic steps with coefficients abc and
+ * eps as for zopt_ns_orthogonalize, bf16 compute. Each result is bitwise the one
+ * zopt_ns_orthogonalize gives with a workspace that holds the job's whole batch. Jobs whose
+ * shorter side is below 1024 and whose output rows are 16-byte aligned run in one persistent
+ * launch per six jobs, the products of each step interleaved across jobs (one job's waits for
+ * its previous product are filled by the other jobs' tiles); the others run product by product.
+ * jobs is read during the call only; d_ws (16-byte aligned) is owned by the call until the
+ * stream passes it. Same errors as zopt_ns_orthogonalize. */
+ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
+                                                const float* abc, float eps, void* d_ws, size_t ws_bytes,
+                                                zopt_stream stream);
+
 /* Device-side failure reporting. Every wait of the tensor-core kernels is bounded (4 s);
  * one that runs out records an error word in mapped host memory, drains the kernel's copies
  * and MMAs, frees its TMEM and returns, so the context stays usable; the next

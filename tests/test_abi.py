@@ -110,3 +110,37 @@ def test_device_calls_validate_before_launch():
     assert L.zopt_adamw_step(lay.handle, None, p, p, p, p, 1, None, ctypes.byref(hp), None, p, None) == 1
     assert L.zopt_adamw_step(lay.handle, tab, ctypes.c_void_p(8), p, p, p, 1, None, ctypes.byref(hp), None, p,
                              None) == 1
+
+
+def test_ns_workspace_many_is_the_sum_of_rounded_single_workspaces():
+    shapes = [(768, 2304, 12), (768, 768, 12), (3072, 768, 12), (130, 70, 1), (4096, 4096, 3)]
+    want = sum(-(-Z.ns_workspace(r, c, b) // 1024) * 1024 for r, c, b in shapes)
+    assert Z.ns_workspace_many(shapes) == want
+    assert Z.ns_workspace_many([(0, 5, 1)]) == 0
+    assert Z.ns_workspace_many([(5, 5, 65536)]) == 0
+    assert Z.lib().zopt_ns_workspace_many(None, 0) == 0
+
+
+def test_ns_orthogonalize_many_validates_before_launch():
+    """Each call fails validation before any CUDA work (the pointers are fake)."""
+    L = Z.lib()
+    coef = (ctypes.c_float * 3)(*Z.DEFAULT_ABC)
+    ws = ctypes.c_void_p(1 << 20)
+    job = Z._NsJob(ctypes.c_void_p(1 << 16), ctypes.c_void_p(1 << 18), 64, 128, 128, 128, 0, 0, 1, Z.BF16)
+    arr = (Z._NsJob * 1)(job)
+    big = 1 << 40
+    assert L.zopt_ns_orthogonalize_many(arr, 0, 5, coef, 1e-7, ws, big, None) == 1
+    assert L.zopt_ns_orthogonalize_many(None, 1, 5, coef, 1e-7, ws, big, None) == 1
+    assert L.zopt_ns_orthogonalize_many(arr, 1, 0, coef, 1e-7, ws, big, None) == 1
+    assert L.zopt_ns_orthogonalize_many(arr, 1, 5, coef, 1e-7, ctypes.c_void_p((1 << 20) + 8), big, None) == 1
+    assert b"aligned" in L.zopt_last_error()
+    assert L.zopt_ns_orthogonalize_many(arr, 1, 5, coef, 1e-7, ws, 1024, None) == 1
+    assert b"workspace" in L.zopt_last_error()
+    bad = (Z._NsJob * 2)(job, Z._NsJob(ctypes.c_void_p(1 << 16), ctypes.c_void_p(1 << 18), 64, 128, 100, 128, 0, 0,
+                                       1, Z.BF16))
+    assert L.zopt_ns_orthogonalize_many(bad, 2, 5, coef, 1e-7, ws, big, None) == 1
+    assert b"leading dimension" in L.zopt_last_error()
+    f16 = (Z._NsJob * 1)(Z._NsJob(ctypes.c_void_p(1 << 16), ctypes.c_void_p(1 << 18), 64, 128, 128, 128, 0, 0, 1, 9))
+    assert L.zopt_ns_orthogonalize_many(f16, 1, 5, coef, 1e-7, ws, big, None) == 2
+    nan = (ctypes.c_float * 3)(float("nan"), 1.0, 1.0)
+    assert L.zopt_ns_orthogonalize_many(arr, 1, 5, nan, 1e-7, ws, big, None) == 1

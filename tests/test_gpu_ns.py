@@ -298,3 +298,30 @@ def test_fp32_compute_with_bf16_io(zopt):
     torch.cuda.synchronize()
     ref = newton_schulz(G.double().cpu().numpy(), steps=5)
     assert rel(X.cpu(), torch.from_numpy(ref)) <= 4e-3  # one bf16 rounding of the output
+
+
+def test_many_jobs_equal_single_calls(zopt):
+    """zopt_ns_orthogonalize_many over jobs of different shapes, dtypes and orientations: seven
+    fused jobs (two launches: six, then one), CTA-pair matrices and an output the TMA cannot
+    address (both product by product). Each job's result is bitwise zopt_ns_orthogonalize's
+    with a workspace holding its whole batch, and one is checked against the oracle."""
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    specs = [(12, 768, 2304, torch.bfloat16, 0), (5, 768, 768, torch.bfloat16, 0), (3, 1000, 300, torch.float32, 0),
+             (2, 130, 70, torch.bfloat16, 0), (1, 256, 512, torch.bfloat16, 0), (2, 64, 64, torch.float32, 0),
+             (1, 17, 100, torch.bfloat16, 0), (2, 1100, 1300, torch.bfloat16, 0), (1, 300, 1000, torch.bfloat16, 3)]
+    pairs, shapes = [], []
+    for b, r, c, dt, pad in specs:
+        G = torch.randn(b, r, c, generator=gen, device="cuda").to(dt)
+        X = torch.zeros(b, r, c + pad, device="cuda", dtype=dt)[:, :, :c]
+        pairs.append((G, X))
+        shapes.append((r, c, b))
+    ws = zopt.new_ns_workspace_many(shapes)
+    zopt.ns_orthogonalize_many(pairs, ws, steps=5)
+    torch.cuda.synchronize()
+    for (G, X), (r, c, b) in zip(pairs, shapes):
+        one = torch.empty(b, r, c, device="cuda", dtype=G.dtype)
+        zopt.ns_orthogonalize(G, one, zopt.new_ns_workspace(r, c, b), steps=5)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X), (r, c, b)
+    ref = newton_schulz(pairs[2][0][1].double().cpu().numpy(), steps=5)
+    assert rel(pairs[2][1][1].cpu(), torch.from_numpy(ref)) <= 2e-2

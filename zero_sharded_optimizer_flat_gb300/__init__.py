@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
                                                  ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
                                                  vp, sz, vp]),
+        "zopt_ns_workspace_many": (sz, [ctypes.POINTER(_NsJob), i32]),
+        "zopt_ns_orthogonalize_many": (ctypes.c_int, [ctypes.POINTER(_NsJob), i32, i32,
+                                                      ctypes.POINTER(ctypes.c_float), ctypes.c_float, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -314,6 +317,48 @@ def new_ns_workspace(rows: int, cols: int, group: int = 1, compute=BF16, device=
     """A workspace for processing ``group`` matrices of this shape per launch."""
     import torch
     return torch.empty(max(ns_workspace(rows, cols, group, compute), 16), dtype=torch.uint8, device=device)
+
+
+class _NsJob(ctypes.Structure):
+    """``zopt_ns_job``: one shape's matrices for ``zopt_ns_orthogonalize_many``."""
+    _fields_ = [("G", ctypes.c_void_p), ("X", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ld_g", ctypes.c_int64), ("ld_x", ctypes.c_int64), ("batch_stride_g", ctypes.c_int64),
+                ("batch_stride_x", ctypes.c_int64), ("batch", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+
+
+def _ns_job(G, X) -> _NsJob:
+    if G.dim() == 2:
+        batch, rows, cols = 1, G.shape[0], G.shape[1]
+        ldg, ldx, sg, sx = G.stride(0), X.stride(0), 0, 0
+    else:
+        batch, rows, cols = G.shape
+        ldg, ldx, sg, sx = G.stride(1), X.stride(1), G.stride(0), X.stride(0)
+    if G.stride(-1) != 1 or X.stride(-1) != 1 or G.dtype != X.dtype or X.shape != G.shape:
+        raise ValueError("G and X must have the same shape and dtype, with a contiguous last dimension")
+    return _NsJob(_ptr(G), _ptr(X), rows, cols, ldg, ldx, sg, sx, batch, _dtype_code(G))
+
+
+def _shape_job(rows: int, cols: int, batch: int) -> _NsJob:
+    return _NsJob(None, None, int(rows), int(cols), int(cols), int(cols), 0, 0, int(batch), BF16)
+
+
+def ns_workspace_many(shapes) -> int:
+    """``zopt_ns_workspace_many`` for jobs of the given (rows, cols, batch)."""
+    arr = (_NsJob * len(shapes))(*[_shape_job(*sh) for sh in shapes])
+    return int(lib().zopt_ns_workspace_many(arr, len(shapes)))
+
+
+def new_ns_workspace_many(shapes, device="cuda"):
+    import torch
+    return torch.empty(max(ns_workspace_many(shapes), 16), dtype=torch.uint8, device=device)
+
+
+def ns_orthogonalize_many(pairs, ws, steps: int = 5, abc=DEFAULT_ABC, eps: float = 1e-7, stream=None) -> None:
+    """``zopt_ns_orthogonalize_many`` over [(G, X), ...]: each a 2-D matrix or a batch [b, rows, cols]."""
+    arr = (_NsJob * len(pairs))(*[_ns_job(G, X) for G, X in pairs])
+    coef = (ctypes.c_float * 3)(*[float(c) for c in abc])
+    _check(lib().zopt_ns_orthogonalize_many(arr, len(pairs), int(steps), coef, float(eps), _ptr(ws), ws.numel(),
+                                            _stream(stream)))
 
 
 def ns_orthogonalize(G, X, ws, steps: int = 5, abc=DEFAULT_ABC, eps: float = 1e-7, compute=BF16, stream=None) -> None:

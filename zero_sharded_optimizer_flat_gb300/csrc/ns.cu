@@ -35,7 +35,9 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <string>
 #include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "norm_impl.cuh"
@@ -1166,59 +1168,66 @@ __global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restric
 
 // ---------------------------------------------------------------------- fused call
 //
-// Below the pair threshold every product of every step of a call can run in one persistent
-// launch of the single-CTA machinery (four-stage ring, TMA epilogue, B' by identity MMAs). Its
-// work list is step-major, then product (X X', B', B'X), then matrix, then tile; CTA c takes
-// items c, c + G, c + 2G, ... Before loading an item, the TMA thread waits until the product
-// the item reads is complete for its matrix: each epilogue warp adds one to its matrix's counter
-// for that product once its stores of an item have landed (release), and the waiter's acquire
-// load is followed by a proxy fence before its TMA loads. An item depends only on earlier items
-// and every CTA is resident (one per SM, a grid no larger than the SM count), so the list always
+// Below the pair threshold every product of every step of a call (and of up to kMaxFusedJobs
+// jobs of different shapes) can run in one persistent launch of the single-CTA machinery
+// (four-stage ring, TMA epilogue, B' by identity MMAs). Its work list is step-major, then
+// product (X X', B', B'X), then job, then matrix, then tile; CTA c takes items c, c + G, c + 2G,
+// ... Before loading an item, the TMA thread waits until the product the item reads is complete
+// for its matrix: each epilogue warp adds one to its matrix's counter for that product once its
+// stores of an item have landed (release), and the waiter's acquire load is followed by a proxy
+// fence before its TMA loads. Between an item and its input lie the items of the other jobs, so
+// one job's waits are filled by another's tiles. An item depends only on earlier items and
+// every CTA is resident (one per SM, a grid no larger than the SM count), so the list always
 // progresses; each wait is bounded like the barrier waits.
 constexpr int kFusedProducts = 4;  // X X', B', B'X, and B'X of the last step (the caller's X)
 constexpr int kCntWord = 16;       // counters at word 16 of each matrix's prep scratch header
+constexpr int kMaxFusedJobs = 6;
 
-struct FusedMaps {
+struct FusedJobMaps {
   CUtensorMap xp[2], xq[2], xmn[2], xe[2];  // X (either buffer): operand boxes, epilogue boxes
   CUtensorMap ap, aq, ae, bp, be, oe;       // A, B' and the caller's X
 };
+struct FusedMaps {
+  FusedJobMaps job[kMaxFusedJobs];
+};
+
+struct FusedJob {
+  GemmArgs prod[kFusedProducts];
+  uint8_t* prep;  // per-matrix prep scratch (kPrepWsBytes apart); counters at kCntWord
+};
 
 struct FusedArgs {
-  GemmArgs prod[kFusedProducts];
+  FusedJob job[kMaxFusedJobs];
+  int n_jobs;
   int steps;
-  int n_item[3];       // items per step of each product (all matrices of the group)
-  int per_step;        // n_item[0] + n_item[1] + n_item[2]
-  uint8_t* prep;       // per-matrix prep scratch (kPrepWsBytes apart); counters at kCntWord
+  int per_step;                   // items of one step (all products, jobs, matrices)
+  int off[3][kMaxFusedJobs + 1];  // within a step, product p's items of job j start at off[p][j]
   int* err;
 };
 
+static_assert(sizeof(FusedMaps) + sizeof(FusedArgs) <= 32000, "the fused kernel's parameters fit a launch");
+
 struct Item {
-  int s, p, mb, ti, tj;
+  int s, p, j, mb, ti, tj;
 };
 
 __device__ __forceinline__ Item fused_item(const FusedArgs& f, int t) {
   Item it;
   it.s = t / f.per_step;
-  int r = t - it.s * f.per_step;
-  it.p = 0;
-  if (r >= f.n_item[0]) {
-    r -= f.n_item[0];
-    it.p = 1;
-    if (r >= f.n_item[1]) {
-      r -= f.n_item[1];
-      it.p = 2;
-    }
-  }
-  tile_coords(f.prod[it.p], r, it.mb, it.ti, it.tj);
+  const int r = t - it.s * f.per_step;
+  it.p = r < f.off[0][f.n_jobs] ? 0 : (r < f.off[1][f.n_jobs] ? 1 : 2);
+  it.j = 0;
+  while (it.j + 1 < f.n_jobs && r >= f.off[it.p][it.j + 1]) ++it.j;
+  tile_coords(f.job[it.j].prod[it.p], r - f.off[it.p][it.j], it.mb, it.ti, it.tj);
   return it;
 }
 
 __device__ __forceinline__ const GemmArgs& fused_args(const FusedArgs& f, const Item& it) {
-  return f.prod[it.p == 2 && it.s == f.steps - 1 ? 3 : it.p];
+  return f.job[it.j].prod[it.p == 2 && it.s == f.steps - 1 ? 3 : it.p];
 }
 
-__device__ __forceinline__ uint32_t* fused_counter(const FusedArgs& f, int mb, int p) {
-  return reinterpret_cast<uint32_t*>(f.prep + static_cast<size_t>(mb) * kPrepWsBytes) + kCntWord + p;
+__device__ __forceinline__ uint32_t* fused_counter(const FusedArgs& f, int j, int mb, int p) {
+  return reinterpret_cast<uint32_t*>(f.job[j].prep + static_cast<size_t>(mb) * kPrepWsBytes) + kCntWord + p;
 }
 
 // The count the item's input product must reach for its matrix (0: nothing to wait for). Each
@@ -1226,10 +1235,10 @@ __device__ __forceinline__ uint32_t* fused_counter(const FusedArgs& f, int mb, i
 __device__ __forceinline__ uint32_t fused_need(const FusedArgs& f, const Item& it, int& dep) {
   if (it.p == 0) {  // X X' of step s reads the X that step s - 1 wrote
     dep = 2;
-    return static_cast<uint32_t>(4 * it.s * f.prod[2].tiles_per_mat);
+    return static_cast<uint32_t>(4 * it.s * f.job[it.j].prod[2].tiles_per_mat);
   }
   dep = it.p - 1;  // B' reads A, B'X reads B' (and X, complete before A started)
-  return static_cast<uint32_t>(4 * (it.s + 1) * f.prod[dep].tiles_per_mat);
+  return static_cast<uint32_t>(4 * (it.s + 1) * f.job[it.j].prod[dep].tiles_per_mat);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -1277,7 +1286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = f.steps * f.per_step;
-  init_identity(ident, f.prod[1].h1, f.prod[1].h2);
+  init_identity(ident, f.job[0].prod[1].h1, f.job[0].prod[1].h2);  // every job has the call's b / c
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(full + s, 1);
@@ -1289,18 +1298,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
-    for (int q = 0; q < 2; ++q) {
-      tc::prefetch_tmap(&mp.xp[q]);
-      tc::prefetch_tmap(&mp.xq[q]);
-      tc::prefetch_tmap(&mp.xmn[q]);
-      tc::prefetch_tmap(&mp.xe[q]);
+    for (int j = 0; j < f.n_jobs; ++j) {
+      const FusedJobMaps& m = mp.job[j];
+      for (int q = 0; q < 2; ++q) {
+        tc::prefetch_tmap(&m.xp[q]);
+        tc::prefetch_tmap(&m.xq[q]);
+        tc::prefetch_tmap(&m.xmn[q]);
+        tc::prefetch_tmap(&m.xe[q]);
+      }
+      tc::prefetch_tmap(&m.ap);
+      tc::prefetch_tmap(&m.aq);
+      tc::prefetch_tmap(&m.ae);
+      tc::prefetch_tmap(&m.bp);
+      tc::prefetch_tmap(&m.be);
+      tc::prefetch_tmap(&m.oe);
     }
-    tc::prefetch_tmap(&mp.ap);
-    tc::prefetch_tmap(&mp.aq);
-    tc::prefetch_tmap(&mp.ae);
-    tc::prefetch_tmap(&mp.bp);
-    tc::prefetch_tmap(&mp.be);
-    tc::prefetch_tmap(&mp.oe);
   }
   if (warp == 1) {
     tc::tmem_alloc(tslot, kTmemCols);
@@ -1326,13 +1338,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const GemmArgs& a = fused_args(f, it);
         int dep = 0;
         const uint32_t need = fused_need(f, it, dep);
-        if (need > 0 && !wait_count(fused_counter(f, it.mb, dep), need, f.err)) {
+        if (need > 0 && !wait_count(fused_counter(f, it.j, it.mb, dep), need, f.err)) {
           ok = false;
           break;
         }
         const int cur = it.s & 1;
-        const CUtensorMap* P = it.p == 0 ? &mp.xp[cur] : (it.p == 1 ? &mp.ap : &mp.bp);
-        const CUtensorMap* Q = it.p == 0 ? &mp.xq[cur] : (it.p == 1 ? &mp.aq : &mp.xmn[cur]);
+        const FusedJobMaps& m = mp.job[it.j];
+        const CUtensorMap* P = it.p == 0 ? &m.xp[cur] : (it.p == 1 ? &m.ap : &m.bp);
+        const CUtensorMap* Q = it.p == 0 ? &m.xq[cur] : (it.p == 1 ? &m.aq : &m.xmn[cur]);
         const int nk = (a.K + BK - 1) / BK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty + s, ph ^ 1u, f.err)) {
@@ -1437,8 +1450,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       tc::fence_after_sync();
       const int cur = it.s & 1;
-      const CUtensorMap* D = it.p == 0 ? &mp.ae
-                                       : (it.p == 1 ? &mp.be : (it.s == f.steps - 1 ? &mp.oe : &mp.xe[cur ^ 1]));
+      const FusedJobMaps& m = mp.job[it.j];
+      const CUtensorMap* D = it.p == 0 ? &m.ae : (it.p == 1 ? &m.be : (it.s == f.steps - 1 ? &m.oe : &m.xe[cur ^ 1]));
       epi_tile_tma<false>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
                           it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par);
       tc::fence_before_sync();
@@ -1447,7 +1460,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // this warp's part of the item has landed: count it for the item's matrix and product
         tc::bulk_wait_all();
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(fused_counter(f, it.mb, it.p)) : "memory");
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(fused_counter(f, it.j, it.mb, it.p))
+                     : "memory");
       }
       __syncwarp();
     }
@@ -1674,8 +1688,9 @@ zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtens
 }
 
 
-// One launch of the fused kernel for every step of a group (see ns_fused_kernel): prod[0..3]
-// hold X X', B', B'X and the last step's B'X with everything but their tile counts.
+// One launch of the fused kernel for every step of f.n_jobs groups (see ns_fused_kernel): each
+// job's prod[0..3] hold X X', B', B'X and the last step's B'X with everything but their tile
+// counts.
 zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -1683,22 +1698,304 @@ zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream
                                        smem_bytes(kEpiTma)));
     attr_set = true;
   }
-  for (int q = 0; q < kFusedProducts; ++q)
-    if (!tiles_1cta(f.prod[q])) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
-  long long per_step = 0;
-  for (int q = 0; q < 3; ++q) {
-    f.n_item[q] = f.prod[q].num_tiles;
-    per_step += f.prod[q].num_tiles;
+  if (f.n_jobs < 1 || f.n_jobs > kMaxFusedJobs) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: job count");
+  long long at = 0;
+  for (int p = 0; p < 3; ++p) {
+    for (int j = 0; j < f.n_jobs; ++j) {
+      if (p == 0)
+        for (int q = 0; q < kFusedProducts; ++q)
+          if (!tiles_1cta(f.job[j].prod[q])) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+      if (at > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+      f.off[p][j] = static_cast<int>(at);
+      at += f.job[j].prod[p].num_tiles;
+    }
+    f.off[p][f.n_jobs] = static_cast<int>(at);
   }
-  if (f.prod[3].num_tiles != f.n_item[2] || per_step * f.steps > 0x7FFFFFFFLL)
-    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
-  f.per_step = static_cast<int>(per_step);
+  if (at * f.steps > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+  f.per_step = static_cast<int>(at);
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
-  const long long total = per_step * f.steps;
+  const long long total = at * f.steps;
   const int grid = total < sms ? static_cast<int>(total) : sms;
   return launch_pdl(ns_fused_kernel, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
                     stream, maps, f);
+}
+
+// The call's coefficients: (a, b, c) and b / c split into two bf16 values for B' on single CTAs.
+struct Coef {
+  float a, b, c, h1, h2;
+  bool id_ok;  // the identity MMAs can carry b A (c != 0, b / c representable)
+};
+
+Coef coef_of(const float* abc) {
+  Coef k;
+  k.a = abc[0];
+  k.b = abc[1];
+  k.c = abc[2];
+  const double bc = k.c != 0.0f ? static_cast<double>(k.b) / static_cast<double>(k.c) : 0.0;
+  k.h1 = bf16_round(static_cast<float>(bc));
+  k.h2 = bf16_round(static_cast<float>(bc - static_cast<double>(k.h1)));
+  k.id_ok = k.c != 0.0f && std::isfinite(bc) && std::isfinite(k.h1) && std::isfinite(k.h2) && std::fabs(bc) < 1e30;
+  return k;
+}
+
+// One group of gs same-shape matrices: the caller's matrices, the workspace regions and the
+// tensor maps over them.
+struct Group {
+  const uint8_t* g;  // the group's first input and output matrix
+  uint8_t* xo;
+  zopt_dtype io;
+  long long rows, cols, ld_g, ld_x, bs_g, bs_x;
+  int gs;
+  bool f32c, transpose, pair, out_tma;
+  long long es, mat_elems;
+  size_t esz;
+  Plan p;
+  uint8_t* ws;  // prep scratch of the group (its matrices' counters live there)
+  zopt_clip_stats* stats;
+  uint8_t *xb[2], *A, *B;
+  CUtensorMap mx_p[2], mx_q[2], mx_mn[2], mx_e[2], ma_p, ma_q, mb_p, ma_e, mb_e, mo_e;
+};
+
+// Fill the derived fields and encode the maps of a group whose workspace is at ws (plan p).
+zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
+  zopt_status st = ZOPT_OK;
+  G.p = p;
+  G.es = G.f32c ? 4 : 2;
+  G.esz = G.io == ZOPT_F32 ? 4 : 2;
+  G.transpose = G.rows > G.cols;
+  G.pair = p.m >= 1024;
+  G.ws = ws;
+  G.stats = reinterpret_cast<zopt_clip_stats*>(ws + p.off_stats);
+  uint8_t* mat0 = ws + p.header;  // matrix 0's region; matrix b at + b * per_mat
+  G.xb[0] = mat0;
+  G.xb[1] = mat0 + p.off_x1;
+  G.A = mat0 + p.off_a;
+  G.B = mat0 + p.off_b;
+  G.mat_elems = static_cast<long long>(p.per_mat) / G.es;
+  // the last product writes the caller's X through the TMA (32 x 32 boxes, transposed for a
+  // tall matrix) when the TMA can address it: 16-byte aligned rows and matrices
+  const long long esz = static_cast<long long>(G.esz);
+  G.out_tma = !G.f32c && (reinterpret_cast<uintptr_t>(G.xo) & 15u) == 0 && (G.ld_x * esz) % 16 == 0 &&
+              (G.gs == 1 || (G.bs_x * esz) % 16 == 0);
+  if (G.f32c) return ok();
+  const long long mb = static_cast<long long>(p.per_mat), grp = p.group;
+  for (int q = 0; q < 2; ++q) {
+    if ((st = make_map(&G.mx_p[q], G.xb[q], p.n, p.m, p.ldx, grp, mb, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&G.mx_q[q], G.xb[q], p.n, p.m, p.ldx, grp, mb, 64, BN)) != ZOPT_OK) return st;
+    if ((st = make_map(&G.mx_mn[q], G.xb[q], p.n, p.m, p.ldx, grp, mb, 64, BK)) != ZOPT_OK) return st;
+    if ((st = make_map(&G.mx_e[q], G.xb[q], p.n, p.m, p.ldx, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK)
+      return st;
+  }
+  if ((st = make_map(&G.ma_p, G.A, p.m, p.m, p.lda, grp, mb, 64, BM)) != ZOPT_OK) return st;
+  if ((st = make_map(&G.ma_q, G.A, p.m, p.m, p.lda, grp, mb, 64, BN)) != ZOPT_OK) return st;
+  if ((st = make_map(&G.mb_p, G.B, p.m, p.m, p.lda, grp, mb, 64, BM)) != ZOPT_OK) return st;
+  if ((st = make_map(&G.ma_e, G.A, p.m, p.m, p.lda, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+  if ((st = make_map(&G.mb_e, G.B, p.m, p.m, p.lda, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+  if (G.out_tma) {
+    const long long xrows = G.transpose ? p.n : p.m, xcols = G.transpose ? p.m : p.n;  // the caller's shape
+    const long long ob = (G.gs == 1 ? xrows * G.ld_x : G.bs_x) * esz;
+    const bool of32 = G.io == ZOPT_F32;
+    if ((st = make_map(&G.mo_e, G.xo, xcols, xrows, G.ld_x, G.gs, ob, 32, 32,
+                       of32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, of32)) != ZOPT_OK)
+      return st;
+  }
+  return ok();
+}
+
+// X0 = G / (||G||_F + eps), oriented, for every matrix of the group (its prep scratch, and so
+// its counters, zeroed first).
+zopt_status group_prep(const Group& G, float eps, int sms, cudaStream_t s) {
+  zopt_status st = ZOPT_OK;
+  const long long rows = G.rows, cols = G.cols, ld_g = G.ld_g, bs_g = G.bs_g;
+  const size_t esz = G.esz;
+  const int gs = G.gs;
+  ZOPT_CUDA_TRY(cudaMemsetAsync(G.ws, 0, static_cast<size_t>(gs) * kPrepWsBytes, s));
+  const bool aligned = (reinterpret_cast<uintptr_t>(G.g) & 15u) == 0 && (bs_g * esz) % 16 == 0;
+  const int flat = (aligned && ld_g == cols) ? 1 : 0;
+  const int vec_rows = (aligned && (ld_g * esz) % 16 == 0) ? 1 : 0;
+  // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
+  // is bitwise the same whatever group it runs in
+  long long bpm = (rows * cols + 8191) / 8192;  // short per-thread chains for small matrices
+  bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
+  const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
+  st = G.io == ZOPT_F32
+           ? launch_pdl(group_sumsq_kernel<float>, sg, dim3(kNormThreads), 0, s, reinterpret_cast<const float*>(G.g),
+                        rows, cols, ld_g, bs_g, flat, vec_rows, G.ws, G.stats)
+           : launch_pdl(group_sumsq_kernel<__nv_bfloat16>, sg, dim3(kNormThreads), 0, s,
+                        reinterpret_cast<const __nv_bfloat16*>(G.g), rows, cols, ld_g, bs_g, flat, vec_rows, G.ws,
+                        G.stats);
+  if (st != ZOPT_OK) return st;
+  int sblk = (sms * 8 + gs - 1) / gs;
+  sblk = sblk < 1 ? 1 : sblk;
+  const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
+  const zopt_clip_stats* stats = G.stats;
+  if (!G.transpose) {
+    const int vec = (aligned && (ld_g * esz) % 16 == 0 && cols % 8 == 0) ? 1 : 0;
+#define ZOPT_SCALE(TI, TO)                                                                                 \
+  st = launch_pdl(group_scale_kernel<TI, TO>, sgrid, dim3(256), 0, s, reinterpret_cast<const TI*>(G.g), rows, \
+                  cols, ld_g, bs_g, vec, stats, static_cast<double>(eps), reinterpret_cast<TO*>(G.xb[0]),       \
+                  G.p.ldx, G.mat_elems)
+    if (G.io == ZOPT_F32 && G.f32c) ZOPT_SCALE(float, float);
+    else if (G.io == ZOPT_F32) ZOPT_SCALE(float, __nv_bfloat16);
+    else if (G.f32c) ZOPT_SCALE(__nv_bfloat16, float);
+    else ZOPT_SCALE(__nv_bfloat16, __nv_bfloat16);
+#undef ZOPT_SCALE
+  } else {
+    const int pair = ((reinterpret_cast<uintptr_t>(G.g) % (2 * esz)) == 0 && ld_g % 2 == 0 && bs_g % 2 == 0) ? 1 : 0;
+    const dim3 tb(32, 8);
+#define ZOPT_TRANSPOSE(TI, TO)                                                                            \
+  st = launch_pdl(group_transpose_kernel<TI, TO>, sgrid, tb, 0, s, reinterpret_cast<const TI*>(G.g), rows,   \
+                  cols, ld_g, bs_g, pair, stats, static_cast<double>(eps), reinterpret_cast<TO*>(G.xb[0]),     \
+                  G.p.ldx, G.mat_elems)
+    if (G.io == ZOPT_F32 && G.f32c) ZOPT_TRANSPOSE(float, float);
+    else if (G.io == ZOPT_F32) ZOPT_TRANSPOSE(float, __nv_bfloat16);
+    else if (G.f32c) ZOPT_TRANSPOSE(__nv_bfloat16, float);
+    else ZOPT_TRANSPOSE(__nv_bfloat16, __nv_bfloat16);
+#undef ZOPT_TRANSPOSE
+  }
+  if (st != ZOPT_OK) return st;
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+// Whether every product of the group can run in the fused kernel.
+bool group_fusable(const Group& G, const Coef& k) { return !G.f32c && !G.pair && G.out_tma && k.id_ok; }
+
+// The group as one job of the fused kernel.
+void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobMaps& m) {
+  for (int q = 0; q < 2; ++q) {
+    m.xp[q] = G.mx_p[q];
+    m.xq[q] = G.mx_q[q];
+    m.xmn[q] = G.mx_mn[q];
+    m.xe[q] = G.mx_e[q];
+  }
+  m.ap = G.ma_p;
+  m.aq = G.ma_q;
+  m.ae = G.ma_e;
+  m.bp = G.mb_p;
+  m.be = G.mb_e;
+  m.oe = G.mo_e;
+  const int mm = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n);
+  GemmArgs g0{};
+  g0.group = G.gs;
+  g0.err = err;
+  g0.alpha = 1.0f;
+  GemmArgs& pa = job.prod[0];  // A = X X'
+  pa = g0;
+  pa.M = mm; pa.N = mm; pa.K = n; pa.symmetric = 1;
+  GemmArgs& pb = job.prod[1];  // B' = c A A' + b A + a I (b A by identity MMAs)
+  pb = g0;
+  pb.M = mm; pb.N = mm; pb.K = mm; pb.symmetric = 1;
+  pb.alpha = k.c; pb.diag = k.a; pb.ident = 1; pb.h1 = k.h1; pb.h2 = k.h2;
+  GemmArgs& px = job.prod[2];  // X = B' X
+  px = g0;
+  px.M = mm; px.N = n; px.K = mm; px.b_mn_major = 1;
+  job.prod[3] = px;  // the last step's, into the caller's X
+  job.prod[3].d_f32 = G.io == ZOPT_F32 ? 1 : 0;
+  job.prod[3].d_trans = G.transpose ? 1 : 0;
+  job.prep = G.ws;
+}
+
+// The group's products one launch at a time (the fp32 mode, the CTA-pair kernel, outputs the
+// TMA cannot address).
+zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, cudaStream_t s) {
+  zopt_status st = ZOPT_OK;
+  const int m = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n), gs = G.gs;
+  const long long mat_elems = G.mat_elems;
+  const Plan& p = G.p;
+  const bool pair = G.pair;
+  int cur = 0;
+  for (int it = 0; it < steps; ++it) {
+    const bool last = it == steps - 1;
+    void* xnext = last ? static_cast<void*>(G.xo) : static_cast<void*>(G.xb[cur ^ 1]);
+    const long long ldnext = last ? G.ld_x : p.ldx;
+    const long long dstr_next = last ? G.bs_x : mat_elems;
+    const int next_f32 = last ? (G.io == ZOPT_F32 ? 1 : 0) : (G.f32c ? 1 : 0);
+    const int next_trans = last && G.transpose ? 1 : 0;
+    if (G.f32c) {
+      float* X0 = reinterpret_cast<float*>(G.xb[cur]);
+      float* Af = reinterpret_cast<float*>(G.A);
+      float* Bf = reinterpret_cast<float*>(G.B);
+      // A = X X'
+      GemmF32Args fa{m, m, n, gs, X0, p.ldx, mat_elems, X0, p.ldx, mat_elems, 0, 1, 1.0f, 0.0f, nullptr, 0, 0,
+                     Af, p.lda, mat_elems, 1, 0};
+      if ((st = launch_gemm_f32(fa, s)) != ZOPT_OK) return st;
+      // B = c A A' + b A
+      GemmF32Args fb{m, m, m, gs, Af, p.lda, mat_elems, Af, p.lda, mat_elems, 0, 1, k.c, k.b, Af, p.lda,
+                     mat_elems, Bf, p.lda, mat_elems, 1, 0};
+      if ((st = launch_gemm_f32(fb, s)) != ZOPT_OK) return st;
+      // X = B X + a X
+      GemmF32Args fx{m, n, m, gs, Bf, p.lda, mat_elems, X0, p.ldx, mat_elems, 1, 0, 1.0f, k.a, X0, p.ldx,
+                     mat_elems, xnext, ldnext, dstr_next, next_f32, next_trans};
+      if ((st = launch_gemm_f32(fx, s)) != ZOPT_OK) return st;
+    } else {
+      GemmArgs ga{};
+      ga.err = err;
+      ga.group = gs;
+      // A = X X'
+      ga.M = m; ga.N = m; ga.K = n;
+      ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
+      ga.ldr = 0; ga.r_stride = 0; ga.D = G.A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
+      if ((st = pair ? launch_gemm_pair(G.mx_p[cur], G.mx_p[cur], nullptr, &G.ma_e, kEpiTma, ga, s)
+                     : launch_gemm(G.mx_p[cur], G.mx_q[cur], nullptr, &G.ma_e, kEpiTma, ga, s)) != ZOPT_OK)
+        return st;
+      // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X.
+      // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
+      // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
+      ga.K = m;
+      ga.alpha = k.c; ga.beta = k.b; ga.diag = k.a;
+      ga.R = reinterpret_cast<const __nv_bfloat16*>(G.A); ga.ldr = p.lda; ga.r_stride = mat_elems;
+      ga.D = G.B; ga.ldd = p.lda; ga.d_stride = mat_elems;
+      if (!pair && k.id_ok) {
+        GemmArgs gi = ga;
+        gi.beta = 0.0f; gi.R = nullptr; gi.ident = 1; gi.h1 = k.h1; gi.h2 = k.h2;
+        st = launch_gemm(G.ma_p, G.ma_q, nullptr, &G.mb_e, kEpiTma, gi, s);
+      } else {
+        st = pair ? launch_gemm_pair(G.ma_p, G.ma_p, &G.ma_e, &G.mb_e, kEpiTmaR, ga, s)
+                  : launch_gemm(G.ma_p, G.ma_q, &G.ma_e, &G.mb_e, kEpiTmaR, ga, s);
+      }
+      if (st != ZOPT_OK) return st;
+      // X = B' X
+      ga.M = m; ga.N = n; ga.K = m;
+      ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f;
+      ga.R = nullptr; ga.ldr = 0; ga.r_stride = 0;
+      ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
+      const int x_epi = (!last || G.out_tma) ? kEpiTma : kEpiRegs;
+      const CUtensorMap* xd = last ? &G.mo_e : &G.mx_e[cur ^ 1];
+      if ((st = pair ? launch_gemm_pair(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)
+                     : launch_gemm(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)) != ZOPT_OK)
+        return st;
+    }
+    cur ^= 1;
+  }
+  return ok();
+}
+
+// The error word, reporting (and clearing) a timeout of an earlier call.
+zopt_status take_error_word(const char* fn, int** dev) {
+  int* h = nullptr;
+  zopt_status st = error_word(&h, dev);
+  if (st != ZOPT_OK) return st;
+  if (*reinterpret_cast<volatile int*>(h) != 0) {
+    *reinterpret_cast<volatile int*>(h) = 0;
+    return fail(ZOPT_ETIMEOUT, std::string(fn) + ": a tensor-core kernel of an earlier call timed out on a wait");
+  }
+  return ok();
+}
+
+// The checks shared by both entry points for one shape's arguments.
+zopt_status check_job(const char* fn, const void* G, const void* X, zopt_dtype io, long long rows, long long cols,
+                      long long ld_g, long long ld_x, long long bs_g, long long bs_x, long long batch) {
+  const std::string f(fn);
+  if (G == nullptr || X == nullptr) return fail(ZOPT_EINVAL, f + ": NULL pointer");
+  if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, f + ": empty matrix or batch");
+  if (rows > (1LL << 31) || cols > (1LL << 31)) return fail(ZOPT_EINVAL, f + ": dimension >= 2^31");
+  if (ld_g < cols || ld_x < cols) return fail(ZOPT_EINVAL, f + ": leading dimension < cols");
+  if (batch > 1 && (bs_g < rows * ld_g || bs_x < rows * ld_x))
+    return fail(ZOPT_EINVAL, f + ": batch strides overlap the matrices");
+  if (io != ZOPT_F32 && io != ZOPT_BF16) return fail(ZOPT_EUNSUPPORTED, f + ": input/output dtype must be fp32 or bf16");
+  return ok();
 }
 
 }  // namespace ns
@@ -1716,16 +2013,11 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
                                              size_t ws_bytes, zopt_stream stream) {
   using namespace zopt;
   using namespace zopt::ns;
-  if (G == nullptr || X == nullptr || d_ws == nullptr || abc == nullptr)
-    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: NULL pointer");
-  if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: empty matrix or batch");
-  if (rows > (1LL << 31) || cols > (1LL << 31)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: dimension >= 2^31");
-  if (ld_g < cols || ld_x < cols) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: leading dimension < cols");
-  if (batch > 1 && (batch_stride_g < rows * ld_g || batch_stride_x < rows * ld_x))
-    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: batch strides overlap the matrices");
+  const char* fn = "zopt_ns_orthogonalize";
+  if (d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: NULL pointer");
+  zopt_status st = check_job(fn, G, X, io_dtype, rows, cols, ld_g, ld_x, batch_stride_g, batch_stride_x, batch);
+  if (st != ZOPT_OK) return st;
   if (steps < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: steps < 1");
-  if (io_dtype != ZOPT_F32 && io_dtype != ZOPT_BF16)
-    return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: input/output dtype must be fp32 or bf16");
   if (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)
     return fail(ZOPT_EUNSUPPORTED, "zopt_ns_orthogonalize: compute dtype must be bf16 or fp32");
   if (!std::isfinite(abc[0]) || !std::isfinite(abc[1]) || !std::isfinite(abc[2]) || !std::isfinite(eps) || eps < 0)
@@ -1746,222 +2038,120 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
   }
   if (group < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: workspace smaller than zopt_ns_workspace");
   const Plan p = plan(rows, cols, es, group);
-
-  int* err_host = nullptr;
   int* err_dev = nullptr;
-  zopt_status st = error_word(&err_host, &err_dev);
-  if (st != ZOPT_OK) return st;
-  if (*reinterpret_cast<volatile int*>(err_host) != 0) {
-    *reinterpret_cast<volatile int*>(err_host) = 0;
-    return fail(ZOPT_ETIMEOUT, "zopt_ns_orthogonalize: a tensor-core kernel of an earlier call timed out on a wait");
-  }
-
+  if ((st = take_error_word(fn, &err_dev)) != ZOPT_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(d_ws);
-  zopt_clip_stats* stats = reinterpret_cast<zopt_clip_stats*>(ws + p.off_stats);
-  uint8_t* mat0 = ws + p.header;  // matrix 0's region; matrix b at + b * per_mat
-  uint8_t* xb[2] = {mat0, mat0 + p.off_x1};
-  uint8_t* A = mat0 + p.off_a;
-  uint8_t* B = mat0 + p.off_b;
-  const long long mat_elems = static_cast<long long>(p.per_mat) / es;  // elements between matrices
-  const bool transpose = rows > cols;
-
-  // Tensor maps over the group's workspace matrices (bf16 tensor-core path only).
-  CUtensorMap mx_p[2], mx_q[2], mx_mn[2], ma_p, ma_q, mb_p;
-  // the single-CTA kernel's epilogue boxes (R, D and mirrors): 32 x 32, 64-byte swizzle
-  CUtensorMap mx_e[2], ma_e, mb_e;
-  if (!f32c) {
-    const long long mb = static_cast<long long>(p.per_mat);
-    for (int q = 0; q < 2; ++q) {
-      if ((st = make_map(&mx_p[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BM)) != ZOPT_OK) return st;
-      if ((st = make_map(&mx_q[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BN)) != ZOPT_OK) return st;
-      if ((st = make_map(&mx_mn[q], xb[q], p.n, p.m, p.ldx, group, mb, 64, BK)) != ZOPT_OK) return st;
-      if ((st = make_map(&mx_e[q], xb[q], p.n, p.m, p.ldx, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK)
-        return st;
-    }
-    if ((st = make_map(&ma_p, A, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
-    if ((st = make_map(&ma_q, A, p.m, p.m, p.lda, group, mb, 64, BN)) != ZOPT_OK) return st;
-    if ((st = make_map(&mb_p, B, p.m, p.m, p.lda, group, mb, 64, BM)) != ZOPT_OK) return st;
-    if ((st = make_map(&ma_e, A, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
-    if ((st = make_map(&mb_e, B, p.m, p.m, p.lda, group, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
-  }
-
-  const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
+  const Coef k = coef_of(abc);
+  const size_t esz = io_dtype == ZOPT_F32 ? 4 : 2;
   for (long long g0i = 0; g0i < batch; g0i += group) {
-    const int gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
-    const uint8_t* g = static_cast<const uint8_t*>(G) + static_cast<size_t>(g0i) * batch_stride_g * esz;
-    uint8_t* xo = static_cast<uint8_t*>(X) + static_cast<size_t>(g0i) * batch_stride_x * esz;
-
-    // X0 = G / (||G||_F + eps), oriented, for every matrix of the group
-    ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, static_cast<size_t>(gs) * kPrepWsBytes, s));
-    const bool aligned = (reinterpret_cast<uintptr_t>(g) & 15u) == 0 && (batch_stride_g * esz) % 16 == 0;
-    const int flat = (aligned && ld_g == cols) ? 1 : 0;
-    const int vec_rows = (aligned && (ld_g * esz) % 16 == 0) ? 1 : 0;
-    // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
-    // is bitwise the same whatever group it runs in
-    long long bpm = (rows * cols + 8191) / 8192;  // short per-thread chains for small matrices
-    bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
-    const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
-    st = io_dtype == ZOPT_F32
-             ? launch_pdl(group_sumsq_kernel<float>, sg, dim3(kNormThreads), 0, s, reinterpret_cast<const float*>(g),
-                          static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g),
-                          static_cast<long long>(batch_stride_g), flat, vec_rows, ws, stats)
-             : launch_pdl(group_sumsq_kernel<__nv_bfloat16>, sg, dim3(kNormThreads), 0, s,
-                          reinterpret_cast<const __nv_bfloat16*>(g), static_cast<long long>(rows),
-                          static_cast<long long>(cols), static_cast<long long>(ld_g),
-                          static_cast<long long>(batch_stride_g), flat, vec_rows, ws, stats);
-    if (st != ZOPT_OK) return st;
-    int sblk = (sms * 8 + gs - 1) / gs;
-    sblk = sblk < 1 ? 1 : sblk;
-    const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
-    if (!transpose) {
-      const int vec = (aligned && (ld_g * esz) % 16 == 0 && cols % 8 == 0) ? 1 : 0;
-#define ZOPT_SCALE(TI, TO)                                                                               \
-  st = launch_pdl(group_scale_kernel<TI, TO>, sgrid, dim3(256), 0, s, reinterpret_cast<const TI*>(g),    \
-                  static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g), \
-                  static_cast<long long>(batch_stride_g), vec, static_cast<const zopt_clip_stats*>(stats),  \
-                  static_cast<double>(eps), reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
-      if (io_dtype == ZOPT_F32 && f32c) ZOPT_SCALE(float, float);
-      else if (io_dtype == ZOPT_F32) ZOPT_SCALE(float, __nv_bfloat16);
-      else if (f32c) ZOPT_SCALE(__nv_bfloat16, float);
-      else ZOPT_SCALE(__nv_bfloat16, __nv_bfloat16);
-#undef ZOPT_SCALE
-    } else {
-      const int pair = ((reinterpret_cast<uintptr_t>(g) % (2 * esz)) == 0 && ld_g % 2 == 0 &&
-                        batch_stride_g % 2 == 0) ? 1 : 0;
-      const dim3 tb(32, 8);
-#define ZOPT_TRANSPOSE(TI, TO)                                                                            \
-  st = launch_pdl(group_transpose_kernel<TI, TO>, sgrid, tb, 0, s, reinterpret_cast<const TI*>(g),        \
-                  static_cast<long long>(rows), static_cast<long long>(cols), static_cast<long long>(ld_g), \
-                  static_cast<long long>(batch_stride_g), pair, static_cast<const zopt_clip_stats*>(stats), \
-                  static_cast<double>(eps), reinterpret_cast<TO*>(xb[0]), p.ldx, mat_elems)
-      if (io_dtype == ZOPT_F32 && f32c) ZOPT_TRANSPOSE(float, float);
-      else if (io_dtype == ZOPT_F32) ZOPT_TRANSPOSE(float, __nv_bfloat16);
-      else if (f32c) ZOPT_TRANSPOSE(__nv_bfloat16, float);
-      else ZOPT_TRANSPOSE(__nv_bfloat16, __nv_bfloat16);
-#undef ZOPT_TRANSPOSE
-    }
-    if (st != ZOPT_OK) return st;
-    ZOPT_CUDA_TRY(cudaGetLastError());
-
-    const int m = static_cast<int>(p.m), n = static_cast<int>(p.n);
-    // b / c as a sum of two bf16 values, for B' on single CTAs
-    const double bc = abc[2] != 0.0f ? static_cast<double>(abc[1]) / static_cast<double>(abc[2]) : 0.0;
-    const float h1 = bf16_round(static_cast<float>(bc));
-    const float h2 = bf16_round(static_cast<float>(bc - static_cast<double>(h1)));
-    const bool id_ok = abc[2] != 0.0f && std::isfinite(bc) && std::isfinite(h1) && std::isfinite(h2) &&
-                       std::fabs(bc) < 1e30;
-    // products with m >= 1024 run on CTA pairs; below that the single-CTA kernel's twice as
-    // many tiles keep more SMs busy
-    const bool pair = m >= 1024;
-    // the last product writes the caller's X through the TMA (32 x 32 boxes, transposed for a
-    // tall matrix) when the TMA can address it: 16-byte aligned rows and matrices
-    CUtensorMap mo_e;
-    const long long xrows = transpose ? p.n : p.m, xcols = transpose ? p.m : p.n;  // the caller's shape
-    const bool out_tma = !f32c && (reinterpret_cast<uintptr_t>(xo) & 15u) == 0 &&
-                         (ld_x * static_cast<long long>(esz)) % 16 == 0 &&
-                         (gs == 1 || (batch_stride_x * static_cast<long long>(esz)) % 16 == 0);
-    if (out_tma) {
-      const long long ob = (gs == 1 ? xrows * ld_x : batch_stride_x) * static_cast<long long>(esz);
-      const bool of32 = io_dtype == ZOPT_F32;
-      if ((st = make_map(&mo_e, xo, xcols, xrows, ld_x, gs, ob, 32, 32,
-                         of32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, of32)) != ZOPT_OK)
-        return st;
-    }
-    // every product of every step in one persistent launch when each can use it
-    if (!f32c && !pair && out_tma && id_ok) {
+    Group Gr;
+    Gr.g = static_cast<const uint8_t*>(G) + static_cast<size_t>(g0i) * batch_stride_g * esz;
+    Gr.xo = static_cast<uint8_t*>(X) + static_cast<size_t>(g0i) * batch_stride_x * esz;
+    Gr.io = io_dtype;
+    Gr.rows = rows; Gr.cols = cols; Gr.ld_g = ld_g; Gr.ld_x = ld_x; Gr.bs_g = batch_stride_g; Gr.bs_x = batch_stride_x;
+    Gr.gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
+    Gr.f32c = f32c;
+    if ((st = group_init(Gr, p, static_cast<uint8_t*>(d_ws))) != ZOPT_OK) return st;
+    if ((st = group_prep(Gr, eps, sms, s)) != ZOPT_OK) return st;
+    if (group_fusable(Gr, k)) {
+      // every product of every step in one persistent launch
       FusedMaps fm;
-      for (int q = 0; q < 2; ++q) {
-        fm.xp[q] = mx_p[q];
-        fm.xq[q] = mx_q[q];
-        fm.xmn[q] = mx_mn[q];
-        fm.xe[q] = mx_e[q];
-      }
-      fm.ap = ma_p; fm.aq = ma_q; fm.ae = ma_e; fm.bp = mb_p; fm.be = mb_e; fm.oe = mo_e;
       FusedArgs fa{};
+      fa.n_jobs = 1;
       fa.steps = steps;
-      fa.prep = ws;
       fa.err = err_dev;
-      GemmArgs g0{};
-      g0.group = gs; g0.err = err_dev; g0.alpha = 1.0f;
-      GemmArgs& pa = fa.prod[0];  // A = X X'
-      pa = g0; pa.M = m; pa.N = m; pa.K = n; pa.symmetric = 1;
-      GemmArgs& pb = fa.prod[1];  // B' = c A A' + b A + a I (b A by identity MMAs)
-      pb = g0; pb.M = m; pb.N = m; pb.K = m; pb.symmetric = 1;
-      pb.alpha = abc[2]; pb.diag = abc[0]; pb.ident = 1; pb.h1 = h1; pb.h2 = h2;
-      GemmArgs& px = fa.prod[2];  // X = B' X
-      px = g0; px.M = m; px.N = n; px.K = m; px.b_mn_major = 1;
-      fa.prod[3] = px;            // the last step's, into the caller's X
-      fa.prod[3].d_f32 = io_dtype == ZOPT_F32 ? 1 : 0;
-      fa.prod[3].d_trans = transpose ? 1 : 0;
+      group_job(Gr, k, err_dev, fa.job[0], fm.job[0]);
       if ((st = launch_fused(fm, fa, s)) != ZOPT_OK) return st;
-      continue;
+    } else if ((st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) {
+      return st;
     }
-    int cur = 0;
-    for (int it = 0; it < steps; ++it) {
-      const bool last = it == steps - 1;
-      void* xnext = last ? static_cast<void*>(xo) : static_cast<void*>(xb[cur ^ 1]);
-      const long long ldnext = last ? ld_x : p.ldx;
-      const long long dstr_next = last ? batch_stride_x : mat_elems;
-      const int next_f32 = last ? (io_dtype == ZOPT_F32 ? 1 : 0) : (f32c ? 1 : 0);
-      const int next_trans = last && transpose ? 1 : 0;
-      if (f32c) {
-        float* X0 = reinterpret_cast<float*>(xb[cur]);
-        float* Af = reinterpret_cast<float*>(A);
-        float* Bf = reinterpret_cast<float*>(B);
-        // A = X X'
-        GemmF32Args fa{m, m, n, gs, X0, p.ldx, mat_elems, X0, p.ldx, mat_elems, 0, 1, 1.0f, 0.0f, nullptr, 0, 0,
-                       Af, p.lda, mat_elems, 1, 0};
-        if ((st = launch_gemm_f32(fa, s)) != ZOPT_OK) return st;
-        // B = c A A' + b A
-        GemmF32Args fb{m, m, m, gs, Af, p.lda, mat_elems, Af, p.lda, mat_elems, 0, 1, abc[2], abc[1], Af, p.lda,
-                       mat_elems, Bf, p.lda, mat_elems, 1, 0};
-        if ((st = launch_gemm_f32(fb, s)) != ZOPT_OK) return st;
-        // X = B X + a X
-        GemmF32Args fx{m, n, m, gs, Bf, p.lda, mat_elems, X0, p.ldx, mat_elems, 1, 0, 1.0f, abc[0], X0, p.ldx,
-                       mat_elems, xnext, ldnext, dstr_next, next_f32, next_trans};
-        if ((st = launch_gemm_f32(fx, s)) != ZOPT_OK) return st;
-      } else {
-        GemmArgs ga{};
-        ga.err = err_dev;
-        ga.group = gs;
-        // A = X X'
-        ga.M = m; ga.N = m; ga.K = n;
-        ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
-        ga.ldr = 0; ga.r_stride = 0; ga.D = A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-        if ((st = pair ? launch_gemm_pair(mx_p[cur], mx_p[cur], nullptr, &ma_e, kEpiTma, ga, s)
-                       : launch_gemm(mx_p[cur], mx_q[cur], nullptr, &ma_e, kEpiTma, ga, s)) != ZOPT_OK)
-          return st;
-        // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X.
-        // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
-        // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
-        ga.K = m;
-        ga.alpha = abc[2]; ga.beta = abc[1]; ga.diag = abc[0];
-        ga.R = reinterpret_cast<const __nv_bfloat16*>(A); ga.ldr = p.lda; ga.r_stride = mat_elems;
-        ga.D = B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-        if (!pair && id_ok) {
-          GemmArgs gi = ga;
-          gi.beta = 0.0f; gi.R = nullptr; gi.ident = 1; gi.h1 = h1; gi.h2 = h2;
-          st = launch_gemm(ma_p, ma_q, nullptr, &mb_e, kEpiTma, gi, s);
-        } else {
-          st = pair ? launch_gemm_pair(ma_p, ma_p, &ma_e, &mb_e, kEpiTmaR, ga, s)
-                    : launch_gemm(ma_p, ma_q, &ma_e, &mb_e, kEpiTmaR, ga, s);
-        }
-        if (st != ZOPT_OK) return st;
-        // X = B' X
-        ga.M = m; ga.N = n; ga.K = m;
-        ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f;
-        ga.R = nullptr; ga.ldr = 0; ga.r_stride = 0;
-        ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
-        const int x_epi = (!last || out_tma) ? kEpiTma : kEpiRegs;
-        if ((st = pair ? launch_gemm_pair(mb_p, mx_mn[cur], nullptr, last ? &mo_e : &mx_e[cur ^ 1], x_epi, ga, s)
-                       : launch_gemm(mb_p, mx_mn[cur], nullptr, last ? &mo_e : &mx_e[cur ^ 1], x_epi, ga, s)) != ZOPT_OK)
-          return st;
-      }
-      cur ^= 1;
+  }
+  return ok();
+}
+
+static_assert(sizeof(zopt_ns_job) == 72, "zopt_ns_job layout");
+
+extern "C" size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs) {
+  if (jobs == nullptr || n_jobs < 1) return 0;
+  size_t total = 0;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const zopt_ns_job& b = jobs[j];
+    if (b.rows < 1 || b.cols < 1 || b.batch < 1 || b.batch > 65535) return 0;
+    total += static_cast<size_t>(zopt::ns::round_up(
+        static_cast<long long>(zopt::ns::plan(b.rows, b.cols, 2, b.batch).total), 1024));
+  }
+  return total;
+}
+
+extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
+                                                  const float* abc, float eps, void* d_ws, size_t ws_bytes,
+                                                  zopt_stream stream) {
+  using namespace zopt;
+  using namespace zopt::ns;
+  const char* fn = "zopt_ns_orthogonalize_many";
+  if (jobs == nullptr || d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: NULL pointer");
+  if (n_jobs < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: no jobs");
+  if (steps < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: steps < 1");
+  if (!std::isfinite(abc[0]) || !std::isfinite(abc[1]) || !std::isfinite(abc[2]) || !std::isfinite(eps) || eps < 0)
+    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: coefficients and eps must be finite (eps >= 0)");
+  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: workspace is not 16-byte aligned");
+  zopt_status st = ZOPT_OK;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const zopt_ns_job& b = jobs[j];
+    if ((st = check_job(fn, b.G, b.X, static_cast<zopt_dtype>(b.io_dtype), b.rows, b.cols, b.ld_g, b.ld_x,
+                        b.batch_stride_g, b.batch_stride_x, b.batch)) != ZOPT_OK)
+      return st;
+    if (b.batch > 65535) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: a job's batch exceeds 65535");
+  }
+  const size_t need = zopt_ns_workspace_many(jobs, n_jobs);
+  if (need == 0 || ws_bytes < need) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: workspace smaller than zopt_ns_workspace_many");
+  int* err_dev = nullptr;
+  if ((st = take_error_word(fn, &err_dev)) != ZOPT_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize_many: no CUDA device");
+  const Coef k = coef_of(abc);
+  // every job's whole batch is one group in its own slice of the workspace; all normalise first,
+  // then the fusable jobs go kMaxFusedJobs to a launch and the others run product by product
+  std::vector<Group> groups(static_cast<size_t>(n_jobs));
+  size_t at = 0;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const zopt_ns_job& b = jobs[j];
+    Group& Gr = groups[static_cast<size_t>(j)];
+    Gr.g = static_cast<const uint8_t*>(b.G);
+    Gr.xo = static_cast<uint8_t*>(b.X);
+    Gr.io = static_cast<zopt_dtype>(b.io_dtype);
+    Gr.rows = b.rows; Gr.cols = b.cols; Gr.ld_g = b.ld_g; Gr.ld_x = b.ld_x;
+    Gr.bs_g = b.batch_stride_g; Gr.bs_x = b.batch_stride_x;
+    Gr.gs = b.batch;
+    Gr.f32c = false;
+    const Plan p = plan(b.rows, b.cols, 2, b.batch);
+    if ((st = group_init(Gr, p, static_cast<uint8_t*>(d_ws) + at)) != ZOPT_OK) return st;
+    at += static_cast<size_t>(round_up(static_cast<long long>(p.total), 1024));
+    if ((st = group_prep(Gr, eps, sms, s)) != ZOPT_OK) return st;
+  }
+  FusedMaps fm;
+  FusedArgs fa{};
+  fa.steps = steps;
+  fa.err = err_dev;
+  for (int32_t j = 0; j <= n_jobs; ++j) {
+    const bool flush = fa.n_jobs == kMaxFusedJobs || (j == n_jobs && fa.n_jobs > 0);
+    if (flush) {
+      if ((st = launch_fused(fm, fa, s)) != ZOPT_OK) return st;
+      fa.n_jobs = 0;
     }
+    if (j == n_jobs) break;
+    const Group& Gr = groups[static_cast<size_t>(j)];
+    if (group_fusable(Gr, k)) {
+      group_job(Gr, k, err_dev, fa.job[fa.n_jobs], fm.job[fa.n_jobs]);
+      ++fa.n_jobs;
+    }
+  }
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const Group& Gr = groups[static_cast<size_t>(j)];
+    if (!group_fusable(Gr, k) && (st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) return st;
   }
   return ok();
 }
