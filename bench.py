@@ -237,6 +237,9 @@ class NsPart:
         # per shape: norm + normalise/orient; then one fused launch per six small shapes, or
         # three products per step for the large ones
         self.launches = 2 * len(self.groups) + -(-fused // 6) + 3 * steps * (len(self.groups) - fused)
+        names = (["ns_fused_kernel (X X', B', B'X of every step, shapes below 1024)"] if fused else []) + \
+                (["gemm_bf16_pair_kernel (X X', B', B'X on CTA pairs)"] if fused < len(self.groups) else [])
+        self.kernel = " + ".join(names)
 
     def run(self, stream):
         self.Z.ns_orthogonalize_many(self.groups, self.ws, steps=self.steps, stream=stream)
@@ -465,7 +468,7 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         tflops = ns.flops / (n_ms * 1e-3) / 1e12
         line["ns"] = {"value": round(tflops * world_procs, 2), "unit": "TFLOP/s", "ms_per_step": round(n_ms, 3),
                       "algorithmic_flops_per_step": ns.flops}
-        line["roofline"] = {"kernel": "gemm_bf16_kernel (X X', A A', B X)", "bound": "tensor",
+        line["roofline"] = {"kernel": ns.kernel, "bound": "tensor",
                             "achieved": round(tflops, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                             "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": None,
                             "peak_source": pk["source"] + " bf16 sustained (the GEMMs run for ~100 ms per step)",
