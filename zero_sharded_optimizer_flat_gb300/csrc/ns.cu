@@ -376,11 +376,14 @@ __device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap*
 // slice boxes at `mine` (D is written over it) and two mirror boxes follow; otherwise `mine`
 // holds four boxes, a D and a mirror box for even blocks and another pair for odd ones (an
 // fp32 box takes a pair). last_par: parity of the last block whose boxes went to the TMA.
-template <bool kSlice>
+// Blocks c_begin .. c_end - 1 of the tile; with one pair of boxes (kPairs == 1) every block
+// reuses the same D and mirror box.
+template <bool kSlice, int kPairs = 2>
 __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
-                                             int i0, int tj, int mb, bool has_r, int lane, int& last_par) {
+                                             int i0, int tj, int mb, bool has_r, int lane, int& last_par,
+                                             int c_begin = 0, int c_end = BN / 32) {
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     const int j0 = tj * BN + 32 * c;
     const int kind = block_kind(a, i0, j0);
     if (kind == 0 || kind == 4) continue;
@@ -390,7 +393,7 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
     float o[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
-    const int par = c & 1;
+    const int par = kPairs == 2 ? (c & 1) : 0;
     uint8_t* dbox = kSlice ? mine + c * kBox : mine + 2 * par * kBox;
     uint8_t* mbox = kSlice ? mine + (8 + par) * kBox : dbox + kBox;
     if (kSlice && has_r) {
@@ -1180,6 +1183,10 @@ __global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restric
 // every CTA is resident (one per SM, a grid no larger than the SM count), so the list always
 // progresses; each wait is bounded like the barrier waits.
 constexpr int kFusedProducts = 4;  // X X', B', B'X, and B'X of the last step (the caller's X)
+// warp 0 TMA, warp 1 MMA, warps 2..9 epilogue: two warps per TMEM lane quadrant, each draining
+// half of a tile's 32-column blocks through one D and one mirror box
+constexpr int kFusedEpiWarps = 8;
+constexpr int kFusedThreads = 32 * (2 + kFusedEpiWarps);
 constexpr int kCntWord = 16;       // counters at word 16 of each matrix's prep scratch header
 constexpr int kMaxFusedJobs = 6;
 
@@ -1231,14 +1238,14 @@ __device__ __forceinline__ uint32_t* fused_counter(const FusedArgs& f, int j, in
 }
 
 // The count the item's input product must reach for its matrix (0: nothing to wait for). Each
-// item of a product is counted once by each of the four epilogue warps of its CTA.
+// item of a product is counted once by each epilogue warp of its CTA.
 __device__ __forceinline__ uint32_t fused_need(const FusedArgs& f, const Item& it, int& dep) {
   if (it.p == 0) {  // X X' of step s reads the X that step s - 1 wrote
     dep = 2;
-    return static_cast<uint32_t>(4 * it.s * f.job[it.j].prod[2].tiles_per_mat);
+    return static_cast<uint32_t>(kFusedEpiWarps * it.s * f.job[it.j].prod[2].tiles_per_mat);
   }
   dep = it.p - 1;  // B' reads A, B'X reads B' (and X, complete before A started)
-  return static_cast<uint32_t>(4 * (it.s + 1) * f.job[it.j].prod[dep].tiles_per_mat);
+  return static_cast<uint32_t>(kFusedEpiWarps * (it.s + 1) * f.job[it.j].prod[dep].tiles_per_mat);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -1268,7 +1275,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, i
   return true;
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kFusedThreads, 1)
     ns_fused_kernel(const __grid_constant__ FusedMaps mp, const FusedArgs f) {
   constexpr int S = STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1294,7 +1301,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
-      tc::mbar_init(tempty + b, 128);
+      tc::mbar_init(tempty + b, 32 * kFusedEpiWarps);
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
@@ -1436,8 +1443,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
-    const int quad = warp & 3;
-    uint8_t* mine = sEpi + quad * (epi_bytes(kEpiTma) / 4);
+    const int quad = warp & 3;        // this warp may read TMEM lanes [32 quad, 32 quad + 32)
+    const int half = (warp - 2) >> 2;  // and drains blocks [4 half, 4 half + 4) of a tile
+    uint8_t* mine = sEpi + (warp - 2) * (epi_bytes(kEpiTma) / kFusedEpiWarps);
     int last_par = -1;
     int n = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++n) {
@@ -1452,8 +1460,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int cur = it.s & 1;
       const FusedJobMaps& m = mp.job[it.j];
       const CUtensorMap* D = it.p == 0 ? &m.ae : (it.p == 1 ? &m.be : (it.s == f.steps - 1 ? &m.oe : &m.xe[cur ^ 1]));
-      epi_tile_tma<false>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
-                          it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par);
+      epi_tile_tma<false, 1>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
+                             it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par, 4 * half, 4 * half + 4);
       tc::fence_before_sync();
       tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
       if (lane == 0) {
@@ -1717,7 +1725,7 @@ zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
   const long long total = at * f.steps;
   const int grid = total < sms ? static_cast<int>(total) : sms;
-  return launch_pdl(ns_fused_kernel, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
+  return launch_pdl(ns_fused_kernel, dim3(grid), dim3(kFusedThreads), static_cast<size_t>(smem_bytes(kEpiTma)),
                     stream, maps, f);
 }
 
