@@ -358,6 +358,30 @@ ZOPT_API zopt_status zopt_muon_step(float* master, float* momentum, const void* 
                                     const zopt_muon_hparams* hparams, zopt_muon_stats* d_stats, void* d_ws,
                                     size_t ws_bytes, zopt_stream stream);
 
+/* One shape's matrices for zopt_muon_step_many: the arguments of zopt_muon_step (grad_dtype a
+ * zopt_dtype; batch at most 65535). 64 bytes. */
+typedef struct zopt_muon_job {
+  float* master;
+  float* momentum;
+  const void* grad;
+  uint16_t* out_bf16;
+  zopt_muon_stats* d_stats;
+  int64_t rows, cols;
+  int32_t batch;
+  int32_t grad_dtype;
+} zopt_muon_job;
+
+/* Workspace bytes for zopt_muon_step_many over these jobs (0 if a job is empty or has more than
+ * 65535 matrices). */
+ZOPT_API size_t zopt_muon_workspace_many(const zopt_muon_job* jobs, int32_t n_jobs);
+/* One Muon step for every matrix of every job with the same hyper-parameters: each job's results
+ * (master, momentum, bf16 weights, stats) are bitwise what zopt_muon_step gives with a workspace
+ * that holds the job's whole batch; the Newton-Schulz part of all jobs is one
+ * zopt_ns_orthogonalize_many call. jobs is read during the call only. Same errors as
+ * zopt_muon_step. */
+ZOPT_API zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_jobs, const zopt_muon_hparams* hparams,
+                                         void* d_ws, size_t ws_bytes, zopt_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

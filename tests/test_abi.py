@@ -144,3 +144,25 @@ def test_ns_orthogonalize_many_validates_before_launch():
     assert L.zopt_ns_orthogonalize_many(f16, 1, 5, coef, 1e-7, ws, big, None) == 2
     nan = (ctypes.c_float * 3)(float("nan"), 1.0, 1.0)
     assert L.zopt_ns_orthogonalize_many(arr, 1, 5, nan, 1e-7, ws, big, None) == 1
+
+
+def test_muon_step_many_validates_before_launch():
+    L = Z.lib()
+    shapes = [(768, 2304, 12), (768, 768, 12)]
+    assert Z.muon_workspace_many(shapes) > Z.muon_workspace_many(shapes[:1]) > 0
+    assert Z.muon_workspace_many([(0, 4, 1)]) == 0
+    hp = Z._muon_hparams(1e-3, 0.95, 0.1, True, True, 5, Z.DEFAULT_ABC, 1e-7, 1000.0)
+    p = ctypes.c_void_p(1 << 20)
+    job = Z._MuonJob(p, p, p, None, ctypes.c_void_p(1 << 16), 64, 128, 1, Z.BF16)
+    arr = (Z._MuonJob * 1)(job)
+    big = 1 << 40
+    assert L.zopt_muon_step_many(arr, 0, ctypes.byref(hp), p, big, None) == 1
+    assert L.zopt_muon_step_many(arr, 1, None, p, big, None) == 1
+    assert L.zopt_muon_step_many(arr, 1, ctypes.byref(hp), p, 64, None) == 1
+    assert b"workspace" in L.zopt_last_error()
+    mis = (Z._MuonJob * 1)(Z._MuonJob(ctypes.c_void_p((1 << 20) + 4), p, p, None, ctypes.c_void_p(1 << 16), 64, 128,
+                                      1, Z.BF16))
+    assert L.zopt_muon_step_many(mis, 1, ctypes.byref(hp), p, big, None) == 1
+    assert b"misaligned" in L.zopt_last_error()
+    bad = Z._muon_hparams(1e-3, 1.5, 0.1, True, True, 5, Z.DEFAULT_ABC, 1e-7, 1000.0)
+    assert L.zopt_muon_step_many(arr, 1, ctypes.byref(bad), p, big, None) == 1

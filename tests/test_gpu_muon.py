@@ -98,3 +98,36 @@ def test_llama_owned_set_one_step(zopt):
         U_ref = newton_schulz(u.astype(np.float64), steps=5)
         applied = (p_old[b] * decay - p[b].cpu().numpy()).astype(np.float64) / float(step)
         assert rel(applied, U_ref) <= 2e-2
+
+
+def test_many_shapes_equal_single_calls(zopt):
+    """zopt_muon_step_many over several shapes (bf16 and fp32 gradients, with and without the
+    bf16 round-out, a tall matrix, a CTA-pair size) for two steps: master, momentum, bf16
+    weights and stats are bitwise what zopt_muon_step gives each shape with its whole batch."""
+    specs = [(4, 256, 768, torch.bfloat16, True), (3, 768, 256, torch.bfloat16, False),
+             (2, 384, 1000, torch.float32, True), (1, 130, 70, torch.bfloat16, True),
+             (2, 1024, 1536, torch.bfloat16, True)]
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    sets = []
+    for b, r, c, gdt, with_out in specs:
+        p = torch.randn(b, r, c, generator=gen, device="cuda") * 0.02
+        sets.append(dict(p=[p.clone(), p.clone()], buf=[torch.zeros_like(p), torch.zeros_like(p)],
+                         out=[torch.zeros(b, r, c, dtype=torch.int16, device="cuda") if with_out else None
+                              for _ in range(2)],
+                         st=[zopt.new_muon_stats(b), zopt.new_muon_stats(b)], gdt=gdt, shape=(b, r, c)))
+    ws = zopt.new_muon_workspace_many([(r, c, b) for b, r, c, _, _ in specs])
+    for step in range(2):
+        grads = [(torch.randn(*d["shape"], generator=gen, device="cuda") * 1e-3).to(d["gdt"]) for d in sets]
+        zopt.muon_step_many([(d["p"][0], d["buf"][0], g, d["out"][0], d["st"][0]) for d, g in zip(sets, grads)], ws,
+                            lr=8e-4)
+        for d, g in zip(sets, grads):
+            b, r, c = d["shape"]
+            zopt.muon_step(d["p"][1], d["buf"][1], g, d["out"][1], zopt.new_muon_workspace(r, c, b), d["st"][1],
+                           lr=8e-4)
+        torch.cuda.synchronize()
+        for d in sets:
+            assert torch.equal(d["p"][0].view(torch.int32), d["p"][1].view(torch.int32)), d["shape"]
+            assert torch.equal(d["buf"][0], d["buf"][1])
+            if d["out"][0] is not None:
+                assert torch.equal(d["out"][0], d["out"][1])
+            assert torch.equal(d["st"][0], d["st"][1])

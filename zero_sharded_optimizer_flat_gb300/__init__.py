@@ -91,6 +91,9 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.c_int, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float,
                                                  vp, sz, vp]),
         "zopt_ns_workspace_many": (sz, [ctypes.POINTER(_NsJob), i32]),
+        "zopt_muon_workspace_many": (sz, [ctypes.POINTER(_MuonJob), i32]),
+        "zopt_muon_step_many": (ctypes.c_int, [ctypes.POINTER(_MuonJob), i32, ctypes.POINTER(_MuonHparams), vp, sz,
+                                               vp]),
         "zopt_ns_orthogonalize_many": (ctypes.c_int, [ctypes.POINTER(_NsJob), i32, i32,
                                                       ctypes.POINTER(ctypes.c_float), ctypes.c_float, vp, sz, vp]),
     }
@@ -406,15 +409,54 @@ def read_muon_stats(t) -> list:
     return out
 
 
+def _muon_hparams(lr, momentum_coef, weight_decay, nesterov, match_rms_adamw, ns_steps, abc, eps, guard):
+    return _MuonHparams(float(lr), float(momentum_coef), float(weight_decay), int(bool(nesterov)),
+                        0 if match_rms_adamw else 1, int(ns_steps), (ctypes.c_float * 3)(*[float(c) for c in abc]),
+                        float(eps), float(guard))
+
+
+class _MuonJob(ctypes.Structure):
+    """``zopt_muon_job``: one shape's matrices for ``zopt_muon_step_many``."""
+    _fields_ = [("master", ctypes.c_void_p), ("momentum", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("out_bf16", ctypes.c_void_p), ("d_stats", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("batch", ctypes.c_int32), ("grad_dtype", ctypes.c_int32)]
+
+
+def muon_workspace_many(shapes) -> int:
+    """``zopt_muon_workspace_many`` for jobs of the given (rows, cols, batch)."""
+    arr = (_MuonJob * len(shapes))(*[_MuonJob(None, None, None, None, None, int(r), int(c), int(b), F32)
+                                     for r, c, b in shapes])
+    return int(lib().zopt_muon_workspace_many(arr, len(shapes)))
+
+
+def new_muon_workspace_many(shapes, device="cuda"):
+    import torch
+    return torch.empty(max(muon_workspace_many(shapes), 16), dtype=torch.uint8, device=device)
+
+
+def muon_step_many(jobs, ws, *, lr: float, momentum_coef: float = 0.95, weight_decay: float = 0.1,
+                   nesterov: bool = True, match_rms_adamw: bool = True, ns_steps: int = 5, abc=DEFAULT_ABC,
+                   eps: float = 1e-7, guard: float = 1000.0, stream=None) -> None:
+    """``zopt_muon_step_many`` over [(master, momentum, grad, out_bf16, stats), ...], each a matrix
+    [rows, cols] or a batch [b, rows, cols] (contiguous); out_bf16 may be None."""
+    arr = []
+    for master, momentum, grad, out_bf16, stats in jobs:
+        shape = tuple(master.shape)
+        batch, rows, cols = (1, *shape) if len(shape) == 2 else shape
+        arr.append(_MuonJob(_ptr(master), _ptr(momentum), _ptr(grad), _ptr(out_bf16), _ptr(stats), rows, cols, batch,
+                            _dtype_code(grad)))
+    c_arr = (_MuonJob * len(arr))(*arr)
+    hp = _muon_hparams(lr, momentum_coef, weight_decay, nesterov, match_rms_adamw, ns_steps, abc, eps, guard)
+    _check(lib().zopt_muon_step_many(c_arr, len(arr), ctypes.byref(hp), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def muon_step(master, momentum, grad, out_bf16, ws, stats, *, lr: float, momentum_coef: float = 0.95,
               weight_decay: float = 0.1, nesterov: bool = True, match_rms_adamw: bool = True, ns_steps: int = 5,
               abc=DEFAULT_ABC, eps: float = 1e-7, guard: float = 1000.0, stream=None) -> None:
     """``zopt_muon_step`` on a matrix [rows, cols] or a batch [b, rows, cols] (contiguous)."""
     shape = tuple(master.shape)
     batch, rows, cols = (1, *shape) if len(shape) == 2 else shape
-    hp = _MuonHparams(float(lr), float(momentum_coef), float(weight_decay), int(bool(nesterov)),
-                      0 if match_rms_adamw else 1, int(ns_steps), (ctypes.c_float * 3)(*[float(c) for c in abc]),
-                      float(eps), float(guard))
+    hp = _muon_hparams(lr, momentum_coef, weight_decay, nesterov, match_rms_adamw, ns_steps, abc, eps, guard)
     _check(lib().zopt_muon_step(_ptr(master), _ptr(momentum), _ptr(grad), _dtype_code(grad), _ptr(out_bf16), rows,
                                 cols, batch, ctypes.byref(hp), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)))
 

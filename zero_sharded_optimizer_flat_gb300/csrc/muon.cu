@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <string>
+#include <vector>
 
 #include "internal.h"
 #include "norm_impl.cuh"
@@ -127,6 +129,109 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// One shape's matrices of a Muon step.
+struct Job {
+  float* master;
+  float* momentum;
+  const void* grad;
+  zopt_dtype gdt;
+  uint16_t* out;
+  long long rows, cols;
+  long long batch;
+  zopt_muon_stats* stats;
+};
+
+zopt_status check_job(const char* fn, const Job& j) {
+  const std::string f(fn);
+  if (j.master == nullptr || j.momentum == nullptr || j.grad == nullptr || j.stats == nullptr)
+    return fail(ZOPT_EINVAL, f + ": NULL pointer");
+  if (j.rows < 1 || j.cols < 1 || j.batch < 1) return fail(ZOPT_EINVAL, f + ": empty matrix or batch");
+  if (!aligned16(j.master) || !aligned16(j.momentum) || !aligned16(j.grad) ||
+      (j.out != nullptr && (reinterpret_cast<uintptr_t>(j.out) & 1u) != 0) ||
+      (reinterpret_cast<uintptr_t>(j.stats) & 3u) != 0)
+    return fail(ZOPT_EINVAL, f + ": a device pointer is misaligned");
+  if (((j.rows * j.cols) & 3) != 0 && j.batch > 1)
+    return fail(ZOPT_EINVAL, f + ": a batch needs rows*cols to be a multiple of 4 (16-byte matrices)");
+  if (j.gdt != ZOPT_F32 && j.gdt != ZOPT_BF16) return fail(ZOPT_EUNSUPPORTED, f + ": gradient dtype must be fp32 or bf16");
+  return ok();
+}
+
+zopt_status check_hparams(const char* fn, const zopt_muon_hparams* hp) {
+  if (!std::isfinite(hp->lr) || hp->lr < 0 || !(hp->momentum >= 0 && hp->momentum < 1) ||
+      !std::isfinite(hp->weight_decay) || hp->ns_steps < 1 ||
+      (hp->adjust != ZOPT_MUON_MATCH_RMS_ADAMW && hp->adjust != ZOPT_MUON_ORIGINAL) || !(hp->guard > 0))
+    return fail(ZOPT_EINVAL, std::string(fn) + ": hyper-parameters out of range");
+  return ok();
+}
+
+// Step 1 for matrices b0 .. b0 + gs - 1 of a job (contiguous): momentum, u into U_in.
+zopt_status launch_momentum(const Job& j, long long b0, int gs, float* U_in, const zopt_muon_hparams* hp, int sms,
+                            cudaStream_t s) {
+  const long long n = j.rows * j.cols, ng = n * gs;
+  const size_t gsz = j.gdt == ZOPT_F32 ? 4 : 2;
+  float* bm = j.momentum + b0 * n;
+  const uint8_t* gm = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
+  const float mu = static_cast<float>(hp->momentum);
+  long long blocks = (ng / 4 + kThreads - 1) / kThreads;
+  if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
+  if (blocks < 1) blocks = 1;
+  if (j.gdt == ZOPT_F32)
+    momentum_kernel<float><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        bm, reinterpret_cast<const float*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
+  else
+    momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        bm, reinterpret_cast<const __nv_bfloat16*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+// Steps 3 and 4 for matrices b0 .. b0 + gs - 1: per-matrix ||U|| and max |U| into the plan's
+// reduction area at ws, then the guarded update and bf16 round-out.
+zopt_status launch_update(const Job& j, long long b0, int gs, uint8_t* ws, const MuonPlan& P, const float* U_out,
+                          const zopt_muon_hparams* hp, cudaStream_t s) {
+  const long long rows = j.rows, cols = j.cols, n = rows * cols;
+  const double scale = hp->adjust == ZOPT_MUON_MATCH_RMS_ADAMW
+                           ? 0.2 * std::sqrt(static_cast<double>(rows > cols ? rows : cols))
+                           : std::sqrt(rows > cols ? static_cast<double>(rows) / static_cast<double>(cols) : 1.0);
+  const float decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+  const float step = static_cast<float>(hp->lr * scale);
+  const float sqrt_min = static_cast<float>(std::sqrt(static_cast<double>(rows < cols ? rows : cols)));
+  unsigned* maxbits = reinterpret_cast<unsigned*>(ws + P.off_max);
+  zopt_clip_stats* cs = reinterpret_cast<zopt_clip_stats*>(ws + P.off_cs);
+  ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, P.off_cs, s));  // reduction counters and maxima start at zero
+  long long bpm = (n + 32767) / 32768;
+  bpm = bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm);
+  const dim3 grid(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
+  ustats_kernel<<<grid, kThreads, 0, s>>>(U_out, n, ws, maxbits, cs);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  update_kernel<<<grid, kThreads, 0, s>>>(j.master + b0 * n, U_out, j.out ? j.out + b0 * n : nullptr, n, cs, maxbits,
+                                          decay, step, hp->guard, sqrt_min, j.stats + b0);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+Job job_of(const zopt_muon_job& b) {
+  return Job{b.master, b.momentum, b.grad, static_cast<zopt_dtype>(b.grad_dtype), b.out_bf16,
+             b.rows, b.cols, b.batch, b.d_stats};
+}
+
+// The Newton-Schulz job of a Muon job: u -> U, fp32 in and out, contiguous matrices.
+zopt_ns_job ns_job_of(const Job& j, const float* U_in, float* U_out) {
+  const long long n = j.rows * j.cols;
+  zopt_ns_job q;
+  q.G = U_in;
+  q.X = U_out;
+  q.rows = j.rows;
+  q.cols = j.cols;
+  q.ld_g = j.cols;
+  q.ld_x = j.cols;
+  q.batch_stride_g = n;
+  q.batch_stride_x = n;
+  q.batch = static_cast<int32_t>(j.batch);
+  q.io_dtype = ZOPT_F32;
+  return q;
+}
+
 }  // namespace
 }  // namespace zopt
 
@@ -140,24 +245,13 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
                                       const zopt_muon_hparams* hp, zopt_muon_stats* d_stats, void* d_ws,
                                       size_t ws_bytes, zopt_stream stream) {
   using namespace zopt;
-  if (master == nullptr || momentum == nullptr || grad == nullptr || hp == nullptr || d_stats == nullptr ||
-      d_ws == nullptr)
-    return fail(ZOPT_EINVAL, "zopt_muon_step: NULL pointer");
-  if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, "zopt_muon_step: empty matrix or batch");
-  if (!aligned16(master) || !aligned16(momentum) || !aligned16(grad) || !aligned16(d_ws) ||
-      (out_bf16 != nullptr && (reinterpret_cast<uintptr_t>(out_bf16) & 1u) != 0) ||
-      (reinterpret_cast<uintptr_t>(d_stats) & 3u) != 0)
-    return fail(ZOPT_EINVAL, "zopt_muon_step: a device pointer is misaligned");
-  if (((rows * cols) & 3) != 0 && batch > 1)
-    return fail(ZOPT_EINVAL, "zopt_muon_step: a batch needs rows*cols to be a multiple of 4 (16-byte matrices)");
-  if (grad_dtype != ZOPT_F32 && grad_dtype != ZOPT_BF16)
-    return fail(ZOPT_EUNSUPPORTED, "zopt_muon_step: gradient dtype must be fp32 or bf16");
-  if (!std::isfinite(hp->lr) || hp->lr < 0 || !(hp->momentum >= 0 && hp->momentum < 1) ||
-      !std::isfinite(hp->weight_decay) || hp->ns_steps < 1 || (hp->adjust != ZOPT_MUON_MATCH_RMS_ADAMW &&
-                                                                hp->adjust != ZOPT_MUON_ORIGINAL) ||
-      !(hp->guard > 0))
-    return fail(ZOPT_EINVAL, "zopt_muon_step: hyper-parameters out of range");
-  const long long n = rows * cols;
+  const char* fn = "zopt_muon_step";
+  if (hp == nullptr || d_ws == nullptr) return fail(ZOPT_EINVAL, "zopt_muon_step: NULL pointer");
+  const Job j{master, momentum, grad, grad_dtype, out_bf16, rows, cols, batch, d_stats};
+  zopt_status st = check_job(fn, j);
+  if (st != ZOPT_OK) return st;
+  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_muon_step: a device pointer is misaligned");
+  if ((st = check_hparams(fn, hp)) != ZOPT_OK) return st;
   long long group = 0;
   {
     const MuonPlan one = muon_plan(rows, cols, 1);
@@ -170,58 +264,88 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
   if (group < 1) return fail(ZOPT_EINVAL, "zopt_muon_step: workspace smaller than zopt_muon_workspace(rows, cols, 1)");
   const MuonPlan P = muon_plan(rows, cols, group);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
-  unsigned* maxbits = reinterpret_cast<unsigned*>(ws + P.off_max);
-  zopt_clip_stats* cs = reinterpret_cast<zopt_clip_stats*>(ws + P.off_cs);
   float* U_in = reinterpret_cast<float*>(ws + P.off_u);
   float* U_out = reinterpret_cast<float*>(ws + P.off_o);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_muon_step: no CUDA device");
-
-  const float mu = static_cast<float>(hp->momentum);
-  const double scale = hp->adjust == ZOPT_MUON_MATCH_RMS_ADAMW
-                           ? 0.2 * std::sqrt(static_cast<double>(rows > cols ? rows : cols))
-                           : std::sqrt(rows > cols ? static_cast<double>(rows) / static_cast<double>(cols) : 1.0);
-  const double lrwd = hp->lr * hp->weight_decay;
-  const float decay = static_cast<float>(1.0 - lrwd);
-  const double lrs = hp->lr * scale;
-  const float step = static_cast<float>(lrs);
-  const float sqrt_min = static_cast<float>(std::sqrt(static_cast<double>(rows < cols ? rows : cols)));
-  const size_t gsz = grad_dtype == ZOPT_F32 ? 4 : 2;
-
+  const long long n = rows * cols;
   for (long long b0 = 0; b0 < batch; b0 += group) {
     const int gs = static_cast<int>(batch - b0 < group ? batch - b0 : group);
-    const long long ng = n * gs;
-    float* pm = master + b0 * n;
-    float* bm = momentum + b0 * n;
-    const uint8_t* gm = static_cast<const uint8_t*>(grad) + static_cast<size_t>(b0 * n) * gsz;
     // 1. momentum over the group's matrices (contiguous), u into the workspace
-    long long blocks = (ng / 4 + kThreads - 1) / kThreads;
-    if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
-    if (blocks < 1) blocks = 1;
-    if (grad_dtype == ZOPT_F32)
-      momentum_kernel<float><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
-          bm, reinterpret_cast<const float*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
-    else
-      momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
-          bm, reinterpret_cast<const __nv_bfloat16*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
-    ZOPT_CUDA_TRY(cudaGetLastError());
+    if ((st = launch_momentum(j, b0, gs, U_in, hp, sms, s)) != ZOPT_OK) return st;
     // 2. U = NewtonSchulz(u), fp32 in and out, bf16 tensor cores
-    zopt_status st = zopt_ns_orthogonalize(U_in, U_out, ZOPT_F32, rows, cols, cols, cols, n, n, gs, ZOPT_BF16,
-                                           hp->ns_steps, hp->abc, hp->eps, ws + P.off_ns, P.ns_bytes, stream);
+    st = zopt_ns_orthogonalize(U_in, U_out, ZOPT_F32, rows, cols, cols, cols, n, n, gs, ZOPT_BF16, hp->ns_steps,
+                               hp->abc, hp->eps, ws + P.off_ns, P.ns_bytes, stream);
     if (st != ZOPT_OK) return st;
-    // 3. per-matrix ||U|| and max |U|
-    ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, P.off_cs, s));  // reduction counters and maxima start at zero
-    long long bpm = (n + 32767) / 32768;
-    bpm = bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm);
-    ustats_kernel<<<dim3(static_cast<unsigned>(bpm), static_cast<unsigned>(gs)), kThreads, 0, s>>>(U_out, n, ws,
-                                                                                                  maxbits, cs);
-    ZOPT_CUDA_TRY(cudaGetLastError());
-    // 4. the guarded update and bf16 round-out
-    update_kernel<<<dim3(static_cast<unsigned>(bpm), static_cast<unsigned>(gs)), kThreads, 0, s>>>(
-        pm, U_out, out_bf16 ? out_bf16 + b0 * n : nullptr, n, cs, maxbits, decay, step, hp->guard, sqrt_min,
-        d_stats + b0);
-    ZOPT_CUDA_TRY(cudaGetLastError());
+    // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
+    if ((st = launch_update(j, b0, gs, ws, P, U_out, hp, s)) != ZOPT_OK) return st;
+  }
+  return ok();
+}
+
+static_assert(sizeof(zopt_muon_job) == 64, "zopt_muon_job layout");
+
+extern "C" size_t zopt_muon_workspace_many(const zopt_muon_job* jobs, int32_t n_jobs) {
+  using namespace zopt;
+  if (jobs == nullptr || n_jobs < 1) return 0;
+  size_t total = 0;
+  std::vector<zopt_ns_job> ns(static_cast<size_t>(n_jobs));
+  for (int32_t k = 0; k < n_jobs; ++k) {
+    const zopt_muon_job& b = jobs[k];
+    if (b.rows < 1 || b.cols < 1 || b.batch < 1 || b.batch > 65535) return 0;
+    total += static_cast<size_t>(round_up(static_cast<long long>(muon_plan(b.rows, b.cols, b.batch).off_ns), 1024));
+    ns[static_cast<size_t>(k)] = ns_job_of(job_of(b), nullptr, nullptr);
+  }
+  const size_t nsb = zopt_ns_workspace_many(ns.data(), n_jobs);
+  return nsb == 0 ? 0 : total + nsb;
+}
+
+extern "C" zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_jobs, const zopt_muon_hparams* hp,
+                                           void* d_ws, size_t ws_bytes, zopt_stream stream) {
+  using namespace zopt;
+  const char* fn = "zopt_muon_step_many";
+  if (jobs == nullptr || hp == nullptr || d_ws == nullptr) return fail(ZOPT_EINVAL, "zopt_muon_step_many: NULL pointer");
+  if (n_jobs < 1) return fail(ZOPT_EINVAL, "zopt_muon_step_many: no jobs");
+  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_muon_step_many: a device pointer is misaligned");
+  zopt_status st = check_hparams(fn, hp);
+  if (st != ZOPT_OK) return st;
+  for (int32_t k = 0; k < n_jobs; ++k) {
+    if ((st = check_job(fn, job_of(jobs[k]))) != ZOPT_OK) return st;
+    if (jobs[k].batch > 65535) return fail(ZOPT_EINVAL, "zopt_muon_step_many: a job's batch exceeds 65535");
+  }
+  const size_t need = zopt_muon_workspace_many(jobs, n_jobs);
+  if (need == 0 || ws_bytes < need)
+    return fail(ZOPT_EINVAL, "zopt_muon_step_many: workspace smaller than zopt_muon_workspace_many");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_muon_step_many: no CUDA device");
+  // every job's whole batch in its own slice of the workspace: momentum for all, Newton-Schulz
+  // for all in one call (the shapes below 1024 share fused launches), then the updates
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  std::vector<zopt_ns_job> ns(static_cast<size_t>(n_jobs));
+  std::vector<size_t> off(static_cast<size_t>(n_jobs));
+  size_t at = 0;
+  for (int32_t k = 0; k < n_jobs; ++k) {
+    const Job j = job_of(jobs[k]);
+    const MuonPlan P = muon_plan(j.rows, j.cols, j.batch);
+    off[static_cast<size_t>(k)] = at;
+    float* U_in = reinterpret_cast<float*>(ws + at + P.off_u);
+    float* U_out = reinterpret_cast<float*>(ws + at + P.off_o);
+    if ((st = launch_momentum(j, 0, static_cast<int>(j.batch), U_in, hp, sms, s)) != ZOPT_OK) return st;
+    ns[static_cast<size_t>(k)] = ns_job_of(j, U_in, U_out);
+    at += static_cast<size_t>(round_up(static_cast<long long>(P.off_ns), 1024));
+  }
+  if ((st = zopt_ns_orthogonalize_many(ns.data(), n_jobs, hp->ns_steps, hp->abc, hp->eps, ws + at, ws_bytes - at,
+                                       stream)) != ZOPT_OK)
+    return st;
+  for (int32_t k = 0; k < n_jobs; ++k) {
+    const Job j = job_of(jobs[k]);
+    const MuonPlan P = muon_plan(j.rows, j.cols, j.batch);
+    uint8_t* wj = ws + off[static_cast<size_t>(k)];
+    if ((st = launch_update(j, 0, static_cast<int>(j.batch), wj, P, reinterpret_cast<const float*>(wj + P.off_o), hp,
+                            s)) != ZOPT_OK)
+      return st;
   }
   return ok();
 }
