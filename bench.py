@@ -35,6 +35,12 @@ WORKLOAD = ("zero2-flat-shard-2e9-w8 + ns-stress-48: rank r of W=8 (S=250,000,00
             "summed into fp32 with the clip stats fused into the last pass, then AdamW with bf16 round-out; "
             "Newton-Schulz (5 steps, bf16) on 16 x 4096^2, 16 x 4096x14336, 16 x 14336x4096")
 ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m, v (12) + bf16 (2)
+# DRAM bytes per element of one adamw_kernel launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum on a 64 Mi-element shard prefix, 1.9 GB per launch, scaled by the element
+# count; see profiles/adamw_kernel_zero2_shard.md), valid while the kernel's sources hash to
+# ADAMW_SRC_DIGEST (otherwise the traffic is reported as null)
+ADAMW_TRAFFIC_PER_ELEM = (1073801216 + 881234304) / 67108864
+ADAMW_SRC_DIGEST = "28b98384ca447d07"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 CPU_SAMPLE = 4_000_000
@@ -156,6 +162,17 @@ def cpu_oracle_run(seconds: float = 10.0) -> dict:
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{steps} steps of 4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out "
                       f"over {n:,} shard elements (numpy fp32 exact-order oracle, {el:.1f} s)"}
+
+
+def adamw_traffic(S: int):
+    """DRAM bytes per adamw_kernel launch over S elements from the committed ncu capture, or
+    None if the kernel's sources changed since."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("adamw.cu", "internal.h"):
+        with open(os.path.join(ROOT, "zero_sharded_optimizer_flat_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return round(ADAMW_TRAFFIC_PER_ELEM * S) if h.hexdigest()[:16] == ADAMW_SRC_DIGEST else None
 
 
 def ns_flops(rows: int, cols: int, steps: int) -> float:
@@ -462,7 +479,7 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
                               "accumulate_ms": round(a_ms - k_ms, 4), "adamw_kernel_ms": round(k_ms, 4)}
         line["roofline_hbm"] = {"kernel": "adamw_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                                "traffic": None, "peak_source": pk["source"],
+                                "traffic": adamw_traffic(S), "peak_source": pk["source"],
                                 "algorithmic_bytes_per_launch": ADAMW_BYTES * S, "avg_launch_ms": round(k_ms, 4)}
     if ns is not None:
         tflops = ns.flops / (n_ms * 1e-3) / 1e12
