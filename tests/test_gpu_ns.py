@@ -325,3 +325,22 @@ def test_many_jobs_equal_single_calls(zopt):
         assert torch.equal(one, X), (r, c, b)
     ref = newton_schulz(pairs[2][0][1].double().cpu().numpy(), steps=5)
     assert rel(pairs[2][1][1].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
+@pytest.mark.parametrize("steps", [1, 2, 7])
+def test_many_jobs_step_counts(zopt, steps):
+    """The fused work list at other step counts: with one step the first B'X is also the last
+    (into the caller's X); each job still equals its single call bit for bit."""
+    gen = torch.Generator(device="cuda").manual_seed(steps)
+    specs = [(3, 256, 768, torch.bfloat16), (2, 768, 256, torch.float32), (1, 100, 130, torch.bfloat16)]
+    pairs = [(torch.randn(b, r, c, generator=gen, device="cuda").to(dt),
+              torch.empty(b, r, c, device="cuda", dtype=dt)) for b, r, c, dt in specs]
+    zopt.ns_orthogonalize_many(pairs, zopt.new_ns_workspace_many([(r, c, b) for b, r, c, _ in specs]), steps=steps)
+    torch.cuda.synchronize()
+    for (G, X), (b, r, c, _) in zip(pairs, specs):
+        one = torch.empty_like(X)
+        zopt.ns_orthogonalize(G, one, zopt.new_ns_workspace(r, c, b), steps=steps)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X), (r, c, steps)
+        ref = newton_schulz(G[0].double().cpu().numpy(), steps=steps)
+        assert rel(X[0].cpu(), torch.from_numpy(ref)) <= 2e-2
