@@ -302,9 +302,12 @@ ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t
  * clears it, without synchronising (read it after the work it covers has completed).
  * zopt_selftest_wait_timeout launches one thread that waits, limited to limit_ns (at most
  * 2 s), on an mbarrier phase that nothing completes: the same bounded-wait code, run out on
- * purpose, so a test can check the reporting path. */
+ * purpose, so a test can check the reporting path. zopt_selftest_count_timeout does the same
+ * with the wait of the fused Newton-Schulz kernel on a per-matrix completion counter (in
+ * global memory) that nothing advances. */
 ZOPT_API int32_t zopt_take_device_error(void);
 ZOPT_API zopt_status zopt_selftest_wait_timeout(int64_t limit_ns, zopt_stream stream);
+ZOPT_API zopt_status zopt_selftest_count_timeout(int64_t limit_ns, zopt_stream stream);
 
 /* ======================================================================================
  * 5. Muon's update around Newton-Schulz (matrices owned whole by this rank)

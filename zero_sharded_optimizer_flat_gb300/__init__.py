@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
         "zopt_muon_workspace": (sz, [i64, i64, i32]),
         "zopt_take_device_error": (i32, []),
         "zopt_selftest_wait_timeout": (ctypes.c_int, [i64, vp]),
+        "zopt_selftest_count_timeout": (ctypes.c_int, [i64, vp]),
         "zopt_muon_step": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, vp, i64, i64, i32, ctypes.POINTER(_MuonHparams),
                                           vp, vp, sz, vp]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
@@ -469,3 +470,8 @@ def take_device_error() -> int:
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     """Run the bounded-wait path on a barrier nothing completes (limit_ns <= 2 s)."""
     _check(lib().zopt_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def selftest_count_timeout(limit_ns: int, stream=None) -> None:
+    """Run the fused kernel's bounded counter wait on a counter nothing advances (limit_ns <= 2 s)."""
+    _check(lib().zopt_selftest_count_timeout(int(limit_ns), _stream(stream)))

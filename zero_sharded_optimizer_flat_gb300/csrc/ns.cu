@@ -495,6 +495,15 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
     tc::mbar_wait_for(&bar, 0, err, limit_ns);
   }
 }
+
+// A completion counter that nothing advances.
+__device__ uint32_t g_never_counted;
+
+// One thread waits, with the given limit, for that counter to reach 1: the bounded wait of the
+// fused kernel's dependencies between products, run on purpose.
+__global__ void count_selftest_kernel(int* err, unsigned long long limit_ns) {
+  if (threadIdx.x == 0) wait_count(&g_never_counted, 1u, err, limit_ns);
+}
 }  // namespace
 }  // namespace ns
 }  // namespace zopt
@@ -508,6 +517,20 @@ extern "C" zopt_status zopt_selftest_wait_timeout(int64_t limit_ns, zopt_stream 
   zopt_status st = ns::error_word(&h, &d);
   if (st != ZOPT_OK) return st;
   ns::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      d, static_cast<unsigned long long>(limit_ns));
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
+
+extern "C" zopt_status zopt_selftest_count_timeout(int64_t limit_ns, zopt_stream stream) {
+  using namespace zopt;
+  if (limit_ns < 1 || limit_ns > 2000000000LL)
+    return fail(ZOPT_EINVAL, "zopt_selftest_count_timeout: limit must lie in (0, 2 s]");
+  int* h = nullptr;
+  int* d = nullptr;
+  zopt_status st = ns::error_word(&h, &d);
+  if (st != ZOPT_OK) return st;
+  ns::count_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       d, static_cast<unsigned long long>(limit_ns));
   ZOPT_CUDA_TRY(cudaGetLastError());
   return ok();

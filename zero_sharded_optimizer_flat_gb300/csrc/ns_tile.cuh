@@ -574,8 +574,11 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// Wait (bounded) until *c >= target; then order the caller's later TMA loads after it.
-__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, int* err) {
+// Wait (bounded by limit_ns) until *c >= target; then order the caller's later TMA loads after
+// it. Gives up like tc::mbar_wait_for: after another thread has reported an error, or at the
+// limit, recording error code 1.
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, int* err,
+                                           unsigned long long limit_ns = tc::kWaitLimitNs) {
   if (ld_acquire(c) < target) {
     const unsigned long long t0 = tc::globaltimer();
     for (uint32_t spin = 1;; ++spin) {
@@ -584,7 +587,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, i
       if ((spin & 15u) == 0) {
         const unsigned long long el = tc::globaltimer() - t0;
         if (el > 1000000ull && *reinterpret_cast<volatile int*>(err) != 0) return false;
-        if (el > tc::kWaitLimitNs) {
+        if (el > limit_ns) {
           atomicExch(err, 1);
           return false;
         }
