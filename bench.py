@@ -355,10 +355,26 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     a_ms = mean(ev_a) if "adamw" in parts else 0.0
     k_ms = mean(ev_k) if "adamw" in parts else 0.0
     n_ms = mean(ev_n) if ns is not None else 0.0
+    # the stand-alone norm / clip / found_inf reduction (zopt_grad_norm_clip, for a gradient that
+    # arrives already summed) over the same fp32 shard gradient (4 B/element, > L2), timed apart
+    # from the steps
+    nr_ms = 0.0
+    if "adamw" in parts:
+        nstats = Z.new_clip_stats()
+        for _ in range(3):
+            Z.grad_norm_clip(g, w.max_norm, ws, nstats, stream=stream)
+        torch.cuda.synchronize()
+        ev_r = [(mk(), mk()) for _ in range(max(K, 3))]
+        for a_ev, b_ev in ev_r:
+            a_ev.record(stream)
+            Z.grad_norm_clip(g, w.max_norm, ws, nstats, stream=stream)
+            b_ev.record(stream)
+        torch.cuda.synchronize()
+        nr_ms = mean(ev_r)
     if dist:
-        tt = torch.tensor([ms, a_ms, k_ms, n_ms], device="cuda")
+        tt = torch.tensor([ms, a_ms, k_ms, n_ms, nr_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, a_ms, k_ms, n_ms = (float(x) for x in tt)
+        ms, a_ms, k_ms, n_ms, nr_ms = (float(x) for x in tt)
         dist.barrier()
 
     # ---- end to end through the public API with host buffers: each part copies its inputs
@@ -477,6 +493,11 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         line["unit"] = "GB/s"
         line["adamw_part"] = {"ms": round(a_ms, 4), "bytes_per_element": ACC_BYTES + ADAMW_BYTES,
                               "accumulate_ms": round(a_ms - k_ms, 4), "adamw_kernel_ms": round(k_ms, 4)}
+        norm_gbs = 4 * S / (nr_ms * 1e-3) / 1e9
+        line["norm_clip"] = {"kernel": "norm_kernel (zopt_grad_norm_clip on the fp32 shard gradient, timed "
+                                       "apart from the steps)", "ms": round(nr_ms, 4), "bytes_per_element": 4,
+                             "achieved": round(norm_gbs, 1), "unit": "GB/s",
+                             "frac": round(norm_gbs / pk["hbm_gbs"], 4)}
         line["roofline_hbm"] = {"kernel": "adamw_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                                 "traffic": adamw_traffic(S), "peak_source": pk["source"],
