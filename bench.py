@@ -262,6 +262,37 @@ class NsPart:
         self.Z.ns_orthogonalize_many(self.groups, self.ws, steps=self.steps, stream=stream)
 
 
+class MuonPart:
+    """One Muon step over the Muon matrices rank 0 of the 1.1B Llama-style set owns (round-robin,
+    W = 8): 4 x 2048^2, 4 x 2048x512, 4 x 2048x11264, bf16 gradients ~N(0, 1e-3)."""
+
+    def __init__(self, Z, torch, seed: int):
+        import workloads
+        self.Z = Z
+        w = workloads.get("c3")
+        shapes = {}
+        for prm in w.owned_muon():
+            shapes[prm.shape] = shapes.get(prm.shape, 0) + 1
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        self.jobs = []
+        for (r, c), b in shapes.items():
+            p = torch.randn(b, r, c, device="cuda", generator=gen).mul_(0.02)
+            g = torch.randn(b, r, c, device="cuda", generator=gen).mul_(1e-3).to(torch.bfloat16)
+            self.jobs.append((p, torch.zeros_like(p), g, torch.empty(b, r, c, dtype=torch.int16, device="cuda"),
+                              Z.new_muon_stats(b)))
+        self.ws = Z.new_muon_workspace_many([(r, c, b) for (r, c), b in shapes.items()])
+        self.count = sum(shapes.values())
+        self.flops = sum(ns_flops(r, c, 5) * b for (r, c), b in shapes.items())
+        n = sum(r * c * b for (r, c), b in shapes.items())
+        self.bytes = 32 * n  # momentum 14 (bf16 grad), statistics 4, update 14 per element
+        self.what = (f"{self.count} matrices {sorted(shapes)} of the 1.1B set owned by rank 0 of 8, "
+                     "zopt_muon_step_many, 5 Newton-Schulz steps")
+        self.lr = w.lr
+
+    def run(self, stream):
+        self.Z.muon_step_many(self.jobs, self.ws, lr=self.lr, stream=stream)
+
+
 def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     import torch
 
@@ -371,10 +402,40 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
             b_ev.record(stream)
         torch.cuda.synchronize()
         nr_ms = mean(ev_r)
+    # zopt_adamw_rescale_step (re-target the step just taken to another gradient scale) over the
+    # shard: 30 B/element like the step itself, timed apart
+    rs_ms = 0.0
+    if "adamw" in parts:
+        rkw = dict(kw, clip_stats=None)
+        for _ in range(3):
+            Z.adamw_rescale_step(lay, p, m, v, g, out, old_scale=1.0, new_scale=0.5, stream=stream, **rkw)
+        torch.cuda.synchronize()
+        ev_s = [(mk(), mk()) for _ in range(max(K, 3))]
+        for a_ev, b_ev in ev_s:
+            a_ev.record(stream)
+            Z.adamw_rescale_step(lay, p, m, v, g, out, old_scale=1.0, new_scale=0.5, stream=stream, **rkw)
+            b_ev.record(stream)
+        torch.cuda.synchronize()
+        rs_ms = mean(ev_s)
+    # one Muon step (zopt_muon_step_many: momentum, Newton-Schulz, statistics, guarded update,
+    # bf16 round-out) over the matrices rank 0 of the 1.1B Llama-style set owns, timed apart
+    mu_ms, mu = 0.0, None
+    if "muon" in parts:
+        mu = MuonPart(Z, torch, 7000 + rank)
+        for _ in range(3):
+            mu.run(stream)
+        torch.cuda.synchronize()
+        ev_m = [(mk(), mk()) for _ in range(max(K, 3))]
+        for a_ev, b_ev in ev_m:
+            a_ev.record(stream)
+            mu.run(stream)
+            b_ev.record(stream)
+        torch.cuda.synchronize()
+        mu_ms = mean(ev_m)
     if dist:
-        tt = torch.tensor([ms, a_ms, k_ms, n_ms, nr_ms], device="cuda")
+        tt = torch.tensor([ms, a_ms, k_ms, n_ms, nr_ms, rs_ms, mu_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, a_ms, k_ms, n_ms, nr_ms = (float(x) for x in tt)
+        ms, a_ms, k_ms, n_ms, nr_ms, rs_ms, mu_ms = (float(x) for x in tt)
         dist.barrier()
 
     # ---- end to end through the public API with host buffers: each part copies its inputs
@@ -498,6 +559,10 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
                                        "apart from the steps)", "ms": round(nr_ms, 4), "bytes_per_element": 4,
                              "achieved": round(norm_gbs, 1), "unit": "GB/s",
                              "frac": round(norm_gbs / pk["hbm_gbs"], 4)}
+        rs_gbs = ADAMW_BYTES * S / (rs_ms * 1e-3) / 1e9
+        line["rescale"] = {"kernel": "rescale_kernel (zopt_adamw_rescale_step over the shard, timed apart)",
+                           "ms": round(rs_ms, 4), "bytes_per_element": ADAMW_BYTES, "achieved": round(rs_gbs, 1),
+                           "unit": "GB/s", "frac": round(rs_gbs / pk["hbm_gbs"], 4)}
         line["roofline_hbm"] = {"kernel": "adamw_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                                 "traffic": adamw_traffic(S), "peak_source": pk["source"],
@@ -516,6 +581,13 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
             line["value"], line["unit"] = line["ns"]["value"], "TFLOP/s"
     elif "adamw" in parts:
         line["roofline"] = line.pop("roofline_hbm")
+    if mu is not None:
+        line["muon_step"] = {"what": mu.what, "ms": round(mu_ms, 4), "matrices": mu.count,
+                             "ns_algorithmic_flops": mu.flops,
+                             "ns_equivalent_tflops": round(mu.flops / (mu_ms * 1e-3) / 1e12, 1),
+                             "elementwise_bytes": mu.bytes,
+                             "note": "the whole step's time against the Newton-Schulz flops alone; the momentum, "
+                                     "statistics and update passes move elementwise_bytes besides"}
     line["clocks"] = clocks
     e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if "adamw" in parts:
@@ -546,7 +618,8 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prequeue-ms", type=float, default=50.0,
                     help="device-side delay (about this many ms at 2 GHz) queued before the timed steps")
-    ap.add_argument("--parts", default="adamw,ns", help="comma list of step parts: adamw, ns")
+    ap.add_argument("--parts", default="adamw,ns,muon",
+                    help="comma list: adamw, ns (the timed step), muon (a Muon step timed apart)")
     ap.add_argument("--ns-set", default="stress", choices=["stress", "gpt2"],
                     help="Newton-Schulz matrices: the 48-matrix 4096-wide stress set, or the GPT-2-small body's 48")
     ap.add_argument("--ns-count", type=int, default=0,
