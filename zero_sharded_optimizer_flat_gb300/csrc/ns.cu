@@ -1,32 +1,30 @@
-// Muon's quintic Newton-Schulz orthogonalisation on whole matrices, on tcgen05 tensor cores.
+// Muon's quintic Newton-Schulz orthogonalisation on whole matrices, on tcgen05 tensor cores:
+// the workspace plan, the tensor maps, the entry points and the failure self-tests.
 //
 // bluscript_zero_ckpt.cpp, ShardedMuon design note: U = NewtonSchulz(M), the iterated matrix
 // polynomial X <- aX + (bXX' + c(XX')^2)X, in which every output entry depends on the whole
 // matrix (so each matrix has one owner rank); 5 steps in the trainer's config.
 //
 // Per step, with X m x n (m <= n; a taller input is processed as its transpose):
-//   A = X X'            (symmetric: only 128x256 tiles touching the upper triangle are
-//                        computed, each writes its upper part directly and its strictly upper
-//                        part mirrored)
+//   A = X X'            (symmetric: only the tiles touching the upper triangle are computed,
+//                        each writes its upper part and, transposed, its mirror)
 //   B' = c A A' + b A + a I
 //                       (A is symmetric, so A^2 = A A': the same symmetric kernel, with the
-//                        b*A term and a on the diagonal added in the epilogue)
+//                        b*A term and a on the diagonal added to the accumulator)
 //   X = B' X            (= aX + BX: the step's aX term rides on B's diagonal, so the largest
 //                        product has no second input to read; a plain GEMM whose B-operand X
 //                        is read MN-major straight from its row-major layout; the last step
 //                        writes the caller's output, in the caller's orientation and dtype)
 // Operands and the products A, B', X are bf16; every product accumulates in fp32 in TMEM.
+// The fp32 compute mode runs the products as the pages write them on the SIMT kernel
+// (ns_simt.cu).
 //
-// Products with m >= 1024 run on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles, see
-// gemm_bf16_pair_kernel); smaller ones on single CTAs as follows.
-// One kernel does all three products: a persistent, warp-specialised tcgen05 GEMM. Warp 0
-// streams 128x64 and 256x64 bf16 tiles into a shared-memory ring with TMA (128-byte swizzle);
-// one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
-// accumulators (2 x 256 fp32 columns), committing stage release and accumulator-ready events
-// to mbarriers; warps 2-5 drain the other accumulator (tcgen05.ld), apply alpha*acc + beta*R
-// (+ the diagonal term) and hand 32 x 32 bf16 boxes to the TMA while the next tile is being
-// multiplied. Every mbarrier wait is bounded; a timeout sets an error word that the next call
-// reports as ZOPT_ETIMEOUT.
+// Where the work runs: ns_prep.cu normalises and orients the inputs; below m = 1024 every
+// product of every step runs in one persistent launch of ns_fused_kernel (ns_fused.cu), several
+// shapes at once; from m = 1024, and whenever an output or the coefficients rule the fused
+// kernel out, each product is one launch of the single-CTA or CTA-pair GEMM (ns_gemm.cu). The
+// tile geometry and the epilogue building blocks they share are in ns_tile.cuh. Every wait is
+// bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
 #include "ns_tile.cuh"
 
 namespace zopt {

@@ -1,5 +1,13 @@
-// The Newton-Schulz products on tcgen05 tensor cores: the single-CTA persistent GEMM and its
-// CTA-pair form, and their host launchers.
+// The Newton-Schulz products on tcgen05 tensor cores, one launch per product: the single-CTA
+// persistent GEMM and its CTA-pair form, and their host launchers.
+//
+// Single CTA: one CTA per SM (persistent), 192 threads. Warp 0 streams 128x64 and 256x64 bf16
+// tiles into a shared-memory ring with TMA (128-byte swizzle); one thread of warp 1 issues
+// tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators (2 x 256 fp32 columns),
+// committing stage-release and accumulator-ready events to mbarriers; warps 2-5 drain the other
+// accumulator (tcgen05.ld), apply alpha*acc (+ beta*R, + the diagonal term) and store it while
+// the next tile is being multiplied: through registers and plain stores (kEpiRegs) or as
+// 32 x 32 bf16 boxes handed to the TMA (kEpiTma, kEpiTmaR).
 #include "ns_tile.cuh"
 
 namespace zopt {
