@@ -143,6 +143,33 @@ def test_output_pitch_and_alignment(zopt, pad, shift, rows, cols, dtype):
     assert bool((flat[:shift] == 7.0).all())
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,cols", [(300, 1000), (1000, 300), (1000, 301), (301, 1000), (700, 13)])
+@pytest.mark.parametrize("pad,shift", [(8, 0), (3, 0), (0, 1)])
+def test_input_pitch_and_alignment(zopt, pad, shift, rows, cols, dtype):
+    """The normalisation reads G through 16-byte accesses when its rows allow them and element by
+    element otherwise (padded rows, a base off the 16-byte grid, a row length that leaves a
+    partial piece): every result is within the oracle's tolerance, and where both reads visit
+    the elements in the same order (16-byte rows, cols % 8 == 0) bitwise the contiguous call's."""
+    batch = 2
+    ld = cols + pad
+    flat = torch.randn(batch * rows * ld + shift, device="cuda").to(dtype)
+    G = flat[shift:].view(batch, rows, ld)[:, :, :cols]
+    X = torch.empty(batch, rows, cols, device="cuda", dtype=dtype)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols, group=2), steps=3)
+    torch.cuda.synchronize()
+    esz = 2 if dtype == torch.bfloat16 else 4
+    same_order = shift == 0 and (ld * esz) % 16 == 0 and cols % 8 == 0
+    for b in range(batch):
+        ref = newton_schulz(G[b].double().cpu().numpy(), steps=3)
+        assert rel(X[b].cpu(), torch.from_numpy(ref)) <= 2e-2, b
+        if same_order:
+            one = torch.empty(rows, cols, device="cuda", dtype=dtype)
+            zopt.ns_orthogonalize(G[b].contiguous(), one, zopt.new_ns_workspace(rows, cols), steps=3)
+            torch.cuda.synchronize()
+            assert torch.equal(one, X[b]), b
+
+
 @pytest.mark.parametrize("compute", ["bf16", "f32"])
 def test_grouped_batch_equals_single_calls(zopt, compute):
     """A workspace for 2 matrices runs a batch of 5 as groups of 2, 2, 1: every product is one

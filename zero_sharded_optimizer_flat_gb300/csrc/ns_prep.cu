@@ -1,59 +1,188 @@
-// Newton-Schulz preparation: the Frobenius norm of every matrix of a group and X0 = G / (||G||
-// + eps) in the compute dtype, transposed for a tall matrix.
+// Newton-Schulz preparation: the Frobenius norm of every matrix and X0 = G / (||G|| + eps) in
+// the compute dtype, transposed for a tall matrix — three launches for every matrix of every
+// job of a call (sum of squares; scaling of the wide; transposition of the tall). Every thread
+// keeps 128 bytes of loads in flight, and the normalising kernels issue their first loads
+// before they reduce the norm.
+#include <algorithm>
+#include <cstring>
+#include <type_traits>
+
 #include "ns_tile.cuh"
 
 namespace zopt {
 namespace ns {
 
-// Sum of squares of each matrix of the group (blockIdx.y = matrix): G_b is rows x cols with
-// leading dimension ld, matrices batch_stride elements apart. `flat` = rows are contiguous
-// (ld == cols) and 16-byte aligned, so the matrix is one vector.
+// Every matrix of a list of groups (one launch for all of them): blockIdx.y is the matrix's
+// index across the list, the item it belongs to found by its `first` index.
+constexpr int kMaxPrepItems = 16;
+constexpr long long kSumsqElems = 32768;  // elements per sum-of-squares block (before the cap)
+constexpr int kScaleVecs = 4096;          // 8-element vectors per scaling block (16 per thread)
+
+struct PrepItem {
+  const void* g;  // the group's first input matrix; matrix b at + b * bs elements
+  long long rows, cols, ld, bs;
+  int flat, vec_rows;  // sum of squares: one contiguous vector; rows of 8-element accesses
+  int vec;             // scaling: rows of 8-element accesses (cols % 8 == 0)
+  int flat_io;         // scaling: G and X0 both contiguous (ld == ldx == cols)
+  int pair;            // fp32-output transpose: 2-element accesses
+  int tvec;            // bf16-output transpose: 16-byte row accesses
+  int bpm;             // sum-of-squares blocks per matrix (depends on the matrix size only)
+  long long chunks;    // scaling / transpose blocks per matrix
+  int first;           // index of the group's first matrix in the list (blockIdx.y)
+  uint8_t* ws;         // prep scratch of matrix 0 (kPrepWsBytes per matrix): partials, counters
+  zopt_clip_stats* stats;
+  void* x0;            // X0 of matrix 0 in the compute dtype; matrix b at + b * x_stride
+  long long ldx, x_stride;
+};
+
+struct PrepList {
+  PrepItem it[kMaxPrepItems];
+  int n;
+  double eps;
+};
+
+__device__ __forceinline__ const PrepItem& prep_item(const PrepList& L, int y) {
+  int k = 0;
+  while (k + 1 < L.n && y >= L.it[k + 1].first) ++k;
+  return L.it[k];
+}
+
+// The sum of 256 threads' values (linear thread id tid, 8 warps) in a fixed order: butterfly
+// within each warp, then over the 8 warp sums; valid in thread 0.
+__device__ __forceinline__ double sum256(double v, int tid, double* smem8) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int warp = tid >> 5, lane = tid & 31;
+  if (lane == 0) smem8[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (warp == 0) {
+    r = lane < 8 ? smem8[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = __dadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+  }
+  __syncthreads();
+  return r;
+}
+
+// fp32 pairwise sum of squares of 8 values (no range check).
+__device__ __forceinline__ float sumsq8f(const float (&x)[8]) {
+  const float s01 = __fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1]));
+  const float s23 = __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3]));
+  const float s45 = __fadd_rn(__fmul_rn(x[4], x[4]), __fmul_rn(x[5], x[5]));
+  const float s67 = __fadd_rn(__fmul_rn(x[6], x[6]), __fmul_rn(x[7], x[7]));
+  return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// Sum of squares of 32 values: fp32 pairwise while every 8-sum lies in [2^-96, 2^124] (no
+// overflow in the 32-sum, no loss to fp32 underflow worth a bf16 result); otherwise each 8 as
+// sumsq8 does (exact fp64 outside the safe range, NaN and Inf carried). One fp64 add per 32
+// elements keeps the fp64 pipe, slow on this part, off the critical path.
+__device__ __forceinline__ double sumsq32(const float (&a)[8], const float (&b)[8], const float (&c)[8],
+                                          const float (&d)[8]) {
+  const float s0 = sumsq8f(a), s1 = sumsq8f(b), s2 = sumsq8f(c), s3 = sumsq8f(d);
+  const float lo = fminf(fminf(s0, s1), fminf(s2, s3)), hi = fmaxf(fmaxf(s0, s1), fmaxf(s2, s3));
+  if (lo >= 0x1p-96f && hi <= 0x1p124f) return static_cast<double>(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)));
+  return __dadd_rn(__dadd_rn(sumsq8(a), sumsq8(b)), __dadd_rn(sumsq8(c), sumsq8(d)));
+}
+
+// The raw bits of 8 elements (one 16-byte load of bf16, two of fp32) and their values.
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads)
-    group_sumsq_kernel(const T* __restrict__ g0, long long rows, long long cols, long long ld,
-                       long long batch_stride, int flat, int vec_rows, uint8_t* ws_base,
-                       zopt_clip_stats* stats) {
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 a;
+};
+template <>
+struct Raw8<float> {
+  uint4 a, b;
+};
+__device__ __forceinline__ void ld_raw8(const __nv_bfloat16* p, Raw8<__nv_bfloat16>& r) {
+  r.a = __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void ld_raw8(const float* p, Raw8<float>& r) {
+  r.a = __ldg(reinterpret_cast<const uint4*>(p));
+  r.b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+}
+__device__ __forceinline__ void unpack8(const Raw8<__nv_bfloat16>& r, float (&x)[8]) {
+  const unsigned int w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void unpack8(const Raw8<float>& r, float (&x)[8]) {
+  x[0] = __uint_as_float(r.a.x); x[1] = __uint_as_float(r.a.y); x[2] = __uint_as_float(r.a.z);
+  x[3] = __uint_as_float(r.a.w); x[4] = __uint_as_float(r.b.x); x[5] = __uint_as_float(r.b.y);
+  x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
+}
+// 8-element vectors per round: 128 bytes of loads in flight per thread.
+template <typename T>
+constexpr int kRound = 16 / static_cast<int>(sizeof(T));
+
+// Partial sums of squares of each matrix (blockIdx.y) over its first bpm blocks: G_b is rows x
+// cols with leading dimension ld, matrices bs elements apart. `flat` = the matrix is one
+// contiguous, 16-byte aligned vector. Threads stride over 8-element vectors, kRound loads in
+// flight per round; block x of a matrix writes partial x to its scratch.
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) prep_sumsq_kernel(const PrepList L) {
+  constexpr int R = kRound<T>;
+  __shared__ double red[8];
   tc::pdl_launch_dependents();
   tc::pdl_wait();
-  const int mb = blockIdx.y;
-  const T* g = g0 + mb * batch_stride;
+  const PrepItem& J = prep_item(L, blockIdx.y);
+  if (static_cast<int>(blockIdx.x) >= J.bpm) return;
+  const int mb = static_cast<int>(blockIdx.y) - J.first;
+  const T* g = static_cast<const T*>(J.g) + mb * J.bs;
+  const long long rows = J.rows, cols = J.cols, ld = J.ld;
   double acc = 0.0;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long stride = static_cast<long long>(J.bpm) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (flat) {
-    const long long n = rows * cols, nvec = n / 8;
-    long long i = tid;
-    for (; i + stride < nvec; i += 2 * stride) {
-      float x[8], y[8];
-      load8(g + 8 * i, x);
-      load8(g + 8 * (i + stride), y);
-      acc = __dadd_rn(acc, __dadd_rn(sumsq8(x), sumsq8(y)));
+  // vector e of the matrix: flat -> g + 8e; rows of c8 vectors -> row e / c8
+  const long long c8 = J.flat ? 0 : (J.vec_rows ? cols / 8 : 0);
+  const long long nvec = J.flat ? rows * cols / 8 : rows * c8;
+  auto at = [&](long long e) -> const T* {
+    if (J.flat) return g + 8 * e;
+    const long long r = e / c8;
+    return g + r * ld + 8 * (e - r * c8);
+  };
+  long long i = tid;
+  for (; i + (R - 1) * stride < nvec; i += R * stride) {
+    Raw8<T> r[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) ld_raw8(at(i + k * stride), r[k]);
+#pragma unroll
+    for (int k = 0; k < R; k += 4) {
+      float x0[8], x1[8], x2[8], x3[8];
+      unpack8(r[k], x0);
+      unpack8(r[k + 1], x1);
+      unpack8(r[k + 2], x2);
+      unpack8(r[k + 3], x3);
+      acc = __dadd_rn(acc, sumsq32(x0, x1, x2, x3));
     }
-    for (; i < nvec; i += stride) {
-      float x[8];
-      load8(g + 8 * i, x);
-      acc = __dadd_rn(acc, sumsq8(x));
-    }
+  }
+  for (; i < nvec; i += stride) {
+    float x[8];
+    load8(at(i), x);
+    acc = __dadd_rn(acc, sumsq8(x));
+  }
+  if (J.flat) {
+    const long long n = rows * cols;
     for (long long k = nvec * 8 + tid; k < n; k += stride) {
       const double d = static_cast<double>(load1(g + k));
       acc = __dadd_rn(acc, __dmul_rn(d, d));
     }
   } else {
-    const long long c8 = vec_rows ? cols / 8 : 0;
-    for (long long e = tid; e < rows * c8; e += stride) {
-      const long long r = e / c8, c = e - r * c8;
-      float x[8];
-      load8(g + r * ld + 8 * c, x);
-      acc = __dadd_rn(acc, sumsq8(x));
-    }
-    const long long tail = cols - 8 * c8;
+    const long long tail = cols - 8 * c8;  // elements of each row past its vectors
     for (long long e = tid; e < rows * tail; e += stride) {
       const long long r = e / tail, c = 8 * c8 + (e - r * tail);
       const double d = static_cast<double>(load1(g + r * ld + c));
       acc = __dadd_rn(acc, __dmul_rn(d, d));
     }
   }
-  finish_sumsq(acc, prep_ws(ws_base, mb), stats + mb, 0.0f);
+  const double block = sum256(acc, static_cast<int>(threadIdx.x), red);
+  if (threadIdx.x == 0) prep_ws(J.ws, mb)->partials[blockIdx.x] = block;
 }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -81,148 +210,324 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&x)[8]) {
   *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(h);
 }
 
-__device__ __forceinline__ float inv_norm(const zopt_clip_stats* st, double eps) {
-  return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(__dsqrt_rn(st->sumsq), eps)));
+// Raw element bits of T (bf16: 16, fp32: 32) and their value.
+template <typename T>
+using RawOf = typename std::conditional<sizeof(T) == 2, unsigned short, unsigned int>::type;
+__device__ __forceinline__ float raw_f32(unsigned short b) { return __uint_as_float(static_cast<unsigned int>(b) << 16); }
+__device__ __forceinline__ float raw_f32(unsigned int b) { return __uint_as_float(b); }
+
+// 1 / (||G_b||_F + eps) of matrix mb, valid in thread 0: every block of the matrix reduces its
+// bpm partials in the same order (threads stride over them, then the 256-thread tree); block 0
+// also keeps the sum in the matrix's stats and zeroes the fused kernel's counters for it.
+__device__ __forceinline__ float prep_inv_norm(const PrepItem& J, int mb, double eps, int tid, bool first_block,
+                                               double* red) {
+  const NormWorkspace* ws = prep_ws(J.ws, mb);
+  double a = 0.0;
+  for (int i = tid; i < J.bpm; i += 256) a = __dadd_rn(a, __ldcg(ws->partials + i));  // from L2: another kernel wrote them
+  const double total = sum256(a, tid, red);
+  if (first_block && tid == 0) {
+    write_clip_stats(J.stats + mb, total, 0.0f);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(J.ws + static_cast<size_t>(mb) * kPrepWsBytes) + kCntWord;
+    cnt[0] = cnt[1] = cnt[2] = 0u;
+  }
+  return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(__dsqrt_rn(total), eps)));
 }
 
 // X0_b = G_b / (||G_b||_F + eps) in the compute dtype U, same orientation (rows <= cols),
-// blockIdx.y = matrix. vec: rows of G are 16-byte aligned with cols % 8 == 0, so each thread
-// moves 8 elements per access; otherwise one element at a time.
+// blockIdx.y = matrix across the list, blockIdx.x = a run of kScaleVecs 8-element vectors.
+// vec: rows of G are 16-byte aligned with cols % 8 == 0, so each thread moves 8 elements per
+// access, kRound loads in flight before their stores (the first round issued before the norm
+// is reduced); otherwise one element at a time.
 template <typename T, typename U>
-__global__ void __launch_bounds__(256) group_scale_kernel(const T* __restrict__ g0, long long rows, long long cols,
-                                                          long long ld, long long batch_stride, int vec,
-                                                          const zopt_clip_stats* stats, double eps,
-                                                          U* __restrict__ x0, long long ldx, long long x_stride) {
+__global__ void __launch_bounds__(256) prep_scale_kernel(const PrepList L) {
+  constexpr int R = kRound<T>;
+  __shared__ double red[8];
   __shared__ float s_inv;
   tc::pdl_launch_dependents();
   tc::pdl_wait();
-  const int mb = blockIdx.y;
-  const T* g = g0 + mb * batch_stride;
-  U* x = x0 + mb * x_stride;
-  if (threadIdx.x == 0) s_inv = inv_norm(stats + mb, eps);
-  __syncthreads();
-  const float inv = s_inv;
-  if (vec) {
-    const long long c8 = cols / 8;
-    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
-      for (long long c = threadIdx.x; c < c8; c += blockDim.x) {
-        float v[8];
-        load8(g + r * ld + 8 * c, v);
+  const PrepItem& J = prep_item(L, blockIdx.y);
+  if (static_cast<long long>(blockIdx.x) >= J.chunks) return;
+  const int mb = static_cast<int>(blockIdx.y) - J.first;
+  const int tid = static_cast<int>(threadIdx.x);
+  const T* g = static_cast<const T*>(J.g) + mb * J.bs;
+  U* x = static_cast<U*>(J.x0) + mb * J.x_stride;
+  const long long rows = J.rows, cols = J.cols, ld = J.ld, ldx = J.ldx;
+  if (J.vec) {
+    const long long c8 = cols / 8, nv = rows * c8;
+    const long long v0 = static_cast<long long>(blockIdx.x) * kScaleVecs + tid;
+    auto g_at = [&](long long e) -> long long {
+      if (J.flat_io) return 8 * e;
+      const long long r = e / c8;
+      return r * ld + 8 * (e - r * c8);
+    };
+    auto x_at = [&](long long e) -> long long {
+      if (J.flat_io) return 8 * e;
+      const long long r = e / c8;
+      return r * ldx + 8 * (e - r * c8);
+    };
+    Raw8<T> raw[R];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] *= inv;
-        store8(x + r * ldx + 8 * c, v);
+    for (int k = 0; k < R; ++k) {
+      const long long e = v0 + static_cast<long long>(k) * 256;
+      if (e < nv) ld_raw8(g + g_at(e), raw[k]);
+    }
+    const float inv_b = prep_inv_norm(J, mb, L.eps, tid, blockIdx.x == 0, red);
+    if (tid == 0) s_inv = inv_b;
+    __syncthreads();
+    const float inv = s_inv;
+#pragma unroll 1
+    for (int u0 = 0; u0 < kScaleVecs / 256; u0 += R) {
+      if (u0 > 0) {
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+          const long long e = v0 + static_cast<long long>(u0 + k) * 256;
+          if (e < nv) ld_raw8(g + g_at(e), raw[k]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        const long long e = v0 + static_cast<long long>(u0 + k) * 256;
+        if (e >= nv) continue;
+        float v[8];
+        unpack8(raw[k], v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] *= inv;
+        store8(x + x_at(e), v);
       }
     }
   } else {
-    for (long long r = blockIdx.x; r < rows; r += gridDim.x)
-      for (long long c = threadIdx.x; c < cols; c += blockDim.x) to_out(to_f32(g[r * ld + c]) * inv, x + r * ldx + c);
+    const float inv_b = prep_inv_norm(J, mb, L.eps, tid, blockIdx.x == 0, red);
+    if (tid == 0) s_inv = inv_b;
+    __syncthreads();
+    const float inv = s_inv;
+    const long long n = rows * cols, e0 = static_cast<long long>(blockIdx.x) * kScaleVecs * 8;
+    const long long e1 = e0 + 8LL * kScaleVecs < n ? e0 + 8LL * kScaleVecs : n;
+    for (long long e = e0 + tid; e < e1; e += 256) {
+      const long long r = e / cols, c = e - r * cols;
+      to_out(to_f32(g[r * ld + c]) * inv, x + r * ldx + c);
+    }
   }
 }
 
-// X0_b = (G_b / (||G_b||_F + eps))' for a tall G (rows > cols): 64 x 64 tiles through shared
-// memory, 32 x 8 threads; pair: G's rows allow 2-element accesses (each warp then reads and
-// writes 128 contiguous bytes of bf16).
-template <typename T, typename U>
-__global__ void __launch_bounds__(256) group_transpose_kernel(const T* __restrict__ g0, long long rows, long long cols,
-                                                              long long ld, long long batch_stride, int pair,
-                                                              const zopt_clip_stats* stats, double eps,
-                                                              U* __restrict__ x0, long long ldx, long long x_stride) {
+// X0_b = (G_b / (||G_b||_F + eps))' in fp32 for a tall G (rows > cols): 64 x 64 tiles through
+// shared memory, 32 x 8 threads, one tile per block; pair: G's rows allow 2-element accesses.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_transpose_f32_kernel(const PrepList L) {
+  __shared__ double red[8];
   __shared__ float s_inv;
   __shared__ float tile[64][65];
   tc::pdl_launch_dependents();
   tc::pdl_wait();
-  const int mb = blockIdx.y;
-  const T* g = g0 + mb * batch_stride;
-  U* x = x0 + mb * x_stride;
-  if (threadIdx.x == 0 && threadIdx.y == 0) s_inv = inv_norm(stats + mb, eps);
+  const PrepItem& J = prep_item(L, blockIdx.y);
+  if (static_cast<long long>(blockIdx.x) >= J.chunks) return;
+  const int mb = static_cast<int>(blockIdx.y) - J.first;
+  const int lin = static_cast<int>(threadIdx.x + 32 * threadIdx.y);
+  const float inv_b = prep_inv_norm(J, mb, L.eps, lin, blockIdx.x == 0, red);
+  if (lin == 0) s_inv = inv_b;
   __syncthreads();
   const float inv = s_inv;
+  const T* g = static_cast<const T*>(J.g) + mb * J.bs;
+  float* x = static_cast<float*>(J.x0) + mb * J.x_stride;
+  const long long rows = J.rows, cols = J.cols, ld = J.ld, ldx = J.ldx;
+  const int pair = J.pair;
   const int tx = threadIdx.x, ty = threadIdx.y;
-  const long long tiles_c = (cols + 63) / 64, tiles_r = (rows + 63) / 64;
-  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * 64, c0 = (tt % tiles_c) * 64;
-    const bool full = r0 + 64 <= rows && c0 + 64 <= cols;
+  const long long tiles_c = (cols + 63) / 64;
+  const long long tt = blockIdx.x;
+  const long long r0 = (tt / tiles_c) * 64, c0 = (tt % tiles_c) * 64;
+  const bool full = r0 + 64 <= rows && c0 + 64 <= cols;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int rr = ty + 8 * k;
-      const long long r = r0 + rr, c = c0 + 2 * tx;
-      if (full && pair) {
-        const float2 v = load2(g + r * ld + c);
-        tile[rr][2 * tx] = v.x * inv;
-        tile[rr][2 * tx + 1] = v.y * inv;
-      } else {
-        tile[rr][2 * tx] = (r < rows && c < cols) ? to_f32(g[r * ld + c]) * inv : 0.0f;
-        tile[rr][2 * tx + 1] = (r < rows && c + 1 < cols) ? to_f32(g[r * ld + c + 1]) * inv : 0.0f;
-      }
+  for (int k = 0; k < 8; ++k) {
+    const int rr = ty + 8 * k;
+    const long long r = r0 + rr, c = c0 + 2 * tx;
+    if (full && pair) {
+      const float2 v = load2(g + r * ld + c);
+      tile[rr][2 * tx] = v.x * inv;
+      tile[rr][2 * tx + 1] = v.y * inv;
+    } else {
+      tile[rr][2 * tx] = (r < rows && c < cols) ? to_f32(g[r * ld + c]) * inv : 0.0f;
+      tile[rr][2 * tx + 1] = (r < rows && c + 1 < cols) ? to_f32(g[r * ld + c + 1]) * inv : 0.0f;
     }
-    __syncthreads();
+  }
+  __syncthreads();
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int cc = ty + 8 * k;                    // X0 row = G column c0 + cc
-      const long long xr = c0 + cc, xc = r0 + 2 * tx;  // X0[c][r] = G[r][c]
-      if (full) {
-        store2(x + xr * ldx + xc, tile[2 * tx][cc], tile[2 * tx + 1][cc]);
-      } else {
-        if (xr < cols && xc < rows) to_out(tile[2 * tx][cc], x + xr * ldx + xc);
-        if (xr < cols && xc + 1 < rows) to_out(tile[2 * tx + 1][cc], x + xr * ldx + xc + 1);
-      }
+  for (int k = 0; k < 8; ++k) {
+    const int cc = ty + 8 * k;                       // X0 row = G column c0 + cc
+    const long long xr = c0 + cc, xc = r0 + 2 * tx;  // X0[c][r] = G[r][c]
+    if (full) {
+      store2(x + xr * ldx + xc, tile[2 * tx][cc], tile[2 * tx + 1][cc]);
+    } else {
+      if (xr < cols && xc < rows) to_out(tile[2 * tx][cc], x + xr * ldx + xc);
+      if (xr < cols && xc + 1 < rows) to_out(tile[2 * tx + 1][cc], x + xr * ldx + xc + 1);
     }
-    __syncthreads();
   }
 }
 
-// X0 = G / (||G||_F + eps), oriented, for every matrix of the group (its prep scratch, and so
-// its counters, zeroed first).
-zopt_status group_prep(const Group& G, float eps, int sms, cudaStream_t s) {
-  zopt_status st = ZOPT_OK;
-  const long long rows = G.rows, cols = G.cols, ld_g = G.ld_g, bs_g = G.bs_g;
-  const size_t esz = G.esz;
-  const int gs = G.gs;
-  ZOPT_CUDA_TRY(cudaMemsetAsync(G.ws, 0, static_cast<size_t>(gs) * kPrepWsBytes, s));
-  const bool aligned = (reinterpret_cast<uintptr_t>(G.g) & 15u) == 0 && (bs_g * esz) % 16 == 0;
-  const int flat = (aligned && ld_g == cols) ? 1 : 0;
-  const int vec_rows = (aligned && (ld_g * esz) % 16 == 0) ? 1 : 0;
-  // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
-  // is bitwise the same whatever group it runs in
-  long long bpm = (rows * cols + 8191) / 8192;  // short per-thread chains for small matrices
-  bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
-  const dim3 sg(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
-  st = G.io == ZOPT_F32
-           ? launch_pdl(group_sumsq_kernel<float>, sg, dim3(kNormThreads), 0, s, reinterpret_cast<const float*>(G.g),
-                        rows, cols, ld_g, bs_g, flat, vec_rows, G.ws, G.stats)
-           : launch_pdl(group_sumsq_kernel<__nv_bfloat16>, sg, dim3(kNormThreads), 0, s,
-                        reinterpret_cast<const __nv_bfloat16*>(G.g), rows, cols, ld_g, bs_g, flat, vec_rows, G.ws,
-                        G.stats);
-  if (st != ZOPT_OK) return st;
-  int sblk = (sms * 8 + gs - 1) / gs;
-  sblk = sblk < 1 ? 1 : sblk;
-  const dim3 sgrid(static_cast<unsigned>(sblk), static_cast<unsigned>(gs));
-  const zopt_clip_stats* stats = G.stats;
-  if (!G.transpose) {
-    const int vec = (aligned && (ld_g * esz) % 16 == 0 && cols % 8 == 0) ? 1 : 0;
-#define ZOPT_SCALE(TI, TO)                                                                                 \
-  st = launch_pdl(group_scale_kernel<TI, TO>, sgrid, dim3(256), 0, s, reinterpret_cast<const TI*>(G.g), rows, \
-                  cols, ld_g, bs_g, vec, stats, static_cast<double>(eps), reinterpret_cast<TO*>(G.xb[0]),       \
-                  G.p.ldx, G.mat_elems)
-    if (G.io == ZOPT_F32 && G.f32c) ZOPT_SCALE(float, float);
-    else if (G.io == ZOPT_F32) ZOPT_SCALE(float, __nv_bfloat16);
-    else if (G.f32c) ZOPT_SCALE(__nv_bfloat16, float);
-    else ZOPT_SCALE(__nv_bfloat16, __nv_bfloat16);
-#undef ZOPT_SCALE
-  } else {
-    const int pair = ((reinterpret_cast<uintptr_t>(G.g) % (2 * esz)) == 0 && ld_g % 2 == 0 && bs_g % 2 == 0) ? 1 : 0;
-    const dim3 tb(32, 8);
-#define ZOPT_TRANSPOSE(TI, TO)                                                                            \
-  st = launch_pdl(group_transpose_kernel<TI, TO>, sgrid, tb, 0, s, reinterpret_cast<const TI*>(G.g), rows,   \
-                  cols, ld_g, bs_g, pair, stats, static_cast<double>(eps), reinterpret_cast<TO*>(G.xb[0]),     \
-                  G.p.ldx, G.mat_elems)
-    if (G.io == ZOPT_F32 && G.f32c) ZOPT_TRANSPOSE(float, float);
-    else if (G.io == ZOPT_F32) ZOPT_TRANSPOSE(float, __nv_bfloat16);
-    else if (G.f32c) ZOPT_TRANSPOSE(__nv_bfloat16, float);
-    else ZOPT_TRANSPOSE(__nv_bfloat16, __nv_bfloat16);
-#undef ZOPT_TRANSPOSE
+// X0_b = (G_b / (||G_b||_F + eps))' in bf16 for a tall G (rows > cols), one tile per block:
+// 64 G rows x 32 16-byte pieces (256 bf16 or 128 fp32 columns). Each warp reads whole 512-byte
+// row runs (8 loads in flight per thread, issued before the norm is reduced) into a
+// row-swizzled shared tile (piece q of row r at q ^ ((r >> 3) & 7)), then each thread gathers
+// 8 consecutive G rows of one G column — 16 bytes of an X0 row, a warp writing four 128-byte
+// runs; both sides are bank-conflict free. The value written is bf16(float(g) * inv), as the
+// scaling kernel computes it.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_transpose_bf16_kernel(const PrepList L) {
+  constexpr int VT = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
+  constexpr int TC = 32 * VT;                             // tile columns
+  using Raw = RawOf<T>;
+  __shared__ double red[8];
+  __shared__ float s_inv;
+  __shared__ __align__(16) uint8_t tile[64 * 512];
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();
+  const PrepItem& J = prep_item(L, blockIdx.y);
+  if (static_cast<long long>(blockIdx.x) >= J.chunks) return;
+  const int mb = static_cast<int>(blockIdx.y) - J.first;
+  const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, w = tid >> 5;
+  const Raw* g = static_cast<const Raw*>(J.g) + mb * J.bs;
+  __nv_bfloat16* x = static_cast<__nv_bfloat16*>(J.x0) + mb * J.x_stride;
+  const long long rows = J.rows, cols = J.cols, ld = J.ld, ldx = J.ldx;
+  const long long tiles_c = (cols + TC - 1) / TC;
+  const long long r0 = (static_cast<long long>(blockIdx.x) / tiles_c) * 64;
+  const long long c0 = (static_cast<long long>(blockIdx.x) % tiles_c) * TC;
+  uint4 buf[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const long long r = r0 + k * 8 + w, c = c0 + static_cast<long long>(lane) * VT;
+    if (J.tvec && r < rows && c + VT <= cols) {
+      buf[k] = __ldg(reinterpret_cast<const uint4*>(g + r * ld + c));
+    } else {
+      Raw e[VT];
+#pragma unroll
+      for (int i = 0; i < VT; ++i) e[i] = (r < rows && c + i < cols) ? g[r * ld + c + i] : Raw(0);
+      memcpy(&buf[k], e, 16);
+    }
   }
-  if (st != ZOPT_OK) return st;
+  const float inv_b = prep_inv_norm(J, mb, L.eps, tid, blockIdx.x == 0, red);
+  if (tid == 0) s_inv = inv_b;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<uint4*>(tile + (k * 8 + w) * 512 + ((lane ^ k) << 4)) = buf[k];
+  __syncthreads();
+  const float inv = s_inv;
+#pragma unroll
+  for (int k = 0; k < VT; ++k) {
+    const int v = k * 256 + tid, xl = v >> 3, seg = v & 7;  // X0 row c0 + xl, G rows seg*8 ..
+    const long long xr = c0 + xl, xc = r0 + seg * 8;
+    const uint8_t* col = tile + ((xl % VT) * static_cast<int>(sizeof(T)));
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rr = seg * 8 + j;
+      o[j] = raw_f32(*reinterpret_cast<const Raw*>(col + rr * 512 + (((xl / VT) ^ seg) << 4))) * inv;
+    }
+    if (xr >= cols) continue;
+    __nv_bfloat16* dst = x + xr * ldx + xc;
+    if (xc + 8 <= rows) {
+      store8(dst, o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (xc + j < rows) to_out(o[j], dst + j);
+    }
+  }
+}
+
+namespace {
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Launches one list: K selects the kernel (0 sum of squares, 1 scale, 2 transpose).
+template <int K, typename T, typename U>
+zopt_status launch_list(PrepList& L, int matrices, long long max_x, cudaStream_t s) {
+  if (L.n == 0) return ok();
+  const dim3 grid(static_cast<unsigned>(max_x), static_cast<unsigned>(matrices));
+  zopt_status st = ZOPT_OK;
+  if constexpr (K == 0) st = launch_pdl(prep_sumsq_kernel<T>, grid, dim3(kNormThreads), 0, s, L);
+  else if constexpr (K == 1) st = launch_pdl(prep_scale_kernel<T, U>, grid, dim3(256), 0, s, L);
+  else if constexpr (std::is_same<U, float>::value)
+    st = launch_pdl(prep_transpose_f32_kernel<T>, grid, dim3(32, 8), 0, s, L);
+  else st = launch_pdl(prep_transpose_bf16_kernel<T>, grid, dim3(256), 0, s, L);
+  L.n = 0;
+  return st;
+}
+
+// Builds the lists of kernel K for input dtype T and compute dtype U over the groups that take
+// it, and launches them (at most kMaxPrepItems groups and 65535 matrices per launch).
+template <int K, typename T, typename U>
+zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
+  PrepList L{};
+  L.eps = static_cast<double>(eps);
+  int matrices = 0;
+  long long max_x = 1;
+  zopt_status st = ZOPT_OK;
+  for (int q = 0; q < n; ++q) {
+    const Group& G = groups[q];
+    const bool t_in = (G.io == ZOPT_F32) == std::is_same<T, float>::value;
+    const bool u_out = G.f32c == std::is_same<U, float>::value;
+    if (!t_in || (K != 0 && !u_out) || (K == 1 && G.transpose) || (K == 2 && !G.transpose)) continue;
+    if (L.n == kMaxPrepItems || matrices + G.gs > 65535) {
+      if ((st = launch_list<K, T, U>(L, matrices, max_x, s)) != ZOPT_OK) return st;
+      matrices = 0;
+      max_x = 1;
+    }
+    const size_t esz = G.esz;
+    const long long rows = G.rows, cols = G.cols, ld_g = G.ld_g, bs_g = G.bs_g;
+    const bool aligned = (reinterpret_cast<uintptr_t>(G.g) & 15u) == 0 && (bs_g * esz) % 16 == 0;
+    const bool rows16 = aligned && (ld_g * esz) % 16 == 0;
+    PrepItem& it = L.it[L.n++];
+    it.g = G.g;
+    it.rows = rows;
+    it.cols = cols;
+    it.ld = ld_g;
+    it.bs = bs_g;
+    it.flat = (aligned && ld_g == cols) ? 1 : 0;
+    it.vec_rows = rows16 ? 1 : 0;
+    it.vec = (rows16 && cols % 8 == 0) ? 1 : 0;
+    it.flat_io = (it.vec && ld_g == cols && G.p.ldx == cols) ? 1 : 0;
+    it.pair = ((reinterpret_cast<uintptr_t>(G.g) % (2 * esz)) == 0 && ld_g % 2 == 0 && bs_g % 2 == 0) ? 1 : 0;
+    it.tvec = rows16 ? 1 : 0;
+    // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
+    // is bitwise the same whatever group or list it runs in
+    long long bpm = ceil_div(rows * cols, kSumsqElems);
+    bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
+    it.bpm = static_cast<int>(bpm);
+    if (K == 0) it.chunks = bpm;
+    else if (K == 1) it.chunks = it.vec ? ceil_div(rows * (cols / 8), kScaleVecs) : ceil_div(rows * cols, 8LL * kScaleVecs);
+    else if (std::is_same<U, float>::value) it.chunks = ceil_div(rows, 64) * ceil_div(cols, 64);
+    else it.chunks = ceil_div(rows, 64) * ceil_div(cols, 32LL * (16 / static_cast<long long>(sizeof(T))));
+    it.chunks = std::max(1LL, it.chunks);
+    if (it.chunks > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: matrix too large");
+    it.first = matrices;
+    it.ws = G.ws;
+    it.stats = G.stats;
+    it.x0 = G.xb[0];
+    it.ldx = G.p.ldx;
+    it.x_stride = G.mat_elems;
+    matrices += G.gs;
+    max_x = std::max(max_x, it.chunks);
+  }
+  return launch_list<K, T, U>(L, matrices, max_x, s);
+}
+
+}  // namespace
+
+// X0 = G / (||G||_F + eps), oriented, for every matrix of every group: one sum-of-squares launch
+// per input dtype, then one scaling and one transpose launch per input and compute dtype that
+// occur (each matrix's partial sums are reduced by the blocks that normalise it; its block 0
+// also zeroes its counters for the fused kernel).
+zopt_status group_prep(const Group* groups, int n, float eps, int sms, cudaStream_t s) {
+  (void)sms;
+  zopt_status st = ZOPT_OK;
+  if ((st = prep_pass<0, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<0, float, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<1, __nv_bfloat16, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<1, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<1, float, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<1, float, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<2, __nv_bfloat16, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<2, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<2, float, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<2, float, float>(groups, n, eps, s)) != ZOPT_OK) return st;
   ZOPT_CUDA_TRY(cudaGetLastError());
   return ok();
 }

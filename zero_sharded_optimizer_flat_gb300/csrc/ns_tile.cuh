@@ -660,8 +660,8 @@ struct Group {
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], mx_e[2], ma_p, ma_q, mb_p, ma_e, mb_e, mo_e;
 };
 
-// X0 = G / (||G||_F + eps), oriented, for every matrix of the group.
-zopt_status group_prep(const Group& G, float eps, int sms, cudaStream_t s);
+// X0 = G / (||G||_F + eps), oriented, for every matrix of n groups (a handful of launches in all).
+zopt_status group_prep(const Group* groups, int n, float eps, int sms, cudaStream_t s);
 
 }  // namespace ns
 }  // namespace zopt
