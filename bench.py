@@ -251,9 +251,14 @@ class NsPart:
                                         for G, _ in self.groups), dtype=torch.uint8, device="cuda")
         self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
         fused = sum(1 for G, _ in self.groups if min(G.shape[1], G.shape[2]) < 1024)
-        # per shape: norm + normalise/orient; then one fused launch per six small shapes, or
-        # three products per step for the large ones
-        self.launches = 2 * len(self.groups) + -(-fused // 6) + 3 * steps * (len(self.groups) - fused)
+        # the norm of every matrix in one launch (bf16 input), then one scaling launch if any
+        # shape is wide or square and one transpose launch if any is tall (at most 16 shapes
+        # to a launch); then one fused launch per six small shapes, or three products per step
+        # for the large ones
+        wide = sum(1 for G, _ in self.groups if G.shape[1] <= G.shape[2])
+        tall = len(self.groups) - wide
+        prep = -(-len(self.groups) // 16) + -(-wide // 16) + -(-tall // 16)
+        self.launches = prep + -(-fused // 6) + 3 * steps * (len(self.groups) - fused)
         names = (["ns_fused_kernel (X X', B', B'X of every step, shapes below 1024)"] if fused else []) + \
                 (["gemm_bf16_pair_kernel (X X', B', B'X on CTA pairs)"] if fused < len(self.groups) else [])
         self.kernel = " + ".join(names)
