@@ -287,3 +287,25 @@ def test_rescale_to_the_clip_coefficient(zopt):
     OA.rescale_step_f32(*spec, g, 1.0, float(coef), H, 2)
     for r, t in zip(spec, (case.p, case.m, case.v)):
         assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [1, 7, 2047, 2048, 2049, 6149])
+def test_rescale_tile_edges(zopt, n):
+    """The rescale kernel walks whole 2048-element tiles and then the tail element by element:
+    shards below one tile, exactly one or two tiles, and a tile plus a ragged tail are each bit
+    for bit the oracle's re-targeting, bf16 weights included."""
+    case = Case(zopt, [workloads.Param("w", (n,), True)], 1 << 20, 1, 0, seed=n, gdtype=torch.bfloat16)
+    for s in range(2):
+        case.step(s, H, max_norm=1e9)
+    g = case.shard([x.float().numpy() for x in workloads.flat_grads(case.params, n, 2, dtype=torch.bfloat16)])
+    g_dev = torch.from_numpy(g).cuda().bfloat16()
+    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, clip_stats=None,
+                    adam_state=case.state)
+    spec = [t.cpu().numpy() for t in (case.p, case.m, case.v)]
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, old_scale=1.0,
+                            new_scale=0.5, adam_state=case.state)
+    torch.cuda.synchronize()
+    OA.rescale_step_f32(*spec, g, 1.0, 0.5, H, 3)
+    for r, t in zip(spec, (case.p, case.m, case.v)):
+        assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))
+    assert np.array_equal(case.out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(spec[0]))

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "zopt")
 LIB = os.path.join(PKG, "libzopt.so")
 
-SOURCES = ["common.cpp", "layout.cpp", "norm.cu", "norm_noalloc.cu", "adamw.cu", "accum.cu", "ns.cu", "ns_gemm.cu",
+SOURCES = ["common.cpp", "layout.cpp", "norm.cu", "norm_noalloc.cu", "adamw.cu", "rescale.cu", "accum.cu", "ns.cu", "ns_gemm.cu",
            "ns_prep.cu", "ns_fused.cu", "ns_simt.cu", "muon.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -23,54 +23,19 @@
 
 #include <cmath>
 
+#include "adam_common.cuh"
 #include "internal.h"
 
 namespace zopt {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kGroup = 4;                        // elements per vector access
-constexpr int kTile = kThreads * kGroup * 2;     // 2048 elements per tile
-constexpr int kBlocksPerSm = 4;
+using namespace adam;
 
 struct HostScalars {
   float b1, omb1, b2, omb2, eps, decay;  // fp64 -> fp32 once
   double lr, beta1, beta2;               // for the t-dependent scalars
   int skip_on_inf;
 };
-
-__device__ __forceinline__ double pow_sq_mul(double base, long long e) {
-  double r = 1.0;
-  while (e > 0) {
-    if (e & 1) r = __dmul_rn(r, base);
-    base = __dmul_rn(base, base);
-    e >>= 1;
-  }
-  return r;
-}
-
-struct Vec4 { float x[4]; };
-
-__device__ __forceinline__ Vec4 ld4(const float* p) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  return Vec4{{a.x, a.y, a.z, a.w}};
-}
-__device__ __forceinline__ void st4(float* p, const Vec4& v) {
-  *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
-}
-__device__ __forceinline__ Vec4 ldg4(const float* p) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  return Vec4{{a.x, a.y, a.z, a.w}};
-}
-__device__ __forceinline__ Vec4 ldg4(const __nv_bfloat16* p) {
-  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-  return Vec4{{__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-               __uint_as_float(u.y & 0xFFFF0000u)}};
-}
-__device__ __forceinline__ float ldg1(const float* p) { return __ldg(p); }
-__device__ __forceinline__ float ldg1(const __nv_bfloat16* p) {
-  return __uint_as_float(static_cast<unsigned int>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
-}
 
 struct StepScalars {
   float coef, b1, omb1, b2, omb2, eps, decay, step_size, bc2s;
@@ -85,10 +50,6 @@ __device__ __forceinline__ void adamw_elem(float& p, float& m, float& v, float g
   v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
   const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.bc2s), s.eps);
   p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, d)));
-}
-
-__device__ __forceinline__ unsigned short bf16_bits(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 // Is shard slot x inside one of the no-decay runs [runs[2k], runs[2k+1]) with k >= cur
@@ -223,100 +184,6 @@ zopt_status launch(const HostScalars& hs, float* P, float* M, float* V, const vo
   return ok();
 }
 
-// ------------------------------------------------------------------ rescale of a taken step
-//
-// DeepSpeed PR #9021, adam_rescale_step commit: given the weights and moments after step t on
-// g*old_scale, write those of step t on g*new_scale from the same starting point, in one
-// pass: m += (1-b1)(new-old)g; v = max(0, v + (1-b2)(new^2-old^2)g^2) (a NaN stays NaN);
-// p += step_size*(m_old/d_old - m_new/d_new) (the decoupled decay does not depend on g).
-
-struct RescaleHost {
-  double beta1, beta2, lr, old_scale, new_scale;
-  float eps;
-};
-
-__device__ __forceinline__ float adam_dir(float m, float v, float bc2s, float eps) {
-  return __fdiv_rn(m, __fadd_rn(__fdiv_rn(__fsqrt_rn(v), bc2s), eps));
-}
-
-template <typename G, bool kOut>
-__global__ void __launch_bounds__(kThreads) rescale_kernel(float* __restrict__ P, float* __restrict__ M,
-                                                            float* __restrict__ V, const G* __restrict__ Gr,
-                                                            uint16_t* __restrict__ out, int64_t n, RescaleHost hs,
-                                                            const zopt_clip_stats* clip,
-                                                            const zopt_adam_state* state) {
-  __shared__ float s_km, s_kv, s_step, s_bc2s;
-  __shared__ int s_skip;
-  if (threadIdx.x == 0) {
-    const long long t = *reinterpret_cast<const volatile long long*>(&state->step);
-    double nw = hs.new_scale;
-    int skip = t < 1 ? 1 : 0;  // no step has been taken yet: nothing to re-target
-    if (clip != nullptr) {
-      nw = static_cast<double>(*reinterpret_cast<const volatile float*>(&clip->clip_coef));
-      if (*reinterpret_cast<const volatile uint8_t*>(&clip->found_inf)) skip = 1;
-    }
-    const double od = hs.old_scale;
-    s_km = __double2float_rn(__dmul_rn(__dsub_rn(1.0, hs.beta1), __dsub_rn(nw, od)));
-    s_kv = __double2float_rn(__dmul_rn(__dsub_rn(1.0, hs.beta2), __dsub_rn(__dmul_rn(nw, nw), __dmul_rn(od, od))));
-    const double bc1 = __dsub_rn(1.0, pow_sq_mul(hs.beta1, t));
-    const double bc2 = __dsub_rn(1.0, pow_sq_mul(hs.beta2, t));
-    s_step = __double2float_rn(__ddiv_rn(hs.lr, bc1));
-    s_bc2s = __double2float_rn(__dsqrt_rn(bc2));
-    s_skip = skip;
-  }
-  __syncthreads();
-  if (s_skip) return;
-  const float km = s_km, kv = s_kv, step = s_step, bc2s = s_bc2s, eps = hs.eps;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t n4 = n / 4;
-  auto one = [&](float& p, float& m, float& v, float g) {
-    const float u_old = adam_dir(m, v, bc2s, eps);
-    m = __fadd_rn(m, __fmul_rn(km, g));
-    const float vv = __fadd_rn(v, __fmul_rn(kv, __fmul_rn(g, g)));
-    v = vv < 0.0f ? 0.0f : vv;
-    const float u_new = adam_dir(m, v, bc2s, eps);
-    p = __fadd_rn(p, __fmul_rn(step, __fsub_rn(u_old, u_new)));
-  };
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
-    Vec4 p = ld4(P + 4 * j), m = ld4(M + 4 * j), v = ld4(V + 4 * j);
-    const Vec4 g = ldg4(Gr + 4 * j);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) one(p.x[k], m.x[k], v.x[k], g.x[k]);
-    st4(P + 4 * j, p);
-    st4(M + 4 * j, m);
-    st4(V + 4 * j, v);
-    if (kOut) {
-      *reinterpret_cast<uint2*>(out + 4 * j) =
-          make_uint2(static_cast<unsigned int>(bf16_bits(p.x[0])) | (static_cast<unsigned int>(bf16_bits(p.x[1])) << 16),
-                     static_cast<unsigned int>(bf16_bits(p.x[2])) | (static_cast<unsigned int>(bf16_bits(p.x[3])) << 16));
-    }
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t k = n4 * 4; k < n; ++k) {
-      float p = P[k], m = M[k], v = V[k];
-      one(p, m, v, ldg1(Gr + k));
-      P[k] = p;
-      M[k] = m;
-      V[k] = v;
-      if (kOut) out[k] = bf16_bits(p);
-    }
-  }
-}
-
-template <typename G, bool kOut>
-zopt_status launch_rescale(const RescaleHost& hs, float* P, float* M, float* V, const void* g, uint16_t* out,
-                           int64_t n, const zopt_clip_stats* clip, const zopt_adam_state* state, cudaStream_t s) {
-  const int sms = sm_count();
-  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_adamw_rescale_step: no CUDA device");
-  int64_t blocks = (n / 4 + kThreads - 1) / kThreads;
-  if (blocks > static_cast<int64_t>(sms) * kBlocksPerSm) blocks = static_cast<int64_t>(sms) * kBlocksPerSm;
-  if (blocks < 1) blocks = 1;
-  rescale_kernel<G, kOut><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(P, M, V, static_cast<const G*>(g), out,
-                                                                             n, hs, clip, state);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  return ok();
-}
-
 }  // namespace
 }  // namespace zopt
 
@@ -372,38 +239,4 @@ extern "C" zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t*
                                         d_clip, d_state, s)
                   : launch<float, false>(hs, master, exp_avg, exp_avg_sq, grad, nullptr, n, d_nodecay_runs, nruns,
                                          d_clip, d_state, s);
-}
-
-extern "C" zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* master, float* exp_avg,
-                                               float* exp_avg_sq, const void* grad, zopt_dtype grad_dtype,
-                                               uint16_t* out_bf16, const zopt_adamw_hparams* hp, float old_scale,
-                                               float new_scale, const zopt_clip_stats* d_clip,
-                                               const zopt_adam_state* d_state, zopt_stream stream) {
-  using namespace zopt;
-  if (layout == nullptr || hp == nullptr) return fail(ZOPT_EINVAL, "zopt_adamw_rescale_step: layout or hparams is NULL");
-  if (master == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || grad == nullptr || d_state == nullptr)
-    return fail(ZOPT_EINVAL, "zopt_adamw_rescale_step: NULL device pointer");
-  if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(grad) ||
-      (out_bf16 != nullptr && !aligned16(out_bf16)) || (reinterpret_cast<uintptr_t>(d_state) & 7u) != 0 ||
-      (d_clip != nullptr && (reinterpret_cast<uintptr_t>(d_clip) & 7u) != 0))
-    return fail(ZOPT_EINVAL, "zopt_adamw_rescale_step: a device pointer is misaligned");
-  if (grad_dtype != ZOPT_F32 && grad_dtype != ZOPT_BF16)
-    return fail(ZOPT_EUNSUPPORTED, "zopt_adamw_rescale_step: gradient dtype must be fp32 or bf16");
-  if (!std::isfinite(hp->lr) || hp->lr < 0.0 || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) ||
-      !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) || !std::isfinite(hp->eps) || hp->eps < 0.0)
-    return fail(ZOPT_EINVAL, "zopt_adamw_rescale_step: hyper-parameters out of range");
-  if (!std::isfinite(old_scale) || (d_clip == nullptr && !std::isfinite(new_scale)))
-    return fail(ZOPT_EINVAL, "zopt_adamw_rescale_step: scales must be finite");
-  RescaleHost hs{hp->beta1, hp->beta2, hp->lr, static_cast<double>(old_scale), static_cast<double>(new_scale),
-                 static_cast<float>(hp->eps)};
-  const int64_t n = layout->shard_len;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (grad_dtype == ZOPT_BF16)
-    return out_bf16 ? launch_rescale<__nv_bfloat16, true>(hs, master, exp_avg, exp_avg_sq, grad, out_bf16, n, d_clip,
-                                                          d_state, s)
-                    : launch_rescale<__nv_bfloat16, false>(hs, master, exp_avg, exp_avg_sq, grad, nullptr, n, d_clip,
-                                                           d_state, s);
-  return out_bf16 ? launch_rescale<float, true>(hs, master, exp_avg, exp_avg_sq, grad, out_bf16, n, d_clip, d_state, s)
-                  : launch_rescale<float, false>(hs, master, exp_avg, exp_avg_sq, grad, nullptr, n, d_clip, d_state,
-                                                 s);
 }
