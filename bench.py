@@ -253,12 +253,13 @@ class NsPart:
         fused = sum(1 for G, _ in self.groups if min(G.shape[1], G.shape[2]) < 1024)
         # the norm of every matrix in one launch (bf16 input), then one scaling launch if any
         # shape is wide or square and one transpose launch if any is tall (at most 16 shapes
-        # to a launch); then one fused launch per six small shapes, or three products per step
-        # for the large ones
+        # to a launch); then one fused launch per six small shapes, and for the large ones each
+        # product of a step in one launch per four shapes
         wide = sum(1 for G, _ in self.groups if G.shape[1] <= G.shape[2])
         tall = len(self.groups) - wide
         prep = -(-len(self.groups) // 16) + -(-wide // 16) + -(-tall // 16)
-        self.launches = prep + -(-fused // 6) + 3 * steps * (len(self.groups) - fused)
+        large = len(self.groups) - fused
+        self.launches = prep + -(-fused // 6) + 3 * steps * -(-large // 4)
         names = (["ns_fused_kernel (X X', B', B'X of every step, shapes below 1024)"] if fused else []) + \
                 (["gemm_bf16_pair_kernel (X X', B', B'X on CTA pairs)"] if fused < len(self.groups) else [])
         self.kernel = " + ".join(names)

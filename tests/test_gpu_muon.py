@@ -131,3 +131,34 @@ def test_many_shapes_equal_single_calls(zopt):
             if d["out"][0] is not None:
                 assert torch.equal(d["out"][0], d["out"][1])
             assert torch.equal(d["st"][0], d["st"][1])
+
+
+@pytest.mark.parametrize("rows,cols,batch,shift", [(129, 77, 1, 1), (96, 100, 2, 2), (1, 3, 1, 0)])
+def test_odd_sizes_and_unaligned_out(zopt, rows, cols, batch, shift):
+    """The statistics and update kernels move 4-element vectors and finish a matrix whose size is
+    not a multiple of 4 element by element; the bf16 round-out takes 8-byte stores only when the
+    output allows them (a base shifted by `shift` elements does not). Master, momentum and bf16
+    weights as the oracle gives them (the update within the Newton-Schulz tolerance)."""
+    h = OM.MuonHyper(lr=8e-4, match_rms_adamw=True)
+    gen = torch.Generator(device="cuda").manual_seed(rows * cols + shift)
+    p = torch.randn(batch, rows, cols, generator=gen, device="cuda") * 0.02
+    buf = torch.zeros_like(p)
+    flat = torch.zeros(batch * rows * cols + shift, dtype=torch.int16, device="cuda")
+    out = flat[shift:].view(batch, rows, cols)
+    stats = zopt.new_muon_stats(batch)
+    g = (torch.randn(batch, rows, cols, generator=gen, device="cuda") * 1e-3).bfloat16()
+    p_old = p.cpu().numpy()
+    zopt.muon_step(p, buf, g, out, zopt.new_muon_workspace(rows, cols), stats, lr=h.lr, match_rms_adamw=True)
+    torch.cuda.synchronize()
+    pn = p.cpu().numpy()
+    decay = np.float32(1.0 - h.lr * h.weight_decay)
+    step = np.float32(h.lr * OM.lr_scale(rows, cols, True))
+    st = zopt.read_muon_stats(stats)
+    for b in range(batch):
+        u = OM.momentum_f32(np.zeros((rows, cols), np.float32), g[b].float().cpu().numpy(), h)
+        U_ref = newton_schulz(u.astype(np.float64), steps=5)
+        applied = (p_old[b] * decay - pn[b]).astype(np.float64) / float(step)
+        assert rel(applied, U_ref) <= 2e-2, b
+        assert not st[b]["rejected"]
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))
+    assert int(flat[:shift].abs().sum()) == 0  # nothing written before the output

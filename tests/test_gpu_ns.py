@@ -371,3 +371,30 @@ def test_many_jobs_step_counts(zopt, steps):
         assert torch.equal(one, X), (r, c, steps)
         ref = newton_schulz(G[0].double().cpu().numpy(), steps=steps)
         assert rel(X[0].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
+def test_many_pair_jobs_batched(zopt):
+    """zopt_ns_orthogonalize_many runs each product of a step for all its CTA-pair jobs (m >= 1024)
+    in one launch, four jobs to a launch and those with the same epilogue together: six pair jobs
+    of different shapes, dtypes and orientations (two launches per product), one whose output the
+    TMA cannot address (its last product by plain stores, in a launch of its own) and a fused job
+    beside them. Each result is bitwise its single call's; one is checked against the oracle."""
+    gen = torch.Generator(device="cuda").manual_seed(29)
+    specs = [(1, 1024, 1024, torch.bfloat16, 0), (2, 1024, 1536, torch.bfloat16, 0), (1, 1100, 1300, torch.float32, 0),
+             (1, 2000, 1030, torch.bfloat16, 0), (1, 1030, 1100, torch.bfloat16, 3), (1, 1280, 1024, torch.float32, 0),
+             (2, 300, 700, torch.bfloat16, 0)]
+    pairs, shapes = [], []
+    for b, r, c, dt, pad in specs:
+        G = torch.randn(b, r, c, generator=gen, device="cuda").to(dt)
+        X = torch.zeros(b, r, c + pad, device="cuda", dtype=dt)[:, :, :c]
+        pairs.append((G, X))
+        shapes.append((r, c, b))
+    zopt.ns_orthogonalize_many(pairs, zopt.new_ns_workspace_many(shapes), steps=3)
+    torch.cuda.synchronize()
+    for (G, X), (r, c, b) in zip(pairs, shapes):
+        one = torch.empty(b, r, c, device="cuda", dtype=G.dtype)
+        zopt.ns_orthogonalize(G, one, zopt.new_ns_workspace(r, c, b), steps=3)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X), (r, c, b)
+    ref = newton_schulz(pairs[3][0][0].double().cpu().numpy(), steps=3)
+    assert rel(pairs[3][1][0].cpu(), torch.from_numpy(ref)) <= 2e-2

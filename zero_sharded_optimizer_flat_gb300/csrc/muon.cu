@@ -75,8 +75,11 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(float* __restrict__ 
   }
 }
 
-// Per matrix (blockIdx.y): sum of squares of U (fp64, as the norm kernel) and max |U| (the
-// fp32 bit patterns of non-negative values order as unsigned integers; NaN sorts above inf).
+// Per matrix (blockIdx.y): sum of squares of U and max |U| (the fp32 bit patterns of
+// non-negative values order as unsigned integers; NaN sorts above inf). Threads stride over
+// 4-element vectors, 8 loads (128 bytes) in flight per round; squares are summed in fp32 over
+// runs of 32 (sumsq32: exact fp64 outside the safe range) and the runs in fp64; one partial per
+// block, the last block of the matrix adding them in a fixed order.
 __global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restrict__ U0, int64_t n, uint8_t* red,
                                                            unsigned* maxbits, zopt_clip_stats* cs) {
   const int mb = blockIdx.y;
@@ -85,11 +88,28 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restric
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   double acc = 0.0;
   unsigned mx = 0;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
-    const float4 x = load4(U + 4 * j);
+  auto amax = [](unsigned m, const float4& x) {
+    return max(m, max(max(__float_as_uint(x.x) & 0x7FFFFFFFu, __float_as_uint(x.y) & 0x7FFFFFFFu),
+                      max(__float_as_uint(x.z) & 0x7FFFFFFFu, __float_as_uint(x.w) & 0x7FFFFFFFu)));
+  };
+  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; j + 7 * stride < n4; j += 8 * stride) {
+    float4 x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = __ldg(reinterpret_cast<const float4*>(U) + j + k * stride);
+    float r[4][8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float* d = r[k >> 1] + 4 * (k & 1);
+      d[0] = x[k].x; d[1] = x[k].y; d[2] = x[k].z; d[3] = x[k].w;
+      mx = amax(mx, x[k]);
+    }
+    acc = __dadd_rn(acc, sumsq32(r[0], r[1], r[2], r[3]));
+  }
+  for (; j < n4; j += stride) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(U) + j);
     acc = __dadd_rn(acc, sumsq44(x, make_float4(0.f, 0.f, 0.f, 0.f)));
-    mx = max(mx, max(max(__float_as_uint(x.x) & 0x7FFFFFFFu, __float_as_uint(x.y) & 0x7FFFFFFFu),
-                     max(__float_as_uint(x.z) & 0x7FFFFFFFu, __float_as_uint(x.w) & 0x7FFFFFFFu)));
+    mx = amax(mx, x);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     for (int64_t k = n4 * 4; k < n; ++k) {
@@ -104,9 +124,12 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restric
   finish_sumsq(acc, reinterpret_cast<NormWorkspace*>(red + mb * kRedBytes), cs + mb, 0.0f);
 }
 
+// p = p * decay - step * U unless the matrix is rejected; the bf16 round-out of p either way.
+// Threads stride over 4-element vectors, two in flight per round (master and U: 64 bytes);
+// `out8`: the bf16 rows allow 8-byte stores.
 __global__ void __launch_bounds__(kThreads)
     update_kernel(float* __restrict__ p0, const float* __restrict__ U0, uint16_t* __restrict__ out0, int64_t n,
-                  const zopt_clip_stats* cs, const unsigned* maxbits, float decay, float step, float guard,
+                  int out8, const zopt_clip_stats* cs, const unsigned* maxbits, float decay, float step, float guard,
                   float sqrt_min_dim, zopt_muon_stats* st) {
   const int mb = blockIdx.y;
   float* p = p0 + mb * n;
@@ -118,14 +141,56 @@ __global__ void __launch_bounds__(kThreads)
     const float fro = cs[mb].norm;
     st[mb] = zopt_muon_stats{fro, __fdiv_rn(fro, sqrt_min_dim), max_abs, rejected ? 1u : 0u};
   }
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += stride) {
-    float v = p[k];
-    if (!rejected) {
-      v = __fsub_rn(__fmul_rn(v, decay), __fmul_rn(step, U[k]));
-      p[k] = v;
+  auto one = [&](float v, float u) { return __fsub_rn(__fmul_rn(v, decay), __fmul_rn(step, u)); };
+  auto put = [&](int64_t k, const float4& v) {
+    const unsigned short b0 = __bfloat16_as_ushort(__float2bfloat16_rn(v.x)),
+                         b1 = __bfloat16_as_ushort(__float2bfloat16_rn(v.y)),
+                         b2 = __bfloat16_as_ushort(__float2bfloat16_rn(v.z)),
+                         b3 = __bfloat16_as_ushort(__float2bfloat16_rn(v.w));
+    if (out8) {
+      *reinterpret_cast<uint2*>(out + 4 * k) =
+          make_uint2(b0 | (static_cast<unsigned>(b1) << 16), b2 | (static_cast<unsigned>(b3) << 16));
+    } else {
+      out[4 * k] = b0; out[4 * k + 1] = b1; out[4 * k + 2] = b2; out[4 * k + 3] = b3;
     }
-    if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  };
+  const int64_t n4 = n / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float4* p4 = reinterpret_cast<float4*>(p);
+  const float4* U4 = reinterpret_cast<const float4*>(U);
+  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; j + stride < n4; j += 2 * stride) {
+    float4 a = p4[j], b = p4[j + stride];
+    if (!rejected) {
+      const float4 ua = __ldg(U4 + j), ub = __ldg(U4 + j + stride);
+      a = make_float4(one(a.x, ua.x), one(a.y, ua.y), one(a.z, ua.z), one(a.w, ua.w));
+      b = make_float4(one(b.x, ub.x), one(b.y, ub.y), one(b.z, ub.z), one(b.w, ub.w));
+      p4[j] = a;
+      p4[j + stride] = b;
+    }
+    if (out) {
+      put(j, a);
+      put(j + stride, b);
+    }
+  }
+  for (; j < n4; j += stride) {
+    float4 a = p4[j];
+    if (!rejected) {
+      const float4 ua = __ldg(U4 + j);
+      a = make_float4(one(a.x, ua.x), one(a.y, ua.y), one(a.z, ua.z), one(a.w, ua.w));
+      p4[j] = a;
+    }
+    if (out) put(j, a);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
+      float v = p[k];
+      if (!rejected) {
+        v = one(v, U[k]);
+        p[k] = v;
+      }
+      if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
   }
 }
 
@@ -204,8 +269,11 @@ zopt_status launch_update(const Job& j, long long b0, int gs, uint8_t* ws, const
   const dim3 grid(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
   ustats_kernel<<<grid, kThreads, 0, s>>>(U_out, n, ws, maxbits, cs);
   ZOPT_CUDA_TRY(cudaGetLastError());
-  update_kernel<<<grid, kThreads, 0, s>>>(j.master + b0 * n, U_out, j.out ? j.out + b0 * n : nullptr, n, cs, maxbits,
-                                          decay, step, hp->guard, sqrt_min, j.stats + b0);
+  uint16_t* out = j.out ? j.out + b0 * n : nullptr;
+  // 8-byte bf16 stores need the first matrix 8-byte aligned and every matrix a multiple of 4
+  const int out8 = out != nullptr && (reinterpret_cast<uintptr_t>(out) & 7u) == 0 && (n & 3) == 0 ? 1 : 0;
+  update_kernel<<<grid, kThreads, 0, s>>>(j.master + b0 * n, U_out, out, n, out8, cs, maxbits, decay, step, hp->guard,
+                                          sqrt_min, j.stats + b0);
   ZOPT_CUDA_TRY(cudaGetLastError());
   return ok();
 }

@@ -25,6 +25,8 @@
 // kernel out, each product is one launch of the single-CTA or CTA-pair GEMM (ns_gemm.cu). The
 // tile geometry and the epilogue building blocks they share are in ns_tile.cuh. Every wait is
 // bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
+#include <cstring>
+
 #include "ns_tile.cuh"
 
 namespace zopt {
@@ -221,14 +223,83 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
   job.prep = G.ws;
 }
 
-// The group's products one launch at a time (the fp32 mode, the CTA-pair kernel, outputs the
-// TMA cannot address).
+// Product `prod` of a step of a CTA-pair group as a job of a pair launch: 0 A = X X', 1 B' =
+// c A A' + b A + a I (b A through the R epilogue), 2 X = B' X (into the caller's X at the last
+// step). X is in buffer `cur`; returns the product's epilogue.
+int pair_job(const Group& G, const Coef& k, int prod, bool last, int cur, int* err, PairJob& J) {
+  const int m = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n);
+  const long long mat_elems = G.mat_elems;
+  GemmArgs& a = J.a;
+  a = GemmArgs{};
+  a.err = err;
+  a.group = G.gs;
+  a.alpha = 1.0f;
+  if (prod == 0) {
+    a.M = m; a.N = m; a.K = n; a.symmetric = 1;
+    a.D = G.A; a.ldd = G.p.lda; a.d_stride = mat_elems;
+    J.P = J.Q = J.R = G.mx_p[cur];
+    J.D = G.ma_e;
+    return kEpiTma;
+  }
+  if (prod == 1) {
+    a.M = m; a.N = m; a.K = m; a.symmetric = 1;
+    a.alpha = k.c; a.beta = k.b; a.diag = k.a;
+    a.R = reinterpret_cast<const __nv_bfloat16*>(G.A); a.ldr = G.p.lda; a.r_stride = mat_elems;
+    a.D = G.B; a.ldd = G.p.lda; a.d_stride = mat_elems;
+    J.P = J.Q = G.ma_p;
+    J.R = G.ma_e;
+    J.D = G.mb_e;
+    return kEpiTmaR;
+  }
+  a.M = m; a.N = n; a.K = m; a.b_mn_major = 1;
+  a.D = last ? static_cast<void*>(G.xo) : static_cast<void*>(G.xb[cur ^ 1]);
+  a.ldd = last ? G.ld_x : G.p.ldx;
+  a.d_stride = last ? G.bs_x : mat_elems;
+  a.d_f32 = last && G.io == ZOPT_F32 ? 1 : 0;
+  a.d_trans = last && G.transpose ? 1 : 0;
+  J.P = G.mb_p;
+  J.Q = J.R = G.mx_mn[cur];
+  J.D = last ? G.mo_e : G.mx_e[cur ^ 1];
+  return (!last || G.out_tma) ? kEpiTma : kEpiRegs;
+}
+
+// The steps of several CTA-pair groups (bf16 compute), each product of a step one launch for
+// all of them (kMaxPairJobs groups to a launch, those with the same epilogue together): the
+// small groups' tiles fill the large ones' waves. Every tile is computed as in a launch of its
+// own group alone, so the results are bitwise those of separate launches.
+zopt_status pair_products(const std::vector<const Group*>& gs, const Coef& k, int steps, int* err, cudaStream_t s) {
+  zopt_status st = ZOPT_OK;
+  int cur = 0;
+  for (int it = 0; it < steps; ++it) {
+    const bool last = it == steps - 1;
+    for (int prod = 0; prod < 3; ++prod) {
+      for (const int epi : {kEpiTma, kEpiTmaR, kEpiRegs}) {
+        PairBatch B;
+        std::memset(&B, 0, sizeof(B));
+        for (size_t q = 0; q <= gs.size(); ++q) {
+          if (B.n == kMaxPairJobs || (q == gs.size() && B.n > 0)) {
+            if ((st = launch_gemm_pair_batch(B, epi, s)) != ZOPT_OK) return st;
+            B.n = 0;
+          }
+          if (q == gs.size()) break;
+          PairJob J;
+          if (pair_job(*gs[q], k, prod, last, cur, err, J) == epi) B.job[B.n++] = J;
+        }
+      }
+    }
+    cur ^= 1;
+  }
+  return ok();
+}
+
+// The group's products one launch at a time (the fp32 mode, the CTA-pair kernel, single-CTA
+// outputs the TMA cannot address).
 zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, cudaStream_t s) {
+  if (G.pair && !G.f32c) return pair_products({&G}, k, steps, err, s);
   zopt_status st = ZOPT_OK;
   const int m = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n), gs = G.gs;
   const long long mat_elems = G.mat_elems;
   const Plan& p = G.p;
-  const bool pair = G.pair;
   int cur = 0;
   for (int it = 0; it < steps; ++it) {
     const bool last = it == steps - 1;
@@ -261,9 +332,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       ga.M = m; ga.N = m; ga.K = n;
       ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
       ga.ldr = 0; ga.r_stride = 0; ga.D = G.A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-      if ((st = pair ? launch_gemm_pair(G.mx_p[cur], G.mx_p[cur], nullptr, &G.ma_e, kEpiTma, ga, s)
-                     : launch_gemm(G.mx_p[cur], G.mx_q[cur], nullptr, &G.ma_e, kEpiTma, ga, s)) != ZOPT_OK)
-        return st;
+      if ((st = launch_gemm(G.mx_p[cur], G.mx_q[cur], nullptr, &G.ma_e, kEpiTma, ga, s)) != ZOPT_OK) return st;
       // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X.
       // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
       // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
@@ -271,13 +340,12 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       ga.alpha = k.c; ga.beta = k.b; ga.diag = k.a;
       ga.R = reinterpret_cast<const __nv_bfloat16*>(G.A); ga.ldr = p.lda; ga.r_stride = mat_elems;
       ga.D = G.B; ga.ldd = p.lda; ga.d_stride = mat_elems;
-      if (!pair && k.id_ok) {
+      if (k.id_ok) {
         GemmArgs gi = ga;
         gi.beta = 0.0f; gi.R = nullptr; gi.ident = 1; gi.h1 = k.h1; gi.h2 = k.h2;
         st = launch_gemm(G.ma_p, G.ma_q, nullptr, &G.mb_e, kEpiTma, gi, s);
       } else {
-        st = pair ? launch_gemm_pair(G.ma_p, G.ma_p, &G.ma_e, &G.mb_e, kEpiTmaR, ga, s)
-                  : launch_gemm(G.ma_p, G.ma_q, &G.ma_e, &G.mb_e, kEpiTmaR, ga, s);
+        st = launch_gemm(G.ma_p, G.ma_q, &G.ma_e, &G.mb_e, kEpiTmaR, ga, s);
       }
       if (st != ZOPT_OK) return st;
       // X = B' X
@@ -287,9 +355,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
       const int x_epi = (!last || G.out_tma) ? kEpiTma : kEpiRegs;
       const CUtensorMap* xd = last ? &G.mo_e : &G.mx_e[cur ^ 1];
-      if ((st = pair ? launch_gemm_pair(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)
-                     : launch_gemm(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)) != ZOPT_OK)
-        return st;
+      if ((st = launch_gemm(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)) != ZOPT_OK) return st;
     }
     cur ^= 1;
   }
@@ -473,9 +539,16 @@ extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32
       ++fa.n_jobs;
     }
   }
+  // the CTA-pair jobs: each product of a step in one launch for all of them
+  std::vector<const Group*> pairs;
   for (int32_t j = 0; j < n_jobs; ++j) {
     const Group& Gr = groups[static_cast<size_t>(j)];
-    if (!group_fusable(Gr, k) && (st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) return st;
+    if (!group_fusable(Gr, k) && Gr.pair) pairs.push_back(&Gr);
+  }
+  if (!pairs.empty() && (st = pair_products(pairs, k, steps, err_dev, s)) != ZOPT_OK) return st;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const Group& Gr = groups[static_cast<size_t>(j)];
+    if (!group_fusable(Gr, k) && !Gr.pair && (st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) return st;
   }
   return ok();
 }

@@ -8,6 +8,8 @@
 // accumulator (tcgen05.ld), apply alpha*acc (+ beta*R, + the diagonal term) and store it while
 // the next tile is being multiplied: through registers and plain stores (kEpiRegs) or as
 // 32 x 32 bf16 boxes handed to the TMA (kEpiTma, kEpiTmaR).
+#include <cstring>
+
 #include "ns_tile.cuh"
 
 namespace zopt {
@@ -269,12 +271,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // the leader's single thread issues the M=256 MMAs, whose commits reach both CTAs; each CTA
 // drains its own 128 TMEM lanes; the epilogue warps of both CTAs release an accumulator on the
 // leader's barrier.
-// tmR, tmD: as for the single-CTA kernel (unused by kEpiRegs).
+// A launch covers the jobs of a PairBatch (one or more products of the same kind): the pairs
+// walk the launch's tile index, and each tile takes its job's maps and arguments.
 template <int kEpi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
-    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                          const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmD,
-                          const GemmArgs a) {
+    gemm_bf16_pair_kernel(const __grid_constant__ PairBatch B) {
   constexpr int S2 = stages2_of(kEpi);
   constexpr bool kTma = kEpi != kEpiRegs;
   extern __shared__ uint8_t smem_raw[];
@@ -295,6 +296,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = tc::cluster_rank();
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int total = B.start[B.n];
+  int* err = B.job[0].a.err;
   if (threadIdx.x == 0) {
     for (int q = 0; q < S2; ++q) {
       tc::mbar_init(full + q, 1);
@@ -308,10 +311,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (kEpi == kEpiTmaR)
       for (int q = 0; q < 4; ++q) tc::mbar_init(rbar + q, 1);
     tc::fence_mbar_init();
-    tc::prefetch_tmap(&tmP);
-    tc::prefetch_tmap(&tmQ);
-    if (kEpi == kEpiTmaR) tc::prefetch_tmap(&tmR);
-    if (kTma) tc::prefetch_tmap(&tmD);
+    for (int j = 0; j < B.n; ++j) {
+      tc::prefetch_tmap(&B.job[j].P);
+      tc::prefetch_tmap(&B.job[j].Q);
+      if (kEpi == kEpiTmaR) tc::prefetch_tmap(&B.job[j].R);
+      if (kTma) tc::prefetch_tmap(&B.job[j].D);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc_pair(tslot, kTmemCols);
@@ -321,7 +326,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc::cluster_sync();  // the peer's barriers exist before anyone arrives on them
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const int nk = (a.K + BK - 1) / BK;
   tc::pdl_launch_dependents();
   tc::pdl_wait();  // the previous product's outputs are complete and visible
 
@@ -333,25 +337,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int armed[S2];
       for (int q = 0; q < S2; ++q) armed[q] = -1;
       bool ok = true;
-      for (int t = pair; ok && t < a.num_tiles; t += npairs) {
+      for (int t = pair; ok && t < total; t += npairs) {
+        const int j = pair_job_of(B, t);
+        const PairJob& J = B.job[j];
         int mb, tp, tj;
-        tile_coords2(a, t, mb, tp, tj);
+        tile_coords2(J.a, t - B.start[j], mb, tp, tj);
+        const int nk = (J.a.K + BK - 1) / BK;
         const int row0 = tp * BM2 + static_cast<int>(rank) * 128;  // this CTA's A rows
         const int col0 = tj * BN + static_cast<int>(rank) * 128;    // this CTA's B columns
         for (int kb = 0; kb < nk; ++kb) {
-          if (!tc::mbar_wait(empty + s, ph ^ 1u, a.err)) {
+          if (!tc::mbar_wait(empty + s, ph ^ 1u, err)) {
             ok = false;
             break;
           }
           if (leader) tc::mbar_arrive_expect_tx(full + s, 4 * kHalf);  // both CTAs' A and B halves
           armed[s] = static_cast<int>(ph);
           const uint32_t bar = tc::map_to_rank(tc::smem_u32(full + s), 0);
-          tc::tma_load_3d_pair(sA + s * kHalf, &tmP, bar, kb * BK, row0, mb);
-          if (!a.b_mn_major) {
-            tc::tma_load_3d_pair(sB + s * kHalf, &tmQ, bar, kb * BK, col0, mb);
+          tc::tma_load_3d_pair(sA + s * kHalf, &J.P, bar, kb * BK, row0, mb);
+          if (!J.a.b_mn_major) {
+            tc::tma_load_3d_pair(sB + s * kHalf, &J.Q, bar, kb * BK, col0, mb);
           } else {
-            tc::tma_load_3d_pair(sB + s * kHalf, &tmQ, bar, col0, kb * BK, mb);
-            tc::tma_load_3d_pair(sB + s * kHalf + kBoxMN, &tmQ, bar, col0 + 64, kb * BK, mb);
+            tc::tma_load_3d_pair(sB + s * kHalf, &J.Q, bar, col0, kb * BK, mb);
+            tc::tma_load_3d_pair(sB + s * kHalf + kBoxMN, &J.Q, bar, col0 + 64, kb * BK, mb);
           }
           if (++s == S2) {
             s = 0;
@@ -367,21 +374,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA issuer (leader)
-      const uint32_t idesc = tc::idesc_bf16_f32(BM2, BN, false, a.b_mn_major != 0);
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = pair; ok && t < a.num_tiles; t += npairs, ++it) {
+      for (int t = pair; ok && t < total; t += npairs, ++it) {
+        const GemmArgs& a = B.job[pair_job_of(B, t)].a;
+        const int nk = (a.K + BK - 1) / BK;
+        const uint32_t idesc = tc::idesc_bf16_f32(BM2, BN, false, a.b_mn_major != 0);
         const int b = it & 1;
         const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!tc::mbar_wait(tempty + b, tph ^ 1u, a.err)) {
+        if (!tc::mbar_wait(tempty + b, tph ^ 1u, err)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!tc::mbar_wait(full + s, ph, a.err)) {
+          if (!tc::mbar_wait(full + s, ph, err)) {
             ok = false;
             break;
           }
@@ -412,51 +421,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int quad = warp & 3;
     uint8_t* mine = sEpi + quad * (epi_bytes(kEpi) / 4);
     uint64_t* rb = rbar + quad;
-    const bool has_r = kEpi == kEpiTmaR && a.beta != 0.0f;
     const uint32_t tempty_leader[2] = {tc::map_to_rank(tc::smem_u32(tempty), 0),
                                        tc::map_to_rank(tc::smem_u32(tempty + 1), 0)};
     const int rows0 = static_cast<int>(rank) * 128 + 32 * quad;  // this warp's rows within a tile
+    auto has_r = [](const GemmArgs& a) { return kEpi == kEpiTmaR && a.beta != 0.0f; };
+    // issues tile t's R slice (when its job has one) on rb; warp-uniform result
+    auto load_r = [&](int t) -> bool {
+      const int j = pair_job_of(B, t);
+      if (!has_r(B.job[j].a)) return false;
+      int mb, tp, tj;
+      tile_coords2(B.job[j].a, t - B.start[j], mb, tp, tj);
+      int l = 0;
+      if (lane == 0) l = epi_load_r(B.job[j].a, &B.job[j].R, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
+      return __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+    };
     bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
     uint32_t rph = 0;
     int last_par = -1;
     int t = pair;
-    if (has_r && t < a.num_tiles) {
-      int mb, tp, tj;
-      tile_coords2(a, t, mb, tp, tj);
-      int l = 0;
-      if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
-      rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
-    }
-    for (int it = 0; t < a.num_tiles; t += npairs, ++it) {
+    if (t < total) rpend = load_r(t);
+    for (int it = 0; t < total; t += npairs, ++it) {
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, err) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       if (rpend) {  // every lane waits, so that each sees the TMA's writes
-        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, a.err) ? 1 : 0)) break;
+        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, err) ? 1 : 0)) break;
         rph ^= 1u;
         rpend = false;
       }
       tc::fence_after_sync();
+      const int j = pair_job_of(B, t);
+      const GemmArgs& a = B.job[j].a;
       int mb, tp, tj;
-      tile_coords2(a, t, mb, tp, tj);
-      epi_tile_tma<kEpi == kEpiTmaR>(a, &tmD, mine,
+      tile_coords2(a, t - B.start[j], mb, tp, tj);
+      epi_tile_tma<kEpi == kEpiTmaR>(a, &B.job[j].D, mine,
                                      tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
-                                     tp * BM2 + rows0, tj, mb, has_r, lane, last_par);
+                                     tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par);
       tc::fence_before_sync();
       tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
-      if (has_r) {
+      const int tn = t + npairs;
+      if (tn < total && has_r(B.job[pair_job_of(B, tn)].a)) {
         // the slice is free once the TMA has read it: then prefetch the next tile's R
         if (lane == 0) tc::bulk_wait_read<0>();
         __syncwarp();
-        const int tn = t + npairs;
-        if (tn < a.num_tiles) {
-          tile_coords2(a, tn, mb, tp, tj);
-          int l = 0;
-          if (lane == 0) l = epi_load_r(a, &tmR, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
-          rpend = __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
-        }
+        rpend = load_r(tn);
       }
     }
     if (lane == 0) {
@@ -471,16 +481,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const uint32_t tempty_leader[2] = {tc::map_to_rank(tc::smem_u32(tempty), 0),
                                        tc::map_to_rank(tc::smem_u32(tempty + 1), 0)};
     int it = 0;
-    for (int t = pair; t < a.num_tiles; t += npairs, ++it) {
+    for (int t = pair; t < total; t += npairs, ++it) {
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, err) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc::fence_after_sync();
+      const int j = pair_job_of(B, t);
+      const GemmArgs& a = B.job[j].a;
       int mb, tp, tj;
-      tile_coords2(a, t, mb, tp, tj);
+      tile_coords2(a, t - B.start[j], mb, tp, tj);
       GemmArgs am = a;
       am.R = a.R + mb * a.r_stride;
       am.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
@@ -508,10 +520,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------------- launchers
 
-// The CTA-pair kernel with epilogue `epi` (maps as for launch_gemm; kEpiTmaR reads R through *R):
-// P is read with 128-row boxes, Q with 128-row (K-major) or 64 x 64 (MN-major) boxes.
-zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
-                             int epi, GemmArgs a, cudaStream_t stream) {
+// The CTA-pair kernel over the jobs of B with epilogue `epi`: P is read with 128-row boxes, Q
+// with 128-row (K-major) or 64 x 64 (MN-major) boxes; kEpiTmaR reads R, the TMA epilogues store
+// D through each job's maps.
+zopt_status launch_gemm_pair_batch(PairBatch& B, int epi, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -522,34 +534,43 @@ zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, const C
                                        smem_bytes2(kEpiTma)));
     attr_set = true;
   }
-  a.tiles_m = static_cast<int>((a.M + BM2 - 1) / BM2);
-  a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
-  long long per = 0;
-  if (a.symmetric) {
-    for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r;
-  } else {
-    per = static_cast<long long>(a.tiles_m) * a.tiles_n;
+  if (B.n < 1 || B.n > kMaxPairJobs) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: bad pair batch");
+  long long total = 0;
+  for (int j = 0; j < B.n; ++j) {
+    GemmArgs& a = B.job[j].a;
+    a.tiles_m = static_cast<int>((a.M + BM2 - 1) / BM2);
+    a.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+    long long per = 0;
+    if (a.symmetric) {
+      for (int r = 0; r < a.tiles_m; ++r) per += a.tiles_n - r;
+    } else {
+      per = static_cast<long long>(a.tiles_m) * a.tiles_n;
+    }
+    const long long tiles = per * a.group;
+    if (tiles < 1 || total + tiles > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
+    a.tiles_per_mat = static_cast<int>(per);
+    a.num_tiles = static_cast<int>(tiles);
+    B.start[j] = static_cast<int>(total);
+    total += tiles;
+    if (epi != kEpiRegs) {
+      if ((epi == kEpiTmaR && (a.d_f32 || a.d_trans)) || (epi == kEpiTma && a.beta != 0.0f) ||
+          (a.symmetric && (a.d_f32 || a.d_trans)))
+        return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
+    }
   }
-  const long long total = per * a.group;
-  if (total < 1 || total > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
-  a.tiles_per_mat = static_cast<int>(per);
-  a.num_tiles = static_cast<int>(total);
+  B.start[B.n] = static_cast<int>(total);
   const int sms = sm_count();
   if (sms < 2) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
-  const int pairs = a.num_tiles < sms / 2 ? a.num_tiles : sms / 2;
+  const long long pairs = total < sms / 2 ? total : sms / 2;
   const dim3 grid(static_cast<unsigned>(2 * pairs));
   if (epi == kEpiRegs)
-    return launch_pdl(gemm_bf16_pair_kernel<kEpiRegs>, grid, dim3(kGemmThreads),
-                      static_cast<size_t>(smem_bytes2(kEpiRegs)), stream, P, Q, P, P, a);
-  if (D == nullptr || (epi == kEpiTmaR && (a.beta != 0.0f && R == nullptr)) ||
-      (epi == kEpiTmaR && (a.d_f32 || a.d_trans)) || (epi == kEpiTma && a.beta != 0.0f) ||
-      (a.symmetric && (a.d_f32 || a.d_trans)))
-    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: TMA epilogue without its maps");
+    return launch_pdl(gemm_bf16_pair_kernel<kEpiRegs>, grid, dim3(kGemmThreads), static_cast<size_t>(smem_bytes2(kEpiRegs)),
+                      stream, B);
   if (epi == kEpiTmaR)
-    return launch_pdl(gemm_bf16_pair_kernel<kEpiTmaR>, grid, dim3(kGemmThreads),
-                      static_cast<size_t>(smem_bytes2(kEpiTmaR)), stream, P, Q, R != nullptr ? *R : P, *D, a);
+    return launch_pdl(gemm_bf16_pair_kernel<kEpiTmaR>, grid, dim3(kGemmThreads), static_cast<size_t>(smem_bytes2(kEpiTmaR)),
+                      stream, B);
   return launch_pdl(gemm_bf16_pair_kernel<kEpiTma>, grid, dim3(kGemmThreads), static_cast<size_t>(smem_bytes2(kEpiTma)),
-                    stream, P, Q, P, *D, a);
+                    stream, B);
 }
 
 // The single-CTA kernel's tiles of a product (128 x 256; a symmetric product only those that

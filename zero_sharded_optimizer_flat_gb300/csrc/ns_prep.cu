@@ -65,62 +65,6 @@ __device__ __forceinline__ double sum256(double v, int tid, double* smem8) {
   return r;
 }
 
-// fp32 pairwise sum of squares of 8 values (no range check).
-__device__ __forceinline__ float sumsq8f(const float (&x)[8]) {
-  const float s01 = __fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1]));
-  const float s23 = __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3]));
-  const float s45 = __fadd_rn(__fmul_rn(x[4], x[4]), __fmul_rn(x[5], x[5]));
-  const float s67 = __fadd_rn(__fmul_rn(x[6], x[6]), __fmul_rn(x[7], x[7]));
-  return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
-}
-
-// Sum of squares of 32 values: fp32 pairwise while every 8-sum lies in [2^-96, 2^124] (no
-// overflow in the 32-sum, no loss to fp32 underflow worth a bf16 result); otherwise each 8 as
-// sumsq8 does (exact fp64 outside the safe range, NaN and Inf carried). One fp64 add per 32
-// elements keeps the fp64 pipe, slow on this part, off the critical path.
-__device__ __forceinline__ double sumsq32(const float (&a)[8], const float (&b)[8], const float (&c)[8],
-                                          const float (&d)[8]) {
-  const float s0 = sumsq8f(a), s1 = sumsq8f(b), s2 = sumsq8f(c), s3 = sumsq8f(d);
-  const float lo = fminf(fminf(s0, s1), fminf(s2, s3)), hi = fmaxf(fmaxf(s0, s1), fmaxf(s2, s3));
-  if (lo >= 0x1p-96f && hi <= 0x1p124f) return static_cast<double>(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)));
-  return __dadd_rn(__dadd_rn(sumsq8(a), sumsq8(b)), __dadd_rn(sumsq8(c), sumsq8(d)));
-}
-
-// The raw bits of 8 elements (one 16-byte load of bf16, two of fp32) and their values.
-template <typename T>
-struct Raw8;
-template <>
-struct Raw8<__nv_bfloat16> {
-  uint4 a;
-};
-template <>
-struct Raw8<float> {
-  uint4 a, b;
-};
-__device__ __forceinline__ void ld_raw8(const __nv_bfloat16* p, Raw8<__nv_bfloat16>& r) {
-  r.a = __ldg(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ void ld_raw8(const float* p, Raw8<float>& r) {
-  r.a = __ldg(reinterpret_cast<const uint4*>(p));
-  r.b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-}
-__device__ __forceinline__ void unpack8(const Raw8<__nv_bfloat16>& r, float (&x)[8]) {
-  const unsigned int w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[2 * k] = __uint_as_float(w[k] << 16);
-    x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-  }
-}
-__device__ __forceinline__ void unpack8(const Raw8<float>& r, float (&x)[8]) {
-  x[0] = __uint_as_float(r.a.x); x[1] = __uint_as_float(r.a.y); x[2] = __uint_as_float(r.a.z);
-  x[3] = __uint_as_float(r.a.w); x[4] = __uint_as_float(r.b.x); x[5] = __uint_as_float(r.b.y);
-  x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
-}
-// 8-element vectors per round: 128 bytes of loads in flight per thread.
-template <typename T>
-constexpr int kRound = 16 / static_cast<int>(sizeof(T));
-
 // Partial sums of squares of each matrix (blockIdx.y) over its first bpm blocks: G_b is rows x
 // cols with leading dimension ld, matrices bs elements apart. `flat` = the matrix is one
 // contiguous, 16-byte aligned vector. Threads stride over 8-element vectors, kRound loads in

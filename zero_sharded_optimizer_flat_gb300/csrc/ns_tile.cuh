@@ -458,6 +458,27 @@ constexpr int smem_bytes2(int e) {
 }
 static_assert(smem_bytes2(kEpiTma) <= 232448 && smem_bytes2(kEpiTmaR) <= 232448, "shared memory per CTA");
 
+// Products of one kind for several jobs in one CTA-pair launch (a grouped GEMM): job j's tiles
+// are [start[j], start[j + 1]) of the launch's tile index, each job with its own maps and
+// arguments (its own shape and batch), so the small products fill the large ones' waves.
+constexpr int kMaxPairJobs = 4;
+struct PairJob {
+  CUtensorMap P, Q, R, D;  // R read by kEpiTmaR; D written by the TMA epilogues
+  GemmArgs a;
+};
+struct PairBatch {
+  PairJob job[kMaxPairJobs];
+  int start[kMaxPairJobs + 1];
+  int n;
+};
+static_assert(sizeof(PairBatch) <= 4096, "kernel parameters");
+
+__device__ __forceinline__ int pair_job_of(const PairBatch& B, int t) {
+  int j = 0;
+  while (j + 1 < B.n && t >= B.start[j + 1]) ++j;
+  return j;
+}
+
 __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, int& tp, int& tj) {
   mb = t / a.tiles_per_mat;
   t -= mb * a.tiles_per_mat;
@@ -629,16 +650,15 @@ struct Plan {
 
 Plan plan(long long rows, long long cols, long long es, long long group);
 long long round_up(long long x, long long a);
-
 // Tile counts of a single-CTA product (fills tiles_m, tiles_n, tiles_per_mat, num_tiles).
 bool tiles_1cta(GemmArgs& a);
 // The single-CTA kernel with epilogue `epi` (tensor maps P, Q for the operands; R, D for the
 // TMA epilogues).
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
                         int epi, GemmArgs a, cudaStream_t stream);
-// The CTA-pair kernel with epilogue `epi`.
-zopt_status launch_gemm_pair(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
-                             int epi, GemmArgs a, cudaStream_t stream);
+// The CTA-pair kernel over the n jobs of B (each job's maps and arguments filled in; the tile
+// counts and starts are set here), all with epilogue `epi`.
+zopt_status launch_gemm_pair_batch(PairBatch& B, int epi, cudaStream_t stream);
 // The fused kernel over f.n_jobs jobs.
 zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream);
 
