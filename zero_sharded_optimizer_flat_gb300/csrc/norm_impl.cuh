@@ -201,22 +201,40 @@ __device__ __forceinline__ void finish_sumsq(double acc, NormWorkspace* ws, zopt
   }
 }
 
+// Σ g² over n elements in one pass. Threads stride over 8-element vectors (16-byte aligned
+// grad), kRound of them per round so that 128 bytes per thread are in flight; squares are
+// summed in fp32 over runs of 32 (sumsq32: exact fp64 outside the safe range) and the runs in
+// fp64 — the fp64 pipe, slow on this part, handles one add per 32 elements. The n % 8 tail
+// goes to thread 0 of block 0 in fp64.
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict__ g, int64_t n, float max_norm,
                                                              NormWorkspace* ws, zopt_clip_stats* stats) {
-  const int64_t n4 = n / 4;
+  constexpr int R = kRound<T>;
+  const int64_t n8 = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double acc = 0.0;
-  for (; j + 3 * stride < n4; j += 4 * stride) {  // four units' loads in flight per thread
-    float4 x[4];
+  for (; j + (R - 1) * stride < n8; j += R * stride) {
+    Raw8<T> r[R];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = load4(g + 4 * (j + u * stride));
-    acc = __dadd_rn(acc, __dadd_rn(sumsq44(x[0], x[1]), sumsq44(x[2], x[3])));
+    for (int k = 0; k < R; ++k) ld_raw8(g + 8 * (j + k * stride), r[k]);
+#pragma unroll
+    for (int k = 0; k < R; k += 4) {
+      float x0[8], x1[8], x2[8], x3[8];
+      unpack8(r[k], x0);
+      unpack8(r[k + 1], x1);
+      unpack8(r[k + 2], x2);
+      unpack8(r[k + 3], x3);
+      acc = __dadd_rn(acc, sumsq32(x0, x1, x2, x3));
+    }
   }
-  for (; j < n4; j += stride) acc = __dadd_rn(acc, sumsq44(load4(g + 4 * j), make_float4(0.f, 0.f, 0.f, 0.f)));
+  for (; j < n8; j += stride) {
+    float x[8];
+    load8(g + 8 * j, x);
+    acc = __dadd_rn(acc, sumsq8(x));
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t k = n4 * 4; k < n; ++k) {
+    for (int64_t k = n8 * 8; k < n; ++k) {
       const double d = static_cast<double>(load1(g + k));
       acc = __dadd_rn(acc, __dmul_rn(d, d));
     }
