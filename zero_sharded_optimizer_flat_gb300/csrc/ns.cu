@@ -444,7 +444,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     Gr.gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
     Gr.f32c = f32c;
     if ((st = group_init(Gr, p, static_cast<uint8_t*>(d_ws))) != ZOPT_OK) return st;
-    if ((st = group_prep(&Gr, 1, eps, sms, s)) != ZOPT_OK) return st;
+    if ((st = group_prep(&Gr, 1, eps, s)) != ZOPT_OK) return st;
     if (group_fusable(Gr, k)) {
       // every product of every step in one persistent launch
       FusedMaps fm;
@@ -521,7 +521,7 @@ extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32
     if ((st = group_init(Gr, p, static_cast<uint8_t*>(d_ws) + at)) != ZOPT_OK) return st;
     at += static_cast<size_t>(round_up(static_cast<long long>(p.total), 1024));
   }
-  if ((st = group_prep(groups.data(), n_jobs, eps, sms, s)) != ZOPT_OK) return st;
+  if ((st = group_prep(groups.data(), n_jobs, eps, s)) != ZOPT_OK) return st;
   FusedMaps fm;
   FusedArgs fa{};
   fa.steps = steps;

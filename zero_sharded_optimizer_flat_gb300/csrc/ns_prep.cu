@@ -459,8 +459,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
 // per input dtype, then one scaling and one transpose launch per input and compute dtype that
 // occur (each matrix's partial sums are reduced by the blocks that normalise it; its block 0
 // also zeroes its counters for the fused kernel).
-zopt_status group_prep(const Group* groups, int n, float eps, int sms, cudaStream_t s) {
-  (void)sms;
+zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s) {
   zopt_status st = ZOPT_OK;
   if ((st = prep_pass<0, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;
   if ((st = prep_pass<0, float, float>(groups, n, eps, s)) != ZOPT_OK) return st;

@@ -681,7 +681,7 @@ struct Group {
 };
 
 // X0 = G / (||G||_F + eps), oriented, for every matrix of n groups (a handful of launches in all).
-zopt_status group_prep(const Group* groups, int n, float eps, int sms, cudaStream_t s);
+zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s);
 
 }  // namespace ns
 }  // namespace zopt
