@@ -162,3 +162,24 @@ def test_odd_sizes_and_unaligned_out(zopt, rows, cols, batch, shift):
         assert not st[b]["rejected"]
     assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))
     assert int(flat[:shift].abs().sum()) == 0  # nothing written before the output
+
+
+def test_nan_gradient_is_rejected(zopt):
+    """A NaN in the gradient reaches U through Newton-Schulz: max |U| is NaN, which the guard
+    (max |U| <= guard) rejects, so the master and its bf16 weights stay as they were while the
+    momentum buffer still advances (the NaN lands in it)."""
+    rows, cols = 256, 512
+    p = torch.randn(rows, cols, device="cuda") * 0.02
+    p0 = p.clone()
+    buf = torch.zeros_like(p)
+    g = (torch.randn(rows, cols, device="cuda") * 1e-3).bfloat16()
+    g[3, 4] = float("nan")
+    out = torch.zeros(rows, cols, dtype=torch.int16, device="cuda")
+    stats = zopt.new_muon_stats()
+    zopt.muon_step(p, buf, g, out, zopt.new_muon_workspace(rows, cols), stats, lr=1e-3)
+    torch.cuda.synchronize()
+    st = zopt.read_muon_stats(stats)[0]
+    assert st["rejected"] and math.isnan(st["max_abs"])
+    assert torch.equal(p.view(torch.int32), p0.view(torch.int32))
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(p0.cpu().numpy()))
+    assert math.isnan(float(buf[3, 4])) and int(torch.isnan(buf).sum()) == 1

@@ -398,3 +398,78 @@ def test_many_pair_jobs_batched(zopt):
         assert torch.equal(one, X), (r, c, b)
     ref = newton_schulz(pairs[3][0][0].double().cpu().numpy(), steps=3)
     assert rel(pairs[3][1][0].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,cols", [(300, 700), (700, 300), (1024, 1100)])
+def test_zero_matrix_gives_zero(zopt, rows, cols, dtype):
+    """G = 0: ||G|| = 0, X0 = 0 / (0 + eps) = 0 and every product stays 0, so the output is
+    exactly zero, as the oracle's plain definition gives; in a many-jobs call as well."""
+    G = torch.zeros(rows, cols, device="cuda", dtype=dtype)
+    X = torch.full_like(G, 7.0)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols), steps=5)
+    torch.cuda.synchronize()
+    assert bool((X == 0).all())
+    assert np.all(newton_schulz(np.zeros((rows, cols)), steps=5) == 0)
+    if dtype == torch.bfloat16:
+        Y = torch.full((1, rows, cols), 7.0, device="cuda", dtype=dtype)
+        H = torch.randn(2, 256, 512, device="cuda").to(dtype)
+        Hx = torch.empty_like(H)
+        zopt.ns_orthogonalize_many([(G[None], Y), (H, Hx)],
+                                   zopt.new_ns_workspace_many([(rows, cols, 1), (256, 512, 2)]), steps=5)
+        torch.cuda.synchronize()
+        assert bool((Y == 0).all()) and bool(torch.isfinite(Hx.float()).all())
+
+
+def p5(s, abc=DEFAULT_ABC, steps=5):
+    a, b, c = abc
+    for _ in range(steps):
+        s = a * s + b * s ** 3 + c * s ** 5
+    return s
+
+
+@pytest.mark.parametrize("rows,cols", [(256, 768), (768, 256), (1024, 1536)])
+def test_rank_one_closed_form(zopt, rows, cols):
+    """An exactly rank-1 G = u v' (entries that bf16 holds exactly) has the one singular value
+    ||G||_F: X0 = G / (||G|| + eps) has singular value s = ||G|| / (||G|| + eps), a step maps it by
+    p(s) = a s + b s^3 + c s^5 and keeps the singular vectors, so one step gives
+    p(s) u v' / (|u| |v|); the GPU result is within the bf16 tolerance of that closed form (the
+    fp64 oracle agrees to 1e-10). One step only: the bf16 rounding of X0 leaves noise of ~2^-9 in
+    the null directions, which every step multiplies by about a = 3.44 (5 steps: ~490x), so
+    a rank-deficient input is a case where bf16 Newton-Schulz parts from the exact result."""
+    g = torch.Generator().manual_seed(rows + cols)
+    u = torch.randint(-4, 5, (rows,), generator=g).double() / 4
+    v = torch.randint(-4, 5, (cols,), generator=g).double() / 4
+    u[0], v[0] = 1.0, 1.0  # nonzero vectors
+    Gd = torch.outer(u, v)
+    G = Gd.to(torch.bfloat16).cuda()
+    assert torch.equal(G.double().cpu(), Gd)  # exactly representable
+    X = torch.empty_like(G)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols), steps=1)
+    torch.cuda.synchronize()
+    fro = float(torch.linalg.norm(Gd))
+    closed = p5(fro / (fro + 1e-7), steps=1) * torch.outer(u / torch.linalg.norm(u), v / torch.linalg.norm(v))
+    assert rel(torch.from_numpy(newton_schulz(Gd.numpy(), steps=1)), closed) <= 1e-10
+    closed5 = p5(fro / (fro + 1e-7)) * torch.outer(u / torch.linalg.norm(u), v / torch.linalg.norm(v))
+    assert rel(torch.from_numpy(newton_schulz(Gd.numpy(), steps=5)), closed5) <= 1e-10
+    assert rel(X.cpu(), closed) <= 2e-2
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_nonfinite_input_propagates_and_context_survives(zopt, bad):
+    """A non-finite element makes ||G|| non-finite: the output carries non-finite values (as the
+    oracle's does); the call returns normally and the next call on finite input is correct."""
+    rows, cols = 256, 768
+    G = gaussian(rows, cols, 3)
+    G[5, 7] = bad
+    X = torch.empty_like(G)
+    ws = zopt.new_ns_workspace(rows, cols)
+    zopt.ns_orthogonalize(G, X, ws, steps=5)
+    torch.cuda.synchronize()
+    assert not bool(torch.isfinite(X.float()).all())
+    with np.errstate(invalid="ignore"):  # inf / inf in the oracle's normalisation is the point
+        assert not np.all(np.isfinite(newton_schulz(G.double().cpu().numpy(), steps=5)))
+    G2 = gaussian(rows, cols, 4)
+    zopt.ns_orthogonalize(G2, X, ws, steps=5)
+    torch.cuda.synchronize()
+    assert rel(X.cpu(), torch.from_numpy(newton_schulz(G2.double().cpu().numpy(), steps=5))) <= 2e-2
