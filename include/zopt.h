@@ -287,7 +287,10 @@ ZOPT_API size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs);
  * zopt_ns_orthogonalize gives with a workspace that holds the job's whole batch. Jobs whose
  * shorter side is below 1024 and whose output rows are 16-byte aligned run in one persistent
  * launch per six jobs, the products of each step interleaved across jobs (one job's waits for
- * its previous product are filled by the other jobs' tiles); the others run product by product.
+ * its previous product are filled by the other jobs' tiles); those of 1024 and above run each
+ * product of a step in one launch for up to four jobs (their tiles filling each other's
+ * waves); any other job runs product by product. The inputs of all jobs are normalised in
+ * three launches before any product.
  * jobs is read during the call only; d_ws (16-byte aligned) is owned by the call until the
  * stream passes it. Same errors as zopt_ns_orthogonalize. */
 ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,

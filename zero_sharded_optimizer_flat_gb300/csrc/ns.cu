@@ -19,10 +19,11 @@
 // The fp32 compute mode runs the products as the pages write them on the SIMT kernel
 // (ns_simt.cu).
 //
-// Where the work runs: ns_prep.cu normalises and orients the inputs; below m = 1024 every
-// product of every step runs in one persistent launch of ns_fused_kernel (ns_fused.cu), several
-// shapes at once; from m = 1024, and whenever an output or the coefficients rule the fused
-// kernel out, each product is one launch of the single-CTA or CTA-pair GEMM (ns_gemm.cu). The
+// Where the work runs: ns_prep.cu normalises and orients the inputs of every job in three
+// launches; below m = 1024 every product of every step runs in one persistent launch of
+// ns_fused_kernel (ns_fused.cu), several shapes at once; from m = 1024 each product of a step is
+// one launch of the CTA-pair GEMM for up to four shapes, and where an output or the
+// coefficients rule the fused kernel out, one launch of the single-CTA GEMM (ns_gemm.cu). The
 // tile geometry and the epilogue building blocks they share are in ns_tile.cuh. Every wait is
 // bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
 #include <cstring>
