@@ -1,5 +1,6 @@
 // The Newton-Schulz products on tcgen05 tensor cores, one launch per product: the single-CTA
-// persistent GEMM and its CTA-pair form, and their host launchers.
+// persistent GEMM and its CTA-pair form (whose launch may cover the same product of up to four
+// shapes), and their host launchers.
 //
 // Single CTA: one CTA per SM (persistent), 192 threads. Warp 0 streams 128x64 and 256x64 bf16
 // tiles into a shared-memory ring with TMA (128-byte swizzle); one thread of warp 1 issues
