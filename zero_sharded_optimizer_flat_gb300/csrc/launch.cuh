@@ -1,0 +1,33 @@
+// Kernel launch with programmatic dependent launch (the Newton-Schulz kernels chain their
+// launches this way).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <utility>
+
+#include "internal.h"
+
+namespace zopt {
+
+// Launches `kernel` on `stream` with programmatic stream serialisation: it may start while
+// the previous kernel finishes (every kernel here waits with griddepcontrol.wait before it
+// touches global memory).
+template <typename... KArgs, typename... Args>
+zopt_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ZOPT_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+  return ok();
+}
+
+}  // namespace zopt

@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "norm_impl.cuh"
 #include "ns_internal.h"
 #include "tc.cuh"
@@ -620,26 +621,6 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, i
 }
 
 // ---------------------------------------------------------------------- host-side declarations
-
-// Launches `kernel` on `stream` with programmatic stream serialisation: it may start while
-// the previous kernel finishes (every kernel here waits with griddepcontrol.wait before it
-// touches global memory).
-template <typename... KArgs, typename... Args>
-zopt_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  ZOPT_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
-  return ok();
-}
 
 // Workspace: a header (per-matrix reduction scratch and stats), then one region per matrix of
 // the group holding X0, X1 (m x ldx), A and B (m x lda) in the compute dtype (es bytes).
