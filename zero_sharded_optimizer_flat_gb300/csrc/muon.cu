@@ -59,11 +59,21 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(float* __restrict__ 
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   float4* b4 = reinterpret_cast<float4*>(buf);
   float4* u4 = reinterpret_cast<float4*>(u);
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
+  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; j + stride < n4; j += 2 * stride) {  // two vectors' loads in flight before any store
+    const float4 ga = load4(g + 4 * j), gb = load4(g + 4 * (j + stride));
+    const float4 ba = b4[j], bb = b4[j + stride];
+    const float4 na = fma4_momentum(mu, ba, ga), nb = fma4_momentum(mu, bb, gb);
+    b4[j] = na;
+    b4[j + stride] = nb;
+    u4[j] = nesterov ? fma4_momentum(mu, na, ga) : na;  // g + mu*buf, as the same two roundings
+    u4[j + stride] = nesterov ? fma4_momentum(mu, nb, gb) : nb;
+  }
+  for (; j < n4; j += stride) {
     const float4 gv = load4(g + 4 * j);
     const float4 b = fma4_momentum(mu, b4[j], gv);
     b4[j] = b;
-    u4[j] = nesterov ? fma4_momentum(mu, b, gv) : b;  // g + mu*buf, as the same two roundings
+    u4[j] = nesterov ? fma4_momentum(mu, b, gv) : b;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     for (int64_t k = n4 * 4; k < n; ++k) {
