@@ -6,11 +6,13 @@
 // and "original" uses sqrt(max(1, rows/cols)); diagnostics nsratio = ||U||_F/sqrt(min(rows,
 // cols)) and a divergence guard that rejects an update with an element above 1000.
 //
-// Per group of matrices (as many as the workspace holds), four steps on the caller's stream:
+// Four steps on the caller's stream, each one launch for every job of a call (for a single
+// shape: per group of matrices, as many as the workspace holds):
 //   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 14-16 B/elem)
 //   2. U = NewtonSchulz(u) through zopt_ns_orthogonalize (fp32 in/out, bf16 tensor cores)
-//   3. per matrix: sum of squares and largest magnitude of U                 (4 B/elem)
-//   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (14 B/elem)
+//   3. per matrix: partial sums of squares and largest magnitudes of U     (4 B/elem)
+//   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (14 B/elem);
+//      each block first reduces its matrix's partials in a fixed order (no atomics, no memset)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,20 +28,23 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxBlocksPerMat = 512;
-constexpr size_t kRedBytes = 256 + sizeof(double) * kMaxBlocksPerMat;  // one NormWorkspace per matrix
+constexpr long long kChunk = 32768;  // elements per block of the element-wise kernels
+constexpr int kMaxItems = 8;         // jobs per element-wise launch
+// per matrix: one fp64 partial sum of squares and one max |U| bit pattern per block
+constexpr size_t kRedBytes = (sizeof(double) + sizeof(unsigned)) * kMaxBlocksPerMat;
 
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
 
 struct MuonPlan {
-  size_t off_max, off_cs, off_u, off_o, off_ns, ns_bytes, total;
+  size_t off_u, off_o, off_ns, ns_bytes, total;
 };
 
+// Workspace of `group` matrices: the reduction area (kRedBytes per matrix), u and U (fp32), then
+// the Newton-Schulz workspace.
 MuonPlan muon_plan(long long rows, long long cols, long long group) {
   MuonPlan p;
   const long long n = rows * cols;
-  p.off_max = static_cast<size_t>(round_up(group * static_cast<long long>(kRedBytes), 256));
-  p.off_cs = static_cast<size_t>(round_up(static_cast<long long>(p.off_max) + group * 4, 256));
-  p.off_u = static_cast<size_t>(round_up(static_cast<long long>(p.off_cs) + group * 32, 1024));
+  p.off_u = static_cast<size_t>(round_up(group * static_cast<long long>(kRedBytes), 1024));
   p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 4, 1024));
   p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 4, 1024));
   p.ns_bytes = zopt_ns_workspace(rows, cols, static_cast<int32_t>(group), ZOPT_BF16);
@@ -47,62 +52,105 @@ MuonPlan muon_plan(long long rows, long long cols, long long group) {
   return p;
 }
 
+// One job of an element-wise launch: `batch` matrices of n elements, back to back.
+struct MuonItem {
+  float* master;
+  float* momentum;
+  const void* grad;
+  float* u_in;          // momentum's output, Newton-Schulz's input
+  const float* u_out;   // Newton-Schulz's output U
+  uint16_t* out;        // bf16 round-out (may be null)
+  zopt_muon_stats* stats;
+  uint8_t* red;         // reduction area: per matrix kMaxBlocksPerMat fp64 sums, then as many maxima
+  long long n;          // elements per matrix
+  long long u0;         // blocks of the launch before this job
+  int batch;
+  int bpm;              // statistics / update blocks per matrix (depends on n only)
+  int out8;             // the bf16 output allows 8-byte stores
+  float decay, step, sqrt_min;
+};
+
+struct MuonList {
+  MuonItem it[kMaxItems];
+  int n;
+  float mu;
+  int nesterov;
+  float guard;
+};
+
+__device__ __forceinline__ int item_of(const MuonList& L, long long u) {
+  int k = 0;
+  while (k + 1 < L.n && u >= L.it[k + 1].u0) ++k;
+  return k;
+}
+
 __device__ __forceinline__ float4 fma4_momentum(float mu, const float4& b, const float4& g) {
   return make_float4(__fadd_rn(__fmul_rn(mu, b.x), g.x), __fadd_rn(__fmul_rn(mu, b.y), g.y),
                      __fadd_rn(__fmul_rn(mu, b.z), g.z), __fadd_rn(__fmul_rn(mu, b.w), g.w));
 }
 
+// Step 1: block u takes chunk u - u0 (kChunk elements) of its job's batch, which is contiguous;
+// threads move 4-element vectors, two in flight; the batch's n*batch % 4 last elements go to
+// the job's last chunk element by element.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) momentum_kernel(float* __restrict__ buf, const T* __restrict__ g,
-                                                             float* __restrict__ u, int64_t n, float mu, int nesterov) {
-  const int64_t n4 = n / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  float4* b4 = reinterpret_cast<float4*>(buf);
-  float4* u4 = reinterpret_cast<float4*>(u);
-  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; j + stride < n4; j += 2 * stride) {  // two vectors' loads in flight before any store
-    const float4 ga = load4(g + 4 * j), gb = load4(g + 4 * (j + stride));
-    const float4 ba = b4[j], bb = b4[j + stride];
+__global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
+  const MuonItem& J = L.it[item_of(L, blockIdx.x)];
+  const long long c = static_cast<long long>(blockIdx.x) - J.u0;
+  const long long total = J.n * J.batch, e0 = c * kChunk;
+  const long long e1 = e0 + kChunk < total ? e0 + kChunk : total;
+  const T* g = static_cast<const T*>(J.grad);
+  float4* b4 = reinterpret_cast<float4*>(J.momentum);
+  float4* u4 = reinterpret_cast<float4*>(J.u_in);
+  const float mu = L.mu;
+  const long long v1 = e1 / 4;  // whole vectors of the chunk (e0 is a multiple of 4)
+  long long j = e0 / 4 + threadIdx.x;
+  for (; j + kThreads < v1; j += 2 * kThreads) {  // two vectors' loads in flight before any store
+    const float4 ga = load4(g + 4 * j), gb = load4(g + 4 * (j + kThreads));
+    const float4 ba = b4[j], bb = b4[j + kThreads];
     const float4 na = fma4_momentum(mu, ba, ga), nb = fma4_momentum(mu, bb, gb);
     b4[j] = na;
-    b4[j + stride] = nb;
-    u4[j] = nesterov ? fma4_momentum(mu, na, ga) : na;  // g + mu*buf, as the same two roundings
-    u4[j + stride] = nesterov ? fma4_momentum(mu, nb, gb) : nb;
+    b4[j + kThreads] = nb;
+    u4[j] = L.nesterov ? fma4_momentum(mu, na, ga) : na;  // g + mu*buf, as the same two roundings
+    u4[j + kThreads] = L.nesterov ? fma4_momentum(mu, nb, gb) : nb;
   }
-  for (; j < n4; j += stride) {
+  for (; j < v1; j += kThreads) {
     const float4 gv = load4(g + 4 * j);
     const float4 b = fma4_momentum(mu, b4[j], gv);
     b4[j] = b;
-    u4[j] = nesterov ? fma4_momentum(mu, b, gv) : b;
+    u4[j] = L.nesterov ? fma4_momentum(mu, b, gv) : b;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t k = n4 * 4; k < n; ++k) {
+  if (e1 == total && threadIdx.x == 0) {
+    for (long long k = v1 * 4; k < total; ++k) {
       const float gv = load1(g + k);
-      const float b = __fadd_rn(__fmul_rn(mu, buf[k]), gv);
-      buf[k] = b;
-      u[k] = nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
+      const float b = __fadd_rn(__fmul_rn(mu, J.momentum[k]), gv);
+      J.momentum[k] = b;
+      J.u_in[k] = L.nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
     }
   }
 }
 
-// Per matrix (blockIdx.y): sum of squares of U and max |U| (the fp32 bit patterns of
-// non-negative values order as unsigned integers; NaN sorts above inf). Threads stride over
-// 4-element vectors, 8 loads (128 bytes) in flight per round; squares are summed in fp32 over
-// runs of 32 (sumsq32: exact fp64 outside the safe range) and the runs in fp64; one partial per
-// block, the last block of the matrix adding them in a fixed order.
-__global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restrict__ U0, int64_t n, uint8_t* red,
-                                                           unsigned* maxbits, zopt_clip_stats* cs) {
-  const int mb = blockIdx.y;
-  const float* U = U0 + mb * n;
+// Step 3: block u is block c = (u - u0) % bpm of matrix mb = (u - u0) / bpm; threads stride over
+// the matrix's 4-element vectors with stride bpm * 256, 8 loads (128 bytes) in flight per round;
+// squares are summed in fp32 over runs of 32 (sumsq32: exact fp64 outside the safe range) and
+// the runs in fp64. The block's sum and its max |U| (the fp32 bit patterns of non-negative
+// values order as unsigned integers; NaN sorts above inf) go to slot c of the matrix's area.
+__global__ void __launch_bounds__(kThreads) ustats_kernel(const MuonList L) {
+  __shared__ double red[32];
+  __shared__ unsigned smax[kThreads / 32];
+  const MuonItem& J = L.it[item_of(L, blockIdx.x)];
+  const long long v = static_cast<long long>(blockIdx.x) - J.u0;
+  const long long mb = v / J.bpm, c = v - mb * J.bpm;
+  const long long n = J.n;
+  const float* U = J.u_out + mb * n;
   const int64_t n4 = n / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
   double acc = 0.0;
   unsigned mx = 0;
   auto amax = [](unsigned m, const float4& x) {
     return max(m, max(max(__float_as_uint(x.x) & 0x7FFFFFFFu, __float_as_uint(x.y) & 0x7FFFFFFFu),
                       max(__float_as_uint(x.z) & 0x7FFFFFFFu, __float_as_uint(x.w) & 0x7FFFFFFFu)));
   };
-  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t j = c * blockDim.x + threadIdx.x;
   for (; j + 7 * stride < n4; j += 8 * stride) {
     float4 x[8];
 #pragma unroll
@@ -121,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restric
     acc = __dadd_rn(acc, sumsq44(x, make_float4(0.f, 0.f, 0.f, 0.f)));
     mx = amax(mx, x);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (c == 0 && threadIdx.x == 0) {
     for (int64_t k = n4 * 4; k < n; ++k) {
       const float x = U[k];
       acc = __dadd_rn(acc, __dmul_rn(static_cast<double>(x), static_cast<double>(x)));
@@ -130,34 +178,66 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const float* __restric
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(maxbits + mb, mx);
-  finish_sumsq(acc, reinterpret_cast<NormWorkspace*>(red + mb * kRedBytes), cs + mb, 0.0f);
+  if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = mx;
+  const double block = block_sum(acc, red);  // (its barriers also publish smax)
+  if (threadIdx.x == 0) {
+    unsigned m = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) m = max(m, smax[w]);
+    uint8_t* area = J.red + mb * kRedBytes;
+    reinterpret_cast<double*>(area)[c] = block;
+    reinterpret_cast<unsigned*>(area + sizeof(double) * kMaxBlocksPerMat)[c] = m;
+  }
 }
 
-// p = p * decay - step * U unless the matrix is rejected; the bf16 round-out of p either way.
-// Threads stride over 4-element vectors, two in flight per round (master and U: 64 bytes);
-// `out8`: the bf16 rows allow 8-byte stores.
-__global__ void __launch_bounds__(kThreads)
-    update_kernel(float* __restrict__ p0, const float* __restrict__ U0, uint16_t* __restrict__ out0, int64_t n,
-                  int out8, const zopt_clip_stats* cs, const unsigned* maxbits, float decay, float step, float guard,
-                  float sqrt_min_dim, zopt_muon_stats* st) {
-  const int mb = blockIdx.y;
-  float* p = p0 + mb * n;
-  const float* U = U0 + mb * n;
-  uint16_t* out = out0 ? out0 + mb * n : nullptr;
-  const float max_abs = __uint_as_float(maxbits[mb]);
-  const bool rejected = !(max_abs <= guard);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    const float fro = cs[mb].norm;
-    st[mb] = zopt_muon_stats{fro, __fdiv_rn(fro, sqrt_min_dim), max_abs, rejected ? 1u : 0u};
+// Step 4: block u updates block c of matrix mb (as step 3 splits it). It first reduces the
+// matrix's bpm partial sums (threads stride over them, then the block tree: the same order in
+// every block) and maxima; block 0 of the matrix writes its stats. Rejected (max |U| above the
+// guard, or NaN): the master is kept, the bf16 round-out is written either way.
+__global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
+  __shared__ double red[32];
+  __shared__ unsigned smax[kThreads / 32];
+  __shared__ unsigned s_max;
+  const MuonItem& J = L.it[item_of(L, blockIdx.x)];
+  const long long v = static_cast<long long>(blockIdx.x) - J.u0;
+  const long long mb = v / J.bpm, c = v - mb * J.bpm;
+  const long long n = J.n;
+  const uint8_t* area = J.red + mb * kRedBytes;
+  double a = 0.0;
+  unsigned m = 0;
+  for (int i = threadIdx.x; i < J.bpm; i += kThreads) {
+    a = __dadd_rn(a, __ldcg(reinterpret_cast<const double*>(area) + i));  // from L2: another kernel wrote them
+    m = max(m, __ldcg(reinterpret_cast<const unsigned*>(area + sizeof(double) * kMaxBlocksPerMat) + i));
   }
-  auto one = [&](float v, float u) { return __fsub_rn(__fmul_rn(v, decay), __fmul_rn(step, u)); };
-  auto put = [&](int64_t k, const float4& v) {
-    const unsigned short b0 = __bfloat16_as_ushort(__float2bfloat16_rn(v.x)),
-                         b1 = __bfloat16_as_ushort(__float2bfloat16_rn(v.y)),
-                         b2 = __bfloat16_as_ushort(__float2bfloat16_rn(v.z)),
-                         b3 = __bfloat16_as_ushort(__float2bfloat16_rn(v.w));
-    if (out8) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = m;
+  const double ss = block_sum(a, red);  // valid in thread 0 (its barriers also publish smax)
+  if (threadIdx.x == 0) {
+    unsigned mm = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) mm = max(mm, smax[w]);
+    s_max = mm;
+    if (c == 0) {
+      const double norm64 = (ss >= 0.0) ? __dsqrt_rn(ss) : __longlong_as_double(0x7FF8000000000000LL);
+      const float fro = __double2float_rn(norm64);
+      const float max_abs = __uint_as_float(mm);
+      J.stats[mb] = zopt_muon_stats{fro, __fdiv_rn(fro, J.sqrt_min), max_abs, !(max_abs <= L.guard) ? 1u : 0u};
+    }
+  }
+  __syncthreads();
+  const bool rejected = !(__uint_as_float(s_max) <= L.guard);
+  float* p = J.master + mb * n;
+  const float* U = J.u_out + mb * n;
+  uint16_t* out = J.out ? J.out + mb * n : nullptr;
+  const float decay = J.decay, step = J.step;
+  auto one = [&](float x, float u) { return __fsub_rn(__fmul_rn(x, decay), __fmul_rn(step, u)); };
+  auto put = [&](int64_t k, const float4& x) {
+    const unsigned short b0 = __bfloat16_as_ushort(__float2bfloat16_rn(x.x)),
+                         b1 = __bfloat16_as_ushort(__float2bfloat16_rn(x.y)),
+                         b2 = __bfloat16_as_ushort(__float2bfloat16_rn(x.z)),
+                         b3 = __bfloat16_as_ushort(__float2bfloat16_rn(x.w));
+    if (J.out8) {
       *reinterpret_cast<uint2*>(out + 4 * k) =
           make_uint2(b0 | (static_cast<unsigned>(b1) << 16), b2 | (static_cast<unsigned>(b3) << 16));
     } else {
@@ -165,41 +245,41 @@ __global__ void __launch_bounds__(kThreads)
     }
   };
   const int64_t n4 = n / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
   float4* p4 = reinterpret_cast<float4*>(p);
   const float4* U4 = reinterpret_cast<const float4*>(U);
-  int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t j = c * blockDim.x + threadIdx.x;
   for (; j + stride < n4; j += 2 * stride) {
-    float4 a = p4[j], b = p4[j + stride];
+    float4 x = p4[j], y = p4[j + stride];
     if (!rejected) {
-      const float4 ua = __ldg(U4 + j), ub = __ldg(U4 + j + stride);
-      a = make_float4(one(a.x, ua.x), one(a.y, ua.y), one(a.z, ua.z), one(a.w, ua.w));
-      b = make_float4(one(b.x, ub.x), one(b.y, ub.y), one(b.z, ub.z), one(b.w, ub.w));
-      p4[j] = a;
-      p4[j + stride] = b;
+      const float4 ux = __ldg(U4 + j), uy = __ldg(U4 + j + stride);
+      x = make_float4(one(x.x, ux.x), one(x.y, ux.y), one(x.z, ux.z), one(x.w, ux.w));
+      y = make_float4(one(y.x, uy.x), one(y.y, uy.y), one(y.z, uy.z), one(y.w, uy.w));
+      p4[j] = x;
+      p4[j + stride] = y;
     }
     if (out) {
-      put(j, a);
-      put(j + stride, b);
+      put(j, x);
+      put(j + stride, y);
     }
   }
   for (; j < n4; j += stride) {
-    float4 a = p4[j];
+    float4 x = p4[j];
     if (!rejected) {
-      const float4 ua = __ldg(U4 + j);
-      a = make_float4(one(a.x, ua.x), one(a.y, ua.y), one(a.z, ua.z), one(a.w, ua.w));
-      p4[j] = a;
+      const float4 ux = __ldg(U4 + j);
+      x = make_float4(one(x.x, ux.x), one(x.y, ux.y), one(x.z, ux.z), one(x.w, ux.w));
+      p4[j] = x;
     }
-    if (out) put(j, a);
+    if (out) put(j, x);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (c == 0 && threadIdx.x == 0) {
     for (int64_t k = n4 * 4; k < n; ++k) {
-      float v = p[k];
+      float x = p[k];
       if (!rejected) {
-        v = one(v, U[k]);
-        p[k] = v;
+        x = one(x, U[k]);
+        p[k] = x;
       }
-      if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
   }
 }
@@ -239,53 +319,83 @@ zopt_status check_hparams(const char* fn, const zopt_muon_hparams* hp) {
   return ok();
 }
 
-// Step 1 for matrices b0 .. b0 + gs - 1 of a job (contiguous): momentum, u into U_in.
-zopt_status launch_momentum(const Job& j, long long b0, int gs, float* U_in, const zopt_muon_hparams* hp, int sms,
-                            cudaStream_t s) {
-  const long long n = j.rows * j.cols, ng = n * gs;
-  const size_t gsz = j.gdt == ZOPT_F32 ? 4 : 2;
-  float* bm = j.momentum + b0 * n;
-  const uint8_t* gm = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
-  const float mu = static_cast<float>(hp->momentum);
-  long long blocks = (ng / 4 + kThreads - 1) / kThreads;
-  if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
-  if (blocks < 1) blocks = 1;
-  if (j.gdt == ZOPT_F32)
-    momentum_kernel<float><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
-        bm, reinterpret_cast<const float*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
-  else
-    momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
-        bm, reinterpret_cast<const __nv_bfloat16*>(gm), U_in, ng, mu, hp->nesterov ? 1 : 0);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  return ok();
-}
-
-// Steps 3 and 4 for matrices b0 .. b0 + gs - 1: per-matrix ||U|| and max |U| into the plan's
-// reduction area at ws, then the guarded update and bf16 round-out.
-zopt_status launch_update(const Job& j, long long b0, int gs, uint8_t* ws, const MuonPlan& P, const float* U_out,
-                          const zopt_muon_hparams* hp, cudaStream_t s) {
+// The element-wise item for matrices b0 .. b0 + gs - 1 of job j, whose workspace slice (plan P)
+// starts at ws.
+MuonItem item_of_job(const Job& j, long long b0, int gs, uint8_t* ws, const MuonPlan& P, const zopt_muon_hparams* hp) {
   const long long rows = j.rows, cols = j.cols, n = rows * cols;
+  const size_t gsz = j.gdt == ZOPT_F32 ? 4 : 2;
   const double scale = hp->adjust == ZOPT_MUON_MATCH_RMS_ADAMW
                            ? 0.2 * std::sqrt(static_cast<double>(rows > cols ? rows : cols))
                            : std::sqrt(rows > cols ? static_cast<double>(rows) / static_cast<double>(cols) : 1.0);
-  const float decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
-  const float step = static_cast<float>(hp->lr * scale);
-  const float sqrt_min = static_cast<float>(std::sqrt(static_cast<double>(rows < cols ? rows : cols)));
-  unsigned* maxbits = reinterpret_cast<unsigned*>(ws + P.off_max);
-  zopt_clip_stats* cs = reinterpret_cast<zopt_clip_stats*>(ws + P.off_cs);
-  ZOPT_CUDA_TRY(cudaMemsetAsync(ws, 0, P.off_cs, s));  // reduction counters and maxima start at zero
-  long long bpm = (n + 32767) / 32768;
-  bpm = bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm);
-  const dim3 grid(static_cast<unsigned>(bpm), static_cast<unsigned>(gs));
-  ustats_kernel<<<grid, kThreads, 0, s>>>(U_out, n, ws, maxbits, cs);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  uint16_t* out = j.out ? j.out + b0 * n : nullptr;
+  MuonItem it{};
+  it.master = j.master + b0 * n;
+  it.momentum = j.momentum + b0 * n;
+  it.grad = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
+  it.u_in = reinterpret_cast<float*>(ws + P.off_u);
+  it.u_out = reinterpret_cast<const float*>(ws + P.off_o);
+  it.out = j.out ? j.out + b0 * n : nullptr;
+  it.stats = j.stats + b0;
+  it.red = ws;
+  it.n = n;
+  it.batch = gs;
+  long long bpm = (n + kChunk - 1) / kChunk;  // depends on n only: a matrix's stats are the same in any call
+  it.bpm = static_cast<int>(bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm));
   // 8-byte bf16 stores need the first matrix 8-byte aligned and every matrix a multiple of 4
-  const int out8 = out != nullptr && (reinterpret_cast<uintptr_t>(out) & 7u) == 0 && (n & 3) == 0 ? 1 : 0;
-  update_kernel<<<grid, kThreads, 0, s>>>(j.master + b0 * n, U_out, out, n, out8, cs, maxbits, decay, step, hp->guard,
-                                          sqrt_min, j.stats + b0);
-  ZOPT_CUDA_TRY(cudaGetLastError());
-  return ok();
+  it.out8 = it.out != nullptr && (reinterpret_cast<uintptr_t>(it.out) & 7u) == 0 && (n & 3) == 0 ? 1 : 0;
+  it.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+  it.step = static_cast<float>(hp->lr * scale);
+  it.sqrt_min = static_cast<float>(std::sqrt(static_cast<double>(rows < cols ? rows : cols)));
+  return it;
+}
+
+enum Pass { kMomentumBf16, kMomentumF32, kStats, kUpdate };
+
+// One pass over every item that takes it (momentum: those with the pass's gradient dtype),
+// kMaxItems to a launch, one block per chunk (momentum) or per matrix block (stats, update).
+zopt_status launch_pass(Pass pass, const std::vector<MuonItem>& items, const std::vector<zopt_dtype>& gdt,
+                        const zopt_muon_hparams* hp, cudaStream_t s) {
+  MuonList L{};
+  L.mu = static_cast<float>(hp->momentum);
+  L.nesterov = hp->nesterov ? 1 : 0;
+  L.guard = hp->guard;
+  long long units = 0;
+  auto flush = [&]() -> zopt_status {
+    if (L.n == 0) return ok();
+    if (units > 0x7FFFFFFFLL) return fail(ZOPT_EINVAL, "zopt_muon_step: too many blocks for one launch");
+    const dim3 grid(static_cast<unsigned>(units)), block(kThreads);
+    if (pass == kMomentumBf16) momentum_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(L);
+    else if (pass == kMomentumF32) momentum_kernel<float><<<grid, block, 0, s>>>(L);
+    else if (pass == kStats) ustats_kernel<<<grid, block, 0, s>>>(L);
+    else update_kernel<<<grid, block, 0, s>>>(L);
+    ZOPT_CUDA_TRY(cudaGetLastError());
+    L.n = 0;
+    units = 0;
+    return ok();
+  };
+  zopt_status st = ZOPT_OK;
+  for (size_t k = 0; k < items.size(); ++k) {
+    if (pass == kMomentumBf16 && gdt[k] != ZOPT_BF16) continue;
+    if (pass == kMomentumF32 && gdt[k] != ZOPT_F32) continue;
+    if (L.n == kMaxItems && (st = flush()) != ZOPT_OK) return st;
+    MuonItem it = items[k];
+    it.u0 = units;
+    units += (pass == kMomentumBf16 || pass == kMomentumF32) ? (it.n * it.batch + kChunk - 1) / kChunk
+                                                             : static_cast<long long>(it.batch) * it.bpm;
+    L.it[L.n++] = it;
+  }
+  return flush();
+}
+
+zopt_status launch_momentum(const std::vector<MuonItem>& items, const std::vector<zopt_dtype>& gdt,
+                            const zopt_muon_hparams* hp, cudaStream_t s) {
+  zopt_status st = launch_pass(kMomentumBf16, items, gdt, hp, s);
+  return st != ZOPT_OK ? st : launch_pass(kMomentumF32, items, gdt, hp, s);
+}
+
+zopt_status launch_update(const std::vector<MuonItem>& items, const std::vector<zopt_dtype>& gdt,
+                          const zopt_muon_hparams* hp, cudaStream_t s) {
+  zopt_status st = launch_pass(kStats, items, gdt, hp, s);
+  return st != ZOPT_OK ? st : launch_pass(kUpdate, items, gdt, hp, s);
 }
 
 Job job_of(const zopt_muon_job& b) {
@@ -348,16 +458,18 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_muon_step: no CUDA device");
   const long long n = rows * cols;
+  const std::vector<zopt_dtype> gdt{grad_dtype};
   for (long long b0 = 0; b0 < batch; b0 += group) {
     const int gs = static_cast<int>(batch - b0 < group ? batch - b0 : group);
+    const std::vector<MuonItem> items{item_of_job(j, b0, gs, ws, P, hp)};
     // 1. momentum over the group's matrices (contiguous), u into the workspace
-    if ((st = launch_momentum(j, b0, gs, U_in, hp, sms, s)) != ZOPT_OK) return st;
+    if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
     // 2. U = NewtonSchulz(u), fp32 in and out, bf16 tensor cores
     st = zopt_ns_orthogonalize(U_in, U_out, ZOPT_F32, rows, cols, cols, cols, n, n, gs, ZOPT_BF16, hp->ns_steps,
                                hp->abc, hp->eps, ws + P.off_ns, P.ns_bytes, stream);
     if (st != ZOPT_OK) return st;
     // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
-    if ((st = launch_update(j, b0, gs, ws, P, U_out, hp, s)) != ZOPT_OK) return st;
+    if ((st = launch_update(items, gdt, hp, s)) != ZOPT_OK) return st;
   }
   return ok();
 }
@@ -402,28 +514,21 @@ extern "C" zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_
   // for all in one call (the shapes below 1024 share fused launches), then the updates
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   std::vector<zopt_ns_job> ns(static_cast<size_t>(n_jobs));
-  std::vector<size_t> off(static_cast<size_t>(n_jobs));
+  std::vector<MuonItem> items(static_cast<size_t>(n_jobs));
+  std::vector<zopt_dtype> gdt(static_cast<size_t>(n_jobs));
   size_t at = 0;
   for (int32_t k = 0; k < n_jobs; ++k) {
     const Job j = job_of(jobs[k]);
     const MuonPlan P = muon_plan(j.rows, j.cols, j.batch);
-    off[static_cast<size_t>(k)] = at;
-    float* U_in = reinterpret_cast<float*>(ws + at + P.off_u);
-    float* U_out = reinterpret_cast<float*>(ws + at + P.off_o);
-    if ((st = launch_momentum(j, 0, static_cast<int>(j.batch), U_in, hp, sms, s)) != ZOPT_OK) return st;
-    ns[static_cast<size_t>(k)] = ns_job_of(j, U_in, U_out);
+    items[static_cast<size_t>(k)] = item_of_job(j, 0, static_cast<int>(j.batch), ws + at, P, hp);
+    gdt[static_cast<size_t>(k)] = j.gdt;
+    ns[static_cast<size_t>(k)] = ns_job_of(j, items[static_cast<size_t>(k)].u_in,
+                                           const_cast<float*>(items[static_cast<size_t>(k)].u_out));
     at += static_cast<size_t>(round_up(static_cast<long long>(P.off_ns), 1024));
   }
+  if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
   if ((st = zopt_ns_orthogonalize_many(ns.data(), n_jobs, hp->ns_steps, hp->abc, hp->eps, ws + at, ws_bytes - at,
                                        stream)) != ZOPT_OK)
     return st;
-  for (int32_t k = 0; k < n_jobs; ++k) {
-    const Job j = job_of(jobs[k]);
-    const MuonPlan P = muon_plan(j.rows, j.cols, j.batch);
-    uint8_t* wj = ws + off[static_cast<size_t>(k)];
-    if ((st = launch_update(j, 0, static_cast<int>(j.batch), wj, P, reinterpret_cast<const float*>(wj + P.off_o), hp,
-                            s)) != ZOPT_OK)
-      return st;
-  }
-  return ok();
+  return launch_update(items, gdt, hp, s);
 }
