@@ -39,8 +39,8 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 # dram__bytes_write.sum on a 64 Mi-element shard prefix, 1.9 GB per launch, scaled by the element
 # count; see profiles/adamw_kernel_zero2_shard.md), valid while the kernel's sources hash to
 # ADAMW_SRC_DIGEST (otherwise the traffic is reported as null)
-ADAMW_TRAFFIC_PER_ELEM = (1073785984 + 881356928) / 67108864
-ADAMW_SRC_DIGEST = "1a0ee1cd43a08efb"
+ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
+ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 CPU_SAMPLE = 4_000_000
@@ -169,7 +169,7 @@ def adamw_traffic(S: int):
     None if the kernel's sources changed since."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("adamw.cu", "adam_common.cuh", "internal.h"):
+    for f in ("adamw.cu", "adam_common.cuh", "internal.h", "launch.cuh"):
         with open(os.path.join(ROOT, "zero_sharded_optimizer_flat_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return round(ADAMW_TRAFFIC_PER_ELEM * S) if h.hexdigest()[:16] == ADAMW_SRC_DIGEST else None

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "norm_impl.cuh"
 
 namespace zopt {
@@ -67,15 +68,14 @@ __global__ void __launch_bounds__(kNormThreads) accum_kernel(float* __restrict__
 template <typename T, bool kFirst, bool kLast>
 zopt_status launch(float* acc, const void* g, int64_t n, float max_norm, NormWorkspace* ws, zopt_clip_stats* stats,
                    cudaStream_t s) {
-  static int occ = 0;
-  if (occ == 0) {
+  const int occ = once([] {
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, accum_kernel<T, kFirst, kLast>, kNormThreads, 0) !=
             cudaSuccess ||
         o < 1)
       o = 1;
-    occ = o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
-  }
+    return o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+  });
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_grad_accumulate: no CUDA device");
   int64_t blocks = static_cast<int64_t>(norm_grid_blocks(n));

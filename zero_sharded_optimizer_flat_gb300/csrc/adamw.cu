@@ -25,6 +25,7 @@
 
 #include "adam_common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace zopt {
 namespace {
@@ -166,13 +167,12 @@ template <typename G, bool kOut>
 zopt_status launch(const HostScalars& hs, float* P, float* M, float* V, const void* g, uint16_t* out, int64_t n,
                    const int64_t* runs, int64_t nruns, const zopt_clip_stats* clip, zopt_adam_state* state,
                    cudaStream_t stream) {
-  static int occ = 0;  // resident blocks per SM for this instantiation
-  if (occ == 0) {
+  const int occ = once([] {  // resident blocks per SM for this instantiation
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, adamw_kernel<G, kOut>, kThreads, 0) != cudaSuccess || o < 1)
       o = kBlocksPerSm;
-    occ = o < kBlocksPerSm ? o : kBlocksPerSm;
-  }
+    return o < kBlocksPerSm ? o : kBlocksPerSm;
+  });
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_adamw_step: no CUDA device");
   const int64_t ntiles = (n + kTile - 1) / kTile;

@@ -10,6 +10,15 @@
 
 namespace zopt {
 
+// init() evaluated once per process, on the first call, and returned on every call: a
+// function-local static of a template instantiated per lambda type, i.e. per call site, so
+// concurrent first calls from several host threads are safe.
+template <typename F>
+auto once(F init) -> decltype(init()) {
+  static const decltype(init()) value = init();
+  return value;
+}
+
 // Launches `kernel` on `stream` with programmatic stream serialisation: it may start while
 // the previous kernel finishes (every kernel here waits with griddepcontrol.wait before it
 // touches global memory).

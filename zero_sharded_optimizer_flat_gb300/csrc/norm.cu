@@ -21,6 +21,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "norm_impl.cuh"
 
 namespace zopt {
@@ -33,21 +34,19 @@ size_t norm_grid_blocks(int64_t n) {
 }
 
 int norm_launch_blocks(int64_t n, zopt_dtype dtype) {
-  static int occ[2] = {0, 0};  // resident blocks per SM of each instantiation
-  const int k = dtype == ZOPT_F32 ? 0 : 1;
-  if (occ[k] == 0) {
+  // resident blocks per SM of each instantiation
+  auto occ_of = [](const void* kernel) {
     int o = 0;
-    const cudaError_t e =
-        k == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, norm_kernel<float>, kNormThreads, 0)
-               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, norm_kernel<__nv_bfloat16>, kNormThreads, 0);
-    if (e != cudaSuccess || o < 1) o = 1;
-    occ[k] = o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
-  }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kNormThreads, 0) != cudaSuccess || o < 1) o = 1;
+    return o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+  };
+  const int occ = dtype == ZOPT_F32 ? once([&] { return occ_of(reinterpret_cast<const void*>(norm_kernel<float>)); })
+                                    : once([&] { return occ_of(reinterpret_cast<const void*>(norm_kernel<__nv_bfloat16>)); });
   const int sms = sm_count();
   if (sms <= 0) return 0;
   // one wave of resident blocks; never more blocks than the workspace was sized for
   int64_t blocks = static_cast<int64_t>(norm_grid_blocks(n));
-  const int64_t wave = static_cast<int64_t>(sms) * occ[k];
+  const int64_t wave = static_cast<int64_t>(sms) * occ;
   return static_cast<int>(blocks < wave ? blocks : wave);
 }
 

@@ -220,12 +220,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 // job's prod[0..3] hold X X', B', B'X and the last step's B'X with everything but their tile
 // counts.
 zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(ns_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes(kEpiTma)));
-    attr_set = true;
-  }
+  ZOPT_CUDA_TRY(once([] {
+    return cudaFuncSetAttribute(ns_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kEpiTma));
+  }));
   if (f.n_jobs < 1 || f.n_jobs > kMaxFusedJobs) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: job count");
   long long at = 0;
   for (int p = 0; p < 3; ++p) {

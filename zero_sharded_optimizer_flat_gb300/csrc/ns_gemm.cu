@@ -525,16 +525,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // with 128-row (K-major) or 64 x 64 (MN-major) boxes; kEpiTmaR reads R, the TMA epilogues store
 // D through each job's maps.
 zopt_status launch_gemm_pair_batch(PairBatch& B, int epi, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes2(kEpiRegs)));
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes2(kEpiTmaR)));
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes2(kEpiTma)));
-    attr_set = true;
-  }
+  ZOPT_CUDA_TRY(once([] {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes2(kEpiRegs));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes2(kEpiTmaR));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_bf16_pair_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes2(kEpiTma));
+    return e;
+  }));
   if (B.n < 1 || B.n > kMaxPairJobs) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: internal: bad pair batch");
   long long total = 0;
   for (int j = 0; j < B.n; ++j) {
@@ -596,16 +594,14 @@ bool tiles_1cta(GemmArgs& a) {
 // D through *D (32 x 32 boxes, 64-byte swizzle).
 zopt_status launch_gemm(const CUtensorMap& P, const CUtensorMap& Q, const CUtensorMap* R, const CUtensorMap* D,
                         int epi, GemmArgs a, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes(kEpiRegs)));
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes(kEpiTmaR)));
-    ZOPT_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes(kEpiTma)));
-    attr_set = true;
-  }
+  ZOPT_CUDA_TRY(once([] {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<kEpiRegs>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kEpiRegs));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTmaR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kEpiTmaR));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_bf16_kernel<kEpiTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kEpiTma));
+    return e;
+  }));
   if (!tiles_1cta(a)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize: too many tiles");
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize: no CUDA device");
