@@ -311,6 +311,12 @@ ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t
 ZOPT_API int32_t zopt_take_device_error(void);
 ZOPT_API zopt_status zopt_selftest_wait_timeout(int64_t limit_ns, zopt_stream stream);
 ZOPT_API zopt_status zopt_selftest_count_timeout(int64_t limit_ns, zopt_stream stream);
+/* The rescale kernel divides sqrt(v) by the launch's constant c = sqrt(1 - beta2^t) through a
+ * reciprocal and one FMA correction (Markstein, IBM J. Res. Develop. 34(1), 1990) instead of an
+ * IEEE division. zopt_selftest_div_by_const compares the two for every bit pattern of v >= 0
+ * at the given c in (0, 1] and adds the number of differing results to *d_mismatches (device
+ * uint64, 8-byte aligned; NaN matches NaN). EINVAL for a bad counter or c. */
+ZOPT_API zopt_status zopt_selftest_div_by_const(float c, unsigned long long* d_mismatches, zopt_stream stream);
 
 /* ======================================================================================
  * 5. Muon's update around Newton-Schulz (matrices owned whole by this rank)

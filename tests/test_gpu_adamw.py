@@ -309,3 +309,29 @@ def test_rescale_tile_edges(zopt, n):
     for r, t in zip(spec, (case.p, case.m, case.v)):
         assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))
     assert np.array_equal(case.out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(spec[0]))
+
+
+def test_rescale_division_by_constant_is_exact(zopt):
+    """The rescale kernel forms sqrt(v) / c, c = sqrt(1 - beta2^t), with a reciprocal and one FMA
+    correction (Markstein's method) instead of an IEEE division. For every bit pattern of
+    v >= 0 (and the positive NaNs) the result equals __fdiv_rn's, at each c of a grid of betas
+    and steps and at 200 random c in (0, 1]."""
+    cs = {1.0, float(np.float32(2.0 ** -20))}
+    for b2 in (0.9, 0.95, 0.98, 0.99, 0.995, 0.999, 0.9999, 0.99999):
+        for t in (1, 2, 3, 5, 7, 10, 30, 100, 300, 1000, 3000, 10000, 100000, 1000000):
+            cs.add(float(np.float32(np.sqrt(1.0 - b2 ** t))))
+    rng = np.random.default_rng(7)
+    cs.update(float(x) for x in rng.uniform(2.0 ** -20, 1.0, 200).astype(np.float32))
+    counter = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for c in sorted(cs):
+        assert 0.0 < c <= 1.0
+        zopt.selftest_div_by_const(c, counter)
+    torch.cuda.synchronize()
+    assert int(counter.item()) == 0
+
+
+def test_rescale_division_selftest_rejects_bad_arguments(zopt):
+    counter = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for c in (0.0, -1.0, 1.5, float("nan")):
+        with pytest.raises(zopt.ZoptError):
+            zopt.selftest_div_by_const(c, counter)

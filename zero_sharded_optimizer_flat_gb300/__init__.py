@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
         "zopt_take_device_error": (i32, []),
         "zopt_selftest_wait_timeout": (ctypes.c_int, [i64, vp]),
         "zopt_selftest_count_timeout": (ctypes.c_int, [i64, vp]),
+        "zopt_selftest_div_by_const": (ctypes.c_int, [ctypes.c_float, vp, vp]),
         "zopt_muon_step": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, vp, i64, i64, i32, ctypes.POINTER(_MuonHparams),
                                           vp, vp, sz, vp]),
         "zopt_ns_orthogonalize": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i32,
@@ -470,6 +471,12 @@ def take_device_error() -> int:
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     """Run the bounded-wait path on a barrier nothing completes (limit_ns <= 2 s)."""
     _check(lib().zopt_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def selftest_div_by_const(c: float, counter, stream=None) -> None:
+    """Add to counter (a 1-element int64 CUDA tensor) the number of v >= 0 bit patterns for which
+    the rescale kernel's sqrt(v) / c differs from the IEEE division."""
+    _check(lib().zopt_selftest_div_by_const(ctypes.c_float(c), ctypes.c_void_p(counter.data_ptr()), _stream(stream)))
 
 
 def selftest_count_timeout(limit_ns: int, stream=None) -> None:

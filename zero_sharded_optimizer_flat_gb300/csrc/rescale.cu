@@ -22,8 +22,24 @@ struct RescaleHost {
   float eps;
 };
 
-__device__ __forceinline__ float adam_dir(float m, float v, float bc2s, float eps) {
-  return __fdiv_rn(m, __fadd_rn(__fdiv_rn(__fsqrt_rn(v), bc2s), eps));
+// x / c, correctly rounded, for the launch's constant c = sqrt(1 - beta2^t) in (0, 1] given
+// rc = RN(1 / c) (__frcp_rn): Markstein's correction (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990). With rc
+// correctly rounded, q = RN(x rc) is within one ulp of x / c, the residual x - q c is exact
+// through an FMA, and RN(q + (x - q c) rc) = RN(x / c) as long as nothing overflows or
+// underflows, which holds for every x = sqrt(v) (v >= 0: x is 0, normal, +inf or NaN). Zero
+// and infinity pass through (the residual of an infinity would be NaN). Checked against
+// __fdiv_rn for every v bit pattern by zopt_selftest_div_by_const.
+__device__ __forceinline__ float div_by_const(float x, float c, float rc) {
+  const float q = __fmul_rn(x, rc);
+  const float e = __fmaf_rn(-q, c, x);
+  const float r = __fmaf_rn(e, rc, q);
+  return (x == 0.0f || isinf(x)) ? x : r;
+}
+
+// m / (sqrt(v) / bc2s + eps), each operation correctly rounded (bc2s: rc = RN(1 / bc2s)).
+__device__ __forceinline__ float adam_dir(float m, float v, float bc2s, float rc, float eps) {
+  return __fdiv_rn(m, __fadd_rn(div_by_const(__fsqrt_rn(v), bc2s, rc), eps));
 }
 
 // Tiles of kTile elements, as adamw_kernel walks them: a thread holds 2 x 4 elements of each
@@ -35,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) rescale_kernel(float* 
                                                                          uint16_t* __restrict__ out, int64_t n,
                                                                          RescaleHost hs, const zopt_clip_stats* clip,
                                                                          const zopt_adam_state* state) {
-  __shared__ float s_km, s_kv, s_step, s_bc2s;
+  __shared__ float s_km, s_kv, s_step, s_bc2s, s_rc;
   __shared__ int s_skip;
   if (threadIdx.x == 0) {
     const long long t = *reinterpret_cast<const volatile long long*>(&state->step);
@@ -52,17 +68,18 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) rescale_kernel(float* 
     const double bc2 = __dsub_rn(1.0, pow_sq_mul(hs.beta2, t));
     s_step = __double2float_rn(__ddiv_rn(hs.lr, bc1));
     s_bc2s = __double2float_rn(__dsqrt_rn(bc2));
+    s_rc = __frcp_rn(s_bc2s);
     s_skip = skip;
   }
   __syncthreads();
   if (s_skip) return;
-  const float km = s_km, kv = s_kv, step = s_step, bc2s = s_bc2s, eps = hs.eps;
+  const float km = s_km, kv = s_kv, step = s_step, bc2s = s_bc2s, rc = s_rc, eps = hs.eps;
   auto one = [&](float& p, float& m, float& v, float g) {
-    const float u_old = adam_dir(m, v, bc2s, eps);
+    const float u_old = adam_dir(m, v, bc2s, rc, eps);
     m = __fadd_rn(m, __fmul_rn(km, g));
     const float vv = __fadd_rn(v, __fmul_rn(kv, __fmul_rn(g, g)));
     v = vv < 0.0f ? 0.0f : vv;
-    const float u_new = adam_dir(m, v, bc2s, eps);
+    const float u_new = adam_dir(m, v, bc2s, rc, eps);
     p = __fadd_rn(p, __fmul_rn(step, __fsub_rn(u_old, u_new)));
   };
   auto put_bf16 = [&](int64_t x, const Vec4& p) {
@@ -116,8 +133,38 @@ zopt_status launch_rescale(const RescaleHost& hs, float* P, float* M, float* V, 
   return ok();
 }
 
+// div_by_const(sqrt(v), c, RN(1 / c)) against __fdiv_rn(sqrt(v), c) for every bit pattern of
+// v >= 0 (and the positive NaNs): the count of results that differ (NaN matching NaN).
+__global__ void __launch_bounds__(256) div_selftest_kernel(float c, unsigned long long* mismatches) {
+  const float rc = __frcp_rn(c);
+  unsigned long long bad = 0;
+  const unsigned int stride = gridDim.x * blockDim.x;
+  for (unsigned int b = blockIdx.x * blockDim.x + threadIdx.x; b < 0x80000000u; b += stride) {
+    const float x = __fsqrt_rn(__uint_as_float(b));
+    const float fast = div_by_const(x, c, rc), ref = __fdiv_rn(x, c);
+    const bool same = __float_as_uint(fast) == __float_as_uint(ref) || (isnan(fast) && isnan(ref));
+    bad += same ? 0u : 1u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+  if ((threadIdx.x & 31) == 0 && bad != 0) atomicAdd(mismatches, bad);
+}
+
 }  // namespace
 }  // namespace zopt
+
+extern "C" zopt_status zopt_selftest_div_by_const(float c, unsigned long long* d_mismatches, zopt_stream stream) {
+  using namespace zopt;
+  if (d_mismatches == nullptr || (reinterpret_cast<uintptr_t>(d_mismatches) & 7u) != 0)
+    return fail(ZOPT_EINVAL, "zopt_selftest_div_by_const: counter is NULL or misaligned");
+  if (!(c > 0.0f && c <= 1.0f)) return fail(ZOPT_EINVAL, "zopt_selftest_div_by_const: c must lie in (0, 1]");
+  const int sms = sm_count();
+  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_selftest_div_by_const: no CUDA device");
+  div_selftest_kernel<<<static_cast<unsigned>(sms * 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      c, d_mismatches);
+  ZOPT_CUDA_TRY(cudaGetLastError());
+  return ok();
+}
 
 extern "C" zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* master, float* exp_avg,
                                                float* exp_avg_sq, const void* grad, zopt_dtype grad_dtype,
