@@ -473,3 +473,37 @@ def test_nonfinite_input_propagates_and_context_survives(zopt, bad):
     zopt.ns_orthogonalize(G2, X, ws, steps=5)
     torch.cuda.synchronize()
     assert rel(X.cpu(), torch.from_numpy(newton_schulz(G2.double().cpu().numpy(), steps=5))) <= 2e-2
+
+
+@pytest.mark.parametrize("abc", [(1.5, -0.5, 0.0), (2.0, -1.5, 0.5), (3.0, -3.2, 1.2)])
+@pytest.mark.parametrize("rows,cols", [(256, 768), (768, 256), (1024, 1100)])
+def test_other_coefficients_match_fp64_oracle(zopt, abc, rows, cols):
+    """The triple is an argument: with c = 0 (the cubic Newton-Schulz 1.5 X - 0.5 X X' X) the b A
+    term cannot ride on identity MMAs scaled by 1/c, so B' takes it through the R epilogue
+    instead of the fused kernel; other triples take the usual paths. Each result is within the
+    bf16 tolerance of the fp64 oracle run with the same triple, and in a many-jobs call bitwise
+    the single call's."""
+    G = gaussian(rows, cols, rows + cols + int(abc[0] * 10))
+    X = torch.empty_like(G)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols), steps=5, abc=abc)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5, abc=abc)
+    assert rel(X.cpu(), torch.from_numpy(ref)) <= 2e-2
+    Y = torch.empty(1, rows, cols, device="cuda", dtype=torch.bfloat16)
+    H = gaussian(300, 700, 5)[None]
+    Hx = torch.empty_like(H)
+    zopt.ns_orthogonalize_many([(G[None], Y), (H, Hx)],
+                               zopt.new_ns_workspace_many([(rows, cols, 1), (300, 700, 1)]), steps=5, abc=abc)
+    torch.cuda.synchronize()
+    assert torch.equal(Y[0], X)
+
+
+@pytest.mark.parametrize("abc", [(1.5, -0.5, 0.0), (2.0, -1.5, 0.5)])
+def test_other_coefficients_fp32_mode(zopt, abc):
+    G = torch.randn(256, 640, device="cuda")
+    X = torch.empty_like(G)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(256, 640, compute=zopt.F32), steps=5, abc=abc,
+                          compute=zopt.F32)
+    torch.cuda.synchronize()
+    ref = newton_schulz(G.double().cpu().numpy(), steps=5, abc=abc)
+    assert rel(X.cpu(), torch.from_numpy(ref)) <= 1e-4
