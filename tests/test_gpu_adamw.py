@@ -335,3 +335,18 @@ def test_rescale_division_selftest_rejects_bad_arguments(zopt):
     for c in (0.0, -1.0, 1.5, float("nan")):
         with pytest.raises(zopt.ZoptError):
             zopt.selftest_div_by_const(c, counter)
+
+
+@pytest.mark.parametrize("hp", [OA.Hyper(lr=3e-4, beta1=0.0, beta2=0.999, eps=1e-8, weight_decay=0.0),
+                                OA.Hyper(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-6, weight_decay=0.01),
+                                OA.Hyper(lr=0.0, beta1=0.8, beta2=0.9, eps=1e-8, weight_decay=0.1),
+                                OA.Hyper(lr=1e-3, beta1=0.99, beta2=0.9999, eps=1e-10, weight_decay=1.0)])
+def test_other_hyperparameters_bitwise(zopt, hp):
+    """The exact-order step holds for any hyper-parameters: no momentum (beta1 = 0), a slow second
+    moment (beta2 = 0.999 / 0.9999: a small bias-correction constant), lr = 0 (decay only by
+    1 - 0 = 1: the master stays put), no weight decay, a large decay; four steps each, master,
+    m, v and bf16 weights bit for bit the oracle's."""
+    case = Case(zopt, SMALL, 4000, 2, 1, seed=31, gdtype=torch.bfloat16)
+    for s in range(4):
+        case.step(s, hp, max_norm=1.0)
+        case.compare()
