@@ -183,3 +183,33 @@ def test_nan_gradient_is_rejected(zopt):
     assert torch.equal(p.view(torch.int32), p0.view(torch.int32))
     assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(p0.cpu().numpy()))
     assert math.isnan(float(buf[3, 4])) and int(torch.isnan(buf).sum()) == 1
+
+
+@pytest.mark.parametrize("nesterov,mom,wd", [(False, 0.9, 0.0), (True, 0.5, 0.05), (False, 0.0, 0.1)])
+def test_momentum_variants(zopt, nesterov, mom, wd):
+    """Plain momentum (u = buf), another coefficient, no or other weight decay, and mu = 0 (u = g):
+    two steps, the momentum buffer bit for bit, the applied update within 2e-2 of the fp64
+    Newton-Schulz of the oracle's u, the bf16 weights bit for bit the new master's."""
+    rows, cols, batch = 256, 512, 2
+    h = OM.MuonHyper(lr=5e-4, momentum=mom, weight_decay=wd, nesterov=nesterov)
+    gen = torch.Generator(device="cuda").manual_seed(int(mom * 100) + int(nesterov))
+    p = torch.randn(batch, rows, cols, generator=gen, device="cuda") * 0.02
+    buf = torch.zeros_like(p)
+    out = torch.zeros(batch, rows, cols, dtype=torch.int16, device="cuda")
+    ws, stats = zopt.new_muon_workspace(rows, cols, batch), zopt.new_muon_stats(batch)
+    ref_buf = np.zeros((batch, rows, cols), np.float32)
+    decay = np.float32(1.0 - h.lr * h.weight_decay)
+    step = np.float32(h.lr * OM.lr_scale(rows, cols, True))
+    for s in range(2):
+        g = (torch.randn(batch, rows, cols, generator=gen, device="cuda") * 1e-3).bfloat16()
+        p_old = p.cpu().numpy()
+        zopt.muon_step(p, buf, g, out, ws, stats, lr=h.lr, momentum_coef=mom, weight_decay=wd, nesterov=nesterov)
+        torch.cuda.synchronize()
+        pn = p.cpu().numpy()
+        for b in range(batch):
+            u = OM.momentum_f32(ref_buf[b], g[b].float().cpu().numpy(), h)
+            U_ref = newton_schulz(u.astype(np.float64), steps=5)
+            applied = (p_old[b] * decay - pn[b]).astype(np.float64) / float(step)
+            assert rel(applied, U_ref) <= 2e-2, (s, b)
+        assert np.array_equal(buf.cpu().numpy().view(np.uint32), ref_buf.view(np.uint32))
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))
