@@ -444,11 +444,13 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         ms, a_ms, k_ms, n_ms, nr_ms, rs_ms, mu_ms = (float(x) for x in tt)
         dist.barrier()
 
-    # ---- end to end through the public API with host buffers: each part copies its inputs
+    # ---- end to end through the public API with host buffers: each part takes its inputs
     # (the micro-step gradients; the Newton-Schulz inputs) from pinned host memory and reads
-    # its results back (the clip stats; the orthogonalised matrices). The copies run on two
-    # copy streams, overlapped with the compute of the previous micro-step or matrix group;
-    # each part is timed from its first copy to its last read-back.
+    # its results back (the clip stats; the orthogonalised matrices). The accumulation passes
+    # read the pinned micro-step gradients themselves, over the CPU-GPU link (no staging copy);
+    # the Newton-Schulz inputs and outputs move on two copy streams, overlapped with the compute
+    # of the previous or next matrix group. Each part is timed from its first transfer to its
+    # last read-back.
     h2d = d2h = 0
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -457,9 +459,6 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         stats_host = torch.empty(Z.CLIP_STATS_BYTES, dtype=torch.uint8).pin_memory()
         h2d += 2 * S * MICRO_STEPS
         d2h += Z.CLIP_STATS_BYTES
-        acc_done = [ev() for _ in micro]
-        for e in acc_done:
-            e.record(stream)
     if ns is not None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
@@ -485,20 +484,9 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         if "adamw" in parts:
             start = mk() if i is None else ee_a[i][0]
             start.record(stream)
-            h2d_s.wait_event(start)
-            landed = []
-            for k, (mg, mh) in enumerate(zip(micro, micro_host)):
-                h2d_s.wait_event(acc_done[k])  # the previous step has read this buffer
-                with torch.cuda.stream(h2d_s):
-                    mg.copy_(mh, non_blocking=True)
-                e = ev()
-                e.record(h2d_s)
-                landed.append(e)
-            for k, mg in enumerate(micro):
-                stream.wait_event(landed[k])
-                Z.grad_accumulate(g, mg, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
+            for k, mh in enumerate(micro_host):
+                Z.grad_accumulate(g, mh, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
                                   stats=clip, stream=stream)
-                acc_done[k].record(stream)
             Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
             stats_host.copy_(clip, non_blocking=True)
             if i is not None:

@@ -153,8 +153,13 @@ ZOPT_API zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype dt
  * in call order). On the micro-step flagged ZOPT_ACC_LAST the same pass also reduces the
  * finished sum exactly as zopt_grad_norm_clip does and writes *d_stats (d_ws and d_stats are
  * only used then; d_ws follows zopt_grad_norm_clip's rules). Both flags together: one part.
- * Errors: EINVAL for n < 1, NULL/misaligned pointers, unknown flags, a missing workspace or
- * stats on the last micro-step; EUNSUPPORTED for a dtype other than fp32/bf16. */
+ * micro_grad may be device memory or page-locked host memory (cudaHostAlloc / cudaHostRegister,
+ * e.g. a pinned torch tensor): the pass then reads it through the memory's device mapping over
+ * the CPU-GPU link, so the host-to-device transfer and the addition are one pass with no staging
+ * buffer in HBM. The caller keeps that host memory unchanged until the call has run on the stream.
+ * Errors: EINVAL for n < 1, NULL/misaligned pointers, pageable host memory or memory of another
+ * device as micro_grad, unknown flags, a missing workspace or stats on the last micro-step;
+ * EUNSUPPORTED for a dtype other than fp32/bf16. */
 #define ZOPT_ACC_FIRST 1
 #define ZOPT_ACC_LAST 2
 ZOPT_API zopt_status zopt_grad_accumulate(float* acc, const void* micro_grad, zopt_dtype dtype, int64_t n,

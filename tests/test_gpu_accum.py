@@ -71,6 +71,27 @@ def test_rejects_bad_arguments(zopt):
         zopt.grad_accumulate(acc, g.half(), first=True, last=False)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("n", [5, 8 * 1027 + 3, 1_000_003])
+def test_page_locked_host_micro_grads(zopt, dtype, n):
+    """Micro-step gradients read straight from pinned host memory give the device path's
+    sum and stats bit for bit (and the oracle's sum)."""
+    gen = torch.Generator().manual_seed(n)
+    parts = [(torch.randn(n, generator=gen) * 1e-3).to(dtype) for _ in range(3)]
+    host = [p.pin_memory() for p in parts]
+    acc_h, st_h = run(zopt, host)
+    acc_d, st_d = run(zopt, [p.cuda() for p in parts])
+    assert torch.equal(acc_h, acc_d) and st_h == st_d
+    ref = accumulate([p.float().numpy() for p in parts])
+    assert np.array_equal(acc_h.cpu().numpy(), ref)
+
+
+def test_pageable_host_micro_grad_is_refused(zopt):
+    acc = torch.zeros(64, device="cuda")
+    with pytest.raises(zopt.ZoptError, match="pageable"):
+        zopt.grad_accumulate(acc, torch.zeros(64, dtype=torch.bfloat16), first=True, last=False)
+
+
 def test_full_size_zero2_micro_steps_with_inf_run(zopt):
     """The 2e9-parameter set's rank-0 shard (S = 250,000,000): 4 bf16 micro-steps summed in
     fp32 (sampled slots bit for bit, the fused sum of squares against the oracle's over the

@@ -12,6 +12,10 @@
 // The arrays are walked in 4-element units, a warp's 32 units contiguous (512 B of fp32, 256 B of
 // bf16 per load instruction); each thread issues the loads of four units before it adds and
 // stores any of them, so that enough bytes are in flight to keep HBM busy.
+//
+// A micro-step gradient may also sit in page-locked host memory: the pass then reads it through
+// the device mapping of that memory, over the CPU-GPU link, with no staging copy in HBM (the
+// host-to-device transfer and the addition are one pass).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -96,6 +100,35 @@ zopt_status dispatch(bool first, bool last, float* acc, const void* g, int64_t n
   return launch<T, false, false>(acc, g, n, max_norm, ws, stats, s);
 }
 
+// The address the kernel reads micro_grad through: device (or managed) memory as it is;
+// page-locked host memory through its device mapping, so the pass itself pulls the micro-step
+// over the host link and no staging copy in HBM is needed. Pageable host memory is refused.
+zopt_status device_view(const void* p, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(ZOPT_EINVAL, "zopt_grad_accumulate: micro_grad is not a CUDA-visible address");
+  }
+  int dev = -1;
+  ZOPT_CUDA_TRY(cudaGetDevice(&dev));
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      if (a.device != dev) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: micro_grad is on another device");
+      *out = p;
+      return ok();
+    case cudaMemoryTypeManaged:
+      *out = p;
+      return ok();
+    case cudaMemoryTypeHost:
+      if (a.devicePointer == nullptr)
+        return fail(ZOPT_EINVAL, "zopt_grad_accumulate: micro_grad's page-locked host memory has no device mapping");
+      *out = a.devicePointer;
+      return ok();
+    default:
+      return fail(ZOPT_EINVAL, "zopt_grad_accumulate: micro_grad is pageable host memory (pin or register it)");
+  }
+}
+
 }  // namespace
 }  // namespace zopt
 
@@ -117,8 +150,12 @@ extern "C" zopt_status zopt_grad_accumulate(float* acc, const void* micro_grad, 
     if (d_ws == nullptr || !aligned16(d_ws) || ws_bytes < zopt_grad_norm_workspace(n))
       return fail(ZOPT_EINVAL, "zopt_grad_accumulate: the last micro-step needs a zopt_grad_norm_workspace(n) workspace");
   }
+  const void* g = nullptr;
+  zopt_status st = device_view(micro_grad, &g);
+  if (st != ZOPT_OK) return st;
+  if (!aligned16(g)) return fail(ZOPT_EINVAL, "zopt_grad_accumulate: micro_grad's device address is not 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   NormWorkspace* ws = static_cast<NormWorkspace*>(d_ws);
-  return dtype == ZOPT_F32 ? dispatch<float>(first, last, acc, micro_grad, n, max_norm, ws, d_stats, s)
-                           : dispatch<__nv_bfloat16>(first, last, acc, micro_grad, n, max_norm, ws, d_stats, s);
+  return dtype == ZOPT_F32 ? dispatch<float>(first, last, acc, g, n, max_norm, ws, d_stats, s)
+                           : dispatch<__nv_bfloat16>(first, last, acc, g, n, max_norm, ws, d_stats, s);
 }
