@@ -133,6 +133,33 @@ def test_many_shapes_equal_single_calls(zopt):
             assert torch.equal(d["st"][0], d["st"][1])
 
 
+def test_many_shapes_beyond_one_elementwise_launch(zopt):
+    """Ten shapes: more than one element-wise launch's worth of items (eight to a launch), so the
+    momentum, statistics and update passes each run twice; every shape is bitwise its single call."""
+    specs = [(1 + j % 2, 64 + 32 * j, 160 - 8 * j, torch.bfloat16 if j % 3 else torch.float32) for j in range(10)]
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    sets = []
+    for b, r, c, gdt in specs:
+        p = torch.randn(b, r, c, generator=gen, device="cuda") * 0.02
+        sets.append(dict(p=[p.clone(), p.clone()], buf=[torch.zeros_like(p), torch.zeros_like(p)],
+                         out=[torch.zeros(b, r, c, dtype=torch.int16, device="cuda") for _ in range(2)],
+                         st=[zopt.new_muon_stats(b), zopt.new_muon_stats(b)], gdt=gdt, shape=(b, r, c)))
+    ws = zopt.new_muon_workspace_many([(r, c, b) for b, r, c, _ in specs])
+    for step in range(2):
+        grads = [(torch.randn(*d["shape"], generator=gen, device="cuda") * 1e-3).to(d["gdt"]) for d in sets]
+        zopt.muon_step_many([(d["p"][0], d["buf"][0], g, d["out"][0], d["st"][0]) for d, g in zip(sets, grads)], ws,
+                            lr=8e-4)
+        for d, g in zip(sets, grads):
+            b, r, c = d["shape"]
+            zopt.muon_step(d["p"][1], d["buf"][1], g, d["out"][1], zopt.new_muon_workspace(r, c, b), d["st"][1],
+                           lr=8e-4)
+        torch.cuda.synchronize()
+        for d in sets:
+            assert torch.equal(d["p"][0].view(torch.int32), d["p"][1].view(torch.int32)), d["shape"]
+            assert torch.equal(d["buf"][0], d["buf"][1]) and torch.equal(d["out"][0], d["out"][1])
+            assert torch.equal(d["st"][0], d["st"][1])
+
+
 @pytest.mark.parametrize("rows,cols,batch,shift", [(129, 77, 1, 1), (96, 100, 2, 2), (1, 3, 1, 0)])
 def test_odd_sizes_and_unaligned_out(zopt, rows, cols, batch, shift):
     """The statistics and update kernels move 4-element vectors and finish a matrix whose size is

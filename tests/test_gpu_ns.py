@@ -373,6 +373,27 @@ def test_many_jobs_step_counts(zopt, steps):
         assert rel(X[0].cpu(), torch.from_numpy(ref)) <= 2e-2
 
 
+def test_many_jobs_beyond_one_preparation_list(zopt):
+    """Nineteen jobs: more than one preparation launch's worth of items (the norm list holds 19,
+    the scaling list 17, the transpose list 2), three fused launches of six jobs, and one job
+    (fp32, 33 columns) whose output the TMA cannot address, product by product. Each job equals
+    its single call bit for bit."""
+    gen = torch.Generator(device="cuda").manual_seed(41)
+    specs = [(1 + j % 3, 64 + 16 * j, 96 + 24 * j, torch.bfloat16 if j % 2 == 0 else torch.float32) for j in range(17)]
+    specs += [(2, 300, 120, torch.bfloat16), (1, 257, 33, torch.float32)]
+    pairs = [(torch.randn(b, r, c, generator=gen, device="cuda").to(dt),
+              torch.empty(b, r, c, device="cuda", dtype=dt)) for b, r, c, dt in specs]
+    zopt.ns_orthogonalize_many(pairs, zopt.new_ns_workspace_many([(r, c, b) for b, r, c, _ in specs]), steps=2)
+    torch.cuda.synchronize()
+    for (G, X), (b, r, c, _) in zip(pairs, specs):
+        one = torch.empty_like(X)
+        zopt.ns_orthogonalize(G, one, zopt.new_ns_workspace(r, c, b), steps=2)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X), (r, c, b)
+    ref = newton_schulz(pairs[17][0][1].double().cpu().numpy(), steps=2)
+    assert rel(pairs[17][1][1].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
 def test_many_pair_jobs_batched(zopt):
     """zopt_ns_orthogonalize_many runs each product of a step for all its CTA-pair jobs (m >= 1024)
     in one launch, four jobs to a launch and those with the same epilogue together: six pair jobs
