@@ -4,6 +4,8 @@ The layout is pinned by brute force: every flat index is mapped forward (bucket 
 rank -> shard slot) with plain integer arithmetic written independently of the oracle's
 piece walk, and the oracle's shard tables must be exactly the inverse of that map.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -115,3 +117,27 @@ def test_sampled_slot_map_equals_enumeration(numel, bucket, world):
         for f, i in zip(idx, owner):
             if f >= 0:
                 assert offsets[i] <= f < offsets[i + 1]
+
+
+def test_round_robin_muon_ownership_counts():
+    """Whole-parameter Muon ownership (bluscript_zero_ckpt.cpp, ShardedMuon: each matrix has one
+    owner rank; matrix i belongs to rank i mod W): over the 1.1B Llama-style set's 96 matrices
+    and W = 8, every matrix has exactly one owner, every rank owns 12, and rank 0's twelve (six
+    matrices per layer, so every eighth one) are Wq, Wv and gate_up, four of each, in model
+    order."""
+    c3 = workloads.get("c3")
+    assert len(c3.muon) == 96
+    seen = {}
+    for r in range(c3.world):
+        w = dataclasses.replace(c3, rank=r)
+        own = w.owned_muon()
+        assert len(own) == 12
+        for p in own:
+            assert p.name not in seen
+            seen[p.name] = r
+    assert len(seen) == 96
+    own0 = c3.owned_muon()
+    assert [p.shape for p in own0] == [(2048, 2048), (2048, 512), (2048, 11264)] * 4
+    assert [p.name for p in own0] == [f"l{4 * q + k}.{n}" for q in range(4) for k, n in
+                                      enumerate(("wq", "wv", "gate_up"))]
+    assert [c3.muon.index(p) for p in own0] == list(range(0, 96, 8))
