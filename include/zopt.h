@@ -2,18 +2,25 @@
  * zopt.h — C ABI of libzopt, the rank-local optimizer step of a ZeRO-sharded trainer on one
  * GB300 (sm_103a).
  *
- * Three parts, each a few calls:
+ * Five parts, each a few calls:
  *   1. the flat bucketed shard layout            (zopt_shard_layout and accessors, host only)
- *   2. the gradient norm / clip / found_inf stats (zopt_grad_norm_clip, device values)
- *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step)
- *   4. Muon's quintic Newton-Schulz               (zopt_ns_orthogonalize)
+ *   2. the gradient norm / clip / found_inf stats (zopt_grad_norm_clip, zopt_clip_finalize,
+ *      zopt_grad_accumulate for micro-step sums with the stats fused; device values)
+ *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step, zopt_adamw_rescale_step)
+ *   4. Muon's quintic Newton-Schulz               (zopt_ns_orthogonalize, _many)
+ *   5. Muon's update around Newton-Schulz         (zopt_muon_step, _many)
  *
  * Conventions shared by every call:
- *   - Pointers named d_* and every tensor argument are DEVICE pointers owned by the caller.
- *     The library allocates no device memory; scratch space is a caller-provided workspace
- *     whose size a *_workspace() query returns.
+ *   - Pointers named d_* and every tensor argument are DEVICE pointers owned by the caller,
+ *     except where a call says otherwise (zopt_grad_accumulate also reads page-locked host
+ *     memory). The library allocates no device memory; scratch space is a caller-provided
+ *     workspace whose size a *_workspace() query returns.
  *   - Every device call is asynchronous on the given stream (a cudaStream_t; NULL is the
- *     legacy default stream) and never synchronises the host.
+ *     legacy default stream) and never synchronises the host. Every per-step quantity (clip
+ *     coefficient, found_inf, the AdamW step counter, the Newton-Schulz norms, the Muon
+ *     guard) stays on the device, so a whole step can be captured in a CUDA graph and
+ *     replayed; make each entry point's first call outside the capture (one-time setup:
+ *     kernel attributes, occupancy queries, the mapped error word).
  *   - Arguments are validated before any launch. On failure a call returns a non-zero
  *     zopt_status, launches nothing, and zopt_last_error() describes the problem.
  *   - Device arrays must start on a 16-byte boundary (128-bit vector access).
