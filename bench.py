@@ -246,9 +246,17 @@ class NsPart:
         # one call over every shape (zopt_ns_orthogonalize_many): each shape's whole batch is one
         # group; shapes below 1024 share persistent fused launches (six to a launch)
         self.ws = Z.new_ns_workspace_many([(G.shape[1], G.shape[2], G.shape[0]) for G, _ in self.groups])
-        # the end-to-end pass calls zopt_ns_orthogonalize on chunks of up to 4 matrices
-        self.ws_chunk = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], min(4, G.shape[0]))
-                                        for G, _ in self.groups), dtype=torch.uint8, device="cuda")
+        # the end-to-end pass calls zopt_ns_orthogonalize on chunks of each shape: at least 4
+        # matrices and up to ~48 MB of input (small matrices: fewer calls, each bound by its
+        # chain of dependent products rather than by its size)
+        self.per_chunk = []
+        for G, _ in self.groups:
+            cap = min(G.shape[0], max(4, (48 << 20) // (G[0].numel() * G.element_size())))
+            pieces = -(-G.shape[0] // cap)
+            self.per_chunk.append(-(-G.shape[0] // pieces))  # even pieces
+        self.ws_chunk = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], per)
+                                        for (G, _), per in zip(self.groups, self.per_chunk)),
+                                    dtype=torch.uint8, device="cuda")
         self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
         fused = sum(1 for G, _ in self.groups if min(G.shape[1], G.shape[2]) < 1024)
         # the norm of every matrix in one launch (bf16 input), then one scaling launch if any
@@ -463,14 +471,15 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
         d2h += sum(X.numel() * 2 for _, X in ns.groups)
-        # chunks of up to 4 matrices, the square group last (its read-back is the shortest)
+        # chunks of ns.per_chunk matrices, the square group last (its read-back is the shortest)
         order = sorted(range(len(ns.groups)), key=lambda gi: ns.groups[gi][0].shape[1] == ns.groups[gi][0].shape[2])
         chunks = []
         for gi in order:
             G, X = ns.groups[gi]
             hG, hX = ns_host[gi]
-            for lo in range(0, G.shape[0], 4):
-                hi = min(G.shape[0], lo + 4)
+            per = ns.per_chunk[gi]
+            for lo in range(0, G.shape[0], per):
+                hi = min(G.shape[0], lo + per)
                 chunks.append((G[lo:hi], X[lo:hi], hG[lo:hi], hX[lo:hi]))
         ns_done = [ev() for _ in chunks]
         out_done = [ev() for _ in chunks]
