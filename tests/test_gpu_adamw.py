@@ -231,38 +231,43 @@ def test_full_size_zero2_shard_sampled(zopt):
     assert zopt.read_adam_state(state)["step"] == 2
 
 
-@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
-def test_rescale_step_bitwise_and_close_to_direct(zopt, gdtype):
+H_BETA1_ZERO = OA.Hyper(lr=1e-3, beta1=0.0, beta2=0.99, eps=1e-8, weight_decay=0.1)
+
+
+@pytest.mark.parametrize("gdtype,h", [(torch.bfloat16, H), (torch.float32, H), (torch.bfloat16, H_BETA1_ZERO)])
+def test_rescale_step_bitwise_and_close_to_direct(zopt, gdtype, h):
     """zopt_adamw_rescale_step (DeepSpeed PR #9021 adam_rescale_step): bit for bit the oracle's
     re-targeting; a rescale to the same scale changes nothing; the result is the step taken
-    directly on the new scale up to rounding (the page measures 7.5e-6 of the update)."""
+    directly on the new scale up to rounding (the page measures 7.5e-6 of the update). Also with
+    betas (0, 0.99), the case the page's rollback (a division by the betas) could not undo."""
     case = Case(zopt, SMALL, 4000, 3, 1, seed=21, gdtype=gdtype)
     for s in range(2):
-        case.step(s, H, max_norm=1e9)  # warm moments, coefficient 1
+        case.step(s, h, max_norm=1e9)  # warm moments, coefficient 1
     grads = workloads.flat_grads(SMALL, 21, 2, dtype=gdtype)
     g = case.shard([x.float().numpy() for x in grads])
     g_dev = torch.from_numpy(g).cuda().to(gdtype)
     before = [t.clone() for t in (case.p, case.m, case.v)]
-    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, clip_stats=None,
-                    adam_state=case.state)  # speculative step t = 3 on the unscaled gradient
+    kw = dict(lr=h.lr, beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay)
+    zopt.adamw_step(case.layout, case.table, case.p, case.m, case.v, g_dev, case.out, clip_stats=None,
+                    adam_state=case.state, **kw)  # speculative step t = 3 on the unscaled gradient
     spec = [t.clone() for t in (case.p, case.m, case.v)]
-    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, old_scale=1.0,
-                            new_scale=1.0, adam_state=case.state)
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, old_scale=1.0, new_scale=1.0,
+                            adam_state=case.state, **kw)
     torch.cuda.synchronize()
     for a, b in zip(spec, (case.p, case.m, case.v)):
         assert torch.equal(a, b)
-    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, lr=H.lr, old_scale=1.0,
-                            new_scale=0.37, adam_state=case.state)
+    zopt.adamw_rescale_step(case.layout, case.p, case.m, case.v, g_dev, case.out, old_scale=1.0, new_scale=0.37,
+                            adam_state=case.state, **kw)
     torch.cuda.synchronize()
     ref = [t.cpu().numpy() for t in spec]
-    OA.rescale_step_f32(*ref, g, 1.0, 0.37, H, 3)
+    OA.rescale_step_f32(*ref, g, 1.0, 0.37, h, 3)
     for r, t in zip(ref, (case.p, case.m, case.v)):
         assert np.array_equal(r.view(np.uint32), t.cpu().numpy().view(np.uint32))
     assert np.array_equal(case.out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(ref[0]))
     # against the step taken directly on the new scale
     direct = [t.cpu().numpy() for t in before]
     mask = OL.decay_mask_of_shard(case.decay, case.numel, case.bucket, case.world, case.rank)
-    OA.step_flat_f32(*direct, g, mask, np.float32(0.37), H, 3)
+    OA.step_flat_f32(*direct, g, mask, np.float32(0.37), h, 3)
     upd = np.max(np.abs(direct[0] - before[0].cpu().numpy()))
     # 1e-4 of the update, plus the two roundings of weights near 1 (the RMSNorm scales)
     assert np.all(np.abs(direct[0] - ref[0]) <= 1e-4 * upd + 2 * np.spacing(np.abs(direct[0])))
