@@ -541,6 +541,32 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ea_ms, en_ms = float(tt[0]), float(tt[1])
 
+    # ---- host cost of one Newton-Schulz call (argument checks, tensor-map encoding, launches),
+    # eager and as a replay of the same call captured in a CUDA graph. The calls' GPU work queues
+    # behind and is drained afterwards; only the host time is taken here.
+    host_ns = None
+    if ns is not None:
+        reps = 8
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            ns.run(stream)
+        eager_us = (time.perf_counter() - t0) / reps * 1e6
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            ns.run(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            graph.replay()
+        replay_us = (time.perf_counter() - t0) / reps * 1e6
+        torch.cuda.synchronize()
+        del graph
+        host_ns = {"eager_us_per_call": round(eager_us, 1), "graph_replay_us_per_call": round(replay_us, 1),
+                   "launches_per_call": ns.launches,
+                   "matrices_per_call": sum(G.shape[0] for G, _ in ns.groups)}
+
     pk = peaks()
     part_bytes = (ACC_BYTES + ADAMW_BYTES) * S
     line = {"metric": METRIC, "n_gpus": world_procs, "steps": K, "warmup": args.warmup,
@@ -573,7 +599,7 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     if ns is not None:
         tflops = ns.flops / (n_ms * 1e-3) / 1e12
         line["ns"] = {"value": round(tflops * world_procs, 2), "unit": "TFLOP/s", "ms_per_step": round(n_ms, 3),
-                      "algorithmic_flops_per_step": ns.flops}
+                      "algorithmic_flops_per_step": ns.flops, "host": host_ns}
         line["roofline"] = {"kernel": ns.kernel, "bound": "tensor",
                             "achieved": round(tflops, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                             "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": None,
