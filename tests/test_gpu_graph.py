@@ -87,3 +87,38 @@ def test_whole_step_replayed_from_a_cuda_graph(zopt):
     for k, (a, b) in enumerate(zip(eager.tensors(), graphed.tensors())):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), k
     assert zopt.take_device_error() == 0
+
+
+def test_replayed_accumulation_reads_the_pinned_buffer_anew(zopt):
+    """The accumulation of micro-step gradients held in pinned host memory, captured once: the
+    graph keeps the buffers' addresses, so each replay sums what the host wrote there since,
+    bit for bit what the eager calls give for the same contents."""
+    n = 1_000_003
+    gen = torch.Generator().manual_seed(7)
+    host = [torch.empty(n, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    acc_g, acc_e = torch.empty(n, device="cuda"), torch.empty(n, device="cuda")
+    ws_g, ws_e = zopt.new_norm_workspace(n), zopt.new_norm_workspace(n)
+    st_g, st_e = zopt.new_clip_stats(), zopt.new_clip_stats()
+
+    def step(acc, ws, st):
+        zopt.grad_accumulate(acc, host[0], first=True, last=False)
+        zopt.grad_accumulate(acc, host[1], first=False, last=True, max_norm=1.0, ws=ws, stats=st)
+
+    for h in host:
+        h.copy_(torch.randn(n, generator=gen).to(torch.bfloat16))
+    step(acc_e, ws_e, st_e)  # first use outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(acc_g, ws_g, st_g)
+    torch.cuda.synchronize()
+    for rnd in range(3):
+        for h in host:  # new contents, same addresses
+            h.copy_((torch.randn(n, generator=gen) * (rnd + 1)).to(torch.bfloat16))
+        g.replay()
+        step(acc_e, ws_e, st_e)
+        torch.cuda.synchronize()
+        assert torch.equal(acc_g.view(torch.int32), acc_e.view(torch.int32)), rnd
+        assert torch.equal(st_g, st_e), rnd
+        want = host[0].float() + host[1].float()
+        assert torch.equal(acc_g.cpu(), want), rnd

@@ -86,7 +86,8 @@ def test_one_step_white_box(zopt, rows, cols):
 
 SHAPES_E2E = [(256, 768), (256, 256), (256, 1536), (768, 256),        # tiny decoder
               (768, 2304), (768, 768), (768, 3072), (3072, 768),       # GPT-2-small body
-              (256, 1024), (1000, 1000), (129, 257), (1, 8), (8, 1), (5, 3)]
+              (256, 1024), (1000, 1000), (129, 257), (1, 8), (8, 1), (5, 3),
+              (1, 1)]                                                   # one element: sign(g) p^5(1)
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES_E2E)
