@@ -104,6 +104,24 @@ def test_small_sets_bitwise(zopt, world, rank, gdtype):
         case.compare()
 
 
+ALL_2D = [workloads.Param("a", (300, 77), True), workloads.Param("b", (129, 50), True)]
+ALL_1D = [workloads.Param("s0", (777,), False), workloads.Param("s1", (5,), False), workloads.Param("s2", (4096,), False)]
+
+
+@pytest.mark.parametrize("params,world,rank,null_table", [(ALL_2D, 3, 2, True), (ALL_2D, 1, 0, False),
+                                                          (ALL_1D, 3, 0, False), (ALL_1D, 8, 5, False)])
+def test_decay_mask_extremes_bitwise(zopt, params, world, rank, null_table):
+    """Every slot decayed (no no-decay runs: the run table may then be NULL) or none decayed
+    (every piece of the shard one run), several ranks; bit for bit the per-tensor oracle."""
+    case = Case(zopt, params, 1000, world, rank, seed=31, gdtype=torch.bfloat16)
+    if null_table:
+        assert case.layout.nodecay_runs().shape[0] == 0
+        case.table = None
+    for s in range(2):
+        case.step(s, H, max_norm=0.05)
+        case.compare()
+
+
 def test_c1_three_steps_bitwise(zopt):
     w = workloads.get("c1")
     case = Case(zopt, w.adamw, w.bucket, 1, 0, seed=w.seed, gdtype=torch.bfloat16)
