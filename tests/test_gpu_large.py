@@ -1,4 +1,5 @@
-"""A shard longer than 2^31 elements: the element-wise kernels index with 64-bit integers.
+"""A shard longer than 2^31 elements: the element-wise kernels (norm, AdamW, rescale,
+accumulation) index with 64-bit integers.
 
 n = 2^31 + 4099 elements (~35 GB of fp32 master, moments and bf16 gradient and weights on the
 device). The inputs repeat with a period of L = 4096 elements and every output element depends
@@ -79,6 +80,15 @@ def test_adamw_step_and_norm_past_2_to_the_31(zopt):
         assert_periodic(t, e.view(np.int32))
     assert_periodic(out, f32_to_bf16_bits(pe).view(np.int16))
     assert zopt.read_adam_state(state)["step"] == 1
+    # the same step re-targeted to half the coefficient, in one pass over the whole shard
+    coef = float(st["clip_coef"])
+    zopt.adamw_rescale_step(lay, p, m, v, g, out, lr=h.lr, old_scale=coef, new_scale=coef / 2, beta1=h.beta1,
+                            beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay, adam_state=state)
+    torch.cuda.synchronize()
+    OA.rescale_step_f32(pe, me, ve, g_np, coef, coef / 2, h, 1)
+    for t, e in ((p, pe), (m, me), (v, ve)):
+        assert_periodic(t, e.view(np.int32))
+    assert_periodic(out, f32_to_bf16_bits(pe).view(np.int16))
     del g, p, m, v, out
     torch.cuda.empty_cache()
 
