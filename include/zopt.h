@@ -255,8 +255,15 @@ ZOPT_API zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* m
  * Muon choice is 3.4445, -4.7750, 2.0315).
  * ====================================================================================== */
 
+/* Size limits of one Newton-Schulz (or Muon) matrix, under which every tile coordinate and
+ * count the kernels form fits in 32 bits and every element offset in 64. */
+#define ZOPT_NS_MAX_DIM (1LL << 30)    /* rows and cols */
+#define ZOPT_NS_MAX_ELEMS (1LL << 36)  /* rows * cols */
+#define ZOPT_NS_MAX_LD (1LL << 32)     /* leading dimensions (elements) */
+#define ZOPT_NS_MAX_SPAN (1LL << 56)   /* (batch - 1) * batch stride (elements) */
+
 /* Workspace bytes to process `group` rows x cols matrices together (0 for an unsupported
- * compute dtype or group < 1). A call processes its batch in groups of as many matrices as its
+ * compute dtype, group < 1, or a shape beyond the limits above). A call processes its batch in groups of as many matrices as its
  * workspace holds: every product of a step is one launch over the whole group, so a larger
  * group means fewer launches and better use of the SMs. */
 ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zopt_dtype compute_dtype);
@@ -267,8 +274,9 @@ ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zop
  *     need agreement with fp64 to about 1e-4);
  *   steps >= 1; abc: 3 host floats; eps >= 0 (1e-7 is the usual choice);
  *   d_ws: at least zopt_ns_workspace(rows, cols, 1, compute_dtype) bytes, 16-byte aligned.
- * G and X must not overlap. Errors: EINVAL for NULL pointers, empty shapes, dimensions
- * >= 2^31, leading dimensions < cols, overlapping batch strides, steps < 1, non-finite
+ * G and X must not overlap. Errors: EINVAL for NULL pointers, empty shapes, shapes, leading
+ * dimensions or batch spans beyond the ZOPT_NS_MAX_* limits, leading dimensions < cols,
+ * overlapping batch strides, steps < 1, non-finite
  * coefficients, a short workspace; EUNSUPPORTED for other dtypes; ETIMEOUT when a kernel of
  * an earlier call gave up on a bounded wait (its results are not valid). */
 ZOPT_API zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype io_dtype, int64_t rows, int64_t cols,
@@ -367,14 +375,15 @@ typedef struct zopt_muon_stats {
 } zopt_muon_stats; /* 16 bytes per matrix, device resident */
 
 /* Workspace bytes to step `group` rows x cols matrices together (the Newton-Schulz workspace
- * plus two fp32 matrices per group member). A call steps its batch in groups of as many
- * matrices as the workspace holds. */
+ * plus two fp32 matrices per group member; 0 for a shape beyond the ZOPT_NS_MAX_* limits). A
+ * call steps its batch in groups of as many matrices as the workspace holds. */
 ZOPT_API size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group);
 /* One Muon step of `batch` rows x cols matrices stored back to back (matrix b at offset
  * b*rows*cols of master, momentum, grad and out_bf16). master, momentum: fp32; grad: fp32 or
  * bf16; out_bf16: may be NULL; d_stats: `batch` structs. Errors: EINVAL for NULL or
  * misaligned pointers (16 bytes; a batch needs rows*cols to be a multiple of 4), an empty
- * shape, out-of-range hyper-parameters (lr < 0, momentum outside [0, 1), steps < 1, guard <=
+ * shape or one beyond the ZOPT_NS_MAX_* limits, a batch of more than 2^46 elements,
+ * out-of-range hyper-parameters (lr < 0, momentum outside [0, 1), steps < 1, guard <=
  * 0), a short workspace; EUNSUPPORTED for another gradient dtype; and the errors of
  * zopt_ns_orthogonalize. */
 ZOPT_API zopt_status zopt_muon_step(float* master, float* momentum, const void* grad, zopt_dtype grad_dtype,

@@ -166,3 +166,39 @@ def test_muon_step_many_validates_before_launch():
     assert b"misaligned" in L.zopt_last_error()
     bad = Z._muon_hparams(1e-3, 1.5, 0.1, True, True, 5, Z.DEFAULT_ABC, 1e-7, 1000.0)
     assert L.zopt_muon_step_many(arr, 1, ctypes.byref(bad), p, big, None) == 1
+
+
+def test_size_limits_validate_before_launch():
+    """Shapes beyond ZOPT_NS_MAX_DIM (2^30), ZOPT_NS_MAX_ELEMS (2^36 elements), ZOPT_NS_MAX_LD
+    (2^32) or ZOPT_NS_MAX_SPAN (2^56 elements per batch), and a Muon batch above 2^46 elements,
+    are refused before any launch: the kernels keep tile coordinates in 32 bits."""
+    L = Z.lib()
+    assert Z.ns_workspace(1, 1 << 31) == 0
+    assert Z.ns_workspace((1 << 30) + 1, 8) == 0
+    assert Z.ns_workspace(1 << 30, 64) > 0          # 2^36 elements: at the limit
+    assert Z.ns_workspace(1 << 30, 65) == 0         # one column more
+    assert Z.ns_workspace_many([(1, 1 << 31, 1)]) == 0
+    assert L.zopt_muon_workspace(1, 1 << 31, 1) == 0
+    coef = (ctypes.c_float * 3)(*Z.DEFAULT_ABC)
+    ws, big = ctypes.c_void_p(1 << 20), 1 << 40
+    G, X = ctypes.c_void_p(1 << 16), ctypes.c_void_p(1 << 18)
+    wide = (Z._NsJob * 1)(Z._NsJob(G, X, 1, 1 << 31, 1 << 31, 1 << 31, 0, 0, 1, Z.BF16))
+    assert L.zopt_ns_orthogonalize_many(wide, 1, 5, coef, 1e-7, ws, big, None) == 1
+    assert b"2^30" in L.zopt_last_error()
+    assert L.zopt_ns_orthogonalize(G, X, Z.BF16, 1, 1 << 31, 1 << 31, 1 << 31, 0, 0, 1, Z.BF16, 5, coef, 1e-7, ws,
+                                   big, None) == 1
+    assert b"2^30" in L.zopt_last_error()
+    ld = (Z._NsJob * 1)(Z._NsJob(G, X, 64, 128, 1 << 33, 128, 0, 0, 1, Z.BF16))
+    assert L.zopt_ns_orthogonalize_many(ld, 1, 5, coef, 1e-7, ws, big, None) == 1
+    assert b"leading dimension above" in L.zopt_last_error()
+    span = (Z._NsJob * 1)(Z._NsJob(G, X, 64, 128, 128, 128, 1 << 56, 64 * 128, 3, Z.BF16))
+    assert L.zopt_ns_orthogonalize_many(span, 1, 5, coef, 1e-7, ws, big, None) == 1
+    assert b"spans" in L.zopt_last_error()
+    hp = Z._muon_hparams(1e-3, 0.95, 0.1, True, True, 5, Z.DEFAULT_ABC, 1e-7, 1000.0)
+    p = ctypes.c_void_p(1 << 20)
+    huge = (Z._MuonJob * 1)(Z._MuonJob(p, p, p, None, ctypes.c_void_p(1 << 16), 1 << 20, 1 << 20, 1, Z.BF16))
+    assert L.zopt_muon_step_many(huge, 1, ctypes.byref(hp), p, big, None) == 1
+    assert b"2^36" in L.zopt_last_error()
+    assert L.zopt_muon_step(p, p, p, Z.BF16, None, 1 << 15, 1 << 15, 1 << 17, ctypes.byref(hp),
+                            ctypes.c_void_p(1 << 16), p, big, None) == 1
+    assert b"2^46" in L.zopt_last_error()

@@ -30,6 +30,7 @@ constexpr int kThreads = 256;
 constexpr int kMaxBlocksPerMat = 512;
 constexpr long long kChunk = 32768;  // elements per block of the element-wise kernels
 constexpr int kMaxItems = 8;         // jobs per element-wise launch
+constexpr long long kMaxCallElems = 1LL << 46;  // elements of one shape's batch (2^31 blocks of kChunk)
 // per matrix: one fp64 partial sum of squares and one max |U| bit pattern per block
 constexpr size_t kRedBytes = (sizeof(double) + sizeof(unsigned)) * kMaxBlocksPerMat;
 
@@ -301,6 +302,10 @@ zopt_status check_job(const char* fn, const Job& j) {
   if (j.master == nullptr || j.momentum == nullptr || j.grad == nullptr || j.stats == nullptr)
     return fail(ZOPT_EINVAL, f + ": NULL pointer");
   if (j.rows < 1 || j.cols < 1 || j.batch < 1) return fail(ZOPT_EINVAL, f + ": empty matrix or batch");
+  if (j.rows > ZOPT_NS_MAX_DIM || j.cols > ZOPT_NS_MAX_DIM || j.rows * j.cols > ZOPT_NS_MAX_ELEMS)
+    return fail(ZOPT_EINVAL, f + ": a dimension above 2^30 or a matrix above 2^36 elements");
+  if (j.batch > kMaxCallElems / (j.rows * j.cols))  // the element-wise grids: one block per kChunk elements
+    return fail(ZOPT_EINVAL, f + ": the batch holds more than 2^46 elements");
   if (!aligned16(j.master) || !aligned16(j.momentum) || !aligned16(j.grad) ||
       (j.out != nullptr && (reinterpret_cast<uintptr_t>(j.out) & 1u) != 0) ||
       (reinterpret_cast<uintptr_t>(j.stats) & 3u) != 0)
@@ -425,6 +430,7 @@ zopt_ns_job ns_job_of(const Job& j, const float* U_in, float* U_out) {
 
 extern "C" size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group) {
   if (rows < 1 || cols < 1 || group < 1) return 0;
+  if (rows > ZOPT_NS_MAX_DIM || cols > ZOPT_NS_MAX_DIM || rows * cols > ZOPT_NS_MAX_ELEMS) return 0;
   return zopt::muon_plan(rows, cols, group).total;
 }
 
@@ -484,6 +490,7 @@ extern "C" size_t zopt_muon_workspace_many(const zopt_muon_job* jobs, int32_t n_
   for (int32_t k = 0; k < n_jobs; ++k) {
     const zopt_muon_job& b = jobs[k];
     if (b.rows < 1 || b.cols < 1 || b.batch < 1 || b.batch > 65535) return 0;
+    if (b.rows > ZOPT_NS_MAX_DIM || b.cols > ZOPT_NS_MAX_DIM || b.rows * b.cols > ZOPT_NS_MAX_ELEMS) return 0;
     total += static_cast<size_t>(round_up(static_cast<long long>(muon_plan(b.rows, b.cols, b.batch).off_ns), 1024));
     ns[static_cast<size_t>(k)] = ns_job_of(job_of(b), nullptr, nullptr);
   }

@@ -375,16 +375,24 @@ zopt_status take_error_word(const char* fn, int** dev) {
   return ok();
 }
 
+// Whether a rows x cols matrix lies within the ZOPT_NS_MAX_DIM / ZOPT_NS_MAX_ELEMS limits.
+bool shape_ok(long long rows, long long cols) {
+  return rows <= ZOPT_NS_MAX_DIM && cols <= ZOPT_NS_MAX_DIM && rows * cols <= ZOPT_NS_MAX_ELEMS;
+}
+
 // The checks shared by both entry points for one shape's arguments.
 zopt_status check_job(const char* fn, const void* G, const void* X, zopt_dtype io, long long rows, long long cols,
                       long long ld_g, long long ld_x, long long bs_g, long long bs_x, long long batch) {
   const std::string f(fn);
   if (G == nullptr || X == nullptr) return fail(ZOPT_EINVAL, f + ": NULL pointer");
   if (rows < 1 || cols < 1 || batch < 1) return fail(ZOPT_EINVAL, f + ": empty matrix or batch");
-  if (rows > (1LL << 31) || cols > (1LL << 31)) return fail(ZOPT_EINVAL, f + ": dimension >= 2^31");
+  if (!shape_ok(rows, cols)) return fail(ZOPT_EINVAL, f + ": a dimension above 2^30 or a matrix above 2^36 elements");
   if (ld_g < cols || ld_x < cols) return fail(ZOPT_EINVAL, f + ": leading dimension < cols");
+  if (ld_g > ZOPT_NS_MAX_LD || ld_x > ZOPT_NS_MAX_LD) return fail(ZOPT_EINVAL, f + ": a leading dimension above 2^32");
   if (batch > 1 && (bs_g < rows * ld_g || bs_x < rows * ld_x))
     return fail(ZOPT_EINVAL, f + ": batch strides overlap the matrices");
+  if (batch > 1 && (bs_g > ZOPT_NS_MAX_SPAN / (batch - 1) || bs_x > ZOPT_NS_MAX_SPAN / (batch - 1)))
+    return fail(ZOPT_EINVAL, f + ": the batch spans more than 2^56 elements");
   if (io != ZOPT_F32 && io != ZOPT_BF16) return fail(ZOPT_EUNSUPPORTED, f + ": input/output dtype must be fp32 or bf16");
   return ok();
 }
@@ -394,6 +402,7 @@ zopt_status check_job(const char* fn, const void* G, const void* X, zopt_dtype i
 
 extern "C" size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zopt_dtype compute_dtype) {
   if (rows < 1 || cols < 1 || group < 1 || (compute_dtype != ZOPT_BF16 && compute_dtype != ZOPT_F32)) return 0;
+  if (!zopt::ns::shape_ok(rows, cols)) return 0;
   return zopt::ns::plan(rows, cols, compute_dtype == ZOPT_F32 ? 4 : 2, group).total;
 }
 
@@ -469,7 +478,7 @@ extern "C" size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs
   size_t total = 0;
   for (int32_t j = 0; j < n_jobs; ++j) {
     const zopt_ns_job& b = jobs[j];
-    if (b.rows < 1 || b.cols < 1 || b.batch < 1 || b.batch > 65535) return 0;
+    if (b.rows < 1 || b.cols < 1 || b.batch < 1 || b.batch > 65535 || !zopt::ns::shape_ok(b.rows, b.cols)) return 0;
     total += static_cast<size_t>(zopt::ns::round_up(
         static_cast<long long>(zopt::ns::plan(b.rows, b.cols, 2, b.batch).total), 1024));
   }
