@@ -14,6 +14,8 @@ import numpy as np
 import pytest
 import torch
 
+import workloads
+
 from oracle.ns import DEFAULT_ABC, newton_schulz
 
 pytestmark = pytest.mark.gpu
@@ -393,6 +395,34 @@ def test_many_jobs_beyond_one_preparation_list(zopt):
         assert torch.equal(one, X), (r, c, b)
     ref = newton_schulz(pairs[17][0][1].double().cpu().numpy(), steps=2)
     assert rel(pairs[17][1][1].cpu(), torch.from_numpy(ref)) <= 2e-2
+
+
+def test_gpt2_small_body_in_one_call(zopt):
+    """The GPT-2-small body's 48 Muon matrices (12 each of 768x2304, 768x768, 768x3072,
+    3072x768; 1e-3-scaled Gaussian gradients) in one zopt_ns_orthogonalize_many call, the launch
+    configuration the small-matrix benchmark times: every shape bitwise its own single call, and
+    the first and last matrix of every shape within 2e-2 of the fp64 oracle."""
+    w = workloads.get("c2")
+    shapes = sorted({p.shape for p in w.muon})
+    pairs = []
+    for k, (r, c) in enumerate(shapes):
+        count = sum(1 for p in w.muon if p.shape == (r, c))
+        G = torch.stack([workloads.ns_input(r, c, w.seed, 100 * k + i, dtype=torch.float32)
+                         for i in range(count)]) * 1e-3
+        G = G.to(torch.bfloat16).cuda()
+        pairs.append((G, torch.empty_like(G)))
+    assert sum(G.shape[0] for G, _ in pairs) == 48
+    zopt.ns_orthogonalize_many(pairs, zopt.new_ns_workspace_many([(G.shape[1], G.shape[2], G.shape[0])
+                                                                  for G, _ in pairs]), steps=5)
+    torch.cuda.synchronize()
+    for G, X in pairs:
+        one = torch.empty_like(X)
+        zopt.ns_orthogonalize(G, one, zopt.new_ns_workspace(G.shape[1], G.shape[2], G.shape[0]), steps=5)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X), tuple(G.shape)
+        for i in (0, G.shape[0] - 1):
+            ref = newton_schulz(G[i].double().cpu().numpy(), steps=5)
+            assert rel(X[i].cpu(), torch.from_numpy(ref)) <= 2e-2, (tuple(G.shape), i)
 
 
 def test_many_pair_jobs_batched(zopt):
