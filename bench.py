@@ -125,43 +125,86 @@ def smi_id(local_rank: int) -> str:
     return str(local_rank)
 
 
-def cpu_oracle_run(seconds: float = 10.0) -> dict:
-    """The oracle as it stands (numpy, one core) on a bounded sample of the same workload:
-    4 bf16 micro-steps summed in fp32, norm/clip, AdamW and the bf16 round-out over
-    CPU_SAMPLE shard elements, repeated for ~`seconds`."""
-    import numpy as np
-    import torch
+class OracleAdamwSample:
+    """The oracle as it stands (numpy, one core) on a bounded sample of the step's workload: 4
+    bf16 micro-steps summed in fp32, norm/clip, AdamW and the bf16 round-out over CPU_SAMPLE
+    shard elements of the 2e9-parameter set's shard."""
 
-    import workloads
-    from oracle import adamw as OA
-    from oracle import clip as OC
-    from oracle.accum import accumulate
-    from oracle.bf16 import f32_to_bf16_bits
+    def __init__(self):
+        import numpy as np
+        import torch
 
-    w = workloads.get("c4")
-    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    n = CPU_SAMPLE
-    p = workloads.shard_vector(n, 0.02, w.seed, 1).numpy()
-    m = np.zeros(n, np.float32)
-    v = np.zeros(n, np.float32)
-    mask = np.ones(n, np.uint8)
-    mask[::1000] = 0
-    micro = [workloads.shard_vector(n, 1e-3, w.seed, 2 + k, dtype=torch.bfloat16).float().numpy()
-             for k in range(MICRO_STEPS)]
-    steps, t0 = 0, time.perf_counter()
+        import workloads
+        from oracle import adamw as OA
+
+        w = workloads.get("c4")
+        self.w, self.h = w, OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        self.n = n = CPU_SAMPLE
+        self.p = workloads.shard_vector(n, 0.02, w.seed, 1).numpy()
+        self.m = np.zeros(n, np.float32)
+        self.v = np.zeros(n, np.float32)
+        self.mask = np.ones(n, np.uint8)
+        self.mask[::1000] = 0
+        self.micro = [workloads.shard_vector(n, 1e-3, w.seed, 2 + k, dtype=torch.bfloat16).float().numpy()
+                      for k in range(MICRO_STEPS)]
+        self.t = 0
+        self.bytes = (ACC_BYTES + ADAMW_BYTES) * n
+
+    def step(self):
+        from oracle import adamw as OA
+        from oracle import clip as OC
+        from oracle.accum import accumulate
+        from oracle.bf16 import f32_to_bf16_bits
+
+        g = accumulate(self.micro)
+        st = OC.clip_stats(g, self.w.max_norm)
+        self.t += 1
+        OA.step_flat_f32(self.p, self.m, self.v, g, self.mask, st["clip_coef"], self.h, self.t)
+        f32_to_bf16_bits(self.p)
+
+    def what(self, steps: int, seconds: float) -> str:
+        return (f"{steps} steps of 4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out over "
+                f"{self.n:,} shard elements (numpy fp32 exact-order oracle, {seconds:.1f} s)")
+
+
+class OracleNsSample:
+    """The fp64 Newton-Schulz oracle on a 256 x 1024 block shaped like the stress set's
+    (numpy's BLAS uses the host's threads)."""
+
+    def __init__(self):
+        import numpy as np
+        import torch
+
+        import workloads
+
+        self.g = workloads.ns_input(256, 1024, 5, 0, dtype=torch.float32).numpy().astype(np.float64)
+        self.flops = ns_flops(256, 1024, 5)
+
+    def step(self):
+        from oracle.ns import newton_schulz
+
+        newton_schulz(self.g, steps=5)
+
+    def what(self, calls: int, seconds: float) -> str:
+        return f"{calls} fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set ({seconds:.1f} s)"
+
+
+def _timed_for(sample, seconds: float):
+    n, t0 = 0, time.perf_counter()
     while True:
-        g = accumulate(micro)
-        st = OC.clip_stats(g, w.max_norm)
-        OA.step_flat_f32(p, m, v, g, mask, st["clip_coef"], h, steps + 1)
-        f32_to_bf16_bits(p)
-        steps += 1
+        sample.step()
+        n += 1
         el = time.perf_counter() - t0
-        if el >= seconds and steps >= 2:
-            break
-    gbs = (ACC_BYTES + ADAMW_BYTES) * n * steps / el / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} steps of 4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out "
-                      f"over {n:,} shard elements (numpy fp32 exact-order oracle, {el:.1f} s)"}
+        if el >= seconds and n >= 2:
+            return n, el
+
+
+def cpu_oracle_run(seconds: float = 10.0) -> dict:
+    """The AdamW-part oracle sample repeated for ~`seconds` (the GPU arm's CPU baseline)."""
+    a = OracleAdamwSample()
+    steps, el = _timed_for(a, seconds)
+    return {"value": round(a.bytes * steps / el / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": a.what(steps, el)}
 
 
 def adamw_traffic(S: int):
@@ -183,39 +226,50 @@ def ns_flops(rows: int, cols: int, steps: int) -> float:
 
 
 def cpu_oracle_ns(seconds: float = 6.0) -> dict:
-    """The fp64 Newton-Schulz oracle on a 256 x 1024 block shaped like the stress set's,
-    repeated for ~`seconds`; numpy's BLAS uses the host's threads."""
-    import numpy as np
-    import torch
-
-    import workloads
-    from oracle.ns import newton_schulz
-
-    g = workloads.ns_input(256, 1024, 5, 0, dtype=torch.float32).numpy().astype(np.float64)
-    calls, t0 = 0, time.perf_counter()
-    while True:
-        newton_schulz(g, steps=5)
-        calls += 1
-        el = time.perf_counter() - t0
-        if el >= seconds and calls >= 2:
-            break
-    flops = ns_flops(256, 1024, 5) * calls
-    return {"value": round(flops / el / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{calls} fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set ({el:.1f} s)"}
+    """The Newton-Schulz oracle sample repeated for ~`seconds` (the GPU arm's CPU baseline)."""
+    x = OracleNsSample()
+    calls, el = _timed_for(x, seconds)
+    return {"value": round(x.flops * calls / el / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": x.what(calls, el)}
 
 
 def run_reference(args, rank: int) -> None:
+    """The oracle as it stands, on the host's cores: `--warmup` untimed then `--steps` timed steps,
+    each one pass of the AdamW-part sample and one Newton-Schulz sample call; rank 0 only."""
     if rank != 0:
         return
-    cpu = cpu_oracle_run(seconds=max(5.0, min(20.0, 2.0 * args.steps)))
-    ns = cpu_oracle_ns(seconds=5.0)
-    line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+    a, x = OracleAdamwSample(), OracleNsSample()
+    for _ in range(args.warmup):
+        a.step()
+        x.step()
+    ta = tn = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        a.step()
+        t1 = time.perf_counter()
+        x.step()
+        t2 = time.perf_counter()
+        ta += t1 - t0
+        tn += t2 - t1
+    K = args.steps
+    value = round(a.bytes * K / ta / 1e9, 3)
+    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{K} timed steps after {args.warmup} warm-up steps; each step: the AdamW-part oracle "
+                     f"(4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out) over {a.n:,} shard "
+                     f"elements ({ta / K * 1e3:.1f} ms, numpy, one core) and one fp64 Newton-Schulz call (5 steps) "
+                     f"on a 256x1024 block of the stress set ({tn / K * 1e3:.1f} ms, numpy's threaded BLAS)"}
+    ns = {"value": round(x.flops * K / tn / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": f"{K} timed fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set, one per "
+                    f"step ({tn:.2f} s)"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round((ta + tn) / K * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
-            "ns": {"value": ns["value"], "unit": "TFLOP/s"},
+            "adamw_part": {"ms": round(ta / K * 1e3, 3), "bytes_per_element": ACC_BYTES + ADAMW_BYTES,
+                           "elements": a.n},
+            "ns": {"value": ns["value"], "unit": "TFLOP/s", "ms_per_step": round(tn / K * 1e3, 3)},
             "cpu_baseline": cpu, "cpu_baseline_ns": ns,
-            "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 

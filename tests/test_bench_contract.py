@@ -25,6 +25,7 @@ def test_reference_arm_line():
                 "vs_baseline", "dtype", "data", "config"):
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["ms_per_step"] > 0 and d["ns"]["value"] > 0  # K timed steps of the sample, averaged
     assert isinstance(d["config"]["workload"], str) and d["value"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
