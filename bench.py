@@ -525,16 +525,18 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
         d2h += sum(X.numel() * 2 for _, X in ns.groups)
-        # chunks of ns.per_chunk matrices, the square group last (its read-back is the shortest)
-        order = sorted(range(len(ns.groups)), key=lambda gi: ns.groups[gi][0].shape[1] == ns.groups[gi][0].shape[2])
+        # chunks of ns.per_chunk matrices, ordered so that the smallest chunks come first and last:
+        # only the first chunk's upload and the last chunk's read-back are not overlapped
         chunks = []
-        for gi in order:
-            G, X = ns.groups[gi]
+        for gi, (G, X) in enumerate(ns.groups):
             hG, hX = ns_host[gi]
             per = ns.per_chunk[gi]
             for lo in range(0, G.shape[0], per):
                 hi = min(G.shape[0], lo + per)
                 chunks.append((G[lo:hi], X[lo:hi], hG[lo:hi], hX[lo:hi]))
+        chunks.sort(key=lambda c: c[0].numel())
+        if len(chunks) > 1:
+            chunks = [chunks[0]] + chunks[2:][::-1] + [chunks[1]]
         ns_done = [ev() for _ in chunks]
         out_done = [ev() for _ in chunks]
         for e in ns_done + out_done:
