@@ -302,13 +302,13 @@ class NsPart:
         self.ws = Z.new_ns_workspace_many([(G.shape[1], G.shape[2], G.shape[0]) for G, _ in self.groups])
         # the end-to-end pass calls zopt_ns_orthogonalize on chunks of each shape: at least 4
         # matrices and up to ~48 MB of input (small matrices: fewer calls, each bound by its
-        # chain of dependent products rather than by its size)
+        # chain of dependent products rather than by its size), or two such chunks merged
         self.per_chunk = []
         for G, _ in self.groups:
             cap = min(G.shape[0], max(4, (48 << 20) // (G[0].numel() * G.element_size())))
             pieces = -(-G.shape[0] // cap)
             self.per_chunk.append(-(-G.shape[0] // pieces))  # even pieces
-        self.ws_chunk = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], per)
+        self.ws_chunk = torch.empty(max(Z.ns_workspace(G.shape[1], G.shape[2], min(G.shape[0], 2 * per))
                                         for (G, _), per in zip(self.groups, self.per_chunk)),
                                     dtype=torch.uint8, device="cuda")
         self.flops = sum(ns_flops(G.shape[1], G.shape[2], steps) * G.shape[0] for G, _ in self.groups)
@@ -525,18 +525,25 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
         d2h += sum(X.numel() * 2 for _, X in ns.groups)
-        # chunks of ns.per_chunk matrices, ordered so that the smallest chunks come first and last:
-        # only the first chunk's upload and the last chunk's read-back are not overlapped
-        chunks = []
-        for gi, (G, X) in enumerate(ns.groups):
-            hG, hX = ns_host[gi]
-            per = ns.per_chunk[gi]
-            for lo in range(0, G.shape[0], per):
-                hi = min(G.shape[0], lo + per)
-                chunks.append((G[lo:hi], X[lo:hi], hG[lo:hi], hX[lo:hi]))
-        chunks.sort(key=lambda c: c[0].numel())
-        if len(chunks) > 1:
-            chunks = [chunks[0]] + chunks[2:][::-1] + [chunks[1]]
+        # chunks of ns.per_chunk matrices: the two smallest go first and last (only their upload
+        # and read-back are not overlapped); in between, neighbouring chunks of one shape are
+        # merged into calls of up to twice as many matrices (their transfers hide behind compute,
+        # and a larger call fills the GPU better), largest first
+        spans = [(gi, lo, min(G.shape[0], lo + ns.per_chunk[gi])) for gi, (G, _) in enumerate(ns.groups)
+                 for lo in range(0, G.shape[0], ns.per_chunk[gi])]
+        size = lambda sp: (sp[2] - sp[1]) * ns.groups[sp[0]][0][0].numel()  # noqa: E731
+        spans.sort(key=size)
+        if len(spans) > 1:
+            mid = []
+            for sp in sorted(spans[2:]):
+                gi = sp[0]
+                if mid and mid[-1][0] == gi and mid[-1][2] == sp[1] and sp[2] - mid[-1][1] <= 2 * ns.per_chunk[gi]:
+                    mid[-1] = (gi, mid[-1][1], sp[2])
+                else:
+                    mid.append(sp)
+            spans = [spans[0]] + sorted(mid, key=size, reverse=True) + [spans[1]]
+        chunks = [(ns.groups[gi][0][lo:hi], ns.groups[gi][1][lo:hi], ns_host[gi][0][lo:hi], ns_host[gi][1][lo:hi])
+                  for gi, lo, hi in spans]
         ns_done = [ev() for _ in chunks]
         out_done = [ev() for _ in chunks]
         for e in ns_done + out_done:
