@@ -83,6 +83,12 @@ ZOPT_API void zopt_layout_free(zopt_layout* layout);
 
 ZOPT_API int64_t zopt_layout_numel(const zopt_layout* layout);       /* N, the unpadded flat length */
 ZOPT_API int64_t zopt_layout_shard_len(const zopt_layout* layout);   /* S = sum over buckets of L/world */
+/* Device bytes of this rank's optimizer state under the layout: the fp32 master, the two fp32
+ * AdamW moments and the shard gradient, per shard slot 12 B + 4 (fp32 gradient) or + 2 (bf16).
+ * With an fp32 gradient this is the per-rank 16/W share of deg/zero.py's memory plan
+ * (sharded_static_bytes: fp32 master + moments + gradient per shard), counted exactly, with the
+ * padding of every bucket's pieces. -1 for a NULL layout or another dtype. */
+ZOPT_API int64_t zopt_layout_state_bytes(const zopt_layout* layout, zopt_dtype grad_dtype);
 ZOPT_API int32_t zopt_layout_world(const zopt_layout* layout);
 ZOPT_API int32_t zopt_layout_rank(const zopt_layout* layout);
 ZOPT_API int32_t zopt_layout_num_buckets(const zopt_layout* layout);

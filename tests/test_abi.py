@@ -202,3 +202,22 @@ def test_size_limits_validate_before_launch():
     assert L.zopt_muon_step(p, p, p, Z.BF16, None, 1 << 15, 1 << 15, 1 << 17, ctypes.byref(hp),
                             ctypes.c_void_p(1 << 16), p, big, None) == 1
     assert b"2^46" in L.zopt_last_error()
+
+
+def test_state_bytes_is_the_sharded_memory_plan():
+    """zopt_layout_state_bytes against deg/zero.py's memory plan (sharded_static_bytes: fp32
+    master + AdamW moments + fp32 gradient per shard, 16 B per parameter over W ranks): each rank
+    holds 16 B per shard slot (14 with a bf16 gradient); over the ranks that is 16 B per padded
+    bucket slot, between 16 N and 16 (N + buckets (W - 1))."""
+    c4 = workloads.get("c4")
+    numel = [p.numel for p in c4.adamw]
+    lay = Z.ShardLayout(numel, None, c4.bucket, 8, 0)
+    assert lay.state_bytes() == 16 * 250_000_000 and lay.state_bytes(Z.BF16) == 14 * 250_000_000
+    for numel, bucket, world in [([100, 3, 77], 64, 3), ([5000, 1, 1234], 1000, 8), (numel, c4.bucket, 8)]:
+        total = sum(Z.ShardLayout(numel, None, bucket, world, r).state_bytes() for r in range(world))
+        padded = sum(L for _, _, L in OL.buckets(numel, bucket, world))
+        assert total == 16 * padded
+        N, nb = sum(numel), len(OL.buckets(numel, bucket, world))
+        assert 16 * N <= total <= 16 * (N + nb * (world - 1))
+    assert Z.lib().zopt_layout_state_bytes(None, 0) == -1
+    assert Z.lib().zopt_layout_state_bytes(lay.handle, 7) == -1

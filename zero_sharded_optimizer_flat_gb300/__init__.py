@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         "zopt_layout_free": (None, [vp]),
         "zopt_layout_numel": (i64, [vp]),
         "zopt_layout_shard_len": (i64, [vp]),
+        "zopt_layout_state_bytes": (i64, [vp, ctypes.c_int]),
         "zopt_layout_world": (i32, [vp]),
         "zopt_layout_rank": (i32, [vp]),
         "zopt_layout_num_buckets": (i32, [vp]),
@@ -175,6 +176,10 @@ class ShardLayout:
     @property
     def shard_len(self) -> int:
         return lib().zopt_layout_shard_len(self._h)
+
+    def state_bytes(self, grad_dtype=F32) -> int:
+        """``zopt_layout_state_bytes``: device bytes of this rank's master, moments and shard gradient."""
+        return int(lib().zopt_layout_state_bytes(self._h, int(grad_dtype)))
 
     @property
     def world(self) -> int:

@@ -97,6 +97,11 @@ extern "C" void zopt_layout_free(zopt_layout* layout) { delete layout; }
 
 extern "C" int64_t zopt_layout_numel(const zopt_layout* L) { return L ? L->numel : -1; }
 extern "C" int64_t zopt_layout_shard_len(const zopt_layout* L) { return L ? L->shard_len : -1; }
+
+extern "C" int64_t zopt_layout_state_bytes(const zopt_layout* L, zopt_dtype grad_dtype) {
+  if (L == nullptr || (grad_dtype != ZOPT_F32 && grad_dtype != ZOPT_BF16)) return -1;
+  return L->shard_len * (12 + (grad_dtype == ZOPT_F32 ? 4 : 2));
+}
 extern "C" int32_t zopt_layout_world(const zopt_layout* L) { return L ? L->world : -1; }
 extern "C" int32_t zopt_layout_rank(const zopt_layout* L) { return L ? L->rank : -1; }
 extern "C" int32_t zopt_layout_num_buckets(const zopt_layout* L) {
