@@ -43,6 +43,8 @@ ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
 ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
+# two parts to a pass: the first pair reads 2 x 2 and writes 4; each later pair also reads the sum
+PAIRED_ACC_BYTES = 8 + 12 * (MICRO_STEPS // 2 - 1)
 CPU_SAMPLE = 4_000_000
 
 
@@ -470,6 +472,25 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
             b_ev.record(stream)
         torch.cuda.synchronize()
         nr_ms = mean(ev_r)
+    # the same step with the micro-steps summed two to a pass (zopt_grad_accumulate2: bit for bit
+    # the four single passes, 20 instead of 36 B/element for the sum), timed apart
+    pa_ms = 0.0
+    if "adamw" in parts:
+        def paired_part():
+            for k in range(0, MICRO_STEPS, 2):
+                Z.grad_accumulate2(g, micro[k], micro[k + 1], first=k == 0, last=k + 2 == MICRO_STEPS,
+                                   max_norm=w.max_norm, ws=ws, stats=clip, stream=stream)
+            Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
+        for _ in range(3):
+            paired_part()
+        torch.cuda.synchronize()
+        ev_p = [(mk(), mk()) for _ in range(max(K, 3))]
+        for a_ev, b_ev in ev_p:
+            a_ev.record(stream)
+            paired_part()
+            b_ev.record(stream)
+        torch.cuda.synchronize()
+        pa_ms = mean(ev_p)
     # zopt_adamw_rescale_step (re-target the step just taken to another gradient scale) over the
     # shard: 30 B/element like the step itself, timed apart
     rs_ms = 0.0
@@ -646,6 +667,12 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         line["unit"] = "GB/s"
         line["adamw_part"] = {"ms": round(a_ms, 4), "bytes_per_element": ACC_BYTES + ADAMW_BYTES,
                               "accumulate_ms": round(a_ms - k_ms, 4), "adamw_kernel_ms": round(k_ms, 4)}
+        paired_bytes = PAIRED_ACC_BYTES + ADAMW_BYTES
+        line["adamw_part_paired"] = {
+            "what": "the same step with the micro-steps summed two to a pass (zopt_grad_accumulate2), timed apart",
+            "ms": round(pa_ms, 4), "bytes_per_element": paired_bytes,
+            "achieved": round(paired_bytes * S / (pa_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "frac": round(paired_bytes * S / (pa_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
         norm_gbs = 4 * S / (nr_ms * 1e-3) / 1e9
         line["norm_clip"] = {"kernel": "norm_kernel (zopt_grad_norm_clip on the fp32 shard gradient, timed "
                                        "apart from the steps)", "ms": round(nr_ms, 4), "bytes_per_element": 4,

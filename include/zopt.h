@@ -178,6 +178,17 @@ ZOPT_API zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype dt
 ZOPT_API zopt_status zopt_grad_accumulate(float* acc, const void* micro_grad, zopt_dtype dtype, int64_t n,
                                           int32_t flags, float max_norm, void* d_ws, size_t ws_bytes,
                                           zopt_clip_stats* d_stats, zopt_stream stream);
+/* Two micro-steps in one pass: the result (acc, and the stats on ZOPT_ACC_LAST) is bit for bit
+ * that of zopt_grad_accumulate(micro_grad_a) followed by zopt_grad_accumulate(micro_grad_b) with
+ * the same flags split between them (ZOPT_ACC_FIRST applies to a, ZOPT_ACC_LAST to b): acc =
+ * fp32(a) + fp32(b) on the first micro-steps, else (acc + a) + b, each addition rounded. It saves
+ * one read and one write of the fp32 sum: 8 B per element instead of 16 for the first two
+ * micro-steps, 12 instead of 20 for two later ones (bf16 parts). Both parts share the dtype and
+ * the rules for micro_grad, and either may be page-locked host memory. Errors: those of
+ * zopt_grad_accumulate, and EINVAL for a NULL micro_grad_b. */
+ZOPT_API zopt_status zopt_grad_accumulate2(float* acc, const void* micro_grad_a, const void* micro_grad_b,
+                                           zopt_dtype dtype, int64_t n, int32_t flags, float max_norm, void* d_ws,
+                                           size_t ws_bytes, zopt_clip_stats* d_stats, zopt_stream stream);
 
 /* ======================================================================================
  * 3. Fused AdamW over the flat fp32 shard

@@ -221,3 +221,14 @@ def test_state_bytes_is_the_sharded_memory_plan():
         assert 16 * N <= total <= 16 * (N + nb * (world - 1))
     assert Z.lib().zopt_layout_state_bytes(None, 0) == -1
     assert Z.lib().zopt_layout_state_bytes(lay.handle, 7) == -1
+
+
+def test_accumulate2_validates_before_launch():
+    L = Z.lib()
+    acc, g = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21)
+    assert L.zopt_grad_accumulate2(acc, g, None, Z.BF16, 64, 1, 1.0, None, 0, None, None) == 1
+    assert L.zopt_grad_accumulate2(acc, g, ctypes.c_void_p((1 << 22) + 8), Z.BF16, 64, 1, 1.0, None, 0, None,
+                                   None) == 1
+    assert b"aligned" in L.zopt_last_error()
+    assert L.zopt_grad_accumulate2(acc, g, g, Z.BF16, 0, 1, 1.0, None, 0, None, None) == 1
+    assert L.zopt_grad_accumulate2(acc, g, g, 9, 64, 1, 1.0, None, 0, None, None) == 2

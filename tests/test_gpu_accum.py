@@ -129,3 +129,23 @@ def test_full_size_zero2_micro_steps_with_inf_run(zopt):
     assert st["found_inf"] and not st["clipped"]
     assert torch.equal(p[idx_d], p0) and int(m.abs().sum()) == 0 and int(out.abs().sum()) == 0
     assert zopt.read_adam_state(state)["step"] == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("n", [1, 7, 8 * 1027 + 3, 2_000_003])
+@pytest.mark.parametrize("parts,host_b", [(2, False), (4, False), (4, True)])
+def test_two_parts_per_pass_bitwise(zopt, dtype, n, parts, host_b):
+    """zopt_grad_accumulate2 (two micro-steps in one pass) equals one zopt_grad_accumulate call per
+    part bit for bit: the fp32 sum in the same order and the fused stats; the second part may
+    come from pinned host memory."""
+    gen = torch.Generator(device="cuda").manual_seed(n + 10 * parts)
+    gs = [(torch.randn(n, generator=gen, device="cuda") * 1e-3).to(dtype) for _ in range(parts)]
+    acc1, st1 = run(zopt, gs)
+    acc2 = torch.full((n,), float("nan"), device="cuda")
+    ws, st = zopt.new_norm_workspace(n), zopt.new_clip_stats()
+    for k in range(0, parts, 2):
+        b = gs[k + 1].cpu().pin_memory() if host_b else gs[k + 1]
+        zopt.grad_accumulate2(acc2, gs[k], b, first=k == 0, last=k + 2 == parts, max_norm=1.0, ws=ws, stats=st)
+    torch.cuda.synchronize()
+    assert torch.equal(acc1.view(torch.int32), acc2.view(torch.int32))
+    assert zopt.read_clip_stats(st) == st1

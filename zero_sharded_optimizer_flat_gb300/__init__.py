@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         "zopt_adamw_rescale_step": (ctypes.c_int, [vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                                    ctypes.c_float, ctypes.c_float, vp, vp, vp]),
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
+        "zopt_grad_accumulate2": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp,
+                                                 vp]),
         "zopt_ns_workspace": (sz, [i64, i64, i32, ctypes.c_int]),
         "zopt_muon_workspace": (sz, [i64, i64, i32]),
         "zopt_take_device_error": (i32, []),
@@ -298,6 +300,19 @@ def grad_accumulate(acc, micro_grad, *, first: bool, last: bool, max_norm: float
     _check(lib().zopt_grad_accumulate(_ptr(acc), _ptr(micro_grad), _dtype_code(micro_grad), n, flags,
                                       float(max_norm), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(stats),
                                       _stream(stream)))
+
+
+def grad_accumulate2(acc, micro_grad_a, micro_grad_b, *, first: bool, last: bool, max_norm: float = 1.0, ws=None,
+                     stats=None, n: int | None = None, stream=None) -> None:
+    """``zopt_grad_accumulate2``: two micro-steps in one pass, bit for bit two grad_accumulate calls
+    (``first`` applies to the first part, ``last`` to the second)."""
+    if micro_grad_a.dtype != micro_grad_b.dtype:
+        raise ValueError("both micro-step gradients must have one dtype")
+    n = acc.numel() if n is None else int(n)
+    flags = (ACC_FIRST if first else 0) | (ACC_LAST if last else 0)
+    _check(lib().zopt_grad_accumulate2(_ptr(acc), _ptr(micro_grad_a), _ptr(micro_grad_b), _dtype_code(micro_grad_a),
+                                       n, flags, float(max_norm), _ptr(ws), 0 if ws is None else ws.numel(),
+                                       _ptr(stats), _stream(stream)))
 
 
 def clip_finalize(stats, max_norm: float, stream=None) -> None:
