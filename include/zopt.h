@@ -5,7 +5,8 @@
  * Five parts, each a few calls:
  *   1. the flat bucketed shard layout            (zopt_shard_layout and accessors, host only)
  *   2. the gradient norm / clip / found_inf stats (zopt_grad_norm_clip, zopt_clip_finalize,
- *      zopt_grad_accumulate for micro-step sums with the stats fused; device values)
+ *      zopt_grad_accumulate / zopt_grad_accumulate2 for micro-step sums with the stats fused;
+ *      device values)
  *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step, zopt_adamw_rescale_step)
  *   4. Muon's quintic Newton-Schulz               (zopt_ns_orthogonalize, _many)
  *   5. Muon's update around Newton-Schulz         (zopt_muon_step, _many)
