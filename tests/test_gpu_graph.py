@@ -122,3 +122,36 @@ def test_replayed_accumulation_reads_the_pinned_buffer_anew(zopt):
         assert torch.equal(st_g, st_e), rnd
         want = host[0].float() + host[1].float()
         assert torch.equal(acc_g.cpu(), want), rnd
+
+
+def test_replayed_two_part_accumulation(zopt):
+    """zopt_grad_accumulate2 captured once (one part on the device, one in pinned host memory):
+    every replay equals the eager calls bit for bit, sum and stats."""
+    n = 777_777
+    gen = torch.Generator().manual_seed(9)
+    dev = [(torch.randn(n, generator=gen) * 1e-3).to(torch.bfloat16).cuda() for _ in range(2)]
+    host = [torch.empty(n, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    out = {}
+    for arm in ("graph", "eager"):
+        out[arm] = (torch.empty(n, device="cuda"), zopt.new_norm_workspace(n), zopt.new_clip_stats())
+
+    def step(acc, ws, st):
+        zopt.grad_accumulate2(acc, dev[0], host[0], first=True, last=False)
+        zopt.grad_accumulate2(acc, dev[1], host[1], first=False, last=True, max_norm=1.0, ws=ws, stats=st)
+
+    for h in host:
+        h.copy_((torch.randn(n, generator=gen) * 1e-3).to(torch.bfloat16))
+    step(*out["eager"])  # first use outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(*out["graph"])
+    torch.cuda.synchronize()
+    for rnd in range(2):
+        for h in host:
+            h.copy_((torch.randn(n, generator=gen) * 1e-3).to(torch.bfloat16))
+        g.replay()
+        step(*out["eager"])
+        torch.cuda.synchronize()
+        assert torch.equal(out["graph"][0].view(torch.int32), out["eager"][0].view(torch.int32)), rnd
+        assert torch.equal(out["graph"][2], out["eager"][2]), rnd
