@@ -37,8 +37,8 @@ WORKLOAD = ("zero2-flat-shard-2e9-w8 + ns-stress-48: rank r of W=8 (S=250,000,00
 ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m, v (12) + bf16 (2)
 # DRAM bytes per element of one adamw_kernel launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum on a 64 Mi-element shard prefix, 1.9 GB per launch, scaled by the element
-# count; see profiles/adamw_kernel_zero2_shard.md), valid while the kernel's sources hash to
-# ADAMW_SRC_DIGEST (otherwise the traffic is reported as null)
+# count), valid while the kernel's sources hash to ADAMW_SRC_DIGEST (otherwise the traffic is
+# reported as null)
 ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
 ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
 MICRO_STEPS = 4

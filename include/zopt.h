@@ -155,8 +155,11 @@ ZOPT_API zopt_status zopt_clip_finalize(zopt_clip_stats* d_stats, float max_norm
  * device current); make that first call before any stream capture. Each call clears the
  * counter itself. All calls share the one array, so calls that overlap on the GPU (other
  * streams, unordered host threads) race and give wrong results; order them on one stream.
- * Errors: those of zopt_grad_norm_clip, and ZOPT_EINVAL when the device's launch would need
- * more than 1024 block partials (never on a 152-SM GB300). */
+ * A launch takes zopt_grad_norm_clip's grid (one wave of resident blocks) capped at 1024
+ * blocks; below the cap (always on a 152-SM GB300) the stats are bit for bit those of
+ * zopt_grad_norm_clip. The looked-up address is cached per device index: after a
+ * cudaDeviceReset of a device it used, a process must not call this entry point again.
+ * Errors: those of zopt_grad_norm_clip. */
 ZOPT_API zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype dtype, int64_t n, float max_norm,
                                                  zopt_clip_stats* d_stats, zopt_stream stream);
 

@@ -92,43 +92,79 @@ def test_pageable_host_micro_grad_is_refused(zopt):
         zopt.grad_accumulate(acc, torch.zeros(64, dtype=torch.bfloat16), first=True, last=False)
 
 
-def test_full_size_zero2_micro_steps_with_inf_run(zopt):
-    """The 2e9-parameter set's rank-0 shard (S = 250,000,000): 4 bf16 micro-steps summed in
-    fp32 (sampled slots bit for bit, the fused sum of squares against the oracle's over the
-    whole sum), then a run with +inf injected at a seeded index of micro-step 2: found_inf is
-    set and the AdamW step that follows changes nothing."""
+def test_full_size_zero2_five_steps_with_inf_step(zopt):
+    """The 2e9-parameter set's rank-0 shard (S = 250,000,000, W = 8) through its five stated
+    steps, in the launch configuration the benchmark times: each step sums four bf16 micro-step
+    gradients in fp32 (zopt_grad_accumulate, the clip stats fused into the last pass) and takes
+    the AdamW step with bf16 round-out (zopt_adamw_step). Step 3 carries +inf at a seeded index of
+    its second micro-step: found_inf is set, the step changes nothing and the counter stays at 2,
+    so steps 4 and 5 run as t = 3 and t = 4 (their bias corrections). After every step, sampled
+    slots (random, first and last, around every no-decay run edge, the poisoned index) of the sum,
+    master, m, v and bf16 weights are bit for bit the oracle's, computed slot by slot; the fused
+    sum of squares is within 1e-6 of the oracle's over the whole sum, the coefficient within 1e-6
+    of the oracle's."""
     import workloads
+    from oracle import adamw as OA
+    from oracle import layout as OL
+    from oracle.bf16 import f32_to_bf16_bits
 
     w = workloads.get("c4")
-    lay = zopt.ShardLayout([p.numel for p in w.adamw], [p.decay for p in w.adamw], w.bucket, w.world, w.rank)
+    assert w.steps == 5 and w.micro_steps == 4
+    numel = [p.numel for p in w.adamw]
+    decay = np.array([p.decay for p in w.adamw])
+    lay = zopt.ShardLayout(numel, decay, w.bucket, w.world, w.rank)
     S = lay.shard_len
-    gen = torch.Generator(device="cuda").manual_seed(44)
-    parts = [(torch.randn(S, generator=gen, device="cuda") * 1e-3).bfloat16() for _ in range(4)]
-    acc, st = run(zopt, parts)
-    rng = np.random.default_rng(44)
-    idx = np.unique(np.concatenate([rng.integers(0, S, 100_000), [0, S - 1]]))
-    idx_d = torch.from_numpy(idx).cuda()
-    ref = accumulate([p[idx_d].float().cpu().numpy() for p in parts])
-    assert np.array_equal(acc[idx_d].cpu().numpy().view(np.uint32), ref.view(np.uint32))
-    ss = OC.sumsq(acc.cpu().numpy())
-    assert close(st["sumsq"], ss) and not st["found_inf"]
-
-    bad = int(rng.integers(0, S))
-    parts[1][bad] = float("inf")
-    p = torch.randn(S, generator=gen, device="cuda") * 0.02
+    table = lay.device_table()
+    gen = torch.Generator(device="cuda").manual_seed(45)
+    p = torch.randn(S, device="cuda", generator=gen) * 0.02
     m, v = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
-    out = torch.zeros(S, dtype=torch.int16, device="cuda")
-    p0 = p[idx_d].clone()
-    clip, state = zopt.new_clip_stats(), zopt.new_adam_state()
-    ws = zopt.new_norm_workspace(S)
-    for k, g in enumerate(parts):
-        zopt.grad_accumulate(acc, g, first=k == 0, last=k == 3, max_norm=1.0, ws=ws, stats=clip)
-    zopt.adamw_step(lay, lay.device_table(), p, m, v, acc, out, lr=w.lr, clip_stats=clip, adam_state=state)
-    torch.cuda.synchronize()
-    st = zopt.read_clip_stats(clip)
-    assert st["found_inf"] and not st["clipped"]
-    assert torch.equal(p[idx_d], p0) and int(m.abs().sum()) == 0 and int(out.abs().sum()) == 0
-    assert zopt.read_adam_state(state)["step"] == 0
+    acc = torch.empty(S, device="cuda")
+    out = torch.empty(S, dtype=torch.int16, device="cuda")
+    clip, state, ws = zopt.new_clip_stats(), zopt.new_adam_state(), zopt.new_norm_workspace(S)
+    rng = np.random.default_rng(45)
+    bad_step, bad_micro, bad = 2, 1, int(rng.integers(0, S))
+    runs = lay.nodecay_runs()
+    edges = np.concatenate([runs.reshape(-1) + d for d in (-2, -1, 0, 1)])
+    idx = np.unique(np.clip(np.concatenate([rng.integers(0, S, 200_000), [0, 1, S - 2, S - 1, bad], edges]), 0, S - 1))
+    idx_d = torch.from_numpy(idx).cuda()
+    owner = OL.param_of_flat(numel, OL.flat_index_of_slots(numel, w.bucket, w.world, w.rank, idx))
+    dec = np.where(owner >= 0, decay[np.maximum(owner, 0)], False)
+    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    sp = p[idx_d].cpu().numpy()
+    sm, sv = np.zeros_like(sp), np.zeros_like(sp)
+    t = 0
+    for s in range(w.steps):
+        parts = [(torch.randn(S, generator=gen, device="cuda") * 1e-3).bfloat16() for _ in range(w.micro_steps)]
+        if s == bad_step:
+            parts[bad_micro][bad] = float("inf")
+        for k, g in enumerate(parts):
+            zopt.grad_accumulate(acc, g, first=k == 0, last=k == w.micro_steps - 1, max_norm=w.max_norm, ws=ws,
+                                 stats=clip)
+        zopt.adamw_step(lay, table, p, m, v, acc, out, lr=h.lr, beta1=h.beta1, beta2=h.beta2, eps=h.eps,
+                        weight_decay=h.weight_decay, clip_stats=clip, adam_state=state)
+        torch.cuda.synchronize()
+        sg = accumulate([g[idx_d].float().cpu().numpy() for g in parts])
+        assert np.array_equal(acc[idx_d].cpu().numpy().view(np.uint32), sg.view(np.uint32)), s
+        st = zopt.read_clip_stats(clip)
+        if s == bad_step:
+            assert st["found_inf"] and not st["clipped"] and st["clip_coef"] == 0.0
+        else:
+            ref = OC.clip_stats(acc.cpu().numpy(), w.max_norm)
+            assert not st["found_inf"] and close(st["sumsq"], ref["sumsq"])
+            assert close(st["clip_coef"], ref["clip_coef"]) and st["clipped"] == ref["clipped"]
+            t += 1
+            sc = OA.scalars_f32(h, t)
+            for mask in (dec, ~dec):
+                pp, mm, vv = sp[mask], sm[mask], sv[mask]
+                OA.adamw_tensor_f32(pp, mm, vv, sg[mask], np.float32(st["clip_coef"]), bool(mask is dec), sc)
+                sp[mask], sm[mask], sv[mask] = pp, mm, vv
+        assert np.array_equal(p[idx_d].cpu().numpy().view(np.uint32), sp.view(np.uint32)), s
+        assert np.array_equal(m[idx_d].cpu().numpy().view(np.uint32), sm.view(np.uint32)), s
+        assert np.array_equal(v[idx_d].cpu().numpy().view(np.uint32), sv.view(np.uint32)), s
+        assert np.array_equal(out[idx_d].cpu().numpy().view(np.uint16), f32_to_bf16_bits(sp)), s
+        assert zopt.read_adam_state(state)["step"] == t, s
+        del parts
+    assert t == 4
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])

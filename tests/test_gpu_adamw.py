@@ -131,25 +131,33 @@ def test_c1_three_steps_bitwise(zopt):
         case.compare()
 
 
-def test_gpt2_small_set_three_wsd_steps_bitwise(zopt):
+def test_gpt2_small_set_ten_wsd_steps_bitwise(zopt):
     """GPT-2-small AdamW set (embedding 50304x768 + 25 scales, N = 38,652,672, 2 buckets of
-    2^25), 1 % zero gradient rows, the WSD learning rate of a 10-step run, W = 1."""
+    2^25), 1 % zero gradient rows, W = 1, through its ten stated steps on the trainer's WSD
+    schedule for a 10-step run (bluscript_zero_ckpt.cpp, get_lr and its short-run rule: warm-up
+    1 step, stable 5, cosine decay over the last 4 to the floor 6e-5): master, m, v and the bf16
+    weights bit for bit after every step."""
     w = workloads.get("c2")
+    assert w.steps == 10
+    lrs = [w.lr_at(s) for s in range(w.steps)]
+    assert lrs[9] == 6e-5 and lrs[7] < lrs[6] == lrs[1] == 6e-4  # the decay phase runs
     case = Case(zopt, w.adamw, w.bucket, 1, 0, seed=w.seed, gdtype=torch.bfloat16)
-    for s in range(3):
-        case.step(s, OA.Hyper(w.lr_at(s), w.beta1, w.beta2, w.eps, w.weight_decay), max_norm=w.max_norm,
+    for s in range(w.steps):
+        case.step(s, OA.Hyper(lrs[s], w.beta1, w.beta2, w.eps, w.weight_decay), max_norm=w.max_norm,
                   zero_row_frac=w.zero_row_frac)
-    case.compare()
+        case.compare()
 
 
-def test_llama_set_rank0_of_8_two_steps_bitwise(zopt):
-    """Llama-style 1.1B AdamW set (embedding 32000x2048 + 33 scales), simulated rank 0 of 8."""
+def test_llama_set_rank0_of_8_five_steps_bitwise(zopt):
+    """Llama-style 1.1B AdamW set (embedding 32000x2048 + 33 scales), simulated rank 0 of 8,
+    through its five stated steps, bit for bit after every step."""
     w = workloads.get("c3")
+    assert w.steps == 5
     case = Case(zopt, w.adamw, w.bucket, w.world, w.rank, seed=w.seed, gdtype=torch.bfloat16)
     h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    for s in range(2):
+    for s in range(w.steps):
         case.step(s, h, max_norm=w.max_norm)
-    case.compare()
+        case.compare()
 
 
 def test_wsd_schedule_lr_changes_each_step(zopt):

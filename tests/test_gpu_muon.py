@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import workloads
 from oracle import muon as OM
 from oracle.bf16 import f32_to_bf16_bits
 from oracle.ns import newton_schulz
@@ -73,31 +74,69 @@ def test_guard_rejects_keeps_master_updates_momentum(zopt):
     assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(p0.cpu().numpy()))
 
 
-def test_llama_owned_set_one_step(zopt):
-    """The 1.1B set's matrices owned by rank 0 of 8 (round-robin): 4 x Wq, 4 x Wv, 4 x gate_up,
-    one Muon step per shape group."""
-    import workloads
+def run_muon_set(Z, params, seed, steps, lr_at, zero_row_frac=0.0):
+    """Steps a parameter set's Muon matrices ``steps`` times, one zopt_muon_step_many call per step
+    over the set's shapes (each shape's matrices one batch, as a trainer groups them), and checks
+    every matrix after every step against the oracle: the momentum buffer bit for bit (carried by
+    the oracle from zero), the applied update within 2e-2 of the fp64 Newton-Schulz of the oracle's
+    u, no rejection, and the bf16 weights bit for bit the new master's. The learning rate of 0-based
+    step s is lr_at(s). Inputs: workloads' masters (N(0, 0.02)) and bf16 gradients (N(0, 1e-3),
+    a seeded fraction of zero rows)."""
+    shapes = []
+    for prm in params:
+        if prm.shape not in shapes:
+            shapes.append(prm.shape)
+    groups = [[i for i, prm in enumerate(params) if prm.shape == sh] for sh in shapes]
+    master = [torch.stack([workloads.master_for(params[i], seed, 20_000 + i) for i in idx]).cuda() for idx in groups]
+    buf = [torch.zeros_like(x) for x in master]
+    out = [torch.zeros(x.shape, dtype=torch.int16, device="cuda") for x in master]
+    stats = [Z.new_muon_stats(len(idx)) for idx in groups]
+    ws = Z.new_muon_workspace_many([(r, c, len(idx)) for (r, c), idx in zip(shapes, groups)])
+    ref_buf = [np.zeros(tuple(x.shape), np.float32) for x in master]
+    for s in range(steps):
+        lr = lr_at(s)
+        h = OM.MuonHyper(lr=lr)
+        grads = [torch.stack([workloads.grad_for(params[i], seed, 300_000 + 1000 * s + i, zero_row_frac)
+                              for i in idx]) for idx in groups]
+        p_old = [x.cpu().numpy() for x in master]
+        Z.muon_step_many([(master[k], buf[k], grads[k].cuda(), out[k], stats[k]) for k in range(len(groups))], ws,
+                         lr=lr)
+        torch.cuda.synchronize()
+        decay = np.float32(1.0 - lr * h.weight_decay)
+        for k, (r, c) in enumerate(shapes):
+            step = np.float32(lr * OM.lr_scale(r, c, h.match_rms_adamw))
+            pn = master[k].cpu().numpy()
+            st = Z.read_muon_stats(stats[k])
+            g_np = grads[k].float().numpy()
+            for b in range(len(groups[k])):
+                u = OM.momentum_f32(ref_buf[k][b], g_np[b], h)
+                U_ref = newton_schulz(u.astype(np.float64), steps=h.ns_steps)
+                applied = (p_old[k][b] * decay - pn[b]).astype(np.float64) / float(step)
+                assert rel(applied, U_ref) <= 2e-2, (s, (r, c), b)
+                assert not st[b]["rejected"]
+            assert np.array_equal(buf[k].cpu().numpy().view(np.uint32), ref_buf[k].view(np.uint32)), (s, (r, c))
+            assert np.array_equal(out[k].cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn)), (s, (r, c))
+
+
+def test_gpt2_body_ten_wsd_steps(zopt):
+    """The GPT-2-small body's 48 Muon matrices (768x2304, 768x768, 768x3072, 3072x768; 1 % zero
+    gradient rows) through the set's ten stated steps, on the WSD curve the AdamW group follows
+    with Muon's own peak and floor (8e-4, 8e-5; bluscript_zero_ckpt.cpp feeds both groups one
+    schedule): the decay phase's learning rates reach the update."""
+    w = workloads.get("c2")
+    lrs = [w.muon_lr_at(s) for s in range(w.steps)]
+    assert w.steps == 10 and len(w.muon) == 48 and lrs[9] == 8e-5 and lrs[8] < lrs[7] < lrs[6] == 8e-4
+    run_muon_set(zopt, w.muon, w.seed, w.steps, w.muon_lr_at, w.zero_row_frac)
+
+
+def test_llama_owned_set_five_steps(zopt):
+    """The 1.1B set's matrices owned by rank 0 of 8 (round-robin: 4 x Wq 2048^2, 4 x Wv 2048x512,
+    4 x gate_up 2048x11264) through the set's five stated steps in one call per step, as the
+    benchmark's Muon step runs them."""
     w = workloads.get("c3")
     owned = w.owned_muon()
-    assert len(owned) == 12
-    shapes = sorted({p.shape for p in owned})
-    h = OM.MuonHyper(lr=8e-4)
-    for (r, c) in shapes:
-        k = sum(1 for p in owned if p.shape == (r, c))
-        p = torch.randn(k, r, c, device="cuda") * 0.02
-        p_old = p.cpu().numpy()
-        buf = torch.zeros_like(p)
-        g = (torch.randn(k, r, c, device="cuda") * 1e-3).bfloat16()
-        stats = zopt.new_muon_stats(k)
-        zopt.muon_step(p, buf, g, None, zopt.new_muon_workspace(r, c, k), stats, lr=h.lr)
-        torch.cuda.synchronize()
-        step = np.float32(h.lr * OM.lr_scale(r, c, True))
-        decay = np.float32(1.0 - h.lr * h.weight_decay)
-        b = k - 1  # check the last matrix of the group against the oracle
-        u = OM.momentum_f32(np.zeros((r, c), np.float32), g[b].float().cpu().numpy(), h)
-        U_ref = newton_schulz(u.astype(np.float64), steps=5)
-        applied = (p_old[b] * decay - p[b].cpu().numpy()).astype(np.float64) / float(step)
-        assert rel(applied, U_ref) <= 2e-2
+    assert len(owned) == 12 and w.steps == 5
+    run_muon_set(zopt, owned, w.seed, w.steps, w.muon_lr_at)
 
 
 def test_many_shapes_equal_single_calls(zopt):

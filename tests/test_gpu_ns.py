@@ -7,8 +7,10 @@ X <- aX + (bXX' + c(XX')^2)X on the whole matrix, 5 steps).
   <= 4e-3: one bf16 rounding of the output plus fp32 accumulation order); A and B' must be
   exactly symmetric.
 * End to end, 5 steps: relative Frobenius error against the fp64 oracle <= 2e-2 (bf16).
-* Full-size stress matrices: against a float32 torch Newton-Schulz on the GPU (the checker)
-  <= 2e-2, and the oracle on the top-left 256 x 1024 block taken as its own input.
+* Full-size stress matrices, in the benchmark's launch configuration: one matrix of each
+  shape against the fp64 oracle <= 2e-2, every matrix against a float32 torch Newton-Schulz
+  on the GPU (the checker) <= 2e-2, and the oracle on the top-left 256 x 1024 block taken as
+  its own input.
 """
 import numpy as np
 import pytest
@@ -247,26 +249,41 @@ def test_llama_owned_matrices_match_fp64_oracle(zopt, rows, cols):
     assert rel(X.cpu(), torch.from_numpy(ref)) <= 2e-2
 
 
-@pytest.mark.parametrize("rows,cols", [(4096, 4096), (4096, 14336), (14336, 4096)])
-def test_stress_shapes_against_fp32_checker(zopt, rows, cols):
+def test_stress_set_as_benchmarked_against_fp64_oracle(zopt):
+    """The Newton-Schulz stress set in the launch configuration the benchmark times: 16 each of
+    4096x4096, 4096x14336 and 14336x4096 bf16 matrices (entries N(0, 1), each divided by its
+    Frobenius norm) in one zopt_ns_orthogonalize_many call, 5 steps, on the CTA-pair kernels.
+    The first matrix of each shape is checked against the fp64 oracle fed the same bf16 input
+    (relative Frobenius error <= 2e-2; bluscript_zero_ckpt.cpp, ShardedMuon note: the polynomial
+    over the whole matrix); every matrix against a float32 Newton-Schulz on the GPU (the checker,
+    TF32 off); and the top-left 256 x 1024 block of each shape's first matrix, taken as its own
+    input, against the oracle."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
     try:
-        G = gaussian(rows, cols, rows ^ cols)
-        G = (G.float() / torch.linalg.norm(G.float())).to(torch.bfloat16)  # Frobenius-normalised input
-        X = torch.empty_like(G)
-        ws = zopt.new_ns_workspace(rows, cols)
-        zopt.ns_orthogonalize(G, X, ws, steps=5)
-        ref = torch_ns_fp32(G)
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        pairs = []
+        for r, c in ((4096, 4096), (4096, 14336), (14336, 4096)):
+            G = torch.randn(16, r, c, generator=gen, device="cuda")
+            G /= torch.linalg.vector_norm(G, dim=(1, 2), keepdim=True)
+            G = G.to(torch.bfloat16)
+            pairs.append((G, torch.empty_like(G)))
+        ws = zopt.new_ns_workspace_many([(G.shape[1], G.shape[2], G.shape[0]) for G, _ in pairs])
+        zopt.ns_orthogonalize_many(pairs, ws, steps=5)
         torch.cuda.synchronize()
-        assert rel(X.float(), ref) <= 2e-2
-        # the top-left 256 x 1024 block as its own input, against the fp64 oracle
-        blk = G[:256, :1024].contiguous()
-        Xb = torch.empty_like(blk)
-        zopt.ns_orthogonalize(blk, Xb, zopt.new_ns_workspace(256, 1024), steps=5)
-        torch.cuda.synchronize()
-        refb = newton_schulz(blk.double().cpu().numpy(), steps=5)
-        assert rel(Xb.cpu(), torch.from_numpy(refb)) <= 2e-2
+        del ws
+        for G, X in pairs:
+            ref = newton_schulz(G[0].double().cpu().numpy(), steps=5)
+            err = rel(X[0].cpu(), torch.from_numpy(ref))
+            assert err <= 2e-2, (tuple(G.shape), err)
+            for i in range(G.shape[0]):
+                assert rel(X[i].float(), torch_ns_fp32(G[i])) <= 2e-2, (tuple(G.shape), i)
+            blk = G[0, :256, :1024].contiguous()
+            Xb = torch.empty_like(blk)
+            zopt.ns_orthogonalize(blk, Xb, zopt.new_ns_workspace(256, 1024), steps=5)
+            torch.cuda.synchronize()
+            refb = newton_schulz(blk.double().cpu().numpy(), steps=5)
+            assert rel(Xb.cpu(), torch.from_numpy(refb)) <= 2e-2
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
 

@@ -66,6 +66,8 @@ class Workload:
     zero_row_frac: float = 0.0
     ns_steps: int = 5
     lr_schedule: tuple | None = None  # (max_lr, min_lr, warmup, stable, max_steps)
+    muon_lr: float = 8e-4
+    muon_lr_schedule: tuple | None = None  # the same curve with Muon's (peak, floor) pair
 
     @property
     def adamw_numel(self) -> int:
@@ -76,6 +78,13 @@ class Workload:
         if self.lr_schedule is None:
             return self.lr
         return wsd_lr(step, *self.lr_schedule)
+
+    def muon_lr_at(self, step: int) -> float:
+        """Host-side Muon learning rate for 0-based step ``step`` (bluscript_zero_ckpt.cpp feeds
+        both optimizer groups the one WSD curve, each with its own peak and floor)."""
+        if self.muon_lr_schedule is None:
+            return self.muon_lr
+        return wsd_lr(step, *self.muon_lr_schedule)
 
     def owned_muon(self) -> list:
         """Muon matrices owned by ``rank`` under round-robin whole-parameter ownership."""
@@ -126,7 +135,8 @@ def _c2() -> Workload:
     adamw += [Param(f"scale{i}", (d,), False) for i in range(2 * layers + 1)]
     warmup, stable = wsd_short_run(10)
     return Workload("c2-gpt2-small", adamw=adamw, muon=muon, steps=10, seed=2, zero_row_frac=0.01,
-                    lr=6e-4, lr_schedule=(6e-4, 6e-5, warmup, stable, 10))
+                    lr=6e-4, lr_schedule=(6e-4, 6e-5, warmup, stable, 10),
+                    muon_lr_schedule=(8e-4, 8e-5, warmup, stable, 10))
 
 
 def _llama_layer(l: int, d: int = 2048) -> list:

@@ -135,6 +135,16 @@ def _stream(stream) -> int | None:
     return getattr(stream, "cuda_stream", stream)
 
 
+def _count(t, n) -> int:
+    """The element count a call covers: all of ``t``, or the first n (never more than it holds)."""
+    if n is None:
+        return t.numel()
+    n = int(n)
+    if n > t.numel():
+        raise ValueError(f"n = {n} exceeds the tensor's {t.numel()} elements")
+    return n
+
+
 def _dtype_code(t) -> int:
     import torch
     if t.dtype == torch.float32:
@@ -263,7 +273,7 @@ def new_norm_workspace(n: int, device="cuda"):
 
 def grad_norm_clip(grad, max_norm: float, ws, stats, n: int | None = None, stream=None) -> None:
     """``zopt_grad_norm_clip`` over the first n elements of ``grad`` (default: all)."""
-    n = grad.numel() if n is None else int(n)
+    n = _count(grad, n)
     _check(lib().zopt_grad_norm_clip(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(ws), ws.numel(),
                                      _ptr(stats), _stream(stream)))
 
@@ -271,7 +281,7 @@ def grad_norm_clip(grad, max_norm: float, ws, stats, n: int | None = None, strea
 def grad_norm_clip_noalloc(grad, max_norm: float, stats, n: int | None = None, stream=None) -> None:
     """``zopt_grad_norm_clip_noalloc``: the same reduction with the library's static scratch
     instead of a workspace, for callers that cannot allocate device memory."""
-    n = grad.numel() if n is None else int(n)
+    n = _count(grad, n)
     _check(lib().zopt_grad_norm_clip_noalloc(_ptr(grad), _dtype_code(grad), n, float(max_norm), _ptr(stats),
                                              _stream(stream)))
 
@@ -295,7 +305,8 @@ def grad_accumulate(acc, micro_grad, *, first: bool, last: bool, max_norm: float
                     n: int | None = None, stream=None) -> None:
     """``zopt_grad_accumulate``: acc (fp32) = / += micro_grad; the last micro-step also
     writes the clip stats of the finished sum."""
-    n = acc.numel() if n is None else int(n)
+    n = _count(acc, n)
+    _count(micro_grad, n)
     flags = (ACC_FIRST if first else 0) | (ACC_LAST if last else 0)
     _check(lib().zopt_grad_accumulate(_ptr(acc), _ptr(micro_grad), _dtype_code(micro_grad), n, flags,
                                       float(max_norm), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(stats),
@@ -308,7 +319,9 @@ def grad_accumulate2(acc, micro_grad_a, micro_grad_b, *, first: bool, last: bool
     (``first`` applies to the first part, ``last`` to the second)."""
     if micro_grad_a.dtype != micro_grad_b.dtype:
         raise ValueError("both micro-step gradients must have one dtype")
-    n = acc.numel() if n is None else int(n)
+    n = _count(acc, n)
+    _count(micro_grad_a, n)
+    _count(micro_grad_b, n)
     flags = (ACC_FIRST if first else 0) | (ACC_LAST if last else 0)
     _check(lib().zopt_grad_accumulate2(_ptr(acc), _ptr(micro_grad_a), _ptr(micro_grad_b), _dtype_code(micro_grad_a),
                                        n, flags, float(max_norm), _ptr(ws), 0 if ws is None else ws.numel(),

@@ -11,11 +11,16 @@
 //
 // Limits: the array holds the arrival counter and kStaticPartials fp64 partial sums, 8,448
 // bytes in all, and every GPU that loads the library keeps it until the process exits. A
-// launch uses one partial per block, and the grid is one wave of resident blocks (at most
-// the SM count times the blocks each SM holds), so on a GB300 (152 SMs) every n >= 1 fits;
-// a device whose wave would exceed kStaticPartials blocks is rejected with ZOPT_EINVAL.
+// launch uses one partial per block. Its grid is the one zopt_grad_norm_clip takes (one wave
+// of resident blocks: 304 for bf16 and 608 for fp32 gradients on a 152-SM GB300), capped at
+// kStaticPartials blocks; the kernel walks the gradient grid-stride, so a capped grid covers
+// every element too (it only changes the order of the fp64 partial sums). Under the cap the
+// result is bit for bit zopt_grad_norm_clip's.
 // All calls share the one array: calls that overlap on the GPU (different streams, or
 // different host threads without ordering) race on it and give wrong results.
+// The address cache below is per device index for the life of the process; after a
+// cudaDeviceReset the module may load elsewhere, so this entry point must not be called
+// again in a process that has reset a device it used.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -68,12 +73,9 @@ extern "C" zopt_status zopt_grad_norm_clip_noalloc(const void* grad, zopt_dtype 
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != ZOPT_OK) return st;
-  const int blocks = norm_launch_blocks(n, dtype);
+  int blocks = norm_launch_blocks(n, dtype);
   if (blocks <= 0) return fail(ZOPT_ECUDA, "zopt_grad_norm_clip_noalloc: no CUDA device");
-  if (blocks > kStaticPartials)
-    return fail(ZOPT_EINVAL, "zopt_grad_norm_clip_noalloc: this device's launch needs " + std::to_string(blocks) +
-                                 " partial sums but the static scratch holds " + std::to_string(kStaticPartials) +
-                                 "; use zopt_grad_norm_clip with a workspace");
+  if (blocks > kStaticPartials) blocks = kStaticPartials;  // grid-stride: fewer blocks still cover n
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the arrival counter must start at zero
   // (the partials are written before they are read).
