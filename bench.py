@@ -45,7 +45,7 @@ MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 # two parts to a pass: the first pair reads 2 x 2 and writes 4; each later pair also reads the sum
 PAIRED_ACC_BYTES = 8 + 12 * (MICRO_STEPS // 2 - 1)
-CPU_SAMPLE = 4_000_000
+BF16_STEP_BYTES = 2 + 28  # norm reads the bf16 gradient; the step reads p, m, v, g (14) and writes p, m, v, bf16 (14)
 
 
 def peaks() -> dict:
@@ -127,88 +127,6 @@ def smi_id(local_rank: int) -> str:
     return str(local_rank)
 
 
-class OracleAdamwSample:
-    """The oracle as it stands (numpy, one core) on a bounded sample of the step's workload: 4
-    bf16 micro-steps summed in fp32, norm/clip, AdamW and the bf16 round-out over CPU_SAMPLE
-    shard elements of the 2e9-parameter set's shard."""
-
-    def __init__(self):
-        import numpy as np
-        import torch
-
-        import workloads
-        from oracle import adamw as OA
-
-        w = workloads.get("c4")
-        self.w, self.h = w, OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-        self.n = n = CPU_SAMPLE
-        self.p = workloads.shard_vector(n, 0.02, w.seed, 1).numpy()
-        self.m = np.zeros(n, np.float32)
-        self.v = np.zeros(n, np.float32)
-        self.mask = np.ones(n, np.uint8)
-        self.mask[::1000] = 0
-        self.micro = [workloads.shard_vector(n, 1e-3, w.seed, 2 + k, dtype=torch.bfloat16).float().numpy()
-                      for k in range(MICRO_STEPS)]
-        self.t = 0
-        self.bytes = (ACC_BYTES + ADAMW_BYTES) * n
-
-    def step(self):
-        from oracle import adamw as OA
-        from oracle import clip as OC
-        from oracle.accum import accumulate
-        from oracle.bf16 import f32_to_bf16_bits
-
-        g = accumulate(self.micro)
-        st = OC.clip_stats(g, self.w.max_norm)
-        self.t += 1
-        OA.step_flat_f32(self.p, self.m, self.v, g, self.mask, st["clip_coef"], self.h, self.t)
-        f32_to_bf16_bits(self.p)
-
-    def what(self, steps: int, seconds: float) -> str:
-        return (f"{steps} steps of 4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out over "
-                f"{self.n:,} shard elements (numpy fp32 exact-order oracle, {seconds:.1f} s)")
-
-
-class OracleNsSample:
-    """The fp64 Newton-Schulz oracle on a 256 x 1024 block shaped like the stress set's
-    (numpy's BLAS uses the host's threads)."""
-
-    def __init__(self):
-        import numpy as np
-        import torch
-
-        import workloads
-
-        self.g = workloads.ns_input(256, 1024, 5, 0, dtype=torch.float32).numpy().astype(np.float64)
-        self.flops = ns_flops(256, 1024, 5)
-
-    def step(self):
-        from oracle.ns import newton_schulz
-
-        newton_schulz(self.g, steps=5)
-
-    def what(self, calls: int, seconds: float) -> str:
-        return f"{calls} fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set ({seconds:.1f} s)"
-
-
-def _timed_for(sample, seconds: float):
-    n, t0 = 0, time.perf_counter()
-    while True:
-        sample.step()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds and n >= 2:
-            return n, el
-
-
-def cpu_oracle_run(seconds: float = 10.0) -> dict:
-    """The AdamW-part oracle sample repeated for ~`seconds` (the GPU arm's CPU baseline)."""
-    a = OracleAdamwSample()
-    steps, el = _timed_for(a, seconds)
-    return {"value": round(a.bytes * steps / el / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": a.what(steps, el)}
-
-
 def adamw_traffic(S: int):
     """DRAM bytes per adamw_kernel launch over S elements from the committed ncu capture, or
     None if the kernel's sources changed since."""
@@ -227,48 +145,237 @@ def ns_flops(rows: int, cols: int, steps: int) -> float:
     return float(steps) * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
 
 
-def cpu_oracle_ns(seconds: float = 6.0) -> dict:
-    """The Newton-Schulz oracle sample repeated for ~`seconds` (the GPU arm's CPU baseline)."""
-    x = OracleNsSample()
-    calls, el = _timed_for(x, seconds)
-    return {"value": round(x.flops * calls / el / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle", "sample": x.what(calls, el)}
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baselines."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# The AdamW-part oracle over whole shards on every host core. The shard is cut into one
+# contiguous slice per core, each stepped by its own spawned process with the oracle's functions
+# unchanged (the step is element-wise). The clip coefficient needs the whole shard's sum of
+# squares, so every step the processes add their slices' sums through shared memory in a fixed
+# order (what W ranks' all-reduce would do) before any of them steps.
+
+def _adamw_oracle_worker(wid, nw, jobs, barrier, sums, marks):
+    os.environ["OMP_NUM_THREADS"] = os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    import numpy as np
+    import torch
+
+    torch.set_num_threads(1)
+    import workloads
+    from oracle import adamw as OA
+    from oracle import clip as OC
+    from oracle.accum import accumulate
+    from oracle.bf16 import f32_to_bf16_bits
+
+    for j, job in enumerate(jobs):
+        S = job["S"]
+        lo, hi = S * wid // nw, S * (wid + 1) // nw
+        n = hi - lo
+        seed = job["seed"]
+        p = workloads.shard_vector(n, 0.02, seed, 1 + 1000 * wid).numpy()
+        m = np.zeros(n, np.float32)
+        v = np.zeros(n, np.float32)
+        mask = np.ones(n, np.uint8)
+        mask[(-lo) % 1000::1000] = 0  # a synthetic decay mask: every 1000th shard slot excluded
+        micro = [workloads.shard_vector(n, 1e-3, seed, 2 + k + 1000 * wid, dtype=torch.bfloat16).float().numpy()
+                 for k in range(job["micro"])]
+        h = OA.Hyper(job["lr"], job["beta1"], job["beta2"], job["eps"], job["weight_decay"])
+        t = 0
+        for it in range(job["warmup"] + job["steps"]):
+            if it == job["warmup"]:
+                barrier.wait()
+                marks[2 * (j * nw + wid)] = time.perf_counter()
+            g = accumulate(micro) if len(micro) > 1 else micro[0]
+            sums[wid] = OC.sumsq(g)
+            barrier.wait()
+            total = sum(sums[k] for k in range(nw))
+            barrier.wait()
+            st = OC.clip_from_sumsq(total, job["max_norm"])
+            t += 1
+            OA.step_flat_f32(p, m, v, g, mask, st["clip_coef"], h, t)
+            f32_to_bf16_bits(p)
+        marks[2 * (j * nw + wid) + 1] = time.perf_counter()
+        del p, m, v, micro
+
+
+def adamw_oracle_on_all_cores(jobs: list) -> list:
+    """Runs each job (a shard of S elements, `micro` bf16 micro-step gradients, `warmup` untimed
+    and `steps` timed steps) through the AdamW-part oracle on every host core; returns, per job,
+    the whole-job seconds of its timed steps (first start to last finish over the processes)."""
+    import multiprocessing as mp
+    nw = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    barrier = ctx.Barrier(nw)
+    sums = ctx.Array("d", nw, lock=False)
+    marks = ctx.Array("d", 2 * nw * len(jobs), lock=False)
+    procs = [ctx.Process(target=_adamw_oracle_worker, args=(k, nw, jobs, barrier, sums, marks)) for k in range(nw)]
+    for pr in procs:
+        pr.start()
+    for pr in procs:
+        pr.join()
+    if any(pr.exitcode != 0 for pr in procs):
+        raise RuntimeError("an AdamW oracle process failed")
+    out = []
+    for j in range(len(jobs)):
+        starts = [marks[2 * (j * nw + k)] for k in range(nw)]
+        ends = [marks[2 * (j * nw + k) + 1] for k in range(nw)]
+        out.append(max(ends) - min(starts))
+    return out
+
+
+def adamw_job(name: str, steps: int, warmup: int) -> dict:
+    """The AdamW part of a parameter set's step as the oracle runs it: the set's whole rank-r
+    shard, its micro-steps summed in fp32, norm/clip, AdamW, bf16 round-out."""
+    import workloads
+    from oracle.layout import shard_len
+    w = workloads.get(name)
+    S = shard_len([p.numel for p in w.adamw], w.bucket, w.world)
+    return {"name": name, "S": S, "micro": max(1, w.micro_steps), "seed": w.seed, "lr": w.lr, "beta1": w.beta1,
+            "beta2": w.beta2, "eps": w.eps, "weight_decay": w.weight_decay, "max_norm": w.max_norm,
+            "steps": steps, "warmup": warmup,
+            "bytes_per_element": ACC_BYTES + ADAMW_BYTES if w.micro_steps > 1 else BF16_STEP_BYTES}
+
+
+def ns_oracle_rates() -> dict:
+    """The fp64 Newton-Schulz oracle (numpy, the host's threaded BLAS) on whole matrix sets: the
+    tiny decoder's 8 matrices, the GPT-2-small body's 48, the 1.1B set's 12 rank-0 matrices, the
+    stress set's 256 x 1024 block and one whole 4096 x 4096 stress matrix. The whole stress set's
+    time is extrapolated from the measured rate of that 4096^2 matrix (labelled so)."""
+    import numpy as np
+    import torch
+
+    import workloads
+    from oracle.ns import newton_schulz
+
+    def timed(mats, reps=1):
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for x in mats:
+                newton_schulz(x, steps=5)
+        return (time.perf_counter() - t0) / reps
+
+    def sets(name):
+        w = workloads.get(name)
+        ps = w.owned_muon() if w.world > 1 else w.muon
+        return [workloads.ns_input(p.shape[0], p.shape[1], w.seed, 600 + i, dtype=torch.bfloat16)
+                .float().numpy().astype(np.float64) for i, p in enumerate(ps)]
+
+    out = {}
+    for name, label in (("c1", "tiny decoder, 8 matrices"), ("c2", "GPT-2-small body, 48 matrices"),
+                        ("c3", "1.1B set, rank 0 of 8, 12 matrices")):
+        mats = sets(name)
+        fl = sum(ns_flops(x.shape[0], x.shape[1], 5) for x in mats)
+        sec = timed(mats, 3 if name == "c1" else 1)
+        out[name] = {"what": label, "s": round(sec, 4), "tflops": round(fl / sec / 1e12, 4)}
+    blk = [workloads.ns_input(256, 1024, 5, 0, dtype=torch.bfloat16).float().numpy().astype(np.float64)]
+    sec = timed(blk, 5)
+    out["c5_block"] = {"what": "stress set's 256x1024 block", "s": round(sec, 4),
+                       "tflops": round(ns_flops(256, 1024, 5) / sec / 1e12, 4)}
+    big = [workloads.ns_input(4096, 4096, 5, 1, dtype=torch.bfloat16, frobenius_normalise=True)
+           .float().numpy().astype(np.float64)]
+    sec = timed(big)
+    rate = ns_flops(4096, 4096, 5) / sec
+    stress = 16 * (ns_flops(4096, 4096, 5) + 2 * ns_flops(4096, 14336, 5))
+    out["c5_4096"] = {"what": "one whole 4096x4096 stress matrix", "s": round(sec, 4),
+                      "tflops": round(rate / 1e12, 4)}
+    out["c5_whole_extrapolated"] = {"what": "the whole 48-matrix stress set, EXTRAPOLATED from the 4096^2 "
+                                            "matrix's rate", "s": round(stress / rate, 1)}
+    return out
+
+
+def cpu_baselines() -> tuple:
+    """The GPU arm's CPU baselines: the AdamW-part oracle on every core over the whole shard of
+    each parameter set (two timed steps after one untimed), and the fp64 Newton-Schulz oracle."""
+    names = ["c4", "c1", "c2", "c3"]
+    jobs = [adamw_job(nm, 2, 1) for nm in names]
+    S = jobs[0]["S"]
+    secs = adamw_oracle_on_all_cores(jobs)
+    cores, model = os.cpu_count(), cpu_model()
+    per = {}
+    for job, sec in zip(jobs, secs):
+        per[job["name"]] = {"shard_len": job["S"], "bytes_per_element": job["bytes_per_element"],
+                            "ms_per_step": round(sec / job["steps"] * 1e3, 2),
+                            "value": round(job["bytes_per_element"] * job["S"] * job["steps"] / sec / 1e9, 3),
+                            "unit": "GB/s"}
+    main = per["c4"]
+    cpu = {"value": main["value"], "unit": "GB/s", "cores": cores, "cpu_model": model, "kind": "oracle",
+           "sample": f"the whole {S:,}-element shard (2e9-parameter set, rank 0 of 8): 4 bf16 micro-steps summed "
+                     "in fp32 + norm/clip + AdamW + bf16 round-out, numpy fp32 exact-order oracle, 2 timed steps "
+                     f"after 1 untimed, one process per core ({cores}) each stepping a 1/{cores} slice, the slices' "
+                     "sums of squares added every step",
+           "per_config": per}
+    ns_t0 = time.perf_counter()
+    ns = ns_oracle_rates()
+    cpu_ns = {"value": ns["c5_4096"]["tflops"], "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
+              "kind": "oracle",
+              "sample": "fp64 Newton-Schulz (5 steps) on one whole 4096x4096 stress matrix, numpy with the host's "
+                        f"threaded BLAS ({time.perf_counter() - ns_t0:.1f} s for all the sets below)",
+              "per_config": ns}
+    return cpu, cpu_ns
 
 
 def run_reference(args, rank: int) -> None:
-    """The oracle as it stands, on the host's cores: `--warmup` untimed then `--steps` timed steps,
-    each one pass of the AdamW-part sample and one Newton-Schulz sample call; rank 0 only."""
+    """The oracle as it stands, on the host's cores: `--warmup` untimed then `--steps` timed steps.
+    A step is the AdamW part over the whole 2e9-parameter shard on every core (the processes add
+    their slices' sums of squares each step) and one fp64 Newton-Schulz call on a whole 4096 x 4096
+    stress matrix (numpy's threaded BLAS); rank 0 only."""
     if rank != 0:
         return
-    a, x = OracleAdamwSample(), OracleNsSample()
+    import numpy as np
+    import torch
+
+    import workloads
+    from oracle.ns import newton_schulz
+
+    job = adamw_job("c4", args.steps, args.warmup)
+    if args.ref_elements > 0:  # a shorter prefix of the shard (quick checks of the line)
+        job["S"] = min(job["S"], args.ref_elements)
+    ta = adamw_oracle_on_all_cores([job])[0]
+    nsz = args.ref_ns_size
+    x = workloads.ns_input(nsz, nsz, 5, 1, dtype=torch.bfloat16, frobenius_normalise=True)\
+        .float().numpy().astype(np.float64)
     for _ in range(args.warmup):
-        a.step()
-        x.step()
-    ta = tn = 0.0
+        newton_schulz(x, steps=5)
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        t0 = time.perf_counter()
-        a.step()
-        t1 = time.perf_counter()
-        x.step()
-        t2 = time.perf_counter()
-        ta += t1 - t0
-        tn += t2 - t1
+        newton_schulz(x, steps=5)
+    tn = time.perf_counter() - t0
     K = args.steps
-    value = round(a.bytes * K / ta / 1e9, 3)
-    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    S = job["S"]
+    value = round(job["bytes_per_element"] * S * K / ta / 1e9, 3)
+    cores, model = os.cpu_count(), cpu_model()
+    cpu = {"value": value, "unit": "GB/s", "cores": cores, "cpu_model": model, "kind": "oracle",
            "sample": f"{K} timed steps after {args.warmup} warm-up steps; each step: the AdamW-part oracle "
-                     f"(4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out) over {a.n:,} shard "
-                     f"elements ({ta / K * 1e3:.1f} ms, numpy, one core) and one fp64 Newton-Schulz call (5 steps) "
-                     f"on a 256x1024 block of the stress set ({tn / K * 1e3:.1f} ms, numpy's threaded BLAS)"}
-    ns = {"value": round(x.flops * K / tn / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-          "sample": f"{K} timed fp64 Newton-Schulz calls (5 steps) on a 256x1024 block of the stress set, one per "
-                    f"step ({tn:.2f} s)"}
+                     f"(4-micro-step fp32 accumulation + norm/clip + AdamW + bf16 round-out) over the whole {S:,}-"
+                     f"element shard ({ta / K * 1e3:.1f} ms, numpy, one process per core each stepping a 1/{cores} "
+                     f"slice) and one fp64 Newton-Schulz call (5 steps) on a whole {nsz}x{nsz} stress matrix "
+                     f"({tn / K * 1e3:.1f} ms, numpy's threaded BLAS)"}
+    fl = ns_flops(nsz, nsz, 5)
+    ns = {"value": round(fl * K / tn / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
+          "kind": "oracle",
+          "sample": f"{K} timed fp64 Newton-Schulz calls (5 steps) on a whole {nsz}x{nsz} stress matrix ({tn:.2f} s)"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": K, "warmup": args.warmup, "ms_per_step": round((ta + tn) / K * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
-            "adamw_part": {"ms": round(ta / K * 1e3, 3), "bytes_per_element": ACC_BYTES + ADAMW_BYTES,
-                           "elements": a.n},
+            "adamw_part": {"ms": round(ta / K * 1e3, 3), "bytes_per_element": job["bytes_per_element"],
+                           "elements": S},
             "ns": {"value": ns["value"], "unit": "TFLOP/s", "ms_per_step": round(tn / K * 1e3, 3)},
             "cpu_baseline": cpu, "cpu_baseline_ns": ns,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -333,13 +440,14 @@ class NsPart:
 
 
 class MuonPart:
-    """One Muon step over the Muon matrices rank 0 of the 1.1B Llama-style set owns (round-robin,
-    W = 8): 4 x 2048^2, 4 x 2048x512, 4 x 2048x11264, bf16 gradients ~N(0, 1e-3)."""
+    """One Muon step over a parameter set's Muon matrices that rank 0 owns (round-robin by index,
+    the set's W): for the 1.1B Llama-style set (W = 8) 4 x 2048^2, 4 x 2048x512, 4 x 2048x11264;
+    for the GPT-2-small body (W = 1) all 48. bf16 gradients ~N(0, 1e-3), masters ~N(0, 0.02)."""
 
-    def __init__(self, Z, torch, seed: int):
+    def __init__(self, Z, torch, seed: int, which: str = "c3"):
         import workloads
         self.Z = Z
-        w = workloads.get("c3")
+        w = workloads.get(which)
         shapes = {}
         for prm in w.owned_muon():
             shapes[prm.shape] = shapes.get(prm.shape, 0) + 1
@@ -355,12 +463,105 @@ class MuonPart:
         self.flops = sum(ns_flops(r, c, 5) * b for (r, c), b in shapes.items())
         n = sum(r * c * b for (r, c), b in shapes.items())
         self.bytes = 32 * n  # momentum 14 (bf16 grad), statistics 4, update 14 per element
-        self.what = (f"{self.count} matrices {sorted(shapes)} of the 1.1B set owned by rank 0 of 8, "
+        owner = f"owned by rank 0 of {w.world}" if w.world > 1 else "(W = 1)"
+        self.what = (f"{self.count} matrices {sorted(shapes)} of the {which} set {owner}, "
                      "zopt_muon_step_many, 5 Newton-Schulz steps")
-        self.lr = w.lr
+        self.lr = w.muon_lr
 
     def run(self, stream):
         self.Z.muon_step_many(self.jobs, self.ws, lr=self.lr, stream=stream)
+
+
+def config_lines(Z, torch, stream, pk, K: int) -> dict:
+    """The smaller parameter sets, each timed apart (3 untimed then K timed iterations, CUDA
+    events on the launching stream): the tiny decoder (1,048,832-element shard), the GPT-2-small
+    set (38,652,672) and the 1.1B set's rank 0 of 8 (8,200,448) take norm/clip and the AdamW step
+    on a bf16 gradient (30 B/element; the adamw_kernel alone 28 B) with a 256 MB L2 flush between
+    iterations, except the tiny set, which is timed L2-resident and makes no roofline claim; the
+    tiny decoder's and the GPT-2-small body's Newton-Schulz sets, and the GPT-2-small body's Muon
+    step, against the burst bf16 peak (each call lasts about a millisecond)."""
+    import statistics as stats_
+
+    import workloads
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = {}
+    for name in ("c1", "c2", "c3"):
+        w = workloads.get(name)
+        lay = Z.ShardLayout([p.numel for p in w.adamw], [p.decay for p in w.adamw], w.bucket, w.world, w.rank)
+        S = lay.shard_len
+        table = lay.device_table()
+        gen = torch.Generator(device="cuda").manual_seed(w.seed)
+        p = torch.randn(S, device="cuda", generator=gen).mul_(0.02)
+        m, v = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
+        g = torch.randn(S, device="cuda", generator=gen).mul_(1e-3).to(torch.bfloat16)
+        out = torch.empty(S, dtype=torch.int16, device="cuda")
+        clip, state, ws = Z.new_clip_stats(), Z.new_adam_state(), Z.new_norm_workspace(S)
+        resident = name == "c1"
+        evs = [(mk(), mk(), mk()) for _ in range(3 + K)]
+        for i, (e0, e1, e2) in enumerate(evs):
+            if not resident:
+                flush.zero_()
+            e0.record(stream)
+            Z.grad_norm_clip(g, w.max_norm, ws, clip, stream=stream)
+            e1.record(stream)
+            Z.adamw_step(lay, table, p, m, v, g, out, lr=w.lr_at(i % w.steps), beta1=w.beta1, beta2=w.beta2,
+                         eps=w.eps, weight_decay=w.weight_decay, clip_stats=clip, adam_state=state, stream=stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        step_ms = stats_.mean(e0.elapsed_time(e2) for e0, _, e2 in evs[3:])
+        kern_ms = stats_.mean(e1.elapsed_time(e2) for _, e1, e2 in evs[3:])
+        part = BF16_STEP_BYTES * S / (step_ms * 1e-3) / 1e9
+        kern = 28 * S / (kern_ms * 1e-3) / 1e9
+        entry = {"shard_len": S, "world": w.world,
+                 "adamw_part": {"what": "zopt_grad_norm_clip + zopt_adamw_step, bf16 gradient", "ms": round(step_ms, 4),
+                                "bytes_per_element": BF16_STEP_BYTES, "achieved": round(part, 1), "unit": "GB/s"},
+                 "l2": "L2-resident (the whole state fits in L2): no roofline claim" if resident
+                       else "256 MB L2 flush between iterations"}
+        if not resident:
+            entry["adamw_part"]["frac"] = round(part / pk["hbm_gbs"], 4)
+            entry["roofline"] = {"kernel": "adamw_kernel (bf16 gradient)", "bound": "hbm", "achieved": round(kern, 1),
+                                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(kern / pk["hbm_gbs"], 4),
+                                 "bytes_per_element": 28, "avg_launch_ms": round(kern_ms, 4)}
+        else:
+            entry["adamw_kernel"] = {"ms": round(kern_ms, 4), "achieved": round(kern, 1), "unit": "GB/s"}
+        res[name] = entry
+        del p, m, v, g, out, ws
+
+    def timed_calls(run):
+        for _ in range(3):
+            run(stream)
+        torch.cuda.synchronize()
+        evs = [(mk(), mk()) for _ in range(K)]
+        for a, b in evs:
+            a.record(stream)
+            run(stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return stats_.mean(a.elapsed_time(b) for a, b in evs)
+
+    for name in ("c1", "c2"):
+        nsp = NsPart(Z, torch, 9000, 5, 0, name)
+        ms_ = timed_calls(nsp.run)
+        tf = nsp.flops / (ms_ * 1e-3) / 1e12
+        res[name]["ns"] = {"what": f"{sum(G.shape[0] for G, _ in nsp.groups)} bf16 matrices "
+                                   f"{[tuple(G.shape[1:]) for G, _ in nsp.groups]}, one zopt_ns_orthogonalize_many "
+                                   "call, 5 steps", "ms": round(ms_, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
+                           "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
+                           "peak_source": pk["source"] + " bf16 burst"}
+        if name == "c1":
+            res[name]["ns"]["note"] = "the set is 3.4 MB (L2-resident) and latency-bound: no roofline claim"
+        del nsp
+    mu2 = MuonPart(Z, torch, 9100, "c2")
+    ms_ = timed_calls(mu2.run)
+    tf = mu2.flops / (ms_ * 1e-3) / 1e12
+    res["c2"]["muon_step"] = {"what": mu2.what, "ms": round(ms_, 4), "ns_equivalent_tflops": round(tf, 1),
+                              "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
+                              "peak_source": pk["source"] + " bf16 burst",
+                              "note": "the whole step's time against the Newton-Schulz flops alone"}
+    del mu2
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
@@ -521,6 +722,8 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
             b_ev.record(stream)
         torch.cuda.synchronize()
         mu_ms = mean(ev_m)
+    # the smaller parameter sets (tiny decoder, GPT-2-small, the 1.1B set's rank 0), timed apart
+    cfg = config_lines(Z, torch, stream, peaks(), max(K, 3)) if "configs" in parts and rank == 0 else None
     if dist:
         tt = torch.tensor([ms, a_ms, k_ms, n_ms, nr_ms, rs_ms, mu_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -529,19 +732,25 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
 
     # ---- end to end through the public API with host buffers: each part takes its inputs
     # (the micro-step gradients; the Newton-Schulz inputs) from pinned host memory and reads
-    # its results back (the clip stats; the orthogonalised matrices). The accumulation passes
-    # read the pinned micro-step gradients themselves, over the CPU-GPU link (no staging copy);
-    # the Newton-Schulz inputs and outputs move on two copy streams, overlapped with the compute
-    # of the previous or next matrix group. Each part is timed from its first transfer to its
-    # last read-back.
+    # its results back to pinned host memory (the clip stats and the bf16 compute weights; the
+    # orthogonalised matrices). The accumulation passes read the pinned micro-step gradients
+    # themselves, over the CPU-GPU link (no staging copy); the bf16 weights go back on a copy
+    # stream while the next step's accumulation reads its gradients (the link is full duplex),
+    # and a step's AdamW launch waits for the previous read-back of the weights it overwrites.
+    # The Newton-Schulz inputs and outputs move on two copy streams, overlapped with the compute
+    # of the previous or next matrix group. Each part runs its steps back to back and is timed
+    # from its first transfer to its last read-back, divided by the steps (steady state).
     h2d = d2h = 0
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
     if "adamw" in parts:
         micro_host = [mg.cpu().pin_memory() for mg in micro]
         stats_host = torch.empty(Z.CLIP_STATS_BYTES, dtype=torch.uint8).pin_memory()
+        out_host = torch.empty(S, dtype=torch.int16).pin_memory()
+        out_read = ev()
+        out_read.record(stream)
         h2d += 2 * S * MICRO_STEPS
-        d2h += Z.CLIP_STATS_BYTES
+        d2h += Z.CLIP_STATS_BYTES + 2 * S
     if ns is not None:
         ns_host = [(G.cpu().pin_memory(), torch.empty(X.shape, dtype=X.dtype).pin_memory()) for G, X in ns.groups]
         h2d += sum(G.numel() * 2 for G, _ in ns.groups)
@@ -569,57 +778,67 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         out_done = [ev() for _ in chunks]
         for e in ns_done + out_done:
             e.record(stream)
-    e2e_steps = max(2, min(K, 5))
-    ee_a = [(mk(), mk()) for _ in range(e2e_steps)]
-    ee_n = [(mk(), mk()) for _ in range(e2e_steps)]
+    e2e_steps = max(3, min(K, 6))
 
-    def e2e_step(i=None):
-        if "adamw" in parts:
-            start = mk() if i is None else ee_a[i][0]
-            start.record(stream)
-            for k, mh in enumerate(micro_host):
-                Z.grad_accumulate(g, mh, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
-                                  stats=clip, stream=stream)
-            Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
-            stats_host.copy_(clip, non_blocking=True)
-            if i is not None:
-                ee_a[i][1].record(stream)
-        if ns is not None:
-            start = mk() if i is None else ee_n[i][0]
-            start.record(stream)
-            h2d_s.wait_event(start)
-            landed = []
-            for ci, (G, X, hG, hX) in enumerate(chunks):
-                h2d_s.wait_event(ns_done[ci])  # the previous step has read G
-                with torch.cuda.stream(h2d_s):
-                    G.copy_(hG, non_blocking=True)
-                e = ev()
-                e.record(h2d_s)
-                landed.append(e)
-            for ci, (G, X, hG, hX) in enumerate(chunks):
-                stream.wait_event(landed[ci])
-                stream.wait_event(out_done[ci])  # the previous step's X has been read back
-                Z.ns_orthogonalize(G, X, ns.ws_chunk, steps=ns.steps, stream=stream)
-                ns_done[ci].record(stream)
-                d2h_s.wait_event(ns_done[ci])
-                with torch.cuda.stream(d2h_s):
-                    hX.copy_(X, non_blocking=True)
-                out_done[ci].record(d2h_s)
-            for e in out_done:
-                stream.wait_event(e)
-            if i is not None:
-                ee_n[i][1].record(stream)
+    def e2e_adamw_step():
+        for k, mh in enumerate(micro_host):
+            Z.grad_accumulate(g, mh, first=k == 0, last=k == MICRO_STEPS - 1, max_norm=w.max_norm, ws=ws,
+                              stats=clip, stream=stream)
+        stream.wait_event(out_read)  # the previous step's weights have reached the host
+        Z.adamw_step(lay, table, p, m, v, g, out, stream=stream, **kw)
+        stats_host.copy_(clip, non_blocking=True)
+        done = ev()
+        done.record(stream)
+        d2h_s.wait_event(done)
+        with torch.cuda.stream(d2h_s):
+            out_host.copy_(out, non_blocking=True)
+        out_read.record(d2h_s)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    ea_ms = mean(ee_a) if "adamw" in parts else 0.0
-    en_ms = mean(ee_n) if ns is not None else 0.0
+    def e2e_ns_step():
+        start = ev()
+        start.record(stream)
+        h2d_s.wait_event(start)
+        landed = []
+        for ci, (G, X, hG, hX) in enumerate(chunks):
+            h2d_s.wait_event(ns_done[ci])  # the previous step has read G
+            with torch.cuda.stream(h2d_s):
+                G.copy_(hG, non_blocking=True)
+            e = ev()
+            e.record(h2d_s)
+            landed.append(e)
+        for ci, (G, X, hG, hX) in enumerate(chunks):
+            stream.wait_event(landed[ci])
+            stream.wait_event(out_done[ci])  # the previous step's X has been read back
+            Z.ns_orthogonalize(G, X, ns.ws_chunk, steps=ns.steps, stream=stream)
+            ns_done[ci].record(stream)
+            d2h_s.wait_event(ns_done[ci])
+            with torch.cuda.stream(d2h_s):
+                hX.copy_(X, non_blocking=True)
+            out_done[ci].record(d2h_s)
+
+    def e2e_leg(one_step, drain):
+        for _ in range(2):
+            one_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a_ev, b_ev = mk(), mk()
+        a_ev.record(stream)
+        for _ in range(e2e_steps):
+            one_step()
+        for e in drain():
+            stream.wait_event(e)
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        return a_ev.elapsed_time(b_ev) / e2e_steps
+
+    ea_ms = e2e_leg(e2e_adamw_step, lambda: [out_read]) if "adamw" in parts else 0.0
+    e2e_clocks = None
+    en_ms = 0.0
+    if ns is not None:
+        with Clocks(smi_id(local_rank)) as clk2:
+            en_ms = e2e_leg(e2e_ns_step, lambda: out_done)
+        e2e_clocks = clk2.summary()
     if dist:
         tt = torch.tensor([ea_ms, en_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -689,7 +908,8 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     if ns is not None:
         tflops = ns.flops / (n_ms * 1e-3) / 1e12
         line["ns"] = {"value": round(tflops * world_procs, 2), "unit": "TFLOP/s", "ms_per_step": round(n_ms, 3),
-                      "algorithmic_flops_per_step": ns.flops, "host": host_ns}
+                      "algorithmic_flops_per_step": ns.flops, "host": host_ns,
+                      "tflops_per_sm_mhz": round(tflops / clocks["sm_mhz"], 4) if clocks.get("sm_mhz") else None}
         line["roofline"] = {"kernel": ns.kernel, "bound": "tensor",
                             "achieved": round(tflops, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                             "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": None,
@@ -713,16 +933,17 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         e2e.update(value=round(part_bytes * world_procs / (ea_ms * 1e-3) / 1e9, 2), unit="GB/s",
                    adamw_part_ms=round(ea_ms, 3))
     if ns is not None:
-        e2e.update(ns_value=round(ns.flops * world_procs / (en_ms * 1e-3) / 1e12, 2), ns_unit="TFLOP/s",
-                   ns_part_ms=round(en_ms, 3))
+        etf = ns.flops / (en_ms * 1e-3) / 1e12
+        e2e.update(ns_value=round(etf * world_procs, 2), ns_unit="TFLOP/s", ns_part_ms=round(en_ms, 3),
+                   ns_clocks=e2e_clocks,
+                   ns_tflops_per_sm_mhz=round(etf / e2e_clocks["sm_mhz"], 4) if e2e_clocks.get("sm_mhz") else None)
     line["e2e"] = e2e
+    if cfg is not None:
+        line["configs"] = cfg
     line["gpu_launches"] = K * ((MICRO_STEPS + 1 if "adamw" in parts else 0) + (ns.launches if ns else 0))
     if rank == 0:
         if world_procs == 1 and not args.no_cpu_baseline:
-            if "adamw" in parts:
-                line["cpu_baseline"] = cpu_oracle_run(seconds=10.0)
-            if ns is not None:
-                line["cpu_baseline_ns"] = cpu_oracle_ns(seconds=6.0)
+            line["cpu_baseline"], line["cpu_baseline_ns"] = cpu_baselines()
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -737,12 +958,17 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prequeue-ms", type=float, default=50.0,
                     help="device-side delay (about this many ms at 2 GHz) queued before the timed steps")
-    ap.add_argument("--parts", default="adamw,ns,muon",
-                    help="comma list: adamw, ns (the timed step), muon (a Muon step timed apart)")
+    ap.add_argument("--parts", default="adamw,ns,muon,configs",
+                    help="comma list: adamw, ns (the timed step), muon (a Muon step timed apart), configs (the "
+                         "smaller parameter sets timed apart)")
     ap.add_argument("--ns-set", default="stress", choices=["stress", "gpt2"],
                     help="Newton-Schulz matrices: the 48-matrix 4096-wide stress set, or the GPT-2-small body's 48")
     ap.add_argument("--ns-count", type=int, default=0,
                     help="matrices per Newton-Schulz shape (profiling captures); 0 = the full set of 16")
+    ap.add_argument("--ref-elements", type=int, default=0,
+                    help="reference arm: step only this many shard elements (quick checks); 0 = the whole shard")
+    ap.add_argument("--ref-ns-size", type=int, default=4096,
+                    help="reference arm: side of the square stress matrix its Newton-Schulz calls take")
     ap.add_argument("--shard-len", type=int, default=0,
                     help="time a shorter prefix of the shard (profiling captures); 0 = the whole shard")
     args = ap.parse_args()

@@ -15,7 +15,8 @@ def run_bench(*args, timeout=300):
 
 
 def test_reference_arm_line():
-    r = run_bench("--impl", "reference", "--steps", "3", "--warmup", "3")
+    r = run_bench("--impl", "reference", "--steps", "3", "--warmup", "3", "--ref-elements", "4000000",
+                  "--ref-ns-size", "512")
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -28,7 +29,8 @@ def test_reference_arm_line():
     assert d["ms_per_step"] > 0 and d["ns"]["value"] > 0  # K timed steps of the sample, averaged
     assert isinstance(d["config"]["workload"], str) and d["value"] > 0
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == os.cpu_count() and cb["value"] == d["value"] and cb["sample"]
+    assert cb["cpu_model"] and d["adamw_part"]["elements"] == 4_000_000
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
