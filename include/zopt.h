@@ -324,14 +324,18 @@ typedef struct zopt_ns_job {
  * rounded up to 1 KiB, summed. */
 ZOPT_API size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs);
 /* Orthogonalise every matrix of every job: `steps` quintic steps with coefficients abc and
- * eps as for zopt_ns_orthogonalize, bf16 compute. Each result is bitwise the one
- * zopt_ns_orthogonalize gives with a workspace that holds the job's whole batch. Jobs whose
- * shorter side is below 1024 and whose output rows are 16-byte aligned run in one persistent
- * launch per six jobs, the products of each step interleaved across jobs (one job's waits for
- * its previous product are filled by the other jobs' tiles); those of 1024 and above run each
- * product of a step in one launch for up to four jobs (their tiles filling each other's
- * waves); any other job runs product by product. The inputs of all jobs are normalised in
- * three launches before any product.
+ * eps as for zopt_ns_orthogonalize, bf16 compute. Jobs whose shorter side m is 1024 and above
+ * run each product of a step in one launch of the CTA-pair kernel for up to four jobs (their
+ * tiles filling each other's waves); when the call has such jobs, jobs with 512 <= m < 1024
+ * join those launches too (their tiles fill the large jobs' last waves instead of running in a
+ * launch of their own). The other jobs whose output rows are 16-byte aligned run in one
+ * persistent launch per six jobs, the products of each step interleaved across jobs (one job's
+ * waits for its previous product are filled by the other jobs' tiles); any other job runs
+ * product by product. The inputs of all jobs are normalised in three launches before any
+ * product. A tile is computed the same way in any launch of its kind, so each result is
+ * bitwise the one zopt_ns_orthogonalize gives with a workspace that holds the job's whole
+ * batch, except for a job with 512 <= m < 1024 in a call with CTA-pair jobs: that result is
+ * bitwise the same in every such call (and within the bf16 tolerance of the single call's).
  * jobs is read during the call only; d_ws (16-byte aligned) is owned by the call until the
  * stream passes it. Same errors as zopt_ns_orthogonalize. */
 ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
@@ -428,10 +432,12 @@ typedef struct zopt_muon_job {
 /* Workspace bytes for zopt_muon_step_many over these jobs (0 if a job is empty or has more than
  * 65535 matrices). */
 ZOPT_API size_t zopt_muon_workspace_many(const zopt_muon_job* jobs, int32_t n_jobs);
-/* One Muon step for every matrix of every job with the same hyper-parameters: each job's results
- * (master, momentum, bf16 weights, stats) are bitwise what zopt_muon_step gives with a workspace
- * that holds the job's whole batch; the Newton-Schulz part of all jobs is one
- * zopt_ns_orthogonalize_many call. jobs is read during the call only. Same errors as
+/* One Muon step for every matrix of every job with the same hyper-parameters: the Newton-Schulz
+ * part of all jobs is one zopt_ns_orthogonalize_many call, so each job's results (master,
+ * momentum, bf16 weights, stats) are bitwise what zopt_muon_step gives with a workspace that
+ * holds the job's whole batch, with that call's one exception (a job with 512 <= min(rows, cols)
+ * < 1024 beside a job with both sides 1024 and above: the momentum is still bitwise, the
+ * update rides the CTA-pair launches). jobs is read during the call only. Same errors as
  * zopt_muon_step. */
 ZOPT_API zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_jobs, const zopt_muon_hparams* hparams,
                                          void* d_ws, size_t ws_bytes, zopt_stream stream);

@@ -22,8 +22,9 @@
 // Where the work runs: ns_prep.cu normalises and orients the inputs of every job in three
 // launches; below m = 1024 every product of every step runs in one persistent launch of
 // ns_fused_kernel (ns_fused.cu), several shapes at once; from m = 1024 each product of a step is
-// one launch of the CTA-pair GEMM for up to four shapes, and where an output or the
-// coefficients rule the fused kernel out, one launch of the single-CTA GEMM (ns_gemm.cu). The
+// one launch of the CTA-pair GEMM for up to four shapes (in a call that has such shapes, those
+// from m = 512 join them), and where an output or the coefficients rule the fused kernel out,
+// one launch of the single-CTA GEMM (ns_gemm.cu). The
 // tile geometry and the epilogue building blocks they share are in ns_tile.cuh. Every wait is
 // bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
 #include <cstring>
@@ -263,6 +264,9 @@ int pair_job(const Group& G, const Coef& k, int prod, bool last, int cur, int* e
   J.D = last ? G.mo_e : G.mx_e[cur ^ 1];
   return (!last || G.out_tma) ? kEpiTma : kEpiRegs;
 }
+
+// The smallest m that joins the CTA-pair launches of a call that has them anyway.
+constexpr long long kPairRideMin = 512;
 
 // The steps of several CTA-pair groups (bf16 compute), each product of a step one launch for
 // all of them (kMaxPairJobs groups to a launch, those with the same epilogue together): the
@@ -531,6 +535,14 @@ extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32
     if ((st = group_init(Gr, p, static_cast<uint8_t*>(d_ws) + at)) != ZOPT_OK) return st;
     at += static_cast<size_t>(round_up(static_cast<long long>(p.total), 1024));
   }
+  // When the call has CTA-pair jobs, jobs with kPairRideMin <= m < 1024 ride their launches: one
+  // launch per product of a step then covers them too, their tiles filling the large jobs' last
+  // waves, instead of a fused launch of their own that would run alone after (or before) them.
+  bool any_pair = false;
+  for (const Group& Gr : groups) any_pair = any_pair || (Gr.pair && !Gr.f32c);
+  if (any_pair)
+    for (Group& Gr : groups)
+      if (!Gr.f32c && Gr.p.m >= kPairRideMin) Gr.pair = true;
   if ((st = group_prep(groups.data(), n_jobs, eps, s)) != ZOPT_OK) return st;
   FusedMaps fm;
   FusedArgs fa{};
