@@ -8,29 +8,33 @@
 //
 // Four steps on the caller's stream, each one launch for every job of a call (for a single
 // shape: per group of matrices, as many as the workspace holds):
-//   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 14-16 B/elem)
-//   2. U = NewtonSchulz(u) through zopt_ns_orthogonalize (fp32 in/out, bf16 tensor cores)
-//   3. per matrix: partial sums of squares and largest magnitudes of U     (4 B/elem)
-//   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (14 B/elem);
+//   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 14-16 B/elem);
+//      each block also sums its share of u^2 into the Newton-Schulz norm's partial sums, so
+//      the normalisation does not read u a second time
+//   2. U = NewtonSchulz(u): fp32 u in, bf16 tensor cores, U written in bf16 (the bf16 method
+//      rounds every product, its last one included, to bf16)
+//   3. per matrix: partial sums of squares and largest magnitudes of U     (2 B/elem)
+//   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (12 B/elem);
 //      each block first reduces its matrix's partials in a fixed order (no atomics, no memset)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <memory>
 #include <string>
 #include <vector>
 
 #include "internal.h"
 #include "norm_impl.cuh"
+#include "ns_internal.h"
 
 namespace zopt {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxBlocksPerMat = 512;
-constexpr long long kChunk = 32768;  // elements per block of the element-wise kernels
 constexpr int kMaxItems = 8;         // jobs per element-wise launch
-constexpr long long kMaxCallElems = 1LL << 46;  // elements of one shape's batch (2^31 blocks of kChunk)
+constexpr long long kMaxCallElems = 1LL << 46;  // elements of one shape's batch
 // per matrix: one fp64 partial sum of squares and one max |U| bit pattern per block
 constexpr size_t kRedBytes = (sizeof(double) + sizeof(unsigned)) * kMaxBlocksPerMat;
 
@@ -40,15 +44,16 @@ struct MuonPlan {
   size_t off_u, off_o, off_ns, ns_bytes, total;
 };
 
-// Workspace of `group` matrices: the reduction area (kRedBytes per matrix), u and U (fp32), then
-// the Newton-Schulz workspace.
+// Workspace of `group` matrices: the reduction area (kRedBytes per matrix), u (fp32) and U
+// (bf16), then the Newton-Schulz workspace.
 MuonPlan muon_plan(long long rows, long long cols, long long group) {
   MuonPlan p;
   const long long n = rows * cols;
   p.off_u = static_cast<size_t>(round_up(group * static_cast<long long>(kRedBytes), 1024));
   p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 4, 1024));
-  p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 4, 1024));
-  p.ns_bytes = zopt_ns_workspace(rows, cols, static_cast<int32_t>(group), ZOPT_BF16);
+  p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 2, 1024));
+  p.ns_bytes = static_cast<size_t>(
+      round_up(static_cast<long long>(zopt_ns_workspace(rows, cols, static_cast<int32_t>(group), ZOPT_BF16)), 1024));
   p.total = p.off_ns + p.ns_bytes;
   return p;
 }
@@ -58,15 +63,17 @@ struct MuonItem {
   float* master;
   float* momentum;
   const void* grad;
-  float* u_in;          // momentum's output, Newton-Schulz's input
-  const float* u_out;   // Newton-Schulz's output U
+  float* u_in;              // momentum's output, Newton-Schulz's input
+  const uint16_t* u_out;    // Newton-Schulz's output U (bf16)
+  double* npart;            // the Newton-Schulz norm partials of matrix 0; matrix b's at + b * npart_stride
+  long long npart_stride;
   uint16_t* out;        // bf16 round-out (may be null)
   zopt_muon_stats* stats;
   uint8_t* red;         // reduction area: per matrix kMaxBlocksPerMat fp64 sums, then as many maxima
   long long n;          // elements per matrix
   long long u0;         // blocks of the launch before this job
   int batch;
-  int bpm;              // statistics / update blocks per matrix (depends on n only)
+  int bpm;              // blocks per matrix of every pass (the norm's partial count: depends on n only)
   int out8;             // the bf16 output allows 8-byte stores
   float decay, step, sqrt_min;
 };
@@ -90,48 +97,75 @@ __device__ __forceinline__ float4 fma4_momentum(float mu, const float4& b, const
                      __fadd_rn(__fmul_rn(mu, b.z), g.z), __fadd_rn(__fmul_rn(mu, b.w), g.w));
 }
 
-// Step 1: block u takes chunk u - u0 (kChunk elements) of its job's batch, which is contiguous;
-// threads move 4-element vectors, two in flight; the batch's n*batch % 4 last elements go to
-// the job's last chunk element by element.
+// Step 1: block u takes part c = (u - u0) % bpm of matrix mb = (u - u0) / bpm of its job; threads
+// stride over the matrix's 4-element vectors with stride bpm * 256, four vectors' loads in flight
+// per round; the matrix's n % 4 last elements go to part 0 element by element. The block's sum of
+// u^2 (fp32 pairwise over runs of 8, exact fp64 outside the safe range, the runs in fp64) is the
+// matrix's norm partial c, which the Newton-Schulz normalisation reads in place of u.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
+  __shared__ double red[32];
   const MuonItem& J = L.it[item_of(L, blockIdx.x)];
-  const long long c = static_cast<long long>(blockIdx.x) - J.u0;
-  const long long total = J.n * J.batch, e0 = c * kChunk;
-  const long long e1 = e0 + kChunk < total ? e0 + kChunk : total;
-  const T* g = static_cast<const T*>(J.grad);
-  float4* b4 = reinterpret_cast<float4*>(J.momentum);
-  float4* u4 = reinterpret_cast<float4*>(J.u_in);
+  const long long v = static_cast<long long>(blockIdx.x) - J.u0;
+  const long long mb = v / J.bpm, c = v - mb * J.bpm;
+  const long long n = J.n;
+  const T* g = static_cast<const T*>(J.grad) + mb * n;
+  float* buf = J.momentum + mb * n;
+  float* u = J.u_in + mb * n;
+  float4* b4 = reinterpret_cast<float4*>(buf);
+  float4* u4 = reinterpret_cast<float4*>(u);
   const float mu = L.mu;
-  const long long v1 = e1 / 4;  // whole vectors of the chunk (e0 is a multiple of 4)
-  long long j = e0 / 4 + threadIdx.x;
-  for (; j + kThreads < v1; j += 2 * kThreads) {  // two vectors' loads in flight before any store
-    const float4 ga = load4(g + 4 * j), gb = load4(g + 4 * (j + kThreads));
-    const float4 ba = b4[j], bb = b4[j + kThreads];
-    const float4 na = fma4_momentum(mu, ba, ga), nb = fma4_momentum(mu, bb, gb);
-    b4[j] = na;
-    b4[j + kThreads] = nb;
-    u4[j] = L.nesterov ? fma4_momentum(mu, na, ga) : na;  // g + mu*buf, as the same two roundings
-    u4[j + kThreads] = L.nesterov ? fma4_momentum(mu, nb, gb) : nb;
+  const int64_t n4 = n / 4;
+  const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
+  double acc = 0.0;
+  int64_t j = c * blockDim.x + threadIdx.x;
+  for (; j + 3 * stride < n4; j += 4 * stride) {  // four vectors' loads in flight before any store
+    float4 gv[4], bv[4], uv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      gv[k] = load4(g + 4 * (j + k * stride));
+      bv[k] = b4[j + k * stride];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 nb = fma4_momentum(mu, bv[k], gv[k]);
+      b4[j + k * stride] = nb;
+      uv[k] = L.nesterov ? fma4_momentum(mu, nb, gv[k]) : nb;  // g + mu*buf, as the same two roundings
+      u4[j + k * stride] = uv[k];
+    }
+    acc = __dadd_rn(acc, sumsq44(uv[0], uv[1]));
+    acc = __dadd_rn(acc, sumsq44(uv[2], uv[3]));
   }
-  for (; j < v1; j += kThreads) {
+  for (; j < n4; j += stride) {
     const float4 gv = load4(g + 4 * j);
-    const float4 b = fma4_momentum(mu, b4[j], gv);
-    b4[j] = b;
-    u4[j] = L.nesterov ? fma4_momentum(mu, b, gv) : b;
+    const float4 nb = fma4_momentum(mu, b4[j], gv);
+    b4[j] = nb;
+    const float4 uv = L.nesterov ? fma4_momentum(mu, nb, gv) : nb;
+    u4[j] = uv;
+    acc = __dadd_rn(acc, sumsq44(uv, make_float4(0.f, 0.f, 0.f, 0.f)));
   }
-  if (e1 == total && threadIdx.x == 0) {
-    for (long long k = v1 * 4; k < total; ++k) {
+  if (c == 0 && threadIdx.x == 0) {
+    for (int64_t k = n4 * 4; k < n; ++k) {
       const float gv = load1(g + k);
-      const float b = __fadd_rn(__fmul_rn(mu, J.momentum[k]), gv);
-      J.momentum[k] = b;
-      J.u_in[k] = L.nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
+      const float b = __fadd_rn(__fmul_rn(mu, buf[k]), gv);
+      buf[k] = b;
+      const float x = L.nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
+      u[k] = x;
+      acc = __dadd_rn(acc, __dmul_rn(static_cast<double>(x), static_cast<double>(x)));
     }
   }
+  const double block = block_sum(acc, red);
+  if (threadIdx.x == 0 && J.npart != nullptr) J.npart[mb * J.npart_stride + c] = block;
 }
 
+__device__ __forceinline__ float4 bf16x4(const uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float bf16x1(const uint16_t h) { return __uint_as_float(static_cast<unsigned>(h) << 16); }
+
 // Step 3: block u is block c = (u - u0) % bpm of matrix mb = (u - u0) / bpm; threads stride over
-// the matrix's 4-element vectors with stride bpm * 256, 8 loads (128 bytes) in flight per round;
+// the matrix's 4-element bf16 vectors with stride bpm * 256, 8 loads (64 bytes) in flight per round;
 // squares are summed in fp32 over runs of 32 (sumsq32: exact fp64 outside the safe range) and
 // the runs in fp64. The block's sum and its max |U| (the fp32 bit patterns of non-negative
 // values order as unsigned integers; NaN sorts above inf) go to slot c of the matrix's area.
@@ -142,7 +176,8 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const MuonList L) {
   const long long v = static_cast<long long>(blockIdx.x) - J.u0;
   const long long mb = v / J.bpm, c = v - mb * J.bpm;
   const long long n = J.n;
-  const float* U = J.u_out + mb * n;
+  const uint16_t* U = J.u_out + mb * n;
+  const uint2* U4 = reinterpret_cast<const uint2*>(U);
   const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
   double acc = 0.0;
@@ -154,8 +189,11 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const MuonList L) {
   int64_t j = c * blockDim.x + threadIdx.x;
   for (; j + 7 * stride < n4; j += 8 * stride) {
     float4 x[8];
+    uint2 w[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = __ldg(reinterpret_cast<const float4*>(U) + j + k * stride);
+    for (int k = 0; k < 8; ++k) w[k] = __ldg(U4 + j + k * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = bf16x4(w[k]);
     float r[4][8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -166,13 +204,13 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const MuonList L) {
     acc = __dadd_rn(acc, sumsq32(r[0], r[1], r[2], r[3]));
   }
   for (; j < n4; j += stride) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(U) + j);
+    const float4 x = bf16x4(__ldg(U4 + j));
     acc = __dadd_rn(acc, sumsq44(x, make_float4(0.f, 0.f, 0.f, 0.f)));
     mx = amax(mx, x);
   }
   if (c == 0 && threadIdx.x == 0) {
     for (int64_t k = n4 * 4; k < n; ++k) {
-      const float x = U[k];
+      const float x = bf16x1(U[k]);
       acc = __dadd_rn(acc, __dmul_rn(static_cast<double>(x), static_cast<double>(x)));
       mx = max(mx, __float_as_uint(x) & 0x7FFFFFFFu);
     }
@@ -229,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
   __syncthreads();
   const bool rejected = !(__uint_as_float(s_max) <= L.guard);
   float* p = J.master + mb * n;
-  const float* U = J.u_out + mb * n;
+  const uint16_t* U = J.u_out + mb * n;
   uint16_t* out = J.out ? J.out + mb * n : nullptr;
   const float decay = J.decay, step = J.step;
   auto one = [&](float x, float u) { return __fsub_rn(__fmul_rn(x, decay), __fmul_rn(step, u)); };
@@ -248,12 +286,12 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
   const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
   float4* p4 = reinterpret_cast<float4*>(p);
-  const float4* U4 = reinterpret_cast<const float4*>(U);
+  const uint2* U4 = reinterpret_cast<const uint2*>(U);
   int64_t j = c * blockDim.x + threadIdx.x;
   for (; j + stride < n4; j += 2 * stride) {
     float4 x = p4[j], y = p4[j + stride];
     if (!rejected) {
-      const float4 ux = __ldg(U4 + j), uy = __ldg(U4 + j + stride);
+      const float4 ux = bf16x4(__ldg(U4 + j)), uy = bf16x4(__ldg(U4 + j + stride));
       x = make_float4(one(x.x, ux.x), one(x.y, ux.y), one(x.z, ux.z), one(x.w, ux.w));
       y = make_float4(one(y.x, uy.x), one(y.y, uy.y), one(y.z, uy.z), one(y.w, uy.w));
       p4[j] = x;
@@ -267,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
   for (; j < n4; j += stride) {
     float4 x = p4[j];
     if (!rejected) {
-      const float4 ux = __ldg(U4 + j);
+      const float4 ux = bf16x4(__ldg(U4 + j));
       x = make_float4(one(x.x, ux.x), one(x.y, ux.y), one(x.z, ux.z), one(x.w, ux.w));
       p4[j] = x;
     }
@@ -277,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
     for (int64_t k = n4 * 4; k < n; ++k) {
       float x = p[k];
       if (!rejected) {
-        x = one(x, U[k]);
+        x = one(x, bf16x1(U[k]));
         p[k] = x;
       }
       if (out) out[k] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -304,7 +342,7 @@ zopt_status check_job(const char* fn, const Job& j) {
   if (j.rows < 1 || j.cols < 1 || j.batch < 1) return fail(ZOPT_EINVAL, f + ": empty matrix or batch");
   if (j.rows > ZOPT_NS_MAX_DIM || j.cols > ZOPT_NS_MAX_DIM || j.rows * j.cols > ZOPT_NS_MAX_ELEMS)
     return fail(ZOPT_EINVAL, f + ": a dimension above 2^30 or a matrix above 2^36 elements");
-  if (j.batch > kMaxCallElems / (j.rows * j.cols))  // the element-wise grids: one block per kChunk elements
+  if (j.batch > kMaxCallElems / (j.rows * j.cols))
     return fail(ZOPT_EINVAL, f + ": the batch holds more than 2^46 elements");
   if (!aligned16(j.master) || !aligned16(j.momentum) || !aligned16(j.grad) ||
       (j.out != nullptr && (reinterpret_cast<uintptr_t>(j.out) & 1u) != 0) ||
@@ -337,14 +375,17 @@ MuonItem item_of_job(const Job& j, long long b0, int gs, uint8_t* ws, const Muon
   it.momentum = j.momentum + b0 * n;
   it.grad = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
   it.u_in = reinterpret_cast<float*>(ws + P.off_u);
-  it.u_out = reinterpret_cast<const float*>(ws + P.off_o);
+  it.u_out = reinterpret_cast<const uint16_t*>(ws + P.off_o);
+  it.npart = nullptr;  // set once the Newton-Schulz workspace is known
+  it.npart_stride = 0;
   it.out = j.out ? j.out + b0 * n : nullptr;
   it.stats = j.stats + b0;
   it.red = ws;
   it.n = n;
   it.batch = gs;
-  long long bpm = (n + kChunk - 1) / kChunk;  // depends on n only: a matrix's stats are the same in any call
-  it.bpm = static_cast<int>(bpm < 1 ? 1 : (bpm > kMaxBlocksPerMat ? kMaxBlocksPerMat : bpm));
+  // depends on n only (a matrix's stats are the same in any call), and equals the Newton-Schulz
+  // norm's partial count, which the momentum pass fills
+  it.bpm = ns::norm_blocks(n);
   // 8-byte bf16 stores need the first matrix 8-byte aligned and every matrix a multiple of 4
   it.out8 = it.out != nullptr && (reinterpret_cast<uintptr_t>(it.out) & 7u) == 0 && (n & 3) == 0 ? 1 : 0;
   it.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
@@ -384,8 +425,7 @@ zopt_status launch_pass(Pass pass, const std::vector<MuonItem>& items, const std
     if (L.n == kMaxItems && (st = flush()) != ZOPT_OK) return st;
     MuonItem it = items[k];
     it.u0 = units;
-    units += (pass == kMomentumBf16 || pass == kMomentumF32) ? (it.n * it.batch + kChunk - 1) / kChunk
-                                                             : static_cast<long long>(it.batch) * it.bpm;
+    units += static_cast<long long>(it.batch) * it.bpm;
     L.it[L.n++] = it;
   }
   return flush();
@@ -408,8 +448,9 @@ Job job_of(const zopt_muon_job& b) {
              b.rows, b.cols, b.batch, b.d_stats};
 }
 
-// The Newton-Schulz job of a Muon job: u -> U, fp32 in and out, contiguous matrices.
-zopt_ns_job ns_job_of(const Job& j, const float* U_in, float* U_out) {
+// The Newton-Schulz job of a Muon job: fp32 u -> U (written in bf16: see muon_ns), contiguous
+// matrices.
+zopt_ns_job ns_job_of(const Job& j, const float* U_in, uint16_t* U_out) {
   const long long n = j.rows * j.cols;
   zopt_ns_job q;
   q.G = U_in;
@@ -423,6 +464,30 @@ zopt_ns_job ns_job_of(const Job& j, const float* U_in, float* U_out) {
   q.batch = static_cast<int32_t>(j.batch);
   q.io_dtype = ZOPT_F32;
   return q;
+}
+
+// Points each item's momentum pass at its Newton-Schulz job's norm partials (ns[] in the
+// Newton-Schulz workspace nws), which the pass fills in place of a sum-of-squares launch.
+void attach_norm_partials(const std::vector<zopt_ns_job>& ns, uint8_t* nws, std::vector<MuonItem>& items) {
+  std::vector<double*> base(ns.size());
+  std::vector<long long> stride(ns.size());
+  ns::many_norm_partials(ns.data(), static_cast<int32_t>(ns.size()), nws, base.data(), stride.data());
+  for (size_t k = 0; k < ns.size(); ++k) {
+    items[k].npart = base[k];
+    items[k].npart_stride = stride[k];
+  }
+}
+
+// Step 2: U = NewtonSchulz(u) for every job in one many-call, its norms taken from the partials
+// the momentum pass wrote and U written in bf16.
+zopt_status muon_ns(const char* fn, const std::vector<zopt_ns_job>& ns, const zopt_muon_hparams* hp, uint8_t* nws,
+                    size_t nws_bytes, cudaStream_t s) {
+  const size_t n = ns.size();
+  const std::vector<zopt_dtype> out(n, ZOPT_BF16);
+  std::unique_ptr<bool[]> ready(new bool[n]);
+  for (size_t k = 0; k < n; ++k) ready[k] = true;
+  return ns::orthogonalize_many(fn, ns.data(), static_cast<int32_t>(n), hp->ns_steps, hp->abc, hp->eps, nws, nws_bytes,
+                                s, out.data(), ready.get());
 }
 
 }  // namespace
@@ -459,21 +524,22 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
   const MuonPlan P = muon_plan(rows, cols, group);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   float* U_in = reinterpret_cast<float*>(ws + P.off_u);
-  float* U_out = reinterpret_cast<float*>(ws + P.off_o);
+  uint16_t* U_out = reinterpret_cast<uint16_t*>(ws + P.off_o);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_muon_step: no CUDA device");
-  const long long n = rows * cols;
   const std::vector<zopt_dtype> gdt{grad_dtype};
   for (long long b0 = 0; b0 < batch; b0 += group) {
     const int gs = static_cast<int>(batch - b0 < group ? batch - b0 : group);
-    const std::vector<MuonItem> items{item_of_job(j, b0, gs, ws, P, hp)};
-    // 1. momentum over the group's matrices (contiguous), u into the workspace
+    std::vector<MuonItem> items{item_of_job(j, b0, gs, ws, P, hp)};
+    Job jg = j;
+    jg.batch = gs;
+    const std::vector<zopt_ns_job> ns{ns_job_of(jg, U_in, U_out)};
+    attach_norm_partials(ns, ws + P.off_ns, items);
+    // 1. momentum over the group's matrices (contiguous), u and its norm partials into the workspace
     if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
-    // 2. U = NewtonSchulz(u), fp32 in and out, bf16 tensor cores
-    st = zopt_ns_orthogonalize(U_in, U_out, ZOPT_F32, rows, cols, cols, cols, n, n, gs, ZOPT_BF16, hp->ns_steps,
-                               hp->abc, hp->eps, ws + P.off_ns, P.ns_bytes, stream);
-    if (st != ZOPT_OK) return st;
+    // 2. U = NewtonSchulz(u), fp32 in, bf16 out, bf16 tensor cores
+    if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s)) != ZOPT_OK) return st;
     // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
     if ((st = launch_update(items, gdt, hp, s)) != ZOPT_OK) return st;
   }
@@ -530,12 +596,11 @@ extern "C" zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_
     items[static_cast<size_t>(k)] = item_of_job(j, 0, static_cast<int>(j.batch), ws + at, P, hp);
     gdt[static_cast<size_t>(k)] = j.gdt;
     ns[static_cast<size_t>(k)] = ns_job_of(j, items[static_cast<size_t>(k)].u_in,
-                                           const_cast<float*>(items[static_cast<size_t>(k)].u_out));
+                                           const_cast<uint16_t*>(items[static_cast<size_t>(k)].u_out));
     at += static_cast<size_t>(round_up(static_cast<long long>(P.off_ns), 1024));
   }
+  attach_norm_partials(ns, ws + at, items);
   if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
-  if ((st = zopt_ns_orthogonalize_many(ns.data(), n_jobs, hp->ns_steps, hp->abc, hp->eps, ws + at, ws_bytes - at,
-                                       stream)) != ZOPT_OK)
-    return st;
+  if ((st = muon_ns(fn, ns, hp, ws + at, ws_bytes - at, s)) != ZOPT_OK) return st;
   return launch_update(items, gdt, hp, s);
 }

@@ -147,6 +147,7 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
   G.p = p;
   G.es = G.f32c ? 4 : 2;
   G.esz = G.io == ZOPT_F32 ? 4 : 2;
+  G.osz = G.out_io == ZOPT_F32 ? 4 : 2;
   G.transpose = G.rows > G.cols;
   G.pair = p.m >= 1024;
   G.ws = ws;
@@ -159,9 +160,9 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
   G.mat_elems = static_cast<long long>(p.per_mat) / G.es;
   // the last product writes the caller's X through the TMA (32 x 32 boxes, transposed for a
   // tall matrix) when the TMA can address it: 16-byte aligned rows and matrices
-  const long long esz = static_cast<long long>(G.esz);
-  G.out_tma = !G.f32c && (reinterpret_cast<uintptr_t>(G.xo) & 15u) == 0 && (G.ld_x * esz) % 16 == 0 &&
-              (G.gs == 1 || (G.bs_x * esz) % 16 == 0);
+  const long long osz = static_cast<long long>(G.osz);
+  G.out_tma = !G.f32c && (reinterpret_cast<uintptr_t>(G.xo) & 15u) == 0 && (G.ld_x * osz) % 16 == 0 &&
+              (G.gs == 1 || (G.bs_x * osz) % 16 == 0);
   if (G.f32c) return ok();
   const long long mb = static_cast<long long>(p.per_mat), grp = p.group;
   for (int q = 0; q < 2; ++q) {
@@ -178,8 +179,8 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
   if ((st = make_map(&G.mb_e, G.B, p.m, p.m, p.lda, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
   if (G.out_tma) {
     const long long xrows = G.transpose ? p.n : p.m, xcols = G.transpose ? p.m : p.n;  // the caller's shape
-    const long long ob = (G.gs == 1 ? xrows * G.ld_x : G.bs_x) * esz;
-    const bool of32 = G.io == ZOPT_F32;
+    const long long ob = (G.gs == 1 ? xrows * G.ld_x : G.bs_x) * osz;
+    const bool of32 = G.out_io == ZOPT_F32;
     if ((st = make_map(&G.mo_e, G.xo, xcols, xrows, G.ld_x, G.gs, ob, 32, 32,
                        of32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, of32)) != ZOPT_OK)
       return st;
@@ -220,7 +221,7 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
   px = g0;
   px.M = mm; px.N = n; px.K = mm; px.b_mn_major = 1;
   job.prod[3] = px;  // the last step's, into the caller's X
-  job.prod[3].d_f32 = G.io == ZOPT_F32 ? 1 : 0;
+  job.prod[3].d_f32 = G.out_io == ZOPT_F32 ? 1 : 0;
   job.prod[3].d_trans = G.transpose ? 1 : 0;
   job.prep = G.ws;
 }
@@ -257,7 +258,7 @@ int pair_job(const Group& G, const Coef& k, int prod, bool last, int cur, int* e
   a.D = last ? static_cast<void*>(G.xo) : static_cast<void*>(G.xb[cur ^ 1]);
   a.ldd = last ? G.ld_x : G.p.ldx;
   a.d_stride = last ? G.bs_x : mat_elems;
-  a.d_f32 = last && G.io == ZOPT_F32 ? 1 : 0;
+  a.d_f32 = last && G.out_io == ZOPT_F32 ? 1 : 0;
   a.d_trans = last && G.transpose ? 1 : 0;
   J.P = G.mb_p;
   J.Q = J.R = G.mx_mn[cur];
@@ -311,7 +312,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
     void* xnext = last ? static_cast<void*>(G.xo) : static_cast<void*>(G.xb[cur ^ 1]);
     const long long ldnext = last ? G.ld_x : p.ldx;
     const long long dstr_next = last ? G.bs_x : mat_elems;
-    const int next_f32 = last ? (G.io == ZOPT_F32 ? 1 : 0) : (G.f32c ? 1 : 0);
+    const int next_f32 = last ? (G.out_io == ZOPT_F32 ? 1 : 0) : (G.f32c ? 1 : 0);
     const int next_trans = last && G.transpose ? 1 : 0;
     if (G.f32c) {
       float* X0 = reinterpret_cast<float*>(G.xb[cur]);
@@ -454,6 +455,8 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     Gr.g = static_cast<const uint8_t*>(G) + static_cast<size_t>(g0i) * batch_stride_g * esz;
     Gr.xo = static_cast<uint8_t*>(X) + static_cast<size_t>(g0i) * batch_stride_x * esz;
     Gr.io = io_dtype;
+    Gr.out_io = io_dtype;
+    Gr.norm_ready = false;
     Gr.rows = rows; Gr.cols = cols; Gr.ld_g = ld_g; Gr.ld_x = ld_x; Gr.bs_g = batch_stride_g; Gr.bs_x = batch_stride_x;
     Gr.gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
     Gr.f32c = f32c;
@@ -489,33 +492,51 @@ extern "C" size_t zopt_ns_workspace_many(const zopt_ns_job* jobs, int32_t n_jobs
   return total;
 }
 
-extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
-                                                  const float* abc, float eps, void* d_ws, size_t ws_bytes,
-                                                  zopt_stream stream) {
-  using namespace zopt;
-  using namespace zopt::ns;
-  const char* fn = "zopt_ns_orthogonalize_many";
-  if (jobs == nullptr || d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: NULL pointer");
-  if (n_jobs < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: no jobs");
-  if (steps < 1) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: steps < 1");
+namespace zopt {
+namespace ns {
+
+int norm_blocks(long long n) {
+  const long long bpm = (n + kSumsqElems - 1) / kSumsqElems;
+  return static_cast<int>(bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm));
+}
+
+void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, double** base, long long* stride_doubles) {
+  size_t at = 0;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const zopt_ns_job& b = jobs[j];
+    // a group's prep scratch opens its workspace slice: matrix b's NormWorkspace at b * kPrepWsBytes
+    base[j] = reinterpret_cast<double*>(static_cast<uint8_t*>(d_ws) + at + offsetof(NormWorkspace, partials));
+    stride_doubles[j] = static_cast<long long>(kPrepWsBytes / sizeof(double));
+    at += static_cast<size_t>(round_up(static_cast<long long>(plan(b.rows, b.cols, 2, b.batch).total), 1024));
+  }
+}
+
+zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
+                               const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
+                               const zopt_dtype* out_io, const bool* norm_ready) {
+  const std::string f(fn);
+  if (jobs == nullptr || d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, f + ": NULL pointer");
+  if (n_jobs < 1) return fail(ZOPT_EINVAL, f + ": no jobs");
+  if (steps < 1) return fail(ZOPT_EINVAL, f + ": steps < 1");
   if (!std::isfinite(abc[0]) || !std::isfinite(abc[1]) || !std::isfinite(abc[2]) || !std::isfinite(eps) || eps < 0)
-    return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: coefficients and eps must be finite (eps >= 0)");
-  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: workspace is not 16-byte aligned");
+    return fail(ZOPT_EINVAL, f + ": coefficients and eps must be finite (eps >= 0)");
+  if (!aligned16(d_ws)) return fail(ZOPT_EINVAL, f + ": workspace is not 16-byte aligned");
   zopt_status st = ZOPT_OK;
   for (int32_t j = 0; j < n_jobs; ++j) {
     const zopt_ns_job& b = jobs[j];
     if ((st = check_job(fn, b.G, b.X, static_cast<zopt_dtype>(b.io_dtype), b.rows, b.cols, b.ld_g, b.ld_x,
                         b.batch_stride_g, b.batch_stride_x, b.batch)) != ZOPT_OK)
       return st;
-    if (b.batch > 65535) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: a job's batch exceeds 65535");
+    if (b.batch > 65535) return fail(ZOPT_EINVAL, f + ": a job's batch exceeds 65535");
+    if (out_io != nullptr && out_io[j] != ZOPT_F32 && out_io[j] != ZOPT_BF16)
+      return fail(ZOPT_EUNSUPPORTED, f + ": output dtype must be fp32 or bf16");
   }
   const size_t need = zopt_ns_workspace_many(jobs, n_jobs);
-  if (need == 0 || ws_bytes < need) return fail(ZOPT_EINVAL, "zopt_ns_orthogonalize_many: workspace smaller than zopt_ns_workspace_many");
+  if (need == 0 || ws_bytes < need) return fail(ZOPT_EINVAL, f + ": workspace smaller than zopt_ns_workspace_many");
   int* err_dev = nullptr;
   if ((st = take_error_word(fn, &err_dev)) != ZOPT_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = sm_count();
-  if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_ns_orthogonalize_many: no CUDA device");
+  if (sms <= 0) return fail(ZOPT_ECUDA, f + ": no CUDA device");
   const Coef k = coef_of(abc);
   // every job's whole batch is one group in its own slice of the workspace; all normalise first,
   // then the fusable jobs go kMaxFusedJobs to a launch and the others run product by product
@@ -527,6 +548,8 @@ extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32
     Gr.g = static_cast<const uint8_t*>(b.G);
     Gr.xo = static_cast<uint8_t*>(b.X);
     Gr.io = static_cast<zopt_dtype>(b.io_dtype);
+    Gr.out_io = out_io != nullptr ? out_io[j] : Gr.io;
+    Gr.norm_ready = norm_ready != nullptr && norm_ready[j];
     Gr.rows = b.rows; Gr.cols = b.cols; Gr.ld_g = b.ld_g; Gr.ld_x = b.ld_x;
     Gr.bs_g = b.batch_stride_g; Gr.bs_x = b.batch_stride_x;
     Gr.gs = b.batch;
@@ -573,6 +596,16 @@ extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32
     if (!group_fusable(Gr, k) && !Gr.pair && (st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) return st;
   }
   return ok();
+}
+
+}  // namespace ns
+}  // namespace zopt
+
+extern "C" zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
+                                                  const float* abc, float eps, void* d_ws, size_t ws_bytes,
+                                                  zopt_stream stream) {
+  return zopt::ns::orthogonalize_many("zopt_ns_orthogonalize_many", jobs, n_jobs, steps, abc, eps, d_ws, ws_bytes,
+                                      reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr);
 }
 
 namespace zopt {

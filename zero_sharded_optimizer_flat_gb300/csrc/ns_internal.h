@@ -1,5 +1,6 @@
-// Internal interface between the Newton-Schulz orchestration (ns.cu) and its fp32 product
-// kernel (ns_simt.cu). Not part of the ABI.
+// Internal interfaces of the Newton-Schulz code: between its orchestration (ns.cu) and its fp32
+// product kernel (ns_simt.cu), and the many-call options the Muon step (muon.cu) uses. Not part
+// of the ABI.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -34,6 +35,22 @@ struct GemmF32Args {
 };
 
 zopt_status launch_gemm_f32(const GemmF32Args& a, cudaStream_t stream);
+
+// zopt_ns_orthogonalize_many with two per-job options for callers inside the library (null: the
+// entry point's behaviour): out_io[j], the dtype job j's X is written in (its G keeps io_dtype);
+// norm_ready[j], job j's matrices' norm partials are already in the workspace (see
+// many_norm_partials), so the sum-of-squares launch skips them.
+zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
+                               const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
+                               const zopt_dtype* out_io, const bool* norm_ready);
+
+// Where job j of a many-call keeps its matrices' norm partials in the workspace d_ws: matrix b's
+// blocks' fp64 sums of squares at base[j] + b * stride_doubles, norm_blocks(rows * cols) of them
+// (the normalising kernels add them in index order).
+void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, double** base, long long* stride_doubles);
+// Norm partial sums a matrix of n elements takes: ceil(n / kSumsqElems), at least 1, at most
+// kPrepBlocks (a function of n only, so a matrix's norm is the same in any call).
+int norm_blocks(long long n);
 
 }  // namespace ns
 }  // namespace zopt

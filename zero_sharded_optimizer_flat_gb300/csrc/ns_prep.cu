@@ -15,7 +15,6 @@ namespace ns {
 // Every matrix of a list of groups (one launch for all of them): blockIdx.y is the matrix's
 // index across the list, the item it belongs to found by its `first` index.
 constexpr int kMaxPrepItems = 16;
-constexpr long long kSumsqElems = 32768;  // elements per sum-of-squares block (before the cap)
 constexpr int kScaleVecs = 4096;          // 8-element vectors per scaling block (16 per thread)
 
 struct PrepItem {
@@ -409,6 +408,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
     const bool t_in = (G.io == ZOPT_F32) == std::is_same<T, float>::value;
     const bool u_out = G.f32c == std::is_same<U, float>::value;
     if (!t_in || (K != 0 && !u_out) || (K == 1 && G.transpose) || (K == 2 && !G.transpose)) continue;
+    if (K == 0 && G.norm_ready) continue;  // its partials are already in the scratch
     if (L.n == kMaxPrepItems || matrices + G.gs > 65535) {
       if ((st = launch_list<K, T, U>(L, matrices, max_x, s)) != ZOPT_OK) return st;
       matrices = 0;
@@ -432,8 +432,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
     it.tvec = rows16 ? 1 : 0;
     // blocks per matrix depend on the matrix size only, so a matrix's sum (and so its result)
     // is bitwise the same whatever group or list it runs in
-    long long bpm = ceil_div(rows * cols, kSumsqElems);
-    bpm = bpm < 1 ? 1 : (bpm > kPrepBlocks ? kPrepBlocks : bpm);
+    const long long bpm = norm_blocks(rows * cols);
     it.bpm = static_cast<int>(bpm);
     if (K == 0) it.chunks = bpm;
     else if (K == 1) it.chunks = it.vec ? ceil_div(rows * (cols / 8), kScaleVecs) : ceil_div(rows * cols, 8LL * kScaleVecs);

@@ -505,6 +505,7 @@ __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, 
 
 // Per-matrix reduction scratch: an arrival counter and up to kPrepBlocks fp64 partials.
 constexpr int kPrepBlocks = 512;
+constexpr long long kSumsqElems = 32768;  // elements per sum-of-squares block (before the cap)
 constexpr size_t kPrepWsBytes = 256 + sizeof(double) * kPrepBlocks;
 
 __device__ __forceinline__ NormWorkspace* prep_ws(uint8_t* base, int mb) {
@@ -648,12 +649,14 @@ zopt_status launch_fused(const FusedMaps& maps, FusedArgs f, cudaStream_t stream
 struct Group {
   const uint8_t* g;  // the group's first input and output matrix
   uint8_t* xo;
-  zopt_dtype io;
+  zopt_dtype io;      // the input's dtype
+  zopt_dtype out_io;  // the output's dtype
+  bool norm_ready;    // the matrices' norm partials are already in the prep scratch
   long long rows, cols, ld_g, ld_x, bs_g, bs_x;
   int gs;
   bool f32c, transpose, pair, out_tma;
   long long es, mat_elems;
-  size_t esz;
+  size_t esz, osz;  // input and output element sizes
   Plan p;
   uint8_t* ws;  // prep scratch of the group (its matrices' counters live there)
   zopt_clip_stats* stats;
@@ -663,6 +666,7 @@ struct Group {
 
 // X0 = G / (||G||_F + eps), oriented, for every matrix of n groups (a handful of launches in all).
 zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s);
+
 
 }  // namespace ns
 }  // namespace zopt
