@@ -284,13 +284,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S2 * kHalf;
   uint8_t* sEpi = sB + S2 * kHalf;  // the TMA epilogue's boxes
-  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + epi_bytes(kEpi));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + epi_bytes2(kEpi));
   uint64_t* empty = full + S2;
   uint64_t* tfull = empty + S2;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* rbar = drain + 1;  // kEpiTmaR: one R barrier per epilogue warp
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(rbar + 4);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 5);
   float* stage_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,13 +308,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(tempty + b, 256);  // the epilogue threads of both CTAs (used in the leader)
     }
     tc::mbar_init(drain, 1);
-    if (kEpi == kEpiTmaR)
-      for (int q = 0; q < 4; ++q) tc::mbar_init(rbar + q, 1);
     tc::fence_mbar_init();
     for (int j = 0; j < B.n; ++j) {
       tc::prefetch_tmap(&B.job[j].P);
       tc::prefetch_tmap(&B.job[j].Q);
-      if (kEpi == kEpiTmaR) tc::prefetch_tmap(&B.job[j].R);
       if (kTma) tc::prefetch_tmap(&B.job[j].D);
     }
   }
@@ -420,60 +416,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if constexpr (kTma) {
     // ------------------------------------------------------- epilogue through the TMA (warps 2..5)
     const int quad = warp & 3;
-    uint8_t* mine = sEpi + quad * (epi_bytes(kEpi) / 4);
-    uint64_t* rb = rbar + quad;
+    uint8_t* mine = sEpi + quad * (epi_bytes2(kEpi) / 4);
     const uint32_t tempty_leader[2] = {tc::map_to_rank(tc::smem_u32(tempty), 0),
                                        tc::map_to_rank(tc::smem_u32(tempty + 1), 0)};
     const int rows0 = static_cast<int>(rank) * 128 + 32 * quad;  // this warp's rows within a tile
     auto has_r = [](const GemmArgs& a) { return kEpi == kEpiTmaR && a.beta != 0.0f; };
-    // issues tile t's R slice (when its job has one) on rb; warp-uniform result
-    auto load_r = [&](int t) -> bool {
-      const int j = pair_job_of(B, t);
-      if (!has_r(B.job[j].a)) return false;
-      int mb, tp, tj;
-      tile_coords2(B.job[j].a, t - B.start[j], mb, tp, tj);
-      int l = 0;
-      if (lane == 0) l = epi_load_r(B.job[j].a, &B.job[j].R, mine, rb, mb, tp * BM2 + rows0, tj) ? 1 : 0;
-      return __shfl_sync(0xFFFFFFFFu, l, 0) != 0;
+    // kEpiTmaR: R's piece for the first block the warp writes in tile t, loaded from L2 into
+    // registers before the tile's accumulator is ready (while its MMAs still run)
+    uint4 r0[4];
+    auto first_r = [&](int t) {
+      if constexpr (kEpi == kEpiTmaR) {
+        const int j = pair_job_of(B, t);
+        const GemmArgs& a = B.job[j].a;
+        if (!has_r(a)) return;
+        int mb, tp, tj;
+        tile_coords2(a, t - B.start[j], mb, tp, tj);
+        prefetch_r_first(a, mb, tp * BM2 + rows0, tj, lane, r0);
+      }
     };
-    bool rpend = false;  // (warp-uniform) R boxes of the current tile are in flight on rb
-    uint32_t rph = 0;
     int last_par = -1;
     int t = pair;
-    if (t < total) rpend = load_r(t);
+    if (t < total) first_r(t);
     for (int it = 0; t < total; t += npairs, ++it) {
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, err) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-      if (rpend) {  // every lane waits, so that each sees the TMA's writes
-        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, err) ? 1 : 0)) break;
-        rph ^= 1u;
-        rpend = false;
-      }
       tc::fence_after_sync();
       const int j = pair_job_of(B, t);
       const GemmArgs& a = B.job[j].a;
       int mb, tp, tj;
       tile_coords2(a, t - B.start[j], mb, tp, tj);
-      epi_tile_tma<kEpi == kEpiTmaR>(a, &B.job[j].D, mine,
-                                     tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
-                                     tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par);
+      epi_tile_tma<false, 2, kEpi == kEpiTmaR>(
+          a, &B.job[j].D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
+          tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par, 0, BN / 32, r0);
       tc::fence_before_sync();
       tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
-      const int tn = t + npairs;
-      if (tn < total && has_r(B.job[pair_job_of(B, tn)].a)) {
-        // the slice is free once the TMA has read it: then prefetch the next tile's R
-        if (lane == 0) tc::bulk_wait_read<0>();
-        __syncwarp();
-        rpend = load_r(tn);
-      }
+      if (t + npairs < total) first_r(t + npairs);
     }
-    if (lane == 0) {
-      tc::bulk_wait_all();                  // every store has reached global memory
-      if (rpend) mbar_wait_drain(rb, rph);  // (after a failed wait) no load left in flight
-    }
+    if (lane == 0) tc::bulk_wait_all();  // every store has reached global memory
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)

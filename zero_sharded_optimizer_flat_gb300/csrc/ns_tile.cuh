@@ -348,23 +348,84 @@ __device__ __forceinline__ bool epi_load_r(const GemmArgs& a, const CUtensorMap*
   return true;
 }
 
+// The first block c >= c of the warp's part of a tile that it writes (neither outside the matrix
+// nor below the diagonal), or c_end.
+__device__ __forceinline__ int next_written_block(const GemmArgs& a, int i0, int tj, int c, int c_end) {
+  for (; c < c_end; ++c) {
+    const int k = block_kind(a, i0, tj * BN + 32 * c);
+    if (k != 0 && k != 4) break;
+  }
+  return c;
+}
+
+// Lane `lane`'s 32 bf16 values of R (matrix base Rm) at row i0 + lane, columns j0 .. j0 + 31,
+// zero outside the M x N matrix as a TMA load would fill them: four 16-byte loads from L2 when
+// the whole row piece lies inside the matrix, element by element otherwise.
+__device__ __forceinline__ void load_r_piece(const GemmArgs& a, const __nv_bfloat16* Rm, int i0, int j0, int lane,
+                                             uint4 (&r)[4]) {
+  const int i = i0 + lane;
+  const __nv_bfloat16* row = Rm + static_cast<long long>(i) * a.ldr;
+  if (i < a.M && j0 + 32 <= a.N) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + j0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r[q] = __ldg(p + q);
+    return;
+  }
+  uint32_t w[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+    const int c0 = j0 + 2 * h;
+    const uint32_t lo = (i < a.M && c0 < a.N) ? __bfloat16_as_ushort(row[c0]) : 0u;
+    const uint32_t hi = (i < a.M && c0 + 1 < a.N) ? __bfloat16_as_ushort(row[c0 + 1]) : 0u;
+    w[h] = lo | (hi << 16);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Loads, into r, R's piece for the first block the warp writes in tile column block tj of
+// matrix mb (kRegR epilogues prefetch it before the tile's accumulator is ready).
+__device__ __forceinline__ void prefetch_r_first(const GemmArgs& a, int mb, int i0, int tj, int lane, uint4 (&r)[4]) {
+  const int c = next_written_block(a, i0, tj, 0, BN / 32);
+  if (c < BN / 32) load_r_piece(a, a.R + mb * a.r_stride, i0, tj * BN + 32 * c, lane, r);
+}
+
 // One epilogue warp's part of a tile through the TMA: its 32 TMEM lanes (rows i0 .. i0 + 31)
 // x 256 columns from taddr (tile column block tj of matrix mb) become alpha * acc + beta * R +
 // diag on the diagonal, handed to the TMA as 32 x 32 boxes. kSlice: R sits in the warp's eight
 // slice boxes at `mine` (D is written over it) and two mirror boxes follow; otherwise `mine`
 // holds four boxes, a D and a mirror box for even blocks and another pair for odd ones (an
-// fp32 box takes a pair). last_par: parity of the last block whose boxes went to the TMA.
+// fp32 box takes a pair). kRegR: R comes through registers instead (rfirst holds the piece of
+// the first block written, as prefetch_r_first loads it; each block loads the next one's while
+// it is processed). last_par: parity of the last block whose boxes went to the TMA.
 // Blocks c_begin .. c_end - 1 of the tile; with one pair of boxes (kPairs == 1) every block
 // reuses the same D and mirror box.
-template <bool kSlice, int kPairs = 2>
+template <bool kSlice, int kPairs = 2, bool kRegR = false>
 __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
                                              int i0, int tj, int mb, bool has_r, int lane, int& last_par,
-                                             int c_begin = 0, int c_end = BN / 32) {
+                                             int c_begin = 0, int c_end = BN / 32, const uint4* rfirst = nullptr) {
+  uint4 rc[4];  // kRegR: R's piece for the block being processed
+  const __nv_bfloat16* Rm = nullptr;
+  if constexpr (kRegR) {
+    if (has_r) {
+      Rm = a.R + mb * a.r_stride;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rc[q] = rfirst[q];
+    }
+  }
 #pragma unroll 1
   for (int c = c_begin; c < c_end; ++c) {
     const int j0 = tj * BN + 32 * c;
     const int kind = block_kind(a, i0, j0);
     if (kind == 0 || kind == 4) continue;
+    uint4 rn[4];  // kRegR: the next written block's piece, loaded while this block is processed
+    int cn = c_end;
+    if constexpr (kRegR) {
+      if (has_r) {
+        cn = next_written_block(a, i0, tj, c + 1, c_end);
+        if (cn < c_end) load_r_piece(a, Rm, i0, tj * BN + 32 * cn, lane, rn);
+      }
+    }
     uint32_t v[32];
     tc::tmem_ld32(taddr + static_cast<uint32_t>(32 * c), v);
     tc::tmem_wait_ld();
@@ -374,16 +435,22 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
     const int par = kPairs == 2 ? (c & 1) : 0;
     uint8_t* dbox = kSlice ? mine + c * kBox : mine + 2 * par * kBox;
     uint8_t* mbox = kSlice ? mine + (8 + par) * kBox : dbox + kBox;
-    if (kSlice && has_r) {
+    if ((kSlice || kRegR) && has_r) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(dbox + box_piece(lane, q));
+        const uint4 u = kRegR ? rc[q] : *reinterpret_cast<const uint4*>(dbox + box_piece(lane, q));
         const uint32_t x[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           o[8 * q + 2 * h] += a.beta * __uint_as_float(x[h] << 16);
           o[8 * q + 2 * h + 1] += a.beta * __uint_as_float(x[h] & 0xFFFF0000u);
         }
+      }
+    }
+    if constexpr (kRegR) {
+      if (has_r && cn < c_end) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rc[q] = rn[q];
       }
     }
     if (a.diag != 0.0f && j0 == i0) {
@@ -449,13 +516,15 @@ __device__ __forceinline__ void init_identity(uint8_t* ident, float h1, float h2
 
 // ---------------------------------------------------------------------- CTA-pair tiles
 
-// The epilogues are the single-CTA kernel's: each CTA drains its own 128 rows of the tile.
-// With R prefetched (kEpiTmaR) the ring keeps four stages, otherwise six.
+// The epilogues are the single-CTA kernel's: each CTA drains its own 128 rows of the tile, except
+// that kEpiTmaR reads R from global memory (L2) into registers, a block ahead, rather than
+// staging a 64 KiB slice in shared memory: every product keeps the six-stage ring.
 constexpr int BM2 = 256, STAGES2 = 6;
 constexpr int kHalf = 128 * BK * 2;  // 16 KiB: 128 rows (or columns) of a 64-deep k-block
-__host__ __device__ constexpr int stages2_of(int e) { return e == kEpiTmaR ? 4 : STAGES2; }
+__host__ __device__ constexpr int stages2_of(int) { return STAGES2; }
+__host__ __device__ constexpr int epi_bytes2(int e) { return e == kEpiRegs ? 0 : 4 * 4 * kBox; }
 constexpr int smem_bytes2(int e) {
-  return stages2_of(e) * 2 * kHalf + epi_bytes(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0);
+  return stages2_of(e) * 2 * kHalf + epi_bytes2(e) + 1024 + 256 + (e == kEpiRegs ? kStageBytes : 0);
 }
 static_assert(smem_bytes2(kEpiTma) <= 232448 && smem_bytes2(kEpiTmaR) <= 232448, "shared memory per CTA");
 
