@@ -73,19 +73,26 @@ __global__ void __launch_bounds__(kNormThreads) accum_kernel(float* __restrict__
   if (kLast) finish_sumsq(ss, ws, stats, max_norm);
 }
 
+template <typename K>
+int resident_blocks(K kernel) {
+  int o = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kNormThreads, 0) != cudaSuccess || o < 1) o = 1;
+  return o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+}
+
 template <typename T, bool kFirst, bool kLast, bool kTwo>
 zopt_status launch(float* acc, const void* g, const void* g2, int64_t n, float max_norm, NormWorkspace* ws,
                    zopt_clip_stats* stats, cudaStream_t s) {
-  // The grid decides how the sum of squares is split over threads and blocks. A two-part pass
-  // takes the grid of the single-part kernel that would run the last of its two parts
-  // (kFirst false), so its stats are bit for bit those of two zopt_grad_accumulate calls.
+  // The grid decides how the sum of squares is split over threads and blocks, so every pass that
+  // produces the stats (kLast) runs on one grid: a wave of whichever of the single-part and
+  // two-part last kernels holds fewer blocks per SM. A two-part last pass is then bit for bit
+  // the single-part calls it replaces, and neither kernel runs its grid in more than one wave.
+  // A pass without stats runs on a wave of its own kernel.
   const int occ = once([] {
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, accum_kernel<T, kTwo ? false : kFirst, kLast, false>,
-                                                      kNormThreads, 0) != cudaSuccess ||
-        o < 1)
-      o = 1;
-    return o < kNormBlocksPerSm ? o : kNormBlocksPerSm;
+    if (!kLast) return resident_blocks(accum_kernel<T, kFirst, kLast, kTwo>);
+    const int one = resident_blocks(accum_kernel<T, false, true, false>);
+    const int two = resident_blocks(accum_kernel<T, false, true, true>);
+    return one < two ? one : two;
   });
   const int sms = sm_count();
   if (sms <= 0) return fail(ZOPT_ECUDA, "zopt_grad_accumulate: no CUDA device");
