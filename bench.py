@@ -41,6 +41,12 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 # reported as null)
 ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
 ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
+# DRAM bytes of one zopt_ns_orthogonalize_many call over the 48-matrix stress set (dram__bytes_read.sum
+# + dram__bytes_write.sum summed over its 18 launches, one ncu pass on the full set), valid while
+# the Newton-Schulz sources hash to NS_SRC_DIGEST
+NS_SOURCES = ("ns.cu", "ns_gemm.cu", "ns_prep.cu", "ns_tile.cuh", "tc.cuh", "launch.cuh", "norm_impl.cuh")
+NS_TRAFFIC_PER_CALL = 181589232640 + 41426764544
+NS_SRC_DIGEST = "d7bd010827aff21e"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 # two parts to a pass: the first pair reads 2 x 2 and writes 4; each later pair also reads the sum
@@ -127,15 +133,29 @@ def smi_id(local_rank: int) -> str:
     return str(local_rank)
 
 
+def source_digest(files) -> str:
+    """The first 16 hex digits of the sha256 of the named kernel sources, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "zero_sharded_optimizer_flat_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def adamw_traffic(S: int):
     """DRAM bytes per adamw_kernel launch over S elements from the committed ncu capture, or
     None if the kernel's sources changed since."""
-    import hashlib
-    h = hashlib.sha256()
-    for f in ("adamw.cu", "adam_common.cuh", "internal.h", "launch.cuh"):
-        with open(os.path.join(ROOT, "zero_sharded_optimizer_flat_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return round(ADAMW_TRAFFIC_PER_ELEM * S) if h.hexdigest()[:16] == ADAMW_SRC_DIGEST else None
+    ok = source_digest(("adamw.cu", "adam_common.cuh", "internal.h", "launch.cuh")) == ADAMW_SRC_DIGEST
+    return round(ADAMW_TRAFFIC_PER_ELEM * S) if ok else None
+
+
+def ns_traffic(ns) -> int | None:
+    """DRAM bytes of one Newton-Schulz call over the whole 48-matrix stress set from the committed
+    ncu capture (all 18 launches), or None for another set or if the kernels' sources changed."""
+    if ns is None or ns.which != "c5" or sum(G.shape[0] for G, _ in ns.groups) != 48:
+        return None
+    return NS_TRAFFIC_PER_CALL if source_digest(NS_SOURCES) == NS_SRC_DIGEST else None
 
 
 def ns_flops(rows: int, cols: int, steps: int) -> float:
@@ -387,7 +407,7 @@ class NsPart:
 
     def __init__(self, Z, torch, seed: int, steps: int, count_limit: int = 0, which: str = "c5"):
         import workloads
-        self.Z, self.steps = Z, steps
+        self.Z, self.steps, self.which = Z, steps, which
         w = workloads.get(which)
         shapes = []
         for prm in w.muon:
@@ -912,7 +932,8 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
                       "tflops_per_sm_mhz": round(tflops / clocks["sm_mhz"], 4) if clocks.get("sm_mhz") else None}
         line["roofline"] = {"kernel": ns.kernel, "bound": "tensor",
                             "achieved": round(tflops, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                            "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                            "frac": round(tflops / pk["bf16_tflops_sustained"], 4), "traffic": ns_traffic(ns),
+                            "traffic_note": "DRAM bytes of one call (all its launches), from an ncu capture",
                             "peak_source": pk["source"] + " bf16 sustained (the GEMMs run for ~100 ms per step)",
                             "note": "achieved = algorithmic flops of the Newton-Schulz calls / their event time "
                                     "(includes the small normalise/orient kernels)"}

@@ -448,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const GemmArgs& a = B.job[j].a;
       int mb, tp, tj;
       tile_coords2(a, t - B.start[j], mb, tp, tj);
-      epi_tile_tma<false, 2, kEpi == kEpiTmaR>(
+      epi_tile_tma<false, 2, kEpi == kEpiTmaR, true>(
           a, &B.job[j].D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
           tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par, 0, BN / 32, r0);
       tc::fence_before_sync();

@@ -399,8 +399,10 @@ __device__ __forceinline__ void prefetch_r_first(const GemmArgs& a, int mb, int 
 // the first block written, as prefetch_r_first loads it; each block loads the next one's while
 // it is processed). last_par: parity of the last block whose boxes went to the TMA.
 // Blocks c_begin .. c_end - 1 of the tile; with one pair of boxes (kPairs == 1) every block
-// reuses the same D and mirror box.
-template <bool kSlice, int kPairs = 2, bool kRegR = false>
+// reuses the same D and mirror box. kStreamOut: the product is read by a later launch, not by
+// this one, so its stores mark their L2 lines to be evicted first, ahead of the operands that
+// this launch's other tiles still read.
+template <bool kSlice, int kPairs = 2, bool kRegR = false, bool kStreamOut = false>
 __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
                                              int i0, int tj, int mb, bool has_r, int lane, int& last_par,
                                              int c_begin = 0, int c_end = BN / 32, const uint4* rfirst = nullptr) {
@@ -485,11 +487,16 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (a.d_trans)  // D[i, j] goes to row j, column i of the caller's matrix
-        tc::tma_store_3d(tmD, dbox, i0, j0, mb);
-      else
-        tc::tma_store_3d(tmD, dbox, j0, i0, mb);
-      if (kind == 2) tc::tma_store_3d(tmD, mbox, i0, j0, mb);
+      // D[i, j] goes to row j, column i of the caller's matrix when a.d_trans
+      const int x0 = a.d_trans ? i0 : j0, x1 = a.d_trans ? j0 : i0;
+      if constexpr (kStreamOut) {
+        const uint64_t pol = tc::l2_evict_first();
+        tc::tma_store_3d_hint(tmD, dbox, x0, x1, mb, pol);
+        if (kind == 2) tc::tma_store_3d_hint(tmD, mbox, i0, j0, mb, pol);
+      } else {
+        tc::tma_store_3d(tmD, dbox, x0, x1, mb);
+        if (kind == 2) tc::tma_store_3d(tmD, mbox, i0, j0, mb);
+      }
       tc::bulk_commit();
     }
     last_par = par;
