@@ -482,7 +482,7 @@ class MuonPart:
         self.count = sum(shapes.values())
         self.flops = sum(ns_flops(r, c, 5) * b for (r, c), b in shapes.items())
         n = sum(r * c * b for (r, c), b in shapes.items())
-        self.bytes = 32 * n  # momentum 14 (bf16 grad), statistics 4, update 14 per element
+        self.bytes = 28 * n  # momentum 14 (bf16 grad), statistics 2 and update 12 (bf16 U) per element
         owner = f"owned by rank 0 of {w.world}" if w.world > 1 else "(W = 1)"
         self.what = (f"{self.count} matrices {sorted(shapes)} of the {which} set {owner}, "
                      "zopt_muon_step_many, 5 Newton-Schulz steps")
