@@ -373,7 +373,8 @@ ZOPT_API zopt_status zopt_selftest_div_by_const(float c, unsigned long long* d_m
  * divergence guard on the largest |U| element.
  *
  * Per matrix, each operation rounded to fp32 as written:
- *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(u) (bf16 compute);
+ *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(u) (bf16 compute,
+ *   U the method's bf16 result; ||u|| summed by the momentum pass itself);
  *   unless max|U| > guard (or not finite): p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U;
  *   out = bf16_rne(p).  A rejected matrix keeps its master; its momentum is still updated.
  * ====================================================================================== */
@@ -400,7 +401,7 @@ typedef struct zopt_muon_stats {
 } zopt_muon_stats; /* 16 bytes per matrix, device resident */
 
 /* Workspace bytes to step `group` rows x cols matrices together (the Newton-Schulz workspace
- * plus two fp32 matrices per group member; 0 for a shape beyond the ZOPT_NS_MAX_* limits). A
+ * plus, per group member, u in fp32 and U in bf16; 0 for a shape beyond the ZOPT_NS_MAX_* limits). A
  * call steps its batch in groups of as many matrices as the workspace holds. */
 ZOPT_API size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group);
 /* One Muon step of `batch` rows x cols matrices stored back to back (matrix b at offset

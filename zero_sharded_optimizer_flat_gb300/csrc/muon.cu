@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxBlocksPerMat = 512;
+static_assert(kMaxBlocksPerMat >= ns::kNormPartialsMax, "a matrix's statistics blocks are its norm blocks");
 constexpr int kMaxItems = 8;         // jobs per element-wise launch
 constexpr long long kMaxCallElems = 1LL << 46;  // elements of one shape's batch
 // per matrix: one fp64 partial sum of squares and one max |U| bit pattern per block

@@ -48,8 +48,9 @@ zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t 
 // blocks' fp64 sums of squares at base[j] + b * stride_doubles, norm_blocks(rows * cols) of them
 // (the normalising kernels add them in index order).
 void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, double** base, long long* stride_doubles);
-// Norm partial sums a matrix of n elements takes: ceil(n / kSumsqElems), at least 1, at most
-// kPrepBlocks (a function of n only, so a matrix's norm is the same in any call).
+// Norm partial sums a matrix of n elements takes: ceil(n / 32768), at least 1, at most
+// kNormPartialsMax (a function of n only, so a matrix's norm is the same in any call).
+constexpr int kNormPartialsMax = 512;
 int norm_blocks(long long n);
 
 }  // namespace ns

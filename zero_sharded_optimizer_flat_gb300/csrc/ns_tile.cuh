@@ -580,7 +580,7 @@ __device__ __forceinline__ void tile_coords2(const GemmArgs& a, int t, int& mb, 
 // ---------------------------------------------------------------------- prep scratch
 
 // Per-matrix reduction scratch: an arrival counter and up to kPrepBlocks fp64 partials.
-constexpr int kPrepBlocks = 512;
+constexpr int kPrepBlocks = kNormPartialsMax;
 constexpr long long kSumsqElems = 32768;  // elements per sum-of-squares block (before the cap)
 constexpr size_t kPrepWsBytes = 256 + sizeof(double) * kPrepBlocks;
 
