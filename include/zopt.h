@@ -401,12 +401,17 @@ typedef struct zopt_muon_stats {
 } zopt_muon_stats; /* 16 bytes per matrix, device resident */
 
 /* Workspace bytes to step `group` rows x cols matrices together (the Newton-Schulz workspace
- * plus, per group member, u in fp32 and U in bf16; 0 for a shape beyond the ZOPT_NS_MAX_* limits). A
- * call steps its batch in groups of as many matrices as the workspace holds. */
+ * plus, per group member, u in fp32, U in bf16 and U's statistics slots: 12 bytes for each
+ * 128 x 256 tile's eight 32-row parts, at least 512 of them; 0 for a shape beyond the
+ * ZOPT_NS_MAX_* limits). A call steps its batch in groups of as many matrices as the workspace
+ * holds. */
 ZOPT_API size_t zopt_muon_workspace(int64_t rows, int64_t cols, int32_t group);
 /* One Muon step of `batch` rows x cols matrices stored back to back (matrix b at offset
  * b*rows*cols of master, momentum, grad and out_bf16). master, momentum: fp32; grad: fp32 or
- * bf16; out_bf16: may be NULL; d_stats: `batch` structs. Errors: EINVAL for NULL or
+ * bf16; out_bf16: may be NULL; d_stats: `batch` structs. U's sum of squares and largest
+ * magnitude come from the epilogue of Newton-Schulz's last product where that writes U through
+ * the TMA, else from a pass over U; either way they are summed in a fixed order, so a call
+ * repeated on the same inputs gives the same stats. Errors: EINVAL for NULL or
  * misaligned pointers (16 bytes; a batch needs rows*cols to be a multiple of 4), an empty
  * shape or one beyond the ZOPT_NS_MAX_* limits, a batch of more than 2^46 elements,
  * out-of-range hyper-parameters (lr < 0, momentum outside [0, 1), steps < 1, guard <=

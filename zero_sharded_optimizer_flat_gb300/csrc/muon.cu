@@ -36,21 +36,27 @@ constexpr int kMaxBlocksPerMat = 512;
 static_assert(kMaxBlocksPerMat >= ns::kNormPartialsMax, "a matrix's statistics blocks are its norm blocks");
 constexpr int kMaxItems = 8;         // jobs per element-wise launch
 constexpr long long kMaxCallElems = 1LL << 46;  // elements of one shape's batch
-// per matrix: one fp64 partial sum of squares and one max |U| bit pattern per block
-constexpr size_t kRedBytes = (sizeof(double) + sizeof(unsigned)) * kMaxBlocksPerMat;
 
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+// Statistics slots per matrix: one fp64 partial sum of squares and one max |U| bit pattern each,
+// written by the statistics pass (a block each) or by the epilogue of Newton-Schulz's last
+// product (an epilogue warp's part of a tile each).
+long long red_cap(long long rows, long long cols) {
+  const long long b = ns::stats_slots_bound(rows, cols);
+  return b > kMaxBlocksPerMat ? b : kMaxBlocksPerMat;
+}
 
 struct MuonPlan {
   size_t off_u, off_o, off_ns, ns_bytes, total;
 };
 
-// Workspace of `group` matrices: the reduction area (kRedBytes per matrix), u (fp32) and U
-// (bf16), then the Newton-Schulz workspace.
+// Workspace of `group` matrices: the reduction area (the group's red_cap partial sums per matrix,
+// then as many maxima), u (fp32) and U (bf16), then the Newton-Schulz workspace.
 MuonPlan muon_plan(long long rows, long long cols, long long group) {
   MuonPlan p;
   const long long n = rows * cols;
-  p.off_u = static_cast<size_t>(round_up(group * static_cast<long long>(kRedBytes), 1024));
+  p.off_u = static_cast<size_t>(round_up(group * red_cap(rows, cols) * 12, 1024));
   p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 4, 1024));
   p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 2, 1024));
   p.ns_bytes = static_cast<size_t>(
@@ -70,7 +76,11 @@ struct MuonItem {
   long long npart_stride;
   uint16_t* out;        // bf16 round-out (may be null)
   zopt_muon_stats* stats;
-  uint8_t* red;         // reduction area: per matrix kMaxBlocksPerMat fp64 sums, then as many maxima
+  double* rsum;         // matrix b's statistics slots: sums at rsum + b * rcap, maxima at rmax + b * rcap
+  unsigned* rmax;
+  long long rcap;
+  int nred;             // slots of each matrix the update reduces (bpm, or the Newton-Schulz epilogue's)
+  int ns_stats;         // the Newton-Schulz epilogue wrote the slots: no statistics pass
   long long n;          // elements per matrix
   long long u0;         // blocks of the launch before this job
   int batch;
@@ -224,16 +234,15 @@ __global__ void __launch_bounds__(kThreads) ustats_kernel(const MuonList L) {
     unsigned m = 0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) m = max(m, smax[w]);
-    uint8_t* area = J.red + mb * kRedBytes;
-    reinterpret_cast<double*>(area)[c] = block;
-    reinterpret_cast<unsigned*>(area + sizeof(double) * kMaxBlocksPerMat)[c] = m;
+    J.rsum[mb * J.rcap + c] = block;
+    J.rmax[mb * J.rcap + c] = m;
   }
 }
 
 // Step 4: block u updates block c of matrix mb (as step 3 splits it). It first reduces the
-// matrix's bpm partial sums (threads stride over them, then the block tree: the same order in
-// every block) and maxima; block 0 of the matrix writes its stats. Rejected (max |U| above the
-// guard, or NaN): the master is kept, the bf16 round-out is written either way.
+// matrix's nred maxima (every block) and partial sums (block 0, which writes the stats; threads
+// stride over the slots, then the block tree). Rejected (max |U| above the guard, or NaN): the
+// master is kept, the bf16 round-out is written either way.
 __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
   __shared__ double red[32];
   __shared__ unsigned smax[kThreads / 32];
@@ -242,12 +251,13 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const MuonList L) {
   const long long v = static_cast<long long>(blockIdx.x) - J.u0;
   const long long mb = v / J.bpm, c = v - mb * J.bpm;
   const long long n = J.n;
-  const uint8_t* area = J.red + mb * kRedBytes;
+  const double* rs = J.rsum + mb * J.rcap;
+  const unsigned* rm = J.rmax + mb * J.rcap;
   double a = 0.0;
   unsigned m = 0;
-  for (int i = threadIdx.x; i < J.bpm; i += kThreads) {
-    a = __dadd_rn(a, __ldcg(reinterpret_cast<const double*>(area) + i));  // from L2: another kernel wrote them
-    m = max(m, __ldcg(reinterpret_cast<const unsigned*>(area + sizeof(double) * kMaxBlocksPerMat) + i));
+  for (int i = threadIdx.x; i < J.nred; i += kThreads) {  // from L2: another kernel wrote them
+    if (c == 0) a = __dadd_rn(a, __ldcg(rs + i));
+    m = max(m, __ldcg(rm + i));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -381,12 +391,16 @@ MuonItem item_of_job(const Job& j, long long b0, int gs, uint8_t* ws, const Muon
   it.npart_stride = 0;
   it.out = j.out ? j.out + b0 * n : nullptr;
   it.stats = j.stats + b0;
-  it.red = ws;
+  it.rcap = red_cap(rows, cols);
+  it.rsum = reinterpret_cast<double*>(ws);
+  it.rmax = reinterpret_cast<unsigned*>(ws + gs * it.rcap * 8);
   it.n = n;
   it.batch = gs;
   // depends on n only (a matrix's stats are the same in any call), and equals the Newton-Schulz
   // norm's partial count, which the momentum pass fills
   it.bpm = ns::norm_blocks(n);
+  it.nred = it.bpm;  // until the Newton-Schulz call says its epilogue writes the slots
+  it.ns_stats = 0;
   // 8-byte bf16 stores need the first matrix 8-byte aligned and every matrix a multiple of 4
   it.out8 = it.out != nullptr && (reinterpret_cast<uintptr_t>(it.out) & 7u) == 0 && (n & 3) == 0 ? 1 : 0;
   it.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
@@ -423,6 +437,7 @@ zopt_status launch_pass(Pass pass, const std::vector<MuonItem>& items, const std
   for (size_t k = 0; k < items.size(); ++k) {
     if (pass == kMomentumBf16 && gdt[k] != ZOPT_BF16) continue;
     if (pass == kMomentumF32 && gdt[k] != ZOPT_F32) continue;
+    if (pass == kStats && items[k].ns_stats) continue;
     if (L.n == kMaxItems && (st = flush()) != ZOPT_OK) return st;
     MuonItem it = items[k];
     it.u0 = units;
@@ -480,15 +495,26 @@ void attach_norm_partials(const std::vector<zopt_ns_job>& ns, uint8_t* nws, std:
 }
 
 // Step 2: U = NewtonSchulz(u) for every job in one many-call, its norms taken from the partials
-// the momentum pass wrote and U written in bf16.
+// the momentum pass wrote and U written in bf16. Where the last product's epilogue is a TMA one,
+// it also writes U's statistics slots (step 3 then skips the item).
 zopt_status muon_ns(const char* fn, const std::vector<zopt_ns_job>& ns, const zopt_muon_hparams* hp, uint8_t* nws,
-                    size_t nws_bytes, cudaStream_t s) {
+                    size_t nws_bytes, cudaStream_t s, std::vector<MuonItem>& items) {
   const size_t n = ns.size();
   const std::vector<zopt_dtype> out(n, ZOPT_BF16);
   std::unique_ptr<bool[]> ready(new bool[n]);
-  for (size_t k = 0; k < n; ++k) ready[k] = true;
-  return ns::orthogonalize_many(fn, ns.data(), static_cast<int32_t>(n), hp->ns_steps, hp->abc, hp->eps, nws, nws_bytes,
-                                s, out.data(), ready.get());
+  std::vector<ns::StatsSink> sinks(n);
+  std::vector<int> slots(n, 0);
+  for (size_t k = 0; k < n; ++k) {
+    ready[k] = true;
+    sinks[k] = ns::StatsSink{items[k].rsum, items[k].rmax, items[k].rcap, items[k].rcap};
+  }
+  const zopt_status st = ns::orthogonalize_many(fn, ns.data(), static_cast<int32_t>(n), hp->ns_steps, hp->abc, hp->eps,
+                                                nws, nws_bytes, s, out.data(), ready.get(), sinks.data(), slots.data());
+  for (size_t k = 0; k < n; ++k) {
+    items[k].ns_stats = slots[k] > 0 ? 1 : 0;
+    items[k].nred = slots[k] > 0 ? slots[k] : items[k].bpm;
+  }
+  return st;
 }
 
 }  // namespace
@@ -540,7 +566,7 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
     // 1. momentum over the group's matrices (contiguous), u and its norm partials into the workspace
     if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
     // 2. U = NewtonSchulz(u), fp32 in, bf16 out, bf16 tensor cores
-    if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s)) != ZOPT_OK) return st;
+    if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s, items)) != ZOPT_OK) return st;
     // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
     if ((st = launch_update(items, gdt, hp, s)) != ZOPT_OK) return st;
   }
@@ -602,6 +628,6 @@ extern "C" zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_
   }
   attach_norm_partials(ns, ws + at, items);
   if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
-  if ((st = muon_ns(fn, ns, hp, ws + at, ws_bytes - at, s)) != ZOPT_OK) return st;
+  if ((st = muon_ns(fn, ns, hp, ws + at, ws_bytes - at, s, items)) != ZOPT_OK) return st;
   return launch_update(items, gdt, hp, s);
 }

@@ -273,7 +273,10 @@ constexpr long long kPairRideMin = 512;
 // all of them (kMaxPairJobs groups to a launch, those with the same epilogue together): the
 // small groups' tiles fill the large ones' waves. Every tile is computed as in a launch of its
 // own group alone, so the results are bitwise those of separate launches.
-zopt_status pair_products(const std::vector<const Group*>& gs, const Coef& k, int steps, int* err, cudaStream_t s) {
+// sinks (optional, one per group): where the last product of the last step writes its output's
+// statistics (a TMA epilogue only).
+zopt_status pair_products(const std::vector<const Group*>& gs, const Coef& k, int steps, int* err, cudaStream_t s,
+                          const std::vector<const StatsSink*>* sinks = nullptr) {
   zopt_status st = ZOPT_OK;
   int cur = 0;
   for (int it = 0; it < steps; ++it) {
@@ -289,13 +292,27 @@ zopt_status pair_products(const std::vector<const Group*>& gs, const Coef& k, in
           }
           if (q == gs.size()) break;
           PairJob J;
-          if (pair_job(*gs[q], k, prod, last, cur, err, J) == epi) B.job[B.n++] = J;
+          if (pair_job(*gs[q], k, prod, last, cur, err, J) == epi) {
+            const StatsSink* sk = sinks != nullptr ? (*sinks)[q] : nullptr;
+            if (sk != nullptr && last && prod == 2 && epi == kEpiTma) {
+              J.a.st_sum = sk->sum;
+              J.a.st_max = sk->max;
+              J.a.st_stride = sk->stride;
+            }
+            B.job[B.n++] = J;
+          }
         }
       }
     }
     cur ^= 1;
   }
   return ok();
+}
+
+long long stats_slots_bound(long long rows, long long cols) {
+  const long long m = rows < cols ? rows : cols, n = rows < cols ? cols : rows;
+  // single-CTA tiles (128 x 256) outnumber CTA-pair tiles (256 x 256); 8 epilogue warps a tile
+  return 8 * ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
 }
 
 // The group's products one launch at a time (the fp32 mode, the CTA-pair kernel, single-CTA
@@ -513,7 +530,8 @@ void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, dou
 
 zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
                                const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
-                               const zopt_dtype* out_io, const bool* norm_ready) {
+                               const zopt_dtype* out_io, const bool* norm_ready, const StatsSink* sinks,
+                               int* slots_out) {
   const std::string f(fn);
   if (jobs == nullptr || d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, f + ": NULL pointer");
   if (n_jobs < 1) return fail(ZOPT_EINVAL, f + ": no jobs");
@@ -533,6 +551,8 @@ zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t 
   }
   const size_t need = zopt_ns_workspace_many(jobs, n_jobs);
   if (need == 0 || ws_bytes < need) return fail(ZOPT_EINVAL, f + ": workspace smaller than zopt_ns_workspace_many");
+  if (slots_out != nullptr)
+    for (int32_t j = 0; j < n_jobs; ++j) slots_out[j] = 0;
   int* err_dev = nullptr;
   if ((st = take_error_word(fn, &err_dev)) != ZOPT_OK) return st;
   const int sms = sm_count();
@@ -580,17 +600,39 @@ zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t 
     if (j == n_jobs) break;
     const Group& Gr = groups[static_cast<size_t>(j)];
     if (group_fusable(Gr, k)) {
-      group_job(Gr, k, err_dev, fa.job[fa.n_jobs], fm.job[fa.n_jobs]);
+      FusedJob& fj = fa.job[fa.n_jobs];
+      group_job(Gr, k, err_dev, fj, fm.job[fa.n_jobs]);
+      if (sinks != nullptr) {  // the last step's B'X writes its output's statistics
+        GemmArgs t3 = fj.prod[3];
+        if (tiles_1cta(t3) && 8LL * t3.tiles_per_mat <= sinks[j].cap) {
+          fj.prod[3].st_sum = sinks[j].sum;
+          fj.prod[3].st_max = sinks[j].max;
+          fj.prod[3].st_stride = sinks[j].stride;
+          slots_out[j] = 8 * t3.tiles_per_mat;
+        }
+      }
       ++fa.n_jobs;
     }
   }
   // the CTA-pair jobs: each product of a step in one launch for all of them
   std::vector<const Group*> pairs;
+  std::vector<const StatsSink*> pair_sinks;
   for (int32_t j = 0; j < n_jobs; ++j) {
     const Group& Gr = groups[static_cast<size_t>(j)];
-    if (!group_fusable(Gr, k) && Gr.pair) pairs.push_back(&Gr);
+    if (!group_fusable(Gr, k) && Gr.pair) {
+      pairs.push_back(&Gr);
+      const StatsSink* sk = nullptr;
+      if (sinks != nullptr && Gr.out_tma) {  // the last B'X's epilogue is a TMA one
+        const long long slots = 8 * ((Gr.p.m + BM2 - 1) / BM2) * ((Gr.p.n + BN - 1) / BN);
+        if (slots <= sinks[j].cap) {
+          sk = &sinks[j];
+          slots_out[j] = static_cast<int>(slots);
+        }
+      }
+      pair_sinks.push_back(sk);
+    }
   }
-  if (!pairs.empty() && (st = pair_products(pairs, k, steps, err_dev, s)) != ZOPT_OK) return st;
+  if (!pairs.empty() && (st = pair_products(pairs, k, steps, err_dev, s, &pair_sinks)) != ZOPT_OK) return st;
   for (int32_t j = 0; j < n_jobs; ++j) {
     const Group& Gr = groups[static_cast<size_t>(j)];
     if (!group_fusable(Gr, k) && !Gr.pair && (st = group_products(Gr, k, steps, err_dev, s)) != ZOPT_OK) return st;

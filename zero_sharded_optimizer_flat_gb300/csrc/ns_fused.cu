@@ -190,8 +190,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int cur = it.s & 1;
       const FusedJobMaps& m = mp.job[it.j];
       const CUtensorMap* D = it.p == 0 ? &m.ae : (it.p == 1 ? &m.be : (it.s == f.steps - 1 ? &m.oe : &m.xe[cur ^ 1]));
+      // statistics slot (when wanted): the tile's index within its matrix, then 8 per tile
+      const int st_slot = a.st_sum != nullptr ? (it.ti + it.tj * a.tiles_m) * 8 + (warp - 2) : -1;
       epi_tile_tma<false, 1>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
-                             it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par, 4 * half, 4 * half + 4);
+                             it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par, 4 * half, 4 * half + 4,
+                             nullptr, st_slot);
       tc::fence_before_sync();
       tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
       if (lane == 0) {

@@ -448,9 +448,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const GemmArgs& a = B.job[j].a;
       int mb, tp, tj;
       tile_coords2(a, t - B.start[j], mb, tp, tj);
+      // statistics slot (when wanted): the tile's index within its matrix, then 8 per tile
+      const int st_slot = a.st_sum != nullptr
+                              ? ((t - B.start[j]) - mb * a.tiles_per_mat) * 8 + static_cast<int>(rank) * 4 + quad
+                              : -1;
       epi_tile_tma<false, 2, kEpi == kEpiTmaR, true>(
           a, &B.job[j].D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
-          tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par, 0, BN / 32, r0);
+          tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par, 0, BN / 32, r0, st_slot);
       tc::fence_before_sync();
       tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
       if (t + npairs < total) first_r(t + npairs);

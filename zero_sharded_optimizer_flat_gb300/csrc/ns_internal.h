@@ -36,13 +36,28 @@ struct GemmF32Args {
 
 zopt_status launch_gemm_f32(const GemmF32Args& a, cudaStream_t stream);
 
-// zopt_ns_orthogonalize_many with two per-job options for callers inside the library (null: the
+// Where a caller wants the statistics of a job's output: the sum of squares and the largest
+// magnitude of each (tile, epilogue warp) part of matrix b's output go to slots of sum + b *
+// stride and max + b * stride, at most cap of them per matrix.
+struct StatsSink {
+  double* sum;
+  unsigned* max;
+  long long stride, cap;
+};
+
+// zopt_ns_orthogonalize_many with per-job options for callers inside the library (null: the
 // entry point's behaviour): out_io[j], the dtype job j's X is written in (its G keeps io_dtype);
 // norm_ready[j], job j's matrices' norm partials are already in the workspace (see
-// many_norm_partials), so the sum-of-squares launch skips them.
+// many_norm_partials), so the sum-of-squares launch skips them; sinks[j], where the epilogue of
+// job j's last product writes its output's statistics when that epilogue is a TMA one (a
+// CTA-pair or fused launch), slots_out[j] then the number of slots per matrix it fills (0: the
+// job's last product runs elsewhere and writes none).
 zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
                                const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
-                               const zopt_dtype* out_io, const bool* norm_ready);
+                               const zopt_dtype* out_io, const bool* norm_ready, const StatsSink* sinks = nullptr,
+                               int* slots_out = nullptr);
+// Statistics slots per matrix that any path of a rows x cols job may fill (a bound for sinks).
+long long stats_slots_bound(long long rows, long long cols);
 
 // Where job j of a many-call keeps its matrices' norm partials in the workspace d_ws: matrix b's
 // blocks' fp64 sums of squares at base[j] + b * stride_doubles, norm_blocks(rows * cols) of them

@@ -73,6 +73,12 @@ struct GemmArgs {
   // at the k-blocks under the tile's columns the A-operand stage meets a 16 x 16 identity
   int ident;
   float h1, h2;
+  // (a Muon call's last product) statistics of the stored output: each epilogue warp writes the
+  // sum of squares and the largest magnitude of its part of a tile to its slot of matrix mb
+  // (st_stride slots apart; see epi_tile_tma); null when not wanted
+  double* st_sum;
+  unsigned* st_max;
+  long long st_stride;
   int* err;
 };
 
@@ -401,11 +407,17 @@ __device__ __forceinline__ void prefetch_r_first(const GemmArgs& a, int mb, int 
 // Blocks c_begin .. c_end - 1 of the tile; with one pair of boxes (kPairs == 1) every block
 // reuses the same D and mirror box. kStreamOut: the product is read by a later launch, not by
 // this one, so its stores mark their L2 lines to be evicted first, ahead of the operands that
-// this launch's other tiles still read.
+// this launch's other tiles still read. st_slot >= 0 (with a.st_sum set): the warp also sums the
+// squares of the values it stores (as stored: bf16-rounded unless a.d_f32; fp32 pairwise over
+// runs of 8, exact fp64 outside the safe range, the runs in fp64) and takes their largest
+// magnitude, and writes both to slot st_slot of matrix mb (every block the warp skips adds 0).
 template <bool kSlice, int kPairs = 2, bool kRegR = false, bool kStreamOut = false>
 __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
                                              int i0, int tj, int mb, bool has_r, int lane, int& last_par,
-                                             int c_begin = 0, int c_end = BN / 32, const uint4* rfirst = nullptr) {
+                                             int c_begin = 0, int c_end = BN / 32, const uint4* rfirst = nullptr,
+                                             int st_slot = -1) {
+  double st_acc = 0.0;
+  unsigned st_mx = 0;
   uint4 rc[4];  // kRegR: R's piece for the block being processed
   const __nv_bfloat16* Rm = nullptr;
   if constexpr (kRegR) {
@@ -460,6 +472,19 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
       for (int k = 0; k < 32; ++k)
         if (k == lane) o[k] += a.diag;
     }
+    if (st_slot >= 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float v = o[8 * q + k];
+          x[k] = a.d_f32 ? v : __bfloat162float(__float2bfloat16_rn(v));
+          st_mx = max(st_mx, __float_as_uint(x[k]) & 0x7FFFFFFFu);
+        }
+        st_acc = __dadd_rn(st_acc, sumsq8(x));
+      }
+    }
     // the boxes of this parity were last handed to the TMA two blocks ago at the latest: wait
     // until it has read them (all groups but the newest, if that one is the other parity's)
     if (lane == 0) {
@@ -500,6 +525,17 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
       tc::bulk_commit();
     }
     last_par = par;
+  }
+  if (st_slot >= 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      st_acc = __dadd_rn(st_acc, __shfl_xor_sync(0xFFFFFFFFu, st_acc, o));
+      st_mx = max(st_mx, __shfl_xor_sync(0xFFFFFFFFu, st_mx, o));
+    }
+    if (lane == 0) {
+      a.st_sum[mb * a.st_stride + st_slot] = st_acc;
+      a.st_max[mb * a.st_stride + st_slot] = st_mx;
+    }
   }
 }
 
