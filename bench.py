@@ -482,7 +482,10 @@ class MuonPart:
         self.count = sum(shapes.values())
         self.flops = sum(ns_flops(r, c, 5) * b for (r, c), b in shapes.items())
         n = sum(r * c * b for (r, c), b in shapes.items())
-        self.bytes = 28 * n  # momentum 14 (bf16 grad), statistics 2 and update 12 (bf16 U) per element
+        # per element: momentum 12 (bf16 grad in; buf in and out; u out in bf16) and update 12
+        # (master in and out, bf16 U in, bf16 weights out); U's statistics come from the last
+        # Newton-Schulz product's epilogue, u's norm from the momentum pass
+        self.bytes = 24 * n
         owner = f"owned by rank 0 of {w.world}" if w.world > 1 else "(W = 1)"
         self.what = (f"{self.count} matrices {sorted(shapes)} of the {which} set {owner}, "
                      "zopt_muon_step_many, 5 Newton-Schulz steps")

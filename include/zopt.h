@@ -373,8 +373,9 @@ ZOPT_API zopt_status zopt_selftest_div_by_const(float c, unsigned long long* d_m
  * divergence guard on the largest |U| element.
  *
  * Per matrix, each operation rounded to fp32 as written:
- *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(u) (bf16 compute,
- *   U the method's bf16 result; ||u|| summed by the momentum pass itself);
+ *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(bf16(u)) (bf16
+ *   compute, normalised by the norm of bf16(u), which the momentum pass sums itself; U the
+ *   method's bf16 result);
  *   unless max|U| > guard (or not finite): p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U;
  *   out = bf16_rne(p).  A rejected matrix keeps its master; its momentum is still updated.
  * ====================================================================================== */
@@ -401,7 +402,7 @@ typedef struct zopt_muon_stats {
 } zopt_muon_stats; /* 16 bytes per matrix, device resident */
 
 /* Workspace bytes to step `group` rows x cols matrices together (the Newton-Schulz workspace
- * plus, per group member, u in fp32, U in bf16 and U's statistics slots: 12 bytes for each
+ * plus, per group member, u and U in bf16 and U's statistics slots: 12 bytes for each
  * 128 x 256 tile's eight 32-row parts, at least 512 of them; 0 for a shape beyond the
  * ZOPT_NS_MAX_* limits). A call steps its batch in groups of as many matrices as the workspace
  * holds. */

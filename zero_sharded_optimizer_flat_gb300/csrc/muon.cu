@@ -52,12 +52,12 @@ struct MuonPlan {
 };
 
 // Workspace of `group` matrices: the reduction area (the group's red_cap partial sums per matrix,
-// then as many maxima), u (fp32) and U (bf16), then the Newton-Schulz workspace.
+// then as many maxima), u and U (both bf16), then the Newton-Schulz workspace.
 MuonPlan muon_plan(long long rows, long long cols, long long group) {
   MuonPlan p;
   const long long n = rows * cols;
   p.off_u = static_cast<size_t>(round_up(group * red_cap(rows, cols) * 12, 1024));
-  p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 4, 1024));
+  p.off_o = p.off_u + static_cast<size_t>(round_up(group * n * 2, 1024));
   p.off_ns = p.off_o + static_cast<size_t>(round_up(group * n * 2, 1024));
   p.ns_bytes = static_cast<size_t>(
       round_up(static_cast<long long>(zopt_ns_workspace(rows, cols, static_cast<int32_t>(group), ZOPT_BF16)), 1024));
@@ -70,7 +70,7 @@ struct MuonItem {
   float* master;
   float* momentum;
   const void* grad;
-  float* u_in;              // momentum's output, Newton-Schulz's input
+  uint16_t* u_in;           // momentum's output in bf16, Newton-Schulz's input
   const uint16_t* u_out;    // Newton-Schulz's output U (bf16)
   double* npart;            // the Newton-Schulz norm partials of matrix 0; matrix b's at + b * npart_stride
   long long npart_stride;
@@ -108,11 +108,22 @@ __device__ __forceinline__ float4 fma4_momentum(float mu, const float4& b, const
                      __fadd_rn(__fmul_rn(mu, b.z), g.z), __fadd_rn(__fmul_rn(mu, b.w), g.w));
 }
 
+__device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float4 bf16r4(const float4& x) {
+  return make_float4(bf16r(x.x), bf16r(x.y), bf16r(x.z), bf16r(x.w));
+}
+// Four bf16-exact floats as 4 bf16 (their high halves).
+__device__ __forceinline__ uint2 pack_bf16x4(const float4& r) {
+  return make_uint2((__float_as_uint(r.x) >> 16) | (__float_as_uint(r.y) & 0xFFFF0000u),
+                    (__float_as_uint(r.z) >> 16) | (__float_as_uint(r.w) & 0xFFFF0000u));
+}
+
 // Step 1: block u takes part c = (u - u0) % bpm of matrix mb = (u - u0) / bpm of its job; threads
 // stride over the matrix's 4-element vectors with stride bpm * 256, four vectors' loads in flight
-// per round; the matrix's n % 4 last elements go to part 0 element by element. The block's sum of
-// u^2 (fp32 pairwise over runs of 8, exact fp64 outside the safe range, the runs in fp64) is the
-// matrix's norm partial c, which the Newton-Schulz normalisation reads in place of u.
+// per round; the matrix's n % 4 last elements go to part 0 element by element. u goes out rounded
+// to bf16, the dtype Newton-Schulz computes in. The block's sum of squares of those bf16 values
+// (fp32 pairwise over runs of 8, exact fp64 outside the safe range, the runs in fp64) is the
+// matrix's norm partial c, which the Newton-Schulz normalisation reads in place of a pass over u.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
   __shared__ double red[32];
@@ -122,9 +133,9 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
   const long long n = J.n;
   const T* g = static_cast<const T*>(J.grad) + mb * n;
   float* buf = J.momentum + mb * n;
-  float* u = J.u_in + mb * n;
+  uint16_t* u = J.u_in + mb * n;
   float4* b4 = reinterpret_cast<float4*>(buf);
-  float4* u4 = reinterpret_cast<float4*>(u);
+  uint2* u4 = reinterpret_cast<uint2*>(u);
   const float mu = L.mu;
   const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(J.bpm) * blockDim.x;
@@ -141,8 +152,8 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
     for (int k = 0; k < 4; ++k) {
       const float4 nb = fma4_momentum(mu, bv[k], gv[k]);
       b4[j + k * stride] = nb;
-      uv[k] = L.nesterov ? fma4_momentum(mu, nb, gv[k]) : nb;  // g + mu*buf, as the same two roundings
-      u4[j + k * stride] = uv[k];
+      uv[k] = bf16r4(L.nesterov ? fma4_momentum(mu, nb, gv[k]) : nb);  // g + mu*buf, as the same two roundings
+      u4[j + k * stride] = pack_bf16x4(uv[k]);
     }
     acc = __dadd_rn(acc, sumsq44(uv[0], uv[1]));
     acc = __dadd_rn(acc, sumsq44(uv[2], uv[3]));
@@ -151,8 +162,8 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
     const float4 gv = load4(g + 4 * j);
     const float4 nb = fma4_momentum(mu, b4[j], gv);
     b4[j] = nb;
-    const float4 uv = L.nesterov ? fma4_momentum(mu, nb, gv) : nb;
-    u4[j] = uv;
+    const float4 uv = bf16r4(L.nesterov ? fma4_momentum(mu, nb, gv) : nb);
+    u4[j] = pack_bf16x4(uv);
     acc = __dadd_rn(acc, sumsq44(uv, make_float4(0.f, 0.f, 0.f, 0.f)));
   }
   if (c == 0 && threadIdx.x == 0) {
@@ -160,8 +171,8 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
       const float gv = load1(g + k);
       const float b = __fadd_rn(__fmul_rn(mu, buf[k]), gv);
       buf[k] = b;
-      const float x = L.nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b;
-      u[k] = x;
+      const float x = bf16r(L.nesterov ? __fadd_rn(__fmul_rn(mu, b), gv) : b);
+      u[k] = static_cast<uint16_t>(__float_as_uint(x) >> 16);
       acc = __dadd_rn(acc, __dmul_rn(static_cast<double>(x), static_cast<double>(x)));
     }
   }
@@ -385,7 +396,7 @@ MuonItem item_of_job(const Job& j, long long b0, int gs, uint8_t* ws, const Muon
   it.master = j.master + b0 * n;
   it.momentum = j.momentum + b0 * n;
   it.grad = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
-  it.u_in = reinterpret_cast<float*>(ws + P.off_u);
+  it.u_in = reinterpret_cast<uint16_t*>(ws + P.off_u);
   it.u_out = reinterpret_cast<const uint16_t*>(ws + P.off_o);
   it.npart = nullptr;  // set once the Newton-Schulz workspace is known
   it.npart_stride = 0;
@@ -464,9 +475,8 @@ Job job_of(const zopt_muon_job& b) {
              b.rows, b.cols, b.batch, b.d_stats};
 }
 
-// The Newton-Schulz job of a Muon job: fp32 u -> U (written in bf16: see muon_ns), contiguous
-// matrices.
-zopt_ns_job ns_job_of(const Job& j, const float* U_in, uint16_t* U_out) {
+// The Newton-Schulz job of a Muon job: u -> U, both bf16, contiguous matrices.
+zopt_ns_job ns_job_of(const Job& j, const uint16_t* U_in, uint16_t* U_out) {
   const long long n = j.rows * j.cols;
   zopt_ns_job q;
   q.G = U_in;
@@ -478,7 +488,7 @@ zopt_ns_job ns_job_of(const Job& j, const float* U_in, uint16_t* U_out) {
   q.batch_stride_g = n;
   q.batch_stride_x = n;
   q.batch = static_cast<int32_t>(j.batch);
-  q.io_dtype = ZOPT_F32;
+  q.io_dtype = ZOPT_BF16;
   return q;
 }
 
@@ -550,7 +560,7 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
   if (group < 1) return fail(ZOPT_EINVAL, "zopt_muon_step: workspace smaller than zopt_muon_workspace(rows, cols, 1)");
   const MuonPlan P = muon_plan(rows, cols, group);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
-  float* U_in = reinterpret_cast<float*>(ws + P.off_u);
+  uint16_t* U_in = reinterpret_cast<uint16_t*>(ws + P.off_u);
   uint16_t* U_out = reinterpret_cast<uint16_t*>(ws + P.off_o);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = sm_count();
@@ -565,7 +575,7 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
     attach_norm_partials(ns, ws + P.off_ns, items);
     // 1. momentum over the group's matrices (contiguous), u and its norm partials into the workspace
     if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
-    // 2. U = NewtonSchulz(u), fp32 in, bf16 out, bf16 tensor cores
+    // 2. U = NewtonSchulz(u), bf16 in and out, bf16 tensor cores
     if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s, items)) != ZOPT_OK) return st;
     // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
     if ((st = launch_update(items, gdt, hp, s)) != ZOPT_OK) return st;
