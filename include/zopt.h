@@ -374,8 +374,10 @@ ZOPT_API zopt_status zopt_selftest_div_by_const(float c, unsigned long long* d_m
  *
  * Per matrix, each operation rounded to fp32 as written:
  *   buf = mu*buf + g;  u = g + mu*buf (nesterov) or buf;  U = NewtonSchulz(bf16(u)) (bf16
- *   compute, normalised by the norm of bf16(u), which the momentum pass sums itself; U the
- *   method's bf16 result);
+ *   compute, normalised by the norm of bf16(u), which the momentum pass sums itself; for a
+ *   matrix no taller than wide with a width that is a multiple of 8 the pass writes bf16(u)
+ *   into Newton-Schulz's own input buffer and the first step's products apply the
+ *   normalisation; U the method's bf16 result);
  *   unless max|U| > guard (or not finite): p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U;
  *   out = bf16_rne(p).  A rejected matrix keeps its master; its momentum is still updated.
  * ====================================================================================== */

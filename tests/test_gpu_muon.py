@@ -279,3 +279,40 @@ def test_momentum_variants(zopt, nesterov, mom, wd):
             assert rel(applied, U_ref) <= 2e-2, (s, b)
         assert np.array_equal(buf.cpu().numpy().view(np.uint32), ref_buf.view(np.uint32))
         assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(256, 768, 2), (768, 256, 1), (1024, 1536, 1), (96, 100, 1)])
+@pytest.mark.parametrize("abc", [OM.DEFAULT_ABC, (1.5, -0.5, 0.0)])
+@pytest.mark.parametrize("ns_steps", [1, 5])
+def test_first_step_normalises_every_path(zopt, rows, cols, batch, abc, ns_steps):
+    """Where a matrix is no taller than wide and its width a multiple of 8, the momentum pass
+    writes u straight into Newton-Schulz's X0, unnormalised, and the first step's products
+    scale by 1 / (||u|| + eps) (X X' by its square). Covered on each path that runs a first
+    step: the persistent fused launch (256 x 768), the CTA-pair launches (1024 x 1536), the
+    product-by-product single-CTA launches (a zero c rules out the identity MMAs), a single step
+    (the first product is also the last), and the shapes that keep the preparation pass (a tall
+    matrix; a width not a multiple of 8). The update within the Newton-Schulz tolerance of the
+    fp64 oracle with the same coefficients."""
+    h = OM.MuonHyper(lr=8e-4, match_rms_adamw=True, ns_steps=ns_steps, abc=tuple(abc))
+    gen = torch.Generator(device="cuda").manual_seed(rows + 7 * cols + ns_steps)
+    p = torch.randn(batch, rows, cols, generator=gen, device="cuda") * 0.02
+    buf = torch.zeros_like(p)
+    out = torch.zeros(batch, rows, cols, dtype=torch.int16, device="cuda")
+    stats = zopt.new_muon_stats(batch)
+    g = (torch.randn(batch, rows, cols, generator=gen, device="cuda") * 1e-3).bfloat16()
+    p_old = p.cpu().numpy()
+    zopt.muon_step(p, buf, g, out, zopt.new_muon_workspace(rows, cols, batch), stats, lr=h.lr, ns_steps=ns_steps,
+                   abc=abc)
+    torch.cuda.synchronize()
+    pn = p.cpu().numpy()
+    decay = np.float32(1.0 - h.lr * h.weight_decay)
+    step = np.float32(h.lr * OM.lr_scale(rows, cols, True))
+    st = zopt.read_muon_stats(stats)
+    for b in range(batch):
+        u = OM.momentum_f32(np.zeros((rows, cols), np.float32), g[b].float().cpu().numpy(), h)
+        U_ref = newton_schulz(u.astype(np.float64), steps=ns_steps, abc=abc)
+        applied = (p_old[b] * decay - pn[b]).astype(np.float64) / float(step)
+        assert rel(applied, U_ref) <= 2e-2, b
+        assert abs(st[b]["update_fro"] / np.linalg.norm(U_ref) - 1) <= 2e-2
+        assert not st[b]["rejected"]
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(pn))

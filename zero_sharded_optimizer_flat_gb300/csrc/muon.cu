@@ -70,7 +70,8 @@ struct MuonItem {
   float* master;
   float* momentum;
   const void* grad;
-  uint16_t* u_in;           // momentum's output in bf16, Newton-Schulz's input
+  uint16_t* u_in;           // momentum's output in bf16, Newton-Schulz's input; matrix b at + b * u_stride
+  long long u_stride;
   const uint16_t* u_out;    // Newton-Schulz's output U (bf16)
   double* npart;            // the Newton-Schulz norm partials of matrix 0; matrix b's at + b * npart_stride
   long long npart_stride;
@@ -121,7 +122,7 @@ __device__ __forceinline__ uint2 pack_bf16x4(const float4& r) {
 // Step 1: block u takes part c = (u - u0) % bpm of matrix mb = (u - u0) / bpm of its job; threads
 // stride over the matrix's 4-element vectors with stride bpm * 256, four vectors' loads in flight
 // per round; the matrix's n % 4 last elements go to part 0 element by element. u goes out rounded
-// to bf16, the dtype Newton-Schulz computes in. The block's sum of squares of those bf16 values
+// to bf16, the dtype Newton-Schulz computes in (where the job allows, straight into its X0). The block's sum of squares of those bf16 values
 // (fp32 pairwise over runs of 8, exact fp64 outside the safe range, the runs in fp64) is the
 // matrix's norm partial c, which the Newton-Schulz normalisation reads in place of a pass over u.
 template <typename T>
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MuonList L) {
   const long long n = J.n;
   const T* g = static_cast<const T*>(J.grad) + mb * n;
   float* buf = J.momentum + mb * n;
-  uint16_t* u = J.u_in + mb * n;
+  uint16_t* u = J.u_in + mb * J.u_stride;
   float4* b4 = reinterpret_cast<float4*>(buf);
   uint2* u4 = reinterpret_cast<uint2*>(u);
   const float mu = L.mu;
@@ -396,7 +397,8 @@ MuonItem item_of_job(const Job& j, long long b0, int gs, uint8_t* ws, const Muon
   it.master = j.master + b0 * n;
   it.momentum = j.momentum + b0 * n;
   it.grad = static_cast<const uint8_t*>(j.grad) + static_cast<size_t>(b0 * n) * gsz;
-  it.u_in = reinterpret_cast<uint16_t*>(ws + P.off_u);
+  it.u_in = reinterpret_cast<uint16_t*>(ws + P.off_u);  // unless the Newton-Schulz X0 takes u (attach_ns)
+  it.u_stride = n;
   it.u_out = reinterpret_cast<const uint16_t*>(ws + P.off_o);
   it.npart = nullptr;  // set once the Newton-Schulz workspace is known
   it.npart_stride = 0;
@@ -493,14 +495,23 @@ zopt_ns_job ns_job_of(const Job& j, const uint16_t* U_in, uint16_t* U_out) {
 }
 
 // Points each item's momentum pass at its Newton-Schulz job's norm partials (ns[] in the
-// Newton-Schulz workspace nws), which the pass fills in place of a sum-of-squares launch.
-void attach_norm_partials(const std::vector<zopt_ns_job>& ns, uint8_t* nws, std::vector<MuonItem>& items) {
-  std::vector<double*> base(ns.size());
-  std::vector<long long> stride(ns.size());
-  ns::many_norm_partials(ns.data(), static_cast<int32_t>(ns.size()), nws, base.data(), stride.data());
-  for (size_t k = 0; k < ns.size(); ++k) {
+// Newton-Schulz workspace nws), which the pass fills in place of a sum-of-squares launch, and,
+// where the job can take it (raw[k] set), at the job's X0 itself: u goes there unnormalised
+// and the first step's products normalise it, so no preparation pass reads u.
+void attach_ns(const std::vector<zopt_ns_job>& ns, uint8_t* nws, std::vector<MuonItem>& items, bool* raw) {
+  const size_t n = ns.size();
+  std::vector<double*> base(n);
+  std::vector<long long> stride(n), xs(n);
+  std::vector<uint16_t*> x0(n);
+  ns::many_norm_partials(ns.data(), static_cast<int32_t>(n), nws, base.data(), stride.data());
+  ns::many_x0(ns.data(), static_cast<int32_t>(n), nws, x0.data(), xs.data(), raw);
+  for (size_t k = 0; k < n; ++k) {
     items[k].npart = base[k];
     items[k].npart_stride = stride[k];
+    if (raw[k]) {
+      items[k].u_in = x0[k];
+      items[k].u_stride = xs[k];
+    }
   }
 }
 
@@ -508,7 +519,7 @@ void attach_norm_partials(const std::vector<zopt_ns_job>& ns, uint8_t* nws, std:
 // the momentum pass wrote and U written in bf16. Where the last product's epilogue is a TMA one,
 // it also writes U's statistics slots (step 3 then skips the item).
 zopt_status muon_ns(const char* fn, const std::vector<zopt_ns_job>& ns, const zopt_muon_hparams* hp, uint8_t* nws,
-                    size_t nws_bytes, cudaStream_t s, std::vector<MuonItem>& items) {
+                    size_t nws_bytes, cudaStream_t s, std::vector<MuonItem>& items, const bool* raw) {
   const size_t n = ns.size();
   const std::vector<zopt_dtype> out(n, ZOPT_BF16);
   std::unique_ptr<bool[]> ready(new bool[n]);
@@ -519,7 +530,8 @@ zopt_status muon_ns(const char* fn, const std::vector<zopt_ns_job>& ns, const zo
     sinks[k] = ns::StatsSink{items[k].rsum, items[k].rmax, items[k].rcap, items[k].rcap};
   }
   const zopt_status st = ns::orthogonalize_many(fn, ns.data(), static_cast<int32_t>(n), hp->ns_steps, hp->abc, hp->eps,
-                                                nws, nws_bytes, s, out.data(), ready.get(), sinks.data(), slots.data());
+                                                nws, nws_bytes, s, out.data(), ready.get(), sinks.data(), slots.data(),
+                                                raw);
   for (size_t k = 0; k < n; ++k) {
     items[k].ns_stats = slots[k] > 0 ? 1 : 0;
     items[k].nred = slots[k] > 0 ? slots[k] : items[k].bpm;
@@ -572,11 +584,12 @@ extern "C" zopt_status zopt_muon_step(float* master, float* momentum, const void
     Job jg = j;
     jg.batch = gs;
     const std::vector<zopt_ns_job> ns{ns_job_of(jg, U_in, U_out)};
-    attach_norm_partials(ns, ws + P.off_ns, items);
+    bool raw[1];
+    attach_ns(ns, ws + P.off_ns, items, raw);
     // 1. momentum over the group's matrices (contiguous), u and its norm partials into the workspace
     if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
     // 2. U = NewtonSchulz(u), bf16 in and out, bf16 tensor cores
-    if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s, items)) != ZOPT_OK) return st;
+    if ((st = muon_ns(fn, ns, hp, ws + P.off_ns, P.ns_bytes, s, items, raw)) != ZOPT_OK) return st;
     // 3, 4. per-matrix statistics, the guarded update and bf16 round-out
     if ((st = launch_update(items, gdt, hp, s)) != ZOPT_OK) return st;
   }
@@ -636,8 +649,9 @@ extern "C" zopt_status zopt_muon_step_many(const zopt_muon_job* jobs, int32_t n_
                                            const_cast<uint16_t*>(items[static_cast<size_t>(k)].u_out));
     at += static_cast<size_t>(round_up(static_cast<long long>(P.off_ns), 1024));
   }
-  attach_norm_partials(ns, ws + at, items);
+  std::unique_ptr<bool[]> raw(new bool[static_cast<size_t>(n_jobs)]);
+  attach_ns(ns, ws + at, items, raw.get());
   if ((st = launch_momentum(items, gdt, hp, s)) != ZOPT_OK) return st;
-  if ((st = muon_ns(fn, ns, hp, ws + at, ws_bytes - at, s, items)) != ZOPT_OK) return st;
+  if ((st = muon_ns(fn, ns, hp, ws + at, ws_bytes - at, s, items, raw.get())) != ZOPT_OK) return st;
   return launch_update(items, gdt, hp, s);
 }

@@ -192,6 +192,13 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
 bool group_fusable(const Group& G, const Coef& k) { return !G.f32c && !G.pair && G.out_tma && k.id_ok; }
 
 // The group as one job of the fused kernel.
+// Matrix 0's factor for the first step's products of a group whose X0 arrives unnormalised
+// (matrix b's kScaleStride floats on): 1 / (||X0|| + eps), squared for X X'.
+constexpr long long kScaleStride = static_cast<long long>(kPrepWsBytes / sizeof(float));
+const float* x0_scale(const Group& G, bool squared) {
+  return reinterpret_cast<const float*>(G.ws) + kScaleWord + (squared ? 1 : 0);
+}
+
 void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobMaps& m) {
   for (int q = 0; q < 2; ++q) {
     m.xp[q] = G.mx_p[q];
@@ -220,6 +227,11 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
   GemmArgs& px = job.prod[2];  // X = B' X
   px = g0;
   px.M = mm; px.N = n; px.K = mm; px.b_mn_major = 1;
+  if (G.x0_raw) {  // the first step normalises: A by 1 / (||X0|| + eps)^2, B'X by 1 / (||X0|| + eps)
+    pa.amat = x0_scale(G, true);
+    px.amat = x0_scale(G, false);
+    pa.amat_stride = px.amat_stride = kScaleStride;
+  }
   job.prod[3] = px;  // the last step's, into the caller's X
   job.prod[3].d_f32 = G.out_io == ZOPT_F32 ? 1 : 0;
   job.prod[3].d_trans = G.transpose ? 1 : 0;
@@ -228,8 +240,9 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
 
 // Product `prod` of a step of a CTA-pair group as a job of a pair launch: 0 A = X X', 1 B' =
 // c A A' + b A + a I (b A through the R epilogue), 2 X = B' X (into the caller's X at the last
-// step). X is in buffer `cur`; returns the product's epilogue.
-int pair_job(const Group& G, const Coef& k, int prod, bool last, int cur, int* err, PairJob& J) {
+// step). X is in buffer `cur`; `first`: the call's first step (which normalises an X0 that
+// arrives unnormalised). Returns the product's epilogue.
+int pair_job(const Group& G, const Coef& k, int prod, bool first, bool last, int cur, int* err, PairJob& J) {
   const int m = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n);
   const long long mat_elems = G.mat_elems;
   GemmArgs& a = J.a;
@@ -237,6 +250,10 @@ int pair_job(const Group& G, const Coef& k, int prod, bool last, int cur, int* e
   a.err = err;
   a.group = G.gs;
   a.alpha = 1.0f;
+  if (first && G.x0_raw && prod != 1) {
+    a.amat = x0_scale(G, prod == 0);
+    a.amat_stride = kScaleStride;
+  }
   if (prod == 0) {
     a.M = m; a.N = m; a.K = n; a.symmetric = 1;
     a.D = G.A; a.ldd = G.p.lda; a.d_stride = mat_elems;
@@ -292,7 +309,7 @@ zopt_status pair_products(const std::vector<const Group*>& gs, const Coef& k, in
           }
           if (q == gs.size()) break;
           PairJob J;
-          if (pair_job(*gs[q], k, prod, last, cur, err, J) == epi) {
+          if (pair_job(*gs[q], k, prod, it == 0, last, cur, err, J) == epi) {
             const StatsSink* sk = sinks != nullptr ? (*sinks)[q] : nullptr;
             if (sk != nullptr && last && prod == 2 && epi == kEpiTma) {
               J.a.st_sum = sk->sum;
@@ -351,7 +368,10 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       GemmArgs ga{};
       ga.err = err;
       ga.group = gs;
+      const bool norm_here = it == 0 && G.x0_raw;  // this step normalises X0
+      ga.amat_stride = kScaleStride;
       // A = X X'
+      ga.amat = norm_here ? x0_scale(G, true) : nullptr;
       ga.M = m; ga.N = m; ga.K = n;
       ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
       ga.ldr = 0; ga.r_stride = 0; ga.D = G.A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
@@ -360,6 +380,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
       // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
       ga.K = m;
+      ga.amat = nullptr;
       ga.alpha = k.c; ga.beta = k.b; ga.diag = k.a;
       ga.R = reinterpret_cast<const __nv_bfloat16*>(G.A); ga.ldr = p.lda; ga.r_stride = mat_elems;
       ga.D = G.B; ga.ldd = p.lda; ga.d_stride = mat_elems;
@@ -372,6 +393,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       }
       if (st != ZOPT_OK) return st;
       // X = B' X
+      ga.amat = norm_here ? x0_scale(G, false) : nullptr;
       ga.M = m; ga.N = n; ga.K = m;
       ga.symmetric = 0; ga.b_mn_major = 1; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f;
       ga.R = nullptr; ga.ldr = 0; ga.r_stride = 0;
@@ -474,6 +496,7 @@ extern "C" zopt_status zopt_ns_orthogonalize(const void* G, void* X, zopt_dtype 
     Gr.io = io_dtype;
     Gr.out_io = io_dtype;
     Gr.norm_ready = false;
+    Gr.x0_raw = false;
     Gr.rows = rows; Gr.cols = cols; Gr.ld_g = ld_g; Gr.ld_x = ld_x; Gr.bs_g = batch_stride_g; Gr.bs_x = batch_stride_x;
     Gr.gs = static_cast<int>(batch - g0i < group ? batch - g0i : group);
     Gr.f32c = f32c;
@@ -528,10 +551,28 @@ void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, dou
   }
 }
 
+bool x0_raw_ok(long long rows, long long cols, zopt_dtype io) {
+  // bf16 compute in the input's orientation, X0's rows packed (its pitch is cols rounded to 8)
+  return io == ZOPT_BF16 && rows <= cols && cols % 8 == 0;
+}
+
+void many_x0(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, uint16_t** base, long long* stride, bool* ok) {
+  size_t at = 0;
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const zopt_ns_job& b = jobs[j];
+    const Plan p = plan(b.rows, b.cols, 2, b.batch);
+    // matrix 0's region opens after the header, X0 first; matrix b's per_mat bytes on
+    base[j] = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(d_ws) + at + p.header);
+    stride[j] = static_cast<long long>(p.per_mat / 2);
+    ok[j] = x0_raw_ok(b.rows, b.cols, static_cast<zopt_dtype>(b.io_dtype));
+    at += static_cast<size_t>(round_up(static_cast<long long>(p.total), 1024));
+  }
+}
+
 zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
                                const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
                                const zopt_dtype* out_io, const bool* norm_ready, const StatsSink* sinks,
-                               int* slots_out) {
+                               int* slots_out, const bool* x0_raw) {
   const std::string f(fn);
   if (jobs == nullptr || d_ws == nullptr || abc == nullptr) return fail(ZOPT_EINVAL, f + ": NULL pointer");
   if (n_jobs < 1) return fail(ZOPT_EINVAL, f + ": no jobs");
@@ -548,6 +589,9 @@ zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t 
     if (b.batch > 65535) return fail(ZOPT_EINVAL, f + ": a job's batch exceeds 65535");
     if (out_io != nullptr && out_io[j] != ZOPT_F32 && out_io[j] != ZOPT_BF16)
       return fail(ZOPT_EUNSUPPORTED, f + ": output dtype must be fp32 or bf16");
+    if (x0_raw != nullptr && x0_raw[j] &&
+        (norm_ready == nullptr || !norm_ready[j] || !x0_raw_ok(b.rows, b.cols, static_cast<zopt_dtype>(b.io_dtype))))
+      return fail(ZOPT_EINVAL, f + ": internal: an unnormalised X0 for a job that cannot take one");
   }
   const size_t need = zopt_ns_workspace_many(jobs, n_jobs);
   if (need == 0 || ws_bytes < need) return fail(ZOPT_EINVAL, f + ": workspace smaller than zopt_ns_workspace_many");
@@ -570,6 +614,7 @@ zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t 
     Gr.io = static_cast<zopt_dtype>(b.io_dtype);
     Gr.out_io = out_io != nullptr ? out_io[j] : Gr.io;
     Gr.norm_ready = norm_ready != nullptr && norm_ready[j];
+    Gr.x0_raw = x0_raw != nullptr && x0_raw[j];
     Gr.rows = b.rows; Gr.cols = b.cols; Gr.ld_g = b.ld_g; Gr.ld_x = b.ld_x;
     Gr.bs_g = b.batch_stride_g; Gr.bs_x = b.batch_stride_x;
     Gr.gs = b.batch;

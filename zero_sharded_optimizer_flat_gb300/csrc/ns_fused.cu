@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int st_slot = a.st_sum != nullptr ? (it.ti + it.tj * a.tiles_m) * 8 + (warp - 2) : -1;
       epi_tile_tma<false, 1>(a, D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
                              it.ti * BM + 32 * quad, it.tj, it.mb, false, lane, last_par, 4 * half, 4 * half + 4,
-                             nullptr, st_slot);
+                             nullptr, st_slot, it.s == 0);
       tc::fence_before_sync();
       tc::mbar_arrive(tempty + b);  // the MMA warp may reuse this accumulator
       if (lane == 0) {

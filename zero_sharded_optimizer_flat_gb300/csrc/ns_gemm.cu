@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::fence_after_sync();
       int mb, ti, tj;
       tile_coords(a, t, mb, ti, tj);
-      GemmArgs am = a;  // this matrix's R and D
+      GemmArgs am = a;  // this matrix's R, D and alpha
+      am.alpha = a.alpha * amat_of(a, mb);
       am.R = a.R + mb * a.r_stride;
       am.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
       const int i = ti * BM + row;
@@ -481,6 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int mb, tp, tj;
       tile_coords2(a, t - B.start[j], mb, tp, tj);
       GemmArgs am = a;
+      am.alpha = a.alpha * amat_of(a, mb);
       am.R = a.R + mb * a.r_stride;
       am.D = static_cast<uint8_t*>(a.D) + mb * a.d_stride * (a.d_f32 ? 4 : 2);
       const int i = tp * BM2 + static_cast<int>(rank) * 128 + row;

@@ -51,11 +51,19 @@ struct StatsSink {
 // many_norm_partials), so the sum-of-squares launch skips them; sinks[j], where the epilogue of
 // job j's last product writes its output's statistics when that epilogue is a TMA one (a
 // CTA-pair or fused launch), slots_out[j] then the number of slots per matrix it fills (0: the
-// job's last product runs elsewhere and writes none).
+// job's last product runs elsewhere and writes none); x0_raw[j], job j's matrices are already
+// in X0, unnormalised (see many_x0).
 zopt_status orthogonalize_many(const char* fn, const zopt_ns_job* jobs, int32_t n_jobs, int32_t steps,
                                const float* abc, float eps, void* d_ws, size_t ws_bytes, cudaStream_t s,
                                const zopt_dtype* out_io, const bool* norm_ready, const StatsSink* sinks = nullptr,
-                               int* slots_out = nullptr);
+                               int* slots_out = nullptr, const bool* x0_raw = nullptr);
+// Whether a job can take its matrices unnormalised in X0 (x0_raw of orthogonalize_many): bf16,
+// rows <= cols, cols a multiple of 8. Such a job's matrices are written by the caller, as bf16
+// with rows cols elements apart, to base[j] + b * stride[j] (elements); its norm partials go
+// where many_norm_partials says (norm_ready), and the first step's products normalise. ok[j]
+// tells whether job j can.
+bool x0_raw_ok(long long rows, long long cols, zopt_dtype io);
+void many_x0(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, uint16_t** base, long long* stride, bool* ok);
 // Statistics slots per matrix that any path of a rows x cols job may fill (a bound for sinks).
 long long stats_slots_bound(long long rows, long long cols);
 

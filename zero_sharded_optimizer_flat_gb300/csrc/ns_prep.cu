@@ -2,7 +2,9 @@
 // the compute dtype, transposed for a tall matrix — three launches for every matrix of every
 // job of a call (sum of squares; scaling of the wide; transposition of the tall). Every thread
 // keeps 128 bytes of loads in flight, and the normalising kernels issue their first loads
-// before they reduce the norm.
+// before they reduce the norm. A matrix that its caller has already put in X0 unnormalised
+// (with its norm partials) takes a fourth, small launch instead: its scale, which the first
+// step's products apply.
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
@@ -174,6 +176,32 @@ __device__ __forceinline__ float prep_inv_norm(const PrepItem& J, int mb, double
     cnt[0] = cnt[1] = cnt[2] = 0u;
   }
   return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(__dsqrt_rn(total), eps)));
+}
+
+// A matrix already in X0, unnormalised (blockIdx.y, one block each): its norm from its partials
+// (the same reduction as prep_inv_norm), kept in its stats; its fused-kernel counters zeroed;
+// d = 1 / (||G_b||_F + eps) in fp64, then fp32(d) and fp32(d * d) at words kScaleWord and
+// kScaleWord + 1 of its scratch header for the first step's B'X and X X' epilogues.
+__global__ void __launch_bounds__(256) prep_finalize_kernel(const PrepList L) {
+  __shared__ double red[8];
+  tc::pdl_launch_dependents();
+  tc::pdl_wait();
+  const PrepItem& J = prep_item(L, blockIdx.y);
+  const int mb = static_cast<int>(blockIdx.y) - J.first;
+  const int tid = static_cast<int>(threadIdx.x);
+  const NormWorkspace* ws = prep_ws(J.ws, mb);
+  double a = 0.0;
+  for (int i = tid; i < J.bpm; i += 256) a = __dadd_rn(a, __ldcg(ws->partials + i));  // from L2: another kernel wrote them
+  const double total = sum256(a, tid, red);
+  if (tid == 0) {
+    write_clip_stats(J.stats + mb, total, 0.0f);
+    uint32_t* w = reinterpret_cast<uint32_t*>(J.ws + static_cast<size_t>(mb) * kPrepWsBytes);
+    w[kCntWord] = w[kCntWord + 1] = w[kCntWord + 2] = 0u;
+    const double d = __ddiv_rn(1.0, __dadd_rn(__dsqrt_rn(total), L.eps));
+    float* sc = reinterpret_cast<float*>(w + kScaleWord);
+    sc[0] = __double2float_rn(d);
+    sc[1] = __double2float_rn(__dmul_rn(d, d));
+  }
 }
 
 // X0_b = G_b / (||G_b||_F + eps) in the compute dtype U, same orientation (rows <= cols),
@@ -379,13 +407,15 @@ namespace {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// Launches one list: K selects the kernel (0 sum of squares, 1 scale, 2 transpose).
+// Launches one list: K selects the kernel (0 sum of squares, 1 scale, 2 transpose, 3 the scale
+// of an X0 that arrived unnormalised).
 template <int K, typename T, typename U>
 zopt_status launch_list(PrepList& L, int matrices, long long max_x, cudaStream_t s) {
   if (L.n == 0) return ok();
   const dim3 grid(static_cast<unsigned>(max_x), static_cast<unsigned>(matrices));
   zopt_status st = ZOPT_OK;
   if constexpr (K == 0) st = launch_pdl(prep_sumsq_kernel<T>, grid, dim3(kNormThreads), 0, s, L);
+  else if constexpr (K == 3) st = launch_pdl(prep_finalize_kernel, grid, dim3(256), 0, s, L);
   else if constexpr (K == 1) st = launch_pdl(prep_scale_kernel<T, U>, grid, dim3(256), 0, s, L);
   else if constexpr (std::is_same<U, float>::value)
     st = launch_pdl(prep_transpose_f32_kernel<T>, grid, dim3(32, 8), 0, s, L);
@@ -409,6 +439,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
     const bool u_out = G.f32c == std::is_same<U, float>::value;
     if (!t_in || (K != 0 && !u_out) || (K == 1 && G.transpose) || (K == 2 && !G.transpose)) continue;
     if (K == 0 && G.norm_ready) continue;  // its partials are already in the scratch
+    if ((K == 3) != G.x0_raw && K != 0) continue;  // X0 is in place: only its scale is wanted
     if (L.n == kMaxPrepItems || matrices + G.gs > 65535) {
       if ((st = launch_list<K, T, U>(L, matrices, max_x, s)) != ZOPT_OK) return st;
       matrices = 0;
@@ -435,6 +466,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
     const long long bpm = norm_blocks(rows * cols);
     it.bpm = static_cast<int>(bpm);
     if (K == 0) it.chunks = bpm;
+    else if (K == 3) it.chunks = 1;
     else if (K == 1) it.chunks = it.vec ? ceil_div(rows * (cols / 8), kScaleVecs) : ceil_div(rows * cols, 8LL * kScaleVecs);
     else if (std::is_same<U, float>::value) it.chunks = ceil_div(rows, 64) * ceil_div(cols, 64);
     else it.chunks = ceil_div(rows, 64) * ceil_div(cols, 32LL * (16 / static_cast<long long>(sizeof(T))));
@@ -470,6 +502,7 @@ zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s) {
   if ((st = prep_pass<2, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;
   if ((st = prep_pass<2, float, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
   if ((st = prep_pass<2, float, float>(groups, n, eps, s)) != ZOPT_OK) return st;
+  if ((st = prep_pass<3, __nv_bfloat16, __nv_bfloat16>(groups, n, eps, s)) != ZOPT_OK) return st;
   ZOPT_CUDA_TRY(cudaGetLastError());
   return ok();
 }

@@ -79,8 +79,17 @@ struct GemmArgs {
   double* st_sum;
   unsigned* st_max;
   long long st_stride;
+  // (the first step of a call whose X0 arrives unnormalised) matrix mb's alpha is multiplied by
+  // amat[mb * amat_stride], the matrix's 1 / (||X0|| + eps) or its square; null otherwise
+  const float* amat;
+  long long amat_stride;
   int* err;
 };
+
+// Matrix mb's factor on alpha (1 unless a.amat is set); another launch wrote it.
+__device__ __forceinline__ float amat_of(const GemmArgs& a, int mb) {
+  return a.amat != nullptr ? __ldcg(a.amat + static_cast<long long>(mb) * a.amat_stride) : 1.0f;
+}
 
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& mb, int& ti, int& tj) {
   mb = t / a.tiles_per_mat;  // matrix-major order: the tiles running together share operands
@@ -411,11 +420,14 @@ __device__ __forceinline__ void prefetch_r_first(const GemmArgs& a, int mb, int 
 // squares of the values it stores (as stored: bf16-rounded unless a.d_f32; fp32 pairwise over
 // runs of 8, exact fp64 outside the safe range, the runs in fp64) and takes their largest
 // magnitude, and writes both to slot st_slot of matrix mb (every block the warp skips adds 0).
+// use_amat: alpha takes the matrix's factor amat_of(a, mb) (a persistent launch whose products
+// serve every step passes false after the first step).
 template <bool kSlice, int kPairs = 2, bool kRegR = false, bool kStreamOut = false>
 __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMap* tmD, uint8_t* mine, uint32_t taddr,
                                              int i0, int tj, int mb, bool has_r, int lane, int& last_par,
                                              int c_begin = 0, int c_end = BN / 32, const uint4* rfirst = nullptr,
-                                             int st_slot = -1) {
+                                             int st_slot = -1, bool use_amat = true) {
+  const float alpha = use_amat ? a.alpha * amat_of(a, mb) : a.alpha;
   double st_acc = 0.0;
   unsigned st_mx = 0;
   uint4 rc[4];  // kRegR: R's piece for the block being processed
@@ -445,7 +457,7 @@ __device__ __forceinline__ void epi_tile_tma(const GemmArgs& a, const CUtensorMa
     tc::tmem_wait_ld();
     float o[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = a.alpha * __uint_as_float(v[k]);
+    for (int k = 0; k < 32; ++k) o[k] = alpha * __uint_as_float(v[k]);
     const int par = kPairs == 2 ? (c & 1) : 0;
     uint8_t* dbox = kSlice ? mine + c * kBox : mine + 2 * par * kBox;
     uint8_t* mbox = kSlice ? mine + (8 + par) * kBox : dbox + kBox;
@@ -643,6 +655,8 @@ constexpr int kFusedProducts = 4;  // X X', B', B'X, and B'X of the last step (t
 constexpr int kFusedEpiWarps = 8;
 constexpr int kFusedThreads = 32 * (2 + kFusedEpiWarps);
 constexpr int kCntWord = 16;       // counters at word 16 of each matrix's prep scratch header
+// (X0 that arrives unnormalised) 1 / (||X0|| + eps) and its square, fp32, at words 24 and 25
+constexpr int kScaleWord = 24;
 constexpr int kMaxFusedJobs = 6;
 
 struct FusedJobMaps {
@@ -764,6 +778,7 @@ struct Group {
   zopt_dtype io;      // the input's dtype
   zopt_dtype out_io;  // the output's dtype
   bool norm_ready;    // the matrices' norm partials are already in the prep scratch
+  bool x0_raw;        // the matrices are already in X0, unnormalised (bf16; norm_ready too)
   long long rows, cols, ld_g, ld_x, bs_g, bs_x;
   int gs;
   bool f32c, transpose, pair, out_tma;
