@@ -502,7 +502,8 @@ def config_lines(Z, torch, stream, pk, K: int) -> dict:
     on a bf16 gradient (30 B/element; the adamw_kernel alone 28 B) with a 256 MB L2 flush between
     iterations, except the tiny set, which is timed L2-resident and makes no roofline claim; the
     tiny decoder's and the GPT-2-small body's Newton-Schulz sets, and the GPT-2-small body's Muon
-    step, against the burst bf16 peak (each call lasts about a millisecond)."""
+    step, against the burst bf16 peak (each call lasts about a millisecond; at least 300 calls
+    are timed, with the SM clock sampled)."""
     import statistics as stats_
 
     import workloads
@@ -552,35 +553,39 @@ def config_lines(Z, torch, stream, pk, K: int) -> dict:
         del p, m, v, g, out, ws
 
     def timed_calls(run):
+        # calls of about a millisecond: at least 300 of them (~0.3 s) so that the clock sampler
+        # sees a few readings
         for _ in range(3):
             run(stream)
         torch.cuda.synchronize()
-        evs = [(mk(), mk()) for _ in range(K)]
-        for a, b in evs:
-            a.record(stream)
-            run(stream)
-            b.record(stream)
-        torch.cuda.synchronize()
-        return stats_.mean(a.elapsed_time(b) for a, b in evs)
+        evs = [(mk(), mk()) for _ in range(max(K, 300))]
+        with Clocks(smi_id(torch.cuda.current_device())) as clk_c:
+            for a, b in evs:
+                a.record(stream)
+                run(stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+        return stats_.mean(a.elapsed_time(b) for a, b in evs), clk_c.summary()
 
     for name in ("c1", "c2"):
         nsp = NsPart(Z, torch, 9000, 5, 0, name)
-        ms_ = timed_calls(nsp.run)
+        ms_, clk_ = timed_calls(nsp.run)
         tf = nsp.flops / (ms_ * 1e-3) / 1e12
         res[name]["ns"] = {"what": f"{sum(G.shape[0] for G, _ in nsp.groups)} bf16 matrices "
                                    f"{[tuple(G.shape[1:]) for G, _ in nsp.groups]}, one zopt_ns_orthogonalize_many "
                                    "call, 5 steps", "ms": round(ms_, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
                            "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
-                           "peak_source": pk["source"] + " bf16 burst"}
+                           "peak_source": pk["source"] + " bf16 burst", "calls_timed": max(K, 300), "clocks": clk_}
         if name == "c1":
             res[name]["ns"]["note"] = "the set is 3.4 MB (L2-resident) and latency-bound: no roofline claim"
         del nsp
     mu2 = MuonPart(Z, torch, 9100, "c2")
-    ms_ = timed_calls(mu2.run)
+    ms_, clk_ = timed_calls(mu2.run)
     tf = mu2.flops / (ms_ * 1e-3) / 1e12
     res["c2"]["muon_step"] = {"what": mu2.what, "ms": round(ms_, 4), "ns_equivalent_tflops": round(tf, 1),
                               "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
                               "peak_source": pk["source"] + " bf16 burst",
+                              "calls_timed": max(K, 300), "clocks": clk_,
                               "note": "the whole step's time against the Newton-Schulz flops alone"}
     del mu2
     torch.cuda.empty_cache()
@@ -733,17 +738,22 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
     # one Muon step (zopt_muon_step_many: momentum, Newton-Schulz, statistics, guarded update,
     # bf16 round-out) over the matrices rank 0 of the 1.1B Llama-style set owns, timed apart
     mu_ms, mu = 0.0, None
+    mu_clocks = None
     if "muon" in parts:
+        # ~3 ms a step: 200 steps (~0.6 s, 2.7 GB touched a step, far above L2) give the clock
+        # sampler a few readings
         mu = MuonPart(Z, torch, 7000 + rank)
         for _ in range(3):
             mu.run(stream)
         torch.cuda.synchronize()
-        ev_m = [(mk(), mk()) for _ in range(max(K, 3))]
-        for a_ev, b_ev in ev_m:
-            a_ev.record(stream)
-            mu.run(stream)
-            b_ev.record(stream)
-        torch.cuda.synchronize()
+        ev_m = [(mk(), mk()) for _ in range(max(K, 200))]
+        with Clocks(smi_id(local_rank)) as clk_m:
+            for a_ev, b_ev in ev_m:
+                a_ev.record(stream)
+                mu.run(stream)
+                b_ev.record(stream)
+            torch.cuda.synchronize()
+        mu_clocks = clk_m.summary()
         mu_ms = mean(ev_m)
     # the smaller parameter sets (tiny decoder, GPT-2-small, the 1.1B set's rank 0), timed apart
     cfg = config_lines(Z, torch, stream, peaks(), max(K, 3)) if "configs" in parts and rank == 0 else None
@@ -948,9 +958,10 @@ def run_ours(args, rank: int, world_procs: int, local_rank: int) -> None:
         line["muon_step"] = {"what": mu.what, "ms": round(mu_ms, 4), "matrices": mu.count,
                              "ns_algorithmic_flops": mu.flops,
                              "ns_equivalent_tflops": round(mu.flops / (mu_ms * 1e-3) / 1e12, 1),
-                             "elementwise_bytes": mu.bytes,
-                             "note": "the whole step's time against the Newton-Schulz flops alone; the momentum, "
-                                     "statistics and update passes move elementwise_bytes besides"}
+                             "elementwise_bytes": mu.bytes, "steps_timed": max(K, 200), "clocks": mu_clocks,
+                             "note": "the whole step's time against the Newton-Schulz flops alone; the momentum and "
+                                     "update passes move elementwise_bytes besides (U's statistics come from the last "
+                                     "product's epilogue)"}
     line["clocks"] = clocks
     e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if "adamw" in parts:
