@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int b = n & 1;
       const uint32_t tph = static_cast<uint32_t>(n >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, f.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_idle(tfull + b, tph, f.err) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       tc::fence_after_sync();
       const int cur = it.s & 1;

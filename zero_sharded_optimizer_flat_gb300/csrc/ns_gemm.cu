@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_idle(tfull + b, tph, a.err) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       if (rpend) {  // every lane waits, so that each sees the TMA's writes
         if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(rb, rph, a.err) ? 1 : 0)) break;
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, a.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_idle(tfull + b, tph, a.err) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc::fence_after_sync();
@@ -306,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
-      tc::mbar_init(tempty + b, 256);  // the epilogue threads of both CTAs (used in the leader)
+      tc::mbar_init(tempty + b, 8);  // the epilogue warps of both CTAs, one arrival each (used in the leader)
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
@@ -442,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_idle(tfull + b, tph, err) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       tc::fence_after_sync();
       const int j = pair_job_of(B, t);
@@ -457,7 +457,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           a, &B.job[j].D, mine, tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(b * BN),
           tp * BM2 + rows0, tj, mb, has_r(a), lane, last_par, 0, BN / 32, r0, st_slot);
       tc::fence_before_sync();
-      tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
+      __syncwarp();  // every lane's TMEM reads are done: one arrival releases the warp's part
+      if (lane == 0) tc::mbar_arrive_cluster(tempty_leader[b]);  // the leader's MMA thread may reuse this accumulator
       if (t + npairs < total) first_r(t + npairs);
     }
     if (lane == 0) tc::bulk_wait_all();  // every store has reached global memory
@@ -473,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int b = it & 1;
       const uint32_t tph = static_cast<uint32_t>(it >> 1) & 1u;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(tfull + b, tph, err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_idle(tfull + b, tph, err) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc::fence_after_sync();
@@ -493,7 +494,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc::tmem_wait_ld();
         if (c == BN / 32 - 1) {
           tc::fence_before_sync();
-          tc::mbar_arrive_cluster(tempty_leader[b]);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive_cluster(tempty_leader[b]);
         }
         epilogue32(am, i, tj * BN + 32 * c, v, stage_base + (warp - 2) * kStageWarp, lane);
       }

@@ -76,6 +76,37 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, in
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
+// try_wait that lets the thread sleep up to `hint_ns` (it wakes when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a thread with nothing else to do for a while (an epilogue warp waiting for the
+// next accumulator): each try sleeps up to 2 us instead of returning to a spin, so the waiting
+// warp leaves its scheduler's issue slots to the TMA and MMA threads it shares them with. Same
+// bounds and error reporting as mbar_wait_for.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
+    if ((spin & 63u) == 0) {
+      const unsigned long long el = globaltimer() - t0;
+      if (el > 1000000ull && *reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (el > kWaitLimitNs) {
+        atomicExch(err, 1);
+        return false;
+      }
+    }
+  }
+}
 
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
