@@ -8,14 +8,20 @@
 //
 // Four steps on the caller's stream, each one launch for every job of a call (for a single
 // shape: per group of matrices, as many as the workspace holds):
-//   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 14-16 B/elem);
-//      each block also sums its share of u^2 into the Newton-Schulz norm's partial sums, so
-//      the normalisation does not read u a second time
-//   2. U = NewtonSchulz(u): fp32 u in, bf16 tensor cores, U written in bf16 (the bf16 method
-//      rounds every product, its last one included, to bf16)
-//   3. per matrix: partial sums of squares and largest magnitudes of U     (2 B/elem)
+//   1. momentum:  buf = mu*buf + g;  u = g + mu*buf (Nesterov) or buf      (fp32, 12-14 B/elem);
+//      u leaves rounded to bf16 (the dtype Newton-Schulz computes in), straight into
+//      Newton-Schulz's input buffer where the shape allows (not tall, cols a multiple of 8),
+//      and each block sums its share of the bf16 u^2 into the Newton-Schulz norm's partial
+//      sums, so no pass reads u a second time
+//   2. U = NewtonSchulz(u): bf16 u in, bf16 tensor cores, U written in bf16 (the bf16 method
+//      rounds every product, its last one included, to bf16); the first step's products apply
+//      the normalisation of an input written in place, and the last product's epilogue writes
+//      U's per-warp sums of squares and largest magnitudes
+//   3. only for a job whose last product ran elsewhere: those statistics from a pass over U
+//      (2 B/elem)
 //   4. p = p*fp32(1 - lr*wd) - fp32(lr*scale)*U unless rejected; bf16 round-out (12 B/elem);
-//      each block first reduces its matrix's partials in a fixed order (no atomics, no memset)
+//      each block first reduces its matrix's statistics slots in a fixed order (no atomics,
+//      no memset)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
