@@ -27,6 +27,10 @@
 // one launch of the single-CTA GEMM (ns_gemm.cu). The
 // tile geometry and the epilogue building blocks they share are in ns_tile.cuh. Every wait is
 // bounded; a timeout sets an error word that the next call reports as ZOPT_ETIMEOUT.
+// Callers inside the library (the Muon step) may hand a job's norm partials already summed, or
+// its X0 already in place and unnormalised (then one small launch turns the partials into the
+// scale that the first step's X X' and B'X epilogues apply), and may collect the statistics of
+// the last product's output from its epilogue (orthogonalize_many).
 #include <cstring>
 
 #include "ns_tile.cuh"
