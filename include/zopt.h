@@ -272,8 +272,11 @@ ZOPT_API zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* m
  * A = X X' (m x m), B = b A + c A A', X = a X + B X. With compute_dtype ZOPT_BF16 the
  * operands and the products A, B, X are bf16 (round-to-nearest-even) with fp32 accumulation
  * on the tensor cores, and the last two are formed as B' = B + a I and X = B' X (the same
- * map; B' is rounded to bf16 once). ZOPT_F32 computes the products as written. (a, b, c) = abc[0..2] (the pages print no triple; the usual quintic
- * Muon choice is 3.4445, -4.7750, 2.0315).
+ * map; B' is rounded to bf16 once). A bf16 G in X's orientation (rows <= cols) with 16-byte
+ * aligned rows and matrices is read in place by the first step, whose X X' and B'X apply
+ * 1/(||G||+eps) (squared for X X') to their fp32 accumulators: X0 is then not rounded to bf16
+ * on its own. ZOPT_F32 computes the products as written. (a, b, c) = abc[0..2] (the pages print
+ * no triple; the usual quintic Muon choice is 3.4445, -4.7750, 2.0315).
  * ====================================================================================== */
 
 /* Size limits of one Newton-Schulz (or Muon) matrix, under which every tile coordinate and

@@ -74,8 +74,13 @@ def test_one_step_white_box(zopt, rows, cols):
     ref0 = Gd / (torch.linalg.norm(Gd) + 1e-7)
     if rows > cols:
         ref0 = ref0.T
-    X0 = region(ws, p["x0"], m, p["ldx"], n)
-    assert rel(X0, ref0) < 4e-3
+    if rows <= cols and cols % 8 == 0:
+        # a bf16 input in X's orientation with 16-byte rows is read in place by the first step,
+        # whose products apply the normalisation: X0 is never stored
+        X0 = ref0.float()
+    else:
+        X0 = region(ws, p["x0"], m, p["ldx"], n)
+        assert rel(X0, ref0) < 4e-3
     A = region(ws, p["a"], m, p["lda"], m)
     assert torch.equal(A, A.T)
     assert rel(A, X0 @ X0.T) < 4e-3

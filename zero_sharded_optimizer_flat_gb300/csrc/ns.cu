@@ -167,6 +167,7 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
   const long long osz = static_cast<long long>(G.osz);
   G.out_tma = !G.f32c && (reinterpret_cast<uintptr_t>(G.xo) & 15u) == 0 && (G.ld_x * osz) % 16 == 0 &&
               (G.gs == 1 || (G.bs_x * osz) % 16 == 0);
+  G.g_in_place = false;
   if (G.f32c) return ok();
   const long long mb = static_cast<long long>(p.per_mat), grp = p.group;
   for (int q = 0; q < 2; ++q) {
@@ -181,6 +182,16 @@ zopt_status group_init(Group& G, const Plan& p, uint8_t* ws) {
   if ((st = make_map(&G.mb_p, G.B, p.m, p.m, p.lda, grp, mb, 64, BM)) != ZOPT_OK) return st;
   if ((st = make_map(&G.ma_e, G.A, p.m, p.m, p.lda, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
   if ((st = make_map(&G.mb_e, G.B, p.m, p.m, p.lda, grp, mb, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != ZOPT_OK) return st;
+  // A bf16 input in X's orientation whose rows and matrices the TMA can address is read in
+  // place by the first step, which also normalises it: no copy of it into X0.
+  G.g_in_place = !G.x0_raw && G.io == ZOPT_BF16 && !G.transpose && (reinterpret_cast<uintptr_t>(G.g) & 15u) == 0 &&
+                 (G.ld_g * 2) % 16 == 0 && (G.gs == 1 || (G.bs_g * 2) % 16 == 0);
+  if (G.g_in_place) {
+    const long long gb = (G.gs == 1 ? p.m * G.ld_g : G.bs_g) * 2;
+    if ((st = make_map(&G.mg_p, G.g, p.n, p.m, G.ld_g, G.gs, gb, 64, BM)) != ZOPT_OK) return st;
+    if ((st = make_map(&G.mg_q, G.g, p.n, p.m, G.ld_g, G.gs, gb, 64, BN)) != ZOPT_OK) return st;
+    if ((st = make_map(&G.mg_mn, G.g, p.n, p.m, G.ld_g, G.gs, gb, 64, BK)) != ZOPT_OK) return st;
+  }
   if (G.out_tma) {
     const long long xrows = G.transpose ? p.n : p.m, xcols = G.transpose ? p.m : p.n;  // the caller's shape
     const long long ob = (G.gs == 1 ? xrows * G.ld_x : G.bs_x) * osz;
@@ -216,6 +227,12 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
   m.bp = G.mb_p;
   m.be = G.mb_e;
   m.oe = G.mo_e;
+  if (G.g_in_place) {
+    m.gp = G.mg_p;
+    m.gq = G.mg_q;
+    m.gmn = G.mg_mn;
+  }
+  job.x0_is_g = G.g_in_place ? 1 : 0;
   const int mm = static_cast<int>(G.p.m), n = static_cast<int>(G.p.n);
   GemmArgs g0{};
   g0.group = G.gs;
@@ -231,7 +248,7 @@ void group_job(const Group& G, const Coef& k, int* err, FusedJob& job, FusedJobM
   GemmArgs& px = job.prod[2];  // X = B' X
   px = g0;
   px.M = mm; px.N = n; px.K = mm; px.b_mn_major = 1;
-  if (G.x0_raw) {  // the first step normalises: A by 1 / (||X0|| + eps)^2, B'X by 1 / (||X0|| + eps)
+  if (first_scales(G)) {  // the first step normalises: A by 1 / (||X0|| + eps)^2, B'X by 1 / (||X0|| + eps)
     pa.amat = x0_scale(G, true);
     px.amat = x0_scale(G, false);
     pa.amat_stride = px.amat_stride = kScaleStride;
@@ -254,14 +271,14 @@ int pair_job(const Group& G, const Coef& k, int prod, bool first, bool last, int
   a.err = err;
   a.group = G.gs;
   a.alpha = 1.0f;
-  if (first && G.x0_raw && prod != 1) {
+  if (first && first_scales(G) && prod != 1) {
     a.amat = x0_scale(G, prod == 0);
     a.amat_stride = kScaleStride;
   }
   if (prod == 0) {
     a.M = m; a.N = m; a.K = n; a.symmetric = 1;
     a.D = G.A; a.ldd = G.p.lda; a.d_stride = mat_elems;
-    J.P = J.Q = J.R = G.mx_p[cur];
+    J.P = J.Q = J.R = first && G.g_in_place ? G.mg_p : G.mx_p[cur];
     J.D = G.ma_e;
     return kEpiTma;
   }
@@ -282,7 +299,7 @@ int pair_job(const Group& G, const Coef& k, int prod, bool first, bool last, int
   a.d_f32 = last && G.out_io == ZOPT_F32 ? 1 : 0;
   a.d_trans = last && G.transpose ? 1 : 0;
   J.P = G.mb_p;
-  J.Q = J.R = G.mx_mn[cur];
+  J.Q = J.R = first && G.g_in_place ? G.mg_mn : G.mx_mn[cur];
   J.D = last ? G.mo_e : G.mx_e[cur ^ 1];
   return (!last || G.out_tma) ? kEpiTma : kEpiRegs;
 }
@@ -372,14 +389,17 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       GemmArgs ga{};
       ga.err = err;
       ga.group = gs;
-      const bool norm_here = it == 0 && G.x0_raw;  // this step normalises X0
+      const bool norm_here = it == 0 && first_scales(G);  // this step normalises X0
+      const bool from_g = it == 0 && G.g_in_place;       // and reads it from the caller's G
       ga.amat_stride = kScaleStride;
       // A = X X'
       ga.amat = norm_here ? x0_scale(G, true) : nullptr;
       ga.M = m; ga.N = m; ga.K = n;
       ga.symmetric = 1; ga.b_mn_major = 0; ga.alpha = 1.0f; ga.beta = 0.0f; ga.diag = 0.0f; ga.R = nullptr;
       ga.ldr = 0; ga.r_stride = 0; ga.D = G.A; ga.ldd = p.lda; ga.d_stride = mat_elems; ga.d_f32 = 0; ga.d_trans = 0;
-      if ((st = launch_gemm(G.mx_p[cur], G.mx_q[cur], nullptr, &G.ma_e, kEpiTma, ga, s)) != ZOPT_OK) return st;
+      if ((st = launch_gemm(from_g ? G.mg_p : G.mx_p[cur], from_g ? G.mg_q : G.mx_q[cur], nullptr, &G.ma_e, kEpiTma, ga,
+                            s)) != ZOPT_OK)
+        return st;
       // B' = c A A' + b A + a I: the step's a X term joins the last product as (B + a I) X.
       // On single CTAs b A rides in the accumulator as c (h1 + h2) A (identity MMAs, h1 + h2 =
       // b / c to about 2^-18), so B' needs no second input and keeps the four-stage ring.
@@ -404,7 +424,7 @@ zopt_status group_products(const Group& G, const Coef& k, int steps, int* err, c
       ga.D = xnext; ga.ldd = ldnext; ga.d_stride = dstr_next; ga.d_f32 = next_f32; ga.d_trans = next_trans;
       const int x_epi = (!last || G.out_tma) ? kEpiTma : kEpiRegs;
       const CUtensorMap* xd = last ? &G.mo_e : &G.mx_e[cur ^ 1];
-      if ((st = launch_gemm(G.mb_p, G.mx_mn[cur], nullptr, xd, x_epi, ga, s)) != ZOPT_OK) return st;
+      if ((st = launch_gemm(G.mb_p, from_g ? G.mg_mn : G.mx_mn[cur], nullptr, xd, x_epi, ga, s)) != ZOPT_OK) return st;
     }
     cur ^= 1;
   }

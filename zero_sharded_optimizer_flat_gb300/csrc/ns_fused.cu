@@ -49,6 +49,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       tc::prefetch_tmap(&m.bp);
       tc::prefetch_tmap(&m.be);
       tc::prefetch_tmap(&m.oe);
+      if (f.job[j].x0_is_g) {
+        tc::prefetch_tmap(&m.gp);
+        tc::prefetch_tmap(&m.gq);
+        tc::prefetch_tmap(&m.gmn);
+      }
     }
   }
   if (warp == 1) {
@@ -81,8 +86,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         const int cur = it.s & 1;
         const FusedJobMaps& m = mp.job[it.j];
-        const CUtensorMap* P = it.p == 0 ? &m.xp[cur] : (it.p == 1 ? &m.ap : &m.bp);
-        const CUtensorMap* Q = it.p == 0 ? &m.xq[cur] : (it.p == 1 ? &m.aq : &m.xmn[cur]);
+        const bool from_g = it.s == 0 && f.job[it.j].x0_is_g;  // the first step reads the caller's G
+        const CUtensorMap* P = it.p == 0 ? (from_g ? &m.gp : &m.xp[cur]) : (it.p == 1 ? &m.ap : &m.bp);
+        const CUtensorMap* Q =
+            it.p == 0 ? (from_g ? &m.gq : &m.xq[cur]) : (it.p == 1 ? &m.aq : (from_g ? &m.gmn : &m.xmn[cur]));
         const int nk = (a.K + BK - 1) / BK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty + s, ph ^ 1u, f.err)) {

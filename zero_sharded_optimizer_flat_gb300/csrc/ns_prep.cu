@@ -439,7 +439,7 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
     const bool u_out = G.f32c == std::is_same<U, float>::value;
     if (!t_in || (K != 0 && !u_out) || (K == 1 && G.transpose) || (K == 2 && !G.transpose)) continue;
     if (K == 0 && G.norm_ready) continue;  // its partials are already in the scratch
-    if ((K == 3) != G.x0_raw && K != 0) continue;  // X0 is in place: only its scale is wanted
+    if ((K == 3) != first_scales(G) && K != 0) continue;  // X0 is in place: only its scale is wanted
     if (L.n == kMaxPrepItems || matrices + G.gs > 65535) {
       if ((st = launch_list<K, T, U>(L, matrices, max_x, s)) != ZOPT_OK) return st;
       matrices = 0;

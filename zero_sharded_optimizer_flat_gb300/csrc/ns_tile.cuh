@@ -662,6 +662,7 @@ constexpr int kMaxFusedJobs = 6;
 struct FusedJobMaps {
   CUtensorMap xp[2], xq[2], xmn[2], xe[2];  // X (either buffer): operand boxes, epilogue boxes
   CUtensorMap ap, aq, ae, bp, be, oe;       // A, B' and the caller's X
+  CUtensorMap gp, gq, gmn;                  // the caller's G as the first step's X (g_in_place)
 };
 struct FusedMaps {
   FusedJobMaps job[kMaxFusedJobs];
@@ -670,6 +671,7 @@ struct FusedMaps {
 struct FusedJob {
   GemmArgs prod[kFusedProducts];
   uint8_t* prep;  // per-matrix prep scratch (kPrepWsBytes apart); counters at kCntWord
+  int x0_is_g;    // the first step reads the caller's G in place (maps gp, gq, gmn)
 };
 
 struct FusedArgs {
@@ -779,6 +781,7 @@ struct Group {
   zopt_dtype out_io;  // the output's dtype
   bool norm_ready;    // the matrices' norm partials are already in the prep scratch
   bool x0_raw;        // the matrices are already in X0, unnormalised (bf16; norm_ready too)
+  bool g_in_place;    // the first step reads the caller's G itself as X0 (maps mg_*), unnormalised
   long long rows, cols, ld_g, ld_x, bs_g, bs_x;
   int gs;
   bool f32c, transpose, pair, out_tma;
@@ -789,7 +792,13 @@ struct Group {
   zopt_clip_stats* stats;
   uint8_t *xb[2], *A, *B;
   CUtensorMap mx_p[2], mx_q[2], mx_mn[2], mx_e[2], ma_p, ma_q, mb_p, ma_e, mb_e, mo_e;
+  CUtensorMap mg_p, mg_q, mg_mn;  // g_in_place: G with the boxes of mx_p, mx_q, mx_mn
 };
+
+// Whether the group's first step normalises its X0 (X0 unnormalised in the workspace, or the
+// caller's G read in place): its X X' and B'X epilogues apply 1 / (||X0|| + eps), squared for
+// X X', which the prep scratch holds.
+inline bool first_scales(const Group& G) { return G.x0_raw || G.g_in_place; }
 
 // X0 = G / (||G||_F + eps), oriented, for every matrix of n groups (a handful of launches in all).
 zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s);
