@@ -42,11 +42,11 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
 ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
 # DRAM bytes of one zopt_ns_orthogonalize_many call over the 48-matrix stress set (dram__bytes_read.sum
-# + dram__bytes_write.sum summed over its 18 launches, one ncu pass on the full set), valid while
+# + dram__bytes_write.sum summed over its launches, one ncu pass on the full set), valid while
 # the Newton-Schulz sources hash to NS_SRC_DIGEST
 NS_SOURCES = ("ns.cu", "ns_gemm.cu", "ns_prep.cu", "ns_tile.cuh", "tc.cuh", "launch.cuh", "norm_impl.cuh")
-NS_TRAFFIC_PER_CALL = 178685804800 + 41426809600
-NS_SRC_DIGEST = "9e5aa6a89f26bf39"
+NS_TRAFFIC_PER_CALL = 258872122112 + 39090095616
+NS_SRC_DIGEST = "dec280e343d3c1ca"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 # two parts to a pass: the first pair reads 2 x 2 and writes 4; each later pair also reads the sum
