@@ -217,6 +217,30 @@ def test_grouped_batch_pair_kernel(zopt):
     assert rel(X[1].cpu(), torch.from_numpy(ref)) <= 2e-2
 
 
+@pytest.mark.parametrize("rows,cols,abc", [(256, 768, DEFAULT_ABC), (1024, 1536, DEFAULT_ABC),
+                                            (512, 1024, (1.5, -0.5, 0.0))])
+def test_first_step_reads_g_in_place_grouped_and_strided(zopt, rows, cols, abc):
+    """A bf16 input no taller than wide, with 16-byte rows, is read in place by the first step
+    (through its own tensor maps, with the caller's pitch and batch stride) on every product
+    path: the fused launch (256 x 768), the CTA-pair launches (1024 x 1536), the single-CTA
+    launches (a zero c rules out the identity MMAs). Rows padded to ld = cols + 16, three rows'
+    gap between matrices, a workspace for groups of 2 over a batch of 3: every matrix bitwise the
+    contiguous single call's, and within the tolerance of the fp64 oracle."""
+    batch, ld, gap = 3, cols + 16, 3
+    flat = torch.randn(batch * (rows + gap) * ld, device="cuda").to(torch.bfloat16)
+    G = flat.view(batch, rows + gap, ld)[:, :rows, :cols]
+    X = torch.empty(batch, rows, cols, device="cuda", dtype=torch.bfloat16)
+    zopt.ns_orthogonalize(G, X, zopt.new_ns_workspace(rows, cols, group=2), steps=5, abc=abc)
+    ws1 = zopt.new_ns_workspace(rows, cols)
+    for b in range(batch):
+        one = torch.empty(rows, cols, device="cuda", dtype=torch.bfloat16)
+        zopt.ns_orthogonalize(G[b].contiguous(), one, ws1, steps=5, abc=abc)
+        torch.cuda.synchronize()
+        assert torch.equal(one, X[b]), b
+        ref = newton_schulz(G[b].double().cpu().numpy(), steps=5, abc=abc)
+        assert rel(X[b].cpu(), torch.from_numpy(ref)) <= 2e-2, b
+
+
 def test_deterministic(zopt):
     G = gaussian(768, 3072, 1)
     ws = zopt.new_ns_workspace(768, 3072)
