@@ -1,10 +1,11 @@
 // Newton-Schulz preparation: the Frobenius norm of every matrix and X0 = G / (||G|| + eps) in
-// the compute dtype, transposed for a tall matrix — three launches for every matrix of every
-// job of a call (sum of squares; scaling of the wide; transposition of the tall). Every thread
-// keeps 128 bytes of loads in flight, and the normalising kernels issue their first loads
-// before they reduce the norm. A matrix that its caller has already put in X0 unnormalised
-// (with its norm partials) takes a fourth, small launch instead: its scale, which the first
-// step's products apply.
+// the compute dtype, transposed for a tall matrix — a few launches for every matrix of every
+// job of a call: the sum of squares (unless the caller supplies the partial sums); then X0 by
+// scaling (an input the first step cannot read in place: fp32, or rows the TMA cannot address)
+// or by transposition (a tall input); or, where the first step reads the input in place (a
+// bf16 G no taller than wide, or X0 that the caller wrote unnormalised), only the scale that
+// the first step's products apply, from a small launch. Every thread keeps 128 bytes of loads
+// in flight, and the normalising kernels issue their first loads before they reduce the norm.
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
@@ -488,8 +489,9 @@ zopt_status prep_pass(const Group* groups, int n, float eps, cudaStream_t s) {
 
 // X0 = G / (||G||_F + eps), oriented, for every matrix of every group: one sum-of-squares launch
 // per input dtype, then one scaling and one transpose launch per input and compute dtype that
-// occur (each matrix's partial sums are reduced by the blocks that normalise it; its block 0
-// also zeroes its counters for the fused kernel).
+// occur, and one launch of the first step's scales (each matrix's partial sums are reduced by
+// the blocks that normalise it or by its finalize block; block 0 of a matrix also zeroes its
+// counters for the fused kernel).
 zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s) {
   zopt_status st = ZOPT_OK;
   if ((st = prep_pass<0, __nv_bfloat16, float>(groups, n, eps, s)) != ZOPT_OK) return st;

@@ -800,7 +800,8 @@ struct Group {
 // X X', which the prep scratch holds.
 inline bool first_scales(const Group& G) { return G.x0_raw || G.g_in_place; }
 
-// X0 = G / (||G||_F + eps), oriented, for every matrix of n groups (a handful of launches in all).
+// X0 = G / (||G||_F + eps), oriented, for every matrix of n groups, or the scale with which the
+// first step normalises an X0 it reads in place (a handful of launches in all).
 zopt_status group_prep(const Group* groups, int n, float eps, cudaStream_t s);
 
 
