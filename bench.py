@@ -39,8 +39,8 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 # dram__bytes_write.sum on a 64 Mi-element shard prefix, 1.9 GB per launch, scaled by the element
 # count), valid while the kernel's sources hash to ADAMW_SRC_DIGEST (otherwise the traffic is
 # reported as null)
-ADAMW_TRAFFIC_PER_ELEM = (1073822848 + 881548544) / 67108864
-ADAMW_SRC_DIGEST = "4ef9f62bb93eaf69"
+ADAMW_TRAFFIC_PER_ELEM = (1073795712 + 881538688) / 67108864
+ADAMW_SRC_DIGEST = "54ebf47afe0cecf6"
 # DRAM bytes of one zopt_ns_orthogonalize_many call over the 48-matrix stress set (dram__bytes_read.sum
 # + dram__bytes_write.sum summed over its launches, one ncu pass on the full set), valid while
 # the Newton-Schulz sources hash to NS_SRC_DIGEST
@@ -499,7 +499,8 @@ def config_lines(Z, torch, stream, pk, K: int) -> dict:
     """The smaller parameter sets, each timed apart (3 untimed then K timed iterations, CUDA
     events on the launching stream): the tiny decoder (1,048,832-element shard), the GPT-2-small
     set (38,652,672) and the 1.1B set's rank 0 of 8 (8,200,448) take norm/clip and the AdamW step
-    on a bf16 gradient (30 B/element; the adamw_kernel alone 28 B) with a 256 MB L2 flush between
+    on a bf16 gradient (30 B/element; the adamw_kernel alone 28 B), as two calls and as the one
+    call zopt_adamw_clip_step, with a 256 MB L2 flush between
     iterations, except the tiny set, which is timed L2-resident and makes no roofline claim; the
     tiny decoder's and the GPT-2-small body's Newton-Schulz sets, and the GPT-2-small body's Muon
     step, against the burst bf16 peak (each call lasts about a millisecond; at least 300 calls
@@ -549,8 +550,28 @@ def config_lines(Z, torch, stream, pk, K: int) -> dict:
                                  "bytes_per_element": 28, "avg_launch_ms": round(kern_ms, 4)}
         else:
             entry["adamw_kernel"] = {"ms": round(kern_ms, 4), "achieved": round(kern, 1), "unit": "GB/s"}
+        # the same step through zopt_adamw_clip_step: the norm / clip reduction and the update in
+        # one launch (same bytes; the gradient's second read mostly from L2)
+        cws = Z.new_adamw_clip_workspace(S)
+        evs = [(mk(), mk()) for _ in range(3 + K)]
+        for i, (e0, e1) in enumerate(evs):
+            if not resident:
+                flush.zero_()
+            e0.record(stream)
+            Z.adamw_clip_step(lay, table, p, m, v, g, out, lr=w.lr_at(i % w.steps), max_norm=w.max_norm, ws=cws,
+                              clip_stats=clip, adam_state=state, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
+                              weight_decay=w.weight_decay, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        fused_ms = stats_.mean(e0.elapsed_time(e1) for e0, e1 in evs[3:])
+        fused = BF16_STEP_BYTES * S / (fused_ms * 1e-3) / 1e9
+        entry["adamw_clip_step"] = {"what": "zopt_adamw_clip_step (the same step in one launch)",
+                                    "ms": round(fused_ms, 4), "bytes_per_element": BF16_STEP_BYTES,
+                                    "achieved": round(fused, 1), "unit": "GB/s"}
+        if not resident:
+            entry["adamw_clip_step"]["frac"] = round(fused / pk["hbm_gbs"], 4)
         res[name] = entry
-        del p, m, v, g, out, ws
+        del p, m, v, g, out, ws, cws
 
     def timed_calls(run):
         # calls of about a millisecond: at least 300 of them (~0.3 s) so that the clock sampler

@@ -7,7 +7,8 @@
  *   2. the gradient norm / clip / found_inf stats (zopt_grad_norm_clip, zopt_clip_finalize,
  *      zopt_grad_accumulate / zopt_grad_accumulate2 for micro-step sums with the stats fused;
  *      device values)
- *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step, zopt_adamw_rescale_step)
+ *   3. the fused AdamW update of the fp32 shard   (zopt_adamw_step, zopt_adamw_clip_step,
+ *                                                 zopt_adamw_rescale_step)
  *   4. Muon's quintic Newton-Schulz               (zopt_ns_orthogonalize, _many)
  *   5. Muon's update around Newton-Schulz         (zopt_muon_step, _many)
  *
@@ -244,6 +245,31 @@ ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d
                             uint16_t* out_bf16, const zopt_adamw_hparams* hparams,
                             const zopt_clip_stats* d_clip, zopt_adam_state* d_state, zopt_stream stream);
 
+/* Workspace bytes zopt_adamw_clip_step needs for a shard of shard_len elements (a 256-byte
+ * header of counters and one fp64 partial sum per block; 0 for shard_len < 1). */
+ZOPT_API size_t zopt_adamw_clip_workspace(int64_t shard_len);
+/* zopt_grad_norm_clip over grad[S] followed by zopt_adamw_step with those stats, in one launch
+ * (for a gradient that arrives whole, with no accumulation pass to carry the sum of squares).
+ * bluscript_zero_ckpt.cpp, global clip block, and dmuon PR #16, sync-free clip stats: the same
+ * arithmetic as the two calls. One cooperative wave of blocks: each block sums the squares of
+ * the run of the shard it then updates, all blocks meet at a grid-wide barrier (bounded: a wait
+ * that gives up is reported as ETIMEOUT by the next call of a kernel with bounded waits, and
+ * nothing is written), and every block adds the blocks' sums in the same fixed order, so the
+ * stats are deterministic for a given S and GPU. The sum of squares is the same sum as
+ * zopt_grad_norm_clip's but added in another order, so it can differ from it in its last
+ * bits. d_clip receives the stats (required); d_ws: at least zopt_adamw_clip_workspace(S)
+ * bytes, 16-byte aligned, zero-filled before its first use; every call leaves its counters (the
+ * first 256 bytes) at zero again (after an ETIMEOUT it must be zero-filled again). Calls sharing a workspace must be ordered
+ * (same stream). Other arguments and errors as zopt_adamw_step, plus EINVAL for a NULL d_clip
+ * or d_ws, a short workspace, max_norm negative or NaN; ECUDA if the device cannot hold the
+ * wave (cooperative launch). */
+ZOPT_API zopt_status zopt_adamw_clip_step(const zopt_layout* layout, const int64_t* d_nodecay_runs, float* master,
+                                         float* exp_avg, float* exp_avg_sq, const void* grad,
+                                         zopt_dtype grad_dtype, uint16_t* out_bf16,
+                                         const zopt_adamw_hparams* hparams, float max_norm, void* d_ws,
+                                         size_t ws_bytes, zopt_clip_stats* d_clip, zopt_adam_state* d_state,
+                                         zopt_stream stream);
+
 /* Re-target the last step (t = d_state->step, not advanced) from g*old_scale to g*new_scale,
  * in one pass (DeepSpeed PR #9021, adam_rescale_step commit: a step taken speculatively on
  * an unclipped gradient becomes the step on the final clip coefficient without an undo and a
@@ -345,10 +371,11 @@ ZOPT_API zopt_status zopt_ns_orthogonalize_many(const zopt_ns_job* jobs, int32_t
                                                 const float* abc, float eps, void* d_ws, size_t ws_bytes,
                                                 zopt_stream stream);
 
-/* Device-side failure reporting. Every wait of the tensor-core kernels is bounded (4 s);
- * one that runs out records an error word in mapped host memory, drains the kernel's copies
- * and MMAs, frees its TMEM and returns, so the context stays usable; the next
- * zopt_ns_orthogonalize / zopt_muon_step then returns ZOPT_ETIMEOUT.
+/* Device-side failure reporting. Every wait of the tensor-core kernels and of
+ * zopt_adamw_clip_step's grid barrier is bounded (4 s); one that runs out records an error
+ * word in mapped host memory, drains the kernel's copies and MMAs, frees its TMEM and returns,
+ * so the context stays usable; the next zopt_ns_orthogonalize / zopt_muon_step /
+ * zopt_adamw_clip_step then returns ZOPT_ETIMEOUT.
  * zopt_take_device_error returns the error word (0 = none, -1 if it cannot be set up) and
  * clears it, without synchronising (read it after the work it covers has completed).
  * zopt_selftest_wait_timeout launches one thread that waits, limited to limit_ns (at most

@@ -32,8 +32,9 @@ def bits(a):
 class Case:
     """Holds a parameter set, the oracle's full tensors and the GPU shard."""
 
-    def __init__(self, Z, params, bucket, world, rank, seed, gdtype):
+    def __init__(self, Z, params, bucket, world, rank, seed, gdtype, fused=False):
         self.Z, self.params, self.bucket, self.world, self.rank = Z, params, bucket, world, rank
+        self.fused = fused  # zopt_adamw_clip_step instead of zopt_grad_norm_clip + zopt_adamw_step
         self.seed, self.gdtype = seed, gdtype
         self.numel = [p.numel for p in params]
         self.decay = [p.decay for p in params]
@@ -53,6 +54,7 @@ class Case:
         self.clip = Z.new_clip_stats()
         self.state = Z.new_adam_state()
         self.ws = Z.new_norm_workspace(S)
+        self.cws = Z.new_adamw_clip_workspace(S)
         self.t = 0
 
     def shard(self, tensors):
@@ -66,11 +68,19 @@ class Case:
             g_full[k][j] = val
         g_shard = self.shard(g_full)
         g_dev = torch.from_numpy(g_shard).cuda().to(self.gdtype)
-        self.Z.grad_norm_clip(g_dev, max_norm, self.ws, self.clip)
-        self.Z.adamw_step(self.layout, self.table, self.p, self.m, self.v, g_dev, self.out, lr=h.lr,
-                          beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,
-                          skip_on_inf=skip_on_inf, clip_stats=self.clip, adam_state=self.state)
+        if self.fused:
+            self.Z.adamw_clip_step(self.layout, self.table, self.p, self.m, self.v, g_dev, self.out, lr=h.lr,
+                                   max_norm=max_norm, ws=self.cws, clip_stats=self.clip, adam_state=self.state,
+                                   beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,
+                                   skip_on_inf=skip_on_inf)
+        else:
+            self.Z.grad_norm_clip(g_dev, max_norm, self.ws, self.clip)
+            self.Z.adamw_step(self.layout, self.table, self.p, self.m, self.v, g_dev, self.out, lr=h.lr,
+                              beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,
+                              skip_on_inf=skip_on_inf, clip_stats=self.clip, adam_state=self.state)
         torch.cuda.synchronize()
+        if self.fused:
+            assert int(self.cws[:256].count_nonzero()) == 0  # every call leaves the counters at zero
         st = self.Z.read_clip_stats(self.clip)
         ref = OC.clip_stats(g_shard, max_norm)
         assert st["found_inf"] == ref["found_inf"]
@@ -381,3 +391,89 @@ def test_other_hyperparameters_bitwise(zopt, hp):
     for s in range(4):
         case.step(s, hp, max_norm=1.0)
         case.compare()
+
+
+# --------------------------------------------------------------------------- zopt_adamw_clip_step
+# The norm / clip reduction and the step in one launch. Same bar as the two-call path: the
+# GPU's own clip coefficient (read back) drives the oracle's per-tensor AdamW, master, m, v and
+# the bf16 weights bit for bit; the coefficient within 1e-6 of the oracle's; found_inf exact; a
+# skipped step changes nothing; and every call leaves the workspace's counters at zero.
+
+
+@pytest.mark.parametrize("world,rank", [(1, 0), (3, 1), (8, 7)])
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
+def test_clip_step_small_sets_bitwise(zopt, world, rank, gdtype):
+    case = Case(zopt, SMALL, 4000, world, rank, seed=11, gdtype=gdtype, fused=True)
+    for s in range(3):
+        case.step(s, H, max_norm=0.05)  # the clip coefficient is active
+        case.compare()
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_clip_step_nonfinite_grad_skips_inside_a_sequence(zopt, bad):
+    case = Case(zopt, SMALL, 4000, 1, 0, seed=3, gdtype=torch.bfloat16, fused=True)
+    case.step(0, H)
+    case.compare()
+    st = case.step(1, H, poison=(2, 17, bad))
+    assert st["found_inf"] and not st["clipped"] and st["clip_coef"] == 0.0
+    case.compare()  # nothing changed, step counter still 1
+    case.step(2, H)
+    case.step(3, H, max_norm=1e30)  # no clipping: coefficient 1
+    case.compare()
+
+
+def test_clip_step_ragged_lengths(zopt):
+    """Shards shorter than a tile, a tile and a vector off it, several tiles and a tail: the
+    blocks' runs, the 8-element sums of squares and the scalar tail all meet the oracle."""
+    for n in (1, 3, 7, 8, 9, 2047, 2048, 2049, 4096 * 3 + 1, 999_999):
+        params = [workloads.Param("a", (n,), True)]
+        case = Case(zopt, params, 1 << 20, 1, 0, seed=n, gdtype=torch.float32, fused=True)
+        case.step(0, H, max_norm=0.5)
+        case.step(1, H, max_norm=0.5)
+        case.compare()
+
+
+@pytest.mark.parametrize("name", ["c2", "c3"])
+def test_clip_step_parameter_sets_bitwise(zopt, name):
+    """The GPT-2-small set (W = 1, 38.65 M slots) and the 1.1B set's rank 0 of 8 (8.2 M), through
+    their stated steps (the GPT-2-small set on its WSD schedule), bit for bit after every step."""
+    w = workloads.get(name)
+    case = Case(zopt, w.adamw, w.bucket, w.world, w.rank, seed=w.seed, gdtype=torch.bfloat16, fused=True)
+    for s in range(w.steps):
+        case.step(s, OA.Hyper(w.lr_at(s), w.beta1, w.beta2, w.eps, w.weight_decay), max_norm=w.max_norm,
+                  zero_row_frac=w.zero_row_frac)
+        case.compare()
+
+
+def test_clip_step_in_a_cuda_graph(zopt):
+    """Captured once and replayed, the fused call gives what the same calls eagerly give: the
+    stats, the weights and the step counter stay on the device, the workspace's counters return
+    to zero."""
+    cases = [Case(zopt, SMALL, 4000, 2, 1, seed=21, gdtype=torch.bfloat16, fused=True) for _ in range(2)]
+    g = [torch.from_numpy(cases[0].shard([x.float().numpy() for x in workloads.flat_grads(SMALL, 21, s)])).cuda()
+         .bfloat16() for s in range(3)]
+    g_in = g[0].clone()
+
+    def call(c, grad):
+        zopt.adamw_clip_step(c.layout, c.table, c.p, c.m, c.v, grad, c.out, lr=H.lr, max_norm=0.05, ws=c.cws,
+                             clip_stats=c.clip, adam_state=c.state)
+
+    eager, graphed = cases
+    call(graphed, g_in)  # the first call sets up the launch outside the capture
+    call(eager, g[0])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            call(graphed, g_in)
+    for s in (1, 2):
+        g_in.copy_(g[s])
+        graph.replay()
+        call(eager, g[s])
+    torch.cuda.synchronize()
+    for a, b in ((graphed.p, eager.p), (graphed.m, eager.m), (graphed.v, eager.v), (graphed.out, eager.out)):
+        assert torch.equal(a, b)
+    assert torch.equal(graphed.clip, eager.clip)
+    assert zopt.read_adam_state(graphed.state) == zopt.read_adam_state(eager.state) == {"step": 3, "arrive": 0}
+    assert int(graphed.cws[:256].count_nonzero()) == 0

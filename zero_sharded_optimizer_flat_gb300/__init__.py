@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
         "zopt_grad_norm_clip_noalloc": (ctypes.c_int, [vp, ctypes.c_int, i64, ctypes.c_float, vp, vp]),
         "zopt_adamw_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                            vp, vp, vp]),
+        "zopt_adamw_clip_workspace": (sz, [i64]),
+        "zopt_adamw_clip_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
+                                                ctypes.c_float, vp, sz, vp, vp, vp]),
         "zopt_adamw_rescale_step": (ctypes.c_int, [vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.POINTER(_Hparams),
                                                    ctypes.c_float, ctypes.c_float, vp, vp, vp]),
         "zopt_grad_accumulate": (ctypes.c_int, [vp, vp, ctypes.c_int, i64, i32, ctypes.c_float, vp, sz, vp, vp]),
@@ -340,6 +343,30 @@ def adamw_step(layout: ShardLayout, table, master, exp_avg, exp_avg_sq, grad, ou
     _check(lib().zopt_adamw_step(layout.handle, _ptr(table), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
                                  _ptr(grad), _dtype_code(grad), _ptr(out_bf16), ctypes.byref(hp),
                                  _ptr(clip_stats), _ptr(adam_state), _stream(stream)))
+
+
+
+def adamw_clip_workspace(shard_len: int) -> int:
+    return int(lib().zopt_adamw_clip_workspace(int(shard_len)))
+
+
+def new_adamw_clip_workspace(shard_len: int, device="cuda"):
+    """A zero-filled workspace for :func:`adamw_clip_step` over a shard of this length (each call
+    leaves its counters at zero again)."""
+    import torch
+    return torch.zeros(max(adamw_clip_workspace(shard_len), 16), dtype=torch.uint8, device=device)
+
+
+def adamw_clip_step(layout: ShardLayout, table, master, exp_avg, exp_avg_sq, grad, out_bf16, *, lr: float,
+                    max_norm: float, ws, clip_stats, adam_state, beta1: float = 0.9, beta2: float = 0.95,
+                    eps: float = 1e-8, weight_decay: float = 0.1, skip_on_inf: bool = True, stream=None) -> None:
+    """``zopt_adamw_clip_step``: the gradient's norm / clip / found_inf and the AdamW step of the
+    rank's shard in one launch (the stats land in ``clip_stats`` as zopt_grad_norm_clip writes them)."""
+    hp = _Hparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(bool(skip_on_inf)), 0)
+    _check(lib().zopt_adamw_clip_step(layout.handle, _ptr(table), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                      _ptr(grad), _dtype_code(grad), _ptr(out_bf16), ctypes.byref(hp),
+                                      float(max_norm), _ptr(ws), ws.numel(), _ptr(clip_stats), _ptr(adam_state),
+                                      _stream(stream)))
 
 
 # --------------------------------------------------------------------------- Newton-Schulz

@@ -438,7 +438,7 @@ zopt_status take_error_word(const char* fn, int** dev) {
   if (st != ZOPT_OK) return st;
   if (*reinterpret_cast<volatile int*>(h) != 0) {
     *reinterpret_cast<volatile int*>(h) = 0;
-    return fail(ZOPT_ETIMEOUT, std::string(fn) + ": a tensor-core kernel of an earlier call timed out on a wait");
+    return fail(ZOPT_ETIMEOUT, std::string(fn) + ": a kernel of an earlier call timed out on a wait");
   }
   return ok();
 }

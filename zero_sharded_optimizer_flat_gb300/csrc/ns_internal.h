@@ -76,5 +76,10 @@ void many_norm_partials(const zopt_ns_job* jobs, int32_t n_jobs, void* d_ws, dou
 constexpr int kNormPartialsMax = 512;
 int norm_blocks(long long n);
 
+// The error word that kernels with bounded waits set when a wait gives up (mapped host memory):
+// returns ZOPT_ETIMEOUT (and clears the word) if a kernel of an earlier call set it, and gives
+// the device address for this call's kernels in *dev.
+zopt_status take_error_word(const char* fn, int** dev);
+
 }  // namespace ns
 }  // namespace zopt
