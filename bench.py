@@ -46,7 +46,7 @@ ADAMW_SRC_DIGEST = "54ebf47afe0cecf6"
 # the Newton-Schulz sources hash to NS_SRC_DIGEST
 NS_SOURCES = ("ns.cu", "ns_gemm.cu", "ns_prep.cu", "ns_tile.cuh", "tc.cuh", "launch.cuh", "norm_impl.cuh")
 NS_TRAFFIC_PER_CALL = 258872122112 + 39090095616
-NS_SRC_DIGEST = "4a87dc39acd41c40"
+NS_SRC_DIGEST = "4cb7bb9b25d943a4"
 MICRO_STEPS = 4
 ACC_BYTES = 6 + 10 * (MICRO_STEPS - 1)  # first part: read bf16 2 + write fp32 4; later: + read fp32 4
 # two parts to a pass: the first pair reads 2 x 2 and writes 4; each later pair also reads the sum
