@@ -250,6 +250,9 @@ ZOPT_API zopt_status zopt_adamw_step(const zopt_layout* layout, const int64_t* d
 ZOPT_API size_t zopt_adamw_clip_workspace(int64_t shard_len);
 /* zopt_grad_norm_clip over grad[S] followed by zopt_adamw_step with those stats, in one launch
  * (for a gradient that arrives whole, with no accumulation pass to carry the sum of squares).
+ * The norm is this shard's own: right for one rank, or a simulated rank; a multi-rank job,
+ * whose clip needs the all-reduced sum of squares, keeps zopt_grad_norm_clip, the all-reduce
+ * and zopt_clip_finalize before zopt_adamw_step.
  * bluscript_zero_ckpt.cpp, global clip block, and dmuon PR #16, sync-free clip stats: the same
  * arithmetic as the two calls. One cooperative wave of blocks: each block sums the squares of
  * the run of the shard it then updates, all blocks meet at a grid-wide barrier (bounded: a wait
