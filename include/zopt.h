@@ -261,9 +261,10 @@ ZOPT_API size_t zopt_adamw_clip_workspace(int64_t shard_len);
  * stats are deterministic for a given S and GPU. The sum of squares is the same sum as
  * zopt_grad_norm_clip's but added in another order, so it can differ from it in its last
  * bits. d_clip receives the stats (required); d_ws: at least zopt_adamw_clip_workspace(S)
- * bytes, 16-byte aligned, zero-filled before its first use; every call leaves its counters (the
- * first 256 bytes) at zero again (after an ETIMEOUT it must be zero-filled again). Calls sharing a workspace must be ordered
- * (same stream). Other arguments and errors as zopt_adamw_step, plus EINVAL for a NULL d_clip
+ * bytes, 16-byte aligned, zero-filled before its first use; every call leaves its counters
+ * (the first 256 bytes) at zero again (after an ETIMEOUT it must be zero-filled again). Calls
+ * sharing a workspace must be ordered (same stream). Other arguments and errors as
+ * zopt_adamw_step, plus EINVAL for a NULL d_clip
  * or d_ws, a short workspace, max_norm negative or NaN; ECUDA if the device cannot hold the
  * wave (cooperative launch). */
 ZOPT_API zopt_status zopt_adamw_clip_step(const zopt_layout* layout, const int64_t* d_nodecay_runs, float* master,
