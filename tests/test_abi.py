@@ -232,3 +232,30 @@ def test_accumulate2_validates_before_launch():
     assert b"aligned" in L.zopt_last_error()
     assert L.zopt_grad_accumulate2(acc, g, g, Z.BF16, 0, 1, 1.0, None, 0, None, None) == 1
     assert L.zopt_grad_accumulate2(acc, g, g, 9, 64, 1, 1.0, None, 0, None, None) == 2
+
+
+def test_adamw_clip_step_validates_before_launch():
+    """zopt_adamw_clip_step takes zopt_adamw_step's checks (shared code) and its own: d_clip and
+    d_ws required and aligned, a workspace of zopt_adamw_clip_workspace(S) bytes, max_norm not
+    negative or NaN. Every call below fails before any CUDA call (the pointers are fake)."""
+    L = Z.lib()
+    lay = Z.ShardLayout([100, 3], [1, 0], 64, 1, 0)  # S = 103 (one partial): 256 + 8 bytes
+    S = lay.shard_len
+    assert L.zopt_adamw_clip_workspace(S) == 256 + 8
+    assert L.zopt_adamw_clip_workspace(0) == 0
+    assert L.zopt_adamw_clip_workspace(2048 * 5000) == 256 + 8 * 4096  # at most 4096 blocks
+    hp = Z._Hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1, 0)
+    bad = Z._Hparams(1e-3, 1.0, 0.95, 1e-8, 0.1, 1, 0)
+    p, tab, clip, ws = ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096), ctypes.c_void_p(512), ctypes.c_void_p(1 << 12)
+    need = L.zopt_adamw_clip_workspace(S)
+    call = lambda h=hp, mn=1.0, w=ws, wb=need, c=clip: L.zopt_adamw_clip_step(  # noqa: E731
+        lay.handle, tab, p, p, p, p, 1, None, ctypes.byref(h), mn, w, wb, c, p, None)
+    assert call(h=bad) == 1 and b"betas" in L.zopt_last_error()
+    assert call(c=None) == 1 and b"NULL" in L.zopt_last_error()
+    assert call(w=None) == 1 and b"NULL" in L.zopt_last_error()
+    assert call(w=ctypes.c_void_p((1 << 12) + 8)) == 1 and b"aligned" in L.zopt_last_error()
+    assert call(mn=-1.0) == 1 and b"max_norm" in L.zopt_last_error()
+    assert call(mn=float("nan")) == 1 and b"max_norm" in L.zopt_last_error()
+    assert call(wb=need - 1) == 1 and b"workspace" in L.zopt_last_error()
+    assert L.zopt_adamw_clip_step(lay.handle, tab, p, p, p, p, 5, None, ctypes.byref(hp), 1.0, ws, need, clip, p,
+                                  None) == 2  # another gradient dtype: EUNSUPPORTED
