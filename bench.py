@@ -40,7 +40,7 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 # count), valid while the kernel's sources hash to ADAMW_SRC_DIGEST (otherwise the traffic is
 # reported as null)
 ADAMW_TRAFFIC_PER_ELEM = (1073795712 + 881538688) / 67108864
-ADAMW_SRC_DIGEST = "54ebf47afe0cecf6"
+ADAMW_SRC_DIGEST = "d44e3d7ac92f1bca"
 # DRAM bytes of one zopt_ns_orthogonalize_many call over the 48-matrix stress set (dram__bytes_read.sum
 # + dram__bytes_write.sum summed over its launches, one ncu pass on the full set), valid while
 # the Newton-Schulz sources hash to NS_SRC_DIGEST

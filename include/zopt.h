@@ -252,21 +252,20 @@ ZOPT_API size_t zopt_adamw_clip_workspace(int64_t shard_len);
  * (for a gradient that arrives whole, with no accumulation pass to carry the sum of squares).
  * The norm is this shard's own: right for one rank, or a simulated rank; a multi-rank job,
  * whose clip needs the all-reduced sum of squares, keeps zopt_grad_norm_clip, the all-reduce
- * and zopt_clip_finalize before zopt_adamw_step.
- * bluscript_zero_ckpt.cpp, global clip block, and dmuon PR #16, sync-free clip stats: the same
- * arithmetic as the two calls. One cooperative wave of blocks: each block sums the squares of
- * the run of the shard it then updates, all blocks meet at a grid-wide barrier (bounded: a wait
- * that gives up is reported as ETIMEOUT by the next call of a kernel with bounded waits, and
- * nothing is written), and every block adds the blocks' sums in the same fixed order, so the
- * stats are deterministic for a given S and GPU. The sum of squares is the same sum as
- * zopt_grad_norm_clip's but added in another order, so it can differ from it in its last
- * bits. d_clip receives the stats (required); d_ws: at least zopt_adamw_clip_workspace(S)
- * bytes, 16-byte aligned, zero-filled before its first use; every call leaves its counters
- * (the first 256 bytes) at zero again (after an ETIMEOUT it must be zero-filled again). Calls
- * sharing a workspace must be ordered (same stream). Other arguments and errors as
- * zopt_adamw_step, plus EINVAL for a NULL d_clip
- * or d_ws, a short workspace, max_norm negative or NaN; ECUDA if the device cannot hold the
- * wave (cooperative launch). */
+ * and zopt_clip_finalize before zopt_adamw_step. bluscript_zero_ckpt.cpp, global clip block,
+ * and dmuon PR #16, sync-free clip stats: the same arithmetic as the two calls. One
+ * cooperative wave of blocks: each block sums the squares of the run of the shard it then
+ * updates, all blocks meet at a grid-wide barrier (bounded: a block whose wait gives up
+ * updates nothing, so the step is left incomplete, and the next call of a kernel with bounded
+ * waits returns ETIMEOUT), and every block adds the blocks' sums in the same fixed order, so
+ * the stats are deterministic for a given S and GPU. The sum of squares is the same sum as
+ * zopt_grad_norm_clip's but added in another order, so it can differ from it in its last bits.
+ * d_clip receives the stats (required); d_ws: at least zopt_adamw_clip_workspace(S) bytes,
+ * 16-byte aligned, zero-filled before its first use; every call leaves its counters (the first
+ * 256 bytes) at zero again (after an ETIMEOUT it must be zero-filled again). Calls sharing a
+ * workspace must be ordered (same stream). Other arguments and errors as zopt_adamw_step, plus
+ * EINVAL for a NULL d_clip or d_ws, a short workspace, max_norm negative or NaN; ECUDA if the
+ * device cannot hold the wave (cooperative launch). */
 ZOPT_API zopt_status zopt_adamw_clip_step(const zopt_layout* layout, const int64_t* d_nodecay_runs, float* master,
                                          float* exp_avg, float* exp_avg_sq, const void* grad,
                                          zopt_dtype grad_dtype, uint16_t* out_bf16,
@@ -317,9 +316,9 @@ ZOPT_API zopt_status zopt_adamw_rescale_step(const zopt_layout* layout, float* m
 #define ZOPT_NS_MAX_SPAN (1LL << 56)   /* (batch - 1) * batch stride (elements) */
 
 /* Workspace bytes to process `group` rows x cols matrices together (0 for an unsupported
- * compute dtype, group < 1, or a shape beyond the limits above). A call processes its batch in groups of as many matrices as its
- * workspace holds: every product of a step is one launch over the whole group, so a larger
- * group means fewer launches and better use of the SMs. */
+ * compute dtype, group < 1, or a shape beyond the limits above). A call processes its batch in
+ * groups of as many matrices as its workspace holds: every product of a step is one launch
+ * over the whole group, so a larger group means fewer launches and better use of the SMs. */
 ZOPT_API size_t zopt_ns_workspace(int64_t rows, int64_t cols, int32_t group, zopt_dtype compute_dtype);
 /* Orthogonalise `batch` matrices G[b] (rows x cols, row-major, leading dimension ld_g,
  * matrix b at G + b*batch_stride_g elements) into X[b] (same shape, ld_x, batch_stride_x).

@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) adamw_clip_kernel(float* __restrict_
     s_ok = ok;
   }
   __syncthreads();
-  if (!s_ok) return;  // the error word reports it; nothing is written
+  if (!s_ok) return;  // the error word reports it; this block updates nothing
   double a = 0.0;
   const volatile double* parts = ws->partials;
   for (unsigned int i = threadIdx.x; i < gridDim.x; i += blockDim.x) a = __dadd_rn(a, parts[i]);
