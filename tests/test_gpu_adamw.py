@@ -352,6 +352,33 @@ def test_rescale_tile_edges(zopt, n):
     assert np.array_equal(case.out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(spec[0]))
 
 
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
+def test_rescale_many_tiles_per_block(zopt, gdtype):
+    """A shard of several 2048-element tiles per block (9,000,001 elements: over 4,000 whole
+    tiles for a grid of at most a few hundred blocks) and a ragged tail: the kernel's loop that
+    issues a half of its next tile's loads while it computes the rest of this one is bit for bit
+    the oracle's re-targeting on every element, bf16 weights included."""
+    n = 9_000_001
+    rng = np.random.default_rng(17)
+    p = rng.normal(0.0, 0.02, n).astype(np.float32)
+    m = rng.normal(0.0, 1e-3, n).astype(np.float32)
+    v = np.abs(rng.normal(0.0, 1e-5, n)).astype(np.float32)
+    g_dev = torch.from_numpy(rng.normal(0.0, 1e-2, n).astype(np.float32)).cuda().to(gdtype)
+    g = g_dev.float().cpu().numpy()
+    lay = zopt.ShardLayout([n], [1], 1 << 24, 1, 0)
+    assert lay.shard_len == n
+    dp, dm, dv = (torch.from_numpy(a.copy()).cuda() for a in (p, m, v))
+    out = torch.empty(n, dtype=torch.int16, device="cuda")
+    state = zopt.new_adam_state()
+    state.view(torch.int64)[0] = 3  # the step being re-targeted is t = 3
+    zopt.adamw_rescale_step(lay, dp, dm, dv, g_dev, out, lr=H.lr, old_scale=1.0, new_scale=0.37, adam_state=state)
+    torch.cuda.synchronize()
+    OA.rescale_step_f32(p, m, v, g, 1.0, 0.37, H, 3)
+    for r, t in zip((p, m, v), (dp, dm, dv)):
+        assert np.array_equal(bits(r), bits(t.cpu().numpy()))
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(p))
+
+
 def test_rescale_division_by_constant_is_exact(zopt):
     """The rescale kernel forms sqrt(v) / c, c = sqrt(1 - beta2^t), with a reciprocal and one FMA
     correction (Markstein's method) instead of an IEEE division. For every bit pattern of
