@@ -40,7 +40,7 @@ ADAMW_BYTES = 30   # per element: read p, m, v (12) + fp32 grad (4); write p, m,
 # count), valid while the kernel's sources hash to ADAMW_SRC_DIGEST (otherwise the traffic is
 # reported as null)
 ADAMW_TRAFFIC_PER_ELEM = (1073795712 + 881538688) / 67108864
-ADAMW_SRC_DIGEST = "d44e3d7ac92f1bca"
+ADAMW_SRC_DIGEST = "4adaedf157834c0e"
 # DRAM bytes of one zopt_ns_orthogonalize_many call over the 48-matrix stress set (dram__bytes_read.sum
 # + dram__bytes_write.sum summed over its launches, one ncu pass on the full set), valid while
 # the Newton-Schulz sources hash to NS_SRC_DIGEST
@@ -551,7 +551,7 @@ def config_lines(Z, torch, stream, pk, K: int) -> dict:
         else:
             entry["adamw_kernel"] = {"ms": round(kern_ms, 4), "achieved": round(kern, 1), "unit": "GB/s"}
         # the same step through zopt_adamw_clip_step: the norm / clip reduction and the update in
-        # one launch (same bytes; the gradient's second read mostly from L2)
+        # one launch (same bytes; the gradient's second read from L2 only where it survives the update's stream)
         cws = Z.new_adamw_clip_workspace(S)
         evs = [(mk(), mk()) for _ in range(3 + K)]
         for i, (e0, e1) in enumerate(evs):

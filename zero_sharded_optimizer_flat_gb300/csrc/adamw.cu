@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(float* __restrict__ P, 
 // range, the runs in fp64, as the norm pass does), publishes the sum, and waits at a grid-wide
 // barrier; then every block adds all the blocks' sums in the same fixed order, so every block
 // holds the same sum of squares, norm, clip coefficient and found_inf (block 0 also writes them
-// out), and the step runs as adamw_kernel's. The gradient is read twice, the second time
-// mostly from L2 when the shard's gradient fits in it.
+// out), and the step runs as adamw_kernel's. The gradient is read twice; the second read finds
+// it in L2 only where the update's own stream has not evicted it first (a small shard).
 constexpr int64_t kClipMaxBlocks = 4096;  // partial sums the workspace holds
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
