@@ -267,6 +267,60 @@ def test_full_size_zero2_shard_sampled(zopt):
     assert zopt.read_adam_state(state)["step"] == 2
 
 
+def test_full_size_zero2_shard_clip_step_sampled(zopt):
+    """zopt_adamw_clip_step on the 2e9-parameter ZeRO-2 shard (rank 0 of 8, S = 250,000,000, an
+    fp32 gradient): one cooperative wave over about 120,000 tiles, each block summing and then
+    updating its own run. The sum of squares within 1e-6 of the oracle's over the whole shard;
+    sampled slots (random, both ends, every no-decay run edge) bit for bit the oracle's step on
+    the call's own clip coefficient; the counters back at zero after each call."""
+    w = workloads.get("c4")
+    numel = [p.numel for p in w.adamw]
+    decay = np.array([p.decay for p in w.adamw])
+    lay = zopt.ShardLayout(numel, decay, w.bucket, w.world, w.rank)
+    S = lay.shard_len
+    table = lay.device_table()
+    gen = torch.Generator(device="cuda").manual_seed(14)
+    p = torch.randn(S, device="cuda", generator=gen) * 0.02
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    out = torch.empty(S, dtype=torch.int16, device="cuda")
+    clip, state = zopt.new_clip_stats(), zopt.new_adam_state()
+    cws = zopt.new_adamw_clip_workspace(S)
+    rng = np.random.default_rng(14)
+    runs = lay.nodecay_runs()
+    edges = np.concatenate([runs.reshape(-1) + d for d in (-2, -1, 0, 1)])
+    idx = np.unique(np.clip(np.concatenate([rng.integers(0, S, 200_000), [0, 1, S - 2, S - 1], edges]), 0, S - 1))
+    idx_d = torch.from_numpy(idx).cuda()
+    flat = OL.flat_index_of_slots(numel, w.bucket, w.world, w.rank, idx)
+    owner = OL.param_of_flat(numel, flat)
+    dec = np.where(owner >= 0, decay[np.maximum(owner, 0)], False)
+    h = OA.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    sp = p[idx_d].cpu().numpy()
+    sm = np.zeros_like(sp)
+    sv = np.zeros_like(sp)
+    for t in range(1, 3):
+        g = torch.randn(S, device="cuda", generator=gen) * 1e-3
+        zopt.adamw_clip_step(lay, table, p, m, v, g, out, lr=h.lr, max_norm=w.max_norm, ws=cws, clip_stats=clip,
+                             adam_state=state, beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay)
+        torch.cuda.synchronize()
+        st = zopt.read_clip_stats(clip)
+        ref_ss = OC.sumsq(g.cpu().numpy())
+        assert abs(st["sumsq"] - ref_ss) <= 1e-6 * ref_ss
+        assert st["clipped"] == 1 and 0.0 < st["clip_coef"] < 1.0  # norm ~16 against max_norm 1
+        assert cws[:256].count_nonzero() == 0
+        sg = g[idx_d].cpu().numpy()
+        sc = OA.scalars_f32(h, t)
+        for mask in (dec, ~dec):
+            pp, mm, vv = sp[mask], sm[mask], sv[mask]
+            OA.adamw_tensor_f32(pp, mm, vv, sg[mask], st["clip_coef"], bool(mask is dec), sc)
+            sp[mask], sm[mask], sv[mask] = pp, mm, vv
+        assert np.array_equal(bits(p[idx_d].cpu().numpy()), bits(sp))
+        assert np.array_equal(bits(m[idx_d].cpu().numpy()), bits(sm))
+        assert np.array_equal(bits(v[idx_d].cpu().numpy()), bits(sv))
+        assert np.array_equal(out[idx_d].cpu().numpy().view(np.uint16), f32_to_bf16_bits(sp))
+    assert zopt.read_adam_state(state)["step"] == 2
+
+
 H_BETA1_ZERO = OA.Hyper(lr=1e-3, beta1=0.0, beta2=0.99, eps=1e-8, weight_decay=0.1)
 
 
