@@ -251,6 +251,31 @@ def test_nan_gradient_is_rejected(zopt):
     assert math.isnan(float(buf[3, 4])) and int(torch.isnan(buf).sum()) == 1
 
 
+@pytest.mark.parametrize("rows,cols", [(256, 512), (1024, 2048), (2048, 1024)])
+def test_zero_gradient_decays_only(zopt, rows, cols):
+    """A zero gradient with a zero momentum buffer: u = 0, so Newton-Schulz gives U = 0 (X0 =
+    0 / (0 + eps)), the guard passes (max |U| = 0), nsratio is 0, and the step is the decoupled
+    decay alone, p * fp32(1 - lr*wd), bit for bit: on the fused path (256 x 512), on CTA pairs
+    with u read in place by the first step (1024 x 2048), and for a tall matrix (2048 x 1024)."""
+    h = OM.MuonHyper(lr=8e-4)
+    p = torch.randn(rows, cols, device="cuda") * 0.02
+    p0 = p.cpu().numpy()
+    buf = torch.zeros_like(p)
+    g = torch.zeros(rows, cols, device="cuda", dtype=torch.bfloat16)
+    out = torch.zeros(rows, cols, dtype=torch.int16, device="cuda")
+    stats = zopt.new_muon_stats()
+    zopt.muon_step(p, buf, g, out, zopt.new_muon_workspace(rows, cols), stats, lr=h.lr)
+    torch.cuda.synchronize()
+    st = zopt.read_muon_stats(stats)[0]
+    ref = OM.muon_step(p0.copy(), np.zeros((rows, cols), np.float32), np.zeros((rows, cols), np.float32), h)
+    assert not ref["rejected"] and ref["max_abs"] == 0.0
+    assert not st["rejected"] and st["max_abs"] == 0.0 and st["ns_ratio"] == 0.0
+    expect = p0 * np.float32(1.0 - h.lr * h.weight_decay)
+    assert np.array_equal(p.cpu().numpy().view(np.uint32), expect.view(np.uint32))
+    assert torch.count_nonzero(buf) == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), f32_to_bf16_bits(expect))
+
+
 @pytest.mark.parametrize("nesterov,mom,wd", [(False, 0.9, 0.0), (True, 0.5, 0.05), (False, 0.0, 0.1)])
 def test_momentum_variants(zopt, nesterov, mom, wd):
     """Plain momentum (u = buf), another coefficient, no or other weight decay, and mu = 0 (u = g):
