@@ -62,7 +62,7 @@ def _worker(rank: int, world: int, port: int, numel: list, bucket: int, q) -> No
         q.put((rank, False, False, repr(e)))
 
 
-@pytest.mark.parametrize("world", [2])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_two_gloo_ranks_cover_and_reduce(world):
     from zero_sharded_optimizer_flat_gb300 import build_lib
     build_lib.build()
